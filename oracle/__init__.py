@@ -1,0 +1,182 @@
+"""fp64 CPU oracle for tree verification -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, the package smoke check and the benchmark's CPU-baseline
+leg import this module.  The product path (the C-ABI library and its binding)
+never imports, links or calls it, and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, pthreads); this file only
+compiles it with gcc and marshals numpy arrays through ctypes.  See the header
+of ``oracle.c`` for what is computed and which passage of the pages each step
+follows.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (no fast math, no fp contraction)."""
+    with _lock:
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+            tmp = _LIB + f".tmp{os.getpid()}"
+            subprocess.check_call(
+                ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                 "-shared", "-pthread", _SRC, "-o", tmp, "-lm"])
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _AttnArgs(C.Structure):
+    _fields_ = [
+        ("batch", C.c_int), ("num_q_heads", C.c_int), ("num_kv_heads", C.c_int),
+        ("head_dim", C.c_int), ("block_size", C.c_int), ("max_blocks_per_seq", C.c_int),
+        ("scale", C.c_double),
+        ("q", C.c_void_p), ("k_prefix", C.c_void_p), ("v_prefix", C.c_void_p),
+        ("block_table", C.c_void_p), ("k_nodes", C.c_void_p), ("v_nodes", C.c_void_p),
+        ("parent", C.c_void_p), ("prefix_lens", C.c_void_p), ("node_offsets", C.c_void_p),
+    ]
+
+
+class _AcceptArgs(C.Structure):
+    _fields_ = [
+        ("batch", C.c_int), ("vocab", C.c_int), ("kind", C.c_int), ("max_nodes", C.c_int),
+        ("target", C.c_void_p), ("draft_probs", C.c_void_p), ("draft_tokens", C.c_void_p),
+        ("parent", C.c_void_p), ("node_offsets", C.c_void_p), ("uniforms", C.c_void_p),
+        ("retained_mask", C.c_void_p), ("pq_replay", C.c_void_p),
+        ("accepted_len", C.c_void_p), ("path", C.c_void_p), ("bonus_token", C.c_void_p),
+        ("status", C.c_void_p), ("pq_out", C.c_void_p),
+    ]
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = C.CDLL(build())
+        lib.oracle_tree_attention_rows.argtypes = [C.POINTER(_AttnArgs), C.c_int, C.c_void_p,
+                                                   C.c_void_p, C.c_int]
+        lib.oracle_tree_attention_rows.restype = C.c_int
+        lib.oracle_accept.argtypes = [C.POINTER(_AcceptArgs), C.c_int]
+        lib.oracle_accept.restype = C.c_int
+        lib.oracle_quantise.argtypes = [C.c_float]
+        lib.oracle_quantise.restype = C.c_uint64
+        lib.oracle_scaled_draw.argtypes = [C.c_float, C.c_uint64]
+        lib.oracle_scaled_draw.restype = C.c_uint64
+        lib.oracle_retained_mass_row.argtypes = [C.c_void_p, C.c_void_p, C.c_int]
+        lib.oracle_retained_mass_row.restype = C.c_float
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def tree_attention_rows(case: dict, rows, nthreads: int | None = None) -> np.ndarray:
+    """fp64 outputs for the listed (b, local node, q head) rows -> [len(rows), D]."""
+    lib = _load()
+    keep = {k: _c(case[k], np.uint16) for k in ("q", "k_prefix", "v_prefix", "k_nodes", "v_nodes")}
+    for k in ("block_table", "parent", "prefix_lens", "node_offsets"):
+        keep[k] = _c(case[k], np.int32)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    hq, hkv, d = case["num_q_heads"], case["num_kv_heads"], case["head_dim"]
+    scale = case.get("softmax_scale") or 1.0 / np.sqrt(d)
+    args = _AttnArgs(int(case["batch"]), int(hq), int(hkv), int(d), int(case["block_size"]),
+                     int(keep["block_table"].shape[1]), float(scale),
+                     *[_ptr(keep[k]) for k in ("q", "k_prefix", "v_prefix", "block_table",
+                                               "k_nodes", "v_nodes", "parent", "prefix_lens",
+                                               "node_offsets")])
+    out = np.zeros((rows.shape[0], d), dtype=np.float64)
+    rc = lib.oracle_tree_attention_rows(C.byref(args), rows.shape[0], _ptr(rows), _ptr(out),
+                                        int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle_tree_attention_rows: unsupported arguments")
+    return out
+
+
+def all_rows(case: dict) -> np.ndarray:
+    """Every (b, i, h) row in output order ([total_nodes][Hq])."""
+    off = np.asarray(case["node_offsets"])
+    hq = case["num_q_heads"]
+    rows = []
+    for b in range(case["batch"]):
+        for i in range(off[b + 1] - off[b]):
+            for h in range(hq):
+                rows.append((b, i, h))
+    return np.asarray(rows, dtype=np.int32).reshape(-1, 3)
+
+
+def tree_attention(case: dict, nthreads: int | None = None) -> np.ndarray:
+    """Full fp64 output [total_nodes][Hq][D]."""
+    rows = all_rows(case)
+    out = tree_attention_rows(case, rows, nthreads)
+    tot = int(np.asarray(case["node_offsets"])[-1])
+    return out.reshape(tot, case["num_q_heads"], case["head_dim"])
+
+
+def accept(case: dict, pq_replay=None, nthreads: int | None = None, want_pq: bool = True) -> dict:
+    """Oracle accept pass.  Returns accepted_len, path, bonus_token, status, pq."""
+    lib = _load()
+    off = _c(case["node_offsets"], np.int32)
+    batch = off.shape[0] - 1
+    tot = int(off[-1])
+    max_nodes = int(case["max_nodes"])
+    keep = {
+        "target": _c(case["target"], np.float32),
+        "draft_probs": _c(case["draft_probs"], np.float32),
+        "draft_tokens": _c(case["draft_tokens"], np.int32),
+        "parent": _c(case["parent"], np.int32),
+        "uniforms": _c(case["uniforms"], np.float32),
+        "retained_mask": _c(case.get("retained_mask"), np.uint32),
+        "pq_replay": _c(pq_replay, np.float32),
+    }
+    out = {
+        "accepted_len": np.zeros(batch, np.int32),
+        "path": np.zeros((batch, max_nodes), np.int32),
+        "bonus_token": np.zeros(batch, np.int32),
+        "status": np.zeros(batch, np.int32),
+        "pq": np.zeros((max(tot, 1), 2), np.float32) if want_pq else None,
+    }
+    kind = 1 if case.get("kind", "probs") == "logits" else 0
+    args = _AcceptArgs(batch, int(case["vocab"]), kind, max_nodes,
+                       _ptr(keep["target"]), _ptr(keep["draft_probs"]), _ptr(keep["draft_tokens"]),
+                       _ptr(keep["parent"]), _ptr(off), _ptr(keep["uniforms"]),
+                       _ptr(keep["retained_mask"]), _ptr(keep["pq_replay"]),
+                       _ptr(out["accepted_len"]), _ptr(out["path"]), _ptr(out["bonus_token"]),
+                       _ptr(out["status"]), _ptr(out["pq"]))
+    rc = lib.oracle_accept(C.byref(args), int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle_accept: unsupported arguments")
+    return out
+
+
+def quantise(r: float) -> int:
+    return int(_load().oracle_quantise(C.c_float(r)))
+
+
+def scaled_draw(u: float, S: int) -> int:
+    return int(_load().oracle_scaled_draw(C.c_float(u), C.c_uint64(S)))
+
+
+def retained_mass(q_row, mask_row) -> float:
+    q = _c(q_row, np.float32)
+    m = None if mask_row is None else _c(mask_row, np.uint32)
+    return float(_load().oracle_retained_mass_row(_ptr(q), _ptr(m), int(q.shape[0])))
