@@ -1,0 +1,442 @@
+#!/usr/bin/env python
+"""Benchmark of one tree-verification step on GB300.
+
+A step is one pass of the whole hot path over one batch of a synthetic
+workload: tv_tree_attention (tree attention over the paged prefix plus the
+tree mask) followed by tv_accept (logits mode: log-sum-exp, pruning
+renormalisation when the workload has a retained-set mask, per-node tests,
+the longest accepted path and the bonus draw).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  `value` is tree-tokens/s (tree nodes
+verified per second, all ranks) with inputs resident in HBM; L2 is flushed
+between timed steps (a 512 MiB write, outside the timed events).  Under
+torchrun each rank runs an independent replica (no collective on the data
+path: sequences are independent), timing is max over ranks.
+`--impl reference` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from speculative_decoding_tree_attention_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "tree-verify tree-tokens/s"
+UNIT = "tree-tokens/s"
+FLUSH_BYTES = 512 << 20
+ATTN_SRC = os.path.join(ROOT, "speculative_decoding_tree_attention_gb300", "csrc",
+                        "tree_attn_kernel.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, help="workload 1..5 (default: 7B-like)")
+    ap.add_argument("--mode", choices=["logits", "probs"], default="logits")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    return ap.parse_args()
+
+
+def workload_desc(cfg, case):
+    ns = np.diff(case["node_offsets"])
+    return {"workload": f"{cfg['name']} (config {cfg['num']})", "batch": int(cfg["batch"]),
+            "q_heads": int(cfg["hq"]), "kv_heads": int(cfg["hkv"]), "head_dim": int(cfg["d"]),
+            "prefix_lens": [int(x) for x in case["prefix_lens"]] if cfg["batch"] <= 4 else
+            [int(min(case["prefix_lens"])), int(max(case["prefix_lens"]))],
+            "tree_nodes": int(ns.sum()), "vocab": int(cfg["vocab"]),
+            "retained_mask": bool(cfg.get("mask_mass")), "block_size": wl.BLOCK_SIZE,
+            "paged_shuffled": bool(cfg.get("shuffle"))}
+
+
+def attention_bytes(case):
+    """Algorithmic bytes of one tree-attention launch: prefix K+V once per
+    (sequence, KV head), Q, tree K/V and the output, all bf16."""
+    hq, hkv, D = case["num_q_heads"], case["num_kv_heads"], case["head_dim"]
+    L = np.asarray(case["prefix_lens"], np.int64)
+    tot = int(case["node_offsets"][-1])
+    return int(4 * L.sum() * hkv * D + 2 * tot * hq * D * 2 + 4 * tot * hkv * D)
+
+
+def attention_flops(case):
+    hq, D = case["num_q_heads"], case["head_dim"]
+    off = case["node_offsets"]
+    f = 0
+    for b in range(case["batch"]):
+        N = int(off[b + 1] - off[b])
+        par = case["parent"][off[b]:off[b + 1]]
+        depth = np.zeros(N, np.int64)
+        for i in range(1, N):
+            depth[i] = depth[par[i]] + 1
+        f += 4 * N * int(case["prefix_lens"][b]) * D * hq + 4 * D * hq * int((depth + 1).sum())
+    return int(f)
+
+
+def accept_bytes(case):
+    """Algorithmic bytes of one accept launch (logits mode): the target row of
+    every node with children (LSE), the draft rows of those nodes and the mask
+    rows when a retained set is given (Z), the two rows of one cut node, and
+    the per-node vectors."""
+    V = case["vocab"]
+    off = case["node_offsets"]
+    internal = 0
+    for b in range(len(off) - 1):
+        internal += len(set(case["parent"][off[b] + 1:off[b + 1]].tolist()))
+    B = len(off) - 1
+    masked = case.get("retained_mask") is not None
+    row = 4 * V
+    mrow = 4 * ((V + 31) // 32)
+    per_node = 4 * 4 * int(off[-1])
+    return int(internal * row + (internal * (row + mrow) if masked else 0)
+               + B * (2 * row + (mrow if masked else 0)) + per_node)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def ncu_traffic(cfg_num):
+    """dram bytes per attention launch from a committed ncu summary, only if it
+    was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    h = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()[:16]
+    e = d.get(str(cfg_num))
+    if not e or e.get("kernel_sha") != h:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index):
+        self.p = None
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(dev_index)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(case, budget_s, threads=None):
+    """The oracle as it stands, on the host cores, on a bounded sample of the
+    same workload: chunks of up to 8 tree nodes (attention for all their query
+    heads), and the accept pass of each tree once its last node is done,
+    until about `budget_s` seconds of CPU work."""
+    import oracle
+    oracle.build()
+    threads = threads or oracle.default_threads()
+    off = case["node_offsets"]
+    hq = case["num_q_heads"]
+    B = case["batch"]
+    done, trees, t0 = 0, 0, time.perf_counter()
+    b, i0 = 0, 0
+    while True:
+        N = int(off[b + 1] - off[b])
+        i1 = min(N, i0 + 8)
+        rows = np.array([(b, i, h) for i in range(i0, i1) for h in range(hq)], np.int32)
+        oracle.tree_attention_rows(case, rows, nthreads=threads)
+        done += i1 - i0
+        if i1 == N:
+            sl = slice(off[b], off[b + 1])
+            sub = {k: case[k] for k in ("vocab", "kind", "max_nodes")}
+            sub.update(node_offsets=np.array([0, N], np.int32), parent=case["parent"][sl],
+                       target=case["target"][sl], draft_probs=case["draft_probs"][sl],
+                       draft_tokens=case["draft_tokens"][sl], uniforms=case["uniforms"][sl],
+                       retained_mask=None if case.get("retained_mask") is None
+                       else case["retained_mask"][sl])
+            oracle.accept(sub, nthreads=threads, want_pq=False)
+            trees += 1
+            b, i0 = (b + 1) % B, 0
+        else:
+            i0 = i1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": done / el, "unit": UNIT, "cores": int(threads), "kind": "oracle",
+            "sample": f"{done} tree nodes (all query heads; attention over the full prefix) and "
+                      f"{trees} complete accept pass(es) in {el:.1f} s"}
+
+
+def run_reference(args):
+    cfg = wl.config(args.config)
+    case = wl.make_case(cfg, parts=("attn", "accept"), kind=args.mode)
+    per_step = min(2.0, 120.0 / max(1, args.steps))
+    cpu_baseline(case, min(per_step, 0.5))  # warm-up: builds and pages in the oracle
+    t0 = time.perf_counter()
+    nodes = 0.0
+    last = None
+    for _ in range(args.steps):
+        r = cpu_baseline(case, per_step)
+        nodes += r["value"] * per_step
+        last = r
+    el = time.perf_counter() - t0
+    value = nodes / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_desc(cfg, case),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": last["cores"],
+                             "kind": "oracle",
+                             "sample": f"{args.steps} steps of about {per_step:.2f} s each; "
+                                       f"last step: {last['sample']}"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+
+    import torch
+    import speculative_decoding_tree_attention_gb300 as tv
+    from speculative_decoding_tree_attention_gb300 import _build
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+    tv.load()
+
+    cfg = wl.config(args.config)
+    case = wl.make_case(cfg, parts=("attn", "accept"), kind=args.mode)
+    tot = int(case["node_offsets"][-1])
+    B = cfg["batch"]
+
+    def to_dev(x, dtype):
+        return torch.from_numpy(np.ascontiguousarray(x).view(dtype)).to(dev)
+
+    host = {
+        "q": case["q"].view(np.int16), "kp": case["k_prefix"].view(np.int16),
+        "vp": case["v_prefix"].view(np.int16), "table": case["block_table"],
+        "kn": case["k_nodes"].view(np.int16), "vn": case["v_nodes"].view(np.int16),
+        "parent": case["parent"], "lens": case["prefix_lens"], "off": case["node_offsets"],
+        "target": case["target"], "draft": case["draft_probs"], "tokens": case["draft_tokens"],
+        "uniforms": case["uniforms"],
+    }
+    if case.get("retained_mask") is not None:
+        host["mask"] = case["retained_mask"].view(np.int32)
+    d = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in host.items()}
+    for k in ("q", "kp", "vp", "kn", "vn"):
+        d[k] = d[k].view(torch.bfloat16)
+    mask = d.get("mask")
+    max_nodes = int(case["max_nodes"])
+    mpl = int(max(1, int(np.max(case["prefix_lens"]))))
+    prm = tv.attention_params(d["q"], d["kp"], d["table"], d["lens"], num_kv_heads=cfg["hkv"],
+                              max_nodes=max_nodes, max_prefix_len=mpl)
+    ws_bytes = tv.attention_workspace_size(prm)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(d["q"])
+    st_attn = torch.empty(B, dtype=torch.int32, device=dev)
+    acc_out = {"accepted_len": torch.empty(B, dtype=torch.int32, device=dev),
+               "path": torch.empty(B, max_nodes, dtype=torch.int32, device=dev),
+               "bonus_token": torch.empty(B, dtype=torch.int32, device=dev),
+               "status": torch.empty(B, dtype=torch.int32, device=dev)}
+    launches_per_step = 2 + (1 if ws_bytes > 0 else 0)
+
+    def attn(src):
+        tv.tree_attention(src["q"], src["kp"], src["vp"], src["table"], src["kn"], src["vn"],
+                          src["parent"], src["lens"], src["off"], max_nodes=max_nodes,
+                          max_prefix_len=mpl, out=out, status=st_attn, workspace=ws)
+
+    def acc(src):
+        tv.accept(src["target"], src["draft"], src["tokens"], src["parent"], src["off"],
+                  src["uniforms"], src.get("mask"), max_nodes=max_nodes, kind=args.mode,
+                  outputs=acc_out)
+
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            attn(d)
+            acc(d)
+        stream.synchronize()
+        assert int(st_attn.max()) == 0 and int(acc_out["status"].max()) == 0, "device status"
+        graph_a = graph_b = None
+        if not args.no_graph:
+            graph_a = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_a, stream=stream):
+                attn(d)
+            graph_b = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_b, stream=stream):
+                acc(d)
+            for _ in range(max(3, args.warmup)):
+                graph_a.replay()
+                graph_b.replay()
+            stream.synchronize()
+
+    def run_attn():
+        graph_a.replay() if graph_a is not None else attn(d)
+
+    def run_acc():
+        graph_b.replay() if graph_b is not None else acc(d)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    clocks = Clocks(vis[local] if local < len(vis) and vis[local].strip().isdigit() else local)
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)  # evicts the inputs from L2 (outside the events)
+            e0, e1, e2 = ev[k]
+            e0.record(stream)
+            run_attn()
+            e1.record(stream)
+            run_acc()
+            e2.record(stream)
+    stream.synchronize()
+    wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    attn_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    acc_ms = [b.elapsed_time(c) for _, b, c in ev]
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+
+    # ---- end to end through the public API with host buffers
+    pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()}
+    e2e_src = {k: torch.empty_like(d[k].view(pinned[k].dtype)) for k in host}
+    res_host = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in acc_out.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = sum(v.numel() * v.element_size() for v in res_host.values())
+    e2e_steps = max(3, min(args.steps, 50))
+    with torch.cuda.stream(stream):
+        src = dict(e2e_src)
+        for k in ("q", "kp", "vp", "kn", "vn"):
+            src[k] = e2e_src[k].view(torch.bfloat16)
+        for _ in range(2):
+            for k in host:
+                e2e_src[k].copy_(pinned[k], non_blocking=True)
+            attn(src)
+            acc(src)
+        stream.synchronize()
+        e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_a.record(stream)
+        for _ in range(e2e_steps):
+            for k in host:
+                e2e_src[k].copy_(pinned[k], non_blocking=True)
+            attn(src)
+            acc(src)
+            for k in res_host:
+                res_host[k].copy_(acc_out[k], non_blocking=True)
+        e_b.record(stream)
+    stream.synchronize()
+    e2e_s = e_a.elapsed_time(e_b) / 1e3
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peak, peak_kind = load_peaks()
+    a_bytes = attention_bytes(case)
+    attn_mean_s = statistics.mean(attn_ms) / 1e3
+    achieved = a_bytes / attn_mean_s / 1e9
+    acc_mean_s = statistics.mean(acc_ms) / 1e3
+    tr = ncu_traffic(cfg["num"])
+    value = world * tot * args.steps / total_s
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes of the pages' workloads, no datasets or weights)",
+        "config": dict(workload_desc(cfg, case), accept_input=args.mode,
+                       l2="flushed between timed steps (512 MiB write)",
+                       launch="CUDA graph replay" if graph_a is not None else "eager",
+                       parallelism="replicas" if world > 1 else "single GPU"),
+        "roofline": {"kernel": "tree_attn_kernel (+ status memset"
+                               + (" + split merge)" if ws_bytes > 0 else ")"),
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": tr, "algorithmic_bytes": a_bytes,
+                     "flops": attention_flops(case), "mean_us": attn_mean_s * 1e6},
+        "accept": {"mean_us": acc_mean_s * 1e6, "trees_per_s": B / acc_mean_s,
+                   "algorithmic_bytes": accept_bytes(case),
+                   "achieved_gbs": accept_bytes(case) / acc_mean_s / 1e9},
+        "e2e": {"value": world * tot * e2e_steps / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed_loop": wall,
+    }
+    if world == 1 and args.cpu_seconds > 0:
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

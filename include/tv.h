@@ -1,0 +1,187 @@
+/*
+ * tv.h -- C ABI of libtv: the target-model tree-verification step of
+ * speculative decoding, on one GB300 GPU (sm_103a).
+ *
+ * Sources (four web pages on speculative decoding; titles abbreviated):
+ *   [EC]  "端云协同推测解码中草稿模型动态生成与验证并行化：探究树形注意力机制与显存碎片整理联合加速"
+ *         (edge-cloud speculative decoding; tree attention; KV defragmentation)
+ *   [LLM] "端侧大模型推测解码草稿模型动态剪枝策略：详解基于重要性采样的树形验证并行加速机制"
+ *         (on-device LLM draft pruning; importance-sampling correction)
+ *   [MM]  "端侧多模态大模型推测解码草稿模型动态剪枝：详解基于重要性采样的树形验证并行加速策略"
+ *         (on-device multimodal draft pruning; importance-sampled tree verification)
+ *
+ * General rules for every entry point
+ *   - The caller owns every buffer.  The library allocates nothing, frees
+ *     nothing and never synchronises the device or the stream; all work is
+ *     enqueued on the caller's stream in order.
+ *   - Pointers are DEVICE pointers unless a comment says "host".
+ *   - Inputs are read only.  Outputs are fully written when the call returns
+ *     TV_OK and the enqueued work completes.
+ *   - Argument errors are found on the host and returned before anything is
+ *     enqueued.  Data errors found on the device (a bad parent index, an
+ *     out-of-range block id or token) are reported per sequence in the
+ *     device-side `status` array; the kernels never trap.
+ *   - Stateless and re-entrant: concurrent calls on different streams are
+ *     safe when their workspaces differ.
+ *
+ * Tree convention (shared by both entry points)
+ *   Sequence b owns tree nodes node_offsets[b] .. node_offsets[b+1]-1 of the
+ *   flattened node arrays ([EC] appendix B: cumulative lengths over the
+ *   flattened tree).  parent[] holds LOCAL indices (0 .. N_b-1): parent of
+ *   the root (local node 0) is -1 and 0 <= parent[i] < i for i >= 1
+ *   ([EC] appendix B, Tree_Parent_Idx, -1 at the root).  Node 0 is the last
+ *   committed token; nodes >= 1 are draft tokens.
+ */
+#ifndef TV_H_
+#define TV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TV_VERSION 100     /* 1.0.0 */
+#define TV_MAX_NODES 512   /* largest tree (nodes per sequence) */
+#define TV_BLOCK_SIZE 16   /* tokens per page of the paged prefix KV pool */
+
+typedef enum {
+  TV_OK = 0,
+  TV_ERR_INVALID_ARG = 1,    /* null pointer, bad size or layout (host) */
+  TV_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. head_dim) */
+  TV_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required */
+  TV_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
+  TV_ERR_BAD_TREE = 5,       /* device: malformed tree, block id or token */
+  TV_ERR_DEVICE_TIMEOUT = 6  /* device: a bounded wait ran out */
+} tv_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* tv_status_string(int status);
+/* TV_VERSION of the loaded library. */
+int tv_version(void);
+
+/* ========================================================================
+ * Tree attention
+ *
+ * For every sequence b, tree node i (local) and query head h, with KV head
+ * kvh = floor(h / (Hq/Hkv)):
+ *
+ *   out[n0+i][h] = sum_k softmax_k(scale * q.k_k) * v_k
+ *
+ * over the key list [prefix tokens 0 .. L_b-1 ; tree nodes j of sequence b]
+ * where every prefix token is visible and tree node j is visible iff j is an
+ * ancestor of i or j == i: the tree mask M_tree[i,j] = 0 iff j is an ancestor
+ * of i or j = i, -inf otherwise ([EC] §2.2.2).  The committed prefix KV is
+ * stored once in a paged pool and reached through block_table ([MM] §3.2
+ * common-prefix merging; [LLM] §2.3.1 cuSeqLens + block_table).  One launch
+ * handles every sequence, every head and every node ([MM] §3.2: one kernel
+ * for all branches).  Inputs bf16, accumulation and softmax fp32, output bf16.
+ * ====================================================================== */
+typedef struct {
+  int32_t batch;              /* B >= 1                                        */
+  int32_t num_q_heads;        /* Hq                                            */
+  int32_t num_kv_heads;       /* Hkv; Hq % Hkv == 0                            */
+  int32_t head_dim;           /* D: 64 or 128                                  */
+  int32_t block_size;         /* tokens per page: must be TV_BLOCK_SIZE (16)   */
+  int32_t max_blocks_per_seq; /* row stride of block_table                     */
+  int32_t num_blocks;         /* pages in the pool                             */
+  int32_t max_nodes;          /* upper bound of N_b (<= TV_MAX_NODES)          */
+  int32_t total_nodes;        /* node_offsets[batch] (host copy)               */
+  int32_t max_prefix_len;     /* upper bound of L_b (host hint for the grid)   */
+  float softmax_scale;        /* 0 => 1/sqrt(D)                                */
+} tv_attn_params;             /* host struct */
+
+/* Bytes of device workspace tv_tree_attention needs for these parameters
+ * (split-KV partial results).  0 on invalid parameters. */
+size_t tv_tree_attention_workspace_size(const tv_attn_params* params);
+
+/* Layouts (all row-major, contiguous):
+ *   q_nodes          bf16 [total_nodes][Hq][D]
+ *   k_prefix_blocks  bf16 [num_blocks][Hkv][block_size][D]   (paged pool)
+ *   v_prefix_blocks  bf16 [num_blocks][Hkv][block_size][D]
+ *   block_table      int32 [batch][max_blocks_per_seq]: page of logical block
+ *                    t/16 of sequence b; entries past ceil(L_b/16) unused
+ *   k_nodes, v_nodes bf16 [total_nodes][Hkv][D]   (K/V of the tree tokens)
+ *   parent           int32 [total_nodes]  local parent, -1 at each root
+ *   prefix_lens      int32 [batch]        L_b >= 0 (<= max_prefix_len)
+ *   node_offsets     int32 [batch+1]      cumulative node counts, N_b >= 1
+ *   out              bf16 [total_nodes][Hq][D]
+ *   status           int32 [batch]        per-sequence TV_OK / TV_ERR_BAD_TREE /
+ *                                         TV_ERR_DEVICE_TIMEOUT (device)
+ *   workspace        device bytes >= tv_tree_attention_workspace_size()
+ * bf16 pointers are passed as uint16_t (bf16 bit patterns).  All device
+ * pointers must be 16-byte aligned.  A sequence whose tree or block ids are
+ * malformed gets status TV_ERR_BAD_TREE and an all-zero output. */
+int tv_tree_attention(const tv_attn_params* params, const uint16_t* q_nodes,
+                      const uint16_t* k_prefix_blocks, const uint16_t* v_prefix_blocks,
+                      const int32_t* block_table, const uint16_t* k_nodes,
+                      const uint16_t* v_nodes, const int32_t* parent,
+                      const int32_t* prefix_lens, const int32_t* node_offsets, uint16_t* out,
+                      int32_t* status, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
+/* ========================================================================
+ * Fused accept pass ([EC] §2.2.3; [LLM] §2.2.1-§2.2.2, §7.1)
+ *
+ * Per tree b, for every draft node i >= 1 with parent j:
+ *   p = target probability of token x_i in row j (probs given, or softmax of
+ *       the logits row, fp32), q = draft probability of x_i in row j.
+ *   Pruning renormalisation when retained_mask is given: on the retained set
+ *   R_j, p~ = p / Z_j and q~ = q / Z_j (log space: add log(1/Z_j)); off R_j
+ *   p~ = q~ = 0 (log space: -inf).  Z_j = the retained draft mass, summed
+ *   exactly in 2^-40 fixed point and rounded once to fp32.  Without a mask
+ *   p~ = p, q~ = q.
+ *   Test: a_i = fl32(u_i * q~) < p~  (u < min(1, p~/q~), strict, NaN rejects).
+ * Walk: the deepest node whose whole root path is accepted (cut at the first
+ *   rejection), ties to the smallest index; accepted_len = its depth.
+ * Bonus token: from the cut node j*: if j* has children, the residual
+ *   max(0, p~ - q~) of row j*; if it is a leaf or the residual is all zero,
+ *   p~ of row j*; if that is all zero too, the smallest index of max p~.
+ *   The draw is an exact inverse CDF in 2^-40 fixed point: quanta
+ *   f_v = floor(min(r_v, 32) * 2^40), S = sum f_v (uint64),
+ *   t = floor(u_0 * S), token = min v with f_0 + .. + f_v > t.
+ * ====================================================================== */
+typedef enum { TV_INPUT_PROBS = 0, TV_INPUT_LOGITS = 1 } tv_input_kind;
+
+typedef struct {
+  int32_t batch;        /* B >= 1                                           */
+  int32_t vocab;        /* V, 1 <= V < 2^18                                 */
+  int32_t max_nodes;    /* row stride of `path`; >= every N_b, <= TV_MAX_NODES */
+  int32_t total_nodes;  /* node_offsets[batch] (host copy)                  */
+  int32_t kind;         /* tv_input_kind: the form of `target`              */
+} tv_accept_params;     /* host struct */
+
+/* Bytes of device workspace tv_accept needs (0: it needs none). */
+size_t tv_accept_workspace_size(const tv_accept_params* params);
+
+/* Layouts:
+ *   target        fp32 [total_nodes][V]  row j = target next-token
+ *                 probabilities (or logits) after node j
+ *   draft_probs   fp32 [total_nodes][V]  row j = draft probabilities after node j
+ *   draft_tokens  int32 [total_nodes]    token of node i (node 0 unused)
+ *   parent, node_offsets                 as for tree attention
+ *   uniforms      fp32 [total_nodes]     u_i in [0,1) tests node i >= 1;
+ *                                        u at each root is the bonus draw u_0
+ *   retained_mask uint32 [total_nodes][ceil(V/32)] or NULL: bit v%32 of word
+ *                 v/32 of row j set iff v is in R_j
+ *   accepted_len  int32 [batch]          accepted draft tokens (-1 on error)
+ *   path          int32 [batch][max_nodes]: local ids of the accepted path at
+ *                 depths 1..accepted_len, then -1
+ *   bonus_token   int32 [batch]          (-1 on error)
+ *   status        int32 [batch]
+ *   debug_pq      fp32 [total_nodes][2] or NULL: (p~, q~) used by the test of
+ *                 each node (0, 0 at roots)
+ * All device pointers 16-byte aligned; V * 4 a multiple of 16 is not required. */
+int tv_accept(const tv_accept_params* params, const float* target, const float* draft_probs,
+              const int32_t* draft_tokens, const int32_t* parent, const int32_t* node_offsets,
+              const float* uniforms, const uint32_t* retained_mask, int32_t* accepted_len,
+              int32_t* path, int32_t* bonus_token, int32_t* status, float* debug_pq,
+              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TV_H_ */

@@ -53,7 +53,7 @@ class _AcceptArgs(C.Structure):
         ("batch", C.c_int), ("vocab", C.c_int), ("kind", C.c_int), ("max_nodes", C.c_int),
         ("target", C.c_void_p), ("draft_probs", C.c_void_p), ("draft_tokens", C.c_void_p),
         ("parent", C.c_void_p), ("node_offsets", C.c_void_p), ("uniforms", C.c_void_p),
-        ("retained_mask", C.c_void_p), ("pq_replay", C.c_void_p),
+        ("retained_mask", C.c_void_p),
         ("accepted_len", C.c_void_p), ("path", C.c_void_p), ("bonus_token", C.c_void_p),
         ("status", C.c_void_p), ("pq_out", C.c_void_p),
     ]
@@ -132,7 +132,7 @@ def tree_attention(case: dict, nthreads: int | None = None) -> np.ndarray:
     return out.reshape(tot, case["num_q_heads"], case["head_dim"])
 
 
-def accept(case: dict, pq_replay=None, nthreads: int | None = None, want_pq: bool = True) -> dict:
+def accept(case: dict, nthreads: int | None = None, want_pq: bool = True) -> dict:
     """Oracle accept pass.  Returns accepted_len, path, bonus_token, status, pq."""
     lib = _load()
     off = _c(case["node_offsets"], np.int32)
@@ -146,7 +146,6 @@ def accept(case: dict, pq_replay=None, nthreads: int | None = None, want_pq: boo
         "parent": _c(case["parent"], np.int32),
         "uniforms": _c(case["uniforms"], np.float32),
         "retained_mask": _c(case.get("retained_mask"), np.uint32),
-        "pq_replay": _c(pq_replay, np.float32),
     }
     out = {
         "accepted_len": np.zeros(batch, np.int32),
@@ -159,7 +158,7 @@ def accept(case: dict, pq_replay=None, nthreads: int | None = None, want_pq: boo
     args = _AcceptArgs(batch, int(case["vocab"]), kind, max_nodes,
                        _ptr(keep["target"]), _ptr(keep["draft_probs"]), _ptr(keep["draft_tokens"]),
                        _ptr(keep["parent"]), _ptr(off), _ptr(keep["uniforms"]),
-                       _ptr(keep["retained_mask"]), _ptr(keep["pq_replay"]),
+                       _ptr(keep["retained_mask"]),
                        _ptr(out["accepted_len"]), _ptr(out["path"]), _ptr(out["bonus_token"]),
                        _ptr(out["status"]), _ptr(out["pq"]))
     rc = lib.oracle_accept(C.byref(args), int(nthreads or default_threads()))

@@ -205,7 +205,6 @@ typedef struct {
   const int32_t *node_offsets;  /* [batch+1]        */
   const float *uniforms;        /* [total_nodes]    */
   const uint32_t *retained_mask;/* NULL or [total_nodes][ceil(V/32)] */
-  const float *pq_replay;       /* NULL or [total_nodes][2]: use these (p~, q~) in the tests */
   int32_t *accepted_len;        /* [batch] */
   int32_t *path;                /* [batch][max_nodes] */
   int32_t *bonus_token;         /* [batch] */
@@ -341,10 +340,6 @@ static void accept_one_tree(const oracle_accept_args *a, int b) {
         p = 0.0f;
         q = 0.0f;
       }
-    }
-    if (a->pq_replay) {
-      p = a->pq_replay[2 * (size_t)(n0 + i) + 0];
-      q = a->pq_replay[2 * (size_t)(n0 + i) + 1];
     }
     pt[i] = p;
     qt[i] = q;

@@ -1,0 +1,195 @@
+"""Tree verification for speculative decoding on GB300 (sm_103a).
+
+Thin Python binding over the C-ABI library ``libtv.so`` (declared in
+``include/tv.h``): argument marshalling only.  Every step of the computation
+runs in the library's CUDA kernels; there is no CPU or PyTorch fallback, and
+the functions raise if the library cannot be loaded.
+
+PyTorch is used for device memory and the current CUDA stream only.
+
+    tree_attention(...)  -> out, status      (tv_tree_attention)
+    accept(...)          -> dict of outputs  (tv_accept)
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+__all__ = ["TVError", "load", "tree_attention", "accept", "attention_workspace_size",
+           "TV_MAX_NODES", "TV_OK", "TV_ERR_BAD_TREE", "TV_ERR_DEVICE_TIMEOUT", "status_string"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libtv.so")
+
+TV_OK = 0
+TV_ERR_INVALID_ARG = 1
+TV_ERR_UNSUPPORTED = 2
+TV_ERR_WORKSPACE = 3
+TV_ERR_CUDA = 4
+TV_ERR_BAD_TREE = 5
+TV_ERR_DEVICE_TIMEOUT = 6
+TV_MAX_NODES = 512
+TV_BLOCK_SIZE = 16
+EXPORTS = ("tv_status_string", "tv_version", "tv_tree_attention_workspace_size",
+           "tv_tree_attention", "tv_accept_workspace_size", "tv_accept")
+
+
+class TVError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+class AttnParams(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("num_q_heads", C.c_int32), ("num_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("block_size", C.c_int32),
+                ("max_blocks_per_seq", C.c_int32), ("num_blocks", C.c_int32),
+                ("max_nodes", C.c_int32), ("total_nodes", C.c_int32),
+                ("max_prefix_len", C.c_int32), ("softmax_scale", C.c_float)]
+
+
+class AcceptParams(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("vocab", C.c_int32), ("max_nodes", C.c_int32),
+                ("total_nodes", C.c_int32), ("kind", C.c_int32)]
+
+
+_lib = None
+
+
+def load(path: str | None = None) -> C.CDLL:
+    """Loads libtv.so (built in-tree by ``_build.build()``); raises if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise OSError(f"libtv.so not found at {p}: build it with "
+                      "speculative_decoding_tree_attention_gb300._build.build()")
+    lib = C.CDLL(p)
+    vp, sz = C.c_void_p, C.c_size_t
+    lib.tv_status_string.argtypes = [C.c_int]
+    lib.tv_status_string.restype = C.c_char_p
+    lib.tv_version.restype = C.c_int
+    lib.tv_tree_attention_workspace_size.argtypes = [C.POINTER(AttnParams)]
+    lib.tv_tree_attention_workspace_size.restype = sz
+    lib.tv_tree_attention.argtypes = [C.POINTER(AttnParams)] + [vp] * 11 + [vp, sz, vp]
+    lib.tv_tree_attention.restype = C.c_int
+    lib.tv_accept_workspace_size.argtypes = [C.POINTER(AcceptParams)]
+    lib.tv_accept_workspace_size.restype = sz
+    lib.tv_accept.argtypes = [C.POINTER(AcceptParams)] + [vp] * 12 + [vp, sz, vp]
+    lib.tv_accept.restype = C.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().tv_status_string(int(code)).decode()
+    except OSError:
+        return {0: "TV_OK", 1: "TV_ERR_INVALID_ARG", 2: "TV_ERR_UNSUPPORTED",
+                3: "TV_ERR_WORKSPACE", 4: "TV_ERR_CUDA", 5: "TV_ERR_BAD_TREE",
+                6: "TV_ERR_DEVICE_TIMEOUT"}.get(int(code), "TV_ERR_UNKNOWN")
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _check_dev(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def attention_params(q_nodes, k_prefix_blocks, block_table, prefix_lens, *, num_kv_heads,
+                     max_nodes, max_prefix_len, softmax_scale=0.0) -> AttnParams:
+    total, hq, d = q_nodes.shape
+    nb = k_prefix_blocks.shape[0]
+    return AttnParams(int(prefix_lens.shape[0]), int(hq), int(num_kv_heads), int(d),
+                      int(k_prefix_blocks.shape[2]), int(block_table.shape[1]), int(nb),
+                      int(max_nodes), int(total), int(max_prefix_len), float(softmax_scale))
+
+
+def attention_workspace_size(params: AttnParams) -> int:
+    return int(load().tv_tree_attention_workspace_size(C.byref(params)))
+
+
+def tree_attention(q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nodes, v_nodes,
+                   parent, prefix_lens, node_offsets, *, max_nodes: int, max_prefix_len: int,
+                   softmax_scale: float = 0.0, out=None, status=None, workspace=None,
+                   stream=None):
+    """tv_tree_attention on the current stream.  Shapes as in include/tv.h:
+    q_nodes [total, Hq, D] bf16; k/v_prefix_blocks [num_blocks, Hkv, 16, D] bf16;
+    block_table [B, max_blocks] int32; k/v_nodes [total, Hkv, D] bf16;
+    parent [total] int32; prefix_lens [B] int32; node_offsets [B+1] int32.
+    Returns (out, status); nothing is synchronised."""
+    import torch
+    lib = load()
+    _check_dev(q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nodes, v_nodes,
+               parent, prefix_lens, node_offsets)
+    prm = attention_params(q_nodes, k_prefix_blocks, block_table, prefix_lens,
+                           num_kv_heads=k_prefix_blocks.shape[1], max_nodes=max_nodes,
+                           max_prefix_len=max_prefix_len, softmax_scale=softmax_scale)
+    if out is None:
+        out = torch.empty_like(q_nodes)
+    if status is None:
+        status = torch.empty(prm.batch, dtype=torch.int32, device=q_nodes.device)
+    need = int(lib.tv_tree_attention_workspace_size(C.byref(prm)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_nodes.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.tv_tree_attention(C.byref(prm), _ptr(q_nodes), _ptr(k_prefix_blocks),
+                               _ptr(v_prefix_blocks), _ptr(block_table), _ptr(k_nodes),
+                               _ptr(v_nodes), _ptr(parent), _ptr(prefix_lens),
+                               _ptr(node_offsets), _ptr(out), _ptr(status), _ptr(workspace),
+                               C.c_size_t(ws_bytes), _stream(stream))
+    if rc != TV_OK:
+        raise TVError(rc, "tv_tree_attention")
+    return out, status
+
+
+def accept(target, draft_probs, draft_tokens, parent, node_offsets, uniforms,
+           retained_mask=None, *, max_nodes: int, kind: str = "probs", debug_pq: bool = False,
+           outputs: dict | None = None, stream=None) -> dict:
+    """tv_accept on the current stream.  target/draft_probs [total, V] fp32,
+    draft_tokens/parent [total] int32, node_offsets [B+1] int32, uniforms
+    [total] fp32, retained_mask [total, ceil(V/32)] int32/uint32 or None.
+    Returns dict(accepted_len, path, bonus_token, status, debug_pq)."""
+    import torch
+    lib = load()
+    _check_dev(target, draft_probs, draft_tokens, parent, node_offsets, uniforms, retained_mask)
+    total, V = target.shape
+    B = node_offsets.shape[0] - 1
+    dev = target.device
+    prm = AcceptParams(int(B), int(V), int(max_nodes), int(total),
+                       1 if kind == "logits" else 0)
+    o = outputs or {}
+    acc = o.get("accepted_len")
+    if acc is None:
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+    path = o.get("path")
+    if path is None:
+        path = torch.empty(B, max_nodes, dtype=torch.int32, device=dev)
+    bonus = o.get("bonus_token")
+    if bonus is None:
+        bonus = torch.empty(B, dtype=torch.int32, device=dev)
+    status = o.get("status")
+    if status is None:
+        status = torch.empty(B, dtype=torch.int32, device=dev)
+    dpq = o.get("debug_pq")
+    if dpq is None and debug_pq:
+        dpq = torch.empty(total, 2, dtype=torch.float32, device=dev)
+    rc = lib.tv_accept(C.byref(prm), _ptr(target), _ptr(draft_probs), _ptr(draft_tokens),
+                       _ptr(parent), _ptr(node_offsets), _ptr(uniforms), _ptr(retained_mask),
+                       _ptr(acc), _ptr(path), _ptr(bonus), _ptr(status), _ptr(dpq), None,
+                       C.c_size_t(0), _stream(stream))
+    if rc != TV_OK:
+        raise TVError(rc, "tv_accept")
+    return dict(accepted_len=acc, path=path, bonus_token=bonus, status=status, debug_pq=dpq)

@@ -1,0 +1,600 @@
+// tree_attn_kernel.cu -- tree attention over a shared paged prefix on sm_103a.
+//
+// Sources (titles abbreviated):
+//   [EC]  "端云协同推测解码中草稿模型动态生成与验证并行化：探究树形注意力机制与显存碎片整理联合加速":
+//         §2.2.2 the tree mask M_tree[i,j] = 0 iff j is an ancestor of i or
+//         j = i, else -inf; appendix B (a tree FlashAttention loop): parent
+//         index per node, per-node ancestor bitmap, fp32 accumulators and an
+//         online softmax.
+//   [MM]  "端侧多模态大模型推测解码草稿模型动态剪枝：详解基于重要性采样的树形验证并行加速策略":
+//         §3.2 the prefix KV is stored once and reached by index; all
+//         branches flattened into one varlen kernel.
+//   [LLM] "端侧大模型推测解码草稿模型动态剪枝策略：详解基于重要性采样的树形验证并行加速机制":
+//         §2.3.1 variable-length batches through cuSeqLens and block_table.
+//
+// GB300 design.  One CTA computes a 128-row tile of packed query rows of one
+// (sequence, KV head): row R = node * g + head-in-group, so every tree node
+// and every query head of a GQA group share each K/V tile that is staged in
+// shared memory.  The CTA walks its key range in 64-key tiles:
+//   warp 4  (TMA)      loads K and V tiles into a 4-stage ring: four 16-token
+//                      pages per tile through the block table (2D tensor map
+//                      over the pool), or 64 tree nodes (3D tensor map);
+//                      pages past the sequence load as zeros (out of bounds).
+//   warp 5  (MMA)      one thread issues tcgen05.mma: S = Q K^T into a
+//                      double-buffered TMEM tile (128 x 64 fp32), and
+//                      O += P V into a TMEM accumulator (128 x D fp32).
+//   warps 0-3          one thread per row: tcgen05.ld of S, scale, the tree
+//                      mask from a per-node ancestor bitmask (shared memory),
+//                      fp32 online softmax with exp2, rescale of O in TMEM
+//                      only when the running max grows by more than 2^8, P as
+//                      bf16 into a double-buffered, 128B-swizzled shared tile.
+// All operands use the 128-byte swizzle that TMA writes, so the MMA reads
+// them straight from the ring.  Long prefixes are split over CTAs (split-KV):
+// each split writes (O, m, l) in fp32 and a merge kernel combines them.
+// Every wait on an mbarrier is bounded; on expiry the CTA reports
+// TV_ERR_DEVICE_TIMEOUT for its sequence, drains its copies and returns.
+#include "tv_device.cuh"
+#include "tv_launch.h"
+
+namespace tv {
+namespace {
+
+constexpr int BM = 128;           // packed query rows per CTA
+constexpr int BN = 64;            // keys per tile
+constexpr int kStages = 4;        // K/V ring depth
+constexpr int kThreads = 192;     // 4 softmax warps + TMA warp + MMA warp
+constexpr int kMaxAncWords = 16;  // 512-node trees
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct Layout {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQ = 0;
+  static constexpr int kQBytes = BM * D * 2;
+  static constexpr int kTileBytes = BN * D * 2;  // one K or V tile
+  static constexpr int kHalfBytes = BN * 128;    // one 64-column half of a tile
+  static constexpr int kStage0 = kQ + kQBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kP0 = kStage0 + kStages * kStageBytes;
+  static constexpr int kPBytes = BM * BN * 2;
+  static constexpr int kAnc = kP0 + 2 * kPBytes;
+  static constexpr int kAncBytes = BM * kMaxAncWords * 4;
+  static constexpr int kParent = kAnc + kAncBytes;
+  static constexpr int kParentBytes = 512 * 4;
+  static constexpr int kBar = kParent + kParentBytes;
+  // full[kStages], empty[kStages], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int kNumBars = 2 * kStages + 7;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kTotal = kMisc + 64;
+  static constexpr int kAlloc = kTotal + 1024;  // slack for 1024-byte alignment
+  static constexpr int kTmemCols = (64 * 2 + D) <= 256 ? 256 : 512;
+};
+
+struct Misc {
+  uint32_t tmem_base;
+  int abort;
+  int bad;
+};
+
+struct Work {
+  int b, kvh, mtile, split;
+  int n0, N, L;
+  int rows;      // N * g
+  int nsplit;    // splits of this sequence
+  int k_begin, k_end;
+  int n_prefix_tiles, n_node_tiles, T;
+  bool last_split;
+};
+
+__device__ __forceinline__ void record_status(int32_t* status, int b, int code) {
+  atomicMax(status + b, code);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    tree_attn_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps) {
+  using Ly = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* s_full = bars + 2 * kStages;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 2;
+  uint64_t* drain = o_done + 2;
+  Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
+  uint32_t* anc = reinterpret_cast<uint32_t*>(smem + Ly::kAnc);
+  int32_t* par = reinterpret_cast<int32_t*>(smem + Ly::kParent);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // ------------------------------------------------------------ work item
+  Work w;
+  w.mtile = blockIdx.x;
+  w.split = blockIdx.y;
+  w.b = blockIdx.z / a.hkv;
+  w.kvh = blockIdx.z % a.hkv;
+  w.n0 = a.node_offsets[w.b];
+  w.N = a.node_offsets[w.b + 1] - w.n0;
+  w.L = max(0, a.prefix_lens[w.b]);
+  w.rows = w.N * a.group;
+  w.nsplit = max(1, (w.L + a.chunk - 1) / a.chunk);
+  if (w.N < 1 || w.mtile * BM >= w.rows || w.split >= w.nsplit) return;  // no work here
+  w.last_split = (w.split == w.nsplit - 1);
+  w.k_begin = w.split * a.chunk;
+  w.k_end = min(w.L, w.k_begin + a.chunk);
+  w.n_prefix_tiles = (w.k_end - w.k_begin + BN - 1) / BN;
+  w.n_node_tiles = w.last_split ? (w.N + BN - 1) / BN : 0;
+  w.T = w.n_prefix_tiles + w.n_node_tiles;
+  const int node_lo = (w.mtile * BM) / a.group;
+  const int g = a.group;
+
+  // ------------------------------------------------------------ prologue
+  if (tid == 0) {
+    misc->abort = 0;
+    misc->bad = (w.N > a.max_nodes || w.N > 512 || w.L > a.max_prefix_len || w.n0 < 0 ||
+                 w.n0 + w.N > a.total_nodes) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!misc->bad) {
+    for (int i = tid; i < w.N; i += kThreads) {
+      const int p = a.parent[w.n0 + i];
+      par[i] = p;
+      if (!(i == 0 ? p == -1 : (p >= 0 && p < i))) misc->bad = 1;
+    }
+    // block ids of this split's pages
+    const int pg0 = w.k_begin / 16, pg1 = (w.k_end + 15) / 16;
+    for (int pg = pg0 + tid; pg < pg1; pg += kThreads) {
+      if (pg >= a.max_blocks_per_seq) {
+        misc->bad = 1;
+        break;
+      }
+      const int blk = a.block_table[static_cast<size_t>(w.b) * a.max_blocks_per_seq + pg];
+      if (blk < 0 || blk >= a.num_blocks) misc->bad = 1;
+    }
+  }
+  __syncthreads();
+  const bool bad = misc->bad != 0;
+  if (bad) {
+    if (tid == 0) record_status(a.status, w.b, kBadTree);
+    const bool rows_addressable = w.n0 >= 0 && w.N <= a.max_nodes && w.n0 + w.N <= a.total_nodes;
+    if (w.nsplit == 1 && rows_addressable) {  // the only writer of these rows: zeros
+      for (int r = tid; r < BM; r += kThreads) {
+        const int R = w.mtile * BM + r;
+        if (R >= w.rows) continue;
+        const int i = R / g, h = w.kvh * g + R % g;
+        uint4* dst = reinterpret_cast<uint4*>(a.out + (static_cast<size_t>(w.n0 + i) * a.hq + h) * D);
+        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    return;
+  }
+
+  if (warp < 4) {
+    // Q tile -> shared memory, 128B-swizzled K-major; padding rows are zero.
+    const int r = tid;
+    const int R = w.mtile * BM + r;
+    const bool live = R < w.rows;
+    const uint4* src = nullptr;
+    if (live) {
+      const int i = R / g, h = w.kvh * g + R % g;
+      src = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(w.n0 + i) * a.hq + h) * D);
+    }
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 v = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      const int half = c >> 3, cc = c & 7;
+      *reinterpret_cast<uint4*>(smem + Ly::kQ + half * (BM * 128) + r * 128 +
+                                ((cc ^ (r & 7)) << 4)) = v;
+    }
+    // ancestor-or-self bitmask of the tile's nodes (only node tiles need it)
+    if (w.last_split) {
+      const int i = node_lo + r;
+      uint32_t* row = anc + r * kMaxAncWords;
+#pragma unroll
+      for (int k = 0; k < kMaxAncWords; ++k) row[k] = 0u;
+      if (i < w.N) {
+        for (int k = i; k >= 0; k = par[k]) row[k >> 5] |= 1u << (k & 31);
+      }
+    }
+    fence_proxy_async_smem();  // Q written by the generic proxy, read by the MMA
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&s_full[k], 1);
+      mbar_init(&p_full[k], 128);
+      mbar_init(&o_done[k], 1);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&misc->tmem_base, Ly::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem_base;
+  const uint32_t tmem_s0 = tmem;        // S buffers at columns 0 and 64
+  const uint32_t tmem_o = tmem + 128;   // O accumulator at columns 128 .. 128+D-1
+  volatile int* abort_flag = &misc->abort;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&maps.k_pool);
+      prefetch_tmap(&maps.v_pool);
+      prefetch_tmap(&maps.k_nodes);
+      prefetch_tmap(&maps.v_nodes);
+      const int pool_rows = a.num_blocks * a.hkv * 16;
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < w.T && ok; ++t) {
+        const int st = t % kStages;
+        if (!mbar_wait(&empty[st], ((t / kStages) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* kdst = smem + Ly::kStage0 + st * Ly::kStageBytes;
+        uint8_t* vdst = kdst + Ly::kTileBytes;
+        mbar_arrive_expect_tx(&full[st], 2 * Ly::kTileBytes);
+        if (t < w.n_prefix_tiles) {
+          const int key0 = w.k_begin + t * BN;
+#pragma unroll
+          for (int pg = 0; pg < BN / 16; ++pg) {
+            const int lp = key0 / 16 + pg;
+            int row = pool_rows;  // out of bounds: zero fill
+            if (lp * 16 < w.k_end) {
+              const int blk = __ldg(a.block_table + static_cast<size_t>(w.b) * a.max_blocks_per_seq + lp);
+              row = (blk * a.hkv + w.kvh) * 16;
+            }
+#pragma unroll
+            for (int h = 0; h < Ly::kHalves; ++h) {
+              tma_load_2d(kdst + h * Ly::kHalfBytes + pg * 2048, &maps.k_pool, &full[st], h * 64, row);
+              tma_load_2d(vdst + h * Ly::kHalfBytes + pg * 2048, &maps.v_pool, &full[st], h * 64, row);
+            }
+          }
+        } else {
+          const int node0 = w.n0 + (t - w.n_prefix_tiles) * BN;
+#pragma unroll
+          for (int h = 0; h < Ly::kHalves; ++h) {
+            tma_load_3d(kdst + h * Ly::kHalfBytes, &maps.k_nodes, &full[st], h * 64, w.kvh, node0);
+            tma_load_3d(vdst + h * Ly::kHalfBytes, &maps.v_nodes, &full[st], h * 64, w.kvh, node0);
+          }
+        }
+        ++issued;
+      }
+      if (!ok) {
+        record_status(a.status, w.b, kDeviceTimeout);
+        misc->abort = 1;
+      }
+      // drain: every issued copy has landed before the CTA may exit
+      for (int t = max(0, issued - kStages); t < issued; ++t)
+        mbar_wait(&full[t % kStages], (t / kStages) & 1);
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);
+      constexpr uint32_t idesc_o = idesc_bf16(BM, D, 1);
+      const uint32_t q_base = smem_u32(smem + Ly::kQ);
+      bool ok = true;
+      auto issue_s = [&](int t) -> bool {
+        const int st = t % kStages;
+        if (!mbar_wait(&full[st], (t / kStages) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t k_base = smem_u32(smem + Ly::kStage0 + st * Ly::kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 0 + ((kk & 3) << 5);
+          const uint64_t ad = smem_desc(q_base + (kk >> 2) * (BM * 128) + off, 16, 1024);
+          const uint64_t bd = smem_desc(k_base + (kk >> 2) * Ly::kHalfBytes + off, 16, 1024);
+          mma_bf16_ss(tmem_s0 + (t & 1) * BN, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[t & 1]);
+        return true;
+      };
+      auto issue_pv = [&](int t) -> bool {
+        const int st = t % kStages;
+        if (!mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t p_base = smem_u32(smem + Ly::kP0 + (t & 1) * Ly::kPBytes);
+        const uint32_t v_base = smem_u32(smem + Ly::kStage0 + st * Ly::kStageBytes + Ly::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t ad = smem_desc(p_base + (kk << 5), 16, 1024);
+          const uint64_t bd = smem_desc(v_base + kk * 2048, Ly::kHalfBytes, 1024);
+          mma_bf16_ss(tmem_o, ad, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&o_done[t & 1]);
+        mma_commit(&empty[st]);
+        return true;
+      };
+      if (w.T > 0) ok = issue_s(0);
+      if (ok && w.T > 1) ok = issue_s(1);
+      for (int t = 0; t < w.T && ok; ++t) {
+        ok = issue_pv(t);
+        if (ok && t + 2 < w.T) ok = issue_s(t + 2);
+      }
+      if (!ok) {
+        record_status(a.status, w.b, kDeviceTimeout);
+        misc->abort = 1;
+      }
+      // drain: all MMAs issued by this thread complete before TMEM is freed
+      mma_commit(drain);
+      mbar_wait(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- softmax warps
+    const int r = tid;                 // row of the tile == TMEM lane
+    const int R = w.mtile * BM + r;
+    const bool live = R < w.rows;
+    const int i_node = live ? R / g : 0;  // local node of this row
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t* my_anc = anc + (i_node - node_lo) * kMaxAncWords;
+    float m_run = -INFINITY;  // reference max (log2 units)
+    float l_run = 0.0f;
+    bool ok = true;
+    for (int t = 0; t < w.T; ++t) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[64];
+      {
+        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+        tmem_ld32(tmem_s0 + (t & 1) * BN + lane_off, lo);
+        tmem_ld32(tmem_s0 + (t & 1) * BN + 32 + lane_off, hi);
+        tmem_ld_wait();
+      }
+      // scale + mask
+      float x[64];
+      float tmax = -INFINITY;
+      int valid_keys = BN;
+      if (t < w.n_prefix_tiles) {
+        valid_keys = min(BN, w.k_end - (w.k_begin + t * BN));
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float s = __uint_as_float(sr[c]) * a.scale_log2;
+          x[c] = c < valid_keys ? s : -INFINITY;
+          tmax = fmaxf(tmax, x[c]);
+        }
+      } else {
+        const int j0 = (t - w.n_prefix_tiles) * BN;
+        const uint32_t w0 = live ? my_anc[j0 >> 5] : 0u;
+        const uint32_t w1 = live ? my_anc[(j0 >> 5) + 1] : 0u;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const uint32_t bit = c < 32 ? (w0 >> c) & 1u : (w1 >> (c - 32)) & 1u;
+          const float s = __uint_as_float(sr[c]) * a.scale_log2;
+          x[c] = (bit && (j0 + c) < w.N) ? s : -INFINITY;
+          tmax = fmaxf(tmax, x[c]);
+        }
+      }
+      // online softmax with a lazily rescaled reference max
+      float alpha = 1.0f;
+      bool rescale = false;
+      if (tmax != -INFINITY) {
+        if (m_run == -INFINITY) {
+          m_run = tmax;
+        } else if (tmax > m_run + kRescaleLog2) {
+          alpha = exp2f(m_run - tmax);
+          m_run = tmax;
+          rescale = true;
+        }
+      }
+      if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
+        // O must be stable: wait for PV(t-1)
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tmem_o + c0 + lane_off, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          tmem_st32(tmem_o + c0 + lane_off, o);
+        }
+        tmem_st_wait();
+      }
+      l_run *= alpha;
+      // P buffer (t & 1) is free once PV(t-2) has completed
+      if (t >= 2) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&o_done[t & 1], ((t - 2) >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+      }
+      const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
+      uint8_t* prow = smem + Ly::kP0 + (t & 1) * Ly::kPBytes + r * 128;
+      float lsum = 0.0f;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float p0 = exp2f(x[c8 * 8 + 2 * k] - mref);
+          const float p1 = exp2f(x[c8 * 8 + 2 * k + 1] - mref);
+          pk[k] = pack_bf16x2(p0, p1);
+          lsum += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
+        }
+        *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      l_run += lsum;
+      // keys past the prefix end in this tile: clear their V rows (page tails
+      // may hold stale data; P is 0 there but 0 * NaN would poison O)
+      if (valid_keys < BN) {
+        const int st = t % kStages;
+        mbar_wait(&full[st], (t / kStages) & 1);  // acquire the TMA writes
+        uint8_t* vt = smem + Ly::kStage0 + st * Ly::kStageBytes + Ly::kTileBytes;
+        for (int idx = r; idx < (BN - valid_keys) * Ly::kHalves; idx += 128) {
+          const int row = valid_keys + idx / Ly::kHalves, h = idx % Ly::kHalves;
+          uint4* p = reinterpret_cast<uint4*>(vt + h * Ly::kHalfBytes + row * 128);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) p[k] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full[t & 1]);
+    }
+    if (!ok) {
+      record_status(a.status, w.b, kDeviceTimeout);
+      misc->abort = 1;
+    } else if (w.T > 0 && __all_sync(0xffffffffu, mbar_wait(&o_done[(w.T - 1) & 1],
+                                                            ((w.T - 1) >> 1) & 1, abort_flag))) {
+      tc_fence_after();
+      // ------------------------------------------------------------ epilogue
+      const bool final_out = (w.nsplit == 1);
+      const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+      const size_t unit = (static_cast<size_t>(w.b) * a.hkv + w.kvh) * a.mtiles_max + w.mtile;
+      const size_t prow_idx = (unit * a.max_splits + w.split) * BM + r;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tmem_o + c0 + lane_off, o);
+        tmem_ld_wait();
+        if (!live) continue;
+        if (final_out) {
+          const int h = w.kvh * g + R % g;
+          uint4* dst = reinterpret_cast<uint4*>(a.out + (static_cast<size_t>(w.n0 + i_node) * a.hq + h) * D + c0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+            dst[k] = v;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(a.ws_o + prow_idx * D + c0);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                 __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+        }
+      }
+      if (live && !final_out) a.ws_ml[prow_idx] = make_float2(m_run, l_run);
+    } else if (w.T > 0) {
+      record_status(a.status, w.b, kDeviceTimeout);
+      misc->abort = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, Ly::kTmemCols);
+}
+
+// Combines the split partials of one (sequence, KV head, m-tile):
+// O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+template <int D>
+__global__ void __launch_bounds__(128) tree_attn_merge(const AttnArgs a) {
+  const int unit = blockIdx.x;
+  const int mtile = unit % a.mtiles_max;
+  const int bk = unit / a.mtiles_max;
+  const int b = bk / a.hkv, kvh = bk % a.hkv;
+  const int n0 = a.node_offsets[b];
+  const int N = a.node_offsets[b + 1] - n0;
+  const int L = max(0, a.prefix_lens[b]);
+  const int nsplit = max(1, (L + a.chunk - 1) / a.chunk);
+  const int rows = N * a.group;
+  if (nsplit == 1 || N < 1 || N > a.max_nodes || L > a.max_prefix_len || n0 < 0 ||
+      n0 + N > a.total_nodes || mtile * BM >= rows)
+    return;
+  const bool bad = a.status[b] == kBadTree;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < BM; r += 4) {
+    const int R = mtile * BM + r;
+    if (R >= rows) break;
+    const int i = R / a.group, h = kvh * a.group + R % a.group;
+    uint16_t* dst = a.out + (static_cast<size_t>(n0 + i) * a.hq + h) * D;
+    if (bad) {
+      for (int d = lane; d < D; d += 32) dst[d] = 0;
+      continue;
+    }
+    const size_t base = (static_cast<size_t>(unit) * a.max_splits) * BM + r;
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, a.ws_ml[base + static_cast<size_t>(s) * BM].x);
+    const float mref = (M == -INFINITY) ? 0.0f : M;
+    float acc[D / 32];
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) acc[k] = 0.0f;
+    float lsum = 0.0f;
+    for (int s = 0; s < nsplit; ++s) {
+      const size_t pr = base + static_cast<size_t>(s) * BM;
+      const float2 ml = a.ws_ml[pr];
+      const float wgt = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - mref);
+      lsum += wgt * ml.y;
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k) acc[k] += wgt * a.ws_o[pr * D + k * 32 + lane];
+    }
+    const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) {
+      const uint32_t pk = pack_bf16x2(acc[k] * inv, 0.0f);
+      dst[k * 32 + lane] = static_cast<uint16_t>(pk & 0xFFFFu);
+    }
+  }
+}
+
+}  // namespace
+
+size_t tree_attention_smem_bytes(int head_dim) {
+  return head_dim == 64 ? Layout<64>::kAlloc : Layout<128>::kAlloc;
+}
+
+int launch_tree_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream) {
+  const dim3 grid(a.mtiles_max, a.max_splits, a.batch * a.hkv);
+  cudaError_t e;
+  static thread_local int attr_set_device = -1;  // the attribute is set once per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_set_device != dev) {
+    cudaFuncSetAttribute(tree_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Layout<128>::kAlloc);
+    cudaFuncSetAttribute(tree_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Layout<64>::kAlloc);
+    attr_set_device = dev;
+  }
+  if (a.head_dim == 128) {
+    const int smem = Layout<128>::kAlloc;
+    tree_attn_kernel<128><<<grid, kThreads, smem, stream>>>(a, maps);
+    e = cudaGetLastError();
+    if (e == cudaSuccess && a.max_splits > 1) {
+      tree_attn_merge<128><<<a.batch * a.hkv * a.mtiles_max, 128, 0, stream>>>(a);
+      e = cudaGetLastError();
+    }
+  } else {
+    const int smem = Layout<64>::kAlloc;
+    tree_attn_kernel<64><<<grid, kThreads, smem, stream>>>(a, maps);
+    e = cudaGetLastError();
+    if (e == cudaSuccess && a.max_splits > 1) {
+      tree_attn_merge<64><<<a.batch * a.hkv * a.mtiles_max, 128, 0, stream>>>(a);
+      e = cudaGetLastError();
+    }
+  }
+  return e == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace tv

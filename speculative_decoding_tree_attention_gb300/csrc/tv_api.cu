@@ -1,0 +1,249 @@
+// tv_api.cu -- the C ABI of libtv (include/tv.h): argument checks on the host,
+// launch configuration, TMA tensor maps, and launches on the caller's stream.
+// The library allocates nothing and never synchronises.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/tv.h"
+#include "tv_launch.h"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int sm_count() {
+  static thread_local int cached_dev = -1, cached_n = 148;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cached_n;
+  if (dev == cached_dev) return cached_n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return cached_n;
+  cached_dev = dev;
+  cached_n = n;
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct AttnPlan {
+  int group, mtiles_max, max_splits, chunk;
+  size_t ws_o_bytes, ws_ml_bytes;
+};
+
+// Launch plan: 128-row tiles of packed (node, head) rows per (sequence, KV
+// head); the prefix is split so that the grid covers about two waves of
+// SMs, with at least 512 keys per split (partials cost 0.5 KB per row).
+bool plan_attention(const tv_attn_params* p, AttnPlan* out) {
+  if (!p) return false;
+  if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1) return false;
+  if (p->num_q_heads % p->num_kv_heads) return false;
+  if (p->head_dim != 64 && p->head_dim != 128) return false;
+  if (p->block_size != TV_BLOCK_SIZE) return false;
+  if (p->max_nodes < 1 || p->max_nodes > TV_MAX_NODES) return false;
+  if (p->total_nodes < p->batch || p->num_blocks < 1 || p->max_blocks_per_seq < 1) return false;
+  if (p->max_prefix_len < 0) return false;
+  if ((p->max_prefix_len + 15) / 16 > p->max_blocks_per_seq) return false;
+  if (static_cast<int64_t>(p->num_blocks) * p->num_kv_heads * 16 >= (1ll << 31)) return false;
+  if (static_cast<int64_t>(p->total_nodes) >= (1ll << 31) / 2) return false;
+  AttnPlan pl;
+  pl.group = p->num_q_heads / p->num_kv_heads;
+  pl.mtiles_max = (p->max_nodes * pl.group + 127) / 128;
+  const long base = static_cast<long>(p->batch) * p->num_kv_heads * pl.mtiles_max;
+  const long target = 2l * sm_count();
+  long splits = 1;
+  if (p->max_prefix_len > 0 && base < target) splits = (target + base - 1) / base;
+  long chunk = (p->max_prefix_len + splits - 1) / splits;
+  chunk = ((chunk + 63) / 64) * 64;
+  if (chunk < 512) chunk = 512;
+  pl.chunk = static_cast<int>(chunk);
+  pl.max_splits = p->max_prefix_len > 0 ? static_cast<int>((p->max_prefix_len + chunk - 1) / chunk) : 1;
+  if (pl.max_splits < 1) pl.max_splits = 1;
+  const size_t prow = static_cast<size_t>(base) * pl.max_splits * 128;
+  pl.ws_o_bytes = pl.max_splits > 1 ? prow * p->head_dim * sizeof(float) : 0;
+  pl.ws_ml_bytes = pl.max_splits > 1 ? prow * sizeof(float2) : 0;
+  *out = pl;
+  return true;
+}
+
+bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+            strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tv_status_string(int s) {
+  switch (s) {
+    case TV_OK: return "TV_OK";
+    case TV_ERR_INVALID_ARG: return "TV_ERR_INVALID_ARG";
+    case TV_ERR_UNSUPPORTED: return "TV_ERR_UNSUPPORTED";
+    case TV_ERR_WORKSPACE: return "TV_ERR_WORKSPACE";
+    case TV_ERR_CUDA: return "TV_ERR_CUDA";
+    case TV_ERR_BAD_TREE: return "TV_ERR_BAD_TREE";
+    case TV_ERR_DEVICE_TIMEOUT: return "TV_ERR_DEVICE_TIMEOUT";
+    default: return "TV_ERR_UNKNOWN";
+  }
+}
+
+int tv_version(void) { return TV_VERSION; }
+
+size_t tv_tree_attention_workspace_size(const tv_attn_params* p) {
+  AttnPlan pl;
+  if (!plan_attention(p, &pl)) return 0;
+  return pl.ws_o_bytes + pl.ws_ml_bytes;
+}
+
+int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
+                      const uint16_t* k_prefix_blocks, const uint16_t* v_prefix_blocks,
+                      const int32_t* block_table, const uint16_t* k_nodes,
+                      const uint16_t* v_nodes, const int32_t* parent,
+                      const int32_t* prefix_lens, const int32_t* node_offsets, uint16_t* out,
+                      int32_t* status, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  if (!p) return TV_ERR_INVALID_ARG;
+  if (p->head_dim != 64 && p->head_dim != 128) return TV_ERR_UNSUPPORTED;
+  AttnPlan pl;
+  if (!plan_attention(p, &pl)) return TV_ERR_INVALID_ARG;
+  const void* ptrs[] = {q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nodes,
+                        v_nodes, parent, prefix_lens, node_offsets, out, status};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return TV_ERR_INVALID_ARG;
+  const size_t need = pl.ws_o_bytes + pl.ws_ml_bytes;
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return TV_ERR_WORKSPACE;
+
+  const int D = p->head_dim, Hkv = p->num_kv_heads;
+  tv::AttnMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D),
+                                static_cast<cuuint64_t>(p->num_blocks) * Hkv * 16};
+    const cuuint64_t str[1] = {static_cast<cuuint64_t>(D) * 2};
+    const cuuint32_t box[2] = {64, 16};
+    if (!encode(&maps.k_pool, k_prefix_blocks, 2, dims, str, box)) return TV_ERR_CUDA;
+    if (!encode(&maps.v_pool, v_prefix_blocks, 2, dims, str, box)) return TV_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+                                static_cast<cuuint64_t>(p->total_nodes)};
+    const cuuint64_t str[2] = {static_cast<cuuint64_t>(D) * 2,
+                               static_cast<cuuint64_t>(D) * 2 * Hkv};
+    const cuuint32_t box[3] = {64, 1, 64};
+    if (!encode(&maps.k_nodes, k_nodes, 3, dims, str, box)) return TV_ERR_CUDA;
+    if (!encode(&maps.v_nodes, v_nodes, 3, dims, str, box)) return TV_ERR_CUDA;
+  }
+
+  tv::AttnArgs a;
+  a.q = q_nodes;
+  a.block_table = block_table;
+  a.parent = parent;
+  a.prefix_lens = prefix_lens;
+  a.node_offsets = node_offsets;
+  a.out = out;
+  a.status = status;
+  a.ws_o = pl.max_splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  a.ws_ml = pl.max_splits > 1
+                ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + pl.ws_o_bytes)
+                : nullptr;
+  a.batch = p->batch;
+  a.hq = p->num_q_heads;
+  a.hkv = Hkv;
+  a.group = pl.group;
+  a.head_dim = D;
+  a.max_blocks_per_seq = p->max_blocks_per_seq;
+  a.num_blocks = p->num_blocks;
+  a.max_nodes = p->max_nodes;
+  a.max_prefix_len = p->max_prefix_len;
+  a.total_nodes = p->total_nodes;
+  a.mtiles_max = pl.mtiles_max;
+  a.max_splits = pl.max_splits;
+  a.chunk = pl.chunk;
+  const float scale = p->softmax_scale > 0.0f ? p->softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  a.scale_log2 = scale * 1.4426950408889634f;
+
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t) * p->batch, stream) != cudaSuccess)
+    return TV_ERR_CUDA;
+  if (tv::launch_tree_attention(a, maps, stream) != 0) return TV_ERR_CUDA;
+  return TV_OK;
+}
+
+size_t tv_accept_workspace_size(const tv_accept_params* p) {
+  (void)p;
+  return 0;
+}
+
+int tv_accept(const tv_accept_params* p, const float* target, const float* draft_probs,
+              const int32_t* draft_tokens, const int32_t* parent, const int32_t* node_offsets,
+              const float* uniforms, const uint32_t* retained_mask, int32_t* accepted_len,
+              int32_t* path, int32_t* bonus_token, int32_t* status, float* debug_pq,
+              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (!p) return TV_ERR_INVALID_ARG;
+  if (p->batch < 1 || p->vocab < 1 || p->vocab >= (1 << 18)) return TV_ERR_INVALID_ARG;
+  if (p->max_nodes < 1 || p->max_nodes > TV_MAX_NODES || p->max_nodes > tv::accept_max_nodes())
+    return TV_ERR_INVALID_ARG;
+  if (p->kind != TV_INPUT_PROBS && p->kind != TV_INPUT_LOGITS) return TV_ERR_INVALID_ARG;
+  if (p->total_nodes < p->batch) return TV_ERR_INVALID_ARG;
+  const void* ptrs[] = {target, draft_probs, draft_tokens, parent, node_offsets, uniforms,
+                        accepted_len, path, bonus_token, status};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return TV_ERR_INVALID_ARG;
+  if ((retained_mask && !aligned16(retained_mask)) || (debug_pq && !aligned16(debug_pq)))
+    return TV_ERR_INVALID_ARG;
+  tv::AcceptArgs a;
+  a.target = target;
+  a.draft = draft_probs;
+  a.tokens = draft_tokens;
+  a.parent = parent;
+  a.node_offsets = node_offsets;
+  a.uniforms = uniforms;
+  a.mask = retained_mask;
+  a.accepted_len = accepted_len;
+  a.path = path;
+  a.bonus_token = bonus_token;
+  a.status = status;
+  a.debug_pq = debug_pq;
+  a.vocab = p->vocab;
+  a.max_nodes = p->max_nodes;
+  a.kind = p->kind;
+  a.batch = p->batch;
+  a.total_nodes = p->total_nodes;
+  // cluster: one CTA per 16K vocabulary entries, at most 8 (portable size)
+  int cluster = (p->vocab + 16383) / 16384;
+  if (cluster < 1) cluster = 1;
+  if (cluster > 8) cluster = 8;
+  if (tv::launch_accept(a, cluster, stream) != 0) return TV_ERR_CUDA;
+  return TV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// tv_launch.h -- argument blocks and launchers shared by the host API and the
+// kernels (internal to libtv; not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tv {
+
+struct AcceptArgs {
+  const float* target;
+  const float* draft;
+  const int32_t* tokens;
+  const int32_t* parent;
+  const int32_t* node_offsets;
+  const float* uniforms;
+  const uint32_t* mask;
+  int32_t* accepted_len;
+  int32_t* path;
+  int32_t* bonus_token;
+  int32_t* status;
+  float* debug_pq;
+  int32_t vocab;
+  int32_t max_nodes;
+  int32_t kind;
+  int32_t batch;
+  int32_t total_nodes;
+};
+
+int launch_accept(const AcceptArgs& a, int cluster_size, cudaStream_t stream);
+int accept_max_nodes();
+
+struct AttnArgs {
+  const uint16_t* q;          // [total_nodes][Hq][D]
+  const int32_t* block_table; // [batch][max_blocks_per_seq]
+  const int32_t* parent;      // [total_nodes]
+  const int32_t* prefix_lens; // [batch]
+  const int32_t* node_offsets;// [batch+1]
+  uint16_t* out;              // [total_nodes][Hq][D]
+  int32_t* status;            // [batch]
+  float* ws_o;                // split partials: [units*max_splits*128][D] fp32
+  float2* ws_ml;              // split partials: [units*max_splits*128] (m, l)
+  int32_t batch, hq, hkv, group, head_dim;
+  int32_t max_blocks_per_seq, num_blocks, max_nodes, max_prefix_len, total_nodes;
+  int32_t mtiles_max;         // ceil(max_nodes * group / 128)
+  int32_t max_splits;         // splits of the longest prefix
+  int32_t chunk;              // prefix keys per split (multiple of 64)
+  float scale_log2;           // softmax scale * log2(e)
+};
+
+struct AttnMaps {
+  CUtensorMap k_pool;   // 2D (D, num_blocks*Hkv*16), box (64, 16), 128B swizzle
+  CUtensorMap v_pool;
+  CUtensorMap k_nodes;  // 3D (D, Hkv, total_nodes), box (64, 1, 64), 128B swizzle
+  CUtensorMap v_nodes;
+};
+
+int launch_tree_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream);
+size_t tree_attention_smem_bytes(int head_dim);
+
+}  // namespace tv

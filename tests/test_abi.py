@@ -1,0 +1,101 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/tv.h declares; host-side argument checks reject bad calls before any
+device work (no GPU needed)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import speculative_decoding_tree_attention_gb300 as tv
+from speculative_decoding_tree_attention_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return tv.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "tv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("tv_tree_attention", "tv_accept", "tv_tree_attention_workspace_size",
+              "tv_accept_workspace_size", "tv_status_string", "tv_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(tv.EXPORTS) <= set(declared_functions())
+
+
+def test_version_and_status_strings(lib):
+    assert lib.tv_version() == 100
+    assert tv.status_string(0) == "TV_OK"
+    assert tv.status_string(5) == "TV_ERR_BAD_TREE"
+    assert tv.status_string(99) == "TV_ERR_UNKNOWN"
+
+
+def _params(**kw):
+    base = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                max_blocks_per_seq=8, num_blocks=16, max_nodes=64, total_nodes=100,
+                max_prefix_len=128, softmax_scale=0.0)
+    base.update(kw)
+    return tv.AttnParams(**base)
+
+
+@pytest.mark.parametrize("bad", [dict(head_dim=96), dict(num_q_heads=7), dict(block_size=32),
+                                 dict(max_nodes=513), dict(max_nodes=0), dict(batch=0),
+                                 dict(max_prefix_len=1000), dict(total_nodes=1)])
+def test_attention_argument_errors_before_launch(lib, bad):
+    p = _params(**bad)
+    dummy = C.c_void_p(4096)  # never dereferenced: the call fails on the host
+    rc = lib.tv_tree_attention(C.byref(p), *([dummy] * 11), None, C.c_size_t(0), None)
+    assert rc in (tv.TV_ERR_INVALID_ARG, tv.TV_ERR_UNSUPPORTED)
+
+
+def test_attention_null_pointer_rejected(lib):
+    p = _params()
+    dummy = C.c_void_p(4096)
+    args = [dummy] * 11
+    args[3] = None
+    assert lib.tv_tree_attention(C.byref(p), *args, None, C.c_size_t(0), None) == tv.TV_ERR_INVALID_ARG
+    args = [dummy] * 11
+    args[0] = C.c_void_p(4097)  # misaligned
+    assert lib.tv_tree_attention(C.byref(p), *args, None, C.c_size_t(0), None) == tv.TV_ERR_INVALID_ARG
+
+
+def test_attention_workspace_size_rules(lib):
+    assert lib.tv_tree_attention_workspace_size(C.byref(_params(head_dim=96))) == 0
+    # a long prefix on few (sequence, head) pairs is split -> needs partials
+    p = _params(batch=1, num_kv_heads=1, num_q_heads=1, max_prefix_len=32768,
+                max_blocks_per_seq=2048, num_blocks=2048, max_nodes=16, total_nodes=16)
+    assert lib.tv_tree_attention_workspace_size(C.byref(p)) > 0
+
+
+@pytest.mark.parametrize("bad", [dict(vocab=0), dict(vocab=1 << 18), dict(max_nodes=600),
+                                 dict(kind=3), dict(batch=0), dict(total_nodes=0)])
+def test_accept_argument_errors_before_launch(lib, bad):
+    base = dict(batch=2, vocab=1000, max_nodes=16, total_nodes=20, kind=0)
+    base.update(bad)
+    p = tv.AcceptParams(**base)
+    dummy = C.c_void_p(4096)
+    args = [dummy] * 12
+    args[6] = None  # retained_mask optional
+    args[11] = None  # debug_pq optional
+    assert lib.tv_accept(C.byref(p), *args, None, C.c_size_t(0), None) == tv.TV_ERR_INVALID_ARG
+    assert lib.tv_accept_workspace_size(C.byref(p)) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(OSError):
+        tv.load(str(tmp_path / "missing_libtv.so"))

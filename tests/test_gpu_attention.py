@@ -1,0 +1,133 @@
+"""GPU parity of tv_tree_attention (through the C ABI) against the fp64 oracle.
+
+Tolerance (bf16 inputs, fp32 accumulation): max-abs 1e-2 and max-rel 2e-2 on
+elements whose oracle value has magnitude >= 1e-2.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_tree_attention_gb300 import workloads as wl
+from tv_testlib import (assert_attention_close, gather_rows, run_attention, sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def full_compare(case, what, **kw):
+    gpu, status = run_attention(case, **kw)
+    assert np.all(status == 0), status
+    ref = oracle.tree_attention(case)
+    return assert_attention_close(gpu, ref, what)
+
+
+# ---------------------------------------------------------------- small shapes
+def test_tiny_config_full():
+    case = wl.make_case(wl.config(1), parts=("attn",))
+    full_compare(case, "tiny")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_single_tile_chain(d):
+    cfg = wl.config(2, hq=2, hkv=2, d=d, prefix=(64, 64), n=(1, 1), batch=1)
+    case = wl.make_case(cfg, parts=("attn",))
+    full_compare(case, f"one tile d={d}")
+
+
+def test_7b_shape_reduced_heads():
+    cfg = wl.config(2, hq=8, hkv=8)
+    case = wl.make_case(cfg, parts=("attn",))
+    full_compare(case, "7b-like, 8 heads")
+
+
+def test_serving_shape_ragged_paged_gqa():
+    cfg = wl.config(3, batch=5, hq=8, hkv=2, prefix=(0, 700), n=(1, 70), depth=6)
+    case = wl.make_case(cfg, parts=("attn",))
+    full_compare(case, "serving reduced")
+
+
+def test_multimodal_shape_group7():
+    cfg = wl.config(4, batch=2, hq=7, hkv=1, prefix=(600, 600), image_tokens=200, vocab=3000)
+    case = wl.make_case(cfg, parts=("attn",))
+    full_compare(case, "multimodal reduced (g=7, 128 nodes)")
+
+
+def test_long_shape_split_kv_and_four_node_tiles():
+    cfg = wl.config(5, batch=1, hq=16, hkv=2, prefix=(5000, 5000), vocab=2000)
+    case = wl.make_case(cfg, parts=("attn",))
+    full_compare(case, "long reduced (splits, 256 nodes)")
+
+
+def test_head_dim_64_gqa_ragged():
+    cfg = wl.config(3, batch=3, hq=12, hkv=3, d=64, prefix=(1, 300), n=(2, 40), shuffle=True)
+    case = wl.make_case(cfg, parts=("attn",))
+    full_compare(case, "d=64")
+
+
+def test_empty_prefix_and_root_only_trees():
+    cfg = wl.config(3, batch=4, hq=4, hkv=1, prefix=(0, 0), n=(1, 3))
+    cfg["prefix_lens"] = [0, 0, 5, 17]
+    cfg["nodes"] = [1, 3, 1, 2]
+    case = wl.make_case(cfg, parts=("attn",))
+    full_compare(case, "empty prefix / N=1")
+
+
+def test_stale_page_tails_do_not_leak():
+    """Pool slots past a sequence's end hold NaN: they must not reach the output."""
+    cfg = wl.config(3, batch=3, hq=4, hkv=2, prefix=(30, 30), n=(5, 9))
+    cfg["prefix_lens"] = [7, 30, 45]
+    case = wl.make_case(cfg, parts=("attn",))
+    nan_bf16 = np.uint16(0x7FC0)
+    for b, L in enumerate(case["prefix_lens"]):
+        for t in range(L, ((L + 63) // 64) * 64):
+            if t // 16 < case["block_table"].shape[1] and t // 16 < (L + 15) // 16:
+                pg = case["block_table"][b, t // 16]
+                case["k_prefix"][pg, :, t % 16] = nan_bf16
+                case["v_prefix"][pg, :, t % 16] = nan_bf16
+    full_compare(case, "NaN page tails")
+
+
+def test_many_sequences_many_splits():
+    cfg = wl.config(3, batch=2, hq=2, hkv=1, prefix=(3000, 9000), n=(3, 20))
+    case = wl.make_case(cfg, parts=("attn",))
+    full_compare(case, "split-kv varlen")
+
+
+def test_max_nodes_512_chain():
+    cfg = wl.config(2, batch=1, hq=2, hkv=2, d=64, prefix=(40, 40))
+    cfg["parent"] = [[-1] + list(range(511))]
+    cfg["nodes"] = [512]
+    cfg["n"] = (512, 512)
+    case = wl.make_case(cfg, parts=("attn",))
+    full_compare(case, "512-node chain", max_nodes=512)
+
+
+def test_bad_tree_and_bad_block_report_status_and_zero_output():
+    cfg = wl.config(3, batch=3, hq=4, hkv=2, prefix=(40, 40), n=(4, 4))
+    case = wl.make_case(cfg, parts=("attn",))
+    off = case["node_offsets"]
+    case["parent"][off[1] + 2] = 3          # parent not before the node
+    case["block_table"][2, 1] = 10 ** 6     # block id out of range
+    gpu, status = run_attention(case)
+    assert list(status) == [0, 5, 5]
+    assert np.all(gpu[off[1]:off[3]] == 0)
+    ref = oracle.tree_attention_rows(case, [(0, i, h) for i in range(4) for h in range(4)])
+    assert_attention_close(gpu[off[0]:off[1]].reshape(-1, case["head_dim"]), ref, "good sequence")
+
+
+def test_repeatable_bitwise():
+    case = wl.make_case(wl.config(3, batch=3, hq=8, hkv=2, prefix=(100, 900)), parts=("attn",))
+    a, _ = run_attention(case)
+    b, _ = run_attention(case)
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- full sizes
+@pytest.mark.parametrize("num", [2, 3, 4, 5])
+def test_full_size_config_sampled_rows(num):
+    case = wl.make_case(wl.config(num), parts=("attn",))
+    gpu, status = run_attention(case)
+    assert np.all(status == 0)
+    assert np.all(np.isfinite(gpu))
+    rows = sample_rows(case, 48, seed=num)
+    ref = oracle.tree_attention_rows(case, rows)
+    assert_attention_close(gather_rows(gpu, case, rows), ref, f"config {num} sampled rows")

@@ -348,14 +348,6 @@ def test_logits_mode_equals_probs_mode_on_log_probabilities():
     assert np.array_equal(a["bonus_token"], b["bonus_token"])
 
 
-def test_replay_of_own_pq_is_identity():
-    c = wl.make_case(wl.config(1), parts=("accept",))
-    a = oracle.accept(c)
-    r = oracle.accept(c, pq_replay=a["pq"])
-    for k in ("accepted_len", "path", "bonus_token", "status"):
-        assert np.array_equal(a[k], r[k])
-
-
 # ---------------------------------------------------------------- lossless
 def test_lossless_first_token_distribution_and_alpha():
     """Chains of one draft token x ~ q: the emitted token (x if accepted, else

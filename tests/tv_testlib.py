@@ -1,0 +1,114 @@
+"""Shared helpers of the GPU parity tests: move a seeded case to the device,
+call the C-ABI library through the binding, and compare with the oracle."""
+import numpy as np
+import torch
+
+import speculative_decoding_tree_attention_gb300 as tv
+from speculative_decoding_tree_attention_gb300 import _build
+from speculative_decoding_tree_attention_gb300 import workloads as wl
+
+# Tolerance for bf16 inputs with fp32 accumulation: every element within
+# atol + rtol*|ref| (allclose semantics), and every output row (one node, one
+# head) within rtol relative to its own largest magnitude.  An element-wise
+# relative bound on small elements is not used: rounding P to bf16 before the
+# P.V product (as any flash-style kernel does) already moves elements near
+# 1e-2 by several percent.
+ATOL, RTOL = 1e-2, 2e-2
+
+
+def ensure_built():
+    _build.build()
+    return tv.load()
+
+
+def _bf16(bits, dev):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def _i32(x, dev):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).to(dev)
+
+
+def attn_device(case, dev="cuda"):
+    return dict(
+        q=_bf16(case["q"], dev), kp=_bf16(case["k_prefix"], dev), vp=_bf16(case["v_prefix"], dev),
+        table=_i32(case["block_table"], dev), kn=_bf16(case["k_nodes"], dev),
+        vn=_bf16(case["v_nodes"], dev), parent=_i32(case["parent"], dev),
+        lens=_i32(case["prefix_lens"], dev), off=_i32(case["node_offsets"], dev))
+
+
+def run_attention(case, dev="cuda", max_prefix_len=None, max_nodes=None):
+    ensure_built()
+    t = attn_device(case, dev)
+    mpl = int(max_prefix_len if max_prefix_len is not None else max(1, int(np.max(case["prefix_lens"]))))
+    mn = int(max_nodes if max_nodes is not None else case["max_nodes"])
+    out, status = tv.tree_attention(t["q"], t["kp"], t["vp"], t["table"], t["kn"], t["vn"],
+                                    t["parent"], t["lens"], t["off"], max_nodes=mn,
+                                    max_prefix_len=mpl,
+                                    softmax_scale=float(case.get("softmax_scale") or 0.0))
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), status.cpu().numpy()
+
+
+def attention_errors(gpu, ref):
+    """(max abs error, max per-row relative error, worst allclose ratio)."""
+    g = np.asarray(gpu, np.float64).reshape(-1, np.shape(gpu)[-1])
+    r = np.asarray(ref, np.float64).reshape(-1, np.shape(ref)[-1])
+    diff = np.abs(g - r)
+    if diff.size == 0:
+        return 0.0, 0.0, 0.0
+    max_abs = float(diff.max())
+    row_rel = float((diff.max(1) / np.maximum(np.abs(r).max(1), 1e-30)).max())
+    ratio = float((diff / (ATOL + RTOL * np.abs(r))).max())
+    return max_abs, row_rel, ratio
+
+
+def assert_attention_close(gpu, ref, what=""):
+    assert np.all(np.isfinite(gpu)), f"non-finite output {what}"
+    max_abs, row_rel, ratio = attention_errors(gpu, ref)
+    assert ratio <= 1.0 and row_rel <= RTOL, \
+        f"{what}: max_abs={max_abs:.3e} row_rel={row_rel:.3e} allclose_ratio={ratio:.3f}"
+    return max_abs, row_rel
+
+
+def accept_device(case, dev="cuda"):
+    m = case.get("retained_mask")
+    return dict(
+        target=torch.from_numpy(np.ascontiguousarray(case["target"], np.float32)).to(dev),
+        draft=torch.from_numpy(np.ascontiguousarray(case["draft_probs"], np.float32)).to(dev),
+        tokens=_i32(case["draft_tokens"], dev), parent=_i32(case["parent"], dev),
+        off=_i32(case["node_offsets"], dev),
+        uniforms=torch.from_numpy(np.ascontiguousarray(case["uniforms"], np.float32)).to(dev),
+        mask=None if m is None else torch.from_numpy(
+            np.ascontiguousarray(m, np.uint32).view(np.int32)).to(dev))
+
+
+def run_accept(case, dev="cuda"):
+    ensure_built()
+    t = accept_device(case, dev)
+    r = tv.accept(t["target"], t["draft"], t["tokens"], t["parent"], t["off"], t["uniforms"],
+                  t["mask"], max_nodes=int(case["max_nodes"]), kind=case.get("kind", "probs"),
+                  debug_pq=True)
+    torch.cuda.synchronize()
+    return {k: (None if v is None else v.cpu().numpy()) for k, v in r.items()}
+
+
+def sample_rows(case, n, seed=0):
+    """n random (b, local node, q head) rows plus each sequence's first and last node."""
+    g = wl.rng(seed, 4242)
+    off = np.asarray(case["node_offsets"])
+    rows = set()
+    B, hq = case["batch"], case["num_q_heads"]
+    for b in range(B):
+        N = off[b + 1] - off[b]
+        rows.add((b, 0, 0))
+        rows.add((b, int(N - 1), hq - 1))
+    while len(rows) < n + 2 * B:
+        b = int(g.integers(0, B))
+        rows.add((b, int(g.integers(0, off[b + 1] - off[b])), int(g.integers(0, hq))))
+    return np.asarray(sorted(rows), np.int32)
+
+
+def gather_rows(out, case, rows):
+    off = np.asarray(case["node_offsets"])
+    return np.stack([out[off[b] + i, h] for b, i, h in rows])
