@@ -123,6 +123,36 @@ int tv_tree_attention(const tv_attn_params* params, const uint16_t* q_nodes,
                       int32_t* status, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Tree attention for callers that cannot allocate (no counterpart on the
+ * pages: an engineering addition of this library).
+ *
+ * Same inputs, outputs, layouts, semantics and status codes as
+ * tv_tree_attention, but no workspace argument: the split-KV partial
+ * results go to a fixed device array inside the library, so a caller that
+ * may not call cudaMalloc (code running under stream capture, an operator
+ * inside an engine that owns all device memory, a service that forbids
+ * allocation after start-up) can still use it.  This entry point allocates
+ * nothing and calls no allocating routine.
+ *   - The array is TV_NO_ALLOC_SCRATCH_BYTES of device memory; every GPU on
+ *     which this entry point runs holds it until the process exits.
+ *   - A call whose partial results would not fit
+ *     (tv_tree_attention_workspace_size(params) > TV_NO_ALLOC_SCRATCH_BYTES)
+ *     returns TV_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on the device.
+ *   - Every call uses the same array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls that overlap on the GPU
+ *     (other streams, other host threads) race on it: serialise them. */
+#define TV_NO_ALLOC_SCRATCH_BYTES (32u << 20)
+int tv_tree_attention_no_alloc(const tv_attn_params* params, const uint16_t* q_nodes,
+                               const uint16_t* k_prefix_blocks, const uint16_t* v_prefix_blocks,
+                               const int32_t* block_table, const uint16_t* k_nodes,
+                               const uint16_t* v_nodes, const int32_t* parent,
+                               const int32_t* prefix_lens, const int32_t* node_offsets,
+                               uint16_t* out, int32_t* status, cudaStream_t stream);
+
 /* ========================================================================
  * Fused accept pass ([EC] §2.2.3; [LLM] §2.2.1-§2.2.2, §7.1)
  *

@@ -78,6 +78,8 @@ def load(path: str | None = None) -> C.CDLL:
     lib.tv_accept_workspace_size.restype = sz
     lib.tv_accept.argtypes = [C.POINTER(AcceptParams)] + [vp] * 12 + [vp, sz, vp]
     lib.tv_accept.restype = C.c_int
+    lib.tv_tree_attention_no_alloc.argtypes = [C.POINTER(AttnParams)] + [vp] * 11 + [vp]
+    lib.tv_tree_attention_no_alloc.restype = C.c_int
     if path is None:
         _lib = lib
     return lib
@@ -152,6 +154,35 @@ def tree_attention(q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nod
                                C.c_size_t(ws_bytes), _stream(stream))
     if rc != TV_OK:
         raise TVError(rc, "tv_tree_attention")
+    return out, status
+
+
+def tree_attention_no_alloc(q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nodes,
+                            v_nodes, parent, prefix_lens, node_offsets, *, max_nodes: int,
+                            max_prefix_len: int, softmax_scale: float = 0.0, out=None,
+                            status=None, stream=None):
+    """tv_tree_attention_no_alloc: as tree_attention, for callers that cannot
+    allocate device memory; the library keeps the split-KV partials in its own
+    fixed device array (see include/tv.h).  Output tensors must be supplied by
+    a caller that cannot allocate; they are created here only for convenience."""
+    import torch
+    lib = load()
+    _check_dev(q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nodes, v_nodes,
+               parent, prefix_lens, node_offsets)
+    prm = attention_params(q_nodes, k_prefix_blocks, block_table, prefix_lens,
+                           num_kv_heads=k_prefix_blocks.shape[1], max_nodes=max_nodes,
+                           max_prefix_len=max_prefix_len, softmax_scale=softmax_scale)
+    if out is None:
+        out = torch.empty_like(q_nodes)
+    if status is None:
+        status = torch.empty(prm.batch, dtype=torch.int32, device=q_nodes.device)
+    rc = lib.tv_tree_attention_no_alloc(C.byref(prm), _ptr(q_nodes), _ptr(k_prefix_blocks),
+                                        _ptr(v_prefix_blocks), _ptr(block_table), _ptr(k_nodes),
+                                        _ptr(v_nodes), _ptr(parent), _ptr(prefix_lens),
+                                        _ptr(node_offsets), _ptr(out), _ptr(status),
+                                        _stream(stream))
+    if rc != TV_OK:
+        raise TVError(rc, "tv_tree_attention_no_alloc")
     return out, status
 
 
