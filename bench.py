@@ -19,6 +19,7 @@ path: sequences are independent), timing is max over ranks.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -292,7 +293,11 @@ def main():
                "path": torch.empty(B, max_nodes, dtype=torch.int32, device=dev),
                "bonus_token": torch.empty(B, dtype=torch.int32, device=dev),
                "status": torch.empty(B, dtype=torch.int32, device=dev)}
-    launches_per_step = 2 + (1 if ws_bytes > 0 else 0)
+    acc_prm = tv.AcceptParams(B, int(cfg["vocab"]), max_nodes, tot, 1 if args.mode == "logits" else 0)
+    acc_ws_bytes = int(tv.load().tv_accept_workspace_size(ctypes.byref(acc_prm)))
+    acc_ws = torch.empty(max(acc_ws_bytes, 16), dtype=torch.uint8, device=dev)
+    acc_stats = args.mode == "logits" or mask is not None
+    launches_per_step = 2 + (1 if ws_bytes > 0 else 0) + (1 if acc_stats else 0)
 
     def attn(src):
         tv.tree_attention(src["q"], src["kp"], src["vp"], src["table"], src["kn"], src["vn"],
@@ -302,7 +307,7 @@ def main():
     def acc(src):
         tv.accept(src["target"], src["draft"], src["tokens"], src["parent"], src["off"],
                   src["uniforms"], src.get("mask"), max_nodes=max_nodes, kind=args.mode,
-                  outputs=acc_out)
+                  outputs=dict(acc_out, workspace=acc_ws))
 
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)

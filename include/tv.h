@@ -184,7 +184,9 @@ typedef struct {
   int32_t kind;         /* tv_input_kind: the form of `target`              */
 } tv_accept_params;     /* host struct */
 
-/* Bytes of device workspace tv_accept needs (0: it needs none). */
+/* Bytes of device workspace tv_accept needs when the target rows are logits
+ * or a retained_mask is given (per-row partial statistics); with
+ * probabilities and no mask the workspace may be NULL. */
 size_t tv_accept_workspace_size(const tv_accept_params* params);
 
 /* Layouts:
@@ -204,6 +206,8 @@ size_t tv_accept_workspace_size(const tv_accept_params* params);
  *   status        int32 [batch]
  *   debug_pq      fp32 [total_nodes][2] or NULL: (p~, q~) used by the test of
  *                 each node (0, 0 at roots)
+ *   workspace     device bytes >= tv_accept_workspace_size() for logits input
+ *                 or with a mask (else may be NULL)
  * All device pointers 16-byte aligned; V * 4 a multiple of 16 is not required. */
 int tv_accept(const tv_accept_params* params, const float* target, const float* draft_probs,
               const int32_t* draft_tokens, const int32_t* parent, const int32_t* node_offsets,

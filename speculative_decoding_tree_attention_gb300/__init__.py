@@ -217,10 +217,15 @@ def accept(target, draft_probs, draft_tokens, parent, node_offsets, uniforms,
     dpq = o.get("debug_pq")
     if dpq is None and debug_pq:
         dpq = torch.empty(total, 2, dtype=torch.float32, device=dev)
+    ws = o.get("workspace")
+    if ws is None and (kind == "logits" or retained_mask is not None):
+        need = int(lib.tv_accept_workspace_size(C.byref(prm)))
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     rc = lib.tv_accept(C.byref(prm), _ptr(target), _ptr(draft_probs), _ptr(draft_tokens),
                        _ptr(parent), _ptr(node_offsets), _ptr(uniforms), _ptr(retained_mask),
-                       _ptr(acc), _ptr(path), _ptr(bonus), _ptr(status), _ptr(dpq), None,
-                       C.c_size_t(0), _stream(stream))
+                       _ptr(acc), _ptr(path), _ptr(bonus), _ptr(status), _ptr(dpq), _ptr(ws),
+                       C.c_size_t(ws_bytes), _stream(stream))
     if rc != TV_OK:
         raise TVError(rc, "tv_accept")
     return dict(accepted_len=acc, path=path, bonus_token=bonus, status=status, debug_pq=dpq)

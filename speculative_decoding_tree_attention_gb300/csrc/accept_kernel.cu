@@ -1,10 +1,10 @@
-// accept_kernel.cu -- the fused accept pass: one thread-block cluster per tree.
+// accept_kernel.cu -- the fused accept pass.
 //
 // Sources (titles abbreviated):
 //   [EC]  "端云协同推测解码中草稿模型动态生成与验证并行化：探究树形注意力机制与显存碎片整理联合加速",
 //         §2.2.3 batch verification: p_accept = min(1, p_target/p_draft) per
 //         node, parallel uniforms -> accept mask, root-first search cut at the
-//         first rejection, longest accepted path, all inside a GPU kernel with
+//         first rejection, longest accepted path, all inside GPU kernels with
 //         no host round trip.
 //   [LLM] "端侧大模型推测解码草稿模型动态剪枝策略：详解基于重要性采样的树形验证并行加速机制",
 //         §2.2.1-§2.2.2 importance correction q~ = q 1_R / Z and the ScaleMask
@@ -12,19 +12,22 @@
 //         log-space chain (log w = -LSE of the kept draft mass); §1.2 step 3
 //         resampling at the rejection.
 //
-// Design (GB300): grid (C, B) with cluster (C,1,1): the C CTAs of a cluster
-// share one tree and talk through distributed shared memory.
-//   phase 1  rows with children: log-sum-exp of the target logits row (fp32,
-//            online max/sum, 128-bit loads) and/or the retained draft mass Z
-//            (exact 2^-40 fixed point, 64-bit integer sums), rows spread over
-//            the cluster; then p~, q~ of the children.
-//   phase 2  every CTA gathers p~, q~ of all nodes over DSMEM, takes the tests
-//            with warp ballots, and walks each node's parent chain over the
-//            ballot bits; a block max over (depth, -index) picks the cut node.
-//   phase 3  the bonus draw: the cut node's row is split across the cluster,
-//            each CTA sums its fixed-point quanta, the partial sums are
-//            combined in rank order over DSMEM, and the CTA whose range holds
-//            t = floor(u0 * S) finds the token with a block scan.
+// Two kernels, one call, no host round trip:
+//   accept_rowstats_kernel  (only for logits input or a retained-set mask)
+//       one CTA per (row with children, 8K-entry chunk of the vocabulary)
+//       over the whole batch: all loads of the chunk issued at once (128-bit),
+//       then the partial log-sum-exp (max, sum of exp) of the target logits
+//       and/or the partial retained draft mass in exact 2^-40 fixed point.
+//   accept_tree_kernel      one thread-block cluster per tree, launched with
+//       programmatic dependent launch so it is resident when the first kernel
+//       ends.  Phase 1: every node's p~, q~ from the combined partials (fixed
+//       combine order); the tests; warp ballots; each thread walks its node's
+//       parent chain over the ballot bits; a block max over (depth, -index)
+//       picks the cut node.  Phase 2: the bonus draw over the cut node's row,
+//       split across the cluster with each thread holding 32 consecutive
+//       entries in registers; exact fixed-point sums are combined in rank
+//       order over distributed shared memory and the thread whose range
+//       holds t = floor(u0 * S) finds the token.
 // Every decision-carrying sum is an exact integer, so the result does not
 // depend on the reduction order.
 #include <cooperative_groups.h>
@@ -37,33 +40,15 @@ namespace cg = cooperative_groups;
 namespace tv {
 namespace {
 
-constexpr int kThreads = 512;
 constexpr int kMaxN = 512;
-constexpr int kWarps = kThreads / 32;
-
-struct AccSmem {
-  int32_t parent[kMaxN];
-  int32_t token[kMaxN];
-  float u[kMaxN];
-  float pq[kMaxN][2];     // p~, q~ of node i (written by the CTA owning parent(i))
-  float row_lse[kMaxN];   // logits mode: LSE of rows owned by this CTA
-  float row_z[kMaxN];     // mask mode: Z of rows owned by this CTA
-  uint8_t has_child[kMaxN];
-  uint32_t acc_bits[kMaxN / 32];
-  // block reductions
-  float red_f0[kWarps], red_f1[kWarps];
-  unsigned long long red_u64[kWarps];
-  uint32_t red_u32[kWarps];
-  int red_i32[kWarps];
-  // cluster exchange slots (read by the other CTAs)
-  float x_m, x_s;            // partial (max, sum) of exp
-  unsigned long long x_u64;  // partial fixed-point sum
-  float x_maxv;
-  int x_maxi;
-  int bad;
-  int cut;                   // j*
-  int cut_len;
-};
+constexpr int kTreeThreads = 512;
+constexpr int kTreeWarps = kTreeThreads / 32;
+constexpr int kSpan = 32;              // vocabulary entries per thread in the bonus draw
+constexpr int kRowThreads = 256;
+constexpr int kRowVec = 8;             // float4 per thread per chunk
+constexpr int kChunk = kRowThreads * kRowVec * 4;  // 8192 entries per row chunk
+constexpr float kTwo40 = 1099511627776.0f;
+constexpr float kTwoM40 = 9.094947017729282379150390625e-13f;
 
 __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float s2) {
   if (m2 == -INFINITY) return;
@@ -88,12 +73,14 @@ __device__ __forceinline__ void lse_push(float& m, float& s, float x) {
     s += expf(x - m);  // NaN x propagates into s
   }
 }
-
 // floor(min(r, 32) * 2^40) for r > 0, else 0 (NaN -> 0)
 __device__ __forceinline__ unsigned long long fix40(float r) {
   if (!(r > 0.0f)) return 0ull;
   r = fminf(r, 32.0f);
-  return __float2ull_rz(__fmul_rn(r, 1099511627776.0f));
+  return __float2ull_rz(__fmul_rn(r, kTwo40));
+}
+__device__ __forceinline__ float z_from_sum(unsigned long long S) {
+  return __fmul_rn(__ull2float_rn(S), kTwoM40);  // exact scaling by 2^-40
 }
 // floor(u * S) exactly for u in [0,1), S < 2^64
 __device__ __forceinline__ unsigned long long scaled_draw(float u, unsigned long long S) {
@@ -109,68 +96,200 @@ __device__ __forceinline__ unsigned long long scaled_draw(float u, unsigned long
   return (lo >> sh) | (hi << (64 - sh));
 }
 
-__device__ __forceinline__ bool mask_bit(const uint32_t* mrow, int v) {
-  return (__ldg(mrow + (v >> 5)) >> (v & 31)) & 1u;
+// Does local node j of the tree starting at n0 (N nodes) have a child?
+// (children have larger indices).  Block-wide; every thread gets the answer.
+__device__ bool block_has_child(const int32_t* parent, int n0, int N, int j) {
+  int found = 0;
+  for (int i = j + 1 + static_cast<int>(threadIdx.x); i < N; i += blockDim.x)
+    if (__ldg(parent + n0 + i) == j) found = 1;
+  return __syncthreads_or(found) != 0;
 }
 
-// ---- block reductions (all threads call; result valid in every thread)
-__device__ unsigned long long block_sum_u64(AccSmem& sm, unsigned long long x) {
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+// ============================================================ row statistics
+__global__ void __launch_bounds__(kRowThreads)
+    accept_rowstats_kernel(const AcceptArgs a, int nchunk, float2* ws_ms, unsigned long long* ws_z) {
+  const long item = blockIdx.x;
+  const int g = static_cast<int>(item / nchunk);  // global row
+  const int c = static_cast<int>(item % nchunk);
+  if (g >= a.total_nodes) return;
+  // tree of row g (binary search over node_offsets)
+  int lo = 0, hi = a.batch;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(a.node_offsets + mid) <= g) lo = mid; else hi = mid;
+  }
+  const int n0 = __ldg(a.node_offsets + lo);
+  const int N = min(__ldg(a.node_offsets + lo + 1) - n0, kMaxN);
+  const int j = g - n0;
+  if (N < 1 || j < 0 || j >= N) return;
+  if (!block_has_child(a.parent, n0, N, j)) return;  // nobody reads this row's statistics
+
+  const int V = a.vocab;
+  const int v0 = c * kChunk, v1 = min(V, v0 + kChunk);
+  const size_t rowbase = static_cast<size_t>(g) * V;
+  const bool vec = (rowbase & 3) == 0;
+  const bool logits = a.kind == 1;
+  const bool masked = a.mask != nullptr;
+  const int W = (V + 31) >> 5;
+  const uint32_t* mrow = masked ? a.mask + static_cast<size_t>(g) * W : nullptr;
+
+  float m = -INFINITY, s = 0.0f;
+  unsigned long long z = 0;
+  if (vec) {
+    float4 tv[kRowVec], dv[kRowVec];
+#pragma unroll
+    for (int k = 0; k < kRowVec; ++k) {
+      const int v = v0 + (k * kRowThreads + threadIdx.x) * 4;
+      if (v + 3 < v1) {
+        if (logits) tv[k] = __ldg(reinterpret_cast<const float4*>(a.target + rowbase + v));
+        if (masked) dv[k] = __ldg(reinterpret_cast<const float4*>(a.draft + rowbase + v));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kRowVec; ++k) {
+      const int v = v0 + (k * kRowThreads + threadIdx.x) * 4;
+      if (v + 3 < v1) {
+        if (logits) {
+          lse_push(m, s, tv[k].x);
+          lse_push(m, s, tv[k].y);
+          lse_push(m, s, tv[k].z);
+          lse_push(m, s, tv[k].w);
+        }
+        if (masked) {
+          const uint32_t w = __ldg(mrow + (v >> 5)) >> (v & 31);
+          if (w & 1u) z += fix40(dv[k].x);
+          if (w & 2u) z += fix40(dv[k].y);
+          if (w & 4u) z += fix40(dv[k].z);
+          if (w & 8u) z += fix40(dv[k].w);
+        }
+      } else {
+        for (int e = v; e < v1 && e < v + 4; ++e) {
+          if (logits) lse_push(m, s, __ldg(a.target + rowbase + e));
+          if (masked && ((__ldg(mrow + (e >> 5)) >> (e & 31)) & 1u)) z += fix40(__ldg(a.draft + rowbase + e));
+        }
+      }
+    }
+  } else {
+    for (int e = v0 + threadIdx.x; e < v1; e += kRowThreads) {
+      if (logits) lse_push(m, s, __ldg(a.target + rowbase + e));
+      if (masked && ((__ldg(mrow + (e >> 5)) >> (e & 31)) & 1u)) z += fix40(__ldg(a.draft + rowbase + e));
+    }
+  }
+  // block reduction
+  __shared__ float sm_m[kRowThreads / 32], sm_s[kRowThreads / 32];
+  __shared__ unsigned long long sm_z[kRowThreads / 32];
+  for (int o = 16; o; o >>= 1) {
+    lse_combine(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
+    z += __shfl_xor_sync(0xffffffffu, z, o);
+  }
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    sm_m[w] = m;
+    sm_s[w] = s;
+    sm_z[w] = z;
+  }
   __syncthreads();
-  if (l == 0) sm.red_u64[w] = x;
+  if (threadIdx.x == 0) {
+    float M = -INFINITY, S = 0.0f;
+    unsigned long long Z = 0;
+    for (int k = 0; k < kRowThreads / 32; ++k) {
+      lse_combine(M, S, sm_m[k], sm_s[k]);
+      Z += sm_z[k];
+    }
+    ws_ms[item] = make_float2(M, S);
+    ws_z[item] = Z;
+  }
+}
+
+// ============================================================ per-tree pass
+struct TreeSmem {
+  int32_t parent[kMaxN];
+  int32_t token[kMaxN];
+  float u[kMaxN];
+  uint8_t has_child[kMaxN];
+  uint32_t acc_bits[kMaxN / 32];
+  float red_f0[kTreeWarps], red_f1[kTreeWarps];
+  unsigned long long red_u64[kTreeWarps];
+  uint32_t red_u32[kTreeWarps];
+  int red_i32[kTreeWarps];
+  // cluster exchange slots (read by the other CTAs of the cluster)
+  float x_m, x_s;
+  unsigned long long x_u64, x_z;
+  float x_maxv;
+  int x_maxi;
+  int bad;
+  int cut, cut_len;
+};
+
+__device__ unsigned long long block_sum_u64(TreeSmem& sm, unsigned long long x) {
+  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm.red_u64[w] = x;
   __syncthreads();
   unsigned long long t = 0;
-  for (int i = 0; i < kWarps; ++i) t += sm.red_u64[i];
+  for (int i = 0; i < kTreeWarps; ++i) t += sm.red_u64[i];
   return t;
 }
-__device__ uint32_t block_max_u32(AccSmem& sm, uint32_t x) {
-  x = __reduce_max_sync(0xffffffffu, x);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+// exclusive prefix over threads in thread order (every thread gets its own)
+__device__ unsigned long long block_exclusive_u64(TreeSmem& sm, unsigned long long x) {
+  unsigned long long inc = x;
+  const int l = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (l >= o) inc += y;
+  }
   __syncthreads();
-  if (l == 0) sm.red_u32[w] = x;
+  if (l == 31) sm.red_u64[w] = inc;
+  __syncthreads();
+  unsigned long long excl = inc - x;
+  for (int k = 0; k < w; ++k) excl += sm.red_u64[k];
+  return excl;
+}
+__device__ uint32_t block_max_u32(TreeSmem& sm, uint32_t x) {
+  x = __reduce_max_sync(0xffffffffu, x);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm.red_u32[w] = x;
   __syncthreads();
   uint32_t t = 0;
-  for (int i = 0; i < kWarps; ++i) t = max(t, sm.red_u32[i]);
+  for (int i = 0; i < kTreeWarps; ++i) t = max(t, sm.red_u32[i]);
   return t;
 }
-__device__ void block_lse(AccSmem& sm, float& m, float& s) {
-  for (int o = 16; o; o >>= 1) {
-    float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    lse_combine(m, s, m2, s2);
-  }
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+__device__ void block_lse(TreeSmem& sm, float& m, float& s) {
+  for (int o = 16; o; o >>= 1)
+    lse_combine(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
+  const int w = threadIdx.x >> 5;
   __syncthreads();
-  if (l == 0) {
+  if ((threadIdx.x & 31) == 0) {
     sm.red_f0[w] = m;
     sm.red_f1[w] = s;
   }
   __syncthreads();
   m = -INFINITY;
   s = 0.0f;
-  for (int i = 0; i < kWarps; ++i) lse_combine(m, s, sm.red_f0[i], sm.red_f1[i]);
+  for (int i = 0; i < kTreeWarps; ++i) lse_combine(m, s, sm.red_f0[i], sm.red_f1[i]);
 }
 // max value, smallest index among equal maxima (NaN ignored)
-__device__ void block_argmax(AccSmem& sm, float& v, int& idx) {
+__device__ void block_argmax(TreeSmem& sm, float& v, int& idx) {
   for (int o = 16; o; o >>= 1) {
-    float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-    int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
     if (v2 > v || (v2 == v && i2 < idx)) {
       v = v2;
       idx = i2;
     }
   }
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
   __syncthreads();
-  if (l == 0) {
+  if ((threadIdx.x & 31) == 0) {
     sm.red_f0[w] = v;
     sm.red_i32[w] = idx;
   }
   __syncthreads();
   v = -INFINITY;
   idx = 0x7fffffff;
-  for (int i = 0; i < kWarps; ++i) {
+  for (int i = 0; i < kTreeWarps; ++i) {
     if (sm.red_f0[i] > v || (sm.red_f0[i] == v && sm.red_i32[i] < idx)) {
       v = sm.red_f0[i];
       idx = sm.red_i32[i];
@@ -178,35 +297,15 @@ __device__ void block_argmax(AccSmem& sm, float& v, int& idx) {
   }
 }
 
-// Visits every element v in [lo, hi) of a row of floats whose first element
-// sits at float index `rowbase` of a 16-byte aligned buffer; 128-bit loads on
-// the aligned body, threads strided.  f(v, value_target, value_draft).
-template <bool kTwo, typename F>
-__device__ __forceinline__ void for_row(const float* t, const float* d, size_t rowbase, int lo,
-                                        int hi, F&& f) {
-  int a0 = lo + static_cast<int>((4 - ((rowbase + lo) & 3)) & 3);
-  if (a0 > hi) a0 = hi;
-  const int a1 = a0 + ((hi - a0) & ~3);
-  for (int v = lo + threadIdx.x; v < a0; v += kThreads) f(v, t[v], kTwo ? d[v] : 0.0f);
-  for (int v = a0 + 4 * threadIdx.x; v < a1; v += 4 * kThreads) {
-    const float4 x = __ldg(reinterpret_cast<const float4*>(t + v));
-    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (kTwo) y = __ldg(reinterpret_cast<const float4*>(d + v));
-    f(v, x.x, y.x);
-    f(v + 1, x.y, y.y);
-    f(v + 2, x.z, y.z);
-    f(v + 3, x.w, y.w);
-  }
-  for (int v = a1 + threadIdx.x; v < hi; v += kThreads) f(v, t[v], kTwo ? d[v] : 0.0f);
-}
-
-__global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a) {
+__global__ void __launch_bounds__(kTreeThreads, 1)
+    accept_tree_kernel(const AcceptArgs a, int nchunk, const float2* ws_ms,
+                       const unsigned long long* ws_z) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
   const int b = blockIdx.y;
   const int tid = threadIdx.x;
-  __shared__ AccSmem sm;
+  __shared__ TreeSmem sm;
 
   const int n0 = a.node_offsets[b];
   const int N = a.node_offsets[b + 1] - n0;
@@ -214,13 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a)
   const int W = (V + 31) >> 5;
   const bool logits = a.kind == 1;
   const bool masked = a.mask != nullptr;
+  const bool stats = logits || masked;
 
-  // ---------------------------------------------------------------- phase 0
+  // ---------------------------------------------------------------- tree
   if (tid == 0)
     sm.bad = (N < 1 || N > a.max_nodes || N > kMaxN || n0 < 0 || n0 + N > a.total_nodes) ? 1 : 0;
   __syncthreads();
   if (!sm.bad) {
-    for (int i = tid; i < N; i += kThreads) {
+    for (int i = tid; i < N; i += kTreeThreads) {
       const int p = a.parent[n0 + i];
       const int x = a.tokens[n0 + i];
       sm.parent[i] = p;
@@ -228,107 +328,73 @@ __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a)
       sm.u[i] = a.uniforms[n0 + i];
       sm.has_child[i] = 0;
       const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i && x >= 0 && x < V);
-      if (!ok) atomicExch(&sm.bad, 1);
+      if (!ok) sm.bad = 1;
     }
   }
   __syncthreads();
   if (sm.bad) {  // identical decision in every CTA of the cluster
     if (rank == 0) {
-      for (int k = tid; k < a.max_nodes; k += kThreads) a.path[(size_t)b * a.max_nodes + k] = -1;
+      for (int k = tid; k < a.max_nodes; k += kTreeThreads) a.path[(size_t)b * a.max_nodes + k] = -1;
       if (tid == 0) {
         a.accepted_len[b] = -1;
         a.bonus_token[b] = -1;
         a.status[b] = kBadTree;
       }
       if (a.debug_pq && N >= 1 && N <= kMaxN && n0 >= 0 && n0 + N <= a.total_nodes)
-        for (int i = tid; i < N; i += kThreads) {
+        for (int i = tid; i < N; i += kTreeThreads) {
           a.debug_pq[2 * (size_t)(n0 + i)] = 0.0f;
           a.debug_pq[2 * (size_t)(n0 + i) + 1] = 0.0f;
         }
     }
     return;
   }
-  for (int i = tid + 1; i < N; i += kThreads) sm.has_child[sm.parent[i]] = 1;
+  for (int i = tid + 1; i < N; i += kTreeThreads) sm.has_child[sm.parent[i]] = 1;
+  // the row statistics come from the previous kernel in the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
 
-  // p~, q~ of child i of row j (whose LSE / Z are known)
-  auto child_pq = [&](int i, int j, float lse, float z) {
-    const size_t row = static_cast<size_t>(n0 + j) * V;
-    const int x = sm.token[i];
-    float p = __ldg(a.target + row + x);
-    if (logits) p = expf(p - lse);
-    float q = __ldg(a.draft + row + x);
-    if (masked) {
-      if (mask_bit(a.mask + static_cast<size_t>(n0 + j) * W, x)) {
-        p = __fdiv_rn(p, z);
-        q = __fdiv_rn(q, z);
-      } else {
-        p = 0.0f;
-        q = 0.0f;
-      }
+  // LSE / Z of local row j (a row with children) from the partials, fixed order
+  auto row_lse = [&](int j) -> float {
+    float m = -INFINITY, s = 0.0f;
+    const float2* p = ws_ms + static_cast<size_t>(n0 + j) * nchunk;
+    for (int c = 0; c < nchunk; ++c) {
+      const float2 e = p[c];
+      lse_combine(m, s, e.x, e.y);
     }
-    sm.pq[i][0] = p;
-    sm.pq[i][1] = q;
+    return m + logf(s);
+  };
+  auto row_z = [&](int j) -> float {
+    unsigned long long S = 0;
+    const unsigned long long* p = ws_z + static_cast<size_t>(n0 + j) * nchunk;
+    for (int c = 0; c < nchunk; ++c) S += p[c];
+    return z_from_sum(S);
   };
 
-  // Z of row j over [lo, hi): sum of quanta of retained draft mass
-  auto row_z_partial = [&](int j, int lo, int hi) -> unsigned long long {
-    const size_t rowbase = static_cast<size_t>(n0 + j) * V;
-    const uint32_t* mrow = a.mask + static_cast<size_t>(n0 + j) * W;
-    unsigned long long acc = 0;
-    for_row<false>(a.draft + rowbase, nullptr, rowbase, lo, hi, [&](int v, float q, float) {
-      if (mask_bit(mrow, v)) acc += fix40(q);
-    });
-    return acc;
-  };
-  auto row_lse_partial = [&](int j, int lo, int hi, float& m, float& s) {
-    const size_t rowbase = static_cast<size_t>(n0 + j) * V;
-    m = -INFINITY;
-    s = 0.0f;
-    for_row<false>(a.target + rowbase, nullptr, rowbase, lo, hi,
-                   [&](int, float x, float) { lse_push(m, s, x); });
-  };
-  auto z_from_sum = [](unsigned long long S) -> float {
-    return __fmul_rn(__ull2float_rn(S), 9.094947017729282379150390625e-13f);  // * 2^-40
-  };
-
-  // ---------------------------------------------------------------- phase 1
-  const bool rows_needed = logits || masked;
-  if (rows_needed) {
-    for (int j = rank; j < N; j += C) {
-      if (!sm.has_child[j]) continue;
-      float lse = 0.0f, z = 1.0f;
-      if (logits) {
-        float m, s;
-        row_lse_partial(j, 0, V, m, s);
-        block_lse(sm, m, s);
-        lse = m + logf(s);
-      }
-      if (masked) z = z_from_sum(block_sum_u64(sm, row_z_partial(j, 0, V)));
-      if (tid == 0) {
-        sm.row_lse[j] = lse;
-        sm.row_z[j] = z;
-      }
-      for (int i = tid + 1; i < N; i += kThreads)
-        if (sm.parent[i] == j) child_pq(i, j, lse, z);
-      __syncthreads();
-    }
-  } else {
-    for (int i = tid + 1; i < N; i += kThreads) child_pq(i, sm.parent[i], 0.0f, 1.0f);
-  }
-  cluster.sync();
-
-  // ---------------------------------------------------------------- phase 2
+  // ---------------------------------------------------------------- tests
   float my_p = 0.0f, my_q = 0.0f;
-  bool acc = false;
   {
-    const int i = tid;  // kThreads == kMaxN: one node per thread
+    const int i = tid;  // kTreeThreads == kMaxN: one node per thread
+    bool acc = false;
     if (i >= 1 && i < N) {
-      const int owner = rows_needed ? (sm.parent[i] % C) : rank;
-      const float* src = (owner == rank) ? &sm.pq[i][0] : cluster.map_shared_rank(&sm.pq[i][0], owner);
-      my_p = src[0];
-      my_q = src[1];
-      acc = __fmul_rn(sm.u[i], my_q) < my_p;
+      const int j = sm.parent[i];
+      const int x = sm.token[i];
+      const size_t row = static_cast<size_t>(n0 + j) * V;
+      float p = __ldg(a.target + row + x);
+      float q = __ldg(a.draft + row + x);
+      if (logits) p = expf(p - row_lse(j));
+      if (masked) {
+        if ((__ldg(a.mask + static_cast<size_t>(n0 + j) * W + (x >> 5)) >> (x & 31)) & 1u) {
+          const float z = row_z(j);
+          p = __fdiv_rn(p, z);
+          q = __fdiv_rn(q, z);
+        } else {
+          p = 0.0f;
+          q = 0.0f;
+        }
+      }
+      my_p = p;
+      my_q = q;
+      acc = __fmul_rn(sm.u[i], q) < p;
     }
     const uint32_t bal = __ballot_sync(0xffffffffu, acc);
     if ((tid & 31) == 0) sm.acc_bits[tid >> 5] = bal;
@@ -361,11 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a)
   const int len = sm.cut_len;
   if (rank == 0) {
     int32_t* path = a.path + static_cast<size_t>(b) * a.max_nodes;
-    for (int k = len + tid; k < a.max_nodes; k += kThreads) path[k] = -1;
+    for (int k = len + tid; k < a.max_nodes; k += kTreeThreads) path[k] = -1;
     if (tid == 0) {
       for (int d = len - 1, v = cut; d >= 0; --d, v = sm.parent[v]) path[d] = v;
       a.accepted_len[b] = len;
-      a.bonus_token[b] = -1;  // overwritten by the draw below (ordered by the cluster barriers)
+      a.bonus_token[b] = -1;  // overwritten by the draw below (ordered by cluster barriers)
       a.status[b] = kOk;
     }
     if (a.debug_pq && tid < N) {
@@ -374,71 +440,89 @@ __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a)
     }
   }
 
-  // ---------------------------------------------------------------- phase 3
-  // LSE / Z of the cut row: from its owner when it has children, else
-  // reduced now across the cluster (chunk per CTA, combined in rank order).
-  const int chunk = (((V + C - 1) / C) + 3) & ~3;
+  // ---------------------------------------------------------------- bonus
+  // This thread's entries of the cut row: [e0, e0 + kSpan) within the CTA's
+  // chunk [lo, hi); kSpan is a multiple of 32, so one mask word covers them.
+  const int chunk = ((V + C - 1) / C + kSpan - 1) / kSpan * kSpan;
   const int lo = min(V, rank * chunk), hi = min(V, lo + chunk);
-  const bool cut_has_child = sm.has_child[cut] != 0;
+  const int e0 = lo + tid * kSpan;
+  const int n_mine = max(0, min(kSpan, hi - e0));
+  const size_t crow = static_cast<size_t>(n0 + cut) * V;
+  float tr[kSpan], dr[kSpan];
+  if (n_mine == kSpan && ((crow + e0) & 3) == 0) {
+#pragma unroll
+    for (int k = 0; k < kSpan / 4; ++k) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(a.target + crow + e0) + k);
+      const float4 y = __ldg(reinterpret_cast<const float4*>(a.draft + crow + e0) + k);
+      tr[4 * k] = x.x; tr[4 * k + 1] = x.y; tr[4 * k + 2] = x.z; tr[4 * k + 3] = x.w;
+      dr[4 * k] = y.x; dr[4 * k + 1] = y.y; dr[4 * k + 2] = y.z; dr[4 * k + 3] = y.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kSpan; ++k) {
+      tr[k] = k < n_mine ? __ldg(a.target + crow + e0 + k) : -INFINITY;
+      dr[k] = k < n_mine ? __ldg(a.draft + crow + e0 + k) : 0.0f;
+    }
+  }
+  uint32_t mbits = 0xFFFFFFFFu;
+  if (masked && n_mine > 0) mbits = __ldg(a.mask + static_cast<size_t>(n0 + cut) * W + (e0 >> 5));
+  if (n_mine < kSpan) mbits &= (n_mine > 0 ? (0xFFFFFFFFu >> (32 - n_mine)) : 0u);
+
+  // LSE / Z of the cut row: from the partials if it has children (the same
+  // values its children were tested with), else reduced here across the cluster
   float lse = 0.0f, z = 1.0f;
-  if (rows_needed) {
-    if (cut_has_child) {
-      const int owner = cut % C;
-      const float* l = owner == rank ? &sm.row_lse[cut] : cluster.map_shared_rank(&sm.row_lse[cut], owner);
-      const float* zz = owner == rank ? &sm.row_z[cut] : cluster.map_shared_rank(&sm.row_z[cut], owner);
-      lse = *l;
-      z = *zz;
+  if (stats) {
+    if (sm.has_child[cut]) {
+      if (logits) lse = row_lse(cut);
+      if (masked) z = row_z(cut);
     } else {
       float m = -INFINITY, s = 0.0f;
       unsigned long long zs = 0;
-      if (logits) {
-        row_lse_partial(cut, lo, hi, m, s);
-        block_lse(sm, m, s);
+#pragma unroll
+      for (int k = 0; k < kSpan; ++k) {
+        if (logits && k < n_mine) lse_push(m, s, tr[k]);  // full-vocabulary softmax
+        if (masked && ((mbits >> k) & 1u)) zs += fix40(dr[k]);
       }
-      if (masked) zs = block_sum_u64(sm, row_z_partial(cut, lo, hi));
+      if (logits) block_lse(sm, m, s);
+      if (masked) zs = block_sum_u64(sm, zs);
       if (tid == 0) {
         sm.x_m = m;
         sm.x_s = s;
-        sm.x_u64 = zs;
+        sm.x_z = zs;
       }
       cluster.sync();
       float M = -INFINITY, Ssum = 0.0f;
       unsigned long long Z = 0;
       for (int c = 0; c < C; ++c) {
-        AccSmem* o = cluster.map_shared_rank(&sm, c);
+        const TreeSmem* o = cluster.map_shared_rank(&sm, c);
         lse_combine(M, Ssum, o->x_m, o->x_s);
-        Z += o->x_u64;
+        Z += o->x_z;
       }
       lse = M + logf(Ssum);
       z = z_from_sum(Z);
-      cluster.sync();  // every CTA has read the slots before they are reused
     }
   }
-
-  const size_t crow = static_cast<size_t>(n0 + cut) * V;
-  const uint32_t* cmask = masked ? a.mask + static_cast<size_t>(n0 + cut) * W : nullptr;
-  // p~_v and q~_v of the cut row
-  auto ptil = [&](int v, float t) -> float {
-    float p = logits ? expf(t - lse) : t;
-    if (masked) p = mask_bit(cmask, v) ? __fdiv_rn(p, z) : 0.0f;
-    return p;
-  };
-  auto qtil = [&](int v, float d) -> float {
-    if (masked) return mask_bit(cmask, v) ? __fdiv_rn(d, z) : 0.0f;
-    return d;
-  };
-  auto quanta = [&](int pass, int v, float t, float d) -> unsigned long long {
-    const float p = ptil(v, t);
-    return fix40(pass == 0 ? __fsub_rn(p, qtil(v, d)) : p);
-  };
+  // p~ and q~ of the cut row in place (0 off the retained set and past V)
+#pragma unroll
+  for (int k = 0; k < kSpan; ++k) {
+    const bool in = (mbits >> k) & 1u;
+    float p = logits ? expf(tr[k] - lse) : tr[k];
+    float q = dr[k];
+    if (masked) {
+      p = __fdiv_rn(p, z);
+      q = __fdiv_rn(q, z);
+    }
+    tr[k] = in ? p : 0.0f;
+    dr[k] = in ? q : 0.0f;
+  }
 
   const float u0 = sm.u[0];
-  int token = -1;
-  for (int pass = cut_has_child ? 0 : 1; pass < 2; ++pass) {
-    unsigned long long part = 0;
-    for_row<true>(a.target + crow, a.draft + crow, crow, lo, hi,
-                  [&](int v, float t, float d) { part += quanta(pass, v, t, d); });
-    part = block_sum_u64(sm, part);
+  bool drawn = false;
+  for (int pass = sm.has_child[cut] ? 0 : 1; pass < 2 && !drawn; ++pass) {
+    unsigned long long mine = 0;
+#pragma unroll
+    for (int k = 0; k < kSpan; ++k) mine += fix40(pass == 0 ? __fsub_rn(tr[k], dr[k]) : tr[k]);
+    const unsigned long long part = block_sum_u64(sm, mine);
     if (tid == 0) sm.x_u64 = part;
     cluster.sync();
     unsigned long long S = 0, before = 0;
@@ -447,54 +531,35 @@ __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a)
       if (c < rank) before += sc;
       S += sc;
     }
-    cluster.sync();
+    cluster.sync();  // the slots may be reused after this point
     if (S == 0) continue;  // the same decision in every CTA
+    drawn = true;
     const unsigned long long t = scaled_draw(u0, S);
-    if (t >= before && t - before < part) {
-      // this CTA holds the token: contiguous sub-ranges per thread, block scan
+    if (t >= before && t - before < part) {  // this CTA holds the token (CTA-uniform)
       const unsigned long long tl = t - before;
-      const int n = hi - lo;
-      const int sub = (n + kThreads - 1) / kThreads;
-      const int s0 = lo + min(n, tid * sub), s1 = lo + min(n, (tid + 1) * sub);
-      unsigned long long mine = 0;
-      for (int v = s0; v < s1; ++v) mine += quanta(pass, v, a.target[crow + v], a.draft[crow + v]);
-      // exclusive scan over threads (warp shuffles + per-warp totals)
-      unsigned long long inc = mine;
-      const int l = tid & 31, w = tid >> 5;
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (l >= o) inc += y;
-      }
-      __syncthreads();
-      if (l == 31) sm.red_u64[w] = inc;
-      __syncthreads();
-      unsigned long long excl = inc - mine;
-      for (int k = 0; k < w; ++k) excl += sm.red_u64[k];
+      const unsigned long long excl = block_exclusive_u64(sm, mine);
       if (mine > 0 && tl >= excl && tl - excl < mine) {
         unsigned long long cum = excl;
-        for (int v = s0; v < s1; ++v) {
-          cum += quanta(pass, v, a.target[crow + v], a.draft[crow + v]);
-          if (cum > tl) {
-            a.bonus_token[b] = v;
-            break;
-          }
+        int tok = -1;
+#pragma unroll
+        for (int k = 0; k < kSpan; ++k) {
+          cum += fix40(pass == 0 ? __fsub_rn(tr[k], dr[k]) : tr[k]);
+          if (tok < 0 && cum > tl) tok = e0 + k;
         }
+        a.bonus_token[b] = tok;
       }
     }
-    token = 0;  // found (written by the owning thread)
-    break;
   }
-  if (token < 0) {
+  if (!drawn) {
     // no mass at all: smallest index of the largest p~ (NaN ignored)
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for_row<false>(a.target + crow, nullptr, crow, lo, hi, [&](int v, float t, float) {
-      const float p = ptil(v, t);
-      if (p > bv || (p == bv && v < bi)) {
-        bv = p;
-        bi = v;
+#pragma unroll
+    for (int k = 0; k < kSpan; ++k)
+      if (k < n_mine && tr[k] > bv) {
+        bv = tr[k];
+        bi = e0 + k;
       }
-    });
     block_argmax(sm, bv, bi);
     if (tid == 0) {
       sm.x_maxv = bv;
@@ -505,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a)
       float best = -INFINITY;
       int idx = 0;
       for (int c = 0; c < C; ++c) {
-        const AccSmem* o = cluster.map_shared_rank(&sm, c);
+        const TreeSmem* o = cluster.map_shared_rank(&sm, c);
         if (o->x_maxv > best) {
           best = o->x_maxv;
           idx = o->x_maxi;
@@ -519,20 +584,57 @@ __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a)
 
 }  // namespace
 
-int launch_accept(const AcceptArgs& a, int cluster_size, cudaStream_t stream) {
+int accept_chunks(int vocab) { return (vocab + kChunk - 1) / kChunk; }
+
+int accept_cluster_size(int vocab) {
+  int c = (vocab + kTreeThreads * kSpan - 1) / (kTreeThreads * kSpan);
+  return c < 1 ? 1 : c;
+}
+
+int launch_accept(const AcceptArgs& a, void* workspace, cudaStream_t stream) {
+  const int nchunk = accept_chunks(a.vocab);
+  const int C = accept_cluster_size(a.vocab);
+  float2* ws_ms = static_cast<float2*>(workspace);
+  unsigned long long* ws_z = reinterpret_cast<unsigned long long*>(
+      static_cast<char*>(workspace) + sizeof(float2) * static_cast<size_t>(a.total_nodes) * nchunk);
+  const bool stats = a.kind == 1 || a.mask != nullptr;
+  if (stats) {
+    const long items = static_cast<long>(a.total_nodes) * nchunk;
+    accept_rowstats_kernel<<<static_cast<unsigned>(items), kRowThreads, 0, stream>>>(a, nchunk, ws_ms,
+                                                                                    ws_z);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+  }
+  static thread_local int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    cudaFuncSetAttribute(accept_tree_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    attr_dev = dev;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cluster_size, a.batch, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.gridDim = dim3(C, a.batch, 1);
+  cfg.blockDim = dim3(kTreeThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster_size;
+  attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = stats ? 1 : 0;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, accept_kernel, a) == cudaSuccess ? 0 : -1;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, accept_tree_kernel, a, nchunk,
+                            static_cast<const float2*>(ws_ms),
+                            static_cast<const unsigned long long*>(ws_z)) == cudaSuccess
+             ? 0
+             : -1;
+}
+
+size_t accept_workspace_bytes(int vocab, int total_nodes) {
+  return static_cast<size_t>(total_nodes) * accept_chunks(vocab) *
+         (sizeof(float2) + sizeof(unsigned long long));
 }
 
 int accept_max_nodes() { return kMaxN; }

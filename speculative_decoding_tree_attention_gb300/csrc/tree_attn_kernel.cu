@@ -359,30 +359,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem_s0 + (t & 1) * BN + 32 + lane_off, hi);
         tmem_ld_wait();
       }
-      // scale + mask
+      // scale + mask (scores stay unscaled here; the scale is folded into
+      // the exponent below), then the row max as a tree of fmaxf
       float x[64];
-      float tmax = -INFINITY;
       int valid_keys = BN;
       if (t < w.n_prefix_tiles) {
         valid_keys = min(BN, w.k_end - (w.k_begin + t * BN));
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float s = __uint_as_float(sr[c]) * a.scale_log2;
-          x[c] = c < valid_keys ? s : -INFINITY;
-          tmax = fmaxf(tmax, x[c]);
-        }
+        for (int c = 0; c < 64; ++c) x[c] = c < valid_keys ? __uint_as_float(sr[c]) : -INFINITY;
       } else {
         const int j0 = (t - w.n_prefix_tiles) * BN;
         const uint32_t w0 = live ? my_anc[j0 >> 5] : 0u;
         const uint32_t w1 = live ? my_anc[(j0 >> 5) + 1] : 0u;
+        const int nvalid = w.N - j0;  // node columns past the tree are masked
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const uint32_t bit = c < 32 ? (w0 >> c) & 1u : (w1 >> (c - 32)) & 1u;
-          const float s = __uint_as_float(sr[c]) * a.scale_log2;
-          x[c] = (bit && (j0 + c) < w.N) ? s : -INFINITY;
-          tmax = fmaxf(tmax, x[c]);
+          x[c] = (bit && c < nvalid) ? __uint_as_float(sr[c]) : -INFINITY;
         }
       }
+      float mx[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) mx[c] = fmaxf(x[c], x[c + 32]);
+#pragma unroll
+      for (int h = 16; h >= 1; h >>= 1)
+#pragma unroll
+        for (int c = 0; c < h; ++c) mx[c] = fmaxf(mx[c], mx[c + h]);
+      const float tmax = mx[0] * a.scale_log2;  // -inf stays -inf
       // online softmax with a lazily rescaled reference max
       float alpha = 1.0f;
       bool rescale = false;
@@ -425,19 +428,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
       uint8_t* prow = smem + Ly::kP0 + (t & 1) * Ly::kPBytes + r * 128;
-      float lsum = 0.0f;
+      float ls[8];
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         uint32_t pk[4];
+        float part = 0.0f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float p0 = exp2f(x[c8 * 8 + 2 * k] - mref);
-          const float p1 = exp2f(x[c8 * 8 + 2 * k + 1] - mref);
+          // p = 2^(s * scale * log2(e) - m); masked scores are -inf -> 0
+          const float p0 = ex2_approx(fmaf(x[c8 * 8 + 2 * k], a.scale_log2, -mref));
+          const float p1 = ex2_approx(fmaf(x[c8 * 8 + 2 * k + 1], a.scale_log2, -mref));
           pk[k] = pack_bf16x2(p0, p1);
-          lsum += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
+          // l accumulates the bf16-rounded weights that the P.V product uses
+          part += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
         }
+        ls[c8] = part;
         *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       l_run += lsum;
       // keys past the prefix end in this tile: clear their V rows (page tails
       // may hold stale data; P is 0 there but 0 * NaN would poison O)

@@ -197,8 +197,8 @@ int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
 }
 
 size_t tv_accept_workspace_size(const tv_accept_params* p) {
-  (void)p;
-  return 0;
+  if (!p || p->vocab < 1 || p->vocab >= (1 << 18) || p->total_nodes < 1) return 0;
+  return tv::accept_workspace_bytes(p->vocab, p->total_nodes);
 }
 
 int tv_accept(const tv_accept_params* p, const float* target, const float* draft_probs,
@@ -206,8 +206,6 @@ int tv_accept(const tv_accept_params* p, const float* target, const float* draft
               const float* uniforms, const uint32_t* retained_mask, int32_t* accepted_len,
               int32_t* path, int32_t* bonus_token, int32_t* status, float* debug_pq,
               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (!p) return TV_ERR_INVALID_ARG;
   if (p->batch < 1 || p->vocab < 1 || p->vocab >= (1 << 18)) return TV_ERR_INVALID_ARG;
   if (p->max_nodes < 1 || p->max_nodes > TV_MAX_NODES || p->max_nodes > tv::accept_max_nodes())
@@ -238,11 +236,12 @@ int tv_accept(const tv_accept_params* p, const float* target, const float* draft
   a.kind = p->kind;
   a.batch = p->batch;
   a.total_nodes = p->total_nodes;
-  // cluster: one CTA per 16K vocabulary entries, at most 8 (portable size)
-  int cluster = (p->vocab + 16383) / 16384;
-  if (cluster < 1) cluster = 1;
-  if (cluster > 8) cluster = 8;
-  if (tv::launch_accept(a, cluster, stream) != 0) return TV_ERR_CUDA;
+  // per-row statistics (logits input or a retained-set mask) need workspace
+  if (p->kind == TV_INPUT_LOGITS || retained_mask) {
+    const size_t need = tv::accept_workspace_bytes(p->vocab, p->total_nodes);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return TV_ERR_WORKSPACE;
+  }
+  if (tv::launch_accept(a, workspace, stream) != 0) return TV_ERR_CUDA;
   return TV_OK;
 }
 

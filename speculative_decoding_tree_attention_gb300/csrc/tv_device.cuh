@@ -187,6 +187,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) 
 }
 
 // ---------------------------------------------------------------- misc
+// 2^x with the hardware approximation (ex2.approx.ftz: about 2 ulp, results
+// below 2^-126 flush to zero); used where the result is rounded to bf16.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

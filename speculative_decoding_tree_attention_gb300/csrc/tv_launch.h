@@ -28,7 +28,12 @@ struct AcceptArgs {
   int32_t total_nodes;
 };
 
-int launch_accept(const AcceptArgs& a, int cluster_size, cudaStream_t stream);
+// Launches the accept pass; `workspace` holds per-(row, chunk) statistics and
+// must be accept_workspace_bytes() long when the input is logits or a mask
+// is given (it is not touched otherwise).
+int launch_accept(const AcceptArgs& a, void* workspace, cudaStream_t stream);
+size_t accept_workspace_bytes(int vocab, int total_nodes);
+int accept_cluster_size(int vocab);
 int accept_max_nodes();
 
 struct AttnArgs {

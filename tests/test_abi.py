@@ -93,7 +93,23 @@ def test_accept_argument_errors_before_launch(lib, bad):
     args[6] = None  # retained_mask optional
     args[11] = None  # debug_pq optional
     assert lib.tv_accept(C.byref(p), *args, None, C.c_size_t(0), None) == tv.TV_ERR_INVALID_ARG
+
+
+def test_accept_workspace_size_rules(lib):
+    # per (row, 8192-entry vocabulary chunk): a float2 and a uint64
+    p = tv.AcceptParams(batch=2, vocab=20000, max_nodes=16, total_nodes=20, kind=1)
+    assert lib.tv_accept_workspace_size(C.byref(p)) == 20 * 3 * 16
+    p = tv.AcceptParams(batch=2, vocab=1 << 18, max_nodes=16, total_nodes=20, kind=1)
     assert lib.tv_accept_workspace_size(C.byref(p)) == 0
+
+
+def test_accept_logits_without_workspace_is_refused(lib):
+    p = tv.AcceptParams(batch=2, vocab=1000, max_nodes=16, total_nodes=20, kind=1)
+    dummy = C.c_void_p(4096)
+    args = [dummy] * 12
+    args[6] = None
+    args[11] = None
+    assert lib.tv_accept(C.byref(p), *args, None, C.c_size_t(0), None) == tv.TV_ERR_WORKSPACE
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
