@@ -43,7 +43,9 @@ namespace {
 constexpr int kMaxN = 512;
 constexpr int kTreeThreads = 512;
 constexpr int kTreeWarps = kTreeThreads / 32;
-constexpr int kSpan = 32;              // vocabulary entries per thread in the bonus draw
+constexpr int kWarpSpan = 1024;        // bonus draw: contiguous entries per warp
+constexpr int kCtaSpan = kWarpSpan * (kTreeThreads / 32);  // 16384 entries per CTA
+constexpr int kTreeSmemBytes = 2 * kCtaSpan * 4 + (kCtaSpan / 32) * 4;
 constexpr int kRowThreads = 256;
 constexpr int kRowVec = 8;             // float4 per thread per chunk
 constexpr int kChunk = kRowThreads * kRowVec * 4;  // 8192 entries per row chunk
@@ -140,33 +142,41 @@ __global__ void __launch_bounds__(kRowThreads)
 #pragma unroll
     for (int k = 0; k < kRowVec; ++k) {
       const int v = v0 + (k * kRowThreads + threadIdx.x) * 4;
+      tv[k] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      dv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (v + 3 < v1) {
         if (logits) tv[k] = __ldg(reinterpret_cast<const float4*>(a.target + rowbase + v));
         if (masked) dv[k] = __ldg(reinterpret_cast<const float4*>(a.draft + rowbase + v));
+      } else {
+        float* tp = &tv[k].x;
+        float* dp = &dv[k].x;
+        for (int e = 0; e < 4 && v + e < v1; ++e) {
+          if (logits) tp[e] = __ldg(a.target + rowbase + v + e);
+          if (masked) dp[e] = __ldg(a.draft + rowbase + v + e);
+        }
       }
     }
+    if (logits) {  // max first, then independent exponentials
 #pragma unroll
-    for (int k = 0; k < kRowVec; ++k) {
-      const int v = v0 + (k * kRowThreads + threadIdx.x) * 4;
-      if (v + 3 < v1) {
-        if (logits) {
-          lse_push(m, s, tv[k].x);
-          lse_push(m, s, tv[k].y);
-          lse_push(m, s, tv[k].z);
-          lse_push(m, s, tv[k].w);
-        }
-        if (masked) {
-          const uint32_t w = __ldg(mrow + (v >> 5)) >> (v & 31);
-          if (w & 1u) z += fix40(dv[k].x);
-          if (w & 2u) z += fix40(dv[k].y);
-          if (w & 4u) z += fix40(dv[k].z);
-          if (w & 8u) z += fix40(dv[k].w);
-        }
-      } else {
-        for (int e = v; e < v1 && e < v + 4; ++e) {
-          if (logits) lse_push(m, s, __ldg(a.target + rowbase + e));
-          if (masked && ((__ldg(mrow + (e >> 5)) >> (e & 31)) & 1u)) z += fix40(__ldg(a.draft + rowbase + e));
-        }
+      for (int k = 0; k < kRowVec; ++k)
+        m = fmaxf(m, fmaxf(fmaxf(tv[k].x, tv[k].y), fmaxf(tv[k].z, tv[k].w)));
+      if (m != -INFINITY) {
+#pragma unroll
+        for (int k = 0; k < kRowVec; ++k)
+          s += (expf(tv[k].x - m) + expf(tv[k].y - m)) + (expf(tv[k].z - m) + expf(tv[k].w - m));
+      }
+      if (m != m) s = m;  // a NaN logit makes the row NaN
+    }
+    if (masked) {
+#pragma unroll
+      for (int k = 0; k < kRowVec; ++k) {
+        const int v = v0 + (k * kRowThreads + threadIdx.x) * 4;
+        if (v >= v1) continue;
+        const uint32_t w = __ldg(mrow + (v >> 5)) >> (v & 31);
+        if ((w & 1u) && v < v1) z += fix40(dv[k].x);
+        if ((w & 2u) && v + 1 < v1) z += fix40(dv[k].y);
+        if ((w & 4u) && v + 2 < v1) z += fix40(dv[k].z);
+        if ((w & 8u) && v + 3 < v1) z += fix40(dv[k].w);
       }
     }
   } else {
@@ -246,6 +256,35 @@ __device__ unsigned long long block_exclusive_u64(TreeSmem& sm, unsigned long lo
   for (int k = 0; k < w; ++k) excl += sm.red_u64[k];
   return excl;
 }
+__device__ float block_max_f32(TreeSmem& sm, float x) {
+  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm.red_f0[w] = x;
+  __syncthreads();
+  float t = -INFINITY;
+  for (int i = 0; i < kTreeWarps; ++i) t = fmaxf(t, sm.red_f0[i]);
+  return t;
+}
+__device__ float block_sum_f32(TreeSmem& sm, float x) {
+  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm.red_f1[w] = x;
+  __syncthreads();
+  float t = 0.0f;
+  for (int i = 0; i < kTreeWarps; ++i) t += sm.red_f1[i];
+  return t;
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
 __device__ uint32_t block_max_u32(TreeSmem& sm, uint32_t x) {
   x = __reduce_max_sync(0xffffffffu, x);
   const int w = threadIdx.x >> 5;
@@ -314,6 +353,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
   const bool logits = a.kind == 1;
   const bool masked = a.mask != nullptr;
   const bool stats = logits || masked;
+  extern __shared__ float4 smem_dyn[];
+  float* smem_rows = reinterpret_cast<float*>(smem_dyn);
 
   // ---------------------------------------------------------------- tree
   if (tid == 0)
@@ -441,32 +482,43 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
   }
 
   // ---------------------------------------------------------------- bonus
-  // This thread's entries of the cut row: [e0, e0 + kSpan) within the CTA's
-  // chunk [lo, hi); kSpan is a multiple of 32, so one mask word covers them.
-  const int chunk = ((V + C - 1) / C + kSpan - 1) / kSpan * kSpan;
+  // The cut row's chunk of this CTA, [lo, hi), goes to shared memory with
+  // cp.async; every pass then reads it coalesced.  The exact find walks
+  // contiguous 1024-entry warp spans in index order with warp scans.
+  float* tbuf = smem_rows;
+  float* dbuf = smem_rows + kCtaSpan;
+  uint32_t* mbuf = reinterpret_cast<uint32_t*>(smem_rows + 2 * kCtaSpan);
+  const int chunk = ((V + C - 1) / C + kWarpSpan - 1) / kWarpSpan * kWarpSpan;
   const int lo = min(V, rank * chunk), hi = min(V, lo + chunk);
-  const int e0 = lo + tid * kSpan;
-  const int n_mine = max(0, min(kSpan, hi - e0));
+  const int n = hi - lo;
   const size_t crow = static_cast<size_t>(n0 + cut) * V;
-  float tr[kSpan], dr[kSpan];
-  if (n_mine == kSpan && ((crow + e0) & 3) == 0) {
-#pragma unroll
-    for (int k = 0; k < kSpan / 4; ++k) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(a.target + crow + e0) + k);
-      const float4 y = __ldg(reinterpret_cast<const float4*>(a.draft + crow + e0) + k);
-      tr[4 * k] = x.x; tr[4 * k + 1] = x.y; tr[4 * k + 2] = x.z; tr[4 * k + 3] = x.w;
-      dr[4 * k] = y.x; dr[4 * k + 1] = y.y; dr[4 * k + 2] = y.z; dr[4 * k + 3] = y.w;
+  {
+    const float* tsrc = a.target + crow + lo;
+    const float* dsrc = a.draft + crow + lo;
+    if (((crow + lo) & 3) == 0) {
+      const int n4 = n >> 2;
+      for (int k = tid; k < n4; k += kTreeThreads) {
+        cp_async16(tbuf + 4 * k, tsrc + 4 * k);
+        cp_async16(dbuf + 4 * k, dsrc + 4 * k);
+      }
+      for (int e = 4 * n4 + tid; e < n; e += kTreeThreads) {
+        cp_async4(tbuf + e, tsrc + e);
+        cp_async4(dbuf + e, dsrc + e);
+      }
+    } else {
+      for (int e = tid; e < n; e += kTreeThreads) {
+        cp_async4(tbuf + e, tsrc + e);
+        cp_async4(dbuf + e, dsrc + e);
+      }
     }
-  } else {
-#pragma unroll
-    for (int k = 0; k < kSpan; ++k) {
-      tr[k] = k < n_mine ? __ldg(a.target + crow + e0 + k) : -INFINITY;
-      dr[k] = k < n_mine ? __ldg(a.draft + crow + e0 + k) : 0.0f;
+    if (masked) {  // lo is a multiple of 32: whole mask words
+      const uint32_t* msrc = a.mask + static_cast<size_t>(n0 + cut) * W + (lo >> 5);
+      for (int k = tid; k < (n + 31) >> 5; k += kTreeThreads) mbuf[k] = __ldg(msrc + k);
     }
+    cp_async_wait_all();
+    __syncthreads();
   }
-  uint32_t mbits = 0xFFFFFFFFu;
-  if (masked && n_mine > 0) mbits = __ldg(a.mask + static_cast<size_t>(n0 + cut) * W + (e0 >> 5));
-  if (n_mine < kSpan) mbits &= (n_mine > 0 ? (0xFFFFFFFFu >> (32 - n_mine)) : 0u);
+  auto in_set = [&](int e) -> bool { return !masked || ((mbuf[e >> 5] >> (e & 31)) & 1u); };
 
   // LSE / Z of the cut row: from the partials if it has children (the same
   // values its children were tested with), else reduced here across the cluster
@@ -476,53 +528,71 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
       if (logits) lse = row_lse(cut);
       if (masked) z = row_z(cut);
     } else {
-      float m = -INFINITY, s = 0.0f;
+      float m = -INFINITY;
       unsigned long long zs = 0;
-#pragma unroll
-      for (int k = 0; k < kSpan; ++k) {
-        if (logits && k < n_mine) lse_push(m, s, tr[k]);  // full-vocabulary softmax
-        if (masked && ((mbits >> k) & 1u)) zs += fix40(dr[k]);
+      for (int e = tid; e < n; e += kTreeThreads) {
+        if (logits) m = fmaxf(m, tbuf[e]);
+        if (masked && in_set(e)) zs += fix40(dbuf[e]);
       }
-      if (logits) block_lse(sm, m, s);
+      if (logits) m = block_max_f32(sm, m);
       if (masked) zs = block_sum_u64(sm, zs);
       if (tid == 0) {
         sm.x_m = m;
-        sm.x_s = s;
         sm.x_z = zs;
       }
       cluster.sync();
-      float M = -INFINITY, Ssum = 0.0f;
+      float M = -INFINITY;
       unsigned long long Z = 0;
       for (int c = 0; c < C; ++c) {
         const TreeSmem* o = cluster.map_shared_rank(&sm, c);
-        lse_combine(M, Ssum, o->x_m, o->x_s);
+        M = fmaxf(M, o->x_m);
         Z += o->x_z;
       }
-      lse = M + logf(Ssum);
       z = z_from_sum(Z);
+      if (logits) {
+        float ssum = 0.0f;
+        if (M != -INFINITY)
+          for (int e = tid; e < n; e += kTreeThreads) ssum += expf(tbuf[e] - M);
+        ssum = block_sum_f32(sm, ssum);
+        if (tid == 0) sm.x_s = ssum;
+        cluster.sync();
+        float Ssum = 0.0f;
+        for (int c = 0; c < C; ++c) Ssum += cluster.map_shared_rank(&sm, c)->x_s;
+        lse = M + logf(Ssum);
+      }
+      cluster.sync();  // every CTA has read the slots before they are reused
     }
   }
-  // p~ and q~ of the cut row in place (0 off the retained set and past V)
-#pragma unroll
-  for (int k = 0; k < kSpan; ++k) {
-    const bool in = (mbits >> k) & 1u;
-    float p = logits ? expf(tr[k] - lse) : tr[k];
-    float q = dr[k];
+  // p~ and q~ of the cut row in place (0 off the retained set)
+  for (int e = tid; e < n; e += kTreeThreads) {
+    const bool in = in_set(e);
+    float p = logits ? expf(tbuf[e] - lse) : tbuf[e];
+    float q = dbuf[e];
     if (masked) {
       p = __fdiv_rn(p, z);
       q = __fdiv_rn(q, z);
     }
-    tr[k] = in ? p : 0.0f;
-    dr[k] = in ? q : 0.0f;
+    tbuf[e] = in ? p : 0.0f;
+    dbuf[e] = in ? q : 0.0f;
   }
+  __syncthreads();
 
   const float u0 = sm.u[0];
   bool drawn = false;
+  const int warp = tid >> 5, lane = tid & 31;
   for (int pass = sm.has_child[cut] ? 0 : 1; pass < 2 && !drawn; ++pass) {
-    unsigned long long mine = 0;
-#pragma unroll
-    for (int k = 0; k < kSpan; ++k) mine += fix40(pass == 0 ? __fsub_rn(tr[k], dr[k]) : tr[k]);
-    const unsigned long long part = block_sum_u64(sm, mine);
+    auto quantum = [&](int e) -> unsigned long long {
+      return e < n ? fix40(pass == 0 ? __fsub_rn(tbuf[e], dbuf[e]) : tbuf[e]) : 0ull;
+    };
+    // per-warp sums over contiguous spans [warp*kWarpSpan, +kWarpSpan)
+    unsigned long long wsum = 0;
+    for (int k = 0; k < kWarpSpan / 32; ++k) wsum += quantum(warp * kWarpSpan + k * 32 + lane);
+    for (int o = 16; o; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    __syncthreads();
+    if (lane == 0) sm.red_u64[warp] = wsum;
+    __syncthreads();
+    unsigned long long part = 0;
+    for (int k = 0; k < kTreeWarps; ++k) part += sm.red_u64[k];
     if (tid == 0) sm.x_u64 = part;
     cluster.sync();
     unsigned long long S = 0, before = 0;
@@ -535,18 +605,32 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     if (S == 0) continue;  // the same decision in every CTA
     drawn = true;
     const unsigned long long t = scaled_draw(u0, S);
-    if (t >= before && t - before < part) {  // this CTA holds the token (CTA-uniform)
-      const unsigned long long tl = t - before;
-      const unsigned long long excl = block_exclusive_u64(sm, mine);
-      if (mine > 0 && tl >= excl && tl - excl < mine) {
-        unsigned long long cum = excl;
-        int tok = -1;
-#pragma unroll
-        for (int k = 0; k < kSpan; ++k) {
-          cum += fix40(pass == 0 ? __fsub_rn(tr[k], dr[k]) : tr[k]);
-          if (tok < 0 && cum > tl) tok = e0 + k;
+    if (t >= before && t - before < part) {  // this CTA holds the token
+      unsigned long long cum = t - before;     // target offset within the CTA
+      int w0 = 0;
+      for (; w0 < kTreeWarps; ++w0) {
+        const unsigned long long ws = sm.red_u64[w0];
+        if (cum < ws) break;
+        cum -= ws;
+      }
+      if (warp == w0) {  // walk the warp's span in steps of 32 entries
+        unsigned long long acc = 0;
+        for (int k = 0; k < kWarpSpan / 32; ++k) {
+          const int e = warp * kWarpSpan + k * 32 + lane;
+          const unsigned long long f = quantum(e);
+          unsigned long long inc = f;
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+          }
+          const bool hit = acc + inc > cum;
+          const uint32_t hits = __ballot_sync(0xffffffffu, hit);
+          if (hits) {
+            if (lane == __ffs(hits) - 1) a.bonus_token[b] = lo + e;
+            break;
+          }
+          acc += __shfl_sync(0xffffffffu, inc, 31);
         }
-        a.bonus_token[b] = tok;
       }
     }
   }
@@ -554,11 +638,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     // no mass at all: smallest index of the largest p~ (NaN ignored)
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-#pragma unroll
-    for (int k = 0; k < kSpan; ++k)
-      if (k < n_mine && tr[k] > bv) {
-        bv = tr[k];
-        bi = e0 + k;
+    for (int e = tid; e < n; e += kTreeThreads)
+      if (tbuf[e] > bv) {
+        bv = tbuf[e];
+        bi = lo + e;
       }
     block_argmax(sm, bv, bi);
     if (tid == 0) {
@@ -587,7 +670,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
 int accept_chunks(int vocab) { return (vocab + kChunk - 1) / kChunk; }
 
 int accept_cluster_size(int vocab) {
-  int c = (vocab + kTreeThreads * kSpan - 1) / (kTreeThreads * kSpan);
+  int c = (vocab + kCtaSpan - 1) / kCtaSpan;
   return c < 1 ? 1 : c;
 }
 
@@ -609,12 +692,14 @@ int launch_accept(const AcceptArgs& a, void* workspace, cudaStream_t stream) {
   cudaGetDevice(&dev);
   if (attr_dev != dev) {
     cudaFuncSetAttribute(accept_tree_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaFuncSetAttribute(accept_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kTreeSmemBytes);
     attr_dev = dev;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, a.batch, 1);
   cfg.blockDim = dim3(kTreeThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = kTreeSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -22,14 +22,15 @@
 //                      pages past the sequence load as zeros (out of bounds).
 //   warp 5  (MMA)      one thread issues tcgen05.mma: S = Q K^T into a
 //                      double-buffered TMEM tile (128 x 64 fp32), and
-//                      O += P V into a TMEM accumulator (128 x D fp32).
-//   warps 0-3          one thread per row: tcgen05.ld of S, scale, the tree
-//                      mask from a per-node ancestor bitmask (shared memory),
-//                      fp32 online softmax with exp2, rescale of O in TMEM
-//                      only when the running max grows by more than 2^8, P as
-//                      bf16 into a double-buffered, 128B-swizzled shared tile.
-// All operands use the 128-byte swizzle that TMA writes, so the MMA reads
-// them straight from the ring.  Long prefixes are split over CTAs (split-KV):
+//                      O += P V into a TMEM accumulator (128 x D fp32) with
+//                      P read from TMEM as the A operand.
+//   warps 0-3          one thread per row: tcgen05.ld of S, the tree mask
+//                      from a per-node ancestor bitmask (shared memory), fp32
+//                      online softmax in base 2, rescale of O in TMEM only
+//                      when the running max grows by more than 2^8, and P as
+//                      bf16 pairs stored back to a double-buffered TMEM tile.
+// Q, K and V use the 128-byte swizzle that TMA writes, so the MMA reads them
+// straight from the ring; P never touches shared memory.  Long prefixes are split over CTAs (split-KV):
 // each split writes (O, m, l) in fp32 and a merge kernel combines them.
 // Every wait on an mbarrier is bounded; on expiry the CTA reports
 // TV_ERR_DEVICE_TIMEOUT for its sequence, drains its copies and returns.
@@ -55,19 +56,20 @@ struct Layout {
   static constexpr int kHalfBytes = BN * 128;    // one 64-column half of a tile
   static constexpr int kStage0 = kQ + kQBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kP0 = kStage0 + kStages * kStageBytes;
-  static constexpr int kPBytes = BM * BN * 2;
-  static constexpr int kAnc = kP0 + 2 * kPBytes;
+  static constexpr int kAnc = kStage0 + kStages * kStageBytes;
   static constexpr int kAncBytes = BM * kMaxAncWords * 4;
   static constexpr int kParent = kAnc + kAncBytes;
   static constexpr int kParentBytes = 512 * 4;
   static constexpr int kBar = kParent + kParentBytes;
-  // full[kStages], empty[kStages], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int kNumBars = 2 * kStages + 7;
+  // full[kStages], empty[kStages], s_full[2], p_full[2], o_done[2], drain,
+  // q_ready, s_free[2]
+  static constexpr int kNumBars = 2 * kStages + 10;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 64;
   static constexpr int kAlloc = kTotal + 1024;  // slack for 1024-byte alignment
-  static constexpr int kTmemCols = (64 * 2 + D) <= 256 ? 256 : 512;
+  // TMEM columns: S[2] at 0 and 64 (fp32), O at 128 (D columns), P[2] at
+  // 256 and 288 (bf16 pairs, 32 columns each)
+  static constexpr int kTmemCols = 512;
 };
 
 struct Misc {
@@ -90,6 +92,17 @@ __device__ __forceinline__ void record_status(int32_t* status, int b, int code) 
   atomicMax(status + b, code);
 }
 
+// Zeros output row r (0..127) of this tile if it is a live row.
+template <int D>
+__device__ __forceinline__ void zero_rows(const AttnArgs& a, const Work& w, int r) {
+  const int R = w.mtile * BM + r;
+  if (R >= w.rows) return;
+  const int i = R / a.group, h = w.kvh * a.group + R % a.group;
+  uint4* dst = reinterpret_cast<uint4*>(a.out + (static_cast<size_t>(w.n0 + i) * a.hq + h) * D);
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tree_attn_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps) {
@@ -104,6 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
   uint64_t* drain = o_done + 2;
+  uint64_t* q_ready = drain + 1;
+  uint64_t* s_free = q_ready + 1;
   Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
   uint32_t* anc = reinterpret_cast<uint32_t*>(smem + Ly::kAnc);
   int32_t* par = reinterpret_cast<int32_t*>(smem + Ly::kParent);
@@ -134,76 +149,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = a.group;
 
   // ------------------------------------------------------------ prologue
+  // Barriers and TMEM first, so that the TMA warp starts streaming K/V at
+  // once; the softmax warps stage Q, validate the tree and build the ancestor
+  // masks meanwhile, and release the first MMA through q_ready.
   if (tid == 0) {
     misc->abort = 0;
     misc->bad = (w.N > a.max_nodes || w.N > 512 || w.L > a.max_prefix_len || w.n0 < 0 ||
                  w.n0 + w.N > a.total_nodes) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!misc->bad) {
-    for (int i = tid; i < w.N; i += kThreads) {
-      const int p = a.parent[w.n0 + i];
-      par[i] = p;
-      if (!(i == 0 ? p == -1 : (p >= 0 && p < i))) misc->bad = 1;
-    }
-    // block ids of this split's pages
-    const int pg0 = w.k_begin / 16, pg1 = (w.k_end + 15) / 16;
-    for (int pg = pg0 + tid; pg < pg1; pg += kThreads) {
-      if (pg >= a.max_blocks_per_seq) {
-        misc->bad = 1;
-        break;
-      }
-      const int blk = a.block_table[static_cast<size_t>(w.b) * a.max_blocks_per_seq + pg];
-      if (blk < 0 || blk >= a.num_blocks) misc->bad = 1;
-    }
-  }
-  __syncthreads();
-  const bool bad = misc->bad != 0;
-  if (bad) {
-    if (tid == 0) record_status(a.status, w.b, kBadTree);
-    const bool rows_addressable = w.n0 >= 0 && w.N <= a.max_nodes && w.n0 + w.N <= a.total_nodes;
-    if (w.nsplit == 1 && rows_addressable) {  // the only writer of these rows: zeros
-      for (int r = tid; r < BM; r += kThreads) {
-        const int R = w.mtile * BM + r;
-        if (R >= w.rows) continue;
-        const int i = R / g, h = w.kvh * g + R % g;
-        uint4* dst = reinterpret_cast<uint4*>(a.out + (static_cast<size_t>(w.n0 + i) * a.hq + h) * D);
-        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    return;
-  }
-
-  if (warp < 4) {
-    // Q tile -> shared memory, 128B-swizzled K-major; padding rows are zero.
-    const int r = tid;
-    const int R = w.mtile * BM + r;
-    const bool live = R < w.rows;
-    const uint4* src = nullptr;
-    if (live) {
-      const int i = R / g, h = w.kvh * g + R % g;
-      src = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(w.n0 + i) * a.hq + h) * D);
-    }
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const uint4 v = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-      const int half = c >> 3, cc = c & 7;
-      *reinterpret_cast<uint4*>(smem + Ly::kQ + half * (BM * 128) + r * 128 +
-                                ((cc ^ (r & 7)) << 4)) = v;
-    }
-    // ancestor-or-self bitmask of the tile's nodes (only node tiles need it)
-    if (w.last_split) {
-      const int i = node_lo + r;
-      uint32_t* row = anc + r * kMaxAncWords;
-#pragma unroll
-      for (int k = 0; k < kMaxAncWords; ++k) row[k] = 0u;
-      if (i < w.N) {
-        for (int k = i; k >= 0; k = par[k]) row[k >> 5] |= 1u << (k & 31);
-      }
-    }
-    fence_proxy_async_smem();  // Q written by the generic proxy, read by the MMA
-  }
-  if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
@@ -214,6 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_done[k], 1);
     }
     mbar_init(drain, 1);
+    mbar_init(q_ready, 128);
+    mbar_init(&s_free[0], 128);
+    mbar_init(&s_free[1], 128);
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -224,8 +179,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
+  if (misc->bad) {  // the sequence's extent itself is malformed: nothing to read
+    if (tid == 0) record_status(a.status, w.b, kBadTree);
+    const bool rows_addressable = w.n0 >= 0 && w.N <= a.max_nodes && w.n0 + w.N <= a.total_nodes;
+    if (w.nsplit == 1 && rows_addressable && warp < 4) zero_rows<D>(a, w, tid);
+    if (warp == 5) tmem_dealloc(tmem, Ly::kTmemCols);
+    return;
+  }
   const uint32_t tmem_s0 = tmem;        // S buffers at columns 0 and 64
   const uint32_t tmem_o = tmem + 128;   // O accumulator at columns 128 .. 128+D-1
+  const uint32_t tmem_p0 = tmem + 256;  // P buffers (A operand of P.V) at 256 and 288
   volatile int* abort_flag = &misc->abort;
 
   if (warp == 4) {
@@ -255,7 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int row = pool_rows;  // out of bounds: zero fill
             if (lp * 16 < w.k_end) {
               const int blk = __ldg(a.block_table + static_cast<size_t>(w.b) * a.max_blocks_per_seq + lp);
-              row = (blk * a.hkv + w.kvh) * 16;
+              if (blk >= 0 && blk < a.num_blocks) {
+                row = (blk * a.hkv + w.kvh) * 16;
+              } else if (!misc->bad) {  // malformed block id: zeros, reported
+                misc->bad = 1;
+                record_status(a.status, w.b, kBadTree);
+              }
             }
 #pragma unroll
             for (int h = 0; h < Ly::kHalves; ++h) {
@@ -288,42 +256,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_o = idesc_bf16(BM, D, 1);
       const uint32_t q_base = smem_u32(smem + Ly::kQ);
       bool ok = true;
-      auto issue_s = [&](int t) -> bool {
+      // S(t) = Q K(t)^T into S buffer t&1 (caller checked K(t) landed and the
+      // buffer is free)
+      auto issue_s = [&](int t) {
         const int st = t % kStages;
-        if (!mbar_wait(&full[st], (t / kStages) & 1, abort_flag)) return false;
-        tc_fence_after();
         const uint32_t k_base = smem_u32(smem + Ly::kStage0 + st * Ly::kStageBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 0 + ((kk & 3) << 5);
+          const uint32_t off = (kk & 3) << 5;
           const uint64_t ad = smem_desc(q_base + (kk >> 2) * (BM * 128) + off, 16, 1024);
           const uint64_t bd = smem_desc(k_base + (kk >> 2) * Ly::kHalfBytes + off, 16, 1024);
           mma_bf16_ss(tmem_s0 + (t & 1) * BN, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[t & 1]);
-        return true;
       };
-      auto issue_pv = [&](int t) -> bool {
+      // O += P(t) V(t) (caller checked P(t) is in TMEM)
+      auto issue_pv = [&](int t) {
         const int st = t % kStages;
-        if (!mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t p_base = smem_u32(smem + Ly::kP0 + (t & 1) * Ly::kPBytes);
         const uint32_t v_base = smem_u32(smem + Ly::kStage0 + st * Ly::kStageBytes + Ly::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t ad = smem_desc(p_base + (kk << 5), 16, 1024);
+          // A = P from TMEM: 16 keys = 8 columns of bf16 pairs per step
           const uint64_t bd = smem_desc(v_base + kk * 2048, Ly::kHalfBytes, 1024);
-          mma_bf16_ss(tmem_o, ad, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem_o, tmem_p0 + (t & 1) * 32 + kk * 8, bd, idesc_o,
+                      (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&o_done[t & 1]);
         mma_commit(&empty[st]);
-        return true;
       };
-      if (w.T > 0) ok = issue_s(0);
-      if (ok && w.T > 1) ok = issue_s(1);
-      for (int t = 0; t < w.T && ok; ++t) {
-        ok = issue_pv(t);
-        if (ok && t + 2 < w.T) ok = issue_s(t + 2);
+      // Issue in whichever order the inputs become ready: S(t) needs K(t) in
+      // the ring and S buffer t&1 released by the softmax of tile t-2
+      // (s_free, right after it loaded S(t-2) into registers), so the tensor
+      // core computes S two tiles ahead; P(t).V(t) needs P(t) (p_full).
+      ok = mbar_wait(q_ready, 0, abort_flag);
+      tc_fence_after();
+      int ns = 0, npv = 0;
+      unsigned long long t_idle = 0;
+      while (ok && npv < w.T) {
+        bool progressed = false;
+        if (ns < w.T && ns < npv + 3 &&
+            (ns < 2 || mbar_test_wait(&s_free[ns & 1], ((ns - 2) >> 1) & 1)) &&
+            mbar_test_wait(&full[ns % kStages], (ns / kStages) & 1)) {
+          tc_fence_after();
+          issue_s(ns);
+          ++ns;
+          progressed = true;
+        }
+        if (npv < ns && mbar_test_wait(&p_full[npv & 1], (npv >> 1) & 1)) {
+          tc_fence_after();
+          issue_pv(npv);
+          ++npv;
+          progressed = true;
+        }
+        if (progressed) {
+          t_idle = 0;
+        } else if (t_idle == 0) {
+          t_idle = global_ns();
+        } else if (global_ns() - t_idle > kWaitLimitNs || misc->abort) {
+          ok = false;
+        }
       }
       if (!ok) {
         record_status(a.status, w.b, kDeviceTimeout);
@@ -339,6 +330,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = tid;                 // row of the tile == TMEM lane
     const int R = w.mtile * BM + r;
     const bool live = R < w.rows;
+    // tree of this sequence into shared memory, validated
+    for (int i = r; i < w.N; i += 128) {
+      const int p = __ldg(a.parent + w.n0 + i);
+      par[i] = p;
+      if (!(i == 0 ? p == -1 : (p >= 0 && p < i))) misc->bad = 1;
+    }
+    // Q tile -> shared memory, 128B-swizzled K-major; padding rows are zero.
+    {
+      const uint4* src = nullptr;
+      if (live) {
+        const int i = R / g, h = w.kvh * g + R % g;
+        src = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(w.n0 + i) * a.hq + h) * D);
+      }
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        const int half = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4*>(smem + Ly::kQ + half * (BM * 128) + r * 128 +
+                                  ((cc ^ (r & 7)) << 4)) = v;
+      }
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps only
+    const bool tree_ok = misc->bad == 0;
+    if (!tree_ok && r == 0) record_status(a.status, w.b, kBadTree);
+    // ancestor-or-self bitmask of the tile's nodes (node tiles only)
+    if (w.last_split) {
+      const int i = node_lo + r;
+      uint32_t* row = anc + r * kMaxAncWords;
+#pragma unroll
+      for (int k = 0; k < kMaxAncWords; ++k) row[k] = 0u;
+      if (tree_ok && i < w.N) {
+        for (int k = i; k >= 0; k = par[k]) row[k >> 5] |= 1u << (k & 31);
+      }
+    }
+    fence_proxy_async_smem();  // Q written by the generic proxy, read by the MMA
+    mbar_arrive(q_ready);
+    asm volatile("bar.sync 1, 128;" ::: "memory");  // ancestor rows are read across threads
     const int i_node = live ? R / g : 0;  // local node of this row
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t* my_anc = anc + (i_node - node_lo) * kMaxAncWords;
@@ -359,6 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem_s0 + (t & 1) * BN + 32 + lane_off, hi);
         tmem_ld_wait();
       }
+      tc_fence_before();
+      mbar_arrive(&s_free[t & 1]);  // S buffer t&1 may now take S(t+2)
       // scale + mask (scores stay unscaled here; the scale is folded into
       // the exponent below), then the row max as a tree of fmaxf
       float x[64];
@@ -427,24 +457,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
-      uint8_t* prow = smem + Ly::kP0 + (t & 1) * Ly::kPBytes + r * 128;
+      uint32_t pk[32];  // P row as bf16 pairs: column c holds keys 2c (low) and 2c+1
       float ls[8];
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
-        uint32_t pk[4];
         float part = 0.0f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           // p = 2^(s * scale * log2(e) - m); masked scores are -inf -> 0
           const float p0 = ex2_approx(fmaf(x[c8 * 8 + 2 * k], a.scale_log2, -mref));
           const float p1 = ex2_approx(fmaf(x[c8 * 8 + 2 * k + 1], a.scale_log2, -mref));
-          pk[k] = pack_bf16x2(p0, p1);
+          const uint32_t q = pack_bf16x2(p0, p1);
+          pk[c8 * 4 + k] = q;
           // l accumulates the bf16-rounded weights that the P.V product uses
-          part += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
+          part += __uint_as_float(q << 16) + __uint_as_float(q & 0xFFFF0000u);
         }
         ls[c8] = part;
-        *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      tmem_st32(tmem_p0 + (t & 1) * 32 + lane_off, pk);
       const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       l_run += lsum;
       // keys past the prefix end in this tile: clear their V rows (page tails
@@ -459,8 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 8; ++k) p[k] = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();  // generic writes, read by the MMA
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[t & 1]);
     }
@@ -511,14 +542,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // a malformed tree or block id: the only writer of these rows writes zeros
+  // (each row by the thread that wrote it in the epilogue, so zeros win)
+  if (misc->bad && w.nsplit == 1 && warp < 4) zero_rows<D>(a, w, tid);
   if (warp == 5) tmem_dealloc(tmem, Ly::kTmemCols);
 }
 
-// Combines the split partials of one (sequence, KV head, m-tile):
-// O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+// Combines the split partials: one warp per packed output row,
+// O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, lanes over D (float4).
+constexpr int kMergeWarps = 8;
 template <int D>
-__global__ void __launch_bounds__(128) tree_attn_merge(const AttnArgs a) {
-  const int unit = blockIdx.x;
+__global__ void __launch_bounds__(kMergeWarps * 32) tree_attn_merge(const AttnArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x / (BM / kMergeWarps);
+  const int r = (blockIdx.x % (BM / kMergeWarps)) * kMergeWarps + warp;
   const int mtile = unit % a.mtiles_max;
   const int bk = unit / a.mtiles_max;
   const int b = bk / a.hkv, kvh = bk % a.hkv;
@@ -528,41 +565,51 @@ __global__ void __launch_bounds__(128) tree_attn_merge(const AttnArgs a) {
   const int nsplit = max(1, (L + a.chunk - 1) / a.chunk);
   const int rows = N * a.group;
   if (nsplit == 1 || N < 1 || N > a.max_nodes || L > a.max_prefix_len || n0 < 0 ||
-      n0 + N > a.total_nodes || mtile * BM >= rows)
+      n0 + N > a.total_nodes)
     return;
-  const bool bad = a.status[b] == kBadTree;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < BM; r += 4) {
-    const int R = mtile * BM + r;
-    if (R >= rows) break;
-    const int i = R / a.group, h = kvh * a.group + R % a.group;
-    uint16_t* dst = a.out + (static_cast<size_t>(n0 + i) * a.hq + h) * D;
-    if (bad) {
-      for (int d = lane; d < D; d += 32) dst[d] = 0;
-      continue;
-    }
-    const size_t base = (static_cast<size_t>(unit) * a.max_splits) * BM + r;
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, a.ws_ml[base + static_cast<size_t>(s) * BM].x);
-    const float mref = (M == -INFINITY) ? 0.0f : M;
-    float acc[D / 32];
+  const int R = mtile * BM + r;
+  if (R >= rows) return;
+  const int i = R / a.group, h = kvh * a.group + R % a.group;
+  uint16_t* dst = a.out + (static_cast<size_t>(n0 + i) * a.hq + h) * D;
+  constexpr int kPer = D / 32;  // elements per lane (4 for D=128, 2 for D=64)
+  if (a.status[b] == kBadTree) {
+    for (int d = lane; d < D; d += 32) dst[d] = 0;
+    return;
+  }
+  const size_t base = (static_cast<size_t>(unit) * a.max_splits) * BM + r;
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, a.ws_ml[base + static_cast<size_t>(s) * BM].x);
+  const float mref = (M == -INFINITY) ? 0.0f : M;
+  float acc[kPer];
 #pragma unroll
-    for (int k = 0; k < D / 32; ++k) acc[k] = 0.0f;
-    float lsum = 0.0f;
-    for (int s = 0; s < nsplit; ++s) {
-      const size_t pr = base + static_cast<size_t>(s) * BM;
-      const float2 ml = a.ws_ml[pr];
-      const float wgt = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - mref);
-      lsum += wgt * ml.y;
-#pragma unroll
-      for (int k = 0; k < D / 32; ++k) acc[k] += wgt * a.ws_o[pr * D + k * 32 + lane];
+  for (int k = 0; k < kPer; ++k) acc[k] = 0.0f;
+  float lsum = 0.0f;
+  for (int s = 0; s < nsplit; ++s) {
+    const size_t pr = base + static_cast<size_t>(s) * BM;
+    const float2 ml = a.ws_ml[pr];
+    const float wgt = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - mref);
+    lsum += wgt * ml.y;
+    const float* src = a.ws_o + pr * D + lane * kPer;
+    if constexpr (kPer == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] += wgt * v.x;
+      acc[1] += wgt * v.y;
+      acc[2] += wgt * v.z;
+      acc[3] += wgt * v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] += wgt * v.x;
+      acc[1] += wgt * v.y;
     }
-    const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
-#pragma unroll
-    for (int k = 0; k < D / 32; ++k) {
-      const uint32_t pk = pack_bf16x2(acc[k] * inv, 0.0f);
-      dst[k * 32 + lane] = static_cast<uint16_t>(pk & 0xFFFFu);
-    }
+  }
+  const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+  if constexpr (kPer == 4) {
+    uint2 o;
+    o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst + lane * 4) = o;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst + lane * 2) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
   }
 }
 
@@ -590,7 +637,8 @@ int launch_tree_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
     tree_attn_kernel<128><<<grid, kThreads, smem, stream>>>(a, maps);
     e = cudaGetLastError();
     if (e == cudaSuccess && a.max_splits > 1) {
-      tree_attn_merge<128><<<a.batch * a.hkv * a.mtiles_max, 128, 0, stream>>>(a);
+      tree_attn_merge<128><<<a.batch * a.hkv * a.mtiles_max * (BM / kMergeWarps),
+                             kMergeWarps * 32, 0, stream>>>(a);
       e = cudaGetLastError();
     }
   } else {
@@ -598,7 +646,8 @@ int launch_tree_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
     tree_attn_kernel<64><<<grid, kThreads, smem, stream>>>(a, maps);
     e = cudaGetLastError();
     if (e == cudaSuccess && a.max_splits > 1) {
-      tree_attn_merge<64><<<a.batch * a.hkv * a.mtiles_max, 128, 0, stream>>>(a);
+      tree_attn_merge<64><<<a.batch * a.hkv * a.mtiles_max * (BM / kMergeWarps),
+                            kMergeWarps * 32, 0, stream>>>(a);
       e = cudaGetLastError();
     }
   }
