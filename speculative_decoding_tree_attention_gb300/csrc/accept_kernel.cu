@@ -43,9 +43,15 @@ namespace {
 constexpr int kMaxN = 512;
 constexpr int kTreeThreads = 512;
 constexpr int kTreeWarps = kTreeThreads / 32;
-constexpr int kWarpSpan = 1024;        // bonus draw: contiguous entries per warp
-constexpr int kCtaSpan = kWarpSpan * (kTreeThreads / 32);  // 16384 entries per CTA
-constexpr int kTreeSmemBytes = 2 * kCtaSpan * 4 + (kCtaSpan / 32) * 4;
+constexpr int kMaxCluster = 16;        // CTAs per tree (non-portable cluster size)
+constexpr int kChunkQuantum = 32 * kTreeWarps;  // a CTA's slice of the cut row: multiple of 512
+constexpr int kMinChunk = 2048;        // entries per CTA before another CTA is worth it
+// Entries of the cut row per CTA (multiple of kChunkQuantum) for C CTAs.
+__host__ __device__ inline int bonus_chunk(int vocab, int C) {
+  const int c = (vocab + C - 1) / C;
+  return (c + kChunkQuantum - 1) / kChunkQuantum * kChunkQuantum;
+}
+__host__ __device__ inline int tree_smem_bytes(int chunk) { return 2 * chunk * 4 + (chunk / 32) * 4; }
 constexpr int kRowThreads = 256;
 constexpr int kRowVec = 8;             // float4 per thread per chunk
 constexpr int kChunk = kRowThreads * kRowVec * 4;  // 8192 entries per row chunk
@@ -485,10 +491,11 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
   // The cut row's chunk of this CTA, [lo, hi), goes to shared memory with
   // cp.async; every pass then reads it coalesced.  The exact find walks
   // contiguous 1024-entry warp spans in index order with warp scans.
+  const int chunk = bonus_chunk(V, C);
+  const int wspan = chunk / kTreeWarps;  // contiguous entries per warp (multiple of 32)
   float* tbuf = smem_rows;
-  float* dbuf = smem_rows + kCtaSpan;
-  uint32_t* mbuf = reinterpret_cast<uint32_t*>(smem_rows + 2 * kCtaSpan);
-  const int chunk = ((V + C - 1) / C + kWarpSpan - 1) / kWarpSpan * kWarpSpan;
+  float* dbuf = smem_rows + chunk;
+  uint32_t* mbuf = reinterpret_cast<uint32_t*>(smem_rows + 2 * chunk);
   const int lo = min(V, rank * chunk), hi = min(V, lo + chunk);
   const int n = hi - lo;
   const size_t crow = static_cast<size_t>(n0 + cut) * V;
@@ -584,9 +591,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     auto quantum = [&](int e) -> unsigned long long {
       return e < n ? fix40(pass == 0 ? __fsub_rn(tbuf[e], dbuf[e]) : tbuf[e]) : 0ull;
     };
-    // per-warp sums over contiguous spans [warp*kWarpSpan, +kWarpSpan)
+    // per-warp sums over contiguous spans [warp*wspan, +wspan)
     unsigned long long wsum = 0;
-    for (int k = 0; k < kWarpSpan / 32; ++k) wsum += quantum(warp * kWarpSpan + k * 32 + lane);
+    for (int k = 0; k < wspan / 32; ++k) wsum += quantum(warp * wspan + k * 32 + lane);
     for (int o = 16; o; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     __syncthreads();
     if (lane == 0) sm.red_u64[warp] = wsum;
@@ -615,8 +622,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
       }
       if (warp == w0) {  // walk the warp's span in steps of 32 entries
         unsigned long long acc = 0;
-        for (int k = 0; k < kWarpSpan / 32; ++k) {
-          const int e = warp * kWarpSpan + k * 32 + lane;
+        for (int k = 0; k < wspan / 32; ++k) {
+          const int e = warp * wspan + k * 32 + lane;
           const unsigned long long f = quantum(e);
           unsigned long long inc = f;
           for (int o = 1; o < 32; o <<= 1) {
@@ -670,8 +677,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
 int accept_chunks(int vocab) { return (vocab + kChunk - 1) / kChunk; }
 
 int accept_cluster_size(int vocab) {
-  int c = (vocab + kCtaSpan - 1) / kCtaSpan;
-  return c < 1 ? 1 : c;
+  const int want = (vocab + kMinChunk - 1) / kMinChunk;
+  int c = 1;
+  while (c < want && c < kMaxCluster) c *= 2;  // 1, 2, 4, 8 or 16 CTAs per tree
+  return c;
 }
 
 int launch_accept(const AcceptArgs& a, void* workspace, cudaStream_t stream) {
@@ -693,13 +702,13 @@ int launch_accept(const AcceptArgs& a, void* workspace, cudaStream_t stream) {
   if (attr_dev != dev) {
     cudaFuncSetAttribute(accept_tree_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaFuncSetAttribute(accept_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kTreeSmemBytes);
+                         tree_smem_bytes(16384));
     attr_dev = dev;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, a.batch, 1);
   cfg.blockDim = dim3(kTreeThreads, 1, 1);
-  cfg.dynamicSmemBytes = kTreeSmemBytes;
+  cfg.dynamicSmemBytes = tree_smem_bytes(bonus_chunk(a.vocab, C));
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

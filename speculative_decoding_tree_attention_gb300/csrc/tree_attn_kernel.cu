@@ -34,6 +34,8 @@
 // each split writes (O, m, l) in fp32 and a merge kernel combines them.
 // Every wait on an mbarrier is bounded; on expiry the CTA reports
 // TV_ERR_DEVICE_TIMEOUT for its sequence, drains its copies and returns.
+#include <climits>
+
 #include "tv_device.cuh"
 #include "tv_launch.h"
 
@@ -42,25 +44,28 @@ namespace {
 
 constexpr int BM = 128;           // packed query rows per CTA
 constexpr int BN = 64;            // keys per tile
-constexpr int kStages = 4;        // K/V ring depth
-constexpr int kThreads = 192;     // 4 softmax warps + TMA warp + MMA warp
+constexpr int kStages = 6;        // K/V ring depth (64-key tiles)
+constexpr int kSoftmaxThreads = 256;  // warps 0-7
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;     // 8 softmax warps + TMA warp + MMA warp
 constexpr int kMaxAncWords = 16;  // 512-node trees
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
 struct Layout {
   static constexpr int kHalves = D / 64;
-  static constexpr int kQ = 0;
-  static constexpr int kQBytes = BM * D * 2;
   static constexpr int kTileBytes = BN * D * 2;  // one K or V tile
   static constexpr int kHalfBytes = BN * 128;    // one 64-column half of a tile
-  static constexpr int kStage0 = kQ + kQBytes;
+  static constexpr int kStage0 = 0;
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kAnc = kStage0 + kStages * kStageBytes;
   static constexpr int kAncBytes = BM * kMaxAncWords * 4;
   static constexpr int kParent = kAnc + kAncBytes;
   static constexpr int kParentBytes = 512 * 4;
-  static constexpr int kBar = kParent + kParentBytes;
+  static constexpr int kXchg = kParent + kParentBytes;  // row max / sum exchange
+  static constexpr int kXchgBytes = 3 * 2 * BM * 4;  // slots 0, 1: per-tile max; 2: row sum
+  static constexpr int kBar = kXchg + kXchgBytes;
   // full[kStages], empty[kStages], s_full[2], p_full[2], o_done[2], drain,
   // q_ready, s_free[2]
   static constexpr int kNumBars = 2 * kStages + 10;
@@ -68,7 +73,7 @@ struct Layout {
   static constexpr int kTotal = kMisc + 64;
   static constexpr int kAlloc = kTotal + 1024;  // slack for 1024-byte alignment
   // TMEM columns: S[2] at 0 and 64 (fp32), O at 128 (D columns), P[2] at
-  // 256 and 288 (bf16 pairs, 32 columns each)
+  // 256 and 288 (bf16 pairs, 32 columns each), Q at 320 (bf16 pairs, D/2)
   static constexpr int kTmemCols = 512;
 };
 
@@ -87,6 +92,19 @@ struct Work {
   int n_prefix_tiles, n_node_tiles, T;
   bool last_split;
 };
+
+// TMEM lane offset of a softmax warp (its 32-lane quarter).
+__device__ __forceinline__ uint32_t lane_off_q(int warp) {
+  return static_cast<uint32_t>((warp & 3) * 32) << 16;
+}
+
+// Named barriers among the 8 softmax warps (ids 1 and 2; 0 is __syncthreads).
+__device__ __forceinline__ void softmax_group_sync() {
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+__device__ __forceinline__ void softmax_pair_sync() {
+  asm volatile("bar.sync 2, 256;" ::: "memory");
+}
 
 __device__ __forceinline__ void record_status(int32_t* status, int b, int code) {
   atomicMax(status + b, code);
@@ -162,16 +180,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(&s_full[k], 1);
-      mbar_init(&p_full[k], 128);
+      mbar_init(&p_full[k], kSoftmaxThreads);
       mbar_init(&o_done[k], 1);
     }
     mbar_init(drain, 1);
-    mbar_init(q_ready, 128);
-    mbar_init(&s_free[0], 128);
-    mbar_init(&s_free[1], 128);
+    mbar_init(q_ready, kSoftmaxThreads);
+    mbar_init(&s_free[0], kSoftmaxThreads);
+    mbar_init(&s_free[1], kSoftmaxThreads);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&misc->tmem_base, Ly::kTmemCols);
     tmem_relinquish();
   }
@@ -183,64 +201,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) record_status(a.status, w.b, kBadTree);
     const bool rows_addressable = w.n0 >= 0 && w.N <= a.max_nodes && w.n0 + w.N <= a.total_nodes;
     if (w.nsplit == 1 && rows_addressable && warp < 4) zero_rows<D>(a, w, tid);
-    if (warp == 5) tmem_dealloc(tmem, Ly::kTmemCols);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, Ly::kTmemCols);
     return;
   }
   const uint32_t tmem_s0 = tmem;        // S buffers at columns 0 and 64
   const uint32_t tmem_o = tmem + 128;   // O accumulator at columns 128 .. 128+D-1
   const uint32_t tmem_p0 = tmem + 256;  // P buffers (A operand of P.V) at 256 and 288
+  const uint32_t tmem_q = tmem + 320;   // Q tile (A operand of Q.K^T)
   volatile int* abort_flag = &misc->abort;
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     // ---------------------------------------------------------- TMA producer
+    // The whole warp issues: lane 0 arms the stage's barrier, then each lane
+    // issues one of the tile's boxes (page pg, 64-column half h, K or V), so
+    // a tile's 16 page copies go out in one warp instruction.
     if (lane == 0) {
       prefetch_tmap(&maps.k_pool);
       prefetch_tmap(&maps.v_pool);
       prefetch_tmap(&maps.k_nodes);
       prefetch_tmap(&maps.v_nodes);
-      const int pool_rows = a.num_blocks * a.hkv * 16;
-      int issued = 0;
-      bool ok = true;
-      for (int t = 0; t < w.T && ok; ++t) {
-        const int st = t % kStages;
-        if (!mbar_wait(&empty[st], ((t / kStages) & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        uint8_t* kdst = smem + Ly::kStage0 + st * Ly::kStageBytes;
-        uint8_t* vdst = kdst + Ly::kTileBytes;
-        mbar_arrive_expect_tx(&full[st], 2 * Ly::kTileBytes);
-        if (t < w.n_prefix_tiles) {
-          const int key0 = w.k_begin + t * BN;
-#pragma unroll
-          for (int pg = 0; pg < BN / 16; ++pg) {
-            const int lp = key0 / 16 + pg;
-            int row = pool_rows;  // out of bounds: zero fill
-            if (lp * 16 < w.k_end) {
-              const int blk = __ldg(a.block_table + static_cast<size_t>(w.b) * a.max_blocks_per_seq + lp);
-              if (blk >= 0 && blk < a.num_blocks) {
-                row = (blk * a.hkv + w.kvh) * 16;
-              } else if (!misc->bad) {  // malformed block id: zeros, reported
-                misc->bad = 1;
-                record_status(a.status, w.b, kBadTree);
-              }
-            }
-#pragma unroll
-            for (int h = 0; h < Ly::kHalves; ++h) {
-              tma_load_2d(kdst + h * Ly::kHalfBytes + pg * 2048, &maps.k_pool, &full[st], h * 64, row);
-              tma_load_2d(vdst + h * Ly::kHalfBytes + pg * 2048, &maps.v_pool, &full[st], h * 64, row);
-            }
+    }
+    constexpr int kPages = BN / 16;
+    constexpr int kBoxes = kPages * Ly::kHalves * 2;  // prefix tile: pages x halves x {K, V}
+    constexpr int kPastEnd = INT_MIN;                 // page past the prefix end -> zeros
+    const int my_pg = lane / (Ly::kHalves * 2);
+    const int my_h = (lane / 2) % Ly::kHalves;
+    const int my_kv = lane & 1;
+    const bool prefix_lane = lane < kBoxes;
+    const bool node_lane = lane < Ly::kHalves * 2;
+    const int pool_rows = a.num_blocks * a.hkv * 16;
+    const int32_t* btab = a.block_table + static_cast<size_t>(w.b) * a.max_blocks_per_seq;
+    auto fetch_block = [&](int t) -> int {
+      const int lp = (w.k_begin + t * BN) / 16 + my_pg;
+      return (prefix_lane && lp * 16 < w.k_end) ? __ldg(btab + lp) : kPastEnd;
+    };
+    int blk_next = w.n_prefix_tiles > 0 ? fetch_block(0) : kPastEnd;
+    int issued = 0;
+    bool ok = true;
+    for (int t = 0; t < w.T; ++t) {
+      const int st = t % kStages;
+      const int blk = blk_next;
+      if (t + 1 < w.n_prefix_tiles) blk_next = fetch_block(t + 1);  // overlaps the wait
+      if (lane == 0) ok = mbar_wait(&empty[st], ((t / kStages) & 1) ^ 1, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], 2 * Ly::kTileBytes);
+      __syncwarp();
+      uint8_t* dst = smem + Ly::kStage0 + st * Ly::kStageBytes + my_kv * Ly::kTileBytes +
+                     my_h * Ly::kHalfBytes;
+      if (t < w.n_prefix_tiles) {
+        if (prefix_lane) {
+          int row = pool_rows;  // out of bounds: zero fill
+          if (blk >= 0 && blk < a.num_blocks) {
+            row = (blk * a.hkv + w.kvh) * 16;
+          } else if (blk != kPastEnd && !misc->bad) {  // malformed block id: zeros, reported
+            misc->bad = 1;
+            record_status(a.status, w.b, kBadTree);
           }
-        } else {
-          const int node0 = w.n0 + (t - w.n_prefix_tiles) * BN;
-#pragma unroll
-          for (int h = 0; h < Ly::kHalves; ++h) {
-            tma_load_3d(kdst + h * Ly::kHalfBytes, &maps.k_nodes, &full[st], h * 64, w.kvh, node0);
-            tma_load_3d(vdst + h * Ly::kHalfBytes, &maps.v_nodes, &full[st], h * 64, w.kvh, node0);
-          }
+          tma_load_2d(dst + my_pg * 2048, my_kv ? &maps.v_pool : &maps.k_pool, &full[st],
+                      my_h * 64, row);
         }
-        ++issued;
+      } else if (node_lane) {
+        const int node0 = w.n0 + (t - w.n_prefix_tiles) * BN;
+        tma_load_3d(dst, my_kv ? &maps.v_nodes : &maps.k_nodes, &full[st], my_h * 64, w.kvh, node0);
       }
+      ++issued;
+    }
+    if (lane == 0) {
       if (!ok) {
         record_status(a.status, w.b, kDeviceTimeout);
         misc->abort = 1;
@@ -249,37 +276,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = max(0, issued - kStages); t < issued; ++t)
         mbar_wait(&full[t % kStages], (t / kStages) & 1);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);
       constexpr uint32_t idesc_o = idesc_bf16(BM, D, 1);
-      const uint32_t q_base = smem_u32(smem + Ly::kQ);
       bool ok = true;
+      // Descriptors are built once; each MMA adds a compile-time offset to the
+      // start-address field (16-byte units; shared addresses stay < 2^18).
+      const uint64_t dk0 = smem_desc(smem_u32(smem + Ly::kStage0), 16, 1024);
+      const uint64_t dv0 = smem_desc(smem_u32(smem + Ly::kStage0 + Ly::kTileBytes), Ly::kHalfBytes, 1024);
       // S(t) = Q K(t)^T into S buffer t&1 (caller checked K(t) landed and the
       // buffer is free)
       auto issue_s = [&](int t) {
-        const int st = t % kStages;
-        const uint32_t k_base = smem_u32(smem + Ly::kStage0 + st * Ly::kStageBytes);
+        const uint64_t dk = dk0 + static_cast<uint64_t>((t % kStages) * (Ly::kStageBytes >> 4));
+        const uint32_t d = tmem_s0 + (t & 1) * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk & 3) << 5;
-          const uint64_t ad = smem_desc(q_base + (kk >> 2) * (BM * 128) + off, 16, 1024);
-          const uint64_t bd = smem_desc(k_base + (kk >> 2) * Ly::kHalfBytes + off, 16, 1024);
-          mma_bf16_ss(tmem_s0 + (t & 1) * BN, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+          // A = Q from TMEM (16 dims = 8 columns per step), B = K from the ring
+          const uint32_t boff = ((kk >> 2) * Ly::kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_bf16_ts(d, tmem_q + kk * 8, dk + boff, idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[t & 1]);
       };
       // O += P(t) V(t) (caller checked P(t) is in TMEM)
       auto issue_pv = [&](int t) {
         const int st = t % kStages;
-        const uint32_t v_base = smem_u32(smem + Ly::kStage0 + st * Ly::kStageBytes + Ly::kTileBytes);
+        const uint64_t dv = dv0 + static_cast<uint64_t>(st * (Ly::kStageBytes >> 4));
+        const uint32_t pa = tmem_p0 + (t & 1) * 32;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           // A = P from TMEM: 16 keys = 8 columns of bf16 pairs per step
-          const uint64_t bd = smem_desc(v_base + kk * 2048, Ly::kHalfBytes, 1024);
-          mma_bf16_ts(tmem_o, tmem_p0 + (t & 1) * 32 + kk * 8, bd, idesc_o,
-                      (t > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem_o, pa + kk * 8, dv + ((kk * 2048) >> 4), idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&o_done[t & 1]);
         mma_commit(&empty[st]);
@@ -327,35 +355,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------- softmax warps
-    const int r = tid;                 // row of the tile == TMEM lane
+    // Warps 0-7: warp w owns rows 32*(w%4)..+31 (its TMEM lane quarter) and
+    // column half hc = w/4 of every 64-key tile, so two threads share a row
+    // and each scheduler runs two softmax warps.
+    const int r = (warp & 3) * 32 + lane;  // row of the tile == TMEM lane
+    const int hc = warp >> 2;              // which 32 keys of each tile
+    const int sid = hc * 128 + r;          // 0..255
     const int R = w.mtile * BM + r;
     const bool live = R < w.rows;
+    float* xchg = reinterpret_cast<float*>(smem + Ly::kXchg);  // [3 slots][2 halves][128 rows]
     // tree of this sequence into shared memory, validated
-    for (int i = r; i < w.N; i += 128) {
+    for (int i = sid; i < w.N; i += kSoftmaxThreads) {
       const int p = __ldg(a.parent + w.n0 + i);
       par[i] = p;
       if (!(i == 0 ? p == -1 : (p >= 0 && p < i))) misc->bad = 1;
     }
-    // Q tile -> shared memory, 128B-swizzled K-major; padding rows are zero.
+    // Q tile -> TMEM (one row per lane, bf16 pairs; this thread stores the
+    // half hc of its row); padding rows are zero.
     {
-      const uint4* src = nullptr;
+      constexpr int kWords = D / 4;  // 32-bit words per half row
+      uint32_t qw[kWords];
       if (live) {
         const int i = R / g, h = w.kvh * g + R % g;
-        src = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(w.n0 + i) * a.hq + h) * D);
-      }
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.q + (static_cast<size_t>(w.n0 + i) * a.hq + h) * D + hc * (D / 2));
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-        const int half = c >> 3, cc = c & 7;
-        *reinterpret_cast<uint4*>(smem + Ly::kQ + half * (BM * 128) + r * 128 +
-                                  ((cc ^ (r & 7)) << 4)) = v;
+        for (int c = 0; c < kWords / 4; ++c) {
+          const uint4 v = __ldg(src + c);
+          qw[4 * c] = v.x;
+          qw[4 * c + 1] = v.y;
+          qw[4 * c + 2] = v.z;
+          qw[4 * c + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kWords; ++c) qw[c] = 0u;
       }
+      if constexpr (kWords == 32) {
+        tmem_st32(tmem_q + hc * 32 + lane_off_q(warp), qw);
+      } else {
+        tmem_st16(tmem_q + hc * 16 + lane_off_q(warp), qw);
+      }
+      tmem_st_wait();
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps only
+    softmax_group_sync();
     const bool tree_ok = misc->bad == 0;
-    if (!tree_ok && r == 0) record_status(a.status, w.b, kBadTree);
+    if (!tree_ok && sid == 0) record_status(a.status, w.b, kBadTree);
     // ancestor-or-self bitmask of the tile's nodes (node tiles only)
-    if (w.last_split) {
+    if (w.last_split && hc == 0) {
       const int i = node_lo + r;
       uint32_t* row = anc + r * kMaxAncWords;
 #pragma unroll
@@ -364,59 +411,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = i; k >= 0; k = par[k]) row[k >> 5] |= 1u << (k & 31);
       }
     }
-    fence_proxy_async_smem();  // Q written by the generic proxy, read by the MMA
+    tc_fence_before();  // Q is in TMEM before the MMA warp is released
     mbar_arrive(q_ready);
-    asm volatile("bar.sync 1, 128;" ::: "memory");  // ancestor rows are read across threads
+    softmax_group_sync();      // ancestor rows are read across threads
     const int i_node = live ? R / g : 0;  // local node of this row
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t* my_anc = anc + (i_node - node_lo) * kMaxAncWords;
-    float m_run = -INFINITY;  // reference max (log2 units)
-    float l_run = 0.0f;
+    float m_run = -INFINITY;  // reference max (log2 units), shared by the pair
+    float l_run = 0.0f;       // this thread's half of the row sum
     bool ok = true;
+    // Every softmax warp passes the same sequence of named barriers (one per
+    // tile): after a failed (timed-out) wait a warp keeps looping but skips
+    // the work, so that its partner warp can never block on it.
     for (int t = 0; t < w.T; ++t) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[64];
-      {
-        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-        tmem_ld32(tmem_s0 + (t & 1) * BN + lane_off, lo);
-        tmem_ld32(tmem_s0 + (t & 1) * BN + 32 + lane_off, hi);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag));
+      uint32_t sr[32];
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(tmem_s0 + (t & 1) * BN + hc * 32 + lane_off, sr);
         tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&s_free[t & 1]);  // S buffer t&1 may now take S(t+2)
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sr[c] = 0u;
       }
-      tc_fence_before();
-      mbar_arrive(&s_free[t & 1]);  // S buffer t&1 may now take S(t+2)
-      // scale + mask (scores stay unscaled here; the scale is folded into
-      // the exponent below), then the row max as a tree of fmaxf
-      float x[64];
+      // mask (scores stay unscaled; the scale is folded into the exponent)
+      float x[32];
       int valid_keys = BN;
       if (t < w.n_prefix_tiles) {
         valid_keys = min(BN, w.k_end - (w.k_begin + t * BN));
+        if (valid_keys == BN) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = c < valid_keys ? __uint_as_float(sr[c]) : -INFINITY;
+          for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(sr[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) x[c] = hc * 32 + c < valid_keys ? __uint_as_float(sr[c]) : -INFINITY;
+        }
       } else {
-        const int j0 = (t - w.n_prefix_tiles) * BN;
-        const uint32_t w0 = live ? my_anc[j0 >> 5] : 0u;
-        const uint32_t w1 = live ? my_anc[(j0 >> 5) + 1] : 0u;
+        const int j0 = (t - w.n_prefix_tiles) * BN + hc * 32;
+        const uint32_t bits = live ? my_anc[j0 >> 5] : 0u;
         const int nvalid = w.N - j0;  // node columns past the tree are masked
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const uint32_t bit = c < 32 ? (w0 >> c) & 1u : (w1 >> (c - 32)) & 1u;
-          x[c] = (bit && c < nvalid) ? __uint_as_float(sr[c]) : -INFINITY;
-        }
+        for (int c = 0; c < 32; ++c)
+          x[c] = (((bits >> c) & 1u) && c < nvalid) ? __uint_as_float(sr[c]) : -INFINITY;
       }
-      float mx[32];
+      float mx[16];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) mx[c] = fmaxf(x[c], x[c + 32]);
+      for (int c = 0; c < 16; ++c) mx[c] = fmaxf(x[c], x[c + 16]);
 #pragma unroll
-      for (int h = 16; h >= 1; h >>= 1)
+      for (int h = 8; h >= 1; h >>= 1)
 #pragma unroll
         for (int c = 0; c < h; ++c) mx[c] = fmaxf(mx[c], mx[c + h]);
-      const float tmax = mx[0] * a.scale_log2;  // -inf stays -inf
-      // online softmax with a lazily rescaled reference max
+      // the row max of both halves (exchange slot t&1, so that the next
+      // tile's write cannot overtake the partner's read)
+      xchg[((t & 1) * 2 + hc) * 128 + r] = mx[0];
+      softmax_pair_sync();
+      if (!ok) continue;  // skip the work, keep the barrier sequence
+      const float tmax = fmaxf(mx[0], xchg[((t & 1) * 2 + (hc ^ 1)) * 128 + r]) * a.scale_log2;
+      // online softmax with a lazily rescaled reference max (same decision
+      // in both threads of a row)
       float alpha = 1.0f;
       bool rescale = false;
       if (tmax != -INFINITY) {
@@ -429,15 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
-        // O must be stable: wait for PV(t-1)
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
+        // O must be stable: wait for PV(t-1); this thread rescales its half of O
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag));
+        if (!ok) continue;
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = hc * (D / 2); c0 < (hc + 1) * (D / 2); c0 += 32) {
           uint32_t o[32];
           tmem_ld32(tmem_o + c0 + lane_off, o);
           tmem_ld_wait();
@@ -450,40 +502,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_run *= alpha;
       // P buffer (t & 1) is free once PV(t-2) has completed
       if (t >= 2) {
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&o_done[t & 1], ((t - 2) >> 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t & 1], ((t - 2) >> 1) & 1, abort_flag));
+        if (!ok) continue;
       }
       const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
-      uint32_t pk[32];  // P row as bf16 pairs: column c holds keys 2c (low) and 2c+1
-      float ls[8];
+      uint32_t pk[16];  // bf16 pairs: column c of this half holds keys 2c (low), 2c+1
+      float ls[4];
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int c4 = 0; c4 < 4; ++c4) {
         float part = 0.0f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           // p = 2^(s * scale * log2(e) - m); masked scores are -inf -> 0
-          const float p0 = ex2_approx(fmaf(x[c8 * 8 + 2 * k], a.scale_log2, -mref));
-          const float p1 = ex2_approx(fmaf(x[c8 * 8 + 2 * k + 1], a.scale_log2, -mref));
-          const uint32_t q = pack_bf16x2(p0, p1);
-          pk[c8 * 4 + k] = q;
-          // l accumulates the bf16-rounded weights that the P.V product uses
-          part += __uint_as_float(q << 16) + __uint_as_float(q & 0xFFFF0000u);
+          const float p0 = ex2_approx(fmaf(x[c4 * 8 + 2 * k], a.scale_log2, -mref));
+          const float p1 = ex2_approx(fmaf(x[c4 * 8 + 2 * k + 1], a.scale_log2, -mref));
+          pk[c4 * 4 + k] = pack_bf16x2(p0, p1);
+          part += p0 + p1;
         }
-        ls[c8] = part;
+        ls[c4] = part;
       }
-      tmem_st32(tmem_p0 + (t & 1) * 32 + lane_off, pk);
-      const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      l_run += lsum;
+      tmem_st16(tmem_p0 + (t & 1) * 32 + hc * 16 + lane_off, pk);
+      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       // keys past the prefix end in this tile: clear their V rows (page tails
       // may hold stale data; P is 0 there but 0 * NaN would poison O)
       if (valid_keys < BN) {
         const int st = t % kStages;
         mbar_wait(&full[st], (t / kStages) & 1);  // acquire the TMA writes
         uint8_t* vt = smem + Ly::kStage0 + st * Ly::kStageBytes + Ly::kTileBytes;
-        for (int idx = r; idx < (BN - valid_keys) * Ly::kHalves; idx += 128) {
+        for (int idx = sid; idx < (BN - valid_keys) * Ly::kHalves; idx += kSoftmaxThreads) {
           const int row = valid_keys + idx / Ly::kHalves, h = idx % Ly::kHalves;
           uint4* p = reinterpret_cast<uint4*>(vt + h * Ly::kHalfBytes + row * 128);
 #pragma unroll
@@ -495,6 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&p_full[t & 1]);
     }
+    // the row sum of both halves (slot 2: the max slots may still be read)
+    xchg[(2 * 2 + hc) * 128 + r] = l_run;
+    softmax_pair_sync();
+    const float l_row = l_run + xchg[(2 * 2 + (hc ^ 1)) * 128 + r];
     if (!ok) {
       record_status(a.status, w.b, kDeviceTimeout);
       misc->abort = 1;
@@ -503,11 +553,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // ------------------------------------------------------------ epilogue
       const bool final_out = (w.nsplit == 1);
-      const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+      const float inv_l = (l_row > 0.0f) ? 1.0f / l_row : 0.0f;
       const size_t unit = (static_cast<size_t>(w.b) * a.hkv + w.kvh) * a.mtiles_max + w.mtile;
       const size_t prow_idx = (unit * a.max_splits + w.split) * BM + r;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = hc * (D / 2); c0 < (hc + 1) * (D / 2); c0 += 32) {
         uint32_t o[32];
         tmem_ld32(tmem_o + c0 + lane_off, o);
         tmem_ld_wait();
@@ -532,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
         }
       }
-      if (live && !final_out) a.ws_ml[prow_idx] = make_float2(m_run, l_run);
+      if (live && !final_out && hc == 0) a.ws_ml[prow_idx] = make_float2(m_run, l_row);
     } else if (w.T > 0) {
       record_status(a.status, w.b, kDeviceTimeout);
       misc->abort = 1;
@@ -545,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a malformed tree or block id: the only writer of these rows writes zeros
   // (each row by the thread that wrote it in the epilogue, so zeros win)
   if (misc->bad && w.nsplit == 1 && warp < 4) zero_rows<D>(a, w, tid);
-  if (warp == 5) tmem_dealloc(tmem, Ly::kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, Ly::kTmemCols);
 }
 
 // Combines the split partials: one warp per packed output row,
