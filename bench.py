@@ -319,8 +319,14 @@ def main():
             acc(d)
         stream.synchronize()
         assert int(st_attn.max()) == 0 and int(acc_out["status"].max()) == 0, "device status"
-        graph_a = graph_b = None
+        graph_a = graph_b = graph_step = None
         if not args.no_graph:
+            # the step (attention then accept) as one graph; and each call as
+            # its own graph for the per-kernel breakdown
+            graph_step = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_step, stream=stream):
+                attn(d)
+                acc(d)
             graph_a = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph_a, stream=stream):
                 attn(d)
@@ -328,9 +334,17 @@ def main():
             with torch.cuda.graph(graph_b, stream=stream):
                 acc(d)
             for _ in range(max(3, args.warmup)):
+                graph_step.replay()
                 graph_a.replay()
                 graph_b.replay()
             stream.synchronize()
+
+    def run_step():
+        if graph_step is not None:
+            graph_step.replay()
+        else:
+            attn(d)
+            acc(d)
 
     def run_attn():
         graph_a.replay() if graph_a is not None else attn(d)
@@ -338,8 +352,8 @@ def main():
     def run_acc():
         graph_b.replay() if graph_b is not None else acc(d)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -349,22 +363,35 @@ def main():
     with torch.cuda.stream(stream):
         for k in range(args.steps):
             flush.fill_(k & 0xFF)  # evicts the inputs from L2 (outside the events)
-            e0, e1, e2 = ev[k]
+            e0, e1 = ev[k]
             e0.record(stream)
-            run_attn()
+            run_step()
             e1.record(stream)
-            run_acc()
-            e2.record(stream)
     stream.synchronize()
     wall = time.perf_counter() - t_wall0
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    attn_ms = [a.elapsed_time(b) for a, b, _ in ev]
-    acc_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms = [a.elapsed_time(b) for a, b in ev]
     total_s = sum(step_ms) / 1e3
+    # per-call breakdown (same flushing), for the roofline of each kernel
+    nb = max(3, min(args.steps, 100))
+    evb = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(nb)]
+    with torch.cuda.stream(stream):
+        for k in range(nb):
+            e0, e1, e2, e3 = evb[k]
+            flush.fill_(k & 0xFF)
+            e0.record(stream)
+            run_attn()
+            e1.record(stream)
+            flush.fill_(k & 0xFF)
+            e2.record(stream)
+            run_acc()
+            e3.record(stream)
+    stream.synchronize()
+    attn_ms = [e0.elapsed_time(e1) for e0, e1, _, _ in evb]
+    acc_ms = [e2.elapsed_time(e3) for _, _, e2, e3 in evb]
     if world > 1:
         t = torch.tensor([total_s], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -418,7 +445,7 @@ def main():
         "data": "synthetic (seeded; shapes of the pages' workloads, no datasets or weights)",
         "config": dict(workload_desc(cfg, case), accept_input=args.mode,
                        l2="flushed between timed steps (512 MiB write)",
-                       launch="CUDA graph replay" if graph_a is not None else "eager",
+                       launch="one CUDA graph per step" if graph_step is not None else "eager",
                        parallelism="replicas" if world > 1 else "single GPU"),
         "roofline": {"kernel": "tree_attn_kernel (+ status memset"
                                + (" + split merge)" if ws_bytes > 0 else ")"),

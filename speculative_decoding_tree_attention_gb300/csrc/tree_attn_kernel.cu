@@ -43,8 +43,7 @@ namespace tv {
 namespace {
 
 constexpr int BM = 128;           // packed query rows per CTA
-constexpr int BN = 64;            // keys per tile
-constexpr int kStages = 6;        // K/V ring depth (64-key tiles)
+constexpr int BN = 128;           // keys per tile
 constexpr int kSoftmaxThreads = 256;  // warps 0-7
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -52,11 +51,18 @@ constexpr int kThreads = 320;     // 8 softmax warps + TMA warp + MMA warp
 constexpr int kMaxAncWords = 16;  // 512-node trees
 constexpr float kRescaleLog2 = 8.0f;
 
+// Shared-memory layout of a K or V tile: 16 groups of 8 keys; a group holds
+// the 64-column halves of its 8 rows one after the other, each half an
+// 8 x 128-byte swizzle atom: [group][half][row][128 B].  A 16-token page is
+// two consecutive groups, so one TMA box brings a whole page, and for a fixed
+// half the 8-row groups sit at a uniform stride (kGroupBytes), which is what
+// the MMA descriptors need (K-major for K, MN-major for V).
 template <int D>
 struct Layout {
   static constexpr int kHalves = D / 64;
-  static constexpr int kTileBytes = BN * D * 2;  // one K or V tile
-  static constexpr int kHalfBytes = BN * 128;    // one 64-column half of a tile
+  static constexpr int kStages = D == 128 ? 3 : 6;     // K/V ring depth (128-key tiles)
+  static constexpr int kGroupBytes = kHalves * 1024;   // 8 keys, all columns
+  static constexpr int kTileBytes = BN * D * 2;        // one K or V tile (16 groups)
   static constexpr int kStage0 = 0;
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kAnc = kStage0 + kStages * kStageBytes;
@@ -72,8 +78,8 @@ struct Layout {
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 64;
   static constexpr int kAlloc = kTotal + 1024;  // slack for 1024-byte alignment
-  // TMEM columns: S[2] at 0 and 64 (fp32), O at 128 (D columns), P[2] at
-  // 256 and 288 (bf16 pairs, 32 columns each), Q at 320 (bf16 pairs, D/2)
+  // TMEM columns: S[2] at 0 and 128 (fp32), O at 256 (D columns), P at 384
+  // (bf16 pairs, 64 columns), Q at 448 (bf16 pairs, D/2 columns)
   static constexpr int kTmemCols = 512;
 };
 
@@ -129,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kBar);
+  constexpr int kStages = Ly::kStages;
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* s_full = bars + 2 * kStages;
@@ -204,17 +211,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp) tmem_dealloc(tmem, Ly::kTmemCols);
     return;
   }
-  const uint32_t tmem_s0 = tmem;        // S buffers at columns 0 and 64
-  const uint32_t tmem_o = tmem + 128;   // O accumulator at columns 128 .. 128+D-1
-  const uint32_t tmem_p0 = tmem + 256;  // P buffers (A operand of P.V) at 256 and 288
-  const uint32_t tmem_q = tmem + 320;   // Q tile (A operand of Q.K^T)
+  const uint32_t tmem_s0 = tmem;        // S buffers at columns 0 and 128
+  const uint32_t tmem_o = tmem + 256;   // O accumulator at columns 256 .. 256+D-1
+  const uint32_t tmem_p = tmem + 384;   // P (A operand of P.V)
+  const uint32_t tmem_q = tmem + 448;   // Q tile (A operand of Q.K^T)
   volatile int* abort_flag = &misc->abort;
 
   if (warp == kTmaWarp) {
     // ---------------------------------------------------------- TMA producer
     // The whole warp issues: lane 0 arms the stage's barrier, then each lane
-    // issues one of the tile's boxes (page pg, 64-column half h, K or V), so
-    // a tile's 16 page copies go out in one warp instruction.
+    // issues one box: a prefix tile is 8 pages x {K, V} (one 5-D box per page
+    // and tensor), a node tile is 16 groups of 8 nodes x {K, V}.
     if (lane == 0) {
       prefetch_tmap(&maps.k_pool);
       prefetch_tmap(&maps.v_pool);
@@ -222,17 +229,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&maps.v_nodes);
     }
     constexpr int kPages = BN / 16;
-    constexpr int kBoxes = kPages * Ly::kHalves * 2;  // prefix tile: pages x halves x {K, V}
     constexpr int kPastEnd = INT_MIN;                 // page past the prefix end -> zeros
-    const int my_pg = lane / (Ly::kHalves * 2);
-    const int my_h = (lane / 2) % Ly::kHalves;
     const int my_kv = lane & 1;
-    const bool prefix_lane = lane < kBoxes;
-    const bool node_lane = lane < Ly::kHalves * 2;
-    const int pool_rows = a.num_blocks * a.hkv * 16;
+    const int my_unit = lane >> 1;                    // page (prefix) or 8-node group (nodes)
+    const bool prefix_lane = my_unit < kPages;
+    const int pool_pages = a.num_blocks * a.hkv;
     const int32_t* btab = a.block_table + static_cast<size_t>(w.b) * a.max_blocks_per_seq;
     auto fetch_block = [&](int t) -> int {
-      const int lp = (w.k_begin + t * BN) / 16 + my_pg;
+      const int lp = (w.k_begin + t * BN) / 16 + my_unit;
       return (prefix_lane && lp * 16 < w.k_end) ? __ldg(btab + lp) : kPastEnd;
     };
     int blk_next = w.n_prefix_tiles > 0 ? fetch_block(0) : kPastEnd;
@@ -247,23 +251,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (lane == 0) mbar_arrive_expect_tx(&full[st], 2 * Ly::kTileBytes);
       __syncwarp();
-      uint8_t* dst = smem + Ly::kStage0 + st * Ly::kStageBytes + my_kv * Ly::kTileBytes +
-                     my_h * Ly::kHalfBytes;
+      uint8_t* tile = smem + Ly::kStage0 + st * Ly::kStageBytes + my_kv * Ly::kTileBytes;
       if (t < w.n_prefix_tiles) {
         if (prefix_lane) {
-          int row = pool_rows;  // out of bounds: zero fill
+          int page = pool_pages;  // out of bounds: zero fill
           if (blk >= 0 && blk < a.num_blocks) {
-            row = (blk * a.hkv + w.kvh) * 16;
+            page = blk * a.hkv + w.kvh;
           } else if (blk != kPastEnd && !misc->bad) {  // malformed block id: zeros, reported
             misc->bad = 1;
             record_status(a.status, w.b, kBadTree);
           }
-          tma_load_2d(dst + my_pg * 2048, my_kv ? &maps.v_pool : &maps.k_pool, &full[st],
-                      my_h * 64, row);
+          tma_load_5d(tile + my_unit * 2 * Ly::kGroupBytes, my_kv ? &maps.v_pool : &maps.k_pool,
+                      &full[st], 0, 0, 0, 0, page);
         }
-      } else if (node_lane) {
-        const int node0 = w.n0 + (t - w.n_prefix_tiles) * BN;
-        tma_load_3d(dst, my_kv ? &maps.v_nodes : &maps.k_nodes, &full[st], my_h * 64, w.kvh, node0);
+      } else {
+        const int node0 = w.n0 + (t - w.n_prefix_tiles) * BN + my_unit * 8;
+        tma_load_4d(tile + my_unit * Ly::kGroupBytes, my_kv ? &maps.v_nodes : &maps.k_nodes,
+                    &full[st], 0, node0, 0, w.kvh);
       }
       ++issued;
     }
@@ -279,13 +283,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);
+      constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);  // M=128, N=128: full-rate shape
       constexpr uint32_t idesc_o = idesc_bf16(BM, D, 1);
       bool ok = true;
       // Descriptors are built once; each MMA adds a compile-time offset to the
       // start-address field (16-byte units; shared addresses stay < 2^18).
-      const uint64_t dk0 = smem_desc(smem_u32(smem + Ly::kStage0), 16, 1024);
-      const uint64_t dv0 = smem_desc(smem_u32(smem + Ly::kStage0 + Ly::kTileBytes), Ly::kHalfBytes, 1024);
+      // K (K-major): 8-row groups at kGroupBytes, halves at +1024.
+      // V (MN-major): 8-key groups at kGroupBytes, column halves at +1024.
+      const uint64_t dk0 = smem_desc(smem_u32(smem + Ly::kStage0), 16, Ly::kGroupBytes);
+      const uint64_t dv0 = smem_desc(smem_u32(smem + Ly::kStage0 + Ly::kTileBytes), 1024, Ly::kGroupBytes);
       // S(t) = Q K(t)^T into S buffer t&1 (caller checked K(t) landed and the
       // buffer is free)
       auto issue_s = [&](int t) {
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // A = Q from TMEM (16 dims = 8 columns per step), B = K from the ring
-          const uint32_t boff = ((kk >> 2) * Ly::kHalfBytes + (kk & 3) * 32) >> 4;
+          const uint32_t boff = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
           mma_bf16_ts(d, tmem_q + kk * 8, dk + boff, idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[t & 1]);
@@ -303,11 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int t) {
         const int st = t % kStages;
         const uint64_t dv = dv0 + static_cast<uint64_t>(st * (Ly::kStageBytes >> 4));
-        const uint32_t pa = tmem_p0 + (t & 1) * 32;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          // A = P from TMEM: 16 keys = 8 columns of bf16 pairs per step
-          mma_bf16_ts(tmem_o, pa + kk * 8, dv + ((kk * 2048) >> 4), idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
+          // A = P from TMEM: 16 keys = 8 columns of bf16 pairs = 2 groups of V
+          mma_bf16_ts(tmem_o, tmem_p + kk * 8, dv + ((kk * 2 * Ly::kGroupBytes) >> 4), idesc_o,
+                      (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&o_done[t & 1]);
         mma_commit(&empty[st]);
@@ -425,42 +431,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the work, so that its partner warp can never block on it.
     for (int t = 0; t < w.T; ++t) {
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag));
-      uint32_t sr[32];
+      // this thread's 64 scores of the tile (keys hc*64 .. hc*64+63)
+      float x[64];
       if (ok) {
+        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
+        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
         tc_fence_after();
-        tmem_ld32(tmem_s0 + (t & 1) * BN + hc * 32 + lane_off, sr);
+        tmem_ld32(tmem_s0 + (t & 1) * BN + hc * 64 + lane_off, lo);
+        tmem_ld32(tmem_s0 + (t & 1) * BN + hc * 64 + 32 + lane_off, hi);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&s_free[t & 1]);  // S buffer t&1 may now take S(t+2)
       } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) sr[c] = 0u;
+        for (int c = 0; c < 64; ++c) x[c] = 0.0f;
       }
       // mask (scores stay unscaled; the scale is folded into the exponent)
-      float x[32];
       int valid_keys = BN;
       if (t < w.n_prefix_tiles) {
         valid_keys = min(BN, w.k_end - (w.k_begin + t * BN));
-        if (valid_keys == BN) {
+        if (valid_keys < BN) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(sr[c]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) x[c] = hc * 32 + c < valid_keys ? __uint_as_float(sr[c]) : -INFINITY;
+          for (int c = 0; c < 64; ++c)
+            if (hc * 64 + c >= valid_keys) x[c] = -INFINITY;
         }
       } else {
-        const int j0 = (t - w.n_prefix_tiles) * BN + hc * 32;
-        const uint32_t bits = live ? my_anc[j0 >> 5] : 0u;
+        const int j0 = (t - w.n_prefix_tiles) * BN + hc * 64;
+        const uint32_t b0 = live ? my_anc[j0 >> 5] : 0u;
+        const uint32_t b1 = live ? my_anc[(j0 >> 5) + 1] : 0u;
         const int nvalid = w.N - j0;  // node columns past the tree are masked
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          x[c] = (((bits >> c) & 1u) && c < nvalid) ? __uint_as_float(sr[c]) : -INFINITY;
+        for (int c = 0; c < 64; ++c) {
+          const uint32_t bit = c < 32 ? (b0 >> c) & 1u : (b1 >> (c - 32)) & 1u;
+          if (!bit || c >= nvalid) x[c] = -INFINITY;
+        }
       }
-      float mx[16];
+      float mx[32];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) mx[c] = fmaxf(x[c], x[c + 16]);
+      for (int c = 0; c < 32; ++c) mx[c] = fmaxf(x[c], x[c + 32]);
 #pragma unroll
-      for (int h = 8; h >= 1; h >>= 1)
+      for (int h = 16; h >= 1; h >>= 1)
 #pragma unroll
         for (int c = 0; c < h; ++c) mx[c] = fmaxf(mx[c], mx[c + h]);
       // the row max of both halves (exchange slot t&1, so that the next
@@ -482,12 +492,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
       }
-      if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
-        // O must be stable: wait for PV(t-1); this thread rescales its half of O
+      // P(t-1).V(t-1) must be complete: it reads the single P buffer and
+      // accumulates into O
+      if (t >= 1) {
         ok = __all_sync(0xffffffffu,
                         mbar_wait(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag));
         if (!ok) continue;
         tc_fence_after();
+      }
+      if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
+        // this thread rescales its half of the O row
 #pragma unroll
         for (int c0 = hc * (D / 2); c0 < (hc + 1) * (D / 2); c0 += 32) {
           uint32_t o[32];
@@ -497,32 +511,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
           tmem_st32(tmem_o + c0 + lane_off, o);
         }
-        tmem_st_wait();
       }
       l_run *= alpha;
-      // P buffer (t & 1) is free once PV(t-2) has completed
-      if (t >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t & 1], ((t - 2) >> 1) & 1, abort_flag));
-        if (!ok) continue;
-      }
       const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
-      uint32_t pk[16];  // bf16 pairs: column c of this half holds keys 2c (low), 2c+1
-      float ls[4];
+      uint32_t pk[32];  // bf16 pairs: column c of this half holds keys 2c (low), 2c+1
+      float ls[8];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c8 = 0; c8 < 8; ++c8) {
         float part = 0.0f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           // p = 2^(s * scale * log2(e) - m); masked scores are -inf -> 0
-          const float p0 = ex2_approx(fmaf(x[c4 * 8 + 2 * k], a.scale_log2, -mref));
-          const float p1 = ex2_approx(fmaf(x[c4 * 8 + 2 * k + 1], a.scale_log2, -mref));
-          pk[c4 * 4 + k] = pack_bf16x2(p0, p1);
+          const float p0 = ex2_approx(fmaf(x[c8 * 8 + 2 * k], a.scale_log2, -mref));
+          const float p1 = ex2_approx(fmaf(x[c8 * 8 + 2 * k + 1], a.scale_log2, -mref));
+          pk[c8 * 4 + k] = pack_bf16x2(p0, p1);
           part += p0 + p1;
         }
-        ls[c4] = part;
+        ls[c8] = part;
       }
-      tmem_st16(tmem_p0 + (t & 1) * 32 + hc * 16 + lane_off, pk);
-      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tmem_st32(tmem_p + hc * 32 + lane_off, pk);
+      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       // keys past the prefix end in this tile: clear their V rows (page tails
       // may hold stale data; P is 0 there but 0 * NaN would poison O)
       if (valid_keys < BN) {
@@ -531,7 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* vt = smem + Ly::kStage0 + st * Ly::kStageBytes + Ly::kTileBytes;
         for (int idx = sid; idx < (BN - valid_keys) * Ly::kHalves; idx += kSoftmaxThreads) {
           const int row = valid_keys + idx / Ly::kHalves, h = idx % Ly::kHalves;
-          uint4* p = reinterpret_cast<uint4*>(vt + h * Ly::kHalfBytes + row * 128);
+          uint4* p = reinterpret_cast<uint4*>(vt + (row >> 3) * Ly::kGroupBytes + h * 1024 +
+                                              (row & 7) * 128);
 #pragma unroll
           for (int k = 0; k < 8; ++k) p[k] = make_uint4(0, 0, 0, 0);
         }

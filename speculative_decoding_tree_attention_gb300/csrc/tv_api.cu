@@ -54,7 +54,8 @@ struct AttnPlan {
 
 // Launch plan: 128-row tiles of packed (node, head) rows per (sequence, KV
 // head); the prefix is split so that the grid covers about two waves of
-// SMs, with at least 512 keys per split (partials cost 0.5 KB per row).
+// SMs, with at least 512 keys per split (partials cost 0.5 KB per row); splits
+// are whole 128-key tiles.
 bool plan_attention(const tv_attn_params* p, AttnPlan* out) {
   if (!p) return false;
   if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1) return false;
@@ -75,7 +76,7 @@ bool plan_attention(const tv_attn_params* p, AttnPlan* out) {
   long splits = 1;
   if (p->max_prefix_len > 0 && base < target) splits = (target + base - 1) / base;
   long chunk = (p->max_prefix_len + splits - 1) / splits;
-  chunk = ((chunk + 63) / 64) * 64;
+  chunk = ((chunk + 127) / 128) * 128;  // whole 128-key tiles
   if (chunk < 512) chunk = 512;
   pl.chunk = static_cast<int>(chunk);
   pl.max_splits = p->max_prefix_len > 0 ? static_cast<int>((p->max_prefix_len + chunk - 1) / chunk) : 1;
@@ -91,7 +92,7 @@ bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
             const cuuint64_t* strides_bytes, const cuuint32_t* box) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
             strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -144,22 +145,30 @@ int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
   const int D = p->head_dim, Hkv = p->num_kv_heads;
   tv::AttnMaps maps;
   std::memset(&maps, 0, sizeof maps);
+  // Paged pool as a 5-D tensor so that one box is one 16-token page of one
+  // KV head, landing in shared memory as [8-row group][64-column half][8 rows]
+  // [128 B]: dims (64 columns, 8 rows, halves, 2 row groups, pages), box
+  // (64, 8, halves, 2, 1).
+  const int halves = D / 64;
   {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D),
-                                static_cast<cuuint64_t>(p->num_blocks) * Hkv * 16};
-    const cuuint64_t str[1] = {static_cast<cuuint64_t>(D) * 2};
-    const cuuint32_t box[2] = {64, 16};
-    if (!encode(&maps.k_pool, k_prefix_blocks, 2, dims, str, box)) return TV_ERR_CUDA;
-    if (!encode(&maps.v_pool, v_prefix_blocks, 2, dims, str, box)) return TV_ERR_CUDA;
+    const cuuint64_t dims[5] = {64, 8, static_cast<cuuint64_t>(halves), 2,
+                                static_cast<cuuint64_t>(p->num_blocks) * Hkv};
+    const cuuint64_t str[4] = {static_cast<cuuint64_t>(D) * 2, 128,
+                               static_cast<cuuint64_t>(D) * 2 * 8, static_cast<cuuint64_t>(D) * 2 * 16};
+    const cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(halves), 2, 1};
+    if (!encode(&maps.k_pool, k_prefix_blocks, 5, dims, str, box)) return TV_ERR_CUDA;
+    if (!encode(&maps.v_pool, v_prefix_blocks, 5, dims, str, box)) return TV_ERR_CUDA;
   }
+  // Tree K/V as a 4-D tensor (64 columns, nodes, halves, KV heads); a box is
+  // 8 consecutive nodes of one head: [half][8 rows][128 B].
   {
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
-                                static_cast<cuuint64_t>(p->total_nodes)};
-    const cuuint64_t str[2] = {static_cast<cuuint64_t>(D) * 2,
-                               static_cast<cuuint64_t>(D) * 2 * Hkv};
-    const cuuint32_t box[3] = {64, 1, 64};
-    if (!encode(&maps.k_nodes, k_nodes, 3, dims, str, box)) return TV_ERR_CUDA;
-    if (!encode(&maps.v_nodes, v_nodes, 3, dims, str, box)) return TV_ERR_CUDA;
+    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(p->total_nodes),
+                                static_cast<cuuint64_t>(halves), static_cast<cuuint64_t>(Hkv)};
+    const cuuint64_t str[3] = {static_cast<cuuint64_t>(D) * 2 * Hkv, 128,
+                               static_cast<cuuint64_t>(D) * 2};
+    const cuuint32_t box[4] = {64, 8, static_cast<cuuint32_t>(halves), 1};
+    if (!encode(&maps.k_nodes, k_nodes, 4, dims, str, box)) return TV_ERR_CUDA;
+    if (!encode(&maps.v_nodes, v_nodes, 4, dims, str, box)) return TV_ERR_CUDA;
   }
 
   tv::AttnArgs a;

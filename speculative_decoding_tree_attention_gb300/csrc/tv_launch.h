@@ -50,14 +50,14 @@ struct AttnArgs {
   int32_t max_blocks_per_seq, num_blocks, max_nodes, max_prefix_len, total_nodes;
   int32_t mtiles_max;         // ceil(max_nodes * group / 128)
   int32_t max_splits;         // splits of the longest prefix
-  int32_t chunk;              // prefix keys per split (multiple of 64)
+  int32_t chunk;              // prefix keys per split (multiple of 128)
   float scale_log2;           // softmax scale * log2(e)
 };
 
 struct AttnMaps {
-  CUtensorMap k_pool;   // 2D (D, num_blocks*Hkv*16), box (64, 16), 128B swizzle
+  CUtensorMap k_pool;   // 5D (64, 8 rows, halves, 2 groups, pages), box = one page, 128B swizzle
   CUtensorMap v_pool;
-  CUtensorMap k_nodes;  // 3D (D, Hkv, total_nodes), box (64, 1, 64), 128B swizzle
+  CUtensorMap k_nodes;  // 4D (64, nodes, halves, Hkv heads), box = 8 nodes of one head
   CUtensorMap v_nodes;
 };
 
