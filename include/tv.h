@@ -94,8 +94,11 @@ typedef struct {
   float softmax_scale;        /* 0 => 1/sqrt(D)                                */
 } tv_attn_params;             /* host struct */
 
-/* Bytes of device workspace tv_tree_attention needs for these parameters
- * (split-KV partial results).  0 on invalid parameters. */
+/* Bytes of device workspace tv_tree_attention needs for these parameters.
+ * This version needs none and returns 0: when a prefix is split over CTAs
+ * (split-KV), the splits of a tile run as one thread-block cluster and merge
+ * their partial results through distributed shared memory.  The workspace
+ * arguments are kept so that a later plan may use device scratch. */
 size_t tv_tree_attention_workspace_size(const tv_attn_params* params);
 
 /* Layouts (all row-major, contiguous):
@@ -128,15 +131,16 @@ int tv_tree_attention(const tv_attn_params* params, const uint16_t* q_nodes,
  * pages: an engineering addition of this library).
  *
  * Same inputs, outputs, layouts, semantics and status codes as
- * tv_tree_attention, but no workspace argument: the split-KV partial
- * results go to a fixed device array inside the library, so a caller that
+ * tv_tree_attention, but no workspace argument: any device scratch a plan
+ * needs comes from a fixed device array inside the library (the current
+ * plans need none), so a caller that
  * may not call cudaMalloc (code running under stream capture, an operator
  * inside an engine that owns all device memory, a service that forbids
  * allocation after start-up) can still use it.  This entry point allocates
  * nothing and calls no allocating routine.
  *   - The array is TV_NO_ALLOC_SCRATCH_BYTES of device memory; every GPU on
  *     which this entry point runs holds it until the process exits.
- *   - A call whose partial results would not fit
+ *   - A call whose scratch would not fit
  *     (tv_tree_attention_workspace_size(params) > TV_NO_ALLOC_SCRATCH_BYTES)
  *     returns TV_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on each device looks up the array's device address

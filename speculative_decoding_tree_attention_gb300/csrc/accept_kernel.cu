@@ -116,6 +116,9 @@ __device__ bool block_has_child(const int32_t* parent, int n0, int N, int j) {
 // ============================================================ row statistics
 __global__ void __launch_bounds__(kRowThreads)
     accept_rowstats_kernel(const AcceptArgs a, int nchunk, float2* ws_ms, unsigned long long* ws_z) {
+  // the per-tree kernel may start now: its prologue (tree loads and checks)
+  // overlaps this kernel; it waits for our results in griddepcontrol.wait
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long item = blockIdx.x;
   const int g = static_cast<int>(item / nchunk);  // global row
   const int c = static_cast<int>(item % nchunk);
@@ -222,15 +225,18 @@ struct TreeSmem {
   int32_t parent[kMaxN];
   int32_t token[kMaxN];
   float u[kMaxN];
+  float lse[kMaxN];  // log-sum-exp of the target logits row of each node with children
+  float z[kMaxN];    // retained draft mass Z of each node with children
   uint8_t has_child[kMaxN];
   uint32_t acc_bits[kMaxN / 32];
   float red_f0[kTreeWarps], red_f1[kTreeWarps];
   unsigned long long red_u64[kTreeWarps];
   uint32_t red_u32[kTreeWarps];
   int red_i32[kTreeWarps];
-  // cluster exchange slots (read by the other CTAs of the cluster)
+  // cluster exchange slots (read by the other CTAs of the cluster); each is
+  // written once per call, so no barrier is needed before a slot is reused
   float x_m, x_s;
-  unsigned long long x_u64, x_z;
+  unsigned long long x_u64[2], x_z;
   float x_maxv;
   int x_maxi;
   int bad;
@@ -246,21 +252,6 @@ __device__ unsigned long long block_sum_u64(TreeSmem& sm, unsigned long long x) 
   unsigned long long t = 0;
   for (int i = 0; i < kTreeWarps; ++i) t += sm.red_u64[i];
   return t;
-}
-// exclusive prefix over threads in thread order (every thread gets its own)
-__device__ unsigned long long block_exclusive_u64(TreeSmem& sm, unsigned long long x) {
-  unsigned long long inc = x;
-  const int l = threadIdx.x & 31, w = threadIdx.x >> 5;
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
-    if (l >= o) inc += y;
-  }
-  __syncthreads();
-  if (l == 31) sm.red_u64[w] = inc;
-  __syncthreads();
-  unsigned long long excl = inc - x;
-  for (int k = 0; k < w; ++k) excl += sm.red_u64[k];
-  return excl;
 }
 __device__ float block_max_f32(TreeSmem& sm, float x) {
   for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
@@ -301,20 +292,6 @@ __device__ uint32_t block_max_u32(TreeSmem& sm, uint32_t x) {
   for (int i = 0; i < kTreeWarps; ++i) t = max(t, sm.red_u32[i]);
   return t;
 }
-__device__ void block_lse(TreeSmem& sm, float& m, float& s) {
-  for (int o = 16; o; o >>= 1)
-    lse_combine(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
-  const int w = threadIdx.x >> 5;
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) {
-    sm.red_f0[w] = m;
-    sm.red_f1[w] = s;
-  }
-  __syncthreads();
-  m = -INFINITY;
-  s = 0.0f;
-  for (int i = 0; i < kTreeWarps; ++i) lse_combine(m, s, sm.red_f0[i], sm.red_f1[i]);
-}
 // max value, smallest index among equal maxima (NaN ignored)
 __device__ void block_argmax(TreeSmem& sm, float& v, int& idx) {
   for (int o = 16; o; o >>= 1) {
@@ -340,6 +317,29 @@ __device__ void block_argmax(TreeSmem& sm, float& v, int& idx) {
       idx = sm.red_i32[i];
     }
   }
+}
+
+// Cluster-wide sum of a per-CTA slot, and the part of it held by ranks below
+// `rank`: lane c of every warp reads CTA c's slot, so the C reads of
+// distributed shared memory are in flight together.
+template <typename T>
+__device__ __forceinline__ T cluster_sum(cg::cluster_group& cluster, const T* slot, int C, int rank,
+                                         T* below) {
+  const int lane = threadIdx.x & 31;
+  T v = lane < C ? *cluster.map_shared_rank(slot, lane) : T(0);
+  T b = lane < rank ? v : T(0);
+  for (int o = 16; o; o >>= 1) {
+    v += __shfl_xor_sync(0xffffffffu, v, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
+  if (below) *below = b;
+  return v;
+}
+__device__ __forceinline__ float cluster_max(cg::cluster_group& cluster, const float* slot, int C) {
+  const int lane = threadIdx.x & 31;
+  float v = lane < C ? *cluster.map_shared_rank(slot, lane) : -INFINITY;
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
 }
 
 __global__ void __launch_bounds__(kTreeThreads, 1)
@@ -417,6 +417,16 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     return z_from_sum(S);
   };
 
+  // LSE / Z of every row with children, once (thread j: row j)
+  if (stats) {
+    const int j = tid;  // kTreeThreads == kMaxN
+    if (j < N && sm.has_child[j]) {
+      if (logits) sm.lse[j] = row_lse(j);
+      if (masked) sm.z[j] = row_z(j);
+    }
+    __syncthreads();
+  }
+
   // ---------------------------------------------------------------- tests
   float my_p = 0.0f, my_q = 0.0f;
   {
@@ -428,10 +438,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
       const size_t row = static_cast<size_t>(n0 + j) * V;
       float p = __ldg(a.target + row + x);
       float q = __ldg(a.draft + row + x);
-      if (logits) p = expf(p - row_lse(j));
+      if (logits) p = expf(p - sm.lse[j]);
       if (masked) {
         if ((__ldg(a.mask + static_cast<size_t>(n0 + j) * W + (x >> 5)) >> (x & 31)) & 1u) {
-          const float z = row_z(j);
+          const float z = sm.z[j];
           p = __fdiv_rn(p, z);
           q = __fdiv_rn(q, z);
         } else {
@@ -532,8 +542,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
   float lse = 0.0f, z = 1.0f;
   if (stats) {
     if (sm.has_child[cut]) {
-      if (logits) lse = row_lse(cut);
-      if (masked) z = row_z(cut);
+      if (logits) lse = sm.lse[cut];
+      if (masked) z = sm.z[cut];
     } else {
       float m = -INFINITY;
       unsigned long long zs = 0;
@@ -548,13 +558,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
         sm.x_z = zs;
       }
       cluster.sync();
-      float M = -INFINITY;
-      unsigned long long Z = 0;
-      for (int c = 0; c < C; ++c) {
-        const TreeSmem* o = cluster.map_shared_rank(&sm, c);
-        M = fmaxf(M, o->x_m);
-        Z += o->x_z;
-      }
+      const float M = cluster_max(cluster, &sm.x_m, C);
+      const unsigned long long Z = cluster_sum(cluster, &sm.x_z, C, rank,
+                                               static_cast<unsigned long long*>(nullptr));
       z = z_from_sum(Z);
       if (logits) {
         float ssum = 0.0f;
@@ -563,11 +569,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
         ssum = block_sum_f32(sm, ssum);
         if (tid == 0) sm.x_s = ssum;
         cluster.sync();
-        float Ssum = 0.0f;
-        for (int c = 0; c < C; ++c) Ssum += cluster.map_shared_rank(&sm, c)->x_s;
+        // the same reduction order in every CTA: the same value everywhere
+        const float Ssum = cluster_sum(cluster, &sm.x_s, C, rank, static_cast<float*>(nullptr));
         lse = M + logf(Ssum);
       }
-      cluster.sync();  // every CTA has read the slots before they are reused
     }
   }
   // p~ and q~ of the cut row in place (0 off the retained set)
@@ -600,15 +605,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     __syncthreads();
     unsigned long long part = 0;
     for (int k = 0; k < kTreeWarps; ++k) part += sm.red_u64[k];
-    if (tid == 0) sm.x_u64 = part;
+    if (tid == 0) sm.x_u64[pass] = part;
     cluster.sync();
-    unsigned long long S = 0, before = 0;
-    for (int c = 0; c < C; ++c) {
-      const unsigned long long sc = cluster.map_shared_rank(&sm, c)->x_u64;
-      if (c < rank) before += sc;
-      S += sc;
-    }
-    cluster.sync();  // the slots may be reused after this point
+    unsigned long long before = 0;
+    const unsigned long long S = cluster_sum(cluster, &sm.x_u64[pass], C, rank, &before);
     if (S == 0) continue;  // the same decision in every CTA
     drawn = true;
     const unsigned long long t = scaled_draw(u0, S);

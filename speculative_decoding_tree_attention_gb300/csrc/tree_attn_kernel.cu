@@ -15,26 +15,30 @@
 // GB300 design.  One CTA computes a 128-row tile of packed query rows of one
 // (sequence, KV head): row R = node * g + head-in-group, so every tree node
 // and every query head of a GQA group share each K/V tile that is staged in
-// shared memory.  The CTA walks its key range in 64-key tiles:
-//   warp 4  (TMA)      loads K and V tiles into a 4-stage ring: four 16-token
-//                      pages per tile through the block table (2D tensor map
-//                      over the pool), or 64 tree nodes (3D tensor map);
+// shared memory.  The CTA walks its key range in 128-key tiles:
+//   warp 8  (TMA)      loads K and V tiles into two shared-memory rings: one 5-D
+//                      box per 16-token page through the block table (eight
+//                      pages per tile and tensor), or 16 boxes of 8 tree nodes;
 //                      pages past the sequence load as zeros (out of bounds).
-//   warp 5  (MMA)      one thread issues tcgen05.mma: S = Q K^T into a
-//                      double-buffered TMEM tile (128 x 64 fp32), and
-//                      O += P V into a TMEM accumulator (128 x D fp32) with
-//                      P read from TMEM as the A operand.
-//   warps 0-3          one thread per row: tcgen05.ld of S, the tree mask
-//                      from a per-node ancestor bitmask (shared memory), fp32
-//                      online softmax in base 2, rescale of O in TMEM only
-//                      when the running max grows by more than 2^8, and P as
-//                      bf16 pairs stored back to a double-buffered TMEM tile.
-// Q, K and V use the 128-byte swizzle that TMA writes, so the MMA reads them
-// straight from the ring; P never touches shared memory.  Long prefixes are split over CTAs (split-KV):
-// each split writes (O, m, l) in fp32 and a merge kernel combines them.
-// Every wait on an mbarrier is bounded; on expiry the CTA reports
-// TV_ERR_DEVICE_TIMEOUT for its sequence, drains its copies and returns.
+//   warps 9, 10 (MMA)  one thread each issues tcgen05.mma: warp 9 S = Q K^T
+//                      into a double-buffered TMEM tile (128 x 128 fp32) with
+//                      Q read from TMEM, warp 10 O += P V into a TMEM
+//                      accumulator (128 x D fp32) with P read from TMEM.
+//   warps 0-7          two threads per row (one per 64-key half): tcgen05.ld
+//                      of S, the tree mask from a per-node ancestor bitmask
+//                      (shared memory), fp32 online softmax in base 2, rescale
+//                      of O in TMEM only when the running max grows by more
+//                      than 2^8, and P as bf16 pairs stored over the S buffer
+//                      it came from.
+// K and V use the 128-byte swizzle that TMA writes, so the MMA reads them
+// straight from the ring; Q and P never touch shared memory.  Long prefixes
+// are split over CTAs (split-KV): each split writes (O, m, l) in fp32 and the
+// last split of a tile to finish combines them.  Every wait on an mbarrier is bounded; on expiry
+// the CTA reports TV_ERR_DEVICE_TIMEOUT for its sequence, drains its copies
+// and returns.
 #include <climits>
+
+#include <cooperative_groups.h>
 
 #include "tv_device.cuh"
 #include "tv_launch.h"
@@ -46,9 +50,11 @@ constexpr int BM = 128;           // packed query rows per CTA
 constexpr int BN = 128;           // keys per tile
 constexpr int kSoftmaxThreads = 256;  // warps 0-7
 constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;     // 8 softmax warps + TMA warp + MMA warp
+constexpr int kMmaWarp = 9;       // issues S = Q K^T; owns the TMEM allocation
+constexpr int kPvWarp = 10;       // issues O += P V
+constexpr int kThreads = 352;     // 8 softmax warps + TMA warp + 2 MMA warps
 constexpr int kMaxAncWords = 16;  // 512-node trees
+constexpr int kAncStride = kMaxAncWords + 1;  // odd word stride: rows of a warp hit distinct banks
 constexpr float kRescaleLog2 = 8.0f;
 
 // Shared-memory layout of a K or V tile: 16 groups of 8 keys; a group holds
@@ -60,26 +66,28 @@ constexpr float kRescaleLog2 = 8.0f;
 template <int D>
 struct Layout {
   static constexpr int kHalves = D / 64;
-  static constexpr int kStages = D == 128 ? 3 : 6;     // K/V ring depth (128-key tiles)
+  static constexpr int kStages = D == 128 ? 3 : 6;     // depth of the K ring and of the V ring
   static constexpr int kGroupBytes = kHalves * 1024;   // 8 keys, all columns
   static constexpr int kTileBytes = BN * D * 2;        // one K or V tile (16 groups)
-  static constexpr int kStage0 = 0;
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kAnc = kStage0 + kStages * kStageBytes;
-  static constexpr int kAncBytes = BM * kMaxAncWords * 4;
+  static constexpr int kKRing = 0;                     // kStages K tiles
+  static constexpr int kVRing = kKRing + kStages * kTileBytes;  // kStages V tiles
+  static constexpr int kAnc = kVRing + kStages * kTileBytes;
+  static constexpr int kAncBytes = BM * kAncStride * 4;
   static constexpr int kParent = kAnc + kAncBytes;
   static constexpr int kParentBytes = 512 * 4;
   static constexpr int kXchg = kParent + kParentBytes;  // row max / sum exchange
   static constexpr int kXchgBytes = 3 * 2 * BM * 4;  // slots 0, 1: per-tile max; 2: row sum
   static constexpr int kBar = kXchg + kXchgBytes;
-  // full[kStages], empty[kStages], s_full[2], p_full[2], o_done[2], drain,
-  // q_ready, s_free[2]
-  static constexpr int kNumBars = 2 * kStages + 10;
+  // kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages],
+  // s_full[2], p_full[2], o_done[2], drain[2], q_ready
+  static constexpr int kNumBars = 4 * kStages + 9;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 64;
   static constexpr int kAlloc = kTotal + 1024;  // slack for 1024-byte alignment
-  // TMEM columns: S[2] at 0 and 128 (fp32), O at 256 (D columns), P at 384
-  // (bf16 pairs, 64 columns), Q at 448 (bf16 pairs, D/2 columns)
+  // TMEM columns: S[2] at 0 and 128 (fp32), O at 256 (D columns), Q at 448
+  // (bf16 pairs, D/2 columns).  P(t) overwrites the S buffer it came from:
+  // the thread owning score columns [64h, 64h+64) stores its 64 probabilities
+  // as bf16 pairs in columns [64h, 64h+32) of the same buffer.
   static constexpr int kTmemCols = 512;
 };
 
@@ -104,12 +112,14 @@ __device__ __forceinline__ uint32_t lane_off_q(int warp) {
   return static_cast<uint32_t>((warp & 3) * 32) << 16;
 }
 
-// Named barriers among the 8 softmax warps (ids 1 and 2; 0 is __syncthreads).
+// Named barriers: id 1 joins the 8 softmax warps; ids 2..5 join the two
+// warps (w and w+4) that share a lane quarter, i.e. the two halves of the
+// same 32 rows (0 is __syncthreads).
 __device__ __forceinline__ void softmax_group_sync() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
-__device__ __forceinline__ void softmax_pair_sync() {
-  asm volatile("bar.sync 2, 256;" ::: "memory");
+__device__ __forceinline__ void softmax_pair_sync(int warp) {
+  asm volatile("bar.sync %0, 64;" ::"r"(2 + (warp & 3)) : "memory");
 }
 
 __device__ __forceinline__ void record_status(int32_t* status, int b, int code) {
@@ -127,6 +137,111 @@ __device__ __forceinline__ void zero_rows(const AttnArgs& a, const Work& w, int 
   for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
 }
 
+// Split-KV partials: each split of a tile keeps its raw O rows (fp32, rows
+// padded by 4 floats so that a warp's row stores and reads are free of bank
+// conflicts) and per-row (m, l) in its own shared memory, over the K ring,
+// which is idle once the last S = Q K^T has completed.
+template <int D>
+struct Partial {
+  static constexpr int kStride = D + 4;                 // floats per row
+  static constexpr int kO = 0;                          // offset in the K ring
+  static constexpr int kMl = BM * kStride * 4;
+  static constexpr int kBytes = kMl + BM * 8;
+  static_assert(kBytes <= Layout<D>::kStages * Layout<D>::kTileBytes, "partial exceeds the K ring");
+};
+
+// Combines the NS splits of this tile (the CTAs of the cluster) for the rows
+// r = rank, rank + NS, ... : O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M)
+// l_s, reading every split's partial through distributed shared memory.  A
+// warp takes a group of rows, four columns per lane, and issues all of the
+// group's loads before combining them (16 partial rows in flight per lane).
+// A tile whose sequence was found malformed by any split (`bad` flag of any
+// CTA of the cluster) gets zeros.
+template <int D, int NS>
+__device__ __forceinline__ void merge_rows_ns(const AttnArgs& a, const Work& w, uint8_t* ring,
+                                              const int* bad_flag, int sid, int rank) {
+  namespace cg = cooperative_groups;
+  using Pt = Partial<D>;
+  constexpr int kWarps = kSoftmaxThreads / 32;
+  constexpr int kRows = (16 / NS) > 0 ? 16 / NS : 1;  // rows per warp and group
+  cg::cluster_group cluster = cg::this_cluster();
+  bool bad = false;
+#pragma unroll
+  for (int s = 0; s < NS; ++s) bad |= *cluster.map_shared_rank(bad_flag, s) != 0;
+  const float* o_peer[NS];
+  const float2* ml_peer[NS];
+#pragma unroll
+  for (int s = 0; s < NS; ++s) {
+    o_peer[s] = cluster.map_shared_rank(reinterpret_cast<const float*>(ring + Pt::kO), s);
+    ml_peer[s] = cluster.map_shared_rank(reinterpret_cast<const float2*>(ring + Pt::kMl), s);
+  }
+  const int lane = sid & 31;
+  for (int r0 = rank + (sid >> 5) * NS; r0 < BM; r0 += kRows * kWarps * NS) {
+    int rr[kRows];
+    bool ok_row[kRows];
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      rr[k] = r0 + k * kWarps * NS;
+      ok_row[k] = rr[k] < BM && w.mtile * BM + rr[k] < w.rows;
+    }
+    for (int c = lane * 4; c < D; c += 128) {
+      float2 ml[kRows][NS];
+      float4 v[kRows][NS];
+#pragma unroll
+      for (int k = 0; k < kRows; ++k)
+#pragma unroll
+        for (int s = 0; s < NS; ++s)
+          if (ok_row[k]) {
+            ml[k][s] = ml_peer[s][rr[k]];
+            v[k][s] = *reinterpret_cast<const float4*>(o_peer[s] + rr[k] * Pt::kStride + c);
+          }
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        if (!ok_row[k]) continue;
+        float M = -INFINITY;
+#pragma unroll
+        for (int s = 0; s < NS; ++s) M = fmaxf(M, ml[k][s].x);
+        const float mref = (M == -INFINITY) ? 0.0f : M;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lsum = 0.0f;
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+          const float wgt = (ml[k][s].x == -INFINITY) ? 0.0f : exp2f(ml[k][s].x - mref);
+          lsum += wgt * ml[k][s].y;
+          acc.x += wgt * v[k][s].x;
+          acc.y += wgt * v[k][s].y;
+          acc.z += wgt * v[k][s].z;
+          acc.w += wgt * v[k][s].w;
+        }
+        const float inv = (lsum > 0.0f) ? __frcp_rn(lsum) : 0.0f;
+        uint2 o = make_uint2(0u, 0u);
+        if (!bad) {
+          o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+          o.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        }
+        const int R = w.mtile * BM + rr[k];
+        const int i = R / a.group, h = w.kvh * a.group + R % a.group;
+        *reinterpret_cast<uint2*>(a.out + (static_cast<size_t>(w.n0 + i) * a.hq + h) * D + c) = o;
+      }
+    }
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void merge_rows(const AttnArgs& a, const Work& w, uint8_t* ring,
+                                           const int* bad_flag, int sid, int rank) {
+  switch (w.nsplit) {
+    case 2: merge_rows_ns<D, 2>(a, w, ring, bad_flag, sid, rank); break;
+    case 3: merge_rows_ns<D, 3>(a, w, ring, bad_flag, sid, rank); break;
+    case 4: merge_rows_ns<D, 4>(a, w, ring, bad_flag, sid, rank); break;
+    case 5: merge_rows_ns<D, 5>(a, w, ring, bad_flag, sid, rank); break;
+    case 6: merge_rows_ns<D, 6>(a, w, ring, bad_flag, sid, rank); break;
+    case 7: merge_rows_ns<D, 7>(a, w, ring, bad_flag, sid, rank); break;
+    case 8: merge_rows_ns<D, 8>(a, w, ring, bad_flag, sid, rank); break;
+    default: break;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tree_attn_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps) {
@@ -136,14 +251,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kBar);
   constexpr int kStages = Ly::kStages;
-  uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* s_full = bars + 2 * kStages;
+  uint64_t* kfull = bars;
+  uint64_t* kempty = bars + kStages;
+  uint64_t* vfull = bars + 2 * kStages;
+  uint64_t* vempty = bars + 3 * kStages;
+  uint64_t* s_full = bars + 4 * kStages;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
-  uint64_t* drain = o_done + 2;
-  uint64_t* q_ready = drain + 1;
-  uint64_t* s_free = q_ready + 1;
+  uint64_t* drain = o_done + 2;  // one per MMA-issuing thread
+  uint64_t* q_ready = drain + 2;
   Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
   uint32_t* anc = reinterpret_cast<uint32_t*>(smem + Ly::kAnc);
   int32_t* par = reinterpret_cast<int32_t*>(smem + Ly::kParent);
@@ -153,47 +269,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
 
   // ------------------------------------------------------------ work item
+  // The sequence's extent is loaded first; barrier set-up and the TMEM
+  // allocation below overlap the load latency.
   Work w;
   w.mtile = blockIdx.x;
   w.split = blockIdx.y;
   w.b = blockIdx.z / a.hkv;
   w.kvh = blockIdx.z % a.hkv;
-  w.n0 = a.node_offsets[w.b];
-  w.N = a.node_offsets[w.b + 1] - w.n0;
-  w.L = max(0, a.prefix_lens[w.b]);
-  w.rows = w.N * a.group;
-  w.nsplit = max(1, (w.L + a.chunk - 1) / a.chunk);
-  if (w.N < 1 || w.mtile * BM >= w.rows || w.split >= w.nsplit) return;  // no work here
-  w.last_split = (w.split == w.nsplit - 1);
-  w.k_begin = w.split * a.chunk;
-  w.k_end = min(w.L, w.k_begin + a.chunk);
-  w.n_prefix_tiles = (w.k_end - w.k_begin + BN - 1) / BN;
-  w.n_node_tiles = w.last_split ? (w.N + BN - 1) / BN : 0;
-  w.T = w.n_prefix_tiles + w.n_node_tiles;
-  const int node_lo = (w.mtile * BM) / a.group;
-  const int g = a.group;
+  w.n0 = __ldg(a.node_offsets + w.b);
+  w.N = __ldg(a.node_offsets + w.b + 1) - w.n0;
+  w.L = max(0, __ldg(a.prefix_lens + w.b));
 
   // ------------------------------------------------------------ prologue
-  // Barriers and TMEM first, so that the TMA warp starts streaming K/V at
-  // once; the softmax warps stage Q, validate the tree and build the ancestor
-  // masks meanwhile, and release the first MMA through q_ready.
   if (tid == 0) {
     misc->abort = 0;
-    misc->bad = (w.N > a.max_nodes || w.N > 512 || w.L > a.max_prefix_len || w.n0 < 0 ||
-                 w.n0 + w.N > a.total_nodes) ? 1 : 0;
+    misc->bad = 0;
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(&s_full[k], 1);
       mbar_init(&p_full[k], kSoftmaxThreads);
       mbar_init(&o_done[k], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     mbar_init(q_ready, kSoftmaxThreads);
-    mbar_init(&s_free[0], kSoftmaxThreads);
-    mbar_init(&s_free[1], kSoftmaxThreads);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -204,7 +308,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
-  if (misc->bad) {  // the sequence's extent itself is malformed: nothing to read
+
+  w.rows = w.N * a.group;
+  // Split-KV: the prefix of each sequence is cut into at most max_splits
+  // ranges of whole 128-key tiles; the splits of one tile form a cluster
+  // (grid y), and a member whose sequence has fewer splits only joins the
+  // cluster barriers.
+  const int chunk = max(BN, ((w.L + a.max_splits - 1) / a.max_splits + BN - 1) / BN * BN);
+  w.nsplit = max(1, (w.L + chunk - 1) / chunk);
+  if (w.N < 1 || w.mtile * BM >= w.rows) {  // no work for the whole cluster
+    if (warp == kMmaWarp) tmem_dealloc(tmem, Ly::kTmemCols);
+    return;
+  }
+  const bool idle = w.split >= w.nsplit;
+  w.last_split = (w.split == w.nsplit - 1);
+  w.k_begin = w.split * chunk;
+  w.k_end = min(w.L, w.k_begin + chunk);
+  w.n_prefix_tiles = idle ? 0 : (w.k_end - w.k_begin + BN - 1) / BN;
+  w.n_node_tiles = w.last_split ? (w.N + BN - 1) / BN : 0;
+  w.T = w.n_prefix_tiles + w.n_node_tiles;
+  const int node_lo = (w.mtile * BM) / a.group;
+  const int g = a.group;
+  // the sequence's extent itself is malformed: nothing to read
+  if (w.N > a.max_nodes || w.N > 512 || w.L > a.max_prefix_len || w.n0 < 0 ||
+      w.n0 + w.N > a.total_nodes) {
     if (tid == 0) record_status(a.status, w.b, kBadTree);
     const bool rows_addressable = w.n0 >= 0 && w.N <= a.max_nodes && w.n0 + w.N <= a.total_nodes;
     if (w.nsplit == 1 && rows_addressable && warp < 4) zero_rows<D>(a, w, tid);
@@ -213,15 +340,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const uint32_t tmem_s0 = tmem;        // S buffers at columns 0 and 128
   const uint32_t tmem_o = tmem + 256;   // O accumulator at columns 256 .. 256+D-1
-  const uint32_t tmem_p = tmem + 384;   // P (A operand of P.V)
   const uint32_t tmem_q = tmem + 448;   // Q tile (A operand of Q.K^T)
   volatile int* abort_flag = &misc->abort;
 
-  if (warp == kTmaWarp) {
+  if (idle) {
+    // a cluster member without keys: straight to the cluster barriers
+  } else if (warp == kTmaWarp) {
     // ---------------------------------------------------------- TMA producer
-    // The whole warp issues: lane 0 arms the stage's barrier, then each lane
-    // issues one box: a prefix tile is 8 pages x {K, V} (one 5-D box per page
-    // and tensor), a node tile is 16 groups of 8 nodes x {K, V}.
+    // K and V stream through separate rings: a K slot is free again as soon
+    // as S = Q K^T has read it, a V slot once P.V has, so K runs ahead of V.
+    // The whole warp issues a tile: lane 0 arms the slot's barrier, then lane
+    // u issues box u: page u of a prefix tile (one 5-D box per 16-token page,
+    // 8 per tile) or the u-th group of 8 nodes of a node tile (16 per tile).
     if (lane == 0) {
       prefetch_tmap(&maps.k_pool);
       prefetch_tmap(&maps.v_pool);
@@ -230,124 +360,146 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     constexpr int kPages = BN / 16;
     constexpr int kPastEnd = INT_MIN;                 // page past the prefix end -> zeros
-    const int my_kv = lane & 1;
-    const int my_unit = lane >> 1;                    // page (prefix) or 8-node group (nodes)
-    const bool prefix_lane = my_unit < kPages;
+    const bool prefix_lane = lane < kPages;
     const int pool_pages = a.num_blocks * a.hkv;
     const int32_t* btab = a.block_table + static_cast<size_t>(w.b) * a.max_blocks_per_seq;
     auto fetch_block = [&](int t) -> int {
-      const int lp = (w.k_begin + t * BN) / 16 + my_unit;
-      return (prefix_lane && lp * 16 < w.k_end) ? __ldg(btab + lp) : kPastEnd;
+      const int lp = (w.k_begin + t * BN) / 16 + lane;
+      return (prefix_lane && t < w.n_prefix_tiles && lp * 16 < w.k_end) ? __ldg(btab + lp) : kPastEnd;
     };
-    int blk_next = w.n_prefix_tiles > 0 ? fetch_block(0) : kPastEnd;
-    int issued = 0;
-    bool ok = true;
-    for (int t = 0; t < w.T; ++t) {
+    // issues tile t of tensor kv (0 = K, 1 = V) into its slot
+    auto issue = [&](int t, int kv, int blk) {
       const int st = t % kStages;
-      const int blk = blk_next;
-      if (t + 1 < w.n_prefix_tiles) blk_next = fetch_block(t + 1);  // overlaps the wait
-      if (lane == 0) ok = mbar_wait(&empty[st], ((t / kStages) & 1) ^ 1, abort_flag);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], 2 * Ly::kTileBytes);
+      uint64_t* bar = kv ? &vfull[st] : &kfull[st];
+      if (lane == 0) mbar_arrive_expect_tx(bar, Ly::kTileBytes);
       __syncwarp();
-      uint8_t* tile = smem + Ly::kStage0 + st * Ly::kStageBytes + my_kv * Ly::kTileBytes;
+      uint8_t* tile = smem + (kv ? Ly::kVRing : Ly::kKRing) + st * Ly::kTileBytes;
       if (t < w.n_prefix_tiles) {
         if (prefix_lane) {
           int page = pool_pages;  // out of bounds: zero fill
           if (blk >= 0 && blk < a.num_blocks) {
             page = blk * a.hkv + w.kvh;
-          } else if (blk != kPastEnd && !misc->bad) {  // malformed block id: zeros, reported
+          } else if (blk != kPastEnd && kv == 0 && !misc->bad) {  // malformed block id: zeros, reported
             misc->bad = 1;
             record_status(a.status, w.b, kBadTree);
           }
-          tma_load_5d(tile + my_unit * 2 * Ly::kGroupBytes, my_kv ? &maps.v_pool : &maps.k_pool,
-                      &full[st], 0, 0, 0, 0, page);
+          tma_load_5d(tile + lane * 2 * Ly::kGroupBytes, kv ? &maps.v_pool : &maps.k_pool, bar,
+                      0, 0, 0, 0, page);
         }
-      } else {
-        const int node0 = w.n0 + (t - w.n_prefix_tiles) * BN + my_unit * 8;
-        tma_load_4d(tile + my_unit * Ly::kGroupBytes, my_kv ? &maps.v_nodes : &maps.k_nodes,
-                    &full[st], 0, node0, 0, w.kvh);
+      } else if (lane < BN / 8) {
+        const int node0 = w.n0 + (t - w.n_prefix_tiles) * BN + lane * 8;
+        tma_load_4d(tile + lane * Ly::kGroupBytes, kv ? &maps.v_nodes : &maps.k_nodes, bar, 0,
+                    node0, 0, w.kvh);
       }
-      ++issued;
+    };
+    int blk_k = fetch_block(0);  // block id of the next K tile, loaded ahead
+    int tk = 0, tv = 0;
+    bool ok = true;
+    unsigned long long t_idle = 0;
+    while (tv < w.T) {
+      bool progressed = false;
+      if (tk < w.T) {
+        int ready = lane == 0 ? mbar_test_wait(&kempty[tk % kStages], ((tk / kStages) & 1) ^ 1) : 0;
+        if (__shfl_sync(0xffffffffu, ready, 0)) {
+          issue(tk, 0, blk_k);
+          ++tk;
+          blk_k = fetch_block(tk);
+          progressed = true;
+        }
+      }
+      if (tv < tk) {
+        int ready = lane == 0 ? mbar_test_wait(&vempty[tv % kStages], ((tv / kStages) & 1) ^ 1) : 0;
+        if (__shfl_sync(0xffffffffu, ready, 0)) {
+          issue(tv, 1, fetch_block(tv));
+          ++tv;
+          progressed = true;
+        }
+      }
+      int stop = 0;
+      if (lane == 0) {
+        if (progressed) {
+          t_idle = 0;
+        } else if (t_idle == 0) {
+          t_idle = global_ns();
+        } else if (global_ns() - t_idle > kWaitLimitNs || misc->abort) {
+          stop = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) {
+        ok = false;
+        break;
+      }
     }
     if (lane == 0) {
       if (!ok) {
         record_status(a.status, w.b, kDeviceTimeout);
         misc->abort = 1;
       }
-      // drain: every issued copy has landed before the CTA may exit
-      for (int t = max(0, issued - kStages); t < issued; ++t)
-        mbar_wait(&full[t % kStages], (t / kStages) & 1);
+      // drain: every issued copy has landed before the CTA may exit (at most
+      // kStages of each ring can still be in flight)
+      for (int t = max(0, tk - kStages); t < tk; ++t)
+        mbar_wait(&kfull[t % kStages], (t / kStages) & 1);
+      for (int t = max(0, tv - kStages); t < tv; ++t)
+        mbar_wait(&vfull[t % kStages], (t / kStages) & 1);
     }
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
+    // ---------------------------------------------------------- MMA issuers
+    // Two threads issue to the tensor core: S = Q K^T from warp 9 and
+    // O += P V from warp 10.  Issuing a tcgen05.mma stalls its thread while
+    // the tensor pipe is busy, so one thread issuing both would hold P(t).V(t)
+    // back behind S(t+1); with two threads each kind goes out as soon as its
+    // inputs are ready and the pipe interleaves them.
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);  // M=128, N=128: full-rate shape
-      constexpr uint32_t idesc_o = idesc_bf16(BM, D, 1);
-      bool ok = true;
-      // Descriptors are built once; each MMA adds a compile-time offset to the
-      // start-address field (16-byte units; shared addresses stay < 2^18).
-      // K (K-major): 8-row groups at kGroupBytes, halves at +1024.
-      // V (MN-major): 8-key groups at kGroupBytes, column halves at +1024.
-      const uint64_t dk0 = smem_desc(smem_u32(smem + Ly::kStage0), 16, Ly::kGroupBytes);
-      const uint64_t dv0 = smem_desc(smem_u32(smem + Ly::kStage0 + Ly::kTileBytes), 1024, Ly::kGroupBytes);
-      // S(t) = Q K(t)^T into S buffer t&1 (caller checked K(t) landed and the
-      // buffer is free)
-      auto issue_s = [&](int t) {
-        const uint64_t dk = dk0 + static_cast<uint64_t>((t % kStages) * (Ly::kStageBytes >> 4));
-        const uint32_t d = tmem_s0 + (t & 1) * BN;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          // A = Q from TMEM (16 dims = 8 columns per step), B = K from the ring
-          const uint32_t boff = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
-          mma_bf16_ts(d, tmem_q + kk * 8, dk + boff, idesc_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&s_full[t & 1]);
-      };
-      // O += P(t) V(t) (caller checked P(t) is in TMEM)
-      auto issue_pv = [&](int t) {
-        const int st = t % kStages;
-        const uint64_t dv = dv0 + static_cast<uint64_t>(st * (Ly::kStageBytes >> 4));
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // A = P from TMEM: 16 keys = 8 columns of bf16 pairs = 2 groups of V
-          mma_bf16_ts(tmem_o, tmem_p + kk * 8, dv + ((kk * 2 * Ly::kGroupBytes) >> 4), idesc_o,
-                      (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&o_done[t & 1]);
-        mma_commit(&empty[st]);
-      };
-      // Issue in whichever order the inputs become ready: S(t) needs K(t) in
-      // the ring and S buffer t&1 released by the softmax of tile t-2
-      // (s_free, right after it loaded S(t-2) into registers), so the tensor
-      // core computes S two tiles ahead; P(t).V(t) needs P(t) (p_full).
-      ok = mbar_wait(q_ready, 0, abort_flag);
+      bool ok = mbar_wait(q_ready, 0, abort_flag);
       tc_fence_after();
-      int ns = 0, npv = 0;
-      unsigned long long t_idle = 0;
-      while (ok && npv < w.T) {
-        bool progressed = false;
-        if (ns < w.T && ns < npv + 3 &&
-            (ns < 2 || mbar_test_wait(&s_free[ns & 1], ((ns - 2) >> 1) & 1)) &&
-            mbar_test_wait(&full[ns % kStages], (ns / kStages) & 1)) {
+      if (warp == kMmaWarp) {
+        constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);  // M=128, N=128: full-rate shape
+        // Descriptors are built once; each MMA adds a compile-time offset to
+        // the start-address field (16-byte units; shared addresses stay
+        // < 2^18).  K (K-major): 8-row groups at kGroupBytes, halves at +1024.
+        const uint64_t dk0 = smem_desc(smem_u32(smem + Ly::kKRing), 16, Ly::kGroupBytes);
+        for (int t = 0; ok && t < w.T; ++t) {
+          // S(t) = Q K(t)^T into S buffer t&1, once K(t) has landed and
+          // P(t-2).V(t-2), the last reader of that buffer, has completed
+          ok = mbar_wait(&kfull[t % kStages], (t / kStages) & 1, abort_flag);
+          if (ok && t >= 2) ok = mbar_wait(&o_done[t & 1], ((t - 2) >> 1) & 1, abort_flag);
+          if (!ok) break;
           tc_fence_after();
-          issue_s(ns);
-          ++ns;
-          progressed = true;
+          const uint64_t dk = dk0 + static_cast<uint64_t>((t % kStages) * (Ly::kTileBytes >> 4));
+          const uint32_t d = tmem_s0 + (t & 1) * BN;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // A = Q from TMEM (16 dims = 8 columns per step), B = K from the ring
+            const uint32_t boff = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
+            mma_bf16_ts(d, tmem_q + kk * 8, dk + boff, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[t & 1]);
+          mma_commit(&kempty[t % kStages]);  // the K slot is free once S(t) is done
         }
-        if (npv < ns && mbar_test_wait(&p_full[npv & 1], (npv >> 1) & 1)) {
+      } else {
+        constexpr uint32_t idesc_o = idesc_bf16(BM, D, 1);
+        // V (MN-major): 8-key groups at kGroupBytes, column halves at +1024.
+        const uint64_t dv0 = smem_desc(smem_u32(smem + Ly::kVRing), 1024, Ly::kGroupBytes);
+        for (int t = 0; ok && t < w.T; ++t) {
+          // O += P(t) V(t), once P(t) is in TMEM and V(t) has landed
+          ok = mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag);
+          if (ok) ok = mbar_wait(&vfull[t % kStages], (t / kStages) & 1, abort_flag);
+          if (!ok) break;
           tc_fence_after();
-          issue_pv(npv);
-          ++npv;
-          progressed = true;
-        }
-        if (progressed) {
-          t_idle = 0;
-        } else if (t_idle == 0) {
-          t_idle = global_ns();
-        } else if (global_ns() - t_idle > kWaitLimitNs || misc->abort) {
-          ok = false;
+          const int st = t % kStages;
+          const uint64_t dv = dv0 + static_cast<uint64_t>(st * (Ly::kTileBytes >> 4));
+          const uint32_t p = tmem_s0 + (t & 1) * BN;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            // A = P from TMEM: 16 keys = 8 columns of bf16 pairs (keys 0-63 in
+            // columns 0-31 of the buffer, keys 64-127 in columns 64-95); B = 2
+            // groups of V
+            mma_bf16_ts(tmem_o, p + (kk >> 2) * 64 + (kk & 3) * 8,
+                        dv + ((kk * 2 * Ly::kGroupBytes) >> 4), idesc_o,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&o_done[t & 1]);
+          mma_commit(&vempty[st]);
         }
       }
       if (!ok) {
@@ -355,8 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         misc->abort = 1;
       }
       // drain: all MMAs issued by this thread complete before TMEM is freed
-      mma_commit(drain);
-      mbar_wait(drain, 0);
+      uint64_t* dr = &drain[warp == kMmaWarp ? 0 : 1];
+      mma_commit(dr);
+      mbar_wait(dr, 0);
     }
     __syncwarp();
   } else {
@@ -370,14 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int R = w.mtile * BM + r;
     const bool live = R < w.rows;
     float* xchg = reinterpret_cast<float*>(smem + Ly::kXchg);  // [3 slots][2 halves][128 rows]
-    // tree of this sequence into shared memory, validated
-    for (int i = sid; i < w.N; i += kSoftmaxThreads) {
-      const int p = __ldg(a.parent + w.n0 + i);
-      par[i] = p;
-      if (!(i == 0 ? p == -1 : (p >= 0 && p < i))) misc->bad = 1;
-    }
     // Q tile -> TMEM (one row per lane, bf16 pairs; this thread stores the
-    // half hc of its row); padding rows are zero.
+    // half hc of its row); padding rows are zero.  The Q loads are issued
+    // before the tree loads so that both latencies overlap.
     {
       constexpr int kWords = D / 4;  // 32-bit words per half row
       uint32_t qw[kWords];
@@ -397,6 +545,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kWords; ++c) qw[c] = 0u;
       }
+      // tree of this sequence into shared memory, validated
+      for (int i = sid; i < w.N; i += kSoftmaxThreads) {
+        const int p = __ldg(a.parent + w.n0 + i);
+        par[i] = p;
+        if (!(i == 0 ? p == -1 : (p >= 0 && p < i))) misc->bad = 1;
+      }
       if constexpr (kWords == 32) {
         tmem_st32(tmem_q + hc * 32 + lane_off_q(warp), qw);
       } else {
@@ -404,25 +558,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
     }
+    tc_fence_before();  // Q is in TMEM before the MMA warp is released
+    mbar_arrive(q_ready);
     softmax_group_sync();
     const bool tree_ok = misc->bad == 0;
     if (!tree_ok && sid == 0) record_status(a.status, w.b, kBadTree);
     // ancestor-or-self bitmask of the tile's nodes (node tiles only)
     if (w.last_split && hc == 0) {
       const int i = node_lo + r;
-      uint32_t* row = anc + r * kMaxAncWords;
+      uint32_t* row = anc + r * kAncStride;
 #pragma unroll
       for (int k = 0; k < kMaxAncWords; ++k) row[k] = 0u;
       if (tree_ok && i < w.N) {
         for (int k = i; k >= 0; k = par[k]) row[k >> 5] |= 1u << (k & 31);
       }
     }
-    tc_fence_before();  // Q is in TMEM before the MMA warp is released
-    mbar_arrive(q_ready);
     softmax_group_sync();      // ancestor rows are read across threads
     const int i_node = live ? R / g : 0;  // local node of this row
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t* my_anc = anc + (i_node - node_lo) * kMaxAncWords;
+    const uint32_t* my_anc = anc + (i_node - node_lo) * kAncStride;
     float m_run = -INFINITY;  // reference max (log2 units), shared by the pair
     float l_run = 0.0f;       // this thread's half of the row sum
     bool ok = true;
@@ -440,8 +594,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem_s0 + (t & 1) * BN + hc * 64 + lane_off, lo);
         tmem_ld32(tmem_s0 + (t & 1) * BN + hc * 64 + 32 + lane_off, hi);
         tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&s_free[t & 1]);  // S buffer t&1 may now take S(t+2)
       } else {
 #pragma unroll
         for (int c = 0; c < 64; ++c) x[c] = 0.0f;
@@ -457,13 +609,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         const int j0 = (t - w.n_prefix_tiles) * BN + hc * 64;
+        // only ancestors-or-self of this node carry a bit, all of them < N,
+        // so node columns past the tree are masked as well
         const uint32_t b0 = live ? my_anc[j0 >> 5] : 0u;
         const uint32_t b1 = live ? my_anc[(j0 >> 5) + 1] : 0u;
-        const int nvalid = w.N - j0;  // node columns past the tree are masked
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const uint32_t bit = c < 32 ? (b0 >> c) & 1u : (b1 >> (c - 32)) & 1u;
-          if (!bit || c >= nvalid) x[c] = -INFINITY;
+        for (int c = 0; c < 32; ++c) {
+          x[c] = (b0 & (1u << c)) ? x[c] : -INFINITY;
+          x[c + 32] = (b1 & (1u << c)) ? x[c + 32] : -INFINITY;
         }
       }
       float mx[32];
@@ -476,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the row max of both halves (exchange slot t&1, so that the next
       // tile's write cannot overtake the partner's read)
       xchg[((t & 1) * 2 + hc) * 128 + r] = mx[0];
-      softmax_pair_sync();
+      softmax_pair_sync(warp);
       if (!ok) continue;  // skip the work, keep the barrier sequence
       const float tmax = fmaxf(mx[0], xchg[((t & 1) * 2 + (hc ^ 1)) * 128 + r]) * a.scale_log2;
       // online softmax with a lazily rescaled reference max (same decision
@@ -492,15 +645,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
       }
-      // P(t-1).V(t-1) must be complete: it reads the single P buffer and
-      // accumulates into O
-      if (t >= 1) {
+      // A rescale of O waits for P(t-1).V(t-1), the last accumulation into
+      // it.  P(t) itself needs no wait: it goes to the buffer S(t) came from,
+      // whose previous reader P(t-2).V(t-2) completed before S(t) did.
+      if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
         ok = __all_sync(0xffffffffu,
                         mbar_wait(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag));
         if (!ok) continue;
         tc_fence_after();
-      }
-      if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
         // this thread rescales its half of the O row
 #pragma unroll
         for (int c0 = hc * (D / 2); c0 < (hc + 1) * (D / 2); c0 += 32) {
@@ -529,14 +681,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ls[c8] = part;
       }
-      tmem_st32(tmem_p + hc * 32 + lane_off, pk);
+      tmem_st32(tmem_s0 + (t & 1) * BN + hc * 64 + lane_off, pk);
       l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       // keys past the prefix end in this tile: clear their V rows (page tails
       // may hold stale data; P is 0 there but 0 * NaN would poison O)
       if (valid_keys < BN) {
         const int st = t % kStages;
-        mbar_wait(&full[st], (t / kStages) & 1);  // acquire the TMA writes
-        uint8_t* vt = smem + Ly::kStage0 + st * Ly::kStageBytes + Ly::kTileBytes;
+        mbar_wait(&vfull[st], (t / kStages) & 1);  // acquire the TMA writes
+        uint8_t* vt = smem + Ly::kVRing + st * Ly::kTileBytes;
         for (int idx = sid; idx < (BN - valid_keys) * Ly::kHalves; idx += kSoftmaxThreads) {
           const int row = valid_keys + idx / Ly::kHalves, h = idx % Ly::kHalves;
           uint4* p = reinterpret_cast<uint4*>(vt + (row >> 3) * Ly::kGroupBytes + h * 1024 +
@@ -552,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the row sum of both halves (slot 2: the max slots may still be read)
     xchg[(2 * 2 + hc) * 128 + r] = l_run;
-    softmax_pair_sync();
+    softmax_pair_sync(warp);
     const float l_row = l_run + xchg[(2 * 2 + (hc ^ 1)) * 128 + r];
     if (!ok) {
       record_status(a.status, w.b, kDeviceTimeout);
@@ -563,8 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ epilogue
       const bool final_out = (w.nsplit == 1);
       const float inv_l = (l_row > 0.0f) ? 1.0f / l_row : 0.0f;
-      const size_t unit = (static_cast<size_t>(w.b) * a.hkv + w.kvh) * a.mtiles_max + w.mtile;
-      const size_t prow_idx = (unit * a.max_splits + w.split) * BM + r;
+      using Pt = Partial<D>;
+      float* part_o = reinterpret_cast<float*>(smem + Ly::kKRing + Pt::kO) + r * Pt::kStride;
 #pragma unroll
       for (int c0 = hc * (D / 2); c0 < (hc + 1) * (D / 2); c0 += 32) {
         uint32_t o[32];
@@ -584,14 +736,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[k] = v;
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(a.ws_o + prow_idx * D + c0);
+          float4* dst = reinterpret_cast<float4*>(part_o + c0);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
                                  __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
         }
       }
-      if (live && !final_out && hc == 0) a.ws_ml[prow_idx] = make_float2(m_run, l_row);
+      if (live && !final_out && hc == 0)
+        reinterpret_cast<float2*>(smem + Ly::kKRing + Pt::kMl)[r] = make_float2(m_run, l_row);
     } else if (w.T > 0) {
       record_status(a.status, w.b, kDeviceTimeout);
       misc->abort = 1;
@@ -601,75 +754,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (a.max_splits > 1) {
+    // launched as clusters of max_splits CTAs: merge this tile's splits
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();  // every split's partial is in its shared memory
+    if (w.nsplit > 1 && !idle && warp < kSoftmaxThreads / 32)
+      merge_rows<D>(a, w, smem + Ly::kKRing, &misc->bad, tid,
+                    static_cast<int>(cluster.block_rank()));
+    cluster.sync();  // no CTA leaves while another may still read its shared memory
+  }
   // a malformed tree or block id: the only writer of these rows writes zeros
   // (each row by the thread that wrote it in the epilogue, so zeros win)
   if (misc->bad && w.nsplit == 1 && warp < 4) zero_rows<D>(a, w, tid);
   if (warp == kMmaWarp) tmem_dealloc(tmem, Ly::kTmemCols);
-}
-
-// Combines the split partials: one warp per packed output row,
-// O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, lanes over D (float4).
-constexpr int kMergeWarps = 8;
-template <int D>
-__global__ void __launch_bounds__(kMergeWarps * 32) tree_attn_merge(const AttnArgs a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int unit = blockIdx.x / (BM / kMergeWarps);
-  const int r = (blockIdx.x % (BM / kMergeWarps)) * kMergeWarps + warp;
-  const int mtile = unit % a.mtiles_max;
-  const int bk = unit / a.mtiles_max;
-  const int b = bk / a.hkv, kvh = bk % a.hkv;
-  const int n0 = a.node_offsets[b];
-  const int N = a.node_offsets[b + 1] - n0;
-  const int L = max(0, a.prefix_lens[b]);
-  const int nsplit = max(1, (L + a.chunk - 1) / a.chunk);
-  const int rows = N * a.group;
-  if (nsplit == 1 || N < 1 || N > a.max_nodes || L > a.max_prefix_len || n0 < 0 ||
-      n0 + N > a.total_nodes)
-    return;
-  const int R = mtile * BM + r;
-  if (R >= rows) return;
-  const int i = R / a.group, h = kvh * a.group + R % a.group;
-  uint16_t* dst = a.out + (static_cast<size_t>(n0 + i) * a.hq + h) * D;
-  constexpr int kPer = D / 32;  // elements per lane (4 for D=128, 2 for D=64)
-  if (a.status[b] == kBadTree) {
-    for (int d = lane; d < D; d += 32) dst[d] = 0;
-    return;
-  }
-  const size_t base = (static_cast<size_t>(unit) * a.max_splits) * BM + r;
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, a.ws_ml[base + static_cast<size_t>(s) * BM].x);
-  const float mref = (M == -INFINITY) ? 0.0f : M;
-  float acc[kPer];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) acc[k] = 0.0f;
-  float lsum = 0.0f;
-  for (int s = 0; s < nsplit; ++s) {
-    const size_t pr = base + static_cast<size_t>(s) * BM;
-    const float2 ml = a.ws_ml[pr];
-    const float wgt = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - mref);
-    lsum += wgt * ml.y;
-    const float* src = a.ws_o + pr * D + lane * kPer;
-    if constexpr (kPer == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
-      acc[0] += wgt * v.x;
-      acc[1] += wgt * v.y;
-      acc[2] += wgt * v.z;
-      acc[3] += wgt * v.w;
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(src);
-      acc[0] += wgt * v.x;
-      acc[1] += wgt * v.y;
-    }
-  }
-  const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
-  if constexpr (kPer == 4) {
-    uint2 o;
-    o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    *reinterpret_cast<uint2*>(dst + lane * 4) = o;
-  } else {
-    *reinterpret_cast<uint32_t*>(dst + lane * 2) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-  }
 }
 
 }  // namespace
@@ -679,8 +777,6 @@ size_t tree_attention_smem_bytes(int head_dim) {
 }
 
 int launch_tree_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream) {
-  const dim3 grid(a.mtiles_max, a.max_splits, a.batch * a.hkv);
-  cudaError_t e;
   static thread_local int attr_set_device = -1;  // the attribute is set once per device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -691,24 +787,26 @@ int launch_tree_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
                          Layout<64>::kAlloc);
     attr_set_device = dev;
   }
+  if (a.max_splits < 1 || a.max_splits > 8) return -1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.mtiles_max, a.max_splits, a.batch * a.hkv);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  // the splits of one tile (grid y) run as one cluster
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = a.max_splits;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.max_splits > 1 ? 1 : 0;
+  cudaError_t e;
   if (a.head_dim == 128) {
-    const int smem = Layout<128>::kAlloc;
-    tree_attn_kernel<128><<<grid, kThreads, smem, stream>>>(a, maps);
-    e = cudaGetLastError();
-    if (e == cudaSuccess && a.max_splits > 1) {
-      tree_attn_merge<128><<<a.batch * a.hkv * a.mtiles_max * (BM / kMergeWarps),
-                             kMergeWarps * 32, 0, stream>>>(a);
-      e = cudaGetLastError();
-    }
+    cfg.dynamicSmemBytes = Layout<128>::kAlloc;
+    e = cudaLaunchKernelEx(&cfg, tree_attn_kernel<128>, a, maps);
   } else {
-    const int smem = Layout<64>::kAlloc;
-    tree_attn_kernel<64><<<grid, kThreads, smem, stream>>>(a, maps);
-    e = cudaGetLastError();
-    if (e == cudaSuccess && a.max_splits > 1) {
-      tree_attn_merge<64><<<a.batch * a.hkv * a.mtiles_max * (BM / kMergeWarps),
-                            kMergeWarps * 32, 0, stream>>>(a);
-      e = cudaGetLastError();
-    }
+    cfg.dynamicSmemBytes = Layout<64>::kAlloc;
+    e = cudaLaunchKernelEx(&cfg, tree_attn_kernel<64>, a, maps);
   }
   return e == cudaSuccess ? 0 : -1;
 }

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -48,14 +49,15 @@ int sm_count() {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct AttnPlan {
-  int group, mtiles_max, max_splits, chunk;
-  size_t ws_o_bytes, ws_ml_bytes;
+  int group, mtiles_max, max_splits;
 };
 
 // Launch plan: 128-row tiles of packed (node, head) rows per (sequence, KV
-// head); the prefix is split so that the grid covers about two waves of
-// SMs, with at least 512 keys per split (partials cost 0.5 KB per row); splits
-// are whole 128-key tiles.
+// head).  When those tiles cover less than about two waves of SMs, each
+// sequence's prefix is also split into up to 8 ranges of whole 128-key tiles
+// (at least 256 keys per split on the longest prefix); the splits of a tile
+// run as one thread-block cluster and merge through distributed shared
+// memory, so no device workspace is needed.
 bool plan_attention(const tv_attn_params* p, AttnPlan* out) {
   if (!p) return false;
   if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1) return false;
@@ -75,15 +77,9 @@ bool plan_attention(const tv_attn_params* p, AttnPlan* out) {
   const long target = 2l * sm_count();
   long splits = 1;
   if (p->max_prefix_len > 0 && base < target) splits = (target + base - 1) / base;
-  long chunk = (p->max_prefix_len + splits - 1) / splits;
-  chunk = ((chunk + 127) / 128) * 128;  // whole 128-key tiles
-  if (chunk < 512) chunk = 512;
-  pl.chunk = static_cast<int>(chunk);
-  pl.max_splits = p->max_prefix_len > 0 ? static_cast<int>((p->max_prefix_len + chunk - 1) / chunk) : 1;
-  if (pl.max_splits < 1) pl.max_splits = 1;
-  const size_t prow = static_cast<size_t>(base) * pl.max_splits * 128;
-  pl.ws_o_bytes = pl.max_splits > 1 ? prow * p->head_dim * sizeof(float) : 0;
-  pl.ws_ml_bytes = pl.max_splits > 1 ? prow * sizeof(float2) : 0;
+  splits = std::min(splits, 8l);
+  splits = std::min(splits, std::max(1l, static_cast<long>(p->max_prefix_len) / 256));
+  pl.max_splits = static_cast<int>(splits);
   *out = pl;
   return true;
 }
@@ -118,9 +114,8 @@ const char* tv_status_string(int s) {
 int tv_version(void) { return TV_VERSION; }
 
 size_t tv_tree_attention_workspace_size(const tv_attn_params* p) {
-  AttnPlan pl;
-  if (!plan_attention(p, &pl)) return 0;
-  return pl.ws_o_bytes + pl.ws_ml_bytes;
+  (void)p;  // split partials are merged through distributed shared memory
+  return 0;
 }
 
 int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
@@ -138,9 +133,8 @@ int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
                         v_nodes, parent, prefix_lens, node_offsets, out, status};
   for (const void* q : ptrs)
     if (!q || !aligned16(q)) return TV_ERR_INVALID_ARG;
-  const size_t need = pl.ws_o_bytes + pl.ws_ml_bytes;
-  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
-    return TV_ERR_WORKSPACE;
+  (void)workspace;  // the split merge happens on chip: no workspace is used
+  (void)workspace_bytes;
 
   const int D = p->head_dim, Hkv = p->num_kv_heads;
   tv::AttnMaps maps;
@@ -179,10 +173,6 @@ int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
   a.node_offsets = node_offsets;
   a.out = out;
   a.status = status;
-  a.ws_o = pl.max_splits > 1 ? static_cast<float*>(workspace) : nullptr;
-  a.ws_ml = pl.max_splits > 1
-                ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + pl.ws_o_bytes)
-                : nullptr;
   a.batch = p->batch;
   a.hq = p->num_q_heads;
   a.hkv = Hkv;
@@ -195,7 +185,6 @@ int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
   a.total_nodes = p->total_nodes;
   a.mtiles_max = pl.mtiles_max;
   a.max_splits = pl.max_splits;
-  a.chunk = pl.chunk;
   const float scale = p->softmax_scale > 0.0f ? p->softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
   a.scale_log2 = scale * 1.4426950408889634f;
 

@@ -44,13 +44,10 @@ struct AttnArgs {
   const int32_t* node_offsets;// [batch+1]
   uint16_t* out;              // [total_nodes][Hq][D]
   int32_t* status;            // [batch]
-  float* ws_o;                // split partials: [units*max_splits*128][D] fp32
-  float2* ws_ml;              // split partials: [units*max_splits*128] (m, l)
   int32_t batch, hq, hkv, group, head_dim;
   int32_t max_blocks_per_seq, num_blocks, max_nodes, max_prefix_len, total_nodes;
   int32_t mtiles_max;         // ceil(max_nodes * group / 128)
-  int32_t max_splits;         // splits of the longest prefix
-  int32_t chunk;              // prefix keys per split (multiple of 128)
+  int32_t max_splits;         // CTAs per cluster (grid y): prefix splits per tile, <= 8
   float scale_log2;           // softmax scale * log2(e)
 };
 

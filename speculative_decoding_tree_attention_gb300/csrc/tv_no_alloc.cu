@@ -23,7 +23,8 @@
 
 namespace {
 
-// Split-KV partials of tv_tree_attention_no_alloc (shared by every call).
+// Device scratch of tv_tree_attention_no_alloc (shared by every call; the
+// current attention plans need none).
 static __device__ __align__(256) unsigned char tv_no_alloc_scratch[TV_NO_ALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;

@@ -74,12 +74,13 @@ def test_attention_null_pointer_rejected(lib):
     assert lib.tv_tree_attention(C.byref(p), *args, None, C.c_size_t(0), None) == tv.TV_ERR_INVALID_ARG
 
 
-def test_attention_workspace_size_rules(lib):
+def test_attention_needs_no_workspace(lib):
     assert lib.tv_tree_attention_workspace_size(C.byref(_params(head_dim=96))) == 0
-    # a long prefix on few (sequence, head) pairs is split -> needs partials
+    # a long prefix on few (sequence, head) pairs is split over a cluster and
+    # merged on chip: still no device workspace
     p = _params(batch=1, num_kv_heads=1, num_q_heads=1, max_prefix_len=32768,
                 max_blocks_per_seq=2048, num_blocks=2048, max_nodes=16, total_nodes=16)
-    assert lib.tv_tree_attention_workspace_size(C.byref(p)) > 0
+    assert lib.tv_tree_attention_workspace_size(C.byref(p)) == 0
 
 
 @pytest.mark.parametrize("bad", [dict(vocab=0), dict(vocab=1 << 18), dict(max_nodes=600),
