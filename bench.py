@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller cases for profiler captures)")
     return ap.parse_args()
 
 
@@ -226,7 +228,7 @@ def cpu_baseline(case, budget_s, threads=None):
 
 
 def run_reference(args):
-    cfg = wl.config(args.config)
+    cfg = wl.config(args.config, **({"batch": args.batch} if args.batch > 0 else {}))
     case = wl.make_case(cfg, parts=("attn", "accept"), kind=args.mode)
     per_step = min(2.0, 120.0 / max(1, args.steps))
     cpu_baseline(case, min(per_step, 0.5))  # warm-up: builds and pages in the oracle
@@ -275,7 +277,7 @@ def main():
     _build.build()
     tv.load()
 
-    cfg = wl.config(args.config)
+    cfg = wl.config(args.config, **({"batch": args.batch} if args.batch > 0 else {}))
     case = wl.make_case(cfg, parts=("attn", "accept"), kind=args.mode)
     tot = int(case["node_offsets"][-1])
     B = cfg["batch"]
