@@ -112,6 +112,13 @@ __device__ __forceinline__ uint32_t lane_off_q(int warp) {
   return static_cast<uint32_t>((warp & 3) * 32) << 16;
 }
 
+// max of three (NaN operands are ignored, as in fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Named barriers: id 1 joins the 8 softmax warps; ids 2..5 join the two
 // warps (w and w+4) that share a lane quarter, i.e. the two halves of the
 // same 32 rows (0 is __syncthreads).
@@ -619,13 +626,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[c + 32] = (b1 & (1u << c)) ? x[c + 32] : -INFINITY;
         }
       }
-      float mx[32];
+      // max of the 64 scores with three-input max: 64 -> 22 -> 8 -> 3 -> 1
+      float mx[22];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) mx[c] = fmaxf(x[c], x[c + 32]);
+      for (int c = 0; c < 21; ++c) mx[c] = fmax3(x[3 * c], x[3 * c + 1], x[3 * c + 2]);
+      mx[21] = x[63];
 #pragma unroll
-      for (int h = 16; h >= 1; h >>= 1)
-#pragma unroll
-        for (int c = 0; c < h; ++c) mx[c] = fmaxf(mx[c], mx[c + h]);
+      for (int c = 0; c < 7; ++c) mx[c] = fmax3(mx[3 * c], mx[3 * c + 1], mx[3 * c + 2]);
+      mx[7] = mx[21];
+      mx[0] = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       // the row max of both halves (exchange slot t&1, so that the next
       // tile's write cannot overtake the partner's read)
       xchg[((t & 1) * 2 + hc) * 128 + r] = mx[0];
