@@ -134,6 +134,12 @@ def ncu_traffic(cfg_num):
     return e.get("dram_bytes_per_launch")
 
 
+def pct(ms):
+    """p10 / p50 / p90 of per-rep times given in ms, in microseconds."""
+    v = np.sort(np.asarray(ms, np.float64)) * 1e3
+    return {k: float(np.percentile(v, q)) for k, q in (("p10", 10), ("p50", 50), ("p90", 90))}
+
+
 def roofline_entry(nbytes, flops, seconds, peak_bw, peak_tf, peak_kind):
     """The bound is whichever roof is lower for this launch's arithmetic
     intensity: HBM (bytes / peak bandwidth) or the bf16 tensor pipe
@@ -417,6 +423,32 @@ def main():
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_s = float(t.item())
 
+    # ---- commit of the accepted path (the step after the walk; reported on its
+    # own, not part of the timed step): the root and the accepted nodes of the
+    # last step's accept results go into fresh pages of an extended pool
+    kpx, vpx, tabx = wl.extend_pool(case, max_nodes + 1)
+    cm = {"kp": torch.from_numpy(kpx.view(np.int16)).to(dev).view(torch.bfloat16),
+          "vp": torch.from_numpy(vpx.view(np.int16)).to(dev).view(torch.bfloat16),
+          "table": torch.from_numpy(tabx).to(dev)}
+    del kpx, vpx
+    cm_out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev))
+    evc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nb)]
+    with torch.cuda.stream(stream):
+        for k in range(nb + 3):
+            flush.fill_(k & 0xFF)
+            if k >= 3:
+                evc[k - 3][0].record(stream)
+            tv.commit_kv(d["kn"], d["vn"], d["parent"], d["off"], acc_out["accepted_len"],
+                         acc_out["path"], cm["table"], d["lens"], cm["kp"], cm["vp"],
+                         max_nodes=max_nodes, new_prefix_lens=cm_out[0], status=cm_out[1])
+            if k >= 3:
+                evc[k - 3][1].record(stream)
+    stream.synchronize()
+    assert int(cm_out[1].max()) == 0, "commit status"
+    commit_ms = [a0.elapsed_time(a1) for a0, a1 in evc]
+    commit_tokens = int(acc_out["accepted_len"].sum().item()) + B
+    del cm
+
     # ---- end to end through the public API with host buffers
     pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()}
     e2e_src = {k: torch.empty_like(d[k].view(pinned[k].dtype)) for k in host}
@@ -478,11 +510,18 @@ def main():
         "e2e": {"value": world * tot * e2e_steps / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * args.steps,
+        "percentiles_us": {"step": pct(step_ms), "attention": pct(attn_ms), "accept": pct(acc_ms)},
+        "commit": {"mean_us": statistics.mean(commit_ms) * 1e3, "tokens": commit_tokens,
+                   "bytes": commit_tokens * 8 * cfg["hkv"] * cfg["d"],  # K+V rows read and written
+                   "note": "tv_commit_kv of the root and accepted path, timed on its own"},
         "clocks": clk,
         "wall_s_timed_loop": wall,
     }
     if world == 1 and args.cpu_seconds > 0:
-        line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+        cb = cpu_baseline(case, args.cpu_seconds)
+        one = cpu_baseline(case, max(1.0, args.cpu_seconds / 4), threads=1)
+        cb["single_thread"] = {"value": one["value"], "unit": one["unit"], "sample": one["sample"]}
+        line["cpu_baseline"] = cb
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -55,7 +55,8 @@ typedef enum {
   TV_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required */
   TV_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
   TV_ERR_BAD_TREE = 5,       /* device: malformed tree, block id or token */
-  TV_ERR_DEVICE_TIMEOUT = 6  /* device: a bounded wait ran out */
+  TV_ERR_DEVICE_TIMEOUT = 6, /* device: a bounded wait ran out */
+  TV_ERR_NO_PAGE = 7         /* device: no pool page for a position to commit */
 } tv_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -218,6 +219,53 @@ int tv_accept(const tv_accept_params* params, const float* target, const float* 
               const float* uniforms, const uint32_t* retained_mask, int32_t* accepted_len,
               int32_t* path, int32_t* bonus_token, int32_t* status, float* debug_pq,
               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ========================================================================
+ * Commit of the accepted path ([MM] §9.1 item 2: the target KV cache is
+ * preallocated and tree-node KV is written into it by a scatter kernel;
+ * [LLM] §2.3.2: pool slots only for the unique accepted path; [EC] §5.2:
+ * the prefix cache grows incrementally by the accepted path).
+ *
+ * For every sequence b with accepted_len a = accepted_len[b] >= 0 and
+ * prefix length L = prefix_lens[b]: the root (local node 0, the token
+ * committed by the previous step, whose K/V this step computed) and the
+ * accepted nodes path[b][0..a-1] become committed tokens at positions
+ * L, L+1, .., L+a.  For every KV head, the K and V rows of node v
+ * (k_nodes/v_nodes row n0 + v) are copied to row pos % 16 of pool page
+ * block_table[b][pos / 16] (layouts as for tree attention), and
+ * new_prefix_lens[b] = L + a + 1; status[b] = TV_OK.
+ * A sequence is left untouched (new_prefix_lens[b] = L, nothing written) with
+ *   TV_ERR_BAD_TREE if a < 0 (its accept pass failed), a >= N_b, its tree
+ *     extent is malformed, or path[b][d] is not a child of path[b][d-1]
+ *     (path[b][-1] = the root);
+ *   TV_ERR_NO_PAGE if a position L..L+a has no page (block id < 0 or >=
+ *     num_blocks, or past max_blocks_per_seq): the caller's allocator
+ *     provides the pages before the call.
+ * Every output is written by the call: status and new_prefix_lens need no
+ * initialisation.  new_prefix_lens must not alias prefix_lens.  Positions
+ * L..L+a of every listed page must not be read by other work in flight.
+ * ====================================================================== */
+typedef struct {
+  int32_t batch;              /* B >= 1                                      */
+  int32_t num_kv_heads;       /* Hkv                                         */
+  int32_t head_dim;           /* D: 64 or 128                                */
+  int32_t block_size;         /* must be TV_BLOCK_SIZE (16)                  */
+  int32_t max_blocks_per_seq; /* row stride of block_table                   */
+  int32_t num_blocks;         /* pages in the pool                           */
+  int32_t max_nodes;          /* row stride of path; >= every N_b            */
+  int32_t total_nodes;        /* node_offsets[batch] (host copy)             */
+} tv_commit_params;           /* host struct */
+
+/* Layouts: k_nodes, v_nodes bf16 [total_nodes][Hkv][D]; parent, node_offsets,
+ * accepted_len, path as produced for / by tv_accept; block_table int32
+ * [batch][max_blocks_per_seq]; prefix_lens, new_prefix_lens, status int32
+ * [batch]; k_prefix_blocks, v_prefix_blocks bf16 [num_blocks][Hkv][16][D]
+ * (written).  All device pointers 16-byte aligned. */
+int tv_commit_kv(const tv_commit_params* params, const uint16_t* k_nodes,
+                 const uint16_t* v_nodes, const int32_t* parent, const int32_t* node_offsets,
+                 const int32_t* accepted_len, const int32_t* path, const int32_t* block_table,
+                 const int32_t* prefix_lens, uint16_t* k_prefix_blocks, uint16_t* v_prefix_blocks,
+                 int32_t* new_prefix_lens, int32_t* status, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -4,10 +4,11 @@ Only the test suite, the package smoke check and the benchmark's CPU-baseline
 leg import this module.  The product path (the C-ABI library and its binding)
 never imports, links or calls it, and shares no code with it.
 
-The arithmetic lives in ``oracle.c`` (plain C, fp64, pthreads); this file only
+The arithmetic lives in ``oracle.c`` (plain C, fp64, pthreads); this file
 compiles it with gcc and marshals numpy arrays through ctypes.  See the header
 of ``oracle.c`` for what is computed and which passage of the pages each step
-follows.
+follows.  The one step without arithmetic, the commit of the accepted path
+(a copy by definition), is written out here with numpy: ``commit_kv``.
 """
 from __future__ import annotations
 
@@ -179,3 +180,59 @@ def retained_mass(q_row, mask_row) -> float:
     q = _c(q_row, np.float32)
     m = None if mask_row is None else _c(mask_row, np.uint32)
     return float(_load().oracle_retained_mass_row(_ptr(q), _ptr(m), int(q.shape[0])))
+
+
+def commit_kv(k_nodes, v_nodes, parent, node_offsets, accepted_len, path, block_table,
+              prefix_lens, k_pool, v_pool, max_nodes):
+    """Commit of the accepted path, by definition (multimodal page §9.1 item 2:
+    tree-node KV scattered into the preallocated target KV cache; on-device
+    LLM page §2.3.2: slots only for the unique accepted path; edge-cloud page
+    §5.2: the prefix cache grows by the accepted path).
+
+    For each sequence b with a = accepted_len[b] and L = prefix_lens[b]: the
+    root (local node 0) and path[b][0..a-1] become positions L .. L+a; the K
+    and V rows of those nodes (every KV head) go to row pos % 16 of page
+    block_table[b][pos // 16].  Status 5 (malformed: a < 0, a >= N, a bad
+    extent, or a path step that is not a child of the previous node) or 7 (a
+    position without a page) leaves the sequence untouched.  Arrays are numpy
+    (bf16 as uint16 bit patterns).  Returns (k_pool, v_pool, new_prefix_lens,
+    status) as new arrays."""
+    k_pool = np.array(k_pool, copy=True)
+    v_pool = np.array(v_pool, copy=True)
+    off = np.asarray(node_offsets, np.int64)
+    B = off.shape[0] - 1
+    total = int(np.asarray(k_nodes).shape[0])
+    num_blocks = k_pool.shape[0]
+    table = np.asarray(block_table)
+    new_lens = np.array(prefix_lens, np.int32, copy=True)
+    status = np.zeros(B, np.int32)
+    for b in range(B):
+        n0, N = int(off[b]), int(off[b + 1] - off[b])
+        a, L = int(accepted_len[b]), int(prefix_lens[b])
+        ok = 1 <= N <= max_nodes and n0 >= 0 and n0 + N <= total and 0 <= a < N and L >= 0
+        nodes = [0]
+        if ok:
+            for d in range(a):
+                v = int(path[b][d])
+                if not (1 <= v < N and int(parent[n0 + v]) == nodes[-1]):
+                    ok = False
+                    break
+                nodes.append(v)
+        if not ok:
+            status[b] = 5
+            continue
+        pages = []
+        for t in range(a + 1):
+            pg = (L + t) // 16
+            blk = int(table[b][pg]) if pg < table.shape[1] else -1
+            if not 0 <= blk < num_blocks:
+                break
+            pages.append(blk)
+        if len(pages) < a + 1:
+            status[b] = 7
+            continue
+        for t, (v, blk) in enumerate(zip(nodes, pages)):
+            k_pool[blk, :, (L + t) % 16, :] = k_nodes[n0 + v]
+            v_pool[blk, :, (L + t) % 16, :] = v_nodes[n0 + v]
+        new_lens[b] = L + a + 1
+    return k_pool, v_pool, new_lens, status

@@ -9,14 +9,16 @@ PyTorch is used for device memory and the current CUDA stream only.
 
     tree_attention(...)  -> out, status      (tv_tree_attention)
     accept(...)          -> dict of outputs  (tv_accept)
+    commit_kv(...)       -> new_prefix_lens, status (tv_commit_kv)
 """
 from __future__ import annotations
 
 import ctypes as C
 import os
 
-__all__ = ["TVError", "load", "tree_attention", "accept", "attention_workspace_size",
-           "TV_MAX_NODES", "TV_OK", "TV_ERR_BAD_TREE", "TV_ERR_DEVICE_TIMEOUT", "status_string"]
+__all__ = ["TVError", "load", "tree_attention", "accept", "commit_kv", "attention_workspace_size",
+           "TV_MAX_NODES", "TV_OK", "TV_ERR_BAD_TREE", "TV_ERR_DEVICE_TIMEOUT", "TV_ERR_NO_PAGE",
+           "status_string"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libtv.so")
@@ -28,10 +30,11 @@ TV_ERR_WORKSPACE = 3
 TV_ERR_CUDA = 4
 TV_ERR_BAD_TREE = 5
 TV_ERR_DEVICE_TIMEOUT = 6
+TV_ERR_NO_PAGE = 7
 TV_MAX_NODES = 512
 TV_BLOCK_SIZE = 16
 EXPORTS = ("tv_status_string", "tv_version", "tv_tree_attention_workspace_size",
-           "tv_tree_attention", "tv_accept_workspace_size", "tv_accept")
+           "tv_tree_attention", "tv_accept_workspace_size", "tv_accept", "tv_commit_kv")
 
 
 class TVError(RuntimeError):
@@ -51,6 +54,12 @@ class AttnParams(C.Structure):
 class AcceptParams(C.Structure):
     _fields_ = [("batch", C.c_int32), ("vocab", C.c_int32), ("max_nodes", C.c_int32),
                 ("total_nodes", C.c_int32), ("kind", C.c_int32)]
+
+
+class CommitParams(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("num_kv_heads", C.c_int32), ("head_dim", C.c_int32),
+                ("block_size", C.c_int32), ("max_blocks_per_seq", C.c_int32),
+                ("num_blocks", C.c_int32), ("max_nodes", C.c_int32), ("total_nodes", C.c_int32)]
 
 
 _lib = None
@@ -80,6 +89,8 @@ def load(path: str | None = None) -> C.CDLL:
     lib.tv_accept.restype = C.c_int
     lib.tv_tree_attention_no_alloc.argtypes = [C.POINTER(AttnParams)] + [vp] * 11 + [vp]
     lib.tv_tree_attention_no_alloc.restype = C.c_int
+    lib.tv_commit_kv.argtypes = [C.POINTER(CommitParams)] + [vp] * 12 + [vp]
+    lib.tv_commit_kv.restype = C.c_int
     if path is None:
         _lib = lib
     return lib
@@ -91,7 +102,7 @@ def status_string(code: int) -> str:
     except OSError:
         return {0: "TV_OK", 1: "TV_ERR_INVALID_ARG", 2: "TV_ERR_UNSUPPORTED",
                 3: "TV_ERR_WORKSPACE", 4: "TV_ERR_CUDA", 5: "TV_ERR_BAD_TREE",
-                6: "TV_ERR_DEVICE_TIMEOUT"}.get(int(code), "TV_ERR_UNKNOWN")
+                6: "TV_ERR_DEVICE_TIMEOUT", 7: "TV_ERR_NO_PAGE"}.get(int(code), "TV_ERR_UNKNOWN")
 
 
 def _ptr(t):
@@ -229,3 +240,33 @@ def accept(target, draft_probs, draft_tokens, parent, node_offsets, uniforms,
     if rc != TV_OK:
         raise TVError(rc, "tv_accept")
     return dict(accepted_len=acc, path=path, bonus_token=bonus, status=status, debug_pq=dpq)
+
+
+def commit_kv(k_nodes, v_nodes, parent, node_offsets, accepted_len, path, block_table,
+              prefix_lens, k_prefix_blocks, v_prefix_blocks, *, max_nodes: int,
+              new_prefix_lens=None, status=None, stream=None):
+    """tv_commit_kv on the current stream: writes the root and the accepted
+    path of every sequence into the paged pool (k/v_prefix_blocks, in place).
+    Shapes as in include/tv.h; path [B, max_nodes] from accept().
+    Returns (new_prefix_lens, status); nothing is synchronised."""
+    import torch
+    lib = load()
+    _check_dev(k_nodes, v_nodes, parent, node_offsets, accepted_len, path, block_table,
+               prefix_lens, k_prefix_blocks, v_prefix_blocks)
+    total, hkv, d = k_nodes.shape
+    B = int(node_offsets.shape[0] - 1)
+    prm = CommitParams(B, int(hkv), int(d), int(k_prefix_blocks.shape[2]),
+                       int(block_table.shape[1]), int(k_prefix_blocks.shape[0]), int(max_nodes),
+                       int(total))
+    dev = k_nodes.device
+    if new_prefix_lens is None:
+        new_prefix_lens = torch.empty(B, dtype=torch.int32, device=dev)
+    if status is None:
+        status = torch.empty(B, dtype=torch.int32, device=dev)
+    rc = lib.tv_commit_kv(C.byref(prm), _ptr(k_nodes), _ptr(v_nodes), _ptr(parent),
+                          _ptr(node_offsets), _ptr(accepted_len), _ptr(path), _ptr(block_table),
+                          _ptr(prefix_lens), _ptr(k_prefix_blocks), _ptr(v_prefix_blocks),
+                          _ptr(new_prefix_lens), _ptr(status), _stream(stream))
+    if rc != TV_OK:
+        raise TVError(rc, "tv_commit_kv")
+    return new_prefix_lens, status

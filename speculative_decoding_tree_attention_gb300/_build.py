@@ -10,7 +10,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtv.so")
-SOURCES = ["tv_api.cu", "tree_attn_kernel.cu", "accept_kernel.cu", "tv_no_alloc.cu"]
+SOURCES = ["tv_api.cu", "tree_attn_kernel.cu", "accept_kernel.cu", "tv_no_alloc.cu",
+           "commit_kernel.cu"]
 HEADERS = ["tv_device.cuh", "tv_launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

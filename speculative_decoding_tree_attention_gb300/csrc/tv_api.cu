@@ -107,6 +107,7 @@ const char* tv_status_string(int s) {
     case TV_ERR_CUDA: return "TV_ERR_CUDA";
     case TV_ERR_BAD_TREE: return "TV_ERR_BAD_TREE";
     case TV_ERR_DEVICE_TIMEOUT: return "TV_ERR_DEVICE_TIMEOUT";
+    case TV_ERR_NO_PAGE: return "TV_ERR_NO_PAGE";
     default: return "TV_ERR_UNKNOWN";
   }
 }
@@ -244,3 +245,46 @@ int tv_accept(const tv_accept_params* p, const float* target, const float* draft
 }
 
 }  // extern "C"
+
+int tv_commit_kv(const tv_commit_params* p, const uint16_t* k_nodes, const uint16_t* v_nodes,
+                 const int32_t* parent, const int32_t* node_offsets, const int32_t* accepted_len,
+                 const int32_t* path, const int32_t* block_table, const int32_t* prefix_lens,
+                 uint16_t* k_prefix_blocks, uint16_t* v_prefix_blocks, int32_t* new_prefix_lens,
+                 int32_t* status, cudaStream_t stream) {
+  if (!p) return TV_ERR_INVALID_ARG;
+  if (p->head_dim != 64 && p->head_dim != 128) return TV_ERR_UNSUPPORTED;
+  if (p->batch < 1 || p->num_kv_heads < 1 || p->block_size != TV_BLOCK_SIZE ||
+      p->max_blocks_per_seq < 1 || p->num_blocks < 1 || p->max_nodes < 1 ||
+      p->max_nodes > TV_MAX_NODES || p->total_nodes < p->batch)
+    return TV_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(p->num_blocks) * p->num_kv_heads * 16 >= (1ll << 31))
+    return TV_ERR_INVALID_ARG;
+  const void* ptrs[] = {k_nodes, v_nodes, parent, node_offsets, accepted_len, path,
+                        block_table, prefix_lens, k_prefix_blocks, v_prefix_blocks,
+                        new_prefix_lens, status};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return TV_ERR_INVALID_ARG;
+  if (static_cast<const void*>(new_prefix_lens) == static_cast<const void*>(prefix_lens))
+    return TV_ERR_INVALID_ARG;
+  tv::CommitArgs a;
+  a.k_nodes = k_nodes;
+  a.v_nodes = v_nodes;
+  a.parent = parent;
+  a.node_offsets = node_offsets;
+  a.accepted_len = accepted_len;
+  a.path = path;
+  a.block_table = block_table;
+  a.prefix_lens = prefix_lens;
+  a.k_pool = k_prefix_blocks;
+  a.v_pool = v_prefix_blocks;
+  a.new_prefix_lens = new_prefix_lens;
+  a.status = status;
+  a.batch = p->batch;
+  a.hkv = p->num_kv_heads;
+  a.head_dim = p->head_dim;
+  a.max_blocks_per_seq = p->max_blocks_per_seq;
+  a.num_blocks = p->num_blocks;
+  a.max_nodes = p->max_nodes;
+  a.total_nodes = p->total_nodes;
+  return tv::launch_commit(a, stream) == 0 ? TV_OK : TV_ERR_CUDA;
+}

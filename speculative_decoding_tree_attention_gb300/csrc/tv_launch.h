@@ -59,6 +59,24 @@ struct AttnMaps {
 };
 
 int launch_tree_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream);
+
+struct CommitArgs {
+  const uint16_t* k_nodes;    // [total_nodes][Hkv][D]
+  const uint16_t* v_nodes;
+  const int32_t* parent;      // [total_nodes]
+  const int32_t* node_offsets;// [batch+1]
+  const int32_t* accepted_len;// [batch]
+  const int32_t* path;        // [batch][max_nodes]
+  const int32_t* block_table; // [batch][max_blocks_per_seq]
+  const int32_t* prefix_lens; // [batch]
+  uint16_t* k_pool;           // [num_blocks][Hkv][16][D]
+  uint16_t* v_pool;
+  int32_t* new_prefix_lens;   // [batch]
+  int32_t* status;            // [batch]
+  int32_t batch, hkv, head_dim, max_blocks_per_seq, num_blocks, max_nodes, total_nodes;
+};
+
+int launch_commit(const CommitArgs& a, cudaStream_t stream);
 size_t tree_attention_smem_bytes(int head_dim);
 
 }  // namespace tv

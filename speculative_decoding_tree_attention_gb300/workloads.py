@@ -34,7 +34,7 @@ import heapq
 import numpy as np
 
 # stream ids (one per tensor family)
-_S_TREE, _S_Q, _S_KP, _S_VP, _S_KN, _S_VN, _S_TABLE, _S_LEN, _S_ROWS, _S_UNI, _S_GUMBEL = range(11)
+_S_TREE, _S_Q, _S_KP, _S_VP, _S_KN, _S_VN, _S_TABLE, _S_LEN, _S_ROWS, _S_UNI, _S_GUMBEL, _S_EXT = range(12)
 
 CONFIGS = {
     1: dict(name="tiny", batch=1, hq=4, hkv=4, d=64, prefix=(128, 128), tree="binary", n=(15, 15),
@@ -330,3 +330,32 @@ def make_case(cfg: dict, parts=("attn", "accept"), kind: str = "probs") -> dict:
         else:
             case["retained_mask"] = None
     return case
+
+
+def extend_pool(case: dict, extra_tokens: int):
+    """Input preparation for committing an accepted path: a copy of the case's
+    paged pool with fresh pages appended (seeded N(0,1) bf16, so that rows a
+    commit must not touch are distinguishable) and every sequence's
+    block-table row extended so that positions up to L_b + extra_tokens - 1
+    have pages; the new pages are handed out in a shuffled order.  Returns
+    (k_pool, v_pool, block_table): uint16 bf16 bits and int32."""
+    B = case["batch"]
+    lens = np.asarray(case["prefix_lens"], np.int64)
+    table0 = np.asarray(case["block_table"], np.int32)
+    have = (lens + BLOCK_SIZE - 1) // BLOCK_SIZE
+    need = (lens + extra_tokens + BLOCK_SIZE - 1) // BLOCK_SIZE
+    add = int(np.sum(need - have))
+    nb0 = int(case["k_prefix"].shape[0])
+    g = rng(case["cfg"]["seed"], _S_EXT)
+    fresh = nb0 + g.permutation(add).astype(np.int32)
+    shape = (add,) + tuple(case["k_prefix"].shape[1:])
+    k_pool = np.concatenate([case["k_prefix"], to_bf16_bits(g.standard_normal(size=shape))])
+    v_pool = np.concatenate([case["v_prefix"], to_bf16_bits(g.standard_normal(size=shape))])
+    table = np.full((B, max(table0.shape[1], int(need.max()))), -1, np.int32)
+    pos = 0
+    for b in range(B):
+        table[b, : have[b]] = table0[b, : have[b]]
+        k = int(need[b] - have[b])
+        table[b, have[b]: need[b]] = fresh[pos: pos + k]
+        pos += k
+    return k_pool, v_pool, table

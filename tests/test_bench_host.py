@@ -52,3 +52,9 @@ def test_reference_arm_line():
     for k in ("metric", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
               "scaling", "vs_baseline", "dtype", "data"):
         assert k in line
+
+
+def test_percentiles_in_microseconds():
+    p = bench.pct([0.001 * k for k in range(1, 102)])  # 1 .. 101 us, given in ms
+    assert p["p50"] == pytest.approx(51.0)
+    assert p["p10"] == pytest.approx(11.0) and p["p90"] == pytest.approx(91.0)
