@@ -446,6 +446,26 @@ def main():
     stream.synchronize()
     assert int(cm_out[1].max()) == 0, "commit status"
     commit_ms = [a0.elapsed_time(a1) for a0, a1 in evc]
+    # ---- retained set of the draft rows (the step before the accept pass's
+    # renormalisation, for workloads that prune): reported on its own
+    retained = None
+    if cfg.get("mask_mass"):
+        evr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nb)]
+        with torch.cuda.stream(stream):
+            for k in range(nb + 3):
+                flush.fill_(k & 0xFF)
+                if k >= 3:
+                    evr[k - 3][0].record(stream)
+                rmask, _, _, _ = tv.retained_set(d["draft"], float(cfg["mask_mass"]))
+                if k >= 3:
+                    evr[k - 3][1].record(stream)
+        stream.synchronize()
+        assert torch.equal(rmask, d["mask"]), "retained set differs from the workload's masks"
+        r_ms = statistics.mean(a0.elapsed_time(a1) for a0, a1 in evr)
+        r_bytes = tot * int(cfg["vocab"]) * 4 + rmask.numel() * 4
+        retained = {"mean_us": r_ms * 1e3, "rows": tot, "bytes": r_bytes,
+                    "achieved_gbs": r_bytes / (r_ms * 1e-3) / 1e9,
+                    "note": "tv_retained_set of every draft row, timed on its own"}
     commit_tokens = int(acc_out["accepted_len"].sum().item()) + B
     del cm
 
@@ -511,6 +531,7 @@ def main():
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * args.steps,
         "percentiles_us": {"step": pct(step_ms), "attention": pct(attn_ms), "accept": pct(acc_ms)},
+        "retained_set": retained,
         "commit": {"mean_us": statistics.mean(commit_ms) * 1e3, "tokens": commit_tokens,
                    "bytes": commit_tokens * 8 * cfg["hkv"] * cfg["d"],  # K+V rows read and written
                    "note": "tv_commit_kv of the root and accepted path, timed on its own"},

@@ -221,6 +221,36 @@ int tv_accept(const tv_accept_params* params, const float* target, const float* 
               void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ========================================================================
+ * Retained set of the draft rows (the step before the accept pass's pruning
+ * renormalisation; [LLM] §2.1.2 soft truncation by cumulative probability
+ * mass, [LLM] §7.1 the same decision in log space).
+ *
+ * For every row r of draft_probs, with key_v = q_v if q_v > 0 else 0 (NaN
+ * and negatives count as 0) and the fixed-point quantum
+ * f_v = floor(min(key_v, 32) * 2^40) used by tv_accept:
+ *   order the tokens by key desc, id asc; R_r = the shortest prefix of that
+ *   order whose sum of f_v reaches T = floor(mass * 2^40), or every token if
+ *   no prefix does (the crossing token is kept; ties go to the lower id).
+ * Outputs: retained_mask bit v%32 of word v/32 of row r set iff v in R_r
+ * (the layout tv_accept takes), and optionally z_fixed[r] = sum of f_v over
+ * R_r (exact, uint64), z[r] = z_fixed[r] * 2^-40 rounded once to fp32 (the
+ * Z that tv_accept divides by), kept[r] = |R_r|.  Every sum is an exact
+ * integer: the result does not depend on the reduction order.
+ * ====================================================================== */
+typedef struct {
+  int32_t rows;   /* R >= 1                                                */
+  int32_t vocab;  /* V, 1 <= V <= 2^18                                     */
+  float mass;     /* retained mass, 1 - Prune_Ratio: 2^-40 <= mass <= 32   */
+} tv_retain_params; /* host struct */
+
+/* Layouts: draft_probs fp32 [rows][V]; retained_mask uint32 [rows][ceil(V/32)];
+ * z_fixed uint64 [rows], z fp32 [rows], kept int32 [rows] (each optional,
+ * NULL to skip).  Device pointers 16-byte aligned. */
+int tv_retained_set(const tv_retain_params* params, const float* draft_probs,
+                    uint32_t* retained_mask, uint64_t* z_fixed, float* z, int32_t* kept,
+                    cudaStream_t stream);
+
+/* ========================================================================
  * Commit of the accepted path ([MM] §9.1 item 2: the target KV cache is
  * preallocated and tree-node KV is written into it by a scatter kernel;
  * [LLM] §2.3.2: pool slots only for the unique accepted path; [EC] §5.2:

@@ -75,6 +75,10 @@ def _load():
         lib.oracle_scaled_draw.restype = C.c_uint64
         lib.oracle_retained_mass_row.argtypes = [C.c_void_p, C.c_void_p, C.c_int]
         lib.oracle_retained_mass_row.restype = C.c_float
+        lib.oracle_retained_set_row.argtypes = [C.c_void_p, C.c_int, C.c_uint64, C.c_void_p,
+                                                C.POINTER(C.c_uint64), C.POINTER(C.c_float),
+                                                C.POINTER(C.c_int)]
+        lib.oracle_retained_set_row.restype = C.c_int
         _lib = lib
     return _lib
 
@@ -236,3 +240,36 @@ def commit_kv(k_nodes, v_nodes, parent, node_offsets, accepted_len, path, block_
             v_pool[blk, :, (L + t) % 16, :] = v_nodes[n0 + v]
         new_lens[b] = L + a + 1
     return k_pool, v_pool, new_lens, status
+
+
+def retained_threshold(mass: float) -> int:
+    """T = floor(mass * 2^40) for an fp32 mass (exact in fp64)."""
+    return int(np.floor(float(np.float32(mass)) * 2.0 ** 40))
+
+
+def retained_set(q_rows, mass: float):
+    """Retained set of every row of q_rows [R][V] fp32 (see oracle.c,
+    oracle_retained_set_row).  Returns (mask [R][ceil(V/32)] uint32,
+    z_fixed [R] uint64, z [R] fp32 = z_fixed * 2^-40 rounded once, kept [R])."""
+    q = _c(np.atleast_2d(q_rows), np.float32)
+    R, V = q.shape
+    T = retained_threshold(mass)
+    masks = np.zeros((R, (V + 31) // 32), np.uint32)
+    zf = np.zeros(R, np.uint64)
+    z32 = np.zeros(R, np.float32)
+    kept = np.zeros(R, np.int32)
+    lib = _load()
+    for r in range(R):
+        z = C.c_uint64(0)
+        zs = C.c_float(0.0)
+        k = C.c_int(0)
+        row = np.ascontiguousarray(q[r])
+        mrow = np.zeros((V + 31) // 32, np.uint32)
+        if lib.oracle_retained_set_row(_ptr(row), int(V), C.c_uint64(T), _ptr(mrow), C.byref(z),
+                                       C.byref(zs), C.byref(k)) != 0:
+            raise ValueError("oracle_retained_set_row: bad arguments")
+        masks[r] = mrow
+        zf[r] = z.value
+        z32[r] = zs.value
+        kept[r] = k.value
+    return masks, zf, z32, kept

@@ -460,3 +460,56 @@ float oracle_retained_mass_row(const float *q, const uint32_t *mask, int vocab) 
   a.retained_mask = mask;
   return retained_mass(&a, 0);
 }
+
+/* ------------------------------------------------------------------------
+ * oracle_retained_set_row -- the retained set R of one draft row, the step
+ * before the accept pass ([LLM] §2.1.2 "soft truncation" by cumulative
+ * probability mass: tokens in descending draft probability, mass Q summed
+ * until Q >= 1 - Prune_Ratio, the crossing token kept; [LLM] §7.1 the same
+ * decision in log space).  Read exactly: tokens ordered by key desc, id asc,
+ * with key = q if q > 0 else 0 (NaN and negatives count as 0); the set is the
+ * shortest prefix of that order whose exact fixed-point mass sum of
+ * quantise(q) reaches T (T = floor(mass * 2^40) >= 1, computed by the
+ * caller); if no prefix does, every token.  Z = the set's fixed-point sum.
+ * Writes the packed mask (bit v%32 of word v/32), *z_fixed, *z (Z rounded
+ * once to fp32, times 2^-40) and *kept.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  float key;
+  int id;
+} rs_item;
+
+static int rs_cmp(const void *a, const void *b) {
+  const rs_item *x = (const rs_item *)a, *y = (const rs_item *)b;
+  if (x->key > y->key) return -1;
+  if (x->key < y->key) return 1;
+  return (x->id > y->id) - (x->id < y->id);
+}
+
+int oracle_retained_set_row(const float *q, int vocab, uint64_t T, uint32_t *mask,
+                            uint64_t *z_fixed, float *z, int *kept) {
+  if (vocab < 1 || T < 1) return 1;
+  rs_item *it = (rs_item *)malloc(sizeof(rs_item) * (size_t)vocab);
+  if (!it) return 1;
+  for (int v = 0; v < vocab; ++v) {
+    it[v].key = (q[v] > 0.0f) ? q[v] : 0.0f;
+    it[v].id = v;
+  }
+  qsort(it, (size_t)vocab, sizeof(rs_item), rs_cmp);
+  const int words = (vocab + 31) / 32;
+  memset(mask, 0, sizeof(uint32_t) * (size_t)words);
+  uint64_t cum = 0;
+  int n = 0;
+  while (n < vocab) {
+    cum += quantise(it[n].key);
+    const int id = it[n].id;
+    mask[id >> 5] |= 1u << (id & 31);
+    ++n;
+    if (cum >= T) break;
+  }
+  *z_fixed = cum;
+  *z = (float)cum * 0x1p-40f; /* one rounding of the sum, then exact scaling */
+  *kept = n;
+  free(it);
+  return 0;
+}

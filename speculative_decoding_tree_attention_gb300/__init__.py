@@ -10,13 +10,15 @@ PyTorch is used for device memory and the current CUDA stream only.
     tree_attention(...)  -> out, status      (tv_tree_attention)
     accept(...)          -> dict of outputs  (tv_accept)
     commit_kv(...)       -> new_prefix_lens, status (tv_commit_kv)
+    retained_set(...)    -> mask, z_fixed, z, kept (tv_retained_set)
 """
 from __future__ import annotations
 
 import ctypes as C
 import os
 
-__all__ = ["TVError", "load", "tree_attention", "accept", "commit_kv", "attention_workspace_size",
+__all__ = ["TVError", "load", "tree_attention", "accept", "commit_kv", "retained_set",
+           "attention_workspace_size",
            "TV_MAX_NODES", "TV_OK", "TV_ERR_BAD_TREE", "TV_ERR_DEVICE_TIMEOUT", "TV_ERR_NO_PAGE",
            "status_string"]
 
@@ -34,7 +36,8 @@ TV_ERR_NO_PAGE = 7
 TV_MAX_NODES = 512
 TV_BLOCK_SIZE = 16
 EXPORTS = ("tv_status_string", "tv_version", "tv_tree_attention_workspace_size",
-           "tv_tree_attention", "tv_accept_workspace_size", "tv_accept", "tv_commit_kv")
+           "tv_tree_attention", "tv_accept_workspace_size", "tv_accept", "tv_commit_kv",
+           "tv_retained_set")
 
 
 class TVError(RuntimeError):
@@ -54,6 +57,10 @@ class AttnParams(C.Structure):
 class AcceptParams(C.Structure):
     _fields_ = [("batch", C.c_int32), ("vocab", C.c_int32), ("max_nodes", C.c_int32),
                 ("total_nodes", C.c_int32), ("kind", C.c_int32)]
+
+
+class RetainParams(C.Structure):
+    _fields_ = [("rows", C.c_int32), ("vocab", C.c_int32), ("mass", C.c_float)]
 
 
 class CommitParams(C.Structure):
@@ -91,6 +98,8 @@ def load(path: str | None = None) -> C.CDLL:
     lib.tv_tree_attention_no_alloc.restype = C.c_int
     lib.tv_commit_kv.argtypes = [C.POINTER(CommitParams)] + [vp] * 12 + [vp]
     lib.tv_commit_kv.restype = C.c_int
+    lib.tv_retained_set.argtypes = [C.POINTER(RetainParams)] + [vp] * 5 + [vp]
+    lib.tv_retained_set.restype = C.c_int
     if path is None:
         _lib = lib
     return lib
@@ -270,3 +279,29 @@ def commit_kv(k_nodes, v_nodes, parent, node_offsets, accepted_len, path, block_
     if rc != TV_OK:
         raise TVError(rc, "tv_commit_kv")
     return new_prefix_lens, status
+
+
+def retained_set(draft_probs, mass: float, *, mask=None, z_fixed=None, z=None, kept=None,
+                 stream=None):
+    """tv_retained_set on the current stream: draft_probs [R, V] fp32.
+    Returns (mask [R, ceil(V/32)] int32 bit patterns, z_fixed [R] int64
+    (uint64 bits), z [R] fp32, kept [R] int32); nothing is synchronised."""
+    import torch
+    lib = load()
+    _check_dev(draft_probs)
+    R, V = draft_probs.shape
+    dev = draft_probs.device
+    if mask is None:
+        mask = torch.empty(R, (V + 31) // 32, dtype=torch.int32, device=dev)
+    if z_fixed is None:
+        z_fixed = torch.empty(R, dtype=torch.int64, device=dev)
+    if z is None:
+        z = torch.empty(R, dtype=torch.float32, device=dev)
+    if kept is None:
+        kept = torch.empty(R, dtype=torch.int32, device=dev)
+    prm = RetainParams(int(R), int(V), float(mass))
+    rc = lib.tv_retained_set(C.byref(prm), _ptr(draft_probs), _ptr(mask), _ptr(z_fixed), _ptr(z),
+                             _ptr(kept), _stream(stream))
+    if rc != TV_OK:
+        raise TVError(rc, "tv_retained_set")
+    return mask, z_fixed, z, kept

@@ -672,6 +672,281 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
   cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
+
+// ============================================================ retained set
+// The step before the accept pass: the retained set R of each draft row
+// ([LLM] §2.1.2: tokens by descending draft probability, mass summed until it
+// reaches 1 - Prune_Ratio, the crossing token kept; [LLM] §7.1 the same in log
+// space), read exactly: order = key desc, id asc with key = q if q > 0 else 0;
+// R = the shortest prefix of that order whose fixed-point mass sum of fix40
+// quanta reaches T (the caller's floor(mass * 2^40)), or the whole row.
+//
+// One cluster of C CTAs per row; thread t of rank k owns the 32 entries of
+// mask word k*512 + t.  Each thread sorts its 32 (key, id) pairs in registers
+// (key = the fp32 bit pattern, which orders non-negative floats; key desc, id
+// asc), so that the entries of one digit form runs.  A radix select over the
+// key, 8 bits a pass from the top, finds the key tau at which the cumulative
+// mass crosses T: each pass adds the quanta of the matching entries into
+// per-warp 256-bucket histograms with one atomic per run, the CTA histograms
+// are added over the cluster through distributed shared memory, and a suffix
+// scan picks the crossing digit.  Keys above tau are kept; of the keys equal
+// to tau, the c lowest ids with c = ceil((T - mass above tau) / fix40(tau)),
+// ranked by a block scan plus the cluster prefix of the per-CTA tie counts.
+// Every sum is an exact integer, so every CTA of the cluster takes the same
+// decisions.
+constexpr int kRsThreads = 512;
+constexpr int kRsWarps = kRsThreads / 32;
+constexpr int kRsChunk = kRsThreads * 32;  // entries per CTA: one mask word per thread
+constexpr int kRsMaxCluster = 16;
+
+struct RsSmem {
+  uint32_t key[kRsChunk + kRsThreads];          // padded: entry i at i + i/32
+  unsigned long long whist[kRsWarps][256];      // per-warp digit histograms
+  unsigned long long slot[4][256];              // this CTA's histogram of pass p
+  unsigned long long red[kRsWarps];
+  unsigned long long x_total, x_gt_count;       // cluster exchange slots
+  int x_ties;
+  int scan[kRsWarps];
+  int digit;
+  unsigned long long above;
+};
+
+// fix40 of the float whose bit pattern is `key` (a q > 0, or 0), in integer
+// arithmetic: a normal q is m * 2^(e - 150) with m the 24-bit significand and
+// e the exponent field, so q * 2^40 = m * 2^(e - 110) and its floor is a
+// shift of m; q >= 32 (and +inf) clamps to 32 * 2^40; denormals give 0.
+__device__ __forceinline__ unsigned long long rs_weight(uint32_t key) {
+  if (key >= 0x42000000u) return 1ull << 45;
+  const uint32_t e = key >> 23;
+  const unsigned long long m = (key & 0x7fffffu) | (e ? 0x800000u : 0u);
+  const int sh = static_cast<int>(e) - 110;
+  return sh >= 0 ? (m << sh) : (sh > -32 ? (m >> -sh) : 0ull);
+}
+
+__global__ void __launch_bounds__(kRsThreads, 1)
+    retained_set_kernel(const RetainArgs a) {
+  extern __shared__ __align__(16) uint8_t rs_raw[];
+  RsSmem& sm = *reinterpret_cast<RsSmem*>(rs_raw);
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int row = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int V = a.vocab;
+  const int lo = rank * kRsChunk;
+  const float* q = a.draft + static_cast<size_t>(row) * V;
+
+  // keys into shared memory (coalesced loads, all 32 of a thread in flight)
+  {
+    float xv[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const int v = lo + tid + r * kRsThreads;
+      xv[r] = v < V ? __ldg(q + v) : 0.0f;
+    }
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const int i = tid + r * kRsThreads;
+      sm.key[i + (i >> 5)] = (xv[r] > 0.0f) ? __float_as_uint(xv[r]) : 0u;
+    }
+  }
+  __syncthreads();
+  // this thread's 32 entries as (key << 5 | 31 - j), sorted descending: key
+  // desc, then id asc
+  unsigned long long e[32];
+  unsigned long long mine = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t k = sm.key[tid * 33 + j];
+    e[j] = (static_cast<unsigned long long>(k) << 5) | static_cast<unsigned long long>(31 - j);
+    mine += rs_weight(k);
+  }
+#pragma unroll
+  for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int l = i ^ jj;
+        if (l > i) {
+          const bool desc = (i & kk) == 0;
+          const unsigned long long x = e[i], y = e[l];
+          const bool sw = desc ? (x < y) : (x > y);
+          e[i] = sw ? y : x;
+          e[l] = sw ? x : y;
+        }
+      }
+    }
+  }
+  // total mass of the row
+  for (int o = 16; o; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) sm.red[warp] = mine;
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long t = 0;
+    for (int w = 0; w < kRsWarps; ++w) t += sm.red[w];
+    sm.x_total = t;
+  }
+  cluster.sync();
+  unsigned long long total = lane < C ? *cluster.map_shared_rank(&sm.x_total, lane) : 0ull;
+  for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+  const unsigned long long T = a.threshold;
+  const int words = (V + 31) >> 5;
+  uint32_t* mrow = a.mask + static_cast<size_t>(row) * words;
+  const int word = rank * kRsThreads + tid;  // this thread's mask word
+
+  if (total < T) {  // the mass never reaches T: every token is kept
+    if (word < words) {
+      const int v0 = word * 32;
+      mrow[word] = (V - v0 >= 32) ? 0xffffffffu : ((1u << (V - v0)) - 1u);
+    }
+    if (rank == 0 && tid == 0) {
+      if (a.z_fixed) a.z_fixed[row] = total;
+      if (a.z) a.z[row] = __fmul_rn(__ull2float_rn(total), kTwoM40);
+      if (a.kept) a.kept[row] = V;
+    }
+    cluster.sync();  // no CTA leaves while another may read its slots
+    return;
+  }
+
+  // radix select: the key tau at which the cumulative mass (keys in
+  // descending order) first reaches T
+  uint32_t prefix = 0;
+  unsigned long long above = 0;  // mass of the keys above the current prefix range
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < kRsWarps * 256; i += kRsThreads) (&sm.whist[0][0])[i] = 0ull;
+    __syncthreads();
+    // matching entries are contiguous in the sorted order, and so are the
+    // entries of one digit: one atomic per run
+    uint32_t cur = 256u;
+    unsigned long long acc = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t k = static_cast<uint32_t>(e[j] >> 5);
+      if (pass == 0 || (k >> (shift + 8)) == prefix) {
+        const unsigned long long w = rs_weight(k);
+        const uint32_t d = (k >> shift) & 255u;
+        if (d != cur) {
+          if (acc) atomicAdd(&sm.whist[warp][cur], acc);
+          cur = d;
+          acc = 0;
+        }
+        acc += w;
+      }
+    }
+    if (acc) atomicAdd(&sm.whist[warp][cur], acc);
+    __syncthreads();
+    if (tid < 256) {
+      unsigned long long h = 0;
+      for (int w = 0; w < kRsWarps; ++w) h += sm.whist[w][tid];
+      sm.slot[pass][tid] = h;
+    }
+    cluster.sync();
+    // digit d = tid (< 256): cluster histogram H[d] and the suffix mass above d
+    unsigned long long H = 0;
+    if (tid < 256)
+      for (int c = 0; c < C; ++c) H += cluster.map_shared_rank(&sm.slot[pass][0], c)[tid];
+    // suffix sums over the 256 digits, descending: warps 0-7 hold digits
+    // 32w .. 32w+31; first within the warp, then across the 8 warps
+    unsigned long long incl = H;  // sum over digits >= d within the warp
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_down_sync(0xffffffffu, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    if (tid < 256 && lane == 0) sm.red[warp] = incl;  // warp totals
+    __syncthreads();
+    if (tid < 256) {
+      unsigned long long higher = 0;  // digits of the warps above
+      for (int w = warp + 1; w < 8; ++w) higher += sm.red[w];
+      const unsigned long long ge = above + higher + incl;  // mass of digits >= d
+      const unsigned long long gt = ge - H;                 // mass of digits > d
+      if (gt < T && ge >= T) {
+        sm.digit = tid;
+        sm.above = gt;
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << 8) | static_cast<uint32_t>(sm.digit);
+    above = sm.above;
+    __syncthreads();  // sm.red / sm.digit are rewritten next pass
+  }
+  const uint32_t tau = prefix;
+  const unsigned long long wt = rs_weight(tau);  // > 0: the crossing adds mass
+  const unsigned long long need = (T - above + wt - 1) / wt;  // ties to keep
+
+  // ranks of the ties (key == tau) in id order: the thread's ties are in id
+  // order already; block scan of the per-thread counts, plus the counts of
+  // the lower-ranked CTAs of the cluster
+  int nt = 0, ngt = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t k = static_cast<uint32_t>(e[j] >> 5);
+    nt += k == tau;
+    ngt += k > tau;
+  }
+  int incl_t = nt;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl_t, o);
+    if (lane >= o) incl_t += y;
+  }
+  int gtw = ngt;
+  for (int o = 16; o; o >>= 1) gtw += __shfl_xor_sync(0xffffffffu, gtw, o);
+  if (lane == 31) sm.scan[warp] = incl_t;
+  if (lane == 0) sm.red[warp] = static_cast<unsigned long long>(gtw);
+  __syncthreads();
+  int before = incl_t - nt;
+  for (int w = 0; w < warp; ++w) before += sm.scan[w];
+  if (tid == 0) {
+    int ties = 0;
+    unsigned long long g = 0;
+    for (int w = 0; w < kRsWarps; ++w) {
+      ties += sm.scan[w];
+      g += sm.red[w];
+    }
+    sm.x_ties = ties;
+    sm.x_gt_count = g;
+  }
+  cluster.sync();
+  int ties_below = 0;
+  unsigned long long n_gt = 0;
+  {
+    const int t = lane < C ? *cluster.map_shared_rank(&sm.x_ties, lane) : 0;
+    const unsigned long long g = lane < C ? *cluster.map_shared_rank(&sm.x_gt_count, lane) : 0ull;
+    int tb = lane < rank ? t : 0;
+    n_gt = g;
+    for (int o = 16; o; o >>= 1) {
+      tb += __shfl_xor_sync(0xffffffffu, tb, o);
+      n_gt += __shfl_xor_sync(0xffffffffu, n_gt, o);
+    }
+    ties_below = tb;
+  }
+  // this thread's mask word, from the sorted entries (bit = id within word)
+  if (word < words) {
+    uint32_t m = 0;
+    int r = ties_below + before;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t k = static_cast<uint32_t>(e[j] >> 5);
+      const int id = 31 - static_cast<int>(e[j] & 31ull);
+      bool keep = k > tau;
+      if (k == tau) {
+        keep = static_cast<unsigned long long>(r) < need;
+        ++r;
+      }
+      if (keep) m |= 1u << id;
+    }
+    if (V - word * 32 < 32) m &= (1u << (V - word * 32)) - 1u;  // no bits past the row
+    mrow[word] = m;
+  }
+  if (rank == 0 && tid == 0) {
+    const unsigned long long Z = above + need * wt;
+    if (a.z_fixed) a.z_fixed[row] = Z;
+    if (a.z) a.z[row] = __fmul_rn(__ull2float_rn(Z), kTwoM40);
+    if (a.kept) a.kept[row] = static_cast<int>(n_gt + need);
+  }
+  cluster.sync();  // no CTA leaves while another may read its slots
+}
 }  // namespace
 
 int accept_chunks(int vocab) { return (vocab + kChunk - 1) / kChunk; }
@@ -732,5 +1007,35 @@ size_t accept_workspace_bytes(int vocab, int total_nodes) {
 }
 
 int accept_max_nodes() { return kMaxN; }
+
+int retained_cluster_size(int vocab) { return (vocab + kRsChunk - 1) / kRsChunk; }
+
+int launch_retained_set(const RetainArgs& a, cudaStream_t stream) {
+  const int C = retained_cluster_size(a.vocab);
+  if (C < 1 || C > kRsMaxCluster) return -1;
+  static thread_local int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    cudaFuncSetAttribute(retained_set_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaFuncSetAttribute(retained_set_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(sizeof(RsSmem)));
+    attr_dev = dev;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, a.rows, 1);
+  cfg.blockDim = dim3(kRsThreads, 1, 1);
+  cfg.dynamicSmemBytes = sizeof(RsSmem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, retained_set_kernel, a) == cudaSuccess ? 0 : -1;
+}
+
 
 }  // namespace tv

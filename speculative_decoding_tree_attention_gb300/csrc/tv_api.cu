@@ -288,3 +288,25 @@ int tv_commit_kv(const tv_commit_params* p, const uint16_t* k_nodes, const uint1
   a.total_nodes = p->total_nodes;
   return tv::launch_commit(a, stream) == 0 ? TV_OK : TV_ERR_CUDA;
 }
+
+int tv_retained_set(const tv_retain_params* p, const float* draft_probs, uint32_t* retained_mask,
+                    uint64_t* z_fixed, float* z, int32_t* kept, cudaStream_t stream) {
+  if (!p || p->rows < 1 || p->rows > 65535 || p->vocab < 1 || p->vocab > (1 << 18))
+    return TV_ERR_INVALID_ARG;
+  if (!(p->mass >= 0x1p-40f && p->mass <= 32.0f)) return TV_ERR_INVALID_ARG;  // NaN fails too
+  if (!draft_probs || !retained_mask || !aligned16(draft_probs) || !aligned16(retained_mask))
+    return TV_ERR_INVALID_ARG;
+  if ((z_fixed && !aligned16(z_fixed)) || (z && !aligned16(z)) || (kept && !aligned16(kept)))
+    return TV_ERR_INVALID_ARG;
+  tv::RetainArgs a;
+  a.draft = draft_probs;
+  a.mask = retained_mask;
+  a.z_fixed = reinterpret_cast<unsigned long long*>(z_fixed);
+  a.z = z;
+  a.kept = kept;
+  a.threshold = static_cast<unsigned long long>(std::floor(static_cast<double>(p->mass) * 0x1p40));
+  a.rows = p->rows;
+  a.vocab = p->vocab;
+  if (a.threshold < 1) return TV_ERR_INVALID_ARG;
+  return tv::launch_retained_set(a, stream) == 0 ? TV_OK : TV_ERR_CUDA;
+}

@@ -32,6 +32,20 @@ struct AcceptArgs {
 // must be accept_workspace_bytes() long when the input is logits or a mask
 // is given (it is not touched otherwise).
 int launch_accept(const AcceptArgs& a, void* workspace, cudaStream_t stream);
+
+struct RetainArgs {
+  const float* draft;          // [rows][vocab]
+  uint32_t* mask;              // [rows][ceil(vocab/32)]
+  unsigned long long* z_fixed; // [rows] or null
+  float* z;                    // [rows] or null
+  int32_t* kept;               // [rows] or null
+  unsigned long long threshold;// T = floor(mass * 2^40) >= 1
+  int32_t rows, vocab;
+};
+
+// Retained set of every row (one cluster of CTAs per row).
+int launch_retained_set(const RetainArgs& a, cudaStream_t stream);
+int retained_cluster_size(int vocab);
 size_t accept_workspace_bytes(int vocab, int total_nodes);
 int accept_cluster_size(int vocab);
 int accept_max_nodes();

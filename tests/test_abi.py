@@ -116,3 +116,34 @@ def test_accept_logits_without_workspace_is_refused(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(OSError):
         tv.load(str(tmp_path / "missing_libtv.so"))
+
+
+@pytest.mark.parametrize("bad", [dict(rows=0), dict(vocab=0), dict(vocab=(1 << 18) + 1),
+                                 dict(mass=0.0), dict(mass=float("nan")), dict(mass=33.0),
+                                 dict(mass=1e-13)])
+def test_retained_set_argument_errors_before_launch(lib, bad):
+    base = dict(rows=4, vocab=1000, mass=0.7)
+    base.update(bad)
+    p = tv.RetainParams(**base)
+    dummy = C.c_void_p(4096)
+    assert lib.tv_retained_set(C.byref(p), dummy, dummy, None, None, None, None) == \
+        tv.TV_ERR_INVALID_ARG
+
+
+def test_commit_argument_errors_before_launch(lib):
+    dummy = C.c_void_p(4096)
+    args = [dummy] * 12
+    ok = dict(batch=2, num_kv_heads=2, head_dim=128, block_size=16, max_blocks_per_seq=8,
+              num_blocks=16, max_nodes=16, total_nodes=20)
+    for bad in (dict(batch=0), dict(block_size=8), dict(max_nodes=600), dict(total_nodes=1)):
+        p = tv.CommitParams(**dict(ok, **bad))
+        assert lib.tv_commit_kv(C.byref(p), *args, None) == tv.TV_ERR_INVALID_ARG
+    p = tv.CommitParams(**dict(ok, head_dim=96))
+    assert lib.tv_commit_kv(C.byref(p), *args, None) == tv.TV_ERR_UNSUPPORTED
+    # new_prefix_lens aliasing prefix_lens is refused
+    p = tv.CommitParams(**ok)
+    aliased = list(args)
+    aliased[7] = C.c_void_p(8192)
+    aliased[10] = C.c_void_p(8192)
+    assert lib.tv_commit_kv(C.byref(p), *aliased, None) == tv.TV_ERR_INVALID_ARG
+    assert tv.status_string(tv.TV_ERR_NO_PAGE) == "TV_ERR_NO_PAGE"
