@@ -220,6 +220,34 @@ int tv_accept(const tv_accept_params* params, const float* target, const float* 
               int32_t* path, int32_t* bonus_token, int32_t* status, float* debug_pq,
               void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Accept-test variants (tv_accept_ex; tv_accept is tv_accept_ex with NULL
+ * options, i.e. TV_TEST_RATIO and no calibration factor):
+ *   TV_TEST_RATIO      a_i = fl32(u_i * q~) < fl32(gamma_b * p~): the test
+ *                      u < min(1, gamma * p/q) with the calibration factor of
+ *                      [MM] §3.3 (gamma = exp(-lambda KL) computed by the
+ *                      caller, one per sequence; gamma = 1 is the plain test).
+ *   TV_TEST_LOG_CLAMP  the log-space test of [LLM] §10.2:
+ *                      r = clamp(log p~ - log q~ + log gamma_b, -L, L) in fp32,
+ *                      a_i = u_i < (r >= 0 ? 1 : exp(r)); p~ = 0 or a NaN r
+ *                      rejects (a pruned token never passes).
+ * The walk and the bonus draw are unchanged (the residual max(0, p~ - q~)).
+ * gamma: device fp32 [batch] or NULL (1); a gamma_b that is not a positive
+ * finite number gives that sequence TV_ERR_BAD_TREE.  log_clamp: L, 0 => 20. */
+typedef enum { TV_TEST_RATIO = 0, TV_TEST_LOG_CLAMP = 1 } tv_accept_test;
+
+typedef struct {
+  int32_t test;        /* tv_accept_test                                 */
+  float log_clamp;     /* L for TV_TEST_LOG_CLAMP, 0 => 20; at most 88    */
+  const float* gamma;  /* device fp32 [batch] calibration factors, or NULL */
+} tv_accept_options;   /* host struct */
+
+int tv_accept_ex(const tv_accept_params* params, const tv_accept_options* options,
+                 const float* target, const float* draft_probs, const int32_t* draft_tokens,
+                 const int32_t* parent, const int32_t* node_offsets, const float* uniforms,
+                 const uint32_t* retained_mask, int32_t* accepted_len, int32_t* path,
+                 int32_t* bonus_token, int32_t* status, float* debug_pq, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream);
+
 /* ========================================================================
  * Retained set of the draft rows (the step before the accept pass's pruning
  * renormalisation; [LLM] §2.1.2 soft truncation by cumulative probability

@@ -57,6 +57,7 @@ class _AcceptArgs(C.Structure):
         ("retained_mask", C.c_void_p),
         ("accepted_len", C.c_void_p), ("path", C.c_void_p), ("bonus_token", C.c_void_p),
         ("status", C.c_void_p), ("pq_out", C.c_void_p),
+        ("test", C.c_int), ("log_clamp", C.c_float), ("gamma", C.c_void_p),
     ]
 
 
@@ -137,8 +138,11 @@ def tree_attention(case: dict, nthreads: int | None = None) -> np.ndarray:
     return out.reshape(tot, case["num_q_heads"], case["head_dim"])
 
 
-def accept(case: dict, nthreads: int | None = None, want_pq: bool = True) -> dict:
-    """Oracle accept pass.  Returns accepted_len, path, bonus_token, status, pq."""
+def accept(case: dict, nthreads: int | None = None, want_pq: bool = True, test: int = 0,
+           log_clamp: float = 20.0, gamma=None) -> dict:
+    """Oracle accept pass.  Returns accepted_len, path, bonus_token, status, pq.
+    test 0: ratio test with calibration factors `gamma` ([batch] fp32, None = 1);
+    test 1: the log-space clamped test with bound `log_clamp`."""
     lib = _load()
     off = _c(case["node_offsets"], np.int32)
     batch = off.shape[0] - 1
@@ -151,6 +155,7 @@ def accept(case: dict, nthreads: int | None = None, want_pq: bool = True) -> dic
         "parent": _c(case["parent"], np.int32),
         "uniforms": _c(case["uniforms"], np.float32),
         "retained_mask": _c(case.get("retained_mask"), np.uint32),
+        "gamma": None if gamma is None else _c(gamma, np.float32),
     }
     out = {
         "accepted_len": np.zeros(batch, np.int32),
@@ -165,7 +170,8 @@ def accept(case: dict, nthreads: int | None = None, want_pq: bool = True) -> dic
                        _ptr(keep["parent"]), _ptr(off), _ptr(keep["uniforms"]),
                        _ptr(keep["retained_mask"]),
                        _ptr(out["accepted_len"]), _ptr(out["path"]), _ptr(out["bonus_token"]),
-                       _ptr(out["status"]), _ptr(out["pq"]))
+                       _ptr(out["status"]), _ptr(out["pq"]), int(test), float(log_clamp),
+                       _ptr(keep["gamma"]))
     rc = lib.oracle_accept(C.byref(args), int(nthreads or default_threads()))
     if rc != 0:
         raise ValueError("oracle_accept: unsupported arguments")

@@ -35,7 +35,9 @@
  *          log(1/Z) on R, -inf elsewhere).  Z_j is the exact sum of the draft
  *          probabilities quantised to 2^-40, rounded once to fp32.
  *       3. per-node test u < min(1, p/q) ([EC] §2.2.3 step 1-2), evaluated as
- *          fl32(u*q) < p (strict; NaN rejects).
+ *          fl32(u*q) < p (strict; NaN rejects); variants: a calibration
+ *          factor g, fl32(u*q) < fl32(g*p) ([MM] §3.3), and the log-space
+ *          clamped test of [LLM] §10.2 (fp32, as the page states it).
  *       4. literal walk: depth-first from the root, children in increasing
  *          index order, descending only into accepted children ([EC] §2.2.3
  *          step 3: cut at the first rejection, keep the longest accepted
@@ -210,6 +212,9 @@ typedef struct {
   int32_t *bonus_token;         /* [batch] */
   int32_t *status;              /* [batch] */
   float *pq_out;                /* NULL or [total_nodes][2] */
+  int test;                     /* 0: ratio test, 1: log-space clamped test */
+  float log_clamp;              /* L of the clamped test */
+  const float *gamma;           /* NULL or [batch] calibration factors */
 } oracle_accept_args;
 
 static const double TWO40 = 1099511627776.0; /* 2^40 */
@@ -303,6 +308,8 @@ static void accept_one_tree(const oracle_accept_args *a, int b) {
   /* validation of the tree and the tokens */
   int bad = (N < 1 || N > a->max_nodes);
   if (!bad && par[0] != -1) bad = 1;
+  const float g = a->gamma ? a->gamma[b] : 1.0f;
+  if (!(g > 0.0f && g <= 3.0e38f)) bad = 1; /* the calibration factor must be positive, finite */
   for (int i = 1; !bad && i < N; ++i)
     if (par[i] < 0 || par[i] >= i || tok[i] < 0 || tok[i] >= V) bad = 1;
   if (bad) {
@@ -343,8 +350,24 @@ static void accept_one_tree(const oracle_accept_args *a, int b) {
     }
     pt[i] = p;
     qt[i] = q;
-    float uq = a->uniforms[n0 + i] * q; /* one fp32 rounding */
-    acc[i] = (unsigned char)(uq < p);
+    const float u = a->uniforms[n0 + i];
+    if (a->test == 0) {
+      /* u < min(1, g p/q) ([MM] §3.3 calibration factor g; g = 1 is the
+       * plain test), as fl32(u q) < fl32(g p) */
+      float uq = u * q;
+      float gp = g * p;
+      acc[i] = (unsigned char)(uq < gp);
+    } else {
+      /* [LLM] §10.2 log-space test: r = clamp(log p - log q + log g, -L, L),
+       * accept iff u < (r >= 0 ? 1 : exp(r)); p = 0 or a NaN r rejects */
+      float r = (logf(p) - logf(q)) + logf(g);
+      if (!(p > 0.0f) || r != r) {
+        acc[i] = 0;
+      } else {
+        float rc = fmaxf(fminf(r, a->log_clamp), -a->log_clamp);
+        acc[i] = (unsigned char)(u < (rc >= 0.0f ? 1.0f : expf(rc)));
+      }
+    }
   }
   if (a->pq_out) {
     a->pq_out[2 * (size_t)n0 + 0] = 0.0f;

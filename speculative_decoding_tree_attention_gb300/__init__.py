@@ -36,7 +36,8 @@ TV_ERR_NO_PAGE = 7
 TV_MAX_NODES = 512
 TV_BLOCK_SIZE = 16
 EXPORTS = ("tv_status_string", "tv_version", "tv_tree_attention_workspace_size",
-           "tv_tree_attention", "tv_accept_workspace_size", "tv_accept", "tv_commit_kv",
+           "tv_tree_attention", "tv_accept_workspace_size", "tv_accept", "tv_accept_ex",
+           "tv_commit_kv",
            "tv_retained_set")
 
 
@@ -57,6 +58,10 @@ class AttnParams(C.Structure):
 class AcceptParams(C.Structure):
     _fields_ = [("batch", C.c_int32), ("vocab", C.c_int32), ("max_nodes", C.c_int32),
                 ("total_nodes", C.c_int32), ("kind", C.c_int32)]
+
+
+class AcceptOptions(C.Structure):
+    _fields_ = [("test", C.c_int32), ("log_clamp", C.c_float), ("gamma", C.c_void_p)]
 
 
 class RetainParams(C.Structure):
@@ -94,6 +99,8 @@ def load(path: str | None = None) -> C.CDLL:
     lib.tv_accept_workspace_size.restype = sz
     lib.tv_accept.argtypes = [C.POINTER(AcceptParams)] + [vp] * 12 + [vp, sz, vp]
     lib.tv_accept.restype = C.c_int
+    lib.tv_accept_ex.argtypes = [C.POINTER(AcceptParams), C.c_void_p] + [vp] * 12 + [vp, sz, vp]
+    lib.tv_accept_ex.restype = C.c_int
     lib.tv_tree_attention_no_alloc.argtypes = [C.POINTER(AttnParams)] + [vp] * 11 + [vp]
     lib.tv_tree_attention_no_alloc.restype = C.c_int
     lib.tv_commit_kv.argtypes = [C.POINTER(CommitParams)] + [vp] * 12 + [vp]
@@ -208,10 +215,14 @@ def tree_attention_no_alloc(q_nodes, k_prefix_blocks, v_prefix_blocks, block_tab
 
 def accept(target, draft_probs, draft_tokens, parent, node_offsets, uniforms,
            retained_mask=None, *, max_nodes: int, kind: str = "probs", debug_pq: bool = False,
-           outputs: dict | None = None, stream=None) -> dict:
-    """tv_accept on the current stream.  target/draft_probs [total, V] fp32,
+           outputs: dict | None = None, stream=None, test: str = "ratio", log_clamp: float = 0.0,
+           gamma=None) -> dict:
+    """tv_accept_ex on the current stream.  target/draft_probs [total, V] fp32,
     draft_tokens/parent [total] int32, node_offsets [B+1] int32, uniforms
     [total] fp32, retained_mask [total, ceil(V/32)] int32/uint32 or None.
+    test: "ratio" (fl32(u q~) < fl32(gamma p~)) or "log_clamp" (the clamped
+    log-space test, bound log_clamp, 0 => 20); gamma: [B] fp32 CUDA tensor of
+    calibration factors or None (1).
     Returns dict(accepted_len, path, bonus_token, status, debug_pq)."""
     import torch
     lib = load()
@@ -242,7 +253,12 @@ def accept(target, draft_probs, draft_tokens, parent, node_offsets, uniforms,
         need = int(lib.tv_accept_workspace_size(C.byref(prm)))
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
-    rc = lib.tv_accept(C.byref(prm), _ptr(target), _ptr(draft_probs), _ptr(draft_tokens),
+    _check_dev(gamma)
+    if test not in ("ratio", "log_clamp"):
+        raise ValueError("test must be 'ratio' or 'log_clamp'")
+    opts = AcceptOptions(0 if test == "ratio" else 1, float(log_clamp),
+                         None if gamma is None else gamma.data_ptr())
+    rc = lib.tv_accept_ex(C.byref(prm), C.byref(opts), _ptr(target), _ptr(draft_probs), _ptr(draft_tokens),
                        _ptr(parent), _ptr(node_offsets), _ptr(uniforms), _ptr(retained_mask),
                        _ptr(acc), _ptr(path), _ptr(bonus), _ptr(status), _ptr(dpq), _ptr(ws),
                        C.c_size_t(ws_bytes), _stream(stream))

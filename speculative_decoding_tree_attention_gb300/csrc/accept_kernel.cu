@@ -364,7 +364,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
 
   // ---------------------------------------------------------------- tree
   if (tid == 0)
-    sm.bad = (N < 1 || N > a.max_nodes || N > kMaxN || n0 < 0 || n0 + N > a.total_nodes) ? 1 : 0;
+    sm.bad = (N < 1 || N > a.max_nodes || N > kMaxN || n0 < 0 || n0 + N > a.total_nodes ||
+              (a.gamma && !(a.gamma[b] > 0.0f && a.gamma[b] <= 3.0e38f))) ? 1 : 0;
   __syncthreads();
   if (!sm.bad) {
     for (int i = tid; i < N; i += kTreeThreads) {
@@ -451,7 +452,22 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
       }
       my_p = p;
       my_q = q;
-      acc = __fmul_rn(sm.u[i], q) < p;
+      const float u = sm.u[i];
+      const float g = a.gamma ? a.gamma[b] : 1.0f;
+      if (a.test == 0) {
+        // u < min(1, g * p~ / q~) as fl32(u * q~) < fl32(g * p~)
+        acc = __fmul_rn(u, q) < __fmul_rn(g, p);
+      } else {
+        // log space with a clamp: r = clamp(log p~ - log q~ + log g, -L, L),
+        // accept iff u < (r >= 0 ? 1 : exp(r)); p~ = 0 or a NaN ratio rejects
+        const float r = (logf(p) - logf(q)) + logf(g);
+        if (!(p > 0.0f) || r != r) {
+          acc = false;
+        } else {
+          const float rc = fmaxf(fminf(r, a.log_clamp), -a.log_clamp);
+          acc = u < (rc >= 0.0f ? 1.0f : expf(rc));
+        }
+      }
     }
     const uint32_t bal = __ballot_sync(0xffffffffu, acc);
     if ((tid & 31) == 0) sm.acc_bits[tid >> 5] = bal;

@@ -205,7 +205,21 @@ int tv_accept(const tv_accept_params* p, const float* target, const float* draft
               const float* uniforms, const uint32_t* retained_mask, int32_t* accepted_len,
               int32_t* path, int32_t* bonus_token, int32_t* status, float* debug_pq,
               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return tv_accept_ex(p, nullptr, target, draft_probs, draft_tokens, parent, node_offsets,
+                      uniforms, retained_mask, accepted_len, path, bonus_token, status, debug_pq,
+                      workspace, workspace_bytes, stream);
+}
+
+int tv_accept_ex(const tv_accept_params* p, const tv_accept_options* opt, const float* target,
+                 const float* draft_probs, const int32_t* draft_tokens, const int32_t* parent,
+                 const int32_t* node_offsets, const float* uniforms,
+                 const uint32_t* retained_mask, int32_t* accepted_len, int32_t* path,
+                 int32_t* bonus_token, int32_t* status, float* debug_pq, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream) {
   if (!p) return TV_ERR_INVALID_ARG;
+  if (opt && opt->test != TV_TEST_RATIO && opt->test != TV_TEST_LOG_CLAMP) return TV_ERR_INVALID_ARG;
+  if (opt && !(opt->log_clamp >= 0.0f && opt->log_clamp <= 88.0f)) return TV_ERR_INVALID_ARG;
+  if (opt && opt->gamma && !aligned16(opt->gamma)) return TV_ERR_INVALID_ARG;
   if (p->batch < 1 || p->vocab < 1 || p->vocab >= (1 << 18)) return TV_ERR_INVALID_ARG;
   if (p->max_nodes < 1 || p->max_nodes > TV_MAX_NODES || p->max_nodes > tv::accept_max_nodes())
     return TV_ERR_INVALID_ARG;
@@ -235,6 +249,9 @@ int tv_accept(const tv_accept_params* p, const float* target, const float* draft
   a.kind = p->kind;
   a.batch = p->batch;
   a.total_nodes = p->total_nodes;
+  a.test = opt ? opt->test : TV_TEST_RATIO;
+  a.log_clamp = (opt && opt->log_clamp > 0.0f) ? opt->log_clamp : 20.0f;
+  a.gamma = opt ? opt->gamma : nullptr;
   // per-row statistics (logits input or a retained-set mask) need workspace
   if (p->kind == TV_INPUT_LOGITS || retained_mask) {
     const size_t need = tv::accept_workspace_bytes(p->vocab, p->total_nodes);

@@ -26,6 +26,9 @@ struct AcceptArgs {
   int32_t kind;
   int32_t batch;
   int32_t total_nodes;
+  int32_t test;          // 0: ratio test, 1: log-space clamped test
+  float log_clamp;       // L of the clamped test
+  const float* gamma;    // [batch] calibration factors or null (1)
 };
 
 // Launches the accept pass; `workspace` holds per-(row, chunk) statistics and

@@ -147,3 +147,16 @@ def test_commit_argument_errors_before_launch(lib):
     aliased[10] = C.c_void_p(8192)
     assert lib.tv_commit_kv(C.byref(p), *aliased, None) == tv.TV_ERR_INVALID_ARG
     assert tv.status_string(tv.TV_ERR_NO_PAGE) == "TV_ERR_NO_PAGE"
+
+
+@pytest.mark.parametrize("bad", [dict(test=2), dict(log_clamp=-1.0), dict(log_clamp=100.0),
+                                 dict(log_clamp=float("nan"))])
+def test_accept_options_checked_before_launch(lib, bad):
+    p = tv.AcceptParams(batch=2, vocab=1000, max_nodes=16, total_nodes=20, kind=0)
+    o = tv.AcceptOptions(**dict(dict(test=0, log_clamp=0.0, gamma=None), **bad))
+    dummy = C.c_void_p(4096)
+    args = [dummy] * 12
+    args[6] = None
+    args[11] = None
+    assert lib.tv_accept_ex(C.byref(p), C.byref(o), *args, None, C.c_size_t(0), None) == \
+        tv.TV_ERR_INVALID_ARG
