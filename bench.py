@@ -134,6 +134,14 @@ def ncu_traffic(cfg_num):
     return e.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The slowest rank's value (replicas: the job ends with its last rank)."""
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def pct(ms):
     """p10 / p50 / p90 of per-rep times given in ms, in microseconds."""
     v = np.sort(np.asarray(ms, np.float64)) * 1e3
@@ -419,9 +427,7 @@ def main():
     attn_ms = [e0.elapsed_time(e1) for e0, e1, _, _ in evb]
     acc_ms = [e2.elapsed_time(e3) for _, _, e2, e3 in evb]
     if world > 1:
-        t = torch.tensor([total_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
+        total_s = max_over_ranks(total_s, dev)
 
     # ---- commit of the accepted path (the step after the walk; reported on its
     # own, not part of the timed step): the root and the accepted nodes of the
