@@ -20,16 +20,21 @@
 //                      box per 16-token page through the block table (eight
 //                      pages per tile and tensor), or 16 boxes of 8 tree nodes;
 //                      pages past the sequence load as zeros (out of bounds).
-//   warps 9, 10 (MMA)  one thread each issues tcgen05.mma: warp 9 S = Q K^T
-//                      into a double-buffered TMEM tile (128 x 128 fp32) with
-//                      Q read from TMEM, warp 10 O += P V into a TMEM
+//   warps 9, 10 (MMA)  one thread each issues tcgen05.mma: warp 9 S(t) = Q K^T
+//                      into one of two TMEM score buffers (128 x 128 fp32)
+//                      with Q read from TMEM, warp 10 O += P(t) V into a TMEM
 //                      accumulator (128 x D fp32) with P read from TMEM.
-//   warps 0-7          two threads per row (one per 64-key half): tcgen05.ld
-//                      of S, the tree mask from a per-node ancestor bitmask
-//                      (shared memory), fp32 online softmax in base 2, rescale
-//                      of O in TMEM only when the running max grows by more
-//                      than 2^8, and P as bf16 pairs stored over the S buffer
-//                      it came from.
+//   warps 0-7          two softmax lanes: warps 0-3 take the even tiles,
+//                      warps 4-7 the odd ones, one thread per row.  Per
+//                      tile: tcgen05.ld of S (the buffer is released at
+//                      once), the tree mask from a per-node ancestor bitmask
+//                      (shared memory), the row max, fp32 online softmax in
+//                      base 2 against a running max that the two lanes hand
+//                      to each other through mbarriers and that moves only
+//                      when it grows by more than 2^8 (O is then rescaled in
+//                      TMEM), and P as bf16 pairs into TMEM.  Each scheduler
+//                      runs one warp of each lane, so the exponentials of one
+//                      tile overlap the loads and maxima of the next.
 // K and V use the 128-byte swizzle that TMA writes, so the MMA reads them
 // straight from the ring; Q and P never touch shared memory.  Long prefixes
 // are split over CTAs (split-KV): each split writes (O, m, l) in fp32 and the
@@ -48,7 +53,7 @@ namespace {
 
 constexpr int BM = 128;           // packed query rows per CTA
 constexpr int BN = 128;           // keys per tile
-constexpr int kSoftmaxThreads = 256;  // warps 0-7
+constexpr int kSoftmaxThreads = 256;  // warps 0-7: two lanes of four warps
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;       // issues S = Q K^T; owns the TMEM allocation
 constexpr int kPvWarp = 10;       // issues O += P V
@@ -56,6 +61,7 @@ constexpr int kThreads = 352;     // 8 softmax warps + TMA warp + 2 MMA warps
 constexpr int kMaxAncWords = 16;  // 512-node trees
 constexpr int kAncStride = kMaxAncWords + 1;  // odd word stride: rows of a warp hit distinct banks
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kOrderMax = 256;    // batches up to this size run longest sequence first
 
 // Shared-memory layout of a K or V tile: 16 groups of 8 keys; a group holds
 // the 64-column halves of its 8 rows one after the other, each half an
@@ -76,18 +82,27 @@ struct Layout {
   static constexpr int kParent = kAnc + kAncBytes;
   static constexpr int kParentBytes = 512 * 4;
   static constexpr int kXchg = kParent + kParentBytes;  // row max / sum exchange
-  static constexpr int kXchgBytes = 3 * 2 * BM * 4;  // slots 0, 1: per-tile max; 2: row sum
-  static constexpr int kBar = kXchg + kXchgBytes;
+  // running max after tile t (slot t & 1, 2 x 128 floats), then the
+  // final (reference max, row sum) of each lane (2 x 128 float2)
+  static constexpr int kXchgBytes = 2 * BM * 4 + 2 * BM * 8;
+  // block ids of the pages of the last 8 K tiles issued (8 per tile), reused
+  // by the V copies of the same tiles
+  static constexpr int kBlk = kXchg + kXchgBytes;
+  static constexpr int kBlkBytes = 8 * 8 * 4;
+  // per-sequence (prefix length, first node, last node + 1) and the
+  // longest-first order of the sequences (batches up to kOrderMax)
+  static constexpr int kSeq = kBlk + kBlkBytes;
+  static constexpr int kSeqBytes = 4 * kOrderMax * 4;
+  static constexpr int kBar = kSeq + kSeqBytes;
   // kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages],
-  // s_full[2], p_full[2], o_done[2], drain[2], q_ready
-  static constexpr int kNumBars = 4 * kStages + 9;
+  // s_full[2], s_free[2], p_full, o_done[2], drain[2], chain[2][4], q_ready
+  static constexpr int kNumBars = 4 * kStages + 18;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 64;
   static constexpr int kAlloc = kTotal + 1024;  // slack for 1024-byte alignment
-  // TMEM columns: S[2] at 0 and 128 (fp32), O at 256 (D columns), Q at 448
-  // (bf16 pairs, D/2 columns).  P(t) overwrites the S buffer it came from:
-  // the thread owning score columns [64h, 64h+64) stores its 64 probabilities
-  // as bf16 pairs in columns [64h, 64h+32) of the same buffer.
+  // TMEM columns: S buffers (128 x 128 fp32) at 0 and 128; O at 256 (D
+  // columns); P (128 keys as bf16 pairs, 64 columns) at 384; Q at 448 (bf16
+  // pairs, D/2 columns).
   static constexpr int kTmemCols = 512;
 };
 
@@ -119,14 +134,9 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// Named barriers: id 1 joins the 8 softmax warps; ids 2..5 join the two
-// warps (w and w+4) that share a lane quarter, i.e. the two halves of the
-// same 32 rows (0 is __syncthreads).
+// Named barrier 1 joins the 8 softmax warps (0 is __syncthreads).
 __device__ __forceinline__ void softmax_group_sync() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
-}
-__device__ __forceinline__ void softmax_pair_sync(int warp) {
-  asm volatile("bar.sync %0, 64;" ::"r"(2 + (warp & 3)) : "memory");
 }
 
 __device__ __forceinline__ void record_status(int32_t* status, int b, int code) {
@@ -263,10 +273,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* vfull = bars + 2 * kStages;
   uint64_t* vempty = bars + 3 * kStages;
   uint64_t* s_full = bars + 4 * kStages;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  // o_done[t & 1] completes with P(t).V.  A wait for P(t-1).V comes after the
+  // same lane has seen P(t-2).V (or before any), so the phase of P(t-3).V is
+  // complete and the parity ((t-1) >> 1) & 1 cannot alias an older phase
+  // (one barrier for all tiles could: P(t-2).V may still be in flight).
+  uint64_t* o_done = p_full + 1;
   uint64_t* drain = o_done + 2;  // one per MMA-issuing thread
-  uint64_t* q_ready = drain + 2;
+  // running-max hand-off: chain[l][q] completes once per tile of lane l
+  // for the rows of lane quarter q (arrived by the warp of lane l, awaited by
+  // the warp of the other lane that owns the same rows)
+  uint64_t* chain = drain + 2;
+  uint64_t* q_ready = chain + 8;
   Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
   uint32_t* anc = reinterpret_cast<uint32_t*>(smem + Ly::kAnc);
   int32_t* par = reinterpret_cast<int32_t*>(smem + Ly::kParent);
@@ -276,16 +295,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
 
   // ------------------------------------------------------------ work item
-  // The sequence's extent is loaded first; barrier set-up and the TMEM
-  // allocation below overlap the load latency.
+  // Grid z enumerates (sequence rank, KV head).  For batches up to
+  // kOrderMax the rank orders the sequences by decreasing work (prefix plus
+  // tree keys, ties by index), so that the CTAs that run longest are
+  // dispatched first and the launch does not end on a tail of long CTAs.
+  // The extents of all sequences are loaded first; barrier set-up and the
+  // TMEM allocation below overlap the load latency.
+  int* seq = reinterpret_cast<int*>(smem + Ly::kSeq);  // [4][kOrderMax]
+  const bool ordered = a.batch <= kOrderMax;
+  if (ordered && tid < a.batch) {
+    seq[tid] = max(0, __ldg(a.prefix_lens + tid));
+    seq[kOrderMax + tid] = __ldg(a.node_offsets + tid);
+    seq[2 * kOrderMax + tid] = __ldg(a.node_offsets + tid + 1);
+  }
   Work w;
   w.mtile = blockIdx.x;
   w.split = blockIdx.y;
-  w.b = blockIdx.z / a.hkv;
   w.kvh = blockIdx.z % a.hkv;
-  w.n0 = __ldg(a.node_offsets + w.b);
-  w.N = __ldg(a.node_offsets + w.b + 1) - w.n0;
-  w.L = max(0, __ldg(a.prefix_lens + w.b));
 
   // ------------------------------------------------------------ prologue
   if (tid == 0) {
@@ -299,11 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(&s_full[k], 1);
-      mbar_init(&p_full[k], kSoftmaxThreads);
-      mbar_init(&o_done[k], 1);
+      mbar_init(&s_free[k], kSoftmaxThreads / 2);
     }
+    mbar_init(p_full, kSoftmaxThreads / 2);
+    mbar_init(&o_done[0], 1);
+    mbar_init(&o_done[1], 1);
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
+    for (int k = 0; k < 8; ++k) mbar_init(&chain[k], 32);
     mbar_init(q_ready, kSoftmaxThreads);
     fence_mbar_init();
   }
@@ -315,6 +344,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
+  if (ordered) {
+    if (tid < a.batch) {
+      const int key = seq[tid] + seq[2 * kOrderMax + tid] - seq[kOrderMax + tid];
+      int rank = 0;
+      for (int u = 0; u < a.batch; ++u) {
+        const int ku = seq[u] + seq[2 * kOrderMax + u] - seq[kOrderMax + u];
+        rank += (ku > key) || (ku == key && u < tid);
+      }
+      seq[3 * kOrderMax + rank] = tid;
+    }
+    __syncthreads();
+    w.b = seq[3 * kOrderMax + blockIdx.z / a.hkv];
+    w.n0 = seq[kOrderMax + w.b];
+    w.N = seq[2 * kOrderMax + w.b] - w.n0;
+    w.L = seq[w.b];
+  } else {
+    w.b = blockIdx.z / a.hkv;
+    w.n0 = __ldg(a.node_offsets + w.b);
+    w.N = __ldg(a.node_offsets + w.b + 1) - w.n0;
+    w.L = max(0, __ldg(a.prefix_lens + w.b));
+  }
 
   w.rows = w.N * a.group;
   // Split-KV: the prefix of each sequence is cut into at most max_splits
@@ -345,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp) tmem_dealloc(tmem, Ly::kTmemCols);
     return;
   }
-  const uint32_t tmem_s0 = tmem;        // S buffers at columns 0 and 128
   const uint32_t tmem_o = tmem + 256;   // O accumulator at columns 256 .. 256+D-1
+  const uint32_t tmem_p = tmem + 384;   // P at columns 384 .. 447
   const uint32_t tmem_q = tmem + 448;   // Q tile (A operand of Q.K^T)
   volatile int* abort_flag = &misc->abort;
 
@@ -399,7 +449,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     node0, 0, w.kvh);
       }
     };
-    int blk_k = fetch_block(0);  // block id of the next K tile, loaded ahead
+    // The block-table reads run two K tiles ahead of the K copies (a global
+    // read under load takes about a microsecond), and the ids of every K
+    // tile issued stay in shared memory until its V copy: V(t) is issued
+    // before K(t+8) can be (K(t+8) needs S(t+5), hence the softmax of tile
+    // t+3, which waits for P(t+1).V and so for V(t)).
+    int* blk_ring = reinterpret_cast<int*>(smem + Ly::kBlk);  // [tile & 7][page]
+    int blk_k = fetch_block(0), blk_k2 = fetch_block(1);
     int tk = 0, tv = 0;
     bool ok = true;
     unsigned long long t_idle = 0;
@@ -408,16 +464,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tk < w.T) {
         int ready = lane == 0 ? mbar_test_wait(&kempty[tk % kStages], ((tk / kStages) & 1) ^ 1) : 0;
         if (__shfl_sync(0xffffffffu, ready, 0)) {
+          if (prefix_lane) blk_ring[(tk & 7) * 8 + lane] = blk_k;
           issue(tk, 0, blk_k);
           ++tk;
-          blk_k = fetch_block(tk);
+          blk_k = blk_k2;
+          blk_k2 = fetch_block(tk + 1);
           progressed = true;
         }
       }
       if (tv < tk) {
         int ready = lane == 0 ? mbar_test_wait(&vempty[tv % kStages], ((tv / kStages) & 1) ^ 1) : 0;
         if (__shfl_sync(0xffffffffu, ready, 0)) {
-          issue(tv, 1, fetch_block(tv));
+          issue(tv, 1, prefix_lane ? blk_ring[(tv & 7) * 8 + lane] : kPastEnd);
           ++tv;
           progressed = true;
         }
@@ -460,20 +518,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(q_ready, 0, abort_flag);
       tc_fence_after();
       if (warp == kMmaWarp) {
-        constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);  // M=128, N=128: full-rate shape
-        // Descriptors are built once; each MMA adds a compile-time offset to
-        // the start-address field (16-byte units; shared addresses stay
-        // < 2^18).  K (K-major): 8-row groups at kGroupBytes, halves at +1024.
+        constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);  // M=128, N=128
+        // Descriptors are built once; each MMA adds an offset to the
+        // start-address field (16-byte units; shared addresses stay < 2^18).
+        // K (K-major): 8-row groups at kGroupBytes, halves at +1024.
         const uint64_t dk0 = smem_desc(smem_u32(smem + Ly::kKRing), 16, Ly::kGroupBytes);
         for (int t = 0; ok && t < w.T; ++t) {
-          // S(t) = Q K(t)^T into S buffer t&1, once K(t) has landed and
-          // P(t-2).V(t-2), the last reader of that buffer, has completed
+          // S(t) = Q K(t)^T into buffer t & 1, once K(t) has landed and the
+          // softmax has read S(t-2) out of that buffer
           ok = mbar_wait(&kfull[t % kStages], (t / kStages) & 1, abort_flag);
-          if (ok && t >= 2) ok = mbar_wait(&o_done[t & 1], ((t - 2) >> 1) & 1, abort_flag);
+          if (ok && t >= 2) ok = mbar_wait(&s_free[t & 1], ((t - 2) >> 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint64_t dk = dk0 + static_cast<uint64_t>((t % kStages) * (Ly::kTileBytes >> 4));
-          const uint32_t d = tmem_s0 + (t & 1) * BN;
+          const uint32_t d = tmem + (t & 1) * BN;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             // A = Q from TMEM (16 dims = 8 columns per step), B = K from the ring
@@ -489,20 +547,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dv0 = smem_desc(smem_u32(smem + Ly::kVRing), 1024, Ly::kGroupBytes);
         for (int t = 0; ok && t < w.T; ++t) {
           // O += P(t) V(t), once P(t) is in TMEM and V(t) has landed
-          ok = mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag);
+          ok = mbar_wait(p_full, t & 1, abort_flag);
           if (ok) ok = mbar_wait(&vfull[t % kStages], (t / kStages) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const int st = t % kStages;
           const uint64_t dv = dv0 + static_cast<uint64_t>(st * (Ly::kTileBytes >> 4));
-          const uint32_t p = tmem_s0 + (t & 1) * BN;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            // A = P from TMEM: 16 keys = 8 columns of bf16 pairs (keys 0-63 in
-            // columns 0-31 of the buffer, keys 64-127 in columns 64-95); B = 2
-            // groups of V
-            mma_bf16_ts(tmem_o, p + (kk >> 2) * 64 + (kk & 3) * 8,
-                        dv + ((kk * 2 * Ly::kGroupBytes) >> 4), idesc_o,
+            // A = P from TMEM: 16 keys = 8 columns of bf16 pairs; B = 2 groups of V
+            mma_bf16_ts(tmem_o, tmem_p + kk * 8, dv + ((kk * 2 * Ly::kGroupBytes) >> 4), idesc_o,
                         (t > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&o_done[t & 1]);
@@ -521,15 +575,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------- softmax warps
-    // Warps 0-7: warp w owns rows 32*(w%4)..+31 (its TMEM lane quarter) and
-    // column half hc = w/4 of every 64-key tile, so two threads share a row
-    // and each scheduler runs two softmax warps.
+    // Warps 0-7: warp w owns rows 32*(w%4)..+31 (its TMEM lane quarter) in
+    // lane hc = w/4, which takes the tiles t = hc, hc + 2, ...; the two
+    // warps of a scheduler belong to different lanes.  In the prologue and
+    // the epilogue hc selects the half of the Q and O columns a thread moves.
     const int r = (warp & 3) * 32 + lane;  // row of the tile == TMEM lane
-    const int hc = warp >> 2;              // which 32 keys of each tile
+    const int hc = warp >> 2;              // softmax lane
     const int sid = hc * 128 + r;          // 0..255
     const int R = w.mtile * BM + r;
     const bool live = R < w.rows;
-    float* xchg = reinterpret_cast<float*>(smem + Ly::kXchg);  // [3 slots][2 halves][128 rows]
+    float* m_slot = reinterpret_cast<float*>(smem + Ly::kXchg);           // [2][128]
+    float2* fin = reinterpret_cast<float2*>(smem + Ly::kXchg + 2 * BM * 4);  // [2 lanes][128]
     // Q tile -> TMEM (one row per lane, bf16 pairs; this thread stores the
     // half hc of its row); padding rows are zero.  The Q loads are issued
     // before the tree loads so that both latencies overlap.
@@ -584,26 +640,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i_node = live ? R / g : 0;  // local node of this row
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t* my_anc = anc + (i_node - node_lo) * kAncStride;
-    float m_run = -INFINITY;  // reference max (log2 units), shared by the pair
-    float l_run = 0.0f;       // this thread's half of the row sum
+    // Online softmax over the tiles of this lane.  The running max m(t)
+    // (log2 units) is a chain through all tiles of both lanes: it moves only
+    // when a tile's max exceeds it by more than 2^8, and P(t) is taken
+    // against m(t).  O always holds sum P V against the latest m (a move
+    // rescales it after the previous P.V); each lane keeps its part of the
+    // row sum against the reference of its own last tile.
+    float m_lane = -INFINITY;  // reference of l_run
+    float l_run = 0.0f;
     bool ok = true;
-    // Every softmax warp passes the same sequence of named barriers (one per
-    // tile): after a failed (timed-out) wait a warp keeps looping but skips
-    // the work, so that its partner warp can never block on it.
-    for (int t = 0; t < w.T; ++t) {
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag));
-      // this thread's 64 scores of the tile (keys hc*64 .. hc*64+63)
-      float x[64];
+    // The warp of the other lane hands over m(t-1) through chain[1-hc][q]:
+    // its k-th completion is tile 2k + (1-hc), and it cannot complete again
+    // before this warp has handed back m(t), so the phase parity of tile t-1
+    // is ((t-1) >> 1) & 1.  After a failed (timed-out) wait a warp keeps
+    // looping and arriving but skips the work.
+    uint64_t* chain_in = &chain[(1 - hc) * 4 + (warp & 3)];
+    uint64_t* chain_out = &chain[hc * 4 + (warp & 3)];
+    for (int t = hc; t < w.T; t += 2) {
       if (ok) {
-        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
-        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag));
+        if (!ok) misc->abort = 1;
+      }
+      // this thread's 128 scores of the tile
+      float x[128];
+      if (ok) {
         tc_fence_after();
-        tmem_ld32(tmem_s0 + (t & 1) * BN + hc * 64 + lane_off, lo);
-        tmem_ld32(tmem_s0 + (t & 1) * BN + hc * 64 + 32 + lane_off, hi);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tmem + (t & 1) * BN + 32 * c + lane_off,
+                    *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
         tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&s_free[t & 1]);  // S(t+2) may overwrite the buffer
       } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = 0.0f;
+        for (int c = 0; c < 128; ++c) x[c] = 0.0f;
       }
       // mask (scores stay unscaled; the scale is folded into the exponent)
       int valid_keys = BN;
@@ -611,60 +682,91 @@ __global__ void __launch_bounds__(kThreads, 1)
         valid_keys = min(BN, w.k_end - (w.k_begin + t * BN));
         if (valid_keys < BN) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (hc * 64 + c >= valid_keys) x[c] = -INFINITY;
+          for (int c = 0; c < 128; ++c)
+            if (c >= valid_keys) x[c] = -INFINITY;
         }
       } else {
-        const int j0 = (t - w.n_prefix_tiles) * BN + hc * 64;
+        const int j0 = (t - w.n_prefix_tiles) * BN;
         // only ancestors-or-self of this node carry a bit, all of them < N,
         // so node columns past the tree are masked as well
-        const uint32_t b0 = live ? my_anc[j0 >> 5] : 0u;
-        const uint32_t b1 = live ? my_anc[(j0 >> 5) + 1] : 0u;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          x[c] = (b0 & (1u << c)) ? x[c] : -INFINITY;
-          x[c + 32] = (b1 & (1u << c)) ? x[c + 32] : -INFINITY;
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t b = live ? my_anc[(j0 >> 5) + k] : 0u;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) x[32 * k + c] = (b & (1u << c)) ? x[32 * k + c] : -INFINITY;
         }
       }
-      // max of the 64 scores with three-input max: 64 -> 22 -> 8 -> 3 -> 1
-      float mx[22];
+      // max of the 128 scores: eight running three-input maxima over the
+      // columns j, j+8, ..., j+120 (few live temporaries next to x)
+      float mx[8];
 #pragma unroll
-      for (int c = 0; c < 21; ++c) mx[c] = fmax3(x[3 * c], x[3 * c + 1], x[3 * c + 2]);
-      mx[21] = x[63];
+      for (int j = 0; j < 8; ++j) {
+        mx[j] = fmax3(x[j], x[j + 8], x[j + 16]);
 #pragma unroll
-      for (int c = 0; c < 7; ++c) mx[c] = fmax3(mx[3 * c], mx[3 * c + 1], mx[3 * c + 2]);
-      mx[7] = mx[21];
-      mx[0] = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-      // the row max of both halves (exchange slot t&1, so that the next
-      // tile's write cannot overtake the partner's read)
-      xchg[((t & 1) * 2 + hc) * 128 + r] = mx[0];
-      softmax_pair_sync(warp);
-      if (!ok) continue;  // skip the work, keep the barrier sequence
-      const float tmax = fmaxf(mx[0], xchg[((t & 1) * 2 + (hc ^ 1)) * 128 + r]) * a.scale_log2;
-      // online softmax with a lazily rescaled reference max (same decision
-      // in both threads of a row)
-      float alpha = 1.0f;
+        for (int k = 3; k < 15; k += 2) mx[j] = fmax3(mx[j], x[j + 8 * k], x[j + 8 * k + 8]);
+        mx[j] = fmaxf(mx[j], x[j + 120]);
+      }
+      const float smax =
+          fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+          a.scale_log2;
+      // the running max after the previous tile (the other lane's)
+      float m_prev = -INFINITY;
+      if (t >= 1) {
+        if (ok) {
+          ok = __all_sync(0xffffffffu, mbar_wait(chain_in, ((t - 1) >> 1) & 1, abort_flag));
+          if (!ok) misc->abort = 1;
+        }
+        m_prev = m_slot[((t - 1) & 1) * BM + r];
+      }
+      float m_new = m_prev, alpha = 1.0f;
       bool rescale = false;
-      if (tmax != -INFINITY) {
-        if (m_run == -INFINITY) {
-          m_run = tmax;
-        } else if (tmax > m_run + kRescaleLog2) {
-          alpha = exp2f(m_run - tmax);
-          m_run = tmax;
+      if (smax != -INFINITY) {
+        if (m_prev == -INFINITY) {
+          m_new = smax;
+        } else if (smax > m_prev + kRescaleLog2) {
+          m_new = smax;
+          alpha = exp2f(m_prev - smax);
           rescale = true;
         }
       }
-      // A rescale of O waits for P(t-1).V(t-1), the last accumulation into
-      // it.  P(t) itself needs no wait: it goes to the buffer S(t) came from,
-      // whose previous reader P(t-2).V(t-2) completed before S(t) did.
-      if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
+      m_slot[(t & 1) * BM + r] = m_new;
+      mbar_arrive(chain_out);  // release: m_slot is visible to the waiter
+      if (!ok) continue;  // skip the work, keep the hand-off sequence
+      if (m_lane != m_new) {  // this lane's row sum follows the reference
+        if (l_run > 0.0f) l_run *= exp2f(m_lane - m_new);
+        m_lane = m_new;
+      }
+      const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
+      // P(t) = 2^(s * scale * log2(e) - m) as bf16 pairs (column c holds keys
+      // 2c, 2c+1); masked scores are -inf -> 0
+      uint32_t pk[64];
+      float ls[16];
+#pragma unroll
+      for (int c8 = 0; c8 < 16; ++c8) {
+        float part = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float p0 = ex2_approx(fmaf(x[c8 * 8 + 2 * k], a.scale_log2, -mref));
+          const float p1 = ex2_approx(fmaf(x[c8 * 8 + 2 * k + 1], a.scale_log2, -mref));
+          pk[c8 * 4 + k] = pack_bf16x2(p0, p1);
+          part += p0 + p1;
+        }
+        ls[c8] = part;
+      }
+      // P(t-1).V is the last reader of the P buffer and the last
+      // accumulation into O
+      if (t >= 1) {
         ok = __all_sync(0xffffffffu,
                         mbar_wait(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag));
-        if (!ok) continue;
-        tc_fence_after();
-        // this thread rescales its half of the O row
+        if (!ok) {
+          misc->abort = 1;
+          continue;
+        }
+      }
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, rescale)) {  // O holds P(0..t-1).V against m_prev
 #pragma unroll
-        for (int c0 = hc * (D / 2); c0 < (hc + 1) * (D / 2); c0 += 32) {
+        for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
           tmem_ld32(tmem_o + c0 + lane_off, o);
           tmem_ld_wait();
@@ -673,32 +775,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tmem_o + c0 + lane_off, o);
         }
       }
-      l_run *= alpha;
-      const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
-      uint32_t pk[32];  // bf16 pairs: column c of this half holds keys 2c (low), 2c+1
-      float ls[8];
+      tmem_st32(tmem_p + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tmem_p + 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      float lsum = 0.0f;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        float part = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          // p = 2^(s * scale * log2(e) - m); masked scores are -inf -> 0
-          const float p0 = ex2_approx(fmaf(x[c8 * 8 + 2 * k], a.scale_log2, -mref));
-          const float p1 = ex2_approx(fmaf(x[c8 * 8 + 2 * k + 1], a.scale_log2, -mref));
-          pk[c8 * 4 + k] = pack_bf16x2(p0, p1);
-          part += p0 + p1;
-        }
-        ls[c8] = part;
-      }
-      tmem_st32(tmem_s0 + (t & 1) * BN + hc * 64 + lane_off, pk);
-      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      // keys past the prefix end in this tile: clear their V rows (page tails
-      // may hold stale data; P is 0 there but 0 * NaN would poison O)
+      for (int k = 0; k < 16; ++k) lsum += ls[k];
+      l_run += lsum;
+      // keys past the prefix end in this tile: clear their V rows (page
+      // tails may hold stale data; P is 0 there but 0 * NaN would poison O)
       if (valid_keys < BN) {
         const int st = t % kStages;
         mbar_wait(&vfull[st], (t / kStages) & 1);  // acquire the TMA writes
         uint8_t* vt = smem + Ly::kVRing + st * Ly::kTileBytes;
-        for (int idx = sid; idx < (BN - valid_keys) * Ly::kHalves; idx += kSoftmaxThreads) {
+        for (int idx = r; idx < (BN - valid_keys) * Ly::kHalves; idx += BM) {
           const int row = valid_keys + idx / Ly::kHalves, h = idx % Ly::kHalves;
           uint4* p = reinterpret_cast<uint4*>(vt + (row >> 3) * Ly::kGroupBytes + h * 1024 +
                                               (row & 7) * 128);
@@ -709,12 +798,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[t & 1]);
+      mbar_arrive(p_full);
     }
-    // the row sum of both halves (slot 2: the max slots may still be read)
-    xchg[(2 * 2 + hc) * 128 + r] = l_run;
-    softmax_pair_sync(warp);
-    const float l_row = l_run + xchg[(2 * 2 + (hc ^ 1)) * 128 + r];
+    // the row sum: both lanes' parts against the final running max
+    fin[hc * BM + r] = make_float2(m_lane, l_run);
+    softmax_group_sync();
+    const float2 f0 = fin[r], f1 = fin[BM + r];
+    const float m_run = fmaxf(f0.x, f1.x);  // the chain only grows: the final max
+    float l_row = 0.0f;
+    if (f0.y > 0.0f) l_row += f0.y * exp2f(f0.x - m_run);
+    if (f1.y > 0.0f) l_row += f1.y * exp2f(f1.x - m_run);
     if (!ok) {
       record_status(a.status, w.b, kDeviceTimeout);
       misc->abort = 1;

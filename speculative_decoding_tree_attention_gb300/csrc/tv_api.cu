@@ -53,11 +53,11 @@ struct AttnPlan {
 };
 
 // Launch plan: 128-row tiles of packed (node, head) rows per (sequence, KV
-// head).  When those tiles cover less than about two waves of SMs, each
-// sequence's prefix is also split into up to 8 ranges of whole 128-key tiles
-// (at least 256 keys per split on the longest prefix); the splits of a tile
-// run as one thread-block cluster and merge through distributed shared
-// memory, so no device workspace is needed.
+// head).  Each sequence's prefix may also be split into up to 8 ranges of
+// whole 128-key tiles (at least 256 keys per split on the longest prefix),
+// the count chosen by the makespan model below; the splits of a tile run as
+// one thread-block cluster and merge through distributed shared memory, so
+// no device workspace is needed.
 bool plan_attention(const tv_attn_params* p, AttnPlan* out) {
   if (!p) return false;
   if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1) return false;
@@ -73,12 +73,26 @@ bool plan_attention(const tv_attn_params* p, AttnPlan* out) {
   AttnPlan pl;
   pl.group = p->num_q_heads / p->num_kv_heads;
   pl.mtiles_max = (p->max_nodes * pl.group + 127) / 128;
+  // Split count S from a makespan model in units of one 128-key tile (about
+  // a microsecond): a CTA costs kFixed tiles of prologue and epilogue, its
+  // share ceil(P / S) of the P prefix tiles, the Nt node tiles (last split)
+  // and kMerge more when S > 1; CTAs run one per SM, so the launch takes
+  // ceil(base * S / SMs) waves.  P, Nt and base are upper bounds from the
+  // host hints (longest prefix, most nodes); ties go to the larger S.
+  constexpr long kFixed = 5, kMerge = 4;
   const long base = static_cast<long>(p->batch) * p->num_kv_heads * pl.mtiles_max;
-  const long target = 2l * sm_count();
-  long splits = 1;
-  if (p->max_prefix_len > 0 && base < target) splits = (target + base - 1) / base;
-  splits = std::min(splits, 8l);
-  splits = std::min(splits, std::max(1l, static_cast<long>(p->max_prefix_len) / 256));
+  const long P = (p->max_prefix_len + 127) / 128, Nt = (p->max_nodes + 127) / 128;
+  const long sms = sm_count();
+  const long s_cap = std::min(8l, std::max(1l, static_cast<long>(p->max_prefix_len) / 256));
+  long splits = 1, best = -1;
+  for (long S = 1; S <= s_cap; ++S) {
+    const long waves = (base * S + sms - 1) / sms;
+    const long cost = waves * (kFixed + (P + S - 1) / S + Nt + (S > 1 ? kMerge : 0));
+    if (best < 0 || cost <= best) {
+      best = cost;
+      splits = S;
+    }
+  }
   pl.max_splits = static_cast<int>(splits);
   *out = pl;
   return true;
