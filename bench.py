@@ -474,6 +474,28 @@ def main():
                     "note": "tv_retained_set of every draft row, timed on its own"}
     commit_tokens = int(acc_out["accepted_len"].sum().item()) + B
     del cm
+    # ---- the multi-candidate accept variant (siblings tried in order with
+    # residual updates) on the same inputs, reported on its own
+    evm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nb)]
+    m_out = {k: torch.empty_like(v) for k, v in acc_out.items()}
+    with torch.cuda.stream(stream):
+        for k in range(nb + 3):
+            flush.fill_(k & 0xFF)
+            if k >= 3:
+                evm[k - 3][0].record(stream)
+            tv.accept(d["target"], d["draft"], d["tokens"], d["parent"], d["off"], d["uniforms"],
+                      d.get("mask"), max_nodes=max_nodes, kind=args.mode, test="multi",
+                      outputs=dict(m_out, workspace=acc_ws))
+            if k >= 3:
+                evm[k - 3][1].record(stream)
+    stream.synchronize()
+    assert int(m_out["status"].max()) == 0, "multi-candidate accept status"
+    m_ms = statistics.mean(a0.elapsed_time(a1) for a0, a1 in evm)
+    multi = {"mean_us": m_ms * 1e3, "trees_per_s": B / (m_ms * 1e-3),
+             "mean_accepted_len": float(m_out["accepted_len"].float().mean().item()),
+             "mean_accepted_len_single": float(acc_out["accepted_len"].float().mean().item()),
+             "note": "tv_accept_ex with TV_TEST_MULTI on the step's inputs, timed on its own"}
+    del m_out
 
     # ---- end to end through the public API with host buffers
     pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()}
@@ -538,6 +560,7 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "percentiles_us": {"step": pct(step_ms), "attention": pct(attn_ms), "accept": pct(acc_ms)},
         "retained_set": retained,
+        "accept_multi": multi,
         "commit": {"mean_us": statistics.mean(commit_ms) * 1e3, "tokens": commit_tokens,
                    "bytes": commit_tokens * 8 * cfg["hkv"] * cfg["d"],  # K+V rows read and written
                    "note": "tv_commit_kv of the root and accepted path, timed on its own"},

@@ -230,10 +230,28 @@ int tv_accept(const tv_accept_params* params, const float* target, const float* 
  *                      r = clamp(log p~ - log q~ + log gamma_b, -L, L) in fp32,
  *                      a_i = u_i < (r >= 0 ? 1 : exp(r)); p~ = 0 or a NaN r
  *                      rejects (a pruned token never passes).
- * The walk and the bonus draw are unchanged (the residual max(0, p~ - q~)).
+ * For these two the walk and the bonus draw are unchanged (the residual
+ * max(0, p~ - q~)).
+ *   TV_TEST_MULTI      multi-candidate verification with residual updates
+ *                      (multi-step speculative sampling of SpecInfer, which
+ *                      the pages cite; the pages only say "resample at the
+ *                      rejection"): from the root, the children c of the
+ *                      current node j are tried in increasing index order
+ *                      against the current target distribution cur (at first
+ *                      p~_j): accept iff fl32(u_c * q~_j(x_c)) <
+ *                      fl32(gamma_b * cur(x_c)), and the first accepted child
+ *                      becomes the current node.  A rejection replaces cur by
+ *                      fl32(r / N) with r = max(0, fl32(cur - q~_j)) and N the
+ *                      fp32 of the exact 2^-40 fixed-point sum of r (cur is
+ *                      kept when that sum is 0).  When every child of the
+ *                      final node is rejected, the bonus is drawn from the
+ *                      last r (from cur when its sum is 0); at a leaf from p~.
+ *                      On a chain it decides exactly as TV_TEST_RATIO.
+ *                      debug_pq holds (cur(x_c), q~(x_c)) of the tested
+ *                      children and zeros for untested nodes.
  * gamma: device fp32 [batch] or NULL (1); a gamma_b that is not a positive
  * finite number gives that sequence TV_ERR_BAD_TREE.  log_clamp: L, 0 => 20. */
-typedef enum { TV_TEST_RATIO = 0, TV_TEST_LOG_CLAMP = 1 } tv_accept_test;
+typedef enum { TV_TEST_RATIO = 0, TV_TEST_LOG_CLAMP = 1, TV_TEST_MULTI = 2 } tv_accept_test;
 
 typedef struct {
   int32_t test;        /* tv_accept_test                                 */

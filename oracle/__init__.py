@@ -142,7 +142,8 @@ def accept(case: dict, nthreads: int | None = None, want_pq: bool = True, test: 
            log_clamp: float = 20.0, gamma=None) -> dict:
     """Oracle accept pass.  Returns accepted_len, path, bonus_token, status, pq.
     test 0: ratio test with calibration factors `gamma` ([batch] fp32, None = 1);
-    test 1: the log-space clamped test with bound `log_clamp`."""
+    test 1: the log-space clamped test with bound `log_clamp`;
+    test 2: the multi-candidate walk (siblings in order, residual updates)."""
     lib = _load()
     off = _c(case["node_offsets"], np.int32)
     batch = off.shape[0] - 1

@@ -46,6 +46,19 @@
  *          when it has children, else from p (the resampling at rejection of
  *          [LLM] §1.2 step 3), with an exact fixed-point inverse CDF
  *          (quanta 2^-40, 64-bit sums, t = floor(u0 * S) in 128-bit integer).
+ *   test 2 replaces steps 3-5 with the multi-candidate walk (siblings tried
+ *       in order with residual updates, the multi-step speculative sampling
+ *       of SpecInfer, which the pages cite among their sources; the pages
+ *       themselves only say "resample at the rejection"): from the root, the
+ *       children c of the current node j are tested in increasing index
+ *       order against the current target distribution cur (at first p~_j):
+ *       accept c iff fl32(u_c q~_j(x_c)) < fl32(g cur(x_c)); the first
+ *       accepted child becomes the current node.  Each rejection replaces cur
+ *       by its normalised residual: r = max(0, fl32(cur - q~_j)), S = sum of
+ *       the 2^-40 quanta of r (exact), N = fp32(S 2^-40), cur = fl32(r / N)
+ *       (cur kept when S = 0).  When every child is rejected the bonus is
+ *       drawn from the last residual r (from cur when its S is 0); at a leaf
+ *       from p~ of the leaf.  On a chain this is exactly steps 3-5.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared -pthread (no fast
  * math, no contraction: every fp32 product below is rounded once).
@@ -212,7 +225,7 @@ typedef struct {
   int32_t *bonus_token;         /* [batch] */
   int32_t *status;              /* [batch] */
   float *pq_out;                /* NULL or [total_nodes][2] */
-  int test;                     /* 0: ratio test, 1: log-space clamped test */
+  int test;                     /* 0: ratio test, 1: log-space clamped test, 2: multi-candidate */
   float log_clamp;              /* L of the clamped test */
   const float *gamma;           /* NULL or [batch] calibration factors */
 } oracle_accept_args;
@@ -296,6 +309,124 @@ static void dfs_deepest(const int32_t *parent, const unsigned char *acc, int N, 
     if (parent[c] == node && acc[c]) dfs_deepest(parent, acc, N, c, depth + 1, best, best_depth);
 }
 
+/* p~ and q~ of row `row` (whole vocabulary): renormalised on the retained set
+ * when a mask is given (0 off it), else as given. */
+static void tilde_rows(const oracle_accept_args *a, size_t row, float *prow, float *ptil, float *qtil) {
+  const int V = a->vocab;
+  target_prob_row(a, row, prow);
+  const float *qrow = a->draft_probs + row * (size_t)V;
+  const float z = a->retained_mask ? retained_mass(a, row) : 1.0f;
+  for (int v = 0; v < V; ++v) {
+    if (a->retained_mask) {
+      if (in_retained(a, row, v)) {
+        ptil[v] = prow[v] / z;
+        qtil[v] = qrow[v] / z;
+      } else {
+        ptil[v] = 0.0f;
+        qtil[v] = 0.0f;
+      }
+    } else {
+      ptil[v] = prow[v];
+      qtil[v] = qrow[v];
+    }
+  }
+}
+
+/* The exact fixed-point inverse-CDF draw over quanta of w[0..V) with u0;
+ * -1 when all quanta are 0. */
+static int draw_quanta(const float *w, int V, float u0) {
+  uint64_t S = 0;
+  for (int v = 0; v < V; ++v) S += quantise(w[v]);
+  if (S == 0) return -1;
+  uint64_t t = scaled_draw(u0, S), cum = 0;
+  for (int v = 0; v < V; ++v) {
+    cum += quantise(w[v]);
+    if (cum > t) return v;
+  }
+  return -1;
+}
+
+/* Smallest index of the largest entry (NaN ignored). */
+static int argmax_row(const float *w, int V) {
+  int token = 0;
+  float best = -INFINITY;
+  for (int v = 0; v < V; ++v)
+    if (w[v] > best) {
+      best = w[v];
+      token = v;
+    }
+  return token;
+}
+
+/* Multi-candidate walk (test 2), the tree already validated. */
+static void accept_one_tree_multi(const oracle_accept_args *a, int b, float g) {
+  const int V = a->vocab;
+  const int n0 = a->node_offsets[b];
+  const int N = a->node_offsets[b + 1] - n0;
+  const int32_t *par = a->parent + n0;
+  const int32_t *tok = a->draft_tokens + n0;
+  int32_t *path = a->path + (size_t)b * a->max_nodes;
+  float *prow = (float *)malloc(sizeof(float) * (size_t)V);
+  float *cur = (float *)malloc(sizeof(float) * (size_t)V);
+  float *qtil = (float *)malloc(sizeof(float) * (size_t)V);
+  float *res = (float *)malloc(sizeof(float) * (size_t)V);
+  if (a->pq_out)
+    for (int i = 0; i < N; ++i) {
+      a->pq_out[2 * (size_t)(n0 + i) + 0] = 0.0f;
+      a->pq_out[2 * (size_t)(n0 + i) + 1] = 0.0f;
+    }
+  int j = 0, len = 0, token = -1;
+  for (;;) {
+    tilde_rows(a, (size_t)(n0 + j), prow, cur, qtil);  /* cur = p~_j */
+    int next = -1, rejected = 0;
+    uint64_t last_S = 0;
+    for (int c = j + 1; c < N && next < 0; ++c) {
+      if (par[c] != j) continue;
+      const float p = cur[tok[c]], q = qtil[tok[c]];
+      if (a->pq_out) {
+        a->pq_out[2 * (size_t)(n0 + c) + 0] = p;
+        a->pq_out[2 * (size_t)(n0 + c) + 1] = q;
+      }
+      const float uq = a->uniforms[n0 + c] * q;
+      const float gp = g * p;
+      if (uq < gp) {
+        next = c;
+        break;
+      }
+      /* rejected: cur <- its normalised residual */
+      uint64_t S = 0;
+      for (int v = 0; v < V; ++v) {
+        const float d = cur[v] - qtil[v];
+        res[v] = d > 0.0f ? d : 0.0f;
+        S += quantise(res[v]);
+      }
+      rejected = 1;
+      last_S = S;
+      if (S > 0) {
+        const float Nf = (float)S * 0x1p-40f;
+        for (int v = 0; v < V; ++v) cur[v] = res[v] / Nf;
+      }
+    }
+    if (next >= 0) {
+      path[len++] = next;
+      j = next;
+      continue;
+    }
+    const float u0 = a->uniforms[n0];
+    if (rejected && last_S > 0) token = draw_quanta(res, V, u0);
+    if (token < 0) token = draw_quanta(cur, V, u0);  /* a leaf, or an empty residual */
+    if (token < 0) token = argmax_row(cur, V);
+    break;
+  }
+  a->accepted_len[b] = len;
+  a->bonus_token[b] = token;
+  a->status[b] = ORACLE_OK;
+  free(prow);
+  free(cur);
+  free(qtil);
+  free(res);
+}
+
 static void accept_one_tree(const oracle_accept_args *a, int b) {
   const int V = a->vocab;
   const int n0 = a->node_offsets[b];
@@ -316,6 +447,10 @@ static void accept_one_tree(const oracle_accept_args *a, int b) {
     a->status[b] = ORACLE_BAD_TREE;
     a->accepted_len[b] = -1;
     a->bonus_token[b] = -1;
+    return;
+  }
+  if (a->test == 2) {
+    accept_one_tree_multi(a, b, g);
     return;
   }
 

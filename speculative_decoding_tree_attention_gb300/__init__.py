@@ -220,9 +220,10 @@ def accept(target, draft_probs, draft_tokens, parent, node_offsets, uniforms,
     """tv_accept_ex on the current stream.  target/draft_probs [total, V] fp32,
     draft_tokens/parent [total] int32, node_offsets [B+1] int32, uniforms
     [total] fp32, retained_mask [total, ceil(V/32)] int32/uint32 or None.
-    test: "ratio" (fl32(u q~) < fl32(gamma p~)) or "log_clamp" (the clamped
-    log-space test, bound log_clamp, 0 => 20); gamma: [B] fp32 CUDA tensor of
-    calibration factors or None (1).
+    test: "ratio" (fl32(u q~) < fl32(gamma p~)), "log_clamp" (the clamped
+    log-space test, bound log_clamp, 0 => 20) or "multi" (siblings tried in
+    order with residual updates); gamma: [B] fp32 CUDA tensor of calibration
+    factors or None (1).
     Returns dict(accepted_len, path, bonus_token, status, debug_pq)."""
     import torch
     lib = load()
@@ -254,10 +255,10 @@ def accept(target, draft_probs, draft_tokens, parent, node_offsets, uniforms,
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check_dev(gamma)
-    if test not in ("ratio", "log_clamp"):
-        raise ValueError("test must be 'ratio' or 'log_clamp'")
-    opts = AcceptOptions(0 if test == "ratio" else 1, float(log_clamp),
-                         None if gamma is None else gamma.data_ptr())
+    tests = {"ratio": 0, "log_clamp": 1, "multi": 2}
+    if test not in tests:
+        raise ValueError("test must be 'ratio', 'log_clamp' or 'multi'")
+    opts = AcceptOptions(tests[test], float(log_clamp), None if gamma is None else gamma.data_ptr())
     rc = lib.tv_accept_ex(C.byref(prm), C.byref(opts), _ptr(target), _ptr(draft_probs), _ptr(draft_tokens),
                        _ptr(parent), _ptr(node_offsets), _ptr(uniforms), _ptr(retained_mask),
                        _ptr(acc), _ptr(path), _ptr(bonus), _ptr(status), _ptr(dpq), _ptr(ws),

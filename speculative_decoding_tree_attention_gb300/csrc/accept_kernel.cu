@@ -28,6 +28,15 @@
 //       entries in registers; exact fixed-point sums are combined in rank
 //       order over distributed shared memory and the thread whose range
 //       holds t = floor(u0 * S) finds the token.
+// The multi-candidate walk (test 2) replaces the parallel tests and the cut:
+// from the root, the children of the current node are tried in index order
+// against the current target distribution cur (at first p~), the first
+// accepted child becomes the current node, and every rejection replaces cur
+// by its normalised residual fl32(r / N), r = max(0, fl32(cur - q~)), N the
+// fp32 of the exact fixed-point sum of r, computed over the cluster's slices
+// of the row (multi-step speculative sampling, SpecInfer, which the pages cite
+// among their sources).  The bonus then comes from the last residual, or from
+// p~ at a leaf.
 // Every decision-carrying sum is an exact integer, so the result does not
 // depend on the reduction order.
 #include <cooperative_groups.h>
@@ -51,7 +60,11 @@ __host__ __device__ inline int bonus_chunk(int vocab, int C) {
   const int c = (vocab + C - 1) / C;
   return (c + kChunkQuantum - 1) / kChunkQuantum * kChunkQuantum;
 }
-__host__ __device__ inline int tree_smem_bytes(int chunk) { return 2 * chunk * 4 + (chunk / 32) * 4; }
+// the cut row's target and draft chunks (and, for the multi-candidate walk,
+// the residual chunk) plus its mask words
+__host__ __device__ inline int tree_smem_bytes(int chunk, bool multi) {
+  return (multi ? 3 : 2) * chunk * 4 + (chunk / 32) * 4;
+}
 constexpr int kRowThreads = 256;
 constexpr int kRowVec = 8;             // float4 per thread per chunk
 constexpr int kChunk = kRowThreads * kRowVec * 4;  // 8192 entries per row chunk
@@ -241,6 +254,8 @@ struct TreeSmem {
   int x_maxi;
   int bad;
   int cut, cut_len;
+  float x_p, x_q;    // multi-candidate walk: the tested child's p~, q~
+  int x_next;        // multi-candidate walk: the next child
 };
 
 __device__ unsigned long long block_sum_u64(TreeSmem& sm, unsigned long long x) {
@@ -428,32 +443,41 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     __syncthreads();
   }
 
+  // p~, q~ of token x in the rows of local node j (a node with children)
+  auto node_pq = [&](int j, int x, float& p, float& q) {
+    const size_t row = static_cast<size_t>(n0 + j) * V;
+    p = __ldg(a.target + row + x);
+    q = __ldg(a.draft + row + x);
+    if (logits) p = expf(p - sm.lse[j]);
+    if (masked) {
+      if ((__ldg(a.mask + static_cast<size_t>(n0 + j) * W + (x >> 5)) >> (x & 31)) & 1u) {
+        const float z = sm.z[j];
+        p = __fdiv_rn(p, z);
+        q = __fdiv_rn(q, z);
+      } else {
+        p = 0.0f;
+        q = 0.0f;
+      }
+    }
+  };
+  const float gam = a.gamma ? a.gamma[b] : 1.0f;
+  const bool multi = a.test == 2;
+  bool m_rejected = false;  // multi-candidate: the final node's children were all rejected
+
   // ---------------------------------------------------------------- tests
   float my_p = 0.0f, my_q = 0.0f;
-  {
+  if (!multi) {
     const int i = tid;  // kTreeThreads == kMaxN: one node per thread
     bool acc = false;
     if (i >= 1 && i < N) {
       const int j = sm.parent[i];
       const int x = sm.token[i];
-      const size_t row = static_cast<size_t>(n0 + j) * V;
-      float p = __ldg(a.target + row + x);
-      float q = __ldg(a.draft + row + x);
-      if (logits) p = expf(p - sm.lse[j]);
-      if (masked) {
-        if ((__ldg(a.mask + static_cast<size_t>(n0 + j) * W + (x >> 5)) >> (x & 31)) & 1u) {
-          const float z = sm.z[j];
-          p = __fdiv_rn(p, z);
-          q = __fdiv_rn(q, z);
-        } else {
-          p = 0.0f;
-          q = 0.0f;
-        }
-      }
+      float p, q;
+      node_pq(j, x, p, q);
       my_p = p;
       my_q = q;
       const float u = sm.u[i];
-      const float g = a.gamma ? a.gamma[b] : 1.0f;
+      const float g = gam;
       if (a.test == 0) {
         // u < min(1, g * p~ / q~) as fl32(u * q~) < fl32(g * p~)
         acc = __fmul_rn(u, q) < __fmul_rn(g, p);
@@ -473,7 +497,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     if ((tid & 31) == 0) sm.acc_bits[tid >> 5] = bal;
   }
   __syncthreads();
-  {
+  if (!multi) {
     uint32_t key = 0;
     const int i = tid;
     if (i < N) {
@@ -496,6 +520,187 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     }
   }
   __syncthreads();
+
+  // ---------------------------------------------------------------- rows
+  // A row's chunk of this CTA, [lo, hi), goes to shared memory with
+  // cp.async; every pass then reads it coalesced.  The exact find walks
+  // contiguous 1024-entry warp spans in index order with warp scans.
+  const int chunk = bonus_chunk(V, C);
+  const int wspan = chunk / kTreeWarps;  // contiguous entries per warp (multiple of 32)
+  float* tbuf = smem_rows;               // p~ (or the current target of the walk)
+  float* dbuf = smem_rows + chunk;       // q~
+  float* rbuf = smem_rows + 2 * chunk;   // the walk's last residual (multi only)
+  uint32_t* mbuf = reinterpret_cast<uint32_t*>(smem_rows + (multi ? 3 : 2) * chunk);
+  const int lo = min(V, rank * chunk), hi = min(V, lo + chunk);
+  const int n = hi - lo;
+  auto in_set = [&](int e) -> bool { return !masked || ((mbuf[e >> 5] >> (e & 31)) & 1u); };
+  // Loads this CTA's chunk of local row `node` and turns it into p~, q~ in
+  // place (0 off the retained set).  LSE / Z come from the partials if the
+  // node has children (the same values its children were tested with), else
+  // they are reduced here across the cluster (at most once per call: the
+  // exchange slots are written once).  Called by every CTA of the cluster.
+  auto load_row = [&](int node) {
+    const size_t crow = static_cast<size_t>(n0 + node) * V;
+    {
+      const float* tsrc = a.target + crow + lo;
+      const float* dsrc = a.draft + crow + lo;
+      if (((crow + lo) & 3) == 0) {
+        const int n4 = n >> 2;
+        for (int k = tid; k < n4; k += kTreeThreads) {
+          cp_async16(tbuf + 4 * k, tsrc + 4 * k);
+          cp_async16(dbuf + 4 * k, dsrc + 4 * k);
+        }
+        for (int e = 4 * n4 + tid; e < n; e += kTreeThreads) {
+          cp_async4(tbuf + e, tsrc + e);
+          cp_async4(dbuf + e, dsrc + e);
+        }
+      } else {
+        for (int e = tid; e < n; e += kTreeThreads) {
+          cp_async4(tbuf + e, tsrc + e);
+          cp_async4(dbuf + e, dsrc + e);
+        }
+      }
+      if (masked) {  // lo is a multiple of 32: whole mask words
+        const uint32_t* msrc = a.mask + static_cast<size_t>(n0 + node) * W + (lo >> 5);
+        for (int k = tid; k < (n + 31) >> 5; k += kTreeThreads) mbuf[k] = __ldg(msrc + k);
+      }
+      cp_async_wait_all();
+      __syncthreads();
+    }
+    float lse = 0.0f, z = 1.0f;
+    if (stats) {
+      if (sm.has_child[node]) {
+        if (logits) lse = sm.lse[node];
+        if (masked) z = sm.z[node];
+      } else {
+        float m = -INFINITY;
+        unsigned long long zs = 0;
+        for (int e = tid; e < n; e += kTreeThreads) {
+          if (logits) m = fmaxf(m, tbuf[e]);
+          if (masked && in_set(e)) zs += fix40(dbuf[e]);
+        }
+        if (logits) m = block_max_f32(sm, m);
+        if (masked) zs = block_sum_u64(sm, zs);
+        if (tid == 0) {
+          sm.x_m = m;
+          sm.x_z = zs;
+        }
+        cluster.sync();
+        const float M = cluster_max(cluster, &sm.x_m, C);
+        const unsigned long long Z = cluster_sum(cluster, &sm.x_z, C, rank,
+                                                 static_cast<unsigned long long*>(nullptr));
+        z = z_from_sum(Z);
+        if (logits) {
+          float ssum = 0.0f;
+          if (M != -INFINITY)
+            for (int e = tid; e < n; e += kTreeThreads) ssum += expf(tbuf[e] - M);
+          ssum = block_sum_f32(sm, ssum);
+          if (tid == 0) sm.x_s = ssum;
+          cluster.sync();
+          // the same reduction order in every CTA: the same value everywhere
+          const float Ssum = cluster_sum(cluster, &sm.x_s, C, rank, static_cast<float*>(nullptr));
+          lse = M + logf(Ssum);
+        }
+      }
+    }
+    // p~ and q~ in place (0 off the retained set)
+    for (int e = tid; e < n; e += kTreeThreads) {
+      const bool in = in_set(e);
+      float p = logits ? expf(tbuf[e] - lse) : tbuf[e];
+      float q = dbuf[e];
+      if (masked) {
+        p = __fdiv_rn(p, z);
+        q = __fdiv_rn(q, z);
+      }
+      tbuf[e] = in ? p : 0.0f;
+      dbuf[e] = in ? q : 0.0f;
+    }
+    __syncthreads();
+  };
+
+  // ------------------------------------------------------ multi-candidate walk
+  // Every CTA of the cluster runs the same walk and takes the same decisions:
+  // the tested values come from one place (the global rows before the first
+  // rejection at a node, the owning CTA's chunk after it) and every sum is an
+  // exact integer combined in rank order.
+  if (multi) {
+    // first child of node j after node `after` (children have larger indices)
+    auto next_child = [&](int j, int after) -> int {
+      const int i = tid;
+      const uint32_t key = (i > after && i < N && sm.parent[i] == j) ? 0xFFFFu - static_cast<uint32_t>(i) : 0u;
+      const uint32_t k = block_max_u32(sm, key);
+      return k ? static_cast<int>(0xFFFFu - k) : -1;
+    };
+    int j = 0, len = 0;
+    for (;;) {
+      int c = next_child(j, j);
+      bool loaded = false, accepted = false;
+      m_rejected = false;
+      while (c >= 0) {
+        const int x = sm.token[c];
+        if (!loaded) {
+          if (tid == 0) {
+            float p, q;
+            node_pq(j, x, p, q);
+            sm.x_p = p;
+            sm.x_q = q;
+          }
+        } else if (tid == 0) {  // the current target lives in the chunk of CTA x / chunk
+          const int owner = x / chunk;
+          sm.x_p = *cluster.map_shared_rank(tbuf + (x - owner * chunk), owner);
+          sm.x_q = *cluster.map_shared_rank(dbuf + (x - owner * chunk), owner);
+        }
+        __syncthreads();
+        const float p = sm.x_p, q = sm.x_q;
+        if (tid == c) {
+          my_p = p;
+          my_q = q;
+        }
+        if (__fmul_rn(sm.u[c], q) < __fmul_rn(gam, p)) {
+          accepted = true;
+          break;
+        }
+        // rejected: cur <- max(0, cur - q~) / N over the cluster
+        if (loaded) cluster.sync();  // every CTA has read the tested value above
+        if (!loaded) {
+          load_row(j);
+          loaded = true;
+        }
+        unsigned long long part = 0;
+        for (int e = tid; e < n; e += kTreeThreads) {
+          const float d = __fsub_rn(tbuf[e], dbuf[e]);
+          const float r = d > 0.0f ? d : 0.0f;
+          rbuf[e] = r;
+          part += fix40(r);
+        }
+        part = block_sum_u64(sm, part);
+        if (tid == 0) sm.x_u64[0] = part;
+        cluster.sync();
+        const unsigned long long S = cluster_sum(cluster, &sm.x_u64[0], C, rank,
+                                                 static_cast<unsigned long long*>(nullptr));
+        if (S > 0) {
+          const float Nf = z_from_sum(S);
+          for (int e = tid; e < n; e += kTreeThreads) tbuf[e] = __fdiv_rn(rbuf[e], Nf);
+        }
+        m_rejected = true;
+        cluster.sync();  // the new current target and every slot read before reuse
+        c = next_child(j, c);
+      }
+      if (accepted) {
+        if (loaded) cluster.sync();  // the chunk is read before the next node's load
+        ++len;
+        j = c;
+        continue;
+      }
+      if (tid == 0) {
+        sm.cut = j;
+        sm.cut_len = len;
+      }
+      __syncthreads();
+      break;
+    }
+  }
+
   const int cut = sm.cut;
   const int len = sm.cut_len;
   if (rank == 0) {
@@ -514,103 +719,20 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
   }
 
   // ---------------------------------------------------------------- bonus
-  // The cut row's chunk of this CTA, [lo, hi), goes to shared memory with
-  // cp.async; every pass then reads it coalesced.  The exact find walks
-  // contiguous 1024-entry warp spans in index order with warp scans.
-  const int chunk = bonus_chunk(V, C);
-  const int wspan = chunk / kTreeWarps;  // contiguous entries per warp (multiple of 32)
-  float* tbuf = smem_rows;
-  float* dbuf = smem_rows + chunk;
-  uint32_t* mbuf = reinterpret_cast<uint32_t*>(smem_rows + 2 * chunk);
-  const int lo = min(V, rank * chunk), hi = min(V, lo + chunk);
-  const int n = hi - lo;
-  const size_t crow = static_cast<size_t>(n0 + cut) * V;
-  {
-    const float* tsrc = a.target + crow + lo;
-    const float* dsrc = a.draft + crow + lo;
-    if (((crow + lo) & 3) == 0) {
-      const int n4 = n >> 2;
-      for (int k = tid; k < n4; k += kTreeThreads) {
-        cp_async16(tbuf + 4 * k, tsrc + 4 * k);
-        cp_async16(dbuf + 4 * k, dsrc + 4 * k);
-      }
-      for (int e = 4 * n4 + tid; e < n; e += kTreeThreads) {
-        cp_async4(tbuf + e, tsrc + e);
-        cp_async4(dbuf + e, dsrc + e);
-      }
-    } else {
-      for (int e = tid; e < n; e += kTreeThreads) {
-        cp_async4(tbuf + e, tsrc + e);
-        cp_async4(dbuf + e, dsrc + e);
-      }
-    }
-    if (masked) {  // lo is a multiple of 32: whole mask words
-      const uint32_t* msrc = a.mask + static_cast<size_t>(n0 + cut) * W + (lo >> 5);
-      for (int k = tid; k < (n + 31) >> 5; k += kTreeThreads) mbuf[k] = __ldg(msrc + k);
-    }
-    cp_async_wait_all();
-    __syncthreads();
-  }
-  auto in_set = [&](int e) -> bool { return !masked || ((mbuf[e >> 5] >> (e & 31)) & 1u); };
-
-  // LSE / Z of the cut row: from the partials if it has children (the same
-  // values its children were tested with), else reduced here across the cluster
-  float lse = 0.0f, z = 1.0f;
-  if (stats) {
-    if (sm.has_child[cut]) {
-      if (logits) lse = sm.lse[cut];
-      if (masked) z = sm.z[cut];
-    } else {
-      float m = -INFINITY;
-      unsigned long long zs = 0;
-      for (int e = tid; e < n; e += kTreeThreads) {
-        if (logits) m = fmaxf(m, tbuf[e]);
-        if (masked && in_set(e)) zs += fix40(dbuf[e]);
-      }
-      if (logits) m = block_max_f32(sm, m);
-      if (masked) zs = block_sum_u64(sm, zs);
-      if (tid == 0) {
-        sm.x_m = m;
-        sm.x_z = zs;
-      }
-      cluster.sync();
-      const float M = cluster_max(cluster, &sm.x_m, C);
-      const unsigned long long Z = cluster_sum(cluster, &sm.x_z, C, rank,
-                                               static_cast<unsigned long long*>(nullptr));
-      z = z_from_sum(Z);
-      if (logits) {
-        float ssum = 0.0f;
-        if (M != -INFINITY)
-          for (int e = tid; e < n; e += kTreeThreads) ssum += expf(tbuf[e] - M);
-        ssum = block_sum_f32(sm, ssum);
-        if (tid == 0) sm.x_s = ssum;
-        cluster.sync();
-        // the same reduction order in every CTA: the same value everywhere
-        const float Ssum = cluster_sum(cluster, &sm.x_s, C, rank, static_cast<float*>(nullptr));
-        lse = M + logf(Ssum);
-      }
-    }
-  }
-  // p~ and q~ of the cut row in place (0 off the retained set)
-  for (int e = tid; e < n; e += kTreeThreads) {
-    const bool in = in_set(e);
-    float p = logits ? expf(tbuf[e] - lse) : tbuf[e];
-    float q = dbuf[e];
-    if (masked) {
-      p = __fdiv_rn(p, z);
-      q = __fdiv_rn(q, z);
-    }
-    tbuf[e] = in ? p : 0.0f;
-    dbuf[e] = in ? q : 0.0f;
-  }
-  __syncthreads();
+  // The cut row (already in shared memory when the walk rejected children
+  // there); pass 0 draws from the residual, pass 1 from p~ (or the current
+  // target of the walk).
+  if (!(multi && m_rejected)) load_row(cut);
+  const bool from_residual = multi ? m_rejected : (sm.has_child[cut] != 0);
 
   const float u0 = sm.u[0];
   bool drawn = false;
   const int warp = tid >> 5, lane = tid & 31;
-  for (int pass = sm.has_child[cut] ? 0 : 1; pass < 2 && !drawn; ++pass) {
+  for (int pass = from_residual ? 0 : 1; pass < 2 && !drawn; ++pass) {
     auto quantum = [&](int e) -> unsigned long long {
-      return e < n ? fix40(pass == 0 ? __fsub_rn(tbuf[e], dbuf[e]) : tbuf[e]) : 0ull;
+      if (e >= n) return 0ull;
+      if (pass == 1) return fix40(tbuf[e]);
+      return fix40(multi ? rbuf[e] : __fsub_rn(tbuf[e], dbuf[e]));
     };
     // per-warp sums over contiguous spans [warp*wspan, +wspan)
     unsigned long long wsum = 0;
@@ -993,13 +1115,13 @@ int launch_accept(const AcceptArgs& a, void* workspace, cudaStream_t stream) {
   if (attr_dev != dev) {
     cudaFuncSetAttribute(accept_tree_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaFuncSetAttribute(accept_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         tree_smem_bytes(16384));
+                         tree_smem_bytes(16384, true));
     attr_dev = dev;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, a.batch, 1);
   cfg.blockDim = dim3(kTreeThreads, 1, 1);
-  cfg.dynamicSmemBytes = tree_smem_bytes(bonus_chunk(a.vocab, C));
+  cfg.dynamicSmemBytes = tree_smem_bytes(bonus_chunk(a.vocab, C), a.test == 2);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -231,7 +231,9 @@ int tv_accept_ex(const tv_accept_params* p, const tv_accept_options* opt, const 
                  int32_t* bonus_token, int32_t* status, float* debug_pq, void* workspace,
                  size_t workspace_bytes, cudaStream_t stream) {
   if (!p) return TV_ERR_INVALID_ARG;
-  if (opt && opt->test != TV_TEST_RATIO && opt->test != TV_TEST_LOG_CLAMP) return TV_ERR_INVALID_ARG;
+  if (opt && opt->test != TV_TEST_RATIO && opt->test != TV_TEST_LOG_CLAMP &&
+      opt->test != TV_TEST_MULTI)
+    return TV_ERR_INVALID_ARG;
   if (opt && !(opt->log_clamp >= 0.0f && opt->log_clamp <= 88.0f)) return TV_ERR_INVALID_ARG;
   if (opt && opt->gamma && !aligned16(opt->gamma)) return TV_ERR_INVALID_ARG;
   if (p->batch < 1 || p->vocab < 1 || p->vocab >= (1 << 18)) return TV_ERR_INVALID_ARG;

@@ -149,7 +149,7 @@ def test_commit_argument_errors_before_launch(lib):
     assert tv.status_string(tv.TV_ERR_NO_PAGE) == "TV_ERR_NO_PAGE"
 
 
-@pytest.mark.parametrize("bad", [dict(test=2), dict(log_clamp=-1.0), dict(log_clamp=100.0),
+@pytest.mark.parametrize("bad", [dict(test=3), dict(test=-1), dict(log_clamp=-1.0), dict(log_clamp=100.0),
                                  dict(log_clamp=float("nan"))])
 def test_accept_options_checked_before_launch(lib, bad):
     p = tv.AcceptParams(batch=2, vocab=1000, max_nodes=16, total_nodes=20, kind=0)
