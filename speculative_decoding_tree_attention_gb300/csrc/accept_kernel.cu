@@ -412,6 +412,19 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     return;
   }
   for (int i = tid + 1; i < N; i += kTreeThreads) sm.has_child[sm.parent[i]] = 1;
+  // The tested entries do not depend on the row statistics: thread i reads
+  // node i's target and draft entries (and mask bit) before waiting for them.
+  // Everything before the row-statistics kernel in the stream has completed.
+  const bool multi = a.test == 2;
+  float raw_p = 0.0f, raw_q = 0.0f;
+  uint32_t raw_in = 1u;
+  if (!multi && tid >= 1 && tid < N) {
+    const int j = sm.parent[tid], x = sm.token[tid];
+    const size_t row = static_cast<size_t>(n0 + j) * V;
+    raw_p = __ldg(a.target + row + x);
+    raw_q = __ldg(a.draft + row + x);
+    if (masked) raw_in = (__ldg(a.mask + static_cast<size_t>(n0 + j) * W + (x >> 5)) >> (x & 31)) & 1u;
+  }
   // the row statistics come from the previous kernel in the stream
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
@@ -443,14 +456,12 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     __syncthreads();
   }
 
-  // p~, q~ of token x in the rows of local node j (a node with children)
-  auto node_pq = [&](int j, int x, float& p, float& q) {
-    const size_t row = static_cast<size_t>(n0 + j) * V;
-    p = __ldg(a.target + row + x);
-    q = __ldg(a.draft + row + x);
+  // p~, q~ of a tested entry of the rows of local node j (a node with
+  // children) from its raw target value p, draft value q and mask bit
+  auto tilde = [&](int j, float& p, float& q, uint32_t in) {
     if (logits) p = expf(p - sm.lse[j]);
     if (masked) {
-      if ((__ldg(a.mask + static_cast<size_t>(n0 + j) * W + (x >> 5)) >> (x & 31)) & 1u) {
+      if (in) {
         const float z = sm.z[j];
         p = __fdiv_rn(p, z);
         q = __fdiv_rn(q, z);
@@ -460,8 +471,16 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
       }
     }
   };
+  // the same for token x, read here
+  auto node_pq = [&](int j, int x, float& p, float& q) {
+    const size_t row = static_cast<size_t>(n0 + j) * V;
+    p = __ldg(a.target + row + x);
+    q = __ldg(a.draft + row + x);
+    const uint32_t in =
+        masked ? (__ldg(a.mask + static_cast<size_t>(n0 + j) * W + (x >> 5)) >> (x & 31)) & 1u : 1u;
+    tilde(j, p, q, in);
+  };
   const float gam = a.gamma ? a.gamma[b] : 1.0f;
-  const bool multi = a.test == 2;
   bool m_rejected = false;  // multi-candidate: the final node's children were all rejected
 
   // ---------------------------------------------------------------- tests
@@ -471,9 +490,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     bool acc = false;
     if (i >= 1 && i < N) {
       const int j = sm.parent[i];
-      const int x = sm.token[i];
-      float p, q;
-      node_pq(j, x, p, q);
+      float p = raw_p, q = raw_q;
+      tilde(j, p, q, raw_in);
       my_p = p;
       my_q = q;
       const float u = sm.u[i];

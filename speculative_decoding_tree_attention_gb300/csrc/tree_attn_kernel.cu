@@ -295,14 +295,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
 
   // ------------------------------------------------------------ work item
-  // Grid z enumerates (sequence rank, KV head).  For batches up to
+  // Grid z enumerates (sequence rank, KV head).  For batches of 2 up to
   // kOrderMax the rank orders the sequences by decreasing work (prefix plus
   // tree keys, ties by index), so that the CTAs that run longest are
   // dispatched first and the launch does not end on a tail of long CTAs.
   // The extents of all sequences are loaded first; barrier set-up and the
   // TMEM allocation below overlap the load latency.
   int* seq = reinterpret_cast<int*>(smem + Ly::kSeq);  // [4][kOrderMax]
-  const bool ordered = a.batch <= kOrderMax;
+  const bool ordered = a.batch > 1 && a.batch <= kOrderMax;
   if (ordered && tid < a.batch) {
     seq[tid] = max(0, __ldg(a.prefix_lens + tid));
     seq[kOrderMax + tid] = __ldg(a.node_offsets + tid);
