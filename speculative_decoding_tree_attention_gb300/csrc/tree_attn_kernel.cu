@@ -37,10 +37,11 @@
 //                      tile overlap the loads and maxima of the next.
 // K and V use the 128-byte swizzle that TMA writes, so the MMA reads them
 // straight from the ring; Q and P never touch shared memory.  Long prefixes
-// are split over CTAs (split-KV): each split writes (O, m, l) in fp32 and the
-// last split of a tile to finish combines them.  Every wait on an mbarrier is bounded; on expiry
-// the CTA reports TV_ERR_DEVICE_TIMEOUT for its sequence, drains its copies
-// and returns.
+// may be split over CTAs (split-KV): the splits of a tile run as one
+// thread-block cluster, each keeps its (O, m, l) in fp32 in its own shared
+// memory, and the cluster combines them through distributed shared memory.
+// Every wait on an mbarrier is bounded; on expiry the CTA reports
+// TV_ERR_DEVICE_TIMEOUT for its sequence, drains its copies and returns.
 #include <climits>
 
 #include <cooperative_groups.h>
