@@ -92,6 +92,15 @@ def test_many_sequences_many_splits():
     full_compare(case, "split-kv varlen")
 
 
+@pytest.mark.parametrize("batch", [256, 300])
+def test_batch_at_and_past_the_ordering_limit(batch):
+    # up to 256 sequences the CTAs take the sequences longest first; past
+    # that they take them in batch order
+    cfg = wl.config(3, batch=batch, hq=2, hkv=1, prefix=(0, 300), n=(1, 6))
+    case = wl.make_case(cfg, parts=("attn",))
+    full_compare(case, f"batch {batch}")
+
+
 def test_max_nodes_512_chain():
     cfg = wl.config(2, batch=1, hq=2, hkv=2, d=64, prefix=(40, 40))
     cfg["parent"] = [[-1] + list(range(511))]
