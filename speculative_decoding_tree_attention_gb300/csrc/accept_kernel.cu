@@ -1107,16 +1107,32 @@ __global__ void __launch_bounds__(kRsThreads, 1)
 
 int accept_chunks(int vocab) { return (vocab + kChunk - 1) / kChunk; }
 
-int accept_cluster_size(int vocab) {
+// CTAs per tree: 1, 2, 4, 8 or 16, about one per kMinChunk entries of the
+// vocabulary; halved while the trees' clusters would not fit one wave of
+// `sms` SMs, but never below what keeps a CTA's chunk within 16384 entries
+// (the shared-memory size the kernel is set up for).
+int accept_cluster_size(int vocab, int batch, int sms) {
   const int want = (vocab + kMinChunk - 1) / kMinChunk;
   int c = 1;
-  while (c < want && c < kMaxCluster) c *= 2;  // 1, 2, 4, 8 or 16 CTAs per tree
+  while (c < want && c < kMaxCluster) c *= 2;
+  int c_min = 1;
+  while (c_min < kMaxCluster && static_cast<long>(c_min) * 16384 < vocab) c_min *= 2;
+  while (c > c_min && static_cast<long>(batch) * c > sms) c /= 2;
   return c;
 }
 
 int launch_accept(const AcceptArgs& a, void* workspace, cudaStream_t stream) {
   const int nchunk = accept_chunks(a.vocab);
-  const int C = accept_cluster_size(a.vocab);
+  static thread_local int sms_dev = -1, sms = 148;
+  {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev != sms_dev &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
+      sms = n;
+      sms_dev = dev;
+    }
+  }
+  const int C = accept_cluster_size(a.vocab, a.batch, sms);
   float2* ws_ms = static_cast<float2*>(workspace);
   unsigned long long* ws_z = reinterpret_cast<unsigned long long*>(
       static_cast<char*>(workspace) + sizeof(float2) * static_cast<size_t>(a.total_nodes) * nchunk);

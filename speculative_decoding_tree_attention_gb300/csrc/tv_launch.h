@@ -50,7 +50,7 @@ struct RetainArgs {
 int launch_retained_set(const RetainArgs& a, cudaStream_t stream);
 int retained_cluster_size(int vocab);
 size_t accept_workspace_bytes(int vocab, int total_nodes);
-int accept_cluster_size(int vocab);
+int accept_cluster_size(int vocab, int batch, int sms);
 int accept_max_nodes();
 
 struct AttnArgs {
