@@ -14,10 +14,12 @@
 //
 // Two kernels, one call, no host round trip:
 //   accept_rowstats_kernel  (only for logits input or a retained-set mask)
-//       one CTA per (row with children, 8K-entry chunk of the vocabulary)
-//       over the whole batch: all loads of the chunk issued at once (128-bit),
-//       then the partial log-sum-exp (max, sum of exp) of the target logits
-//       and/or the partial retained draft mass in exact 2^-40 fixed point.
+//       nparts CTAs per row of the batch (rows without children exit after
+//       finding their tree); CTA k of a row takes every nparts-th 8K-entry
+//       chunk, each with all its loads issued at once (128-bit), and keeps
+//       per thread a running log-sum-exp (max, sum of exp) of the target
+//       logits and/or the retained draft mass in exact 2^-40 fixed point;
+//       one partial per CTA.  nparts gives about four CTAs per SM.
 //   accept_tree_kernel      one thread-block cluster per tree, launched with
 //       programmatic dependent launch so it is resident when the first kernel
 //       ends.  Phase 1: every node's p~, q~ from the combined partials (fixed
@@ -127,14 +129,15 @@ __device__ bool block_has_child(const int32_t* parent, int n0, int N, int j) {
 }
 
 // ============================================================ row statistics
-__global__ void __launch_bounds__(kRowThreads)
-    accept_rowstats_kernel(const AcceptArgs a, int nchunk, float2* ws_ms, unsigned long long* ws_z) {
+__global__ void __launch_bounds__(kRowThreads, 3)
+    accept_rowstats_kernel(const AcceptArgs a, int nchunk, int nparts, float2* ws_ms,
+                           unsigned long long* ws_z) {
   // the per-tree kernel may start now: its prologue (tree loads and checks)
   // overlaps this kernel; it waits for our results in griddepcontrol.wait
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long item = blockIdx.x;
-  const int g = static_cast<int>(item / nchunk);  // global row
-  const int c = static_cast<int>(item % nchunk);
+  const int g = static_cast<int>(item / nparts);  // global row
+  const int part = static_cast<int>(item % nparts);
   if (g >= a.total_nodes) return;
   // tree of row g (binary search over node_offsets)
   int lo = 0, hi = a.batch;
@@ -149,7 +152,6 @@ __global__ void __launch_bounds__(kRowThreads)
   if (!block_has_child(a.parent, n0, N, j)) return;  // nobody reads this row's statistics
 
   const int V = a.vocab;
-  const int v0 = c * kChunk, v1 = min(V, v0 + kChunk);
   const size_t rowbase = static_cast<size_t>(g) * V;
   const bool vec = (rowbase & 3) == 0;
   const bool logits = a.kind == 1;
@@ -157,54 +159,61 @@ __global__ void __launch_bounds__(kRowThreads)
   const int W = (V + 31) >> 5;
   const uint32_t* mrow = masked ? a.mask + static_cast<size_t>(g) * W : nullptr;
 
+  // this CTA's chunks c = part, part + nparts, ...: each thread keeps one
+  // running (max, sum of exp) and one exact fixed-point sum over all of them
   float m = -INFINITY, s = 0.0f;
   unsigned long long z = 0;
-  if (vec) {
-    float4 tv[kRowVec], dv[kRowVec];
-#pragma unroll
-    for (int k = 0; k < kRowVec; ++k) {
-      const int v = v0 + (k * kRowThreads + threadIdx.x) * 4;
-      tv[k] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      dv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (v + 3 < v1) {
-        if (logits) tv[k] = __ldg(reinterpret_cast<const float4*>(a.target + rowbase + v));
-        if (masked) dv[k] = __ldg(reinterpret_cast<const float4*>(a.draft + rowbase + v));
-      } else {
-        float* tp = &tv[k].x;
-        float* dp = &dv[k].x;
-        for (int e = 0; e < 4 && v + e < v1; ++e) {
-          if (logits) tp[e] = __ldg(a.target + rowbase + v + e);
-          if (masked) dp[e] = __ldg(a.draft + rowbase + v + e);
-        }
-      }
-    }
-    if (logits) {  // max first, then independent exponentials
-#pragma unroll
-      for (int k = 0; k < kRowVec; ++k)
-        m = fmaxf(m, fmaxf(fmaxf(tv[k].x, tv[k].y), fmaxf(tv[k].z, tv[k].w)));
-      if (m != -INFINITY) {
-#pragma unroll
-        for (int k = 0; k < kRowVec; ++k)
-          s += (expf(tv[k].x - m) + expf(tv[k].y - m)) + (expf(tv[k].z - m) + expf(tv[k].w - m));
-      }
-      if (m != m) s = m;  // a NaN logit makes the row NaN
-    }
-    if (masked) {
+  for (int c = part; c < nchunk; c += nparts) {
+    const int v0 = c * kChunk, v1 = min(V, v0 + kChunk);
+    if (vec) {
+      float4 tv[kRowVec], dv[kRowVec];
 #pragma unroll
       for (int k = 0; k < kRowVec; ++k) {
         const int v = v0 + (k * kRowThreads + threadIdx.x) * 4;
-        if (v >= v1) continue;
-        const uint32_t w = __ldg(mrow + (v >> 5)) >> (v & 31);
-        if ((w & 1u) && v < v1) z += fix40(dv[k].x);
-        if ((w & 2u) && v + 1 < v1) z += fix40(dv[k].y);
-        if ((w & 4u) && v + 2 < v1) z += fix40(dv[k].z);
-        if ((w & 8u) && v + 3 < v1) z += fix40(dv[k].w);
+        tv[k] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        dv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (v + 3 < v1) {
+          if (logits) tv[k] = __ldg(reinterpret_cast<const float4*>(a.target + rowbase + v));
+          if (masked) dv[k] = __ldg(reinterpret_cast<const float4*>(a.draft + rowbase + v));
+        } else {
+          float* tp = &tv[k].x;
+          float* dp = &dv[k].x;
+          for (int e = 0; e < 4 && v + e < v1; ++e) {
+            if (logits) tp[e] = __ldg(a.target + rowbase + v + e);
+            if (masked) dp[e] = __ldg(a.draft + rowbase + v + e);
+          }
+        }
       }
-    }
-  } else {
-    for (int e = v0 + threadIdx.x; e < v1; e += kRowThreads) {
-      if (logits) lse_push(m, s, __ldg(a.target + rowbase + e));
-      if (masked && ((__ldg(mrow + (e >> 5)) >> (e & 31)) & 1u)) z += fix40(__ldg(a.draft + rowbase + e));
+      if (logits) {  // the chunk's max first, then independent exponentials
+        float cm = -INFINITY, cs = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kRowVec; ++k)
+          cm = fmaxf(cm, fmaxf(fmaxf(tv[k].x, tv[k].y), fmaxf(tv[k].z, tv[k].w)));
+        if (cm != -INFINITY) {
+#pragma unroll
+          for (int k = 0; k < kRowVec; ++k)
+            cs += (expf(tv[k].x - cm) + expf(tv[k].y - cm)) + (expf(tv[k].z - cm) + expf(tv[k].w - cm));
+        }
+        if (cm != cm) cs = cm;  // a NaN logit makes the row NaN
+        lse_combine(m, s, cm, cs);
+      }
+      if (masked) {
+#pragma unroll
+        for (int k = 0; k < kRowVec; ++k) {
+          const int v = v0 + (k * kRowThreads + threadIdx.x) * 4;
+          if (v >= v1) continue;
+          const uint32_t w = __ldg(mrow + (v >> 5)) >> (v & 31);
+          if ((w & 1u) && v < v1) z += fix40(dv[k].x);
+          if ((w & 2u) && v + 1 < v1) z += fix40(dv[k].y);
+          if ((w & 4u) && v + 2 < v1) z += fix40(dv[k].z);
+          if ((w & 8u) && v + 3 < v1) z += fix40(dv[k].w);
+        }
+      }
+    } else {
+      for (int e = v0 + threadIdx.x; e < v1; e += kRowThreads) {
+        if (logits) lse_push(m, s, __ldg(a.target + rowbase + e));
+        if (masked && ((__ldg(mrow + (e >> 5)) >> (e & 31)) & 1u)) z += fix40(__ldg(a.draft + rowbase + e));
+      }
     }
   }
   // block reduction
@@ -358,7 +367,7 @@ __device__ __forceinline__ float cluster_max(cg::cluster_group& cluster, const f
 }
 
 __global__ void __launch_bounds__(kTreeThreads, 1)
-    accept_tree_kernel(const AcceptArgs a, int nchunk, const float2* ws_ms,
+    accept_tree_kernel(const AcceptArgs a, int nparts, const float2* ws_ms,
                        const unsigned long long* ws_z) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = static_cast<int>(cluster.num_blocks());
@@ -432,8 +441,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
   // LSE / Z of local row j (a row with children) from the partials, fixed order
   auto row_lse = [&](int j) -> float {
     float m = -INFINITY, s = 0.0f;
-    const float2* p = ws_ms + static_cast<size_t>(n0 + j) * nchunk;
-    for (int c = 0; c < nchunk; ++c) {
+    const float2* p = ws_ms + static_cast<size_t>(n0 + j) * nparts;
+    for (int c = 0; c < nparts; ++c) {
       const float2 e = p[c];
       lse_combine(m, s, e.x, e.y);
     }
@@ -441,8 +450,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
   };
   auto row_z = [&](int j) -> float {
     unsigned long long S = 0;
-    const unsigned long long* p = ws_z + static_cast<size_t>(n0 + j) * nchunk;
-    for (int c = 0; c < nchunk; ++c) S += p[c];
+    const unsigned long long* p = ws_z + static_cast<size_t>(n0 + j) * nparts;
+    for (int c = 0; c < nparts; ++c) S += p[c];
     return z_from_sum(S);
   };
 
@@ -1137,9 +1146,12 @@ int launch_accept(const AcceptArgs& a, void* workspace, cudaStream_t stream) {
   unsigned long long* ws_z = reinterpret_cast<unsigned long long*>(
       static_cast<char*>(workspace) + sizeof(float2) * static_cast<size_t>(a.total_nodes) * nchunk);
   const bool stats = a.kind == 1 || a.mask != nullptr;
+  // CTAs per row: enough for about four CTAs per SM over all rows (most of
+  // which are leaves and exit at once); each takes every nparts-th chunk
+  const int nparts = max(1, min(nchunk, static_cast<int>((4l * sms + a.total_nodes - 1) / a.total_nodes)));
   if (stats) {
-    const long items = static_cast<long>(a.total_nodes) * nchunk;
-    accept_rowstats_kernel<<<static_cast<unsigned>(items), kRowThreads, 0, stream>>>(a, nchunk, ws_ms,
+    const long items = static_cast<long>(a.total_nodes) * nparts;
+    accept_rowstats_kernel<<<static_cast<unsigned>(items), kRowThreads, 0, stream>>>(a, nchunk, nparts, ws_ms,
                                                                                     ws_z);
     if (cudaGetLastError() != cudaSuccess) return -1;
   }
@@ -1166,7 +1178,7 @@ int launch_accept(const AcceptArgs& a, void* workspace, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = stats ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, accept_tree_kernel, a, nchunk,
+  return cudaLaunchKernelEx(&cfg, accept_tree_kernel, a, nparts,
                             static_cast<const float2*>(ws_ms),
                             static_cast<const unsigned long long*>(ws_z)) == cudaSuccess
              ? 0
