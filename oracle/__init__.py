@@ -46,6 +46,9 @@ class _AttnArgs(C.Structure):
         ("q", C.c_void_p), ("k_prefix", C.c_void_p), ("v_prefix", C.c_void_p),
         ("block_table", C.c_void_p), ("k_nodes", C.c_void_p), ("v_nodes", C.c_void_p),
         ("parent", C.c_void_p), ("prefix_lens", C.c_void_p), ("node_offsets", C.c_void_p),
+        ("dtype", C.c_int),
+        ("q_scale", C.c_void_p), ("k_prefix_scale", C.c_void_p), ("v_prefix_scale", C.c_void_p),
+        ("k_nodes_scale", C.c_void_p), ("v_nodes_scale", C.c_void_p),
     ]
 
 
@@ -97,9 +100,14 @@ def default_threads() -> int:
 
 
 def tree_attention_rows(case: dict, rows, nthreads: int | None = None) -> np.ndarray:
-    """fp64 outputs for the listed (b, local node, q head) rows -> [len(rows), D]."""
+    """fp64 outputs for the listed (b, local node, q head) rows -> [len(rows), D].
+    Inputs are bf16 bit patterns, or, when case["dtype"] == "e4m3", E4M3 codes
+    (uint8) with fp32 row scales case["<name>_scale"] (one per row of D)."""
     lib = _load()
-    keep = {k: _c(case[k], np.uint16) for k in ("q", "k_prefix", "v_prefix", "k_nodes", "v_nodes")}
+    e4m3 = case.get("dtype", "bf16") == "e4m3"
+    names = ("q", "k_prefix", "v_prefix", "k_nodes", "v_nodes")
+    keep = {k: _c(case[k], np.uint8 if e4m3 else np.uint16) for k in names}
+    scales = {k: (_c(case[k + "_scale"], np.float32) if e4m3 else None) for k in names}
     for k in ("block_table", "parent", "prefix_lens", "node_offsets"):
         keep[k] = _c(case[k], np.int32)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
@@ -109,7 +117,8 @@ def tree_attention_rows(case: dict, rows, nthreads: int | None = None) -> np.nda
                      int(keep["block_table"].shape[1]), float(scale),
                      *[_ptr(keep[k]) for k in ("q", "k_prefix", "v_prefix", "block_table",
                                                "k_nodes", "v_nodes", "parent", "prefix_lens",
-                                               "node_offsets")])
+                                               "node_offsets")],
+                     1 if e4m3 else 0, *[_ptr(scales[k]) for k in names])
     out = np.zeros((rows.shape[0], d), dtype=np.float64)
     rc = lib.oracle_tree_attention_rows(C.byref(args), rows.shape[0], _ptr(rows), _ptr(out),
                                         int(nthreads or default_threads()))
@@ -177,6 +186,14 @@ def accept(case: dict, nthreads: int | None = None, want_pq: bool = True, test: 
     if rc != 0:
         raise ValueError("oracle_accept: unsupported arguments")
     return out
+
+
+def e4m3_value(code: int) -> float:
+    """The oracle's decoding of one E4M3 code."""
+    lib = _load()
+    lib.oracle_e4m3_to_f64.restype = C.c_double
+    lib.oracle_e4m3_to_f64.argtypes = [C.c_uint8]
+    return float(lib.oracle_e4m3_to_f64(code))
 
 
 def quantise(r: float) -> int:

@@ -25,6 +25,13 @@
  *       -inf.  Ancestry is decided literally, by walking parent pointers up from
  *       i (parent = -1 at the root, [EC] appendix B "Tree_Parent_Idx").
  *       Softmax with max subtraction and the weighted sum of V, all in fp64.
+ *       Inputs are bf16, or E4M3 codes with one fp32 scale per row of D
+ *       elements (the FP8 KV cache with per-block scales that [EC] §9.3 and
+ *       [LLM] §9.1 mention; one block = one row of a token and head): each
+ *       element is decoded from the E4M3 definition (1 sign, 4 exponent bits
+ *       with bias 7, 3 mantissa bits; exponent field 0 is subnormal; the
+ *       all-ones pattern S.1111.111 is NaN; no infinities) and multiplied by
+ *       its row's scale, exactly, in fp64.
  *
  *   oracle_accept -- the fused accept pass, one tree at a time:
  *       1. p, q of node i taken from the rows of its parent (the distribution
@@ -82,6 +89,18 @@ static double bf16_to_f64(uint16_t bits) {
   return (double)f;
 }
 
+/* E4M3 -> fp64 from the definition. */
+static double e4m3_to_f64(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);          /* subnormal: 2^-6 * m/8 */
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7); /* normal: 2^(e-7) * (1 + m/8) */
+  return sign ? -v : v;
+}
+
 /* Is j an ancestor of i, or i itself?  Literal parent-pointer walk. */
 static int visible_tree_key(const int32_t *parent_local, int i, int j) {
   int k = i;
@@ -95,16 +114,35 @@ static int visible_tree_key(const int32_t *parent_local, int i, int j) {
 typedef struct {
   int batch, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq;
   double scale;
-  const uint16_t *q;          /* [total_nodes][Hq][D] bf16 bits         */
-  const uint16_t *k_prefix;   /* [num_blocks][Hkv][block_size][D] bf16  */
-  const uint16_t *v_prefix;
+  const void *q;              /* [total_nodes][Hq][D] bf16 bits (or E4M3) */
+  const void *k_prefix;       /* [num_blocks][Hkv][block_size][D]        */
+  const void *v_prefix;
   const int32_t *block_table; /* [batch][max_blocks_per_seq]             */
-  const uint16_t *k_nodes;    /* [total_nodes][Hkv][D] bf16              */
-  const uint16_t *v_nodes;
+  const void *k_nodes;        /* [total_nodes][Hkv][D]                   */
+  const void *v_nodes;
   const int32_t *parent;      /* [total_nodes], local, -1 at the root    */
   const int32_t *prefix_lens; /* [batch]                                 */
   const int32_t *node_offsets;/* [batch+1]                               */
+  int dtype;                  /* 0: bf16; 1: E4M3 codes with row scales  */
+  /* E4M3 only: one fp32 scale per row of D elements, indexed like the rows:
+   * q [total_nodes][Hq], k/v prefix [num_blocks][Hkv][block_size],
+   * k/v nodes [total_nodes][Hkv].  q, k_prefix, ... then point to uint8. */
+  const float *q_scale, *k_prefix_scale, *v_prefix_scale, *k_nodes_scale, *v_nodes_scale;
 } oracle_attn_args;
+
+/* Row `row` (D elements) of an input tensor, widened to fp64. */
+static void load_row(const oracle_attn_args *a, const void *base, const float *scales, size_t row,
+                     double *dst) {
+  const int D = a->head_dim;
+  if (a->dtype == 0) {
+    const uint16_t *p = (const uint16_t *)base + row * (size_t)D;
+    for (int d = 0; d < D; ++d) dst[d] = bf16_to_f64(p[d]);
+  } else {
+    const uint8_t *p = (const uint8_t *)base + row * (size_t)D;
+    const double sc = (double)scales[row];
+    for (int d = 0; d < D; ++d) dst[d] = e4m3_to_f64(p[d]) * sc;
+  }
+}
 
 typedef struct {
   const oracle_attn_args *a;
@@ -122,27 +160,25 @@ static void attn_one_row(const oracle_attn_args *a, int b, int i, int h, double 
   const int L = a->prefix_lens[b];
   const int n0 = a->node_offsets[b], N = a->node_offsets[b + 1] - n0;
   const int nkeys = L + N;
-  const uint16_t *q = a->q + ((size_t)(n0 + i) * Hq + h) * D;
   double *s = (double *)malloc(sizeof(double) * (size_t)(nkeys > 0 ? nkeys : 1));
   unsigned char *vis = (unsigned char *)malloc((size_t)(nkeys > 0 ? nkeys : 1));
-  double qd[512];
-  for (int d = 0; d < D; ++d) qd[d] = bf16_to_f64(q[d]);
+  double qd[512], kv[512];
+  load_row(a, a->q, a->q_scale, (size_t)(n0 + i) * Hq + h, qd);
 
   /* 1. key list [prefix 0..L-1 ; tree nodes 0..N-1] and dense scores */
   for (int t = 0; t < nkeys; ++t) {
-    const uint16_t *k;
     if (t < L) {
       int page = a->block_table[(size_t)b * a->max_blocks_per_seq + t / a->block_size];
       int slot = t % a->block_size;
-      k = a->k_prefix + (((size_t)page * Hkv + kvh) * a->block_size + slot) * D;
+      load_row(a, a->k_prefix, a->k_prefix_scale, ((size_t)page * Hkv + kvh) * a->block_size + slot, kv);
       vis[t] = 1; /* the committed prefix is visible to every node */
     } else {
       int j = t - L;
-      k = a->k_nodes + ((size_t)(n0 + j) * Hkv + kvh) * D;
+      load_row(a, a->k_nodes, a->k_nodes_scale, (size_t)(n0 + j) * Hkv + kvh, kv);
       vis[t] = (unsigned char)visible_tree_key(a->parent + n0, i, j);
     }
     double acc = 0.0;
-    for (int d = 0; d < D; ++d) acc += qd[d] * bf16_to_f64(k[d]);
+    for (int d = 0; d < D; ++d) acc += qd[d] * kv[d];
     s[t] = acc * a->scale;
   }
   /* 2. softmax over the visible keys (mask = -inf elsewhere) */
@@ -158,16 +194,15 @@ static void attn_one_row(const oracle_attn_args *a, int b, int i, int h, double 
   for (int d = 0; d < D; ++d) o[d] = 0.0;
   for (int t = 0; t < nkeys; ++t) {
     if (!vis[t]) continue;
-    const uint16_t *v;
     if (t < L) {
       int page = a->block_table[(size_t)b * a->max_blocks_per_seq + t / a->block_size];
       int slot = t % a->block_size;
-      v = a->v_prefix + (((size_t)page * Hkv + kvh) * a->block_size + slot) * D;
+      load_row(a, a->v_prefix, a->v_prefix_scale, ((size_t)page * Hkv + kvh) * a->block_size + slot, kv);
     } else {
-      v = a->v_nodes + ((size_t)(n0 + (t - L)) * Hkv + kvh) * D;
+      load_row(a, a->v_nodes, a->v_nodes_scale, (size_t)(n0 + (t - L)) * Hkv + kvh, kv);
     }
     double w = s[t] / l;
-    for (int d = 0; d < D; ++d) o[d] += w * bf16_to_f64(v[d]);
+    for (int d = 0; d < D; ++d) o[d] += w * kv[d];
   }
   free(s);
   free(vis);
@@ -190,6 +225,10 @@ static void *attn_worker(void *arg) {
 int oracle_tree_attention_rows(const oracle_attn_args *a, int nrows, const int32_t *rows,
                                double *out, int nthreads) {
   if (a->head_dim > 512 || a->num_kv_heads <= 0 || a->num_q_heads % a->num_kv_heads) return -1;
+  if (a->dtype != 0 && a->dtype != 1) return -1;
+  if (a->dtype == 1 && (!a->q_scale || !a->k_prefix_scale || !a->v_prefix_scale ||
+                        !a->k_nodes_scale || !a->v_nodes_scale))
+    return -1;
   attn_job job;
   job.a = a;
   job.rows = rows;
@@ -609,6 +648,7 @@ int oracle_accept(const oracle_accept_args *a, int nthreads) {
 
 /* Exposed for the pins: the fixed-point pieces on their own. */
 uint64_t oracle_quantise(float r) { return quantise(r); }
+double oracle_e4m3_to_f64(uint8_t c) { return e4m3_to_f64(c); }
 uint64_t oracle_scaled_draw(float u, uint64_t S) { return scaled_draw(u, S); }
 float oracle_retained_mass_row(const float *q, const uint32_t *mask, int vocab) {
   oracle_accept_args a;

@@ -81,6 +81,55 @@ def bf16_bits_to_f32(bits) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+# ------------------------------------------------------------------ E4M3 inputs
+# The FP8 form of the attention inputs (the caller's FP8 KV cache): E4M3 codes
+# with one fp32 scale per row of D elements (a token of one head).  Only input
+# preparation lives here; decoding belongs to the consumers.
+E4M3_MAX = 448.0
+
+
+def _e4m3_magnitudes() -> np.ndarray:
+    """Values of the non-negative finite codes 0..126, ascending (the code order)."""
+    e, m = np.arange(127) >> 3, np.arange(127) & 7
+    return np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 codes (uint8) of real values: round to nearest, ties to the even
+    code, magnitudes above 448 saturate to 448, NaN -> 0x7F."""
+    x = np.asarray(x, dtype=np.float64)
+    mags = _e4m3_magnitudes()
+    ax = np.abs(x)
+    hi = np.clip(np.searchsorted(mags, np.minimum(ax, E4M3_MAX), side="left"), 1, 126)
+    lo = hi - 1
+    d_lo, d_hi = ax - mags[lo], mags[hi] - ax
+    code = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(ax >= E4M3_MAX, 126, code)
+    code = np.where(ax == 0.0, 0, code).astype(np.uint8)
+    code = np.where(np.signbit(x), code | np.uint8(0x80), code).astype(np.uint8)
+    return np.where(np.isnan(x), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def quantize_e4m3_rows(values) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row (last axis) scales s = max|row| / 448 in fp32 (1 for an all-zero
+    row) and the codes of row / s."""
+    v = np.asarray(values, dtype=np.float64)
+    amax = np.abs(v).max(axis=-1)
+    scale = np.where(amax > 0, amax / E4M3_MAX, 1.0).astype(np.float32)
+    codes = e4m3_encode(v / scale.astype(np.float64)[..., None])
+    return codes, scale
+
+
+def e4m3_case(case: dict) -> dict:
+    """The E4M3 form of an attention case: every bf16 input re-quantised per row."""
+    out = dict(case, dtype="e4m3")
+    for k in ("q", "k_prefix", "v_prefix", "k_nodes", "v_nodes"):
+        codes, scale = quantize_e4m3_rows(bf16_bits_to_f32(case[k]))
+        out[k] = codes
+        out[k + "_scale"] = scale
+    return out
+
+
 def _softmax32(x: np.ndarray, out: np.ndarray | None = None) -> np.ndarray:
     """Input preparation: probabilities from logits in fp64 (row blocks), rounded to fp32."""
     x = np.atleast_2d(x)
