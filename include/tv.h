@@ -64,6 +64,20 @@ const char* tv_status_string(int status);
 /* TV_VERSION of the loaded library. */
 int tv_version(void);
 
+/* Self-test of the device-timeout path.  Every wait of the library's kernels
+ * on an mbarrier is bounded (2 s); when one runs out the kernel records
+ * TV_ERR_DEVICE_TIMEOUT in the sequence's status, releases what it holds and
+ * returns, so the context stays usable.  This entry point enqueues one
+ * kernel that waits on an mbarrier nothing ever arrives at, through the same
+ * bounded wait, with the limit `limit_ns` (1 ms .. 1 s), then writes the
+ * outcome: status[0] = TV_ERR_DEVICE_TIMEOUT (or TV_OK had the wait ended)
+ * and waited_ns[0] = the nanoseconds it waited.  status, waited_ns: device
+ * pointers (int32, uint64), 4- and 8-byte aligned.  Returns
+ * TV_ERR_INVALID_ARG (nothing enqueued) for a NULL pointer or a limit out of
+ * range, TV_ERR_CUDA if the launch fails, else TV_OK. */
+int tv_selftest_wait_timeout(int32_t* status, unsigned long long* waited_ns,
+                             unsigned long long limit_ns, cudaStream_t stream);
+
 /* ========================================================================
  * Tree attention
  *

@@ -38,7 +38,7 @@ TV_BLOCK_SIZE = 16
 EXPORTS = ("tv_status_string", "tv_version", "tv_tree_attention_workspace_size",
            "tv_tree_attention", "tv_accept_workspace_size", "tv_accept", "tv_accept_ex",
            "tv_commit_kv",
-           "tv_retained_set")
+           "tv_retained_set", "tv_selftest_wait_timeout")
 
 
 class TVError(RuntimeError):
@@ -103,6 +103,8 @@ def load(path: str | None = None) -> C.CDLL:
     lib.tv_accept_ex.restype = C.c_int
     lib.tv_tree_attention_no_alloc.argtypes = [C.POINTER(AttnParams)] + [vp] * 11 + [vp]
     lib.tv_tree_attention_no_alloc.restype = C.c_int
+    lib.tv_selftest_wait_timeout.argtypes = [vp, vp, C.c_ulonglong, vp]
+    lib.tv_selftest_wait_timeout.restype = C.c_int
     lib.tv_commit_kv.argtypes = [C.POINTER(CommitParams)] + [vp] * 12 + [vp]
     lib.tv_commit_kv.restype = C.c_int
     lib.tv_retained_set.argtypes = [C.POINTER(RetainParams)] + [vp] * 5 + [vp]
@@ -266,6 +268,21 @@ def accept(target, draft_probs, draft_tokens, parent, node_offsets, uniforms,
     if rc != TV_OK:
         raise TVError(rc, "tv_accept")
     return dict(accepted_len=acc, path=path, bonus_token=bonus, status=status, debug_pq=dpq)
+
+
+def selftest_wait_timeout(limit_ms: float = 10.0, stream=None):
+    """tv_selftest_wait_timeout: a device wait that nothing ends, bounded by
+    limit_ms.  Returns (status, waited_ns) after synchronising."""
+    import torch
+    lib = load()
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    rc = lib.tv_selftest_wait_timeout(_ptr(status), _ptr(waited), C.c_ulonglong(int(limit_ms * 1e6)),
+                                      _stream(stream))
+    if rc != TV_OK:
+        raise TVError(rc, "tv_selftest_wait_timeout")
+    torch.cuda.synchronize()
+    return int(status.item()), int(waited.item())
 
 
 def commit_kv(k_nodes, v_nodes, parent, node_offsets, accepted_len, path, block_table,

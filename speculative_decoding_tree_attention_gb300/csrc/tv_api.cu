@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "../../include/tv.h"
+#include "tv_device.cuh"
 #include "tv_launch.h"
 
 namespace {
@@ -127,6 +128,34 @@ const char* tv_status_string(int s) {
 }
 
 int tv_version(void) { return TV_VERSION; }
+
+namespace {
+// One thread block waits on an mbarrier that nothing arrives at, through the
+// kernels' bounded wait, and reports the outcome.
+__global__ void selftest_wait_timeout_kernel(int32_t* status, unsigned long long* waited_ns,
+                                             unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    tv::mbar_init(&bar, 1);
+    tv::fence_mbar_init();
+  }
+  __syncthreads();
+  const unsigned long long t0 = tv::global_ns();
+  const bool done = tv::mbar_wait(&bar, 0, nullptr, limit_ns);
+  if (threadIdx.x == 0) {
+    *status = done ? tv::kOk : tv::kDeviceTimeout;
+    *waited_ns = tv::global_ns() - t0;
+  }
+}
+}  // namespace
+
+int tv_selftest_wait_timeout(int32_t* status, unsigned long long* waited_ns,
+                             unsigned long long limit_ns, cudaStream_t stream) {
+  if (!status || !waited_ns) return TV_ERR_INVALID_ARG;
+  if (limit_ns < 1000000ull || limit_ns > 1000000000ull) return TV_ERR_INVALID_ARG;
+  selftest_wait_timeout_kernel<<<1, 32, 0, stream>>>(status, waited_ns, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
 
 size_t tv_tree_attention_workspace_size(const tv_attn_params* p) {
   (void)p;  // split partials are merged through distributed shared memory

@@ -73,17 +73,18 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase of `parity` to complete.  Returns false if the wait ran
-// out (the caller records kDeviceTimeout and winds down).  `*abort` lets one
-// thread's timeout stop the others quickly.
+// out after `limit_ns` (the caller records kDeviceTimeout and winds down).
+// `*abort` lets one thread's timeout stop the others quickly.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort = nullptr) {
+                                          volatile int* abort = nullptr,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (abort && *abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) return false;
+      if (global_ns() - t0 > limit_ns) return false;
     }
   }
 }

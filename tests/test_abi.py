@@ -160,3 +160,12 @@ def test_accept_options_checked_before_launch(lib, bad):
     args[11] = None
     assert lib.tv_accept_ex(C.byref(p), C.byref(o), *args, None, C.c_size_t(0), None) == \
         tv.TV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("limit_ns", [0, 999_999, 1_000_000_001])
+def test_selftest_wait_timeout_checks_arguments(lib, limit_ns):
+    dummy = C.c_void_p(4096)
+    assert lib.tv_selftest_wait_timeout(dummy, dummy, C.c_ulonglong(limit_ns), None) == \
+        tv.TV_ERR_INVALID_ARG
+    assert lib.tv_selftest_wait_timeout(None, dummy, C.c_ulonglong(10_000_000), None) == \
+        tv.TV_ERR_INVALID_ARG
