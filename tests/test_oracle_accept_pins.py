@@ -383,8 +383,11 @@ def test_golden_hand_worked_examples():
         case = accept_case([ex["parent"]], ex["vocab"], ex["target"], ex["draft"],
                            ex["tokens"], ex["uniforms"],
                            mask=None if ex.get("mask") is None else np.asarray(ex["mask"], np.uint32))
-        out = oracle.accept(case)
-        want = ex["expect"]
-        assert out["accepted_len"][0] == want["accepted_len"], name
-        assert list(out["path"][0, : want["accepted_len"]]) == want["path"], name
-        assert out["bonus_token"][0] == want["bonus_token"], name
+        checks = [(ex.get("test", 0), ex["expect"])]
+        if "expect_ratio_test" in ex:
+            checks.append((0, ex["expect_ratio_test"]))
+        for test, want in checks:
+            out = oracle.accept(case, test=test)
+            assert out["accepted_len"][0] == want["accepted_len"], (name, test)
+            assert list(out["path"][0, : want["accepted_len"]]) == want["path"], (name, test)
+            assert out["bonus_token"][0] == want["bonus_token"], (name, test)
