@@ -17,7 +17,9 @@ Tree shapes
   * ``binary``: the full binary tree of depth 3 (15 nodes), parent(i) = (i-1)//2.
   * ``topk``: breadth-first growth; every node shallower than ``depth`` gets
     k ~ U{1..kmax} children, the k most probable tokens of its draft row, until
-    ``n`` nodes exist.
+    ``n`` nodes exist; if every branch reaches the depth limit first, nodes in
+    discovery order get their next most probable tokens (up to kmax children)
+    until ``n`` nodes exist.
   * ``importance``: the importance-sampled tree of the on-device multimodal
     pruning page (§3.1): each node offers the top-8 draft tokens of its retained
     set, weighted w_i = p_i^beta / sum_j p_j^beta with beta = 0.6; nodes are
@@ -220,6 +222,24 @@ def _grow_tree(cfg, b, n_target, rows: _Rows):
                 parent.append(j)
                 token.append(int(tok))
                 depth.append(depth[j] + 1)
+        if kind == "topk":
+            # the growth can stop short of n nodes (every branch at the depth
+            # limit); top up: nodes in discovery order get their next most
+            # probable tokens, up to kmax children each, until n nodes exist
+            j = 0
+            while len(parent) < n_target and j < len(parent):
+                if depth[j] < cfg["depth"]:
+                    have = {token[i] for i in range(1, len(parent)) if parent[i] == j}
+                    for tok in _desc_order(rows.get(j)[1], cfg["kmax"]):
+                        if len(parent) >= n_target or len(have) >= cfg["kmax"]:
+                            break
+                        if int(tok) in have:
+                            continue
+                        have.add(int(tok))
+                        parent.append(j)
+                        token.append(int(tok))
+                        depth.append(depth[j] + 1)
+                j += 1
         return parent, token
     if kind == "importance":
         gg = rng(cfg["seed"], _S_GUMBEL, b)
