@@ -31,7 +31,8 @@ struct AcceptArgs {
   const float* gamma;    // [batch] calibration factors or null (1)
 };
 
-// Launches the accept pass; `workspace` holds per-(row, chunk) statistics and
+// Launches the accept pass; `workspace` holds per-(row, part) statistics (at
+// most one part per 8K-entry chunk of the vocabulary) and
 // must be accept_workspace_bytes() long when the input is logits or a mask
 // is given (it is not touched otherwise).
 int launch_accept(const AcceptArgs& a, void* workspace, cudaStream_t stream);
