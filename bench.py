@@ -546,7 +546,8 @@ def main():
         "config": dict(workload_desc(cfg, case), accept_input=args.mode,
                        l2="flushed between timed steps (512 MiB write)",
                        launch="one CUDA graph per step" if graph_step is not None else "eager",
-                       parallelism="replicas" if world > 1 else "single GPU"),
+                       parallelism="replicas" if world > 1 else "single GPU",
+                       prefix_splits=tv.attention_splits(prm)),
         "roofline": dict(
             {"kernel": "tree_attn_kernel (+ status memset; split-KV merged in-cluster)"},
             **roofline_entry(a_bytes, a_flops, attn_mean_s, peak_bw, peak_tf, peak_kind),

@@ -116,6 +116,15 @@ typedef struct {
  * arguments are kept so that a later plan may use device scratch. */
 size_t tv_tree_attention_workspace_size(const tv_attn_params* params);
 
+/* The number of prefix splits (CTAs per 128-row tile, 1..8) that
+ * tv_tree_attention will use for these parameters on the current device, or
+ * -1 if the parameters are invalid.  Chosen by a makespan model from the host
+ * hints (batch, heads, max_nodes, max_prefix_len) and the SM count (148 when
+ * no device is visible): a CTA costs a fixed prologue and epilogue, its share
+ * of the prefix tiles, the node tiles and, when split, a merge; CTAs run one
+ * per SM in waves.  Host-only; nothing is enqueued. */
+int tv_tree_attention_splits(const tv_attn_params* params);
+
 /* Layouts (all row-major, contiguous):
  *   q_nodes          bf16 [total_nodes][Hq][D]
  *   k_prefix_blocks  bf16 [num_blocks][Hkv][block_size][D]   (paged pool)

@@ -38,7 +38,7 @@ TV_BLOCK_SIZE = 16
 EXPORTS = ("tv_status_string", "tv_version", "tv_tree_attention_workspace_size",
            "tv_tree_attention", "tv_accept_workspace_size", "tv_accept", "tv_accept_ex",
            "tv_commit_kv",
-           "tv_retained_set", "tv_selftest_wait_timeout")
+           "tv_retained_set", "tv_selftest_wait_timeout", "tv_tree_attention_splits")
 
 
 class TVError(RuntimeError):
@@ -105,6 +105,8 @@ def load(path: str | None = None) -> C.CDLL:
     lib.tv_tree_attention_no_alloc.restype = C.c_int
     lib.tv_selftest_wait_timeout.argtypes = [vp, vp, C.c_ulonglong, vp]
     lib.tv_selftest_wait_timeout.restype = C.c_int
+    lib.tv_tree_attention_splits.argtypes = [C.POINTER(AttnParams)]
+    lib.tv_tree_attention_splits.restype = C.c_int
     lib.tv_commit_kv.argtypes = [C.POINTER(CommitParams)] + [vp] * 12 + [vp]
     lib.tv_commit_kv.restype = C.c_int
     lib.tv_retained_set.argtypes = [C.POINTER(RetainParams)] + [vp] * 5 + [vp]
@@ -150,6 +152,11 @@ def attention_params(q_nodes, k_prefix_blocks, block_table, prefix_lens, *, num_
 
 def attention_workspace_size(params: AttnParams) -> int:
     return int(load().tv_tree_attention_workspace_size(C.byref(params)))
+
+
+def attention_splits(params: AttnParams) -> int:
+    """tv_tree_attention_splits: prefix splits per 128-row tile (-1: invalid)."""
+    return int(load().tv_tree_attention_splits(C.byref(params)))
 
 
 def tree_attention(q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nodes, v_nodes,

@@ -162,6 +162,12 @@ size_t tv_tree_attention_workspace_size(const tv_attn_params* p) {
   return 0;
 }
 
+int tv_tree_attention_splits(const tv_attn_params* p) {
+  AttnPlan pl;
+  if (!plan_attention(p, &pl)) return -1;
+  return pl.max_splits;
+}
+
 int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
                       const uint16_t* k_prefix_blocks, const uint16_t* v_prefix_blocks,
                       const int32_t* block_table, const uint16_t* k_nodes,

@@ -169,3 +169,26 @@ def test_selftest_wait_timeout_checks_arguments(lib, limit_ns):
         tv.TV_ERR_INVALID_ARG
     assert lib.tv_selftest_wait_timeout(None, dummy, C.c_ulonglong(10_000_000), None) == \
         tv.TV_ERR_INVALID_ARG
+
+
+def _plan(batch, hq, hkv, d, max_nodes, max_prefix):
+    blocks = (max_prefix + 15) // 16
+    return tv.AttnParams(batch, hq, hkv, d, 16, max(1, blocks), max(1, batch * blocks), max_nodes,
+                         batch * max_nodes, max_prefix, 0.0)
+
+
+@pytest.mark.parametrize("shape, splits", [
+    ((1, 4, 4, 64, 15, 128), 1),          # tiny
+    ((1, 32, 32, 128, 64, 1024), 4),      # 7B-like: 32 tiles, latency-bound: split
+    ((16, 32, 8, 128, 64, 3959), 1),      # serving: 256 tiles, two waves already
+    ((4, 28, 4, 128, 128, 1600), 1),      # multimodal: 112 tiles, one wave unsplit
+    ((4, 64, 8, 128, 256, 32768), 2),     # long: 512 tiles; two splits fill the waves
+    ((1, 64, 8, 128, 256, 32768), 1),     # long, one sequence: 128 tiles, one wave
+])
+def test_split_count_model(lib, shape, splits):
+    assert tv.attention_splits(_plan(*shape)) == splits
+
+
+def test_split_count_rejects_invalid_params(lib):
+    assert tv.attention_splits(_plan(1, 6, 4, 128, 64, 1024)) == -1   # Hq % Hkv != 0
+    assert tv.attention_splits(_plan(1, 4, 4, 96, 64, 1024)) == -1    # head size
