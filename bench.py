@@ -7,13 +7,16 @@ tree mask) followed by tv_accept (logits mode: log-sum-exp, pruning
 renormalisation when the workload has a retained-set mask, per-node tests,
 the longest accepted path and the bonus draw).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 5] [--impl ours|reference]
 
 Prints ONE JSON line on rank 0.  `value` is tree-tokens/s (tree nodes
 verified per second, all ranks) with inputs resident in HBM; L2 is flushed
 between timed steps (a 512 MiB write, outside the timed events).  Under
 torchrun each rank runs an independent replica (no collective on the data
 path: sequences are independent), timing is max over ranks.
+The headline is the 32K long-context workload (config 5); the serving and
+7B-like workloads (configs 3 and 2) are timed in the same run and reported
+under "workloads", each call on its own.
 `--impl reference` times the fp64 CPU oracle on the host cores instead.
 """
 from __future__ import annotations
@@ -47,11 +50,14 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, help="workload 1..5 (default: 7B-like)")
+    ap.add_argument("--config", type=int, default=5,
+                    help="workload 1..5 (default: 5, the 32K long-context batch)")
     ap.add_argument("--mode", choices=["logits", "probs"], default="logits")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-side", dest="side", action="store_false",
+                    help="skip the serving and 7B-like figures reported beside the headline")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiler captures)")
     return ap.parse_args()
@@ -163,42 +169,69 @@ def roofline_entry(nbytes, flops, seconds, peak_bw, peak_tf, peak_kind):
 
 
 class Clocks:
+    """nvidia-smi samples (every 20 ms) read by a thread, each stamped with the
+    host time it arrived.  `load(t0, t1)` marks a window in which the GPU ran
+    this benchmark's kernels; the reported median SM clock is over the samples
+    inside those windows, the throttle reasons over every sample."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, dev_index):
+        import threading
         self.p = None
+        self.samples = []   # (host time, sm MHz, max MHz, power W, reasons)
+        self.windows = []
         try:
             self.p = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(dev_index)], stdout=subprocess.PIPE,
+                 "-lms", "20", "-i", str(dev_index)], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.p = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
 
-    def stop(self):
-        if self.p is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.p.terminate()
-        out, _ = self.p.communicate(timeout=10)
-        sm, mx, reasons = [], [], set()
+    def _read(self):
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for line in self.p.stdout:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                sm, mx = float(f[1]), float(f[2])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+            try:
+                pw = float(f[3])
+            except ValueError:
+                pw = None
+            r = [n for n, v in zip(names, f[5:9]) if v.lower().startswith("active")]
+            self.samples.append((time.time(), sm, mx, pw, r))
+
+    def load(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.1)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.t.join(timeout=5)
+        s = list(self.samples)
+        under = [x for x in s if any(a <= x[0] <= b + 0.05 for a, b in self.windows)]
+        reasons = sorted({n for x in s for n in x[4]})
+        pw = [x[3] for x in under if x[3] is not None]
+        return {"sm_mhz": statistics.median(x[1] for x in under) if under else None,
+                "sm_max_mhz": max(x[2] for x in s) if s else None, "reasons": reasons,
+                "samples": len(s), "samples_under_load": len(under),
+                "power_w_max": max(pw) if pw else None}
 
 
 def cpu_baseline(case, budget_s, threads=None):
@@ -269,6 +302,126 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def host_arrays(case):
+    """The step's inputs as host arrays (bf16 as int16 bit patterns)."""
+    host = {
+        "q": case["q"].view(np.int16), "kp": case["k_prefix"].view(np.int16),
+        "vp": case["v_prefix"].view(np.int16), "table": case["block_table"],
+        "kn": case["k_nodes"].view(np.int16), "vn": case["v_nodes"].view(np.int16),
+        "parent": case["parent"], "lens": case["prefix_lens"], "off": case["node_offsets"],
+        "target": case["target"], "draft": case["draft_probs"], "tokens": case["draft_tokens"],
+        "uniforms": case["uniforms"],
+    }
+    if case.get("retained_mask") is not None:
+        host["mask"] = case["retained_mask"].view(np.int32)
+    return host
+
+
+class Step:
+    """One workload resident on the device, with its output buffers and the
+    two library calls of a step (tree attention, then accept)."""
+
+    def __init__(self, tv, case, cfg, mode, dev):
+        import torch
+        self.tv, self.case, self.cfg, self.mode = tv, case, cfg, mode
+        self.host = host_arrays(case)
+        d = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in self.host.items()}
+        for k in ("q", "kp", "vp", "kn", "vn"):
+            d[k] = d[k].view(torch.bfloat16)
+        self.d = d
+        B = cfg["batch"]
+        self.B = B
+        self.tot = int(case["node_offsets"][-1])
+        self.max_nodes = int(case["max_nodes"])
+        self.mpl = int(max(1, int(np.max(case["prefix_lens"]))))
+        self.prm = tv.attention_params(d["q"], d["kp"], d["table"], d["lens"],
+                                       num_kv_heads=cfg["hkv"], max_nodes=self.max_nodes,
+                                       max_prefix_len=self.mpl)
+        ws_bytes = tv.attention_workspace_size(self.prm)
+        self.ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        self.out = torch.empty_like(d["q"])
+        self.st_attn = torch.empty(B, dtype=torch.int32, device=dev)
+        self.acc_out = {"accepted_len": torch.empty(B, dtype=torch.int32, device=dev),
+                        "path": torch.empty(B, self.max_nodes, dtype=torch.int32, device=dev),
+                        "bonus_token": torch.empty(B, dtype=torch.int32, device=dev),
+                        "status": torch.empty(B, dtype=torch.int32, device=dev)}
+        acc_prm = tv.AcceptParams(B, int(cfg["vocab"]), self.max_nodes, self.tot,
+                                  1 if mode == "logits" else 0)
+        acc_ws_bytes = int(tv.load().tv_accept_workspace_size(ctypes.byref(acc_prm)))
+        self.acc_ws = torch.empty(max(acc_ws_bytes, 16), dtype=torch.uint8, device=dev)
+        acc_stats = mode == "logits" or d.get("mask") is not None
+        # kernels of ours per step: tree_attn_kernel, accept_tree_kernel and,
+        # for logits or a retained mask, accept_rowstats_kernel (memsets not
+        # counted)
+        self.launches_per_step = 2 + (1 if acc_stats else 0)
+
+    def attn(self, src=None):
+        src = src or self.d
+        self.tv.tree_attention(src["q"], src["kp"], src["vp"], src["table"], src["kn"], src["vn"],
+                               src["parent"], src["lens"], src["off"], max_nodes=self.max_nodes,
+                               max_prefix_len=self.mpl, out=self.out, status=self.st_attn,
+                               workspace=self.ws)
+
+    def acc(self, src=None, test="ratio", outputs=None):
+        src = src or self.d
+        self.tv.accept(src["target"], src["draft"], src["tokens"], src["parent"], src["off"],
+                       src["uniforms"], src.get("mask"), max_nodes=self.max_nodes, kind=self.mode,
+                       test=test, outputs=dict(outputs or self.acc_out, workspace=self.acc_ws))
+
+    def check(self):
+        assert int(self.st_attn.max()) == 0 and int(self.acc_out["status"].max()) == 0, "status"
+
+
+def timed(fn, n, stream, flush, warm=3):
+    """CUDA-event times (ms) of n calls of fn on `stream`, each after an L2
+    flush outside its events, after `warm` untimed calls."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for k in range(n + warm):
+            flush.fill_(k & 0xFF)
+            if k >= warm:
+                ev[k - warm][0].record(stream)
+            fn()
+            if k >= warm:
+                ev[k - warm][1].record(stream)
+    stream.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def graphed(fn, stream):
+    """fn captured once into a CUDA graph; returns its replay."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g.replay
+
+
+def kernel_entries(step, attn_ms, acc_ms, peaks, cfg_num):
+    """Roofline of the attention call and the HBM fraction of the accept call."""
+    peak_bw, peak_tf, peak_kind = peaks
+    case = step.case
+    a_bytes, a_flops = attention_bytes(case), attention_flops(case)
+    attn_s = statistics.mean(attn_ms) / 1e3
+    acc_s = statistics.mean(acc_ms) / 1e3
+    ab = accept_bytes(case)
+    src = "of measured (MEASURED_PEAKS.json)" if peak_kind == "measured" else "of fallback"
+    roof = dict({"kernel": "tree_attn_kernel (+ status memset)"},
+                **roofline_entry(a_bytes, a_flops, attn_s, peak_bw, peak_tf, peak_kind),
+                traffic=ncu_traffic(cfg_num), algorithmic_bytes=a_bytes, flops=a_flops,
+                mean_us=attn_s * 1e6, hbm_gbs=a_bytes / attn_s / 1e9,
+                hbm_frac=a_bytes / attn_s / 1e9 / peak_bw,
+                tflops=a_flops / attn_s / 1e12, tensor_frac=a_flops / attn_s / 1e12 / peak_tf)
+    acc = {"mean_us": acc_s * 1e6, "trees_per_s": step.B / acc_s,
+           "accepted_tokens_per_s": float(step.acc_out["accepted_len"].sum().item()) / acc_s,
+           "algorithmic_bytes": ab, "achieved_gbs": ab / acc_s / 1e9,
+           "peak": peak_bw, "frac": ab / acc_s / 1e9 / peak_bw,
+           "peak_source": src + " hbm_gbs", "bound": "hbm"}
+    return roof, acc
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -290,109 +443,51 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     _build.build()
     tv.load()
+    peaks = load_peaks()
 
     cfg = wl.config(args.config, **({"batch": args.batch} if args.batch > 0 else {}))
     case = wl.make_case(cfg, parts=("attn", "accept"), kind=args.mode)
-    tot = int(case["node_offsets"][-1])
-    B = cfg["batch"]
-
-    def to_dev(x, dtype):
-        return torch.from_numpy(np.ascontiguousarray(x).view(dtype)).to(dev)
-
-    host = {
-        "q": case["q"].view(np.int16), "kp": case["k_prefix"].view(np.int16),
-        "vp": case["v_prefix"].view(np.int16), "table": case["block_table"],
-        "kn": case["k_nodes"].view(np.int16), "vn": case["v_nodes"].view(np.int16),
-        "parent": case["parent"], "lens": case["prefix_lens"], "off": case["node_offsets"],
-        "target": case["target"], "draft": case["draft_probs"], "tokens": case["draft_tokens"],
-        "uniforms": case["uniforms"],
-    }
-    if case.get("retained_mask") is not None:
-        host["mask"] = case["retained_mask"].view(np.int32)
-    d = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in host.items()}
-    for k in ("q", "kp", "vp", "kn", "vn"):
-        d[k] = d[k].view(torch.bfloat16)
-    mask = d.get("mask")
-    max_nodes = int(case["max_nodes"])
-    mpl = int(max(1, int(np.max(case["prefix_lens"]))))
-    prm = tv.attention_params(d["q"], d["kp"], d["table"], d["lens"], num_kv_heads=cfg["hkv"],
-                              max_nodes=max_nodes, max_prefix_len=mpl)
-    ws_bytes = tv.attention_workspace_size(prm)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    out = torch.empty_like(d["q"])
-    st_attn = torch.empty(B, dtype=torch.int32, device=dev)
-    acc_out = {"accepted_len": torch.empty(B, dtype=torch.int32, device=dev),
-               "path": torch.empty(B, max_nodes, dtype=torch.int32, device=dev),
-               "bonus_token": torch.empty(B, dtype=torch.int32, device=dev),
-               "status": torch.empty(B, dtype=torch.int32, device=dev)}
-    acc_prm = tv.AcceptParams(B, int(cfg["vocab"]), max_nodes, tot, 1 if args.mode == "logits" else 0)
-    acc_ws_bytes = int(tv.load().tv_accept_workspace_size(ctypes.byref(acc_prm)))
-    acc_ws = torch.empty(max(acc_ws_bytes, 16), dtype=torch.uint8, device=dev)
-    acc_stats = args.mode == "logits" or mask is not None
-    # kernels of ours per step: tree_attn_kernel, accept_tree_kernel and, for
-    # logits or a retained mask, accept_rowstats_kernel (memsets not counted)
-    launches_per_step = 2 + (1 if acc_stats else 0)
-
-    def attn(src):
-        tv.tree_attention(src["q"], src["kp"], src["vp"], src["table"], src["kn"], src["vn"],
-                          src["parent"], src["lens"], src["off"], max_nodes=max_nodes,
-                          max_prefix_len=mpl, out=out, status=st_attn, workspace=ws)
-
-    def acc(src):
-        tv.accept(src["target"], src["draft"], src["tokens"], src["parent"], src["off"],
-                  src["uniforms"], src.get("mask"), max_nodes=max_nodes, kind=args.mode,
-                  outputs=dict(acc_out, workspace=acc_ws))
+    # the other HBM-bound workloads, reported beside the headline (rank 0)
+    side_nums = [n for n in (3, 2) if n != cfg["num"]] if (rank == 0 and args.side) else []
+    side_cases = {n: wl.make_case(wl.config(n), parts=("attn", "accept"), kind=args.mode)
+                  for n in side_nums}
+    step = Step(tv, case, cfg, args.mode, dev)
+    tot, B = step.tot, step.B
 
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    clocks = Clocks(vis[local] if local < len(vis) and vis[local].strip().isdigit() else local)
+    t_load0 = time.time()
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
-            attn(d)
-            acc(d)
+            step.attn()
+            step.acc()
         stream.synchronize()
-        assert int(st_attn.max()) == 0 and int(acc_out["status"].max()) == 0, "device status"
-        graph_a = graph_b = graph_step = None
+        step.check()
+        run_step = run_attn = run_acc = None
         if not args.no_graph:
             # the step (attention then accept) as one graph; and each call as
             # its own graph for the per-kernel breakdown
-            graph_step = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph_step, stream=stream):
-                attn(d)
-                acc(d)
-            graph_a = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph_a, stream=stream):
-                attn(d)
-            graph_b = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph_b, stream=stream):
-                acc(d)
+            run_step = graphed(lambda: (step.attn(), step.acc()), stream)
+            run_attn = graphed(step.attn, stream)
+            run_acc = graphed(step.acc, stream)
             for _ in range(max(3, args.warmup)):
-                graph_step.replay()
-                graph_a.replay()
-                graph_b.replay()
+                run_step()
+                run_attn()
+                run_acc()
             stream.synchronize()
-
-    def run_step():
-        if graph_step is not None:
-            graph_step.replay()
         else:
-            attn(d)
-            acc(d)
-
-    def run_attn():
-        graph_a.replay() if graph_a is not None else attn(d)
-
-    def run_acc():
-        graph_b.replay() if graph_b is not None else acc(d)
+            run_step = lambda: (step.attn(), step.acc())
+            run_attn, run_acc = step.attn, step.acc
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
-    clocks = Clocks(vis[local] if local < len(vis) and vis[local].strip().isdigit() else local)
     t_wall0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for k in range(args.steps):
@@ -406,98 +501,85 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_s = sum(step_ms) / 1e3
     # per-call breakdown (same flushing), for the roofline of each kernel
     nb = max(3, min(args.steps, 100))
-    evb = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(nb)]
-    with torch.cuda.stream(stream):
-        for k in range(nb):
-            e0, e1, e2, e3 = evb[k]
-            flush.fill_(k & 0xFF)
-            e0.record(stream)
-            run_attn()
-            e1.record(stream)
-            flush.fill_(k & 0xFF)
-            e2.record(stream)
-            run_acc()
-            e3.record(stream)
-    stream.synchronize()
-    attn_ms = [e0.elapsed_time(e1) for e0, e1, _, _ in evb]
-    acc_ms = [e2.elapsed_time(e3) for _, _, e2, e3 in evb]
+    attn_ms = timed(run_attn, nb, stream, flush)
+    acc_ms = timed(run_acc, nb, stream, flush)
     if world > 1:
         total_s = max_over_ranks(total_s, dev)
+    roof, acc_entry = kernel_entries(step, attn_ms, acc_ms, peaks, cfg["num"])
+
+    # ---- the other HBM-bound workloads: each call timed on its own, as above
+    side = {}
+    for n, c in side_cases.items():
+        st = Step(tv, c, wl.config(n), args.mode, dev)
+        with torch.cuda.stream(stream):
+            st.attn()
+            st.acc()
+        stream.synchronize()
+        st.check()
+        ra = graphed(st.attn, stream) if not args.no_graph else st.attn
+        rc = graphed(st.acc, stream) if not args.no_graph else st.acc
+        a_ms = timed(ra, nb, stream, flush, warm=5)
+        c_ms = timed(rc, nb, stream, flush, warm=5)
+        r, a = kernel_entries(st, a_ms, c_ms, peaks, n)
+        side[f"{wl.config(n)['name']} (config {n})"] = {
+            "tree_nodes": st.tot, "attention": r, "accept": a,
+            "step_us": (statistics.mean(a_ms) + statistics.mean(c_ms)) * 1e3,
+            "prefix_splits": tv.attention_splits(st.prm)}
+        del st, ra, rc
+    torch.cuda.synchronize()
+    clocks.load(t_load0, time.time())
+    clk = clocks.stop()
 
     # ---- commit of the accepted path (the step after the walk; reported on its
     # own, not part of the timed step): the root and the accepted nodes of the
     # last step's accept results go into fresh pages of an extended pool
+    d, max_nodes = step.d, step.max_nodes
+    acc_out = step.acc_out
     kpx, vpx, tabx = wl.extend_pool(case, max_nodes + 1)
     cm = {"kp": torch.from_numpy(kpx.view(np.int16)).to(dev).view(torch.bfloat16),
           "vp": torch.from_numpy(vpx.view(np.int16)).to(dev).view(torch.bfloat16),
           "table": torch.from_numpy(tabx).to(dev)}
     del kpx, vpx
     cm_out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev))
-    evc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nb)]
-    with torch.cuda.stream(stream):
-        for k in range(nb + 3):
-            flush.fill_(k & 0xFF)
-            if k >= 3:
-                evc[k - 3][0].record(stream)
-            tv.commit_kv(d["kn"], d["vn"], d["parent"], d["off"], acc_out["accepted_len"],
-                         acc_out["path"], cm["table"], d["lens"], cm["kp"], cm["vp"],
-                         max_nodes=max_nodes, new_prefix_lens=cm_out[0], status=cm_out[1])
-            if k >= 3:
-                evc[k - 3][1].record(stream)
-    stream.synchronize()
+    commit_ms = timed(lambda: tv.commit_kv(d["kn"], d["vn"], d["parent"], d["off"],
+                                           acc_out["accepted_len"], acc_out["path"], cm["table"],
+                                           d["lens"], cm["kp"], cm["vp"], max_nodes=max_nodes,
+                                           new_prefix_lens=cm_out[0], status=cm_out[1]),
+                      nb, stream, flush)
     assert int(cm_out[1].max()) == 0, "commit status"
-    commit_ms = [a0.elapsed_time(a1) for a0, a1 in evc]
+    commit_tokens = int(acc_out["accepted_len"].sum().item()) + B
+    del cm
     # ---- retained set of the draft rows (the step before the accept pass's
     # renormalisation, for workloads that prune): reported on its own
     retained = None
     if cfg.get("mask_mass"):
-        evr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nb)]
-        with torch.cuda.stream(stream):
-            for k in range(nb + 3):
-                flush.fill_(k & 0xFF)
-                if k >= 3:
-                    evr[k - 3][0].record(stream)
-                rmask, _, _, _ = tv.retained_set(d["draft"], float(cfg["mask_mass"]))
-                if k >= 3:
-                    evr[k - 3][1].record(stream)
-        stream.synchronize()
-        assert torch.equal(rmask, d["mask"]), "retained set differs from the workload's masks"
-        r_ms = statistics.mean(a0.elapsed_time(a1) for a0, a1 in evr)
-        r_bytes = tot * int(cfg["vocab"]) * 4 + rmask.numel() * 4
-        retained = {"mean_us": r_ms * 1e3, "rows": tot, "bytes": r_bytes,
-                    "achieved_gbs": r_bytes / (r_ms * 1e-3) / 1e9,
+        res = {}
+        r_ms = timed(lambda: res.__setitem__("m", tv.retained_set(d["draft"], float(cfg["mask_mass"]))),
+                     nb, stream, flush)
+        assert torch.equal(res["m"][0], d["mask"]), "retained set differs from the workload's masks"
+        r_s = statistics.mean(r_ms) / 1e3
+        r_bytes = tot * int(cfg["vocab"]) * 4 + res["m"][0].numel() * 4
+        retained = {"mean_us": r_s * 1e6, "rows": tot, "bytes": r_bytes,
+                    "achieved_gbs": r_bytes / r_s / 1e9, "frac": r_bytes / r_s / 1e9 / peaks[0],
                     "note": "tv_retained_set of every draft row, timed on its own"}
-    commit_tokens = int(acc_out["accepted_len"].sum().item()) + B
-    del cm
     # ---- the multi-candidate accept variant (siblings tried in order with
     # residual updates) on the same inputs, reported on its own
-    evm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nb)]
     m_out = {k: torch.empty_like(v) for k, v in acc_out.items()}
-    with torch.cuda.stream(stream):
-        for k in range(nb + 3):
-            flush.fill_(k & 0xFF)
-            if k >= 3:
-                evm[k - 3][0].record(stream)
-            tv.accept(d["target"], d["draft"], d["tokens"], d["parent"], d["off"], d["uniforms"],
-                      d.get("mask"), max_nodes=max_nodes, kind=args.mode, test="multi",
-                      outputs=dict(m_out, workspace=acc_ws))
-            if k >= 3:
-                evm[k - 3][1].record(stream)
-    stream.synchronize()
+    m_ms = timed(lambda: step.acc(test="multi", outputs=m_out), nb, stream, flush)
     assert int(m_out["status"].max()) == 0, "multi-candidate accept status"
-    m_ms = statistics.mean(a0.elapsed_time(a1) for a0, a1 in evm)
-    multi = {"mean_us": m_ms * 1e3, "trees_per_s": B / (m_ms * 1e-3),
+    m_s = statistics.mean(m_ms) / 1e3
+    multi = {"mean_us": m_s * 1e6, "trees_per_s": B / m_s,
              "mean_accepted_len": float(m_out["accepted_len"].float().mean().item()),
              "mean_accepted_len_single": float(acc_out["accepted_len"].float().mean().item()),
              "note": "tv_accept_ex with TV_TEST_MULTI on the step's inputs, timed on its own"}
     del m_out
 
     # ---- end to end through the public API with host buffers
+    host = step.host
     pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()}
     e2e_src = {k: torch.empty_like(d[k].view(pinned[k].dtype)) for k in host}
     res_host = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in acc_out.items()}
@@ -511,16 +593,16 @@ def main():
         for _ in range(2):
             for k in host:
                 e2e_src[k].copy_(pinned[k], non_blocking=True)
-            attn(src)
-            acc(src)
+            step.attn(src)
+            step.acc(src)
         stream.synchronize()
         e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e_a.record(stream)
         for _ in range(e2e_steps):
             for k in host:
                 e2e_src[k].copy_(pinned[k], non_blocking=True)
-            attn(src)
-            acc(src)
+            step.attn(src)
+            step.acc(src)
             for k in res_host:
                 res_host[k].copy_(acc_out[k], non_blocking=True)
         e_b.record(stream)
@@ -531,12 +613,6 @@ def main():
         if world > 1:
             torch.distributed.destroy_process_group()
         return
-    peak_bw, peak_tf, peak_kind = load_peaks()
-    a_bytes = attention_bytes(case)
-    a_flops = attention_flops(case)
-    attn_mean_s = statistics.mean(attn_ms) / 1e3
-    acc_mean_s = statistics.mean(acc_ms) / 1e3
-    tr = ncu_traffic(cfg["num"])
     value = world * tot * args.steps / total_s
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -545,20 +621,15 @@ def main():
         "data": "synthetic (seeded; shapes of the pages' workloads, no datasets or weights)",
         "config": dict(workload_desc(cfg, case), accept_input=args.mode,
                        l2="flushed between timed steps (512 MiB write)",
-                       launch="one CUDA graph per step" if graph_step is not None else "eager",
+                       launch="one CUDA graph per step" if not args.no_graph else "eager",
                        parallelism="replicas" if world > 1 else "single GPU",
-                       prefix_splits=tv.attention_splits(prm)),
-        "roofline": dict(
-            {"kernel": "tree_attn_kernel (+ status memset; split-KV merged in-cluster)"},
-            **roofline_entry(a_bytes, a_flops, attn_mean_s, peak_bw, peak_tf, peak_kind),
-            traffic=tr, algorithmic_bytes=a_bytes, flops=a_flops,
-            mean_us=attn_mean_s * 1e6),
-        "accept": {"mean_us": acc_mean_s * 1e6, "trees_per_s": B / acc_mean_s,
-                   "algorithmic_bytes": accept_bytes(case),
-                   "achieved_gbs": accept_bytes(case) / acc_mean_s / 1e9},
+                       prefix_splits=tv.attention_splits(step.prm)),
+        "roofline": roof,
+        "accept": acc_entry,
+        "workloads": side,
         "e2e": {"value": world * tot * e2e_steps / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": step.launches_per_step * args.steps,
         "percentiles_us": {"step": pct(step_ms), "attention": pct(attn_ms), "accept": pct(acc_ms)},
         "retained_set": retained,
         "accept_multi": multi,

@@ -198,9 +198,10 @@ def tree_attention_no_alloc(q_nodes, k_prefix_blocks, v_prefix_blocks, block_tab
                             max_prefix_len: int, softmax_scale: float = 0.0, out=None,
                             status=None, stream=None):
     """tv_tree_attention_no_alloc: as tree_attention, for callers that cannot
-    allocate device memory; the library keeps the split-KV partials in its own
-    fixed device array (see include/tv.h).  Output tensors must be supplied by
-    a caller that cannot allocate; they are created here only for convenience."""
+    allocate device memory; any device scratch the launch plan needs comes
+    from a fixed device array owned by the library (see include/tv.h).  Output
+    tensors must be supplied by a caller that cannot allocate; they are
+    created here only for convenience."""
     import torch
     lib = load()
     _check_dev(q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nodes, v_nodes,

@@ -392,7 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       w.n0 + w.N > a.total_nodes) {
     if (tid == 0) record_status(a.status, w.b, kBadTree);
     const bool rows_addressable = w.n0 >= 0 && w.N <= a.max_nodes && w.n0 + w.N <= a.total_nodes;
-    if (w.nsplit == 1 && rows_addressable && warp < 4) zero_rows<D>(a, w, tid);
+    // every CTA of the cluster takes this branch; split 0 writes the zeros
+    if (w.split == 0 && rows_addressable && warp < 4) zero_rows<D>(a, w, tid);
     if (warp == kMmaWarp) tmem_dealloc(tmem, Ly::kTmemCols);
     return;
   }

@@ -7,14 +7,14 @@
 // offers no scratch API, or a service that forbids allocation after start-up
 // so that latency and memory use stay fixed.  tv_tree_attention_no_alloc
 // serves them: it takes the same inputs and outputs as tv_tree_attention, but
-// keeps the split-KV partial results in a fixed array that lives in the
-// library itself, so the caller passes no workspace and nothing is allocated
-// at call time.
+// no workspace.  Whatever device scratch a launch plan asks for
+// (tv_tree_attention_workspace_size) comes from a fixed array that lives in
+// the library itself, so nothing is allocated at call time.
 //
-// The array below is TV_NO_ALLOC_SCRATCH_BYTES (32 MiB) of device memory.
-// Each GPU on which this entry point is used holds it from the first call
-// until the process exits.  Calls that need more partial-result space than
-// that are rejected with TV_ERR_WORKSPACE before anything is enqueued.
+// The array below is TV_NO_ALLOC_SCRATCH_BYTES of device memory.  Each GPU on
+// which this entry point is used holds it from the first call until the
+// process exits.  Calls whose plan needs more than that are rejected with
+// TV_ERR_WORKSPACE before anything is enqueued.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -23,8 +23,7 @@
 
 namespace {
 
-// Device scratch of tv_tree_attention_no_alloc (shared by every call; the
-// current attention plans need none).
+// Device scratch of tv_tree_attention_no_alloc, shared by every call.
 static __device__ __align__(256) unsigned char tv_no_alloc_scratch[TV_NO_ALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;

@@ -54,7 +54,7 @@ def test_no_alloc_matches_workspace_entry_point_twice(num, overrides):
         assert np.array_equal(status.cpu().numpy(), ref_status.cpu().numpy())
         assert np.all(np.isfinite(got))
         max_abs, row_rel, ratio = attention_errors(got, ref)
-        assert ratio <= 1.0 and row_rel <= RTOL, (call, max_abs, row_rel)
+        assert max_abs <= ATOL and ratio <= 1.0 and row_rel <= RTOL, (call, max_abs, row_rel)
 
 
 def lib_scratch_bytes():

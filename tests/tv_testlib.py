@@ -7,13 +7,18 @@ import speculative_decoding_tree_attention_gb300 as tv
 from speculative_decoding_tree_attention_gb300 import _build
 from speculative_decoding_tree_attention_gb300 import workloads as wl
 
-# Tolerance for bf16 inputs with fp32 accumulation: every element within
-# atol + rtol*|ref| (allclose semantics), and every output row (one node, one
-# head) within rtol relative to its own largest magnitude.  An element-wise
-# relative bound on small elements is not used: rounding P to bf16 before the
-# P.V product (as any flash-style kernel does) already moves elements near
-# 1e-2 by several percent.
+# Tolerance for bf16 inputs with fp32 accumulation, as stated for this path:
+# max-abs error 1e-2 and max-rel error 2e-2.  Asserted on every comparison:
+#   * max |g - r| <= ATOL over all elements (the max-abs bound);
+#   * |g - r| <= ATOL + RTOL*|r| element by element (allclose);
+#   * per output row (one node, one head): max |g - r| / max |r| <= RTOL.
+# The element-wise relative error over elements with |r| >= 1e-2 is computed
+# and reported (attention_report) but not asserted against RTOL: rounding P to
+# bf16 before the P.V product moves an element that is a small difference of
+# large terms by up to about 2^-9 of those terms, which is more than 2 % of an
+# element near 1e-2 even when the row is accurate to a fraction of a percent.
 ATOL, RTOL = 1e-2, 2e-2
+REL_FLOOR = 1e-2   # elements at least this large enter the element-wise max-rel
 
 
 def ensure_built():
@@ -63,12 +68,45 @@ def attention_errors(gpu, ref):
     return max_abs, row_rel, ratio
 
 
+def attention_report(gpu, ref):
+    """Every error figure of one comparison: max_abs, row_rel, allclose ratio,
+    elem_rel (max |g - r| / |r| over elements with |r| >= REL_FLOOR),
+    elem_rel_p999 (its 99.9th percentile), frac_over_rtol (share of those
+    elements whose relative error exceeds RTOL) and norm_rel
+    (max|g - r| / max|r| over the whole output)."""
+    g = np.asarray(gpu, np.float64).reshape(-1, np.shape(gpu)[-1])
+    r = np.asarray(ref, np.float64).reshape(-1, np.shape(ref)[-1])
+    max_abs, row_rel, ratio = attention_errors(g, r)
+    big = np.abs(r) >= REL_FLOOR
+    rel = np.abs(g - r)[big] / np.abs(r)[big]
+    return dict(max_abs=max_abs, row_rel=row_rel, allclose_ratio=ratio,
+                elem_rel=float(rel.max()) if rel.size else 0.0,
+                elem_rel_p999=float(np.percentile(rel, 99.9)) if rel.size else 0.0,
+                frac_over_rtol=float((rel > RTOL).mean()) if rel.size else 0.0,
+                norm_rel=float(np.abs(g - r).max() / max(np.abs(r).max(), 1e-30)) if r.size else 0.0,
+                elements=int(r.size))
+
+
+def _record(what, rep):
+    """Appends the figures of one comparison to $TV_PARITY_LOG (JSON lines) if set."""
+    import json
+    import os
+    path = os.environ.get("TV_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(what=what, **rep)) + "\n")
+
+
 def assert_attention_close(gpu, ref, what=""):
     assert np.all(np.isfinite(gpu)), f"non-finite output {what}"
-    max_abs, row_rel, ratio = attention_errors(gpu, ref)
-    assert ratio <= 1.0 and row_rel <= RTOL, \
-        f"{what}: max_abs={max_abs:.3e} row_rel={row_rel:.3e} allclose_ratio={ratio:.3f}"
-    return max_abs, row_rel
+    rep = attention_report(gpu, ref)
+    _record(what, rep)
+    msg = (f"{what}: max_abs={rep['max_abs']:.3e} row_rel={rep['row_rel']:.3e} "
+           f"allclose_ratio={rep['allclose_ratio']:.3f} elem_rel={rep['elem_rel']:.3e}")
+    assert rep["max_abs"] <= ATOL, msg
+    assert rep["allclose_ratio"] <= 1.0, msg
+    assert rep["row_rel"] <= RTOL, msg
+    return rep["max_abs"], rep["row_rel"]
 
 
 def accept_device(case, dev="cuda"):
