@@ -408,7 +408,7 @@ def kernel_entries(step, attn_ms, acc_ms, peaks, cfg_num):
     acc_s = statistics.mean(acc_ms) / 1e3
     ab = accept_bytes(case)
     src = "of measured (MEASURED_PEAKS.json)" if peak_kind == "measured" else "of fallback"
-    roof = dict({"kernel": "tree_attn_kernel (+ status memset)"},
+    roof = dict({"kernel": "tree_attn_kernel (+ status and counter memsets)"},
                 **roofline_entry(a_bytes, a_flops, attn_s, peak_bw, peak_tf, peak_kind),
                 traffic=ncu_traffic(cfg_num), algorithmic_bytes=a_bytes, flops=a_flops,
                 mean_us=attn_s * 1e6, hbm_gbs=a_bytes / attn_s / 1e9,
@@ -528,7 +528,7 @@ def main():
         side[f"{wl.config(n)['name']} (config {n})"] = {
             "tree_nodes": st.tot, "attention": r, "accept": a,
             "step_us": (statistics.mean(a_ms) + statistics.mean(c_ms)) * 1e3,
-            "prefix_splits": tv.attention_splits(st.prm)}
+            "plan": tv.attention_plan(st.prm)}
         del st, ra, rc
     torch.cuda.synchronize()
     clocks.load(t_load0, time.time())
@@ -623,7 +623,7 @@ def main():
                        l2="flushed between timed steps (512 MiB write)",
                        launch="one CUDA graph per step" if not args.no_graph else "eager",
                        parallelism="replicas" if world > 1 else "single GPU",
-                       prefix_splits=tv.attention_splits(step.prm)),
+                       attention_plan=tv.attention_plan(step.prm)),
         "roofline": roof,
         "accept": acc_entry,
         "workloads": side,

@@ -93,8 +93,11 @@ int tv_selftest_wait_timeout(int32_t* status, unsigned long long* waited_ns,
  * stored once in a paged pool and reached through block_table ([MM] §3.2
  * common-prefix merging; [LLM] §2.3.1 cuSeqLens + block_table).  One launch
  * handles every sequence, every head and every node ([MM] §3.2: one kernel
- * for all branches).  Inputs bf16, accumulation and softmax fp32, output bf16.
+ * for all branches).  Inputs bf16, accumulation and softmax fp32, output bf16
+ * (or fp32, out_dtype).
  * ====================================================================== */
+typedef enum { TV_OUT_BF16 = 0, TV_OUT_FP32 = 1 } tv_out_dtype;
+
 typedef struct {
   int32_t batch;              /* B >= 1                                        */
   int32_t num_q_heads;        /* Hq                                            */
@@ -107,23 +110,39 @@ typedef struct {
   int32_t total_nodes;        /* node_offsets[batch] (host copy)               */
   int32_t max_prefix_len;     /* upper bound of L_b (host hint for the grid)   */
   float softmax_scale;        /* 0 => 1/sqrt(D)                                */
+  int32_t out_dtype;          /* tv_out_dtype of `out`: bf16 (0) or fp32 (1).
+                                 The bf16 output is the fp32 result rounded
+                                 once to nearest even.                         */
 } tv_attn_params;             /* host struct */
 
-/* Bytes of device workspace tv_tree_attention needs for these parameters.
- * This version needs none and returns 0: when a prefix is split over CTAs
- * (split-KV), the splits of a tile run as one thread-block cluster and merge
- * their partial results through distributed shared memory.  The workspace
- * arguments are kept so that a later plan may use device scratch. */
+/* Bytes of device workspace tv_tree_attention needs for these parameters on
+ * the current device (0 if the parameters are invalid).  The workspace holds
+ * one arrival counter per CTA (zeroed by every call, on the stream) and two
+ * partial-result slots per CTA: when the line of key tiles is cut inside a
+ * unit (256 packed rows of one sequence and KV head), each piece leaves its
+ * unnormalised output and (max, sum) per row there and the last piece to
+ * finish merges them.  About 2 * SMs * (256 * D * 4 + 2 KB) bytes: 40.5 MB at
+ * D = 128 on 152 SMs. */
 size_t tv_tree_attention_workspace_size(const tv_attn_params* params);
 
-/* The number of prefix splits (CTAs per 128-row tile, 1..8) that
- * tv_tree_attention will use for these parameters on the current device, or
- * -1 if the parameters are invalid.  Chosen by a makespan model from the host
- * hints (batch, heads, max_nodes, max_prefix_len) and the SM count (148 when
- * no device is visible): a CTA costs a fixed prologue and epilogue, its share
- * of the prefix tiles, the node tiles and, when split, a merge; CTAs run one
- * per SM in waves.  Host-only; nothing is enqueued. */
-int tv_tree_attention_splits(const tv_attn_params* params);
+/* Launch plan of tv_tree_attention (host only; nothing is enqueued):
+ * persistent CTAs (at most one per SM) in virtual CTAs of `lanes` CTAs, one
+ * lane per m-tile pair of a layer of a (sequence, KV head); the virtual CTAs
+ * share the line of key tiles (sequence, KV head, layer, tile) in equal
+ * contiguous ranges of at least min_tiles tiles, computed on the device from
+ * prefix_lens and node_offsets. */
+typedef struct {
+  int32_t ctas;            /* CTAs launched = virtual_ctas * lanes          */
+  int32_t lanes;           /* CTAs per virtual CTA                          */
+  int32_t virtual_ctas;    /* at most SMs / lanes                           */
+  int32_t min_tiles;       /* fewest 128-key tiles per virtual CTA          */
+  size_t workspace_bytes;  /* = tv_tree_attention_workspace_size on `sms`   */
+} tv_attn_plan;
+
+/* The plan for `sms` SMs (sms <= 0: the current device's count, 148 when no
+ * device is visible).  Returns TV_OK, or TV_ERR_INVALID_ARG for invalid
+ * parameters or a NULL `plan`. */
+int tv_tree_attention_plan(const tv_attn_params* params, int32_t sms, tv_attn_plan* plan);
 
 /* Layouts (all row-major, contiguous):
  *   q_nodes          bf16 [total_nodes][Hq][D]
@@ -135,10 +154,13 @@ int tv_tree_attention_splits(const tv_attn_params* params);
  *   parent           int32 [total_nodes]  local parent, -1 at each root
  *   prefix_lens      int32 [batch]        L_b >= 0 (<= max_prefix_len)
  *   node_offsets     int32 [batch+1]      cumulative node counts, N_b >= 1
- *   out              bf16 [total_nodes][Hq][D]
+ *   out              bf16 or fp32 (out_dtype) [total_nodes][Hq][D]
  *   status           int32 [batch]        per-sequence TV_OK / TV_ERR_BAD_TREE /
  *                                         TV_ERR_DEVICE_TIMEOUT (device)
  *   workspace        device bytes >= tv_tree_attention_workspace_size()
+ *                    (TV_ERR_WORKSPACE otherwise); contents need no
+ *                    initialisation; calls that overlap on the GPU need
+ *                    distinct workspaces
  * bf16 pointers are passed as uint16_t (bf16 bit patterns).  All device
  * pointers must be 16-byte aligned.  A sequence whose tree or block ids are
  * malformed gets status TV_ERR_BAD_TREE and an all-zero output. */
@@ -146,7 +168,7 @@ int tv_tree_attention(const tv_attn_params* params, const uint16_t* q_nodes,
                       const uint16_t* k_prefix_blocks, const uint16_t* v_prefix_blocks,
                       const int32_t* block_table, const uint16_t* k_nodes,
                       const uint16_t* v_nodes, const int32_t* parent,
-                      const int32_t* prefix_lens, const int32_t* node_offsets, uint16_t* out,
+                      const int32_t* prefix_lens, const int32_t* node_offsets, void* out,
                       int32_t* status, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream);
 
@@ -155,31 +177,33 @@ int tv_tree_attention(const tv_attn_params* params, const uint16_t* q_nodes,
  * pages: an engineering addition of this library).
  *
  * Same inputs, outputs, layouts, semantics and status codes as
- * tv_tree_attention, but no workspace argument: any device scratch a plan
- * needs comes from a fixed device array inside the library (the current
- * plans need none), so a caller that
- * may not call cudaMalloc (code running under stream capture, an operator
- * inside an engine that owns all device memory, a service that forbids
- * allocation after start-up) can still use it.  This entry point allocates
- * nothing and calls no allocating routine.
- *   - The array is TV_NO_ALLOC_SCRATCH_BYTES of device memory; every GPU on
- *     which this entry point runs holds it until the process exits.
+ * tv_tree_attention, but no workspace argument: the device scratch the plan
+ * needs (tv_tree_attention_workspace_size: arrival counters and
+ * partial-result slots) comes from a fixed device array inside the library,
+ * so a caller that may not call cudaMalloc (code running under stream
+ * capture, an operator inside an engine that owns all device memory, a
+ * service that forbids allocation after start-up) can still use it.  This
+ * entry point allocates nothing and calls no allocating routine.
+ *   - The array is TV_NO_ALLOC_SCRATCH_BYTES (64 MiB) of device memory; every
+ *     GPU on which this entry point runs holds it until the process exits.
  *   - A call whose scratch would not fit
  *     (tv_tree_attention_workspace_size(params) > TV_NO_ALLOC_SCRATCH_BYTES)
  *     returns TV_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture on the device.
- *   - Every call uses the same array and it keeps the last call's contents
- *     (nothing in it needs to start at zero).  Calls that overlap on the GPU
- *     (other streams, other host threads) race on it: serialise them. */
-#define TV_NO_ALLOC_SCRATCH_BYTES (32u << 20)
+ *     (cudaGetSymbolAddress) with that device current and keeps it for the
+ *     life of the process; make that first call before any stream capture on
+ *     the device, and do not reset the device's primary context afterwards.
+ *   - Every call uses the same array and it keeps the last call's contents;
+ *     the counters that must start at zero are cleared by each call on its
+ *     stream.  Calls that overlap on the GPU (other streams, other host
+ *     threads) race on the array: serialise them. */
+#define TV_NO_ALLOC_SCRATCH_BYTES (64u << 20)
 int tv_tree_attention_no_alloc(const tv_attn_params* params, const uint16_t* q_nodes,
                                const uint16_t* k_prefix_blocks, const uint16_t* v_prefix_blocks,
                                const int32_t* block_table, const uint16_t* k_nodes,
                                const uint16_t* v_nodes, const int32_t* parent,
                                const int32_t* prefix_lens, const int32_t* node_offsets,
-                               uint16_t* out, int32_t* status, cudaStream_t stream);
+                               void* out, int32_t* status, cudaStream_t stream);
 
 /* ========================================================================
  * Fused accept pass ([EC] §2.2.3; [LLM] §2.2.1-§2.2.2, §7.1)

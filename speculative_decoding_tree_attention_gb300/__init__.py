@@ -18,7 +18,7 @@ import ctypes as C
 import os
 
 __all__ = ["TVError", "load", "tree_attention", "accept", "commit_kv", "retained_set",
-           "attention_workspace_size",
+           "attention_workspace_size", "attention_plan", "attention_params",
            "TV_MAX_NODES", "TV_OK", "TV_ERR_BAD_TREE", "TV_ERR_DEVICE_TIMEOUT", "TV_ERR_NO_PAGE",
            "status_string"]
 
@@ -38,7 +38,8 @@ TV_BLOCK_SIZE = 16
 EXPORTS = ("tv_status_string", "tv_version", "tv_tree_attention_workspace_size",
            "tv_tree_attention", "tv_accept_workspace_size", "tv_accept", "tv_accept_ex",
            "tv_commit_kv",
-           "tv_retained_set", "tv_selftest_wait_timeout", "tv_tree_attention_splits")
+           "tv_retained_set", "tv_selftest_wait_timeout", "tv_tree_attention_plan",
+           "tv_tree_attention_no_alloc")
 
 
 class TVError(RuntimeError):
@@ -52,7 +53,13 @@ class AttnParams(C.Structure):
                 ("head_dim", C.c_int32), ("block_size", C.c_int32),
                 ("max_blocks_per_seq", C.c_int32), ("num_blocks", C.c_int32),
                 ("max_nodes", C.c_int32), ("total_nodes", C.c_int32),
-                ("max_prefix_len", C.c_int32), ("softmax_scale", C.c_float)]
+                ("max_prefix_len", C.c_int32), ("softmax_scale", C.c_float),
+                ("out_dtype", C.c_int32)]
+
+
+class AttnPlan(C.Structure):
+    _fields_ = [("ctas", C.c_int32), ("lanes", C.c_int32), ("virtual_ctas", C.c_int32),
+                ("min_tiles", C.c_int32), ("workspace_bytes", C.c_size_t)]
 
 
 class AcceptParams(C.Structure):
@@ -105,8 +112,8 @@ def load(path: str | None = None) -> C.CDLL:
     lib.tv_tree_attention_no_alloc.restype = C.c_int
     lib.tv_selftest_wait_timeout.argtypes = [vp, vp, C.c_ulonglong, vp]
     lib.tv_selftest_wait_timeout.restype = C.c_int
-    lib.tv_tree_attention_splits.argtypes = [C.POINTER(AttnParams)]
-    lib.tv_tree_attention_splits.restype = C.c_int
+    lib.tv_tree_attention_plan.argtypes = [C.POINTER(AttnParams), C.c_int32, C.POINTER(AttnPlan)]
+    lib.tv_tree_attention_plan.restype = C.c_int
     lib.tv_commit_kv.argtypes = [C.POINTER(CommitParams)] + [vp] * 12 + [vp]
     lib.tv_commit_kv.restype = C.c_int
     lib.tv_retained_set.argtypes = [C.POINTER(RetainParams)] + [vp] * 5 + [vp]
@@ -141,32 +148,42 @@ def _check_dev(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
+OUT_DTYPES = {"bf16": 0, "fp32": 1}
+
+
 def attention_params(q_nodes, k_prefix_blocks, block_table, prefix_lens, *, num_kv_heads,
-                     max_nodes, max_prefix_len, softmax_scale=0.0) -> AttnParams:
+                     max_nodes, max_prefix_len, softmax_scale=0.0, out_dtype="bf16") -> AttnParams:
     total, hq, d = q_nodes.shape
     nb = k_prefix_blocks.shape[0]
     return AttnParams(int(prefix_lens.shape[0]), int(hq), int(num_kv_heads), int(d),
                       int(k_prefix_blocks.shape[2]), int(block_table.shape[1]), int(nb),
-                      int(max_nodes), int(total), int(max_prefix_len), float(softmax_scale))
+                      int(max_nodes), int(total), int(max_prefix_len), float(softmax_scale),
+                      OUT_DTYPES[out_dtype])
 
 
 def attention_workspace_size(params: AttnParams) -> int:
     return int(load().tv_tree_attention_workspace_size(C.byref(params)))
 
 
-def attention_splits(params: AttnParams) -> int:
-    """tv_tree_attention_splits: prefix splits per 128-row tile (-1: invalid)."""
-    return int(load().tv_tree_attention_splits(C.byref(params)))
+def attention_plan(params: AttnParams, sms: int = 0) -> dict:
+    """tv_tree_attention_plan: the launch plan for `sms` SMs (0: the current
+    device).  Raises TVError for invalid parameters."""
+    plan = AttnPlan()
+    rc = load().tv_tree_attention_plan(C.byref(params), int(sms), C.byref(plan))
+    if rc != TV_OK:
+        raise TVError(rc, "tv_tree_attention_plan")
+    return {k: int(getattr(plan, k)) for k, _ in AttnPlan._fields_}
 
 
 def tree_attention(q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nodes, v_nodes,
                    parent, prefix_lens, node_offsets, *, max_nodes: int, max_prefix_len: int,
                    softmax_scale: float = 0.0, out=None, status=None, workspace=None,
-                   stream=None):
+                   stream=None, out_dtype: str = "bf16"):
     """tv_tree_attention on the current stream.  Shapes as in include/tv.h:
     q_nodes [total, Hq, D] bf16; k/v_prefix_blocks [num_blocks, Hkv, 16, D] bf16;
     block_table [B, max_blocks] int32; k/v_nodes [total, Hkv, D] bf16;
     parent [total] int32; prefix_lens [B] int32; node_offsets [B+1] int32.
+    out_dtype "bf16" or "fp32" (the output tensor's type).
     Returns (out, status); nothing is synchronised."""
     import torch
     lib = load()
@@ -174,9 +191,11 @@ def tree_attention(q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nod
                parent, prefix_lens, node_offsets)
     prm = attention_params(q_nodes, k_prefix_blocks, block_table, prefix_lens,
                            num_kv_heads=k_prefix_blocks.shape[1], max_nodes=max_nodes,
-                           max_prefix_len=max_prefix_len, softmax_scale=softmax_scale)
+                           max_prefix_len=max_prefix_len, softmax_scale=softmax_scale,
+                           out_dtype=out_dtype)
     if out is None:
-        out = torch.empty_like(q_nodes)
+        out = torch.empty(q_nodes.shape, device=q_nodes.device,
+                          dtype=torch.float32 if out_dtype == "fp32" else torch.bfloat16)
     if status is None:
         status = torch.empty(prm.batch, dtype=torch.int32, device=q_nodes.device)
     need = int(lib.tv_tree_attention_workspace_size(C.byref(prm)))

@@ -12,39 +12,54 @@
 //   [LLM] "端侧大模型推测解码草稿模型动态剪枝策略：详解基于重要性采样的树形验证并行加速机制":
 //         §2.3.1 variable-length batches through cuSeqLens and block_table.
 //
-// GB300 design.  One CTA computes a 128-row tile of packed query rows of one
-// (sequence, KV head): row R = node * g + head-in-group, so every tree node
-// and every query head of a GQA group share each K/V tile that is staged in
-// shared memory.  The CTA walks its key range in 128-key tiles:
+// GB300 design.
+//
+// Rows.  The packed query rows of one (sequence, KV head) are R = node * g +
+// head-in-group, so every tree node and every query head of a GQA group share
+// each K/V tile.  A unit is 256 consecutive rows (two 128-row m-tiles, an
+// "m-tile pair") of one (sequence, KV head); its keys are the prefix (128-key
+// tiles) followed by the tree nodes (128-node tiles).
+//
+// Work.  The grid is persistent: at most one CTA per SM.  The key tiles of all
+// units are laid out in one line, ordered (sequence, KV head, layer, key
+// tile), where a layer holds `lanes` consecutive m-tile pairs of a (sequence,
+// KV head).  The line is cut into `vctas` contiguous ranges of equal length,
+// one per virtual CTA of `lanes` CTAs; CTA lane i of a virtual CTA computes
+// m-tile pair layer * lanes + i of every (sequence, KV head, layer) in its
+// range.  So every CTA gets the same number of tiles, and the CTAs that read
+// the same K/V tiles (the m-tile pairs of one KV head) walk them at the same
+// time, which keeps the repeated reads in L2.  A range boundary inside a unit
+// splits it into pieces: each piece leaves its unnormalised O and (m, l) in a
+// workspace slot, and the last piece to finish (an arrival counter per unit)
+// merges the slots in a fixed order, so results do not depend on timing.
+//
+// One CTA has 320 threads:
 //   warp 8  (TMA)      loads K and V tiles into two shared-memory rings: one 5-D
 //                      box per 16-token page through the block table (eight
 //                      pages per tile and tensor), or 16 boxes of 8 tree nodes;
 //                      pages past the sequence load as zeros (out of bounds).
-//   warps 9, 10 (MMA)  one thread each issues tcgen05.mma: warp 9 S(t) = Q K^T
-//                      into one of two TMEM score buffers (128 x 128 fp32)
-//                      with Q read from TMEM, warp 10 O += P(t) V into a TMEM
-//                      accumulator (128 x D fp32) with P read from TMEM.
-//   warps 0-7          two softmax lanes: warps 0-3 take the even tiles,
-//                      warps 4-7 the odd ones, one thread per row.  Per
-//                      tile: tcgen05.ld of S (the buffer is released at
-//                      once), the tree mask from a per-node ancestor bitmask
-//                      (shared memory), the row max, fp32 online softmax in
-//                      base 2 against a running max that the two lanes hand
-//                      to each other through mbarriers and that moves only
-//                      when it grows by more than 2^8 (O is then rescaled in
-//                      TMEM), and P as bf16 pairs into TMEM.  Each scheduler
-//                      runs one warp of each lane, so the exponentials of one
-//                      tile overlap the loads and maxima of the next.
-// K and V use the 128-byte swizzle that TMA writes, so the MMA reads them
-// straight from the ring; Q and P never touch shared memory.  Long prefixes
-// may be split over CTAs (split-KV): the splits of a tile run as one
-// thread-block cluster, each keeps its (O, m, l) in fp32 in its own shared
-// memory, and the cluster combines them through distributed shared memory.
+//   warp 9  (MMA)      one thread issues tcgen05.mma for both m-tiles h:
+//                      S_h = Q_h K^T into TMEM (Q_h and K from shared memory),
+//                      O_h += P_h V with P_h read from TMEM, in the order
+//                      PV_0(t), S_0(t+1), PV_1(t), S_1(t+1).  P_h(t) is written
+//                      over the columns of S_h(t); the tensor pipe runs the
+//                      MMAs of one thread in order, so S_h(t+1) overwrites them
+//                      only after PV_h(t) has read them.  While one m-tile's
+//                      softmax runs, the tensor pipe works on the other's.
+//   warps 0-3, 4-7     the softmax of m-tile 0 and of m-tile 1, one thread per
+//                      row: tcgen05.ld of S, the tree mask from a per-row
+//                      ancestor bitmask, the row max, fp32 online softmax in
+//                      base 2 against a running max that moves only when it
+//                      grows by more than 2^8 (O is then rescaled in TMEM), and
+//                      P as bf16 pairs into TMEM; the row sum adds the rounded
+//                      P, so O / l weights V exactly as the P V product did.
+//                      They also load Q (cp.async, in the 128-byte swizzled
+//                      layout the MMA reads), build the ancestor masks and
+//                      write or merge the results.
+// TMEM (512 columns): S_0/P_0 at 0, S_1/P_1 at 128, O_0 at 256, O_1 at 256+D.
 // Every wait on an mbarrier is bounded; on expiry the CTA reports
 // TV_ERR_DEVICE_TIMEOUT for its sequence, drains its copies and returns.
 #include <climits>
-
-#include <cooperative_groups.h>
 
 #include "tv_device.cuh"
 #include "tv_launch.h"
@@ -52,78 +67,91 @@
 namespace tv {
 namespace {
 
-constexpr int BM = 128;           // packed query rows per CTA
-constexpr int BN = 128;           // keys per tile
-constexpr int kSoftmaxThreads = 256;  // warps 0-7: two lanes of four warps
+constexpr int BM = 128;               // rows of one m-tile
+constexpr int BN = 128;               // keys per tile
+constexpr int kUnitRows = 2 * BM;     // rows of one m-tile pair
+constexpr int kSoftmaxThreads = 256;  // warps 0-7: two groups of four warps
 constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;       // issues S = Q K^T; owns the TMEM allocation
-constexpr int kPvWarp = 10;       // issues O += P V
-constexpr int kThreads = 352;     // 8 softmax warps + TMA warp + 2 MMA warps
-constexpr int kMaxAncWords = 16;  // 512-node trees
+constexpr int kMmaWarp = 9;           // issues every MMA; owns the TMEM allocation
+constexpr int kThreads = 320;
+constexpr int kMaxNodes = 512;
+constexpr int kMaxAncWords = kMaxNodes / 32;
 constexpr int kAncStride = kMaxAncWords + 1;  // odd word stride: rows of a warp hit distinct banks
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kOrderMax = 256;    // batches up to this size run longest sequence first
+constexpr int kMaxPieces = 32;        // pieces per scheduling round
 
-// Shared-memory layout of a K or V tile: 16 groups of 8 keys; a group holds
-// the 64-column halves of its 8 rows one after the other, each half an
-// 8 x 128-byte swizzle atom: [group][half][row][128 B].  A 16-token page is
-// two consecutive groups, so one TMA box brings a whole page, and for a fixed
-// half the 8-row groups sit at a uniform stride (kGroupBytes), which is what
-// the MMA descriptors need (K-major for K, MN-major for V).
+// Named barriers (0 is __syncthreads): one per softmax group, both groups.
+constexpr int kBarGroup0 = 1;         // group h uses kBarGroup0 + h
+constexpr int kBarPair = 3;
+
+// A piece: the key tiles [t0, t1) of one unit that this CTA computes.
+struct Piece {
+  int b, kvh, mp;   // sequence, KV head, m-tile pair
+  int t0, t1;       // key tiles of the unit
+  int P;            // prefix tiles of the sequence (node tiles follow)
+  int L, n0, N;     // prefix length, first node, nodes of the sequence
+  int rows;         // packed rows of the unit (1 .. 256)
+  int nm;           // m-tiles with rows (1 or 2)
+  int slot;         // partial-result slot, -1 when the piece is the whole unit
+  int cnt;          // arrival counter of a split unit
+  int npieces;      // pieces of a split unit
+  int vfirst;       // virtual CTA of the unit's first piece
+  int pad;
+};
+
 template <int D>
 struct Layout {
   static constexpr int kHalves = D / 64;
-  static constexpr int kStages = D == 128 ? 3 : 6;     // depth of the K ring and of the V ring
-  static constexpr int kGroupBytes = kHalves * 1024;   // 8 keys, all columns
-  static constexpr int kTileBytes = BN * D * 2;        // one K or V tile (16 groups)
-  static constexpr int kKRing = 0;                     // kStages K tiles
-  static constexpr int kVRing = kKRing + kStages * kTileBytes;  // kStages V tiles
-  static constexpr int kAnc = kVRing + kStages * kTileBytes;
-  static constexpr int kAncBytes = BM * kAncStride * 4;
-  static constexpr int kParent = kAnc + kAncBytes;
-  static constexpr int kParentBytes = 512 * 4;
-  static constexpr int kXchg = kParent + kParentBytes;  // row max / sum exchange
-  // running max after tile t (slot t & 1, 2 x 128 floats), then the
-  // final (reference max, row sum) of each lane (2 x 128 float2)
-  static constexpr int kXchgBytes = 2 * BM * 4 + 2 * BM * 8;
+  static constexpr int kStages = D == 128 ? 2 : 4;     // depth of the K ring and of the V ring
+  static constexpr int kGroupBytes = kHalves * 1024;   // 8 rows, all columns
+  static constexpr int kTileBytes = BN * D * 2;        // one K or V tile
+  static constexpr int kQBytes = BM * D * 2;           // Q of one m-tile
+  static constexpr int kQ = 0;                         // Q_0, Q_1
+  static constexpr int kKRing = kQ + 2 * kQBytes;
+  static constexpr int kVRing = kKRing + kStages * kTileBytes;
+  static constexpr int kAnc = kVRing + kStages * kTileBytes;  // [2][128][kAncStride] words
+  static constexpr int kAncBytes = 2 * BM * kAncStride * 4;
+  static constexpr int kParent = kAnc + kAncBytes;            // [2][512]
+  static constexpr int kParentBytes = 2 * kMaxNodes * 4;
+  static constexpr int kPieces = kParent + kParentBytes;
+  static constexpr int kPiecesBytes = kMaxPieces * static_cast<int>(sizeof(Piece));
+  static constexpr int kScan = kPieces + kPiecesBytes;        // 8 warp sums (int64)
+  static constexpr int kScanBytes = 128;
   // block ids of the pages of the last 8 K tiles issued (8 per tile), reused
   // by the V copies of the same tiles
-  static constexpr int kBlk = kXchg + kXchgBytes;
+  static constexpr int kBlk = kScan + kScanBytes;
   static constexpr int kBlkBytes = 8 * 8 * 4;
-  // per-sequence (prefix length, first node, last node + 1) and the
-  // longest-first order of the sequences (batches up to kOrderMax)
-  static constexpr int kSeq = kBlk + kBlkBytes;
-  static constexpr int kSeqBytes = 4 * kOrderMax * 4;
-  static constexpr int kBar = kSeq + kSeqBytes;
-  // kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages],
-  // s_full[2], s_free[2], p_full, o_done[2], drain[2], chain[2][4], q_ready
-  static constexpr int kNumBars = 4 * kStages + 18;
+  static constexpr int kBar = kBlk + kBlkBytes;
+  // kfull[S], kempty[S], vfull[S], vempty[S], s_full[2], p_full[2],
+  // o_done[2], q_full[2], drain
+  static constexpr int kNumBars = 4 * kStages + 9;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kTotal = kMisc + 64;
+  static constexpr int kMiscBytes = 512;
+  static constexpr int kTotal = kMisc + kMiscBytes;
   static constexpr int kAlloc = kTotal + 1024;  // slack for 1024-byte alignment
-  // TMEM columns: S buffers (128 x 128 fp32) at 0 and 128; O at 256 (D
-  // columns); P (128 keys as bf16 pairs, 64 columns) at 384; Q at 448 (bf16
-  // pairs, D/2 columns).
   static constexpr int kTmemCols = 512;
+  static_assert(kAlloc <= 232448, "shared memory per CTA");
 };
 
 struct Misc {
   uint32_t tmem_base;
   int abort;
-  int bad;
+  int npieces;                // pieces of this round
+  int more;                   // another round follows
+  int merge;                  // this CTA merges the current split unit
+  int tree_bad[2];            // per group: the tree of its current piece is malformed
+  int piece_bad[kMaxPieces];  // a block id of the piece was out of range
 };
 
-struct Work {
-  int b, kvh, mtile, split;
-  int n0, N, L;
-  int rows;      // N * g
-  int nsplit;    // splits of this sequence
-  int k_begin, k_end;
-  int n_prefix_tiles, n_node_tiles, T;
-  bool last_split;
+// Partial-result slot: O rows (fp32, unnormalised), (m, l) per row, a flag.
+template <int D>
+struct Slot {
+  static constexpr size_t kO = 0;
+  static constexpr size_t kMl = static_cast<size_t>(kUnitRows) * D * 4;
+  static constexpr size_t kFlag = kMl + kUnitRows * 8;
+  static constexpr size_t kBytes = kFlag + 256;
 };
 
-// TMEM lane offset of a softmax warp (its 32-lane quarter).
 __device__ __forceinline__ uint32_t lane_off_q(int warp) {
   return static_cast<uint32_t>((warp & 3) * 32) << 16;
 }
@@ -135,206 +163,326 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// Named barrier 1 joins the 8 softmax warps (0 is __syncthreads).
-__device__ __forceinline__ void softmax_group_sync() {
-  asm volatile("bar.sync 1, 256;" ::: "memory");
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ void record_status(int32_t* status, int b, int code) {
   atomicMax(status + b, code);
 }
 
-// Zeros output row r (0..127) of this tile if it is a live row.
-template <int D>
-__device__ __forceinline__ void zero_rows(const AttnArgs& a, const Work& w, int r) {
-  const int R = w.mtile * BM + r;
-  if (R >= w.rows) return;
-  const int i = R / a.group, h = w.kvh * a.group + R % a.group;
-  uint4* dst = reinterpret_cast<uint4*>(a.out + (static_cast<size_t>(w.n0 + i) * a.hq + h) * D);
-#pragma unroll
-  for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-}
-
-// Split-KV partials: each split of a tile keeps its raw O rows (fp32, rows
-// padded by 4 floats so that a warp's row stores and reads are free of bank
-// conflicts) and per-row (m, l) in its own shared memory, over the K ring,
-// which is idle once the last S = Q K^T has completed.
-template <int D>
-struct Partial {
-  static constexpr int kStride = D + 4;                 // floats per row
-  static constexpr int kO = 0;                          // offset in the K ring
-  static constexpr int kMl = BM * kStride * 4;
-  static constexpr int kBytes = kMl + BM * 8;
-  static_assert(kBytes <= Layout<D>::kStages * Layout<D>::kTileBytes, "partial exceeds the K ring");
+// ---------------------------------------------------------------- schedule
+struct SeqInfo {
+  int L, n0, N;
+  int P, T;          // prefix tiles; key tiles of a unit (prefix + node tiles)
+  int mpairs;        // m-tile pairs (units per KV head)
+  int layers;        // ceil(mpairs / lanes)
+  int valid;         // extent well formed
+  long long W;       // tiles of the sequence on the line
 };
 
-// Combines the NS splits of this tile (the CTAs of the cluster) for the rows
-// r = rank, rank + NS, ... : O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M)
-// l_s, reading every split's partial through distributed shared memory.  A
-// warp takes a group of rows, four columns per lane, and issues all of the
-// group's loads before combining them (16 partial rows in flight per lane).
-// A tile whose sequence was found malformed by any split (`bad` flag of any
-// CTA of the cluster) gets zeros.
-template <int D, int NS>
-__device__ __forceinline__ void merge_rows_ns(const AttnArgs& a, const Work& w, uint8_t* ring,
-                                              const int* bad_flag, int sid, int rank) {
-  namespace cg = cooperative_groups;
-  using Pt = Partial<D>;
-  constexpr int kWarps = kSoftmaxThreads / 32;
-  constexpr int kRows = (16 / NS) > 0 ? 16 / NS : 1;  // rows per warp and group
-  cg::cluster_group cluster = cg::this_cluster();
-  bool bad = false;
+__device__ __forceinline__ SeqInfo seq_info(const AttnArgs& a, int b) {
+  SeqInfo s;
+  s.L = max(0, __ldg(a.prefix_lens + b));
+  s.n0 = __ldg(a.node_offsets + b);
+  s.N = __ldg(a.node_offsets + b + 1) - s.n0;
+  s.valid = s.N >= 1 && s.N <= a.max_nodes && s.N <= kMaxNodes && s.n0 >= 0 &&
+            s.n0 + s.N <= a.total_nodes && s.L <= a.max_prefix_len;
+  s.P = (s.L + BN - 1) / BN;
+  s.T = s.P + (s.N + BN - 1) / BN;
+  s.mpairs = s.valid ? (s.N * a.group + kUnitRows - 1) / kUnitRows : 0;
+  s.layers = (s.mpairs + a.lanes - 1) / a.lanes;
+  s.W = s.valid ? static_cast<long long>(a.hkv) * s.layers * s.T : 0;
+  return s;
+}
+
+// Exclusive scan over the 256 softmax threads; *total = the sum.
+__device__ __forceinline__ long long scan256(long long v, long long* scratch, int sid,
+                                             long long* total) {
+  const int lane = sid & 31, w = sid >> 5;
+  long long x = v;
 #pragma unroll
-  for (int s = 0; s < NS; ++s) bad |= *cluster.map_shared_rank(bad_flag, s) != 0;
-  const float* o_peer[NS];
-  const float2* ml_peer[NS];
-#pragma unroll
-  for (int s = 0; s < NS; ++s) {
-    o_peer[s] = cluster.map_shared_rank(reinterpret_cast<const float*>(ring + Pt::kO), s);
-    ml_peer[s] = cluster.map_shared_rank(reinterpret_cast<const float2*>(ring + Pt::kMl), s);
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  const int lane = sid & 31;
-  for (int r0 = rank + (sid >> 5) * NS; r0 < BM; r0 += kRows * kWarps * NS) {
-    int rr[kRows];
-    bool ok_row[kRows];
+  if (lane == 31) scratch[w] = x;
+  named_sync(kBarPair, kSoftmaxThreads);
+  long long before = 0, all = 0;
 #pragma unroll
-    for (int k = 0; k < kRows; ++k) {
-      rr[k] = r0 + k * kWarps * NS;
-      ok_row[k] = rr[k] < BM && w.mtile * BM + rr[k] < w.rows;
+  for (int k = 0; k < 8; ++k) {
+    const long long s = scratch[k];
+    if (k < w) before += s;
+    all += s;
+  }
+  named_sync(kBarPair, kSoftmaxThreads);  // scratch may be reused
+  *total = all;
+  return before + x - v;
+}
+
+// The virtual CTA whose range [floor(v W / V), floor((v+1) W / V)) holds
+// line position p (0 <= p < W).
+__device__ __forceinline__ int vcta_of(long long p, long long W, int V) {
+  int v = static_cast<int>((p * V) / W);
+  while (v + 1 < V && ((v + 1) * W) / V <= p) ++v;
+  while (v > 0 && (v * W) / V > p) --v;
+  return v;
+}
+
+// Builds this CTA's pieces of scheduling round `round` into shared memory
+// (run by the 256 softmax threads).  In round 0 it also zeroes the output of
+// sequences whose extent is malformed (every row it can address) and records
+// their status.
+template <int D>
+__device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int sid) {
+  using Ly = Layout<D>;
+  Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
+  Piece* pieces = reinterpret_cast<Piece*>(smem + Ly::kPieces);
+  long long* scratch = reinterpret_cast<long long*>(smem + Ly::kScan);
+  const size_t out_elem = a.out_fp32 ? 4 : 2;
+  // the length of the line; malformed sequences of this CTA (b mod grid)
+  long long W = 0;
+  for (int base = 0; base < a.batch; base += kSoftmaxThreads) {
+    const int b = base + sid;
+    long long w = 0;
+    if (b < a.batch) {
+      const SeqInfo s = seq_info(a, b);
+      w = s.W;
+      if (round == 0 && !s.valid && s.N >= 1 && b % gridDim.x == blockIdx.x)
+        record_status(a.status, b, kBadTree);
     }
-    for (int c = lane * 4; c < D; c += 128) {
-      float2 ml[kRows][NS];
-      float4 v[kRows][NS];
-#pragma unroll
-      for (int k = 0; k < kRows; ++k)
-#pragma unroll
-        for (int s = 0; s < NS; ++s)
-          if (ok_row[k]) {
-            ml[k][s] = ml_peer[s][rr[k]];
-            v[k][s] = *reinterpret_cast<const float4*>(o_peer[s] + rr[k] * Pt::kStride + c);
+    long long tot;
+    scan256(w, scratch, sid, &tot);
+    W += tot;
+  }
+  if (round == 0) {
+    // the rows of a malformed sequence that can be addressed get zeros
+    for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
+      const SeqInfo s = seq_info(a, b);
+      if (s.valid || s.N < 1 || s.n0 < 0 || s.n0 + s.N > a.total_nodes) continue;
+      const size_t n = static_cast<size_t>(s.N) * a.hq * D * out_elem / 16;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) +
+                                            static_cast<size_t>(s.n0) * a.hq * D * out_elem);
+      for (size_t k = sid; k < n; k += kSoftmaxThreads) dst[k] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  const int lanes = a.lanes;
+  const int v = static_cast<int>(blockIdx.x) / lanes, li = static_cast<int>(blockIdx.x) % lanes;
+  const int V = static_cast<int>(
+      max(1ll, min(static_cast<long long>(a.vctas), W / max(1, a.min_tiles))));
+  int count = 0;  // pieces of this CTA before the current chunk (all rounds)
+  if (W > 0 && v < V) {
+    const long long s_v = (v * W) / V, e_v = ((v + 1) * W) / V;
+    long long cum = 0;
+    for (int base = 0; base < a.batch; base += kSoftmaxThreads) {
+      const int b = base + sid;
+      SeqInfo s;
+      s.W = 0;
+      s.T = 1;
+      s.layers = 1;
+      if (b < a.batch) s = seq_info(a, b);
+      long long tot;
+      const long long c0 = cum + scan256(s.W, scratch, sid, &tot);
+      // the units of b that meet [s_v, e_v), in line order; the unit of a
+      // lane past the sequence's m-tile pairs is idle and skipped
+      int mine = 0;
+      long long lo = 0, hi = 0;
+      if (s.W > 0) {
+        lo = max(s_v, c0) - c0;
+        hi = min(e_v, c0 + s.W) - c0;
+        if (lo < hi)
+          for (long long ui = lo / s.T; ui <= (hi - 1) / s.T; ++ui)
+            if (static_cast<int>(ui % s.layers) * lanes + li < s.mpairs) ++mine;
+      }
+      long long ptot;
+      const int first = count + static_cast<int>(scan256(mine, scratch, sid, &ptot));
+      if (mine > 0) {
+        int k = first;
+        for (long long ui = lo / s.T; ui <= (hi - 1) / s.T; ++ui) {
+          const int kvh = static_cast<int>(ui / s.layers), layer = static_cast<int>(ui % s.layers);
+          const int mp = layer * lanes + li;
+          if (mp >= s.mpairs) continue;
+          const int slot_i = k - round * kMaxPieces;
+          ++k;
+          if (slot_i < 0 || slot_i >= kMaxPieces) continue;
+          Piece pc;
+          const long long u0 = c0 + ui * s.T;  // line position of the unit's first tile
+          pc.b = b;
+          pc.kvh = kvh;
+          pc.mp = mp;
+          pc.t0 = static_cast<int>(max(lo, ui * s.T) - ui * s.T);
+          pc.t1 = static_cast<int>(min(hi, (ui + 1) * s.T) - ui * s.T);
+          pc.P = s.P;
+          pc.L = s.L;
+          pc.n0 = s.n0;
+          pc.N = s.N;
+          pc.rows = min(kUnitRows, s.N * a.group - mp * kUnitRows);
+          pc.nm = pc.rows > BM ? 2 : 1;
+          if (pc.t0 == 0 && pc.t1 == s.T) {
+            pc.slot = -1;
+            pc.cnt = -1;
+            pc.npieces = 1;
+            pc.vfirst = v;
+          } else {
+            // the first piece (it holds tile 0) uses the CTA's slot 1, every
+            // later piece (it starts the CTA's range) slot 0
+            const int vf = vcta_of(u0, W, V), vl = vcta_of(u0 + s.T - 1, W, V);
+            pc.vfirst = vf;
+            pc.npieces = vl - vf + 1;
+            pc.cnt = vf * lanes + li;
+            pc.slot = 2 * static_cast<int>(blockIdx.x) + (pc.t0 > 0 ? 0 : 1);
           }
-#pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        if (!ok_row[k]) continue;
-        float M = -INFINITY;
-#pragma unroll
-        for (int s = 0; s < NS; ++s) M = fmaxf(M, ml[k][s].x);
-        const float mref = (M == -INFINITY) ? 0.0f : M;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float lsum = 0.0f;
-#pragma unroll
-        for (int s = 0; s < NS; ++s) {
-          const float wgt = (ml[k][s].x == -INFINITY) ? 0.0f : exp2f(ml[k][s].x - mref);
-          lsum += wgt * ml[k][s].y;
-          acc.x += wgt * v[k][s].x;
-          acc.y += wgt * v[k][s].y;
-          acc.z += wgt * v[k][s].z;
-          acc.w += wgt * v[k][s].w;
+          pc.pad = 0;
+          pieces[slot_i] = pc;
         }
-        const float inv = (lsum > 0.0f) ? __frcp_rn(lsum) : 0.0f;
-        uint2 o = make_uint2(0u, 0u);
-        if (!bad) {
-          o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-          o.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        }
-        const int R = w.mtile * BM + rr[k];
-        const int i = R / a.group, h = w.kvh * a.group + R % a.group;
-        *reinterpret_cast<uint2*>(a.out + (static_cast<size_t>(w.n0 + i) * a.hq + h) * D + c) = o;
+      }
+      count += static_cast<int>(ptot);
+      cum += tot;
+    }
+  }
+  if (sid == 0) {
+    const int n = count - round * kMaxPieces;
+    misc->npieces = max(0, min(kMaxPieces, n));
+    misc->more = n > kMaxPieces;
+    for (int k = 0; k < kMaxPieces; ++k) misc->piece_bad[k] = 0;
+  }
+}
+
+// ---------------------------------------------------------------- output
+// Writes 32 values of one output row (fp32 or bf16) at column c0.
+template <int D>
+__device__ __forceinline__ void store_row_chunk(const AttnArgs& a, size_t row, int c0,
+                                                const float (&v)[32]) {
+  if (a.out_fp32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + row * D + c0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + row * D + c0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint4 w;
+      w.x = pack_bf16x2(v[8 * k + 0], v[8 * k + 1]);
+      w.y = pack_bf16x2(v[8 * k + 2], v[8 * k + 3]);
+      w.z = pack_bf16x2(v[8 * k + 4], v[8 * k + 5]);
+      w.w = pack_bf16x2(v[8 * k + 6], v[8 * k + 7]);
+      dst[k] = w;
+    }
+  }
+}
+
+__device__ __forceinline__ int piece_slot(const AttnArgs& a, const Piece& pc, int s) {
+  const int cta = (pc.vfirst + s) * a.lanes + static_cast<int>(blockIdx.x) % a.lanes;
+  return s == 0 ? 2 * cta + 1 : 2 * cta;
+}
+
+// Merges the pieces of a split unit: O = sum_s 2^(m_s - M) O_s /
+// sum_s 2^(m_s - M) l_s over the slots in piece order.  `nthreads` threads
+// (thread sid) take the rows, a warp per row, the lanes D/32 columns each.
+template <int D>
+__device__ void merge_unit(const AttnArgs& a, const Piece& pc, int sid, int nthreads) {
+  using Sl = Slot<D>;
+  constexpr int kCols = D / 32;  // columns per lane
+  const int lane = sid & 31, w = sid >> 5, nw = nthreads >> 5;
+  bool bad = false;
+  for (int s = 0; s < pc.npieces; ++s)
+    bad |= __ldcg(reinterpret_cast<const int*>(a.slots + piece_slot(a, pc, s) * Sl::kBytes +
+                                               Sl::kFlag)) != 0;
+  const int g = a.group;
+  for (int ur = w; ur < pc.rows; ur += nw) {
+    float M = -INFINITY;
+    for (int s = 0; s < pc.npieces; ++s) {
+      const float2 ml = __ldcg(
+          reinterpret_cast<const float2*>(a.slots + piece_slot(a, pc, s) * Sl::kBytes + Sl::kMl) + ur);
+      M = fmaxf(M, ml.x);
+    }
+    const float mref = M == -INFINITY ? 0.0f : M;
+    float acc[kCols];
+#pragma unroll
+    for (int k = 0; k < kCols; ++k) acc[k] = 0.0f;
+    float lsum = 0.0f;
+    for (int s = 0; s < pc.npieces; ++s) {
+      const uint8_t* base = a.slots + piece_slot(a, pc, s) * Sl::kBytes;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + ur);
+      const float wgt = ml.x == -INFINITY ? 0.0f : exp2f(ml.x - mref);
+      lsum += wgt * ml.y;
+      const float* o = reinterpret_cast<const float*>(base + Sl::kO) + static_cast<size_t>(ur) * D + lane * kCols;
+      if constexpr (kCols == 4) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(o));
+        acc[0] += wgt * x.x;
+        acc[1] += wgt * x.y;
+        acc[2] += wgt * x.z;
+        acc[3] += wgt * x.w;
+      } else {
+        const float2 x = __ldcg(reinterpret_cast<const float2*>(o));
+        acc[0] += wgt * x.x;
+        acc[1] += wgt * x.y;
+      }
+    }
+    const float inv = (lsum > 0.0f && !bad) ? 1.0f / lsum : 0.0f;
+    const int R = pc.mp * kUnitRows + ur;
+    const size_t row = static_cast<size_t>(pc.n0 + R / g) * a.hq + pc.kvh * g + R % g;
+    if (a.out_fp32) {
+      float* dst = static_cast<float*>(a.out) + row * D + lane * kCols;
+      if constexpr (kCols == 4) {
+        *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+      } else {
+        *reinterpret_cast<float2*>(dst) = make_float2(acc[0] * inv, acc[1] * inv);
+      }
+    } else {
+      uint16_t* dst = static_cast<uint16_t*>(a.out) + row * D + lane * kCols;
+      if constexpr (kCols == 4) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                    pack_bf16x2(acc[2] * inv, acc[3] * inv));
+      } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
       }
     }
   }
 }
 
+// ---------------------------------------------------------------- the kernel
 template <int D>
-__device__ __forceinline__ void merge_rows(const AttnArgs& a, const Work& w, uint8_t* ring,
-                                           const int* bad_flag, int sid, int rank) {
-  switch (w.nsplit) {
-    case 2: merge_rows_ns<D, 2>(a, w, ring, bad_flag, sid, rank); break;
-    case 3: merge_rows_ns<D, 3>(a, w, ring, bad_flag, sid, rank); break;
-    case 4: merge_rows_ns<D, 4>(a, w, ring, bad_flag, sid, rank); break;
-    case 5: merge_rows_ns<D, 5>(a, w, ring, bad_flag, sid, rank); break;
-    case 6: merge_rows_ns<D, 6>(a, w, ring, bad_flag, sid, rank); break;
-    case 7: merge_rows_ns<D, 7>(a, w, ring, bad_flag, sid, rank); break;
-    case 8: merge_rows_ns<D, 8>(a, w, ring, bad_flag, sid, rank); break;
-    default: break;
-  }
-}
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
     tree_attn_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps) {
   using Ly = Layout<D>;
+  using Sl = Slot<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kBar);
   constexpr int kStages = Ly::kStages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kBar);
   uint64_t* kfull = bars;
   uint64_t* kempty = bars + kStages;
   uint64_t* vfull = bars + 2 * kStages;
   uint64_t* vempty = bars + 3 * kStages;
-  uint64_t* s_full = bars + 4 * kStages;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  // o_done[t & 1] completes with P(t).V.  A wait for P(t-1).V comes after the
-  // same lane has seen P(t-2).V (or before any), so the phase of P(t-3).V is
-  // complete and the parity ((t-1) >> 1) & 1 cannot alias an older phase
-  // (one barrier for all tiles could: P(t-2).V may still be in flight).
-  uint64_t* o_done = p_full + 1;
-  uint64_t* drain = o_done + 2;  // one per MMA-issuing thread
-  // running-max hand-off: chain[l][q] completes once per tile of lane l
-  // for the rows of lane quarter q (arrived by the warp of lane l, awaited by
-  // the warp of the other lane that owns the same rows)
-  uint64_t* chain = drain + 2;
-  uint64_t* q_ready = chain + 8;
+  uint64_t* s_full = bars + 4 * kStages;  // [2]: S_h(t) complete (and every MMA before it)
+  uint64_t* p_full = s_full + 2;          // [2]: P_h(t) in TMEM (128 arrivals)
+  uint64_t* o_done = p_full + 2;          // [2]: the last P_h V of a piece complete
+  uint64_t* q_full = o_done + 2;          // [2]: Q_h of a piece in shared memory (128 arrivals)
+  uint64_t* drain = q_full + 2;           // every MMA issued so far complete (once per round)
   Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
-  uint32_t* anc = reinterpret_cast<uint32_t*>(smem + Ly::kAnc);
-  int32_t* par = reinterpret_cast<int32_t*>(smem + Ly::kParent);
+  Piece* pieces = reinterpret_cast<Piece*>(smem + Ly::kPieces);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // ------------------------------------------------------------ work item
-  // Grid z enumerates (sequence rank, KV head).  For batches of 2 up to
-  // kOrderMax the rank orders the sequences by decreasing work (prefix plus
-  // tree keys, ties by index), so that the CTAs that run longest are
-  // dispatched first and the launch does not end on a tail of long CTAs.
-  // The extents of all sequences are loaded first; barrier set-up and the
-  // TMEM allocation below overlap the load latency.
-  int* seq = reinterpret_cast<int*>(smem + Ly::kSeq);  // [4][kOrderMax]
-  const bool ordered = a.batch > 1 && a.batch <= kOrderMax;
-  if (ordered && tid < a.batch) {
-    seq[tid] = max(0, __ldg(a.prefix_lens + tid));
-    seq[kOrderMax + tid] = __ldg(a.node_offsets + tid);
-    seq[2 * kOrderMax + tid] = __ldg(a.node_offsets + tid + 1);
-  }
-  Work w;
-  w.mtile = blockIdx.x;
-  w.split = blockIdx.y;
-  w.kvh = blockIdx.z % a.hkv;
-
-  // ------------------------------------------------------------ prologue
   if (tid == 0) {
     misc->abort = 0;
-    misc->bad = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&kfull[s], 1);
       mbar_init(&kempty[s], 1);
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 1);
     }
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(&s_full[k], 1);
-      mbar_init(&s_free[k], kSoftmaxThreads / 2);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&s_full[h], 1);
+      mbar_init(&p_full[h], BM);
+      mbar_init(&o_done[h], 1);
+      mbar_init(&q_full[h], BM);
     }
-    mbar_init(p_full, kSoftmaxThreads / 2);
-    mbar_init(&o_done[0], 1);
-    mbar_init(&o_done[1], 1);
-    mbar_init(&drain[0], 1);
-    mbar_init(&drain[1], 1);
-    for (int k = 0; k < 8; ++k) mbar_init(&chain[k], 32);
-    mbar_init(q_ready, kSoftmaxThreads);
+    mbar_init(drain, 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -345,539 +493,511 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
-  if (ordered) {
-    if (tid < a.batch) {
-      const int key = seq[tid] + seq[2 * kOrderMax + tid] - seq[kOrderMax + tid];
-      int rank = 0;
-      for (int u = 0; u < a.batch; ++u) {
-        const int ku = seq[u] + seq[2 * kOrderMax + u] - seq[kOrderMax + u];
-        rank += (ku > key) || (ku == key && u < tid);
-      }
-      seq[3 * kOrderMax + rank] = tid;
-    }
-    __syncthreads();
-    w.b = seq[3 * kOrderMax + blockIdx.z / a.hkv];
-    w.n0 = seq[kOrderMax + w.b];
-    w.N = seq[2 * kOrderMax + w.b] - w.n0;
-    w.L = seq[w.b];
-  } else {
-    w.b = blockIdx.z / a.hkv;
-    w.n0 = __ldg(a.node_offsets + w.b);
-    w.N = __ldg(a.node_offsets + w.b + 1) - w.n0;
-    w.L = max(0, __ldg(a.prefix_lens + w.b));
-  }
-
-  w.rows = w.N * a.group;
-  // Split-KV: the prefix of each sequence is cut into at most max_splits
-  // ranges of whole 128-key tiles; the splits of one tile form a cluster
-  // (grid y), and a member whose sequence has fewer splits only joins the
-  // cluster barriers.
-  const int chunk = max(BN, ((w.L + a.max_splits - 1) / a.max_splits + BN - 1) / BN * BN);
-  w.nsplit = max(1, (w.L + chunk - 1) / chunk);
-  if (w.N < 1 || w.mtile * BM >= w.rows) {  // no work for the whole cluster
-    if (warp == kMmaWarp) tmem_dealloc(tmem, Ly::kTmemCols);
-    return;
-  }
-  const bool idle = w.split >= w.nsplit;
-  w.last_split = (w.split == w.nsplit - 1);
-  w.k_begin = w.split * chunk;
-  w.k_end = min(w.L, w.k_begin + chunk);
-  w.n_prefix_tiles = idle ? 0 : (w.k_end - w.k_begin + BN - 1) / BN;
-  w.n_node_tiles = w.last_split ? (w.N + BN - 1) / BN : 0;
-  w.T = w.n_prefix_tiles + w.n_node_tiles;
-  const int node_lo = (w.mtile * BM) / a.group;
-  const int g = a.group;
-  // the sequence's extent itself is malformed: nothing to read
-  if (w.N > a.max_nodes || w.N > 512 || w.L > a.max_prefix_len || w.n0 < 0 ||
-      w.n0 + w.N > a.total_nodes) {
-    if (tid == 0) record_status(a.status, w.b, kBadTree);
-    const bool rows_addressable = w.n0 >= 0 && w.N <= a.max_nodes && w.n0 + w.N <= a.total_nodes;
-    // every CTA of the cluster takes this branch; split 0 writes the zeros
-    if (w.split == 0 && rows_addressable && warp < 4) zero_rows<D>(a, w, tid);
-    if (warp == kMmaWarp) tmem_dealloc(tmem, Ly::kTmemCols);
-    return;
-  }
-  const uint32_t tmem_o = tmem + 256;   // O accumulator at columns 256 .. 256+D-1
-  const uint32_t tmem_p = tmem + 384;   // P at columns 384 .. 447
-  const uint32_t tmem_q = tmem + 448;   // Q tile (A operand of Q.K^T)
   volatile int* abort_flag = &misc->abort;
+  const int g = a.group;
 
-  if (idle) {
-    // a cluster member without keys: straight to the cluster barriers
-  } else if (warp == kTmaWarp) {
-    // ---------------------------------------------------------- TMA producer
-    // K and V stream through separate rings: a K slot is free again as soon
-    // as S = Q K^T has read it, a V slot once P.V has, so K runs ahead of V.
-    // The whole warp issues a tile: lane 0 arms the slot's barrier, then lane
-    // u issues box u: page u of a prefix tile (one 5-D box per 16-token page,
-    // 8 per tile) or the u-th group of 8 nodes of a node tile (16 per tile).
-    if (lane == 0) {
-      prefetch_tmap(&maps.k_pool);
-      prefetch_tmap(&maps.v_pool);
-      prefetch_tmap(&maps.k_nodes);
-      prefetch_tmap(&maps.v_nodes);
-    }
-    constexpr int kPages = BN / 16;
-    constexpr int kPastEnd = INT_MIN;                 // page past the prefix end -> zeros
-    const bool prefix_lane = lane < kPages;
-    const int pool_pages = a.num_blocks * a.hkv;
-    const int32_t* btab = a.block_table + static_cast<size_t>(w.b) * a.max_blocks_per_seq;
-    auto fetch_block = [&](int t) -> int {
-      const int lp = (w.k_begin + t * BN) / 16 + lane;
-      return (prefix_lane && t < w.n_prefix_tiles && lp * 16 < w.k_end) ? __ldg(btab + lp) : kPastEnd;
-    };
-    // issues tile t of tensor kv (0 = K, 1 = V) into its slot
-    auto issue = [&](int t, int kv, int blk) {
-      const int st = t % kStages;
-      uint64_t* bar = kv ? &vfull[st] : &kfull[st];
-      if (lane == 0) mbar_arrive_expect_tx(bar, Ly::kTileBytes);
-      __syncwarp();
-      uint8_t* tile = smem + (kv ? Ly::kVRing : Ly::kKRing) + st * Ly::kTileBytes;
-      if (t < w.n_prefix_tiles) {
-        if (prefix_lane) {
-          int page = pool_pages;  // out of bounds: zero fill
-          if (blk >= 0 && blk < a.num_blocks) {
-            page = blk * a.hkv + w.kvh;
-          } else if (blk != kPastEnd && kv == 0 && !misc->bad) {  // malformed block id: zeros, reported
-            misc->bad = 1;
-            record_status(a.status, w.b, kBadTree);
+  // Progress kept across pieces and rounds (ring slots and barrier phases):
+  // g_tile = K/V tiles of every earlier round; in a role, the tiles and the
+  // pieces of m-tile h so far (MMA: both m-tiles; softmax: its own).
+  int g_tile = 0;
+  int tiles_h0 = 0, tiles_h1 = 0, pieces_h0 = 0, pieces_h1 = 0;
+
+  for (int round = 0;; ++round) {
+    if (warp < kTmaWarp) build_schedule<D>(a, smem, round, tid);
+    __syncthreads();
+    const int npieces = misc->npieces;
+    const bool more = misc->more != 0;
+    if (npieces == 0 || misc->abort) break;
+
+    if (warp == kTmaWarp) {
+      // ------------------------------------------------------ TMA producer
+      // The whole warp issues a tile: lane 0 arms the slot's barrier, then
+      // lane u issues box u: page u of a prefix tile (one 5-D box per
+      // 16-token page, 8 per tile) or the u-th group of 8 nodes of a node
+      // tile (16 per tile).  K runs ahead of V: a K slot is free again once
+      // the last S of its tile is done, a V slot once the last P V is.
+      if (round == 0 && lane == 0) {
+        prefetch_tmap(&maps.k_pool);
+        prefetch_tmap(&maps.v_pool);
+        prefetch_tmap(&maps.k_nodes);
+        prefetch_tmap(&maps.v_nodes);
+      }
+      constexpr int kPages = BN / 16;
+      constexpr int kPastEnd = INT_MIN;  // page past the prefix end -> zeros
+      const bool page_lane = lane < kPages;
+      const int pool_pages = a.num_blocks * a.hkv;
+      int* blk_ring = reinterpret_cast<int*>(smem + Ly::kBlk);  // [tile & 7][page]
+      volatile int* piece_bad = misc->piece_bad;
+      auto fetch_block = [&](int p, int t) -> int {
+        if (p >= npieces || !page_lane) return kPastEnd;
+        const Piece& pc = pieces[p];
+        if (t >= pc.P) return kPastEnd;
+        const int lp = t * kPages + lane;
+        return lp * 16 < pc.L
+                   ? __ldg(a.block_table + static_cast<size_t>(pc.b) * a.max_blocks_per_seq + lp)
+                   : kPastEnd;
+      };
+      // issues tile t of piece p (global tile tau) of tensor kv (0 = K, 1 = V)
+      auto issue = [&](int p, int t, int tau, int kv, int blk) {
+        const Piece& pc = pieces[p];
+        const int st = tau % kStages;
+        uint64_t* bar = kv ? &vfull[st] : &kfull[st];
+        if (lane == 0) mbar_arrive_expect_tx(bar, Ly::kTileBytes);
+        __syncwarp();
+        uint8_t* tile = smem + (kv ? Ly::kVRing : Ly::kKRing) + st * Ly::kTileBytes;
+        if (t < pc.P) {
+          if (page_lane) {
+            int page = pool_pages;  // out of bounds: zero fill
+            if (blk >= 0 && blk < a.num_blocks) {
+              page = blk * a.hkv + pc.kvh;
+            } else if (blk != kPastEnd && kv == 0) {  // malformed block id: zeros, reported
+              piece_bad[p] = 1;
+              record_status(a.status, pc.b, kBadTree);
+            }
+            tma_load_5d(tile + lane * 2 * Ly::kGroupBytes, kv ? &maps.v_pool : &maps.k_pool, bar,
+                        0, 0, 0, 0, page);
           }
-          tma_load_5d(tile + lane * 2 * Ly::kGroupBytes, kv ? &maps.v_pool : &maps.k_pool, bar,
-                      0, 0, 0, 0, page);
+        } else if (lane < BN / 8) {
+          const int node0 = pc.n0 + (t - pc.P) * BN + lane * 8;
+          tma_load_4d(tile + lane * Ly::kGroupBytes, kv ? &maps.v_nodes : &maps.k_nodes, bar, 0,
+                      node0, 0, pc.kvh);
         }
-      } else if (lane < BN / 8) {
-        const int node0 = w.n0 + (t - w.n_prefix_tiles) * BN + lane * 8;
-        tma_load_4d(tile + lane * Ly::kGroupBytes, kv ? &maps.v_nodes : &maps.k_nodes, bar, 0,
-                    node0, 0, w.kvh);
-      }
-    };
-    // The block-table reads run two K tiles ahead of the K copies (a global
-    // read under load takes about a microsecond), and the ids of every K
-    // tile issued stay in shared memory until its V copy: V(t) is issued
-    // before K(t+8) can be (K(t+8) needs S(t+5), hence the softmax of tile
-    // t+3, which waits for P(t+1).V and so for V(t)).
-    int* blk_ring = reinterpret_cast<int*>(smem + Ly::kBlk);  // [tile & 7][page]
-    int blk_k = fetch_block(0), blk_k2 = fetch_block(1);
-    int tk = 0, tv = 0;
-    bool ok = true;
-    unsigned long long t_idle = 0;
-    while (tv < w.T) {
-      bool progressed = false;
-      if (tk < w.T) {
-        int ready = lane == 0 ? mbar_test_wait(&kempty[tk % kStages], ((tk / kStages) & 1) ^ 1) : 0;
-        if (__shfl_sync(0xffffffffu, ready, 0)) {
-          if (prefix_lane) blk_ring[(tk & 7) * 8 + lane] = blk_k;
-          issue(tk, 0, blk_k);
-          ++tk;
-          blk_k = blk_k2;
-          blk_k2 = fetch_block(tk + 1);
-          progressed = true;
+      };
+      auto advance = [&](int& p, int& t) {
+        if (++t >= pieces[p].t1) {
+          ++p;
+          if (p < npieces) t = pieces[p].t0;
+        }
+      };
+      int kp = 0, kt = pieces[0].t0, vp = 0, vt = pieces[0].t0;
+      int blk_k = fetch_block(kp, kt);  // the block ids of the next K tile, read ahead
+      int tk = g_tile, tv = g_tile;
+      bool ok = true;
+      unsigned long long t_idle = 0;
+      while (vp < npieces) {
+        bool progressed = false;
+        if (kp < npieces) {
+          int ready = lane == 0 ? mbar_test_wait(&kempty[tk % kStages], ((tk / kStages) & 1) ^ 1) : 0;
+          if (__shfl_sync(0xffffffffu, ready, 0)) {
+            if (page_lane) blk_ring[(tk & 7) * 8 + lane] = blk_k;
+            issue(kp, kt, tk, 0, blk_k);
+            ++tk;
+            advance(kp, kt);
+            blk_k = fetch_block(kp, kt);
+            progressed = true;
+          }
+        }
+        if (tv < tk) {
+          int ready = lane == 0 ? mbar_test_wait(&vempty[tv % kStages], ((tv / kStages) & 1) ^ 1) : 0;
+          if (__shfl_sync(0xffffffffu, ready, 0)) {
+            issue(vp, vt, tv, 1, page_lane ? blk_ring[(tv & 7) * 8 + lane] : kPastEnd);
+            ++tv;
+            advance(vp, vt);
+            progressed = true;
+          }
+        }
+        int stop = 0;
+        if (lane == 0) {
+          if (progressed) {
+            t_idle = 0;
+          } else if (t_idle == 0) {
+            t_idle = global_ns();
+          } else if (global_ns() - t_idle > kWaitLimitNs || misc->abort) {
+            stop = 1;
+          }
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) {
+          ok = false;
+          break;
         }
       }
-      if (tv < tk) {
-        int ready = lane == 0 ? mbar_test_wait(&vempty[tv % kStages], ((tv / kStages) & 1) ^ 1) : 0;
-        if (__shfl_sync(0xffffffffu, ready, 0)) {
-          issue(tv, 1, prefix_lane ? blk_ring[(tv & 7) * 8 + lane] : kPastEnd);
-          ++tv;
-          progressed = true;
-        }
-      }
-      int stop = 0;
       if (lane == 0) {
-        if (progressed) {
-          t_idle = 0;
-        } else if (t_idle == 0) {
-          t_idle = global_ns();
-        } else if (global_ns() - t_idle > kWaitLimitNs || misc->abort) {
-          stop = 1;
+        if (!ok) {
+          record_status(a.status, pieces[min(vp, npieces - 1)].b, kDeviceTimeout);
+          misc->abort = 1;
         }
+        // every issued copy has landed before the ring is reused or the CTA
+        // exits (at most kStages of each ring can still be in flight)
+        for (int t = max(g_tile, tk - kStages); t < tk; ++t)
+          mbar_wait(&kfull[t % kStages], (t / kStages) & 1);
+        for (int t = max(g_tile, tv - kStages); t < tv; ++t)
+          mbar_wait(&vfull[t % kStages], (t / kStages) & 1);
       }
-      if (__shfl_sync(0xffffffffu, stop, 0)) {
-        ok = false;
-        break;
-      }
-    }
-    if (lane == 0) {
-      if (!ok) {
-        record_status(a.status, w.b, kDeviceTimeout);
-        misc->abort = 1;
-      }
-      // drain: every issued copy has landed before the CTA may exit (at most
-      // kStages of each ring can still be in flight)
-      for (int t = max(0, tk - kStages); t < tk; ++t)
-        mbar_wait(&kfull[t % kStages], (t / kStages) & 1);
-      for (int t = max(0, tv - kStages); t < tv; ++t)
-        mbar_wait(&vfull[t % kStages], (t / kStages) & 1);
-    }
-  } else if (warp == kMmaWarp || warp == kPvWarp) {
-    // ---------------------------------------------------------- MMA issuers
-    // Two threads issue to the tensor core: S = Q K^T from warp 9 and
-    // O += P V from warp 10.  Issuing a tcgen05.mma stalls its thread while
-    // the tensor pipe is busy, so one thread issuing both would hold P(t).V(t)
-    // back behind S(t+1); with two threads each kind goes out as soon as its
-    // inputs are ready and the pipe interleaves them.
-    if (lane == 0) {
-      bool ok = mbar_wait(q_ready, 0, abort_flag);
-      tc_fence_after();
-      if (warp == kMmaWarp) {
-        constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);  // M=128, N=128
-        // Descriptors are built once; each MMA adds an offset to the
-        // start-address field (16-byte units; shared addresses stay < 2^18).
-        // K (K-major): 8-row groups at kGroupBytes, halves at +1024.
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);  // M=128, N=128, K-major K
+        constexpr uint32_t idesc_o = idesc_bf16(BM, D, 1);   // M=128, N=D, MN-major V
+        // Descriptors are built once; each MMA adds an offset to the start
+        // address field (16-byte units).  K and Q (K-major): 8-row groups at
+        // kGroupBytes, 64-column halves at +1024.  V (MN-major): 8-key groups
+        // at kGroupBytes, column halves at +1024.
         const uint64_t dk0 = smem_desc(smem_u32(smem + Ly::kKRing), 16, Ly::kGroupBytes);
-        for (int t = 0; ok && t < w.T; ++t) {
-          // S(t) = Q K(t)^T into buffer t & 1, once K(t) has landed and the
-          // softmax has read S(t-2) out of that buffer
-          ok = mbar_wait(&kfull[t % kStages], (t / kStages) & 1, abort_flag);
-          if (ok && t >= 2) ok = mbar_wait(&s_free[t & 1], ((t - 2) >> 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
+        const uint64_t dv0 = smem_desc(smem_u32(smem + Ly::kVRing), 1024, Ly::kGroupBytes);
+        const uint64_t dq0 = smem_desc(smem_u32(smem + Ly::kQ), 16, Ly::kGroupBytes);
+        auto issue_s = [&](int h, int t) {  // S_h = Q_h K(t)^T into columns 128 h
           const uint64_t dk = dk0 + static_cast<uint64_t>((t % kStages) * (Ly::kTileBytes >> 4));
-          const uint32_t d = tmem + (t & 1) * BN;
+          const uint64_t dq = dq0 + static_cast<uint64_t>(h * (Ly::kQBytes >> 4));
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            // A = Q from TMEM (16 dims = 8 columns per step), B = K from the ring
-            const uint32_t boff = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
-            mma_bf16_ts(d, tmem_q + kk * 8, dk + boff, idesc_s, kk > 0 ? 1u : 0u);
+            const uint32_t off = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
+            mma_bf16_ss(tmem + h * BN, dq + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&s_full[t & 1]);
-          mma_commit(&kempty[t % kStages]);  // the K slot is free once S(t) is done
-        }
-      } else {
-        constexpr uint32_t idesc_o = idesc_bf16(BM, D, 1);
-        // V (MN-major): 8-key groups at kGroupBytes, column halves at +1024.
-        const uint64_t dv0 = smem_desc(smem_u32(smem + Ly::kVRing), 1024, Ly::kGroupBytes);
-        for (int t = 0; ok && t < w.T; ++t) {
-          // O += P(t) V(t), once P(t) is in TMEM and V(t) has landed
-          ok = mbar_wait(p_full, t & 1, abort_flag);
-          if (ok) ok = mbar_wait(&vfull[t % kStages], (t / kStages) & 1, abort_flag);
+          mma_commit(&s_full[h]);
+        };
+        auto issue_pv = [&](int h, int t, bool acc) {  // O_h (+)= P_h V(t)
+          const uint64_t dv = dv0 + static_cast<uint64_t>((t % kStages) * (Ly::kTileBytes >> 4));
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_bf16_ts(tmem + 256 + h * D, tmem + h * BN + kk * 8,
+                        dv + ((kk * 2 * Ly::kGroupBytes) >> 4), idesc_o, (acc || kk > 0) ? 1u : 0u);
+        };
+        bool ok = true;
+        int tau = g_tile;
+        for (int p = 0; p < npieces && ok; ++p) {
+          const Piece& pc = pieces[p];
+          const int nm = pc.nm, T = pc.t1 - pc.t0;
+          // the piece's first S of each m-tile, once its Q is loaded and K has landed
+          for (int h = 0; h < nm && ok; ++h) {
+            ok = mbar_wait(&q_full[h], (h ? pieces_h1 : pieces_h0) & 1, abort_flag);
+            if (ok && h == 0) ok = mbar_wait(&kfull[tau % kStages], (tau / kStages) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(h, tau);
+          }
           if (!ok) break;
-          tc_fence_after();
-          const int st = t % kStages;
-          const uint64_t dv = dv0 + static_cast<uint64_t>(st * (Ly::kTileBytes >> 4));
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            // A = P from TMEM: 16 keys = 8 columns of bf16 pairs; B = 2 groups of V
-            mma_bf16_ts(tmem_o, tmem_p + kk * 8, dv + ((kk * 2 * Ly::kGroupBytes) >> 4), idesc_o,
-                        (t > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&kempty[tau % kStages]);
+          for (int i = 0; i < T && ok; ++i) {
+            const int t = tau + i;
+            for (int h = 0; h < nm; ++h) {
+              ok = mbar_wait(&p_full[h], (h ? tiles_h1 : tiles_h0) & 1, abort_flag);
+              if (ok && h == 0) ok = mbar_wait(&vfull[t % kStages], (t / kStages) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(h, t, i > 0);
+              if (i + 1 < T) {
+                if (h == 0) {
+                  ok = mbar_wait(&kfull[(t + 1) % kStages], ((t + 1) / kStages) & 1, abort_flag);
+                  if (!ok) break;
+                  tc_fence_after();
+                }
+                issue_s(h, t + 1);
+              }
+              if (h) ++tiles_h1; else ++tiles_h0;
+            }
+            if (!ok) break;
+            mma_commit(&vempty[t % kStages]);
+            if (i + 1 < T) mma_commit(&kempty[(t + 1) % kStages]);
           }
-          mma_commit(&o_done[t & 1]);
-          mma_commit(&vempty[st]);
+          if (!ok) break;
+          mma_commit(&o_done[0]);
+          ++pieces_h0;
+          if (nm == 2) {
+            mma_commit(&o_done[1]);
+            ++pieces_h1;
+          }
+          tau += T;
         }
-      }
-      if (!ok) {
-        record_status(a.status, w.b, kDeviceTimeout);
-        misc->abort = 1;
-      }
-      // drain: all MMAs issued by this thread complete before TMEM is freed
-      uint64_t* dr = &drain[warp == kMmaWarp ? 0 : 1];
-      mma_commit(dr);
-      mbar_wait(dr, 0);
-    }
-    __syncwarp();
-  } else {
-    // ---------------------------------------------------------- softmax warps
-    // Warps 0-7: warp w owns rows 32*(w%4)..+31 (its TMEM lane quarter) in
-    // lane hc = w/4, which takes the tiles t = hc, hc + 2, ...; the two
-    // warps of a scheduler belong to different lanes.  In the prologue and
-    // the epilogue hc selects the half of the Q and O columns a thread moves.
-    const int r = (warp & 3) * 32 + lane;  // row of the tile == TMEM lane
-    const int hc = warp >> 2;              // softmax lane
-    const int sid = hc * 128 + r;          // 0..255
-    const int R = w.mtile * BM + r;
-    const bool live = R < w.rows;
-    float* m_slot = reinterpret_cast<float*>(smem + Ly::kXchg);           // [2][128]
-    float2* fin = reinterpret_cast<float2*>(smem + Ly::kXchg + 2 * BM * 4);  // [2 lanes][128]
-    // Q tile -> TMEM (one row per lane, bf16 pairs; this thread stores the
-    // half hc of its row); padding rows are zero.  The Q loads are issued
-    // before the tree loads so that both latencies overlap.
-    {
-      constexpr int kWords = D / 4;  // 32-bit words per half row
-      uint32_t qw[kWords];
-      if (live) {
-        const int i = R / g, h = w.kvh * g + R % g;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            a.q + (static_cast<size_t>(w.n0 + i) * a.hq + h) * D + hc * (D / 2));
-#pragma unroll
-        for (int c = 0; c < kWords / 4; ++c) {
-          const uint4 v = __ldg(src + c);
-          qw[4 * c] = v.x;
-          qw[4 * c + 1] = v.y;
-          qw[4 * c + 2] = v.z;
-          qw[4 * c + 3] = v.w;
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kWords; ++c) qw[c] = 0u;
-      }
-      // tree of this sequence into shared memory, validated
-      for (int i = sid; i < w.N; i += kSoftmaxThreads) {
-        const int p = __ldg(a.parent + w.n0 + i);
-        par[i] = p;
-        if (!(i == 0 ? p == -1 : (p >= 0 && p < i))) misc->bad = 1;
-      }
-      if constexpr (kWords == 32) {
-        tmem_st32(tmem_q + hc * 32 + lane_off_q(warp), qw);
-      } else {
-        tmem_st16(tmem_q + hc * 16 + lane_off_q(warp), qw);
-      }
-      tmem_st_wait();
-    }
-    tc_fence_before();  // Q is in TMEM before the MMA warp is released
-    mbar_arrive(q_ready);
-    softmax_group_sync();
-    const bool tree_ok = misc->bad == 0;
-    if (!tree_ok && sid == 0) record_status(a.status, w.b, kBadTree);
-    // ancestor-or-self bitmask of the tile's nodes (node tiles only)
-    if (w.last_split && hc == 0) {
-      const int i = node_lo + r;
-      uint32_t* row = anc + r * kAncStride;
-#pragma unroll
-      for (int k = 0; k < kMaxAncWords; ++k) row[k] = 0u;
-      if (tree_ok && i < w.N) {
-        for (int k = i; k >= 0; k = par[k]) row[k >> 5] |= 1u << (k & 31);
-      }
-    }
-    softmax_group_sync();      // ancestor rows are read across threads
-    const int i_node = live ? R / g : 0;  // local node of this row
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t* my_anc = anc + (i_node - node_lo) * kAncStride;
-    // Online softmax over the tiles of this lane.  The running max m(t)
-    // (log2 units) is a chain through all tiles of both lanes: it moves only
-    // when a tile's max exceeds it by more than 2^8, and P(t) is taken
-    // against m(t).  O always holds sum P V against the latest m (a move
-    // rescales it after the previous P.V); each lane keeps its part of the
-    // row sum against the reference of its own last tile.
-    float m_lane = -INFINITY;  // reference of l_run
-    float l_run = 0.0f;
-    bool ok = true;
-    // The warp of the other lane hands over m(t-1) through chain[1-hc][q]:
-    // its k-th completion is tile 2k + (1-hc), and it cannot complete again
-    // before this warp has handed back m(t), so the phase parity of tile t-1
-    // is ((t-1) >> 1) & 1.  After a failed (timed-out) wait a warp keeps
-    // looping and arriving but skips the work.
-    uint64_t* chain_in = &chain[(1 - hc) * 4 + (warp & 3)];
-    uint64_t* chain_out = &chain[hc * 4 + (warp & 3)];
-    for (int t = hc; t < w.T; t += 2) {
-      if (ok) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag));
-        if (!ok) misc->abort = 1;
-      }
-      // this thread's 128 scores of the tile
-      float x[128];
-      if (ok) {
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(tmem + (t & 1) * BN + 32 * c + lane_off,
-                    *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&s_free[t & 1]);  // S(t+2) may overwrite the buffer
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = 0.0f;
-      }
-      // mask (scores stay unscaled; the scale is folded into the exponent)
-      int valid_keys = BN;
-      if (t < w.n_prefix_tiles) {
-        valid_keys = min(BN, w.k_end - (w.k_begin + t * BN));
-        if (valid_keys < BN) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= valid_keys) x[c] = -INFINITY;
-        }
-      } else {
-        const int j0 = (t - w.n_prefix_tiles) * BN;
-        // only ancestors-or-self of this node carry a bit, all of them < N,
-        // so node columns past the tree are masked as well
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t b = live ? my_anc[(j0 >> 5) + k] : 0u;
-#pragma unroll
-          for (int c = 0; c < 32; ++c) x[32 * k + c] = (b & (1u << c)) ? x[32 * k + c] : -INFINITY;
-        }
-      }
-      // max of the 128 scores: eight running three-input maxima over the
-      // columns j, j+8, ..., j+120 (few live temporaries next to x)
-      float mx[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        mx[j] = fmax3(x[j], x[j + 8], x[j + 16]);
-#pragma unroll
-        for (int k = 3; k < 15; k += 2) mx[j] = fmax3(mx[j], x[j + 8 * k], x[j + 8 * k + 8]);
-        mx[j] = fmaxf(mx[j], x[j + 120]);
-      }
-      const float smax =
-          fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
-          a.scale_log2;
-      // the running max after the previous tile (the other lane's)
-      float m_prev = -INFINITY;
-      if (t >= 1) {
-        if (ok) {
-          ok = __all_sync(0xffffffffu, mbar_wait(chain_in, ((t - 1) >> 1) & 1, abort_flag));
-          if (!ok) misc->abort = 1;
-        }
-        m_prev = m_slot[((t - 1) & 1) * BM + r];
-      }
-      float m_new = m_prev, alpha = 1.0f;
-      bool rescale = false;
-      if (smax != -INFINITY) {
-        if (m_prev == -INFINITY) {
-          m_new = smax;
-        } else if (smax > m_prev + kRescaleLog2) {
-          m_new = smax;
-          alpha = exp2f(m_prev - smax);
-          rescale = true;
-        }
-      }
-      m_slot[(t & 1) * BM + r] = m_new;
-      mbar_arrive(chain_out);  // release: m_slot is visible to the waiter
-      if (!ok) continue;  // skip the work, keep the hand-off sequence
-      if (m_lane != m_new) {  // this lane's row sum follows the reference
-        if (l_run > 0.0f) l_run *= exp2f(m_lane - m_new);
-        m_lane = m_new;
-      }
-      const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
-      // P(t) = 2^(s * scale * log2(e) - m) as bf16 pairs (column c holds keys
-      // 2c, 2c+1); masked scores are -inf -> 0
-      uint32_t pk[64];
-      float ls[16];
-#pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        float part = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float p0 = ex2_approx(fmaf(x[c8 * 8 + 2 * k], a.scale_log2, -mref));
-          const float p1 = ex2_approx(fmaf(x[c8 * 8 + 2 * k + 1], a.scale_log2, -mref));
-          pk[c8 * 4 + k] = pack_bf16x2(p0, p1);
-          part += p0 + p1;
-        }
-        ls[c8] = part;
-      }
-      // P(t-1).V is the last reader of the P buffer and the last
-      // accumulation into O
-      if (t >= 1) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag));
         if (!ok) {
+          record_status(a.status, pieces[0].b, kDeviceTimeout);
           misc->abort = 1;
+        }
+        // every MMA issued so far completes before the next round or the exit
+        mma_commit(drain);
+        mbar_wait(drain, round & 1);
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------ softmax groups
+      // Warps 4h .. 4h+3 own m-tile h; warp w's rows are its TMEM lane
+      // quarter 32 (w % 4) .. +31.
+      const int h = warp >> 2;
+      const int r = (warp & 3) * 32 + lane;  // row of the m-tile == TMEM lane
+      const uint32_t lane_off = lane_off_q(warp);
+      const uint32_t tmem_s = tmem + h * BN;
+      const uint32_t tmem_o = tmem + 256 + h * D;
+      uint32_t* anc = reinterpret_cast<uint32_t*>(smem + Ly::kAnc) + (h * BM + r) * kAncStride;
+      int32_t* par = reinterpret_cast<int32_t*>(smem + Ly::kParent) + h * kMaxNodes;
+      uint8_t* qh = smem + Ly::kQ + h * Ly::kQBytes;
+      volatile int* piece_bad = misc->piece_bad;
+      int my_tiles = h ? tiles_h1 : tiles_h0;
+      int my_pieces = h ? pieces_h1 : pieces_h0;
+      bool ok = true;
+      int tau = g_tile;  // global index of the piece's first tile
+      for (int p = 0; p < npieces; ++p) {
+        const Piece pc = pieces[p];
+        const int T = pc.t1 - pc.t0;
+        if (h >= pc.nm) {  // this m-tile has no rows in the unit
+          tau += T;
           continue;
         }
-      }
-      tc_fence_after();
-      if (__any_sync(0xffffffffu, rescale)) {  // O holds P(0..t-1).V against m_prev
+        const int bar_group = kBarGroup0 + h;
+        const int ur = h * BM + r;                 // row of the unit
+        const int R = pc.mp * kUnitRows + ur;      // packed row of the (sequence, KV head)
+        const bool live = ur < pc.rows;
+        const int i_node = live ? R / g : 0;
+        const size_t out_row = static_cast<size_t>(pc.n0 + i_node) * a.hq + pc.kvh * g + R % g;
+        // Q rows -> shared memory in the 128-byte swizzled K-major layout
+        // (the 16-byte chunk c of row r sits at chunk c ^ (r % 8)); rows past
+        // the unit are zero.  The buffer is free: the previous piece's last
+        // S_h completed before its epilogue.
+        {
+          uint8_t* dst = qh + (r >> 3) * Ly::kGroupBytes + (r & 7) * 128;
+          if (live) {
+            const uint16_t* src = a.q + out_row * D;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(tmem_o + c0 + lane_off, o);
+            for (int hf = 0; hf < Ly::kHalves; ++hf)
+#pragma unroll
+              for (int c = 0; c < 8; ++c) cpa16(dst + hf * 1024 + ((c ^ (r & 7)) << 4), src + hf * 64 + c * 8);
+          } else {
+#pragma unroll
+            for (int hf = 0; hf < Ly::kHalves; ++hf)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(dst + hf * 1024 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        // the tree of the sequence (pieces with node tiles): parents, the
+        // check 0 <= parent[i] < i (parent[0] = -1), and this row's
+        // ancestor-or-self bitmask
+        const bool has_nodes = pc.t1 > pc.P;
+        bool tree_bad = false;
+        if (has_nodes) {
+          if (r == 0) misc->tree_bad[h] = 0;
+          named_sync(bar_group, BM);
+          for (int k = r; k < pc.N; k += BM) {
+            const int q = __ldg(a.parent + pc.n0 + k);
+            par[k] = q;
+            if (!(k == 0 ? q == -1 : (q >= 0 && q < k))) misc->tree_bad[h] = 1;
+          }
+          named_sync(bar_group, BM);
+          tree_bad = misc->tree_bad[h] != 0;
+#pragma unroll
+          for (int k = 0; k < kMaxAncWords; ++k) anc[k] = 0u;
+          if (!tree_bad && live)
+            for (int k = i_node; k >= 0; k = par[k]) anc[k >> 5] |= 1u << (k & 31);
+          if (tree_bad && r == 0) record_status(a.status, pc.b, kBadTree);
+          named_sync(bar_group, BM);  // tree_bad is reset by the next piece
+        }
+        cpa_wait_all();
+        fence_proxy_async_smem();  // generic writes of Q, read by the MMA
+        mbar_arrive(&q_full[h]);
+
+        float m_run = -INFINITY;  // running max (log2 units)
+        float l_run = 0.0f;       // row sum against m_run
+        for (int i = 0; i < T; ++i) {
+          const int t = pc.t0 + i;  // tile of the unit
+          const int gt = tau + i;   // global tile (ring slot)
+          if (ok) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[h], my_tiles & 1, abort_flag));
+            if (!ok) misc->abort = 1;
+          }
+          ++my_tiles;
+          if (!ok) {
+            mbar_arrive(&p_full[h]);
+            continue;
+          }
+          float x[128];
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tmem_ld32(tmem_s + 32 * c + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
           tmem_ld_wait();
+          // mask (scores stay unscaled; the scale is folded into the exponent)
+          int valid_keys = BN;
+          if (t < pc.P) {
+            valid_keys = min(BN, pc.L - t * BN);
+            if (valid_keys < BN) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-          tmem_st32(tmem_o + c0 + lane_off, o);
+              for (int c = 0; c < 128; ++c)
+                if (c >= valid_keys) x[c] = -INFINITY;
+            }
+          } else {
+            // only ancestors-or-self of this node carry a bit, all of them
+            // < N, so node columns past the tree are masked as well
+            const int j0 = (t - pc.P) * BN;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t bits = live ? anc[(j0 >> 5) + k] : 0u;
+#pragma unroll
+              for (int c = 0; c < 32; ++c) x[32 * k + c] = (bits & (1u << c)) ? x[32 * k + c] : -INFINITY;
+            }
+          }
+          // max of the 128 scores: eight running three-input maxima
+          float mx[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            mx[j] = fmax3(x[j], x[j + 8], x[j + 16]);
+#pragma unroll
+            for (int k = 3; k < 15; k += 2) mx[j] = fmax3(mx[j], x[j + 8 * k], x[j + 8 * k + 8]);
+            mx[j] = fmaxf(mx[j], x[j + 120]);
+          }
+          const float smax =
+              fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+              a.scale_log2;
+          float alpha = 1.0f;
+          bool rescale = false;
+          if (smax != -INFINITY) {
+            if (m_run == -INFINITY) {
+              m_run = smax;
+            } else if (smax > m_run + kRescaleLog2) {
+              alpha = exp2f(m_run - smax);
+              m_run = smax;
+              rescale = true;
+            }
+          }
+          const float mref = m_run == -INFINITY ? 0.0f : m_run;
+          // P = 2^(s * scale * log2(e) - m) as bf16 pairs (column c holds keys
+          // 2c, 2c+1), written over S_h in four 16-column stores; masked
+          // scores are -inf -> 0.  The row sum adds the rounded values.
+          float lsum = 0.0f;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t pk[16];
+            float part = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float p0 = ex2_approx(fmaf(x[32 * q4 + 2 * k], a.scale_log2, -mref));
+              const float p1 = ex2_approx(fmaf(x[32 * q4 + 2 * k + 1], a.scale_log2, -mref));
+              const uint32_t pp = pack_bf16x2(p0, p1);
+              pk[k] = pp;
+              part += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xFFFF0000u);
+            }
+            tmem_st16(tmem_s + 16 * q4 + lane_off, pk);
+            lsum += part;
+          }
+          if (__any_sync(0xffffffffu, rescale)) {
+            // O holds P(..t-1) V against the old max; P_h(t-1) V is complete
+            // (S_h(t), which this thread has seen complete, was issued after it)
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld32(tmem_o + c0 + lane_off, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st32(tmem_o + c0 + lane_off, o);
+            }
+            l_run *= alpha;  // (this tile's sum is added below, against the new max)
+          }
+          l_run += lsum;
+          // keys past the prefix end in this tile: clear their V rows (page
+          // tails may hold stale data; P is 0 there but 0 * NaN would poison
+          // O).  Group 0 does it before P_0(t) V(t), the tile's first reader.
+          if (h == 0 && valid_keys < BN) {
+            const int st = gt % kStages;
+            mbar_wait(&vfull[st], (gt / kStages) & 1, abort_flag);  // acquire the TMA writes
+            uint8_t* vtile = smem + Ly::kVRing + st * Ly::kTileBytes;
+            for (int idx = r; idx < (BN - valid_keys) * Ly::kHalves; idx += BM) {
+              const int row = valid_keys + idx / Ly::kHalves, hf = idx % Ly::kHalves;
+              uint4* pz = reinterpret_cast<uint4*>(vtile + (row >> 3) * Ly::kGroupBytes + hf * 1024 +
+                                                   (row & 7) * 128);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) pz[k] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();  // generic writes, read by the MMA
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&p_full[h]);
         }
-      }
-      tmem_st32(tmem_p + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tmem_p + 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      float lsum = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) lsum += ls[k];
-      l_run += lsum;
-      // keys past the prefix end in this tile: clear their V rows (page
-      // tails may hold stale data; P is 0 there but 0 * NaN would poison O)
-      if (valid_keys < BN) {
-        const int st = t % kStages;
-        mbar_wait(&vfull[st], (t / kStages) & 1);  // acquire the TMA writes
-        uint8_t* vt = smem + Ly::kVRing + st * Ly::kTileBytes;
-        for (int idx = r; idx < (BN - valid_keys) * Ly::kHalves; idx += BM) {
-          const int row = valid_keys + idx / Ly::kHalves, h = idx % Ly::kHalves;
-          uint4* p = reinterpret_cast<uint4*>(vt + (row >> 3) * Ly::kGroupBytes + h * 1024 +
-                                              (row & 7) * 128);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) p[k] = make_uint4(0, 0, 0, 0);
+        // -------------------------------------------------- piece epilogue
+        bool done = false;
+        if (ok) {
+          done = __all_sync(0xffffffffu, mbar_wait(&o_done[h], my_pieces & 1, abort_flag));
+          if (!done) {
+            ok = false;
+            misc->abort = 1;
+            record_status(a.status, pc.b, kDeviceTimeout);
+          }
         }
-        fence_proxy_async_smem();  // generic writes, read by the MMA
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_full);
-    }
-    // the row sum: both lanes' parts against the final running max
-    fin[hc * BM + r] = make_float2(m_lane, l_run);
-    softmax_group_sync();
-    const float2 f0 = fin[r], f1 = fin[BM + r];
-    const float m_run = fmaxf(f0.x, f1.x);  // the chain only grows: the final max
-    float l_row = 0.0f;
-    if (f0.y > 0.0f) l_row += f0.y * exp2f(f0.x - m_run);
-    if (f1.y > 0.0f) l_row += f1.y * exp2f(f1.x - m_run);
-    if (!ok) {
-      record_status(a.status, w.b, kDeviceTimeout);
-      misc->abort = 1;
-    } else if (w.T > 0 && __all_sync(0xffffffffu, mbar_wait(&o_done[(w.T - 1) & 1],
-                                                            ((w.T - 1) >> 1) & 1, abort_flag))) {
-      tc_fence_after();
-      // ------------------------------------------------------------ epilogue
-      const bool final_out = (w.nsplit == 1);
-      const float inv_l = (l_row > 0.0f) ? 1.0f / l_row : 0.0f;
-      using Pt = Partial<D>;
-      float* part_o = reinterpret_cast<float*>(smem + Ly::kKRing + Pt::kO) + r * Pt::kStride;
+        ++my_pieces;
+        const bool bad = tree_bad || piece_bad[p] != 0;
+        tc_fence_after();
+        if (pc.slot < 0) {
+          // the whole unit: normalise and write
+          const float inv_l = (l_run > 0.0f && !bad) ? 1.0f / l_run : 0.0f;
 #pragma unroll
-      for (int c0 = hc * (D / 2); c0 < (hc + 1) * (D / 2); c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(tmem_o + c0 + lane_off, o);
-        tmem_ld_wait();
-        if (!live) continue;
-        if (final_out) {
-          const int h = w.kvh * g + R % g;
-          uint4* dst = reinterpret_cast<uint4*>(a.out + (static_cast<size_t>(w.n0 + i_node) * a.hq + h) * D + c0);
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
-            dst[k] = v;
+            for (int k = 0; k < 32; ++k) o[k] = 0u;
+            if (done) {
+              tmem_ld32(tmem_o + c0 + lane_off, o);
+              tmem_ld_wait();
+            }
+            float v[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv_l;
+            if (live && done) store_row_chunk<D>(a, out_row, c0, v);
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(part_o + c0);
+          // a piece of a split unit: raw O and (m, l) into the slot; the last
+          // piece of the unit to arrive merges every slot of the unit
+          uint8_t* sl = a.slots + static_cast<size_t>(pc.slot) * Sl::kBytes;
+          float* so = reinterpret_cast<float*>(sl + Sl::kO) + static_cast<size_t>(ur) * D;
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
-                                 __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = 0u;
+            if (done) {
+              tmem_ld32(tmem_o + c0 + lane_off, o);
+              tmem_ld_wait();
+            }
+            if (live) {
+              float4* dst = reinterpret_cast<float4*>(so + c0);
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                     __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+            }
+          }
+          if (live) reinterpret_cast<float2*>(sl + Sl::kMl)[ur] = make_float2(m_run, l_run);
+          if (ur == 0) *reinterpret_cast<int*>(sl + Sl::kFlag) = (bad || !done) ? 1 : 0;
+          __threadfence();
+          const int nthr = pc.nm * BM;
+          const int bar = pc.nm == 2 ? kBarPair : kBarGroup0;
+          named_sync(bar, nthr);
+          if (ur == 0) {
+            const int prev = atomicAdd(a.counters + pc.cnt, 1);
+            misc->merge = prev == pc.npieces - 1;
+          }
+          named_sync(bar, nthr);
+          if (misc->merge) {
+            __threadfence();
+            merge_unit<D>(a, pc, ur, nthr);
+          }
+          named_sync(bar, nthr);  // misc->merge is rewritten by the next split piece
         }
+        tc_fence_before();
+        tau += T;
       }
-      if (live && !final_out && hc == 0)
-        reinterpret_cast<float2*>(smem + Ly::kKRing + Pt::kMl)[r] = make_float2(m_run, l_row);
-    } else if (w.T > 0) {
-      record_status(a.status, w.b, kDeviceTimeout);
-      misc->abort = 1;
+      if (h) {
+        tiles_h1 = my_tiles;
+        pieces_h1 = my_pieces;
+      } else {
+        tiles_h0 = my_tiles;
+        pieces_h0 = my_pieces;
+      }
     }
+    // every role has finished the round's pieces (the TMA copies have
+    // landed, the MMAs are complete)
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    for (int p = 0; p < npieces; ++p) g_tile += pieces[p].t1 - pieces[p].t0;
+    __syncthreads();  // the piece list is rebuilt next round
+    if (!more || misc->abort) break;
   }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (a.max_splits > 1) {
-    // launched as clusters of max_splits CTAs: merge this tile's splits
-    namespace cg = cooperative_groups;
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();  // every split's partial is in its shared memory
-    if (w.nsplit > 1 && !idle && warp < kSoftmaxThreads / 32)
-      merge_rows<D>(a, w, smem + Ly::kKRing, &misc->bad, tid,
-                    static_cast<int>(cluster.block_rank()));
-    cluster.sync();  // no CTA leaves while another may still read its shared memory
-  }
-  // a malformed tree or block id: the only writer of these rows writes zeros
-  // (each row by the thread that wrote it in the epilogue, so zeros win)
-  if (misc->bad && w.nsplit == 1 && warp < 4) zero_rows<D>(a, w, tid);
   if (warp == kMmaWarp) tmem_dealloc(tmem, Ly::kTmemCols);
 }
 
 }  // namespace
 
-size_t tree_attention_smem_bytes(int head_dim) {
-  return head_dim == 64 ? Layout<64>::kAlloc : Layout<128>::kAlloc;
+size_t attn_slot_bytes(int head_dim) {
+  return head_dim == 64 ? Slot<64>::kBytes : Slot<128>::kBytes;
 }
 
 int launch_tree_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream) {
@@ -891,28 +1011,14 @@ int launch_tree_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
                          Layout<64>::kAlloc);
     attr_set_device = dev;
   }
-  if (a.max_splits < 1 || a.max_splits > 8) return -1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.mtiles_max, a.max_splits, a.batch * a.hkv);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.stream = stream;
-  // the splits of one tile (grid y) run as one cluster
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = a.max_splits;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = a.max_splits > 1 ? 1 : 0;
-  cudaError_t e;
+  const int ctas = a.vctas * a.lanes;
+  if (ctas < 1) return -1;
   if (a.head_dim == 128) {
-    cfg.dynamicSmemBytes = Layout<128>::kAlloc;
-    e = cudaLaunchKernelEx(&cfg, tree_attn_kernel<128>, a, maps);
+    tree_attn_kernel<128><<<ctas, kThreads, Layout<128>::kAlloc, stream>>>(a, maps);
   } else {
-    cfg.dynamicSmemBytes = Layout<64>::kAlloc;
-    e = cudaLaunchKernelEx(&cfg, tree_attn_kernel<64>, a, maps);
+    tree_attn_kernel<64><<<ctas, kThreads, Layout<64>::kAlloc, stream>>>(a, maps);
   }
-  return e == cudaSuccess ? 0 : -1;
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace tv

@@ -50,17 +50,27 @@ int sm_count() {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct AttnPlan {
-  int group, mtiles_max, max_splits;
+  int group;        // query heads per KV head
+  int lanes;        // CTAs per virtual CTA (m-tile pairs of one layer)
+  int vctas;        // virtual CTAs
+  int min_tiles;    // fewest key tiles per virtual CTA
+  size_t workspace; // counters + partial-result slots
 };
 
-// Launch plan: 128-row tiles of packed (node, head) rows per (sequence, KV
-// head).  Each sequence's prefix may also be split into up to 8 ranges of
-// whole 128-key tiles (at least 256 keys per split on the longest prefix),
-// the count chosen by the makespan model below; the splits of a tile run as
-// one thread-block cluster and merge through distributed shared memory, so
-// no device workspace is needed.
-bool plan_attention(const tv_attn_params* p, AttnPlan* out) {
-  if (!p) return false;
+// Fewest 128-key tiles a virtual CTA is given: below this a unit is not split
+// further, since a split piece costs about this much in fixed work (its Q
+// load, the pipeline fill and its partial-result write).
+constexpr int kMinTiles = 4;
+
+// Launch plan for `sms` SMs (one persistent CTA per SM).  A layer of `lanes`
+// CTAs takes the m-tile pairs (256 packed rows) of a (sequence, KV head): as
+// many lanes as the largest tree has pairs, so that the CTAs reading the
+// same K/V tiles run together.  The virtual CTAs (sms / lanes of them, fewer
+// when the host hints bound the work below kMinTiles tiles each) share the
+// line of key tiles equally on the device.  Workspace: one arrival counter
+// per CTA, then two partial-result slots per CTA.
+bool plan_attention(const tv_attn_params* p, int sms, AttnPlan* out) {
+  if (!p || sms < 1) return false;
   if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1) return false;
   if (p->num_q_heads % p->num_kv_heads) return false;
   if (p->head_dim != 64 && p->head_dim != 128) return false;
@@ -69,32 +79,20 @@ bool plan_attention(const tv_attn_params* p, AttnPlan* out) {
   if (p->total_nodes < p->batch || p->num_blocks < 1 || p->max_blocks_per_seq < 1) return false;
   if (p->max_prefix_len < 0) return false;
   if ((p->max_prefix_len + 15) / 16 > p->max_blocks_per_seq) return false;
+  if (p->out_dtype != TV_OUT_BF16 && p->out_dtype != TV_OUT_FP32) return false;
   if (static_cast<int64_t>(p->num_blocks) * p->num_kv_heads * 16 >= (1ll << 31)) return false;
-  if (static_cast<int64_t>(p->total_nodes) >= (1ll << 31) / 2) return false;
+  if (static_cast<int64_t>(p->total_nodes) * p->num_q_heads >= (1ll << 31)) return false;
   AttnPlan pl;
   pl.group = p->num_q_heads / p->num_kv_heads;
-  pl.mtiles_max = (p->max_nodes * pl.group + 127) / 128;
-  // Split count S from a makespan model in units of one 128-key tile (about
-  // a microsecond): a CTA costs kFixed tiles of prologue and epilogue, its
-  // share ceil(P / S) of the P prefix tiles, the Nt node tiles (last split)
-  // and kMerge more when S > 1; CTAs run one per SM, so the launch takes
-  // ceil(base * S / SMs) waves.  P, Nt and base are upper bounds from the
-  // host hints (longest prefix, most nodes); ties go to the larger S.
-  constexpr long kFixed = 5, kMerge = 4;
-  const long base = static_cast<long>(p->batch) * p->num_kv_heads * pl.mtiles_max;
-  const long P = (p->max_prefix_len + 127) / 128, Nt = (p->max_nodes + 127) / 128;
-  const long sms = sm_count();
-  const long s_cap = std::min(8l, std::max(1l, static_cast<long>(p->max_prefix_len) / 256));
-  long splits = 1, best = -1;
-  for (long S = 1; S <= s_cap; ++S) {
-    const long waves = (base * S + sms - 1) / sms;
-    const long cost = waves * (kFixed + (P + S - 1) / S + Nt + (S > 1 ? kMerge : 0));
-    if (best < 0 || cost <= best) {
-      best = cost;
-      splits = S;
-    }
-  }
-  pl.max_splits = static_cast<int>(splits);
+  const long long mpairs = (static_cast<long long>(p->max_nodes) * pl.group + 255) / 256;
+  pl.lanes = static_cast<int>(std::min<long long>(mpairs, sms));
+  const long long layers = (mpairs + pl.lanes - 1) / pl.lanes;
+  const long long tiles = (p->max_prefix_len + 127) / 128 + (p->max_nodes + 127) / 128;
+  const long long wmax = static_cast<long long>(p->batch) * p->num_kv_heads * layers * tiles;
+  pl.min_tiles = kMinTiles;
+  pl.vctas = static_cast<int>(std::max(1ll, std::min<long long>(sms / pl.lanes, wmax / kMinTiles)));
+  const size_t ctas = static_cast<size_t>(pl.vctas) * pl.lanes;
+  pl.workspace = (ctas * 4 + 255) / 256 * 256 + 2 * ctas * tv::attn_slot_bytes(p->head_dim);
   *out = pl;
   return true;
 }
@@ -158,33 +156,40 @@ int tv_selftest_wait_timeout(int32_t* status, unsigned long long* waited_ns,
 }
 
 size_t tv_tree_attention_workspace_size(const tv_attn_params* p) {
-  (void)p;  // split partials are merged through distributed shared memory
-  return 0;
+  AttnPlan pl;
+  if (!plan_attention(p, sm_count(), &pl)) return 0;
+  return pl.workspace;
 }
 
-int tv_tree_attention_splits(const tv_attn_params* p) {
+int tv_tree_attention_plan(const tv_attn_params* p, int32_t sms, tv_attn_plan* out) {
+  if (!out) return TV_ERR_INVALID_ARG;
   AttnPlan pl;
-  if (!plan_attention(p, &pl)) return -1;
-  return pl.max_splits;
+  if (!plan_attention(p, sms > 0 ? sms : sm_count(), &pl)) return TV_ERR_INVALID_ARG;
+  out->ctas = pl.vctas * pl.lanes;
+  out->lanes = pl.lanes;
+  out->virtual_ctas = pl.vctas;
+  out->min_tiles = pl.min_tiles;
+  out->workspace_bytes = pl.workspace;
+  return TV_OK;
 }
 
 int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
                       const uint16_t* k_prefix_blocks, const uint16_t* v_prefix_blocks,
                       const int32_t* block_table, const uint16_t* k_nodes,
                       const uint16_t* v_nodes, const int32_t* parent,
-                      const int32_t* prefix_lens, const int32_t* node_offsets, uint16_t* out,
+                      const int32_t* prefix_lens, const int32_t* node_offsets, void* out,
                       int32_t* status, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream) {
   if (!p) return TV_ERR_INVALID_ARG;
   if (p->head_dim != 64 && p->head_dim != 128) return TV_ERR_UNSUPPORTED;
   AttnPlan pl;
-  if (!plan_attention(p, &pl)) return TV_ERR_INVALID_ARG;
+  if (!plan_attention(p, sm_count(), &pl)) return TV_ERR_INVALID_ARG;
   const void* ptrs[] = {q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nodes,
                         v_nodes, parent, prefix_lens, node_offsets, out, status};
   for (const void* q : ptrs)
     if (!q || !aligned16(q)) return TV_ERR_INVALID_ARG;
-  (void)workspace;  // the split merge happens on chip: no workspace is used
-  (void)workspace_bytes;
+  if (!workspace || workspace_bytes < pl.workspace || !aligned16(workspace))
+    return TV_ERR_WORKSPACE;
 
   const int D = p->head_dim, Hkv = p->num_kv_heads;
   tv::AttnMaps maps;
@@ -215,6 +220,7 @@ int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
     if (!encode(&maps.v_nodes, v_nodes, 4, dims, str, box)) return TV_ERR_CUDA;
   }
 
+  const size_t ctas = static_cast<size_t>(pl.vctas) * pl.lanes;
   tv::AttnArgs a;
   a.q = q_nodes;
   a.block_table = block_table;
@@ -223,6 +229,8 @@ int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
   a.node_offsets = node_offsets;
   a.out = out;
   a.status = status;
+  a.counters = static_cast<int32_t*>(workspace);
+  a.slots = static_cast<uint8_t*>(workspace) + (ctas * 4 + 255) / 256 * 256;
   a.batch = p->batch;
   a.hq = p->num_q_heads;
   a.hkv = Hkv;
@@ -233,13 +241,17 @@ int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
   a.max_nodes = p->max_nodes;
   a.max_prefix_len = p->max_prefix_len;
   a.total_nodes = p->total_nodes;
-  a.mtiles_max = pl.mtiles_max;
-  a.max_splits = pl.max_splits;
+  a.lanes = pl.lanes;
+  a.vctas = pl.vctas;
+  a.min_tiles = pl.min_tiles;
+  a.out_fp32 = p->out_dtype == TV_OUT_FP32 ? 1 : 0;
   const float scale = p->softmax_scale > 0.0f ? p->softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
   a.scale_log2 = scale * 1.4426950408889634f;
 
+  // status and the arrival counters of split units start at zero
   if (cudaMemsetAsync(status, 0, sizeof(int32_t) * p->batch, stream) != cudaSuccess)
     return TV_ERR_CUDA;
+  if (cudaMemsetAsync(a.counters, 0, ctas * 4, stream) != cudaSuccess) return TV_ERR_CUDA;
   if (tv::launch_tree_attention(a, maps, stream) != 0) return TV_ERR_CUDA;
   return TV_OK;
 }

@@ -60,12 +60,16 @@ struct AttnArgs {
   const int32_t* parent;      // [total_nodes]
   const int32_t* prefix_lens; // [batch]
   const int32_t* node_offsets;// [batch+1]
-  uint16_t* out;              // [total_nodes][Hq][D]
+  void* out;                  // [total_nodes][Hq][D], bf16 or fp32 (out_fp32)
   int32_t* status;            // [batch]
+  int32_t* counters;          // [ctas] arrival counters of split units (zeroed per call)
+  uint8_t* slots;             // [2 * ctas] partial-result slots of attn_slot_bytes(D)
   int32_t batch, hq, hkv, group, head_dim;
   int32_t max_blocks_per_seq, num_blocks, max_nodes, max_prefix_len, total_nodes;
-  int32_t mtiles_max;         // ceil(max_nodes * group / 128)
-  int32_t max_splits;         // CTAs per cluster (grid y): prefix splits per tile, <= 8
+  int32_t lanes;              // CTAs per virtual CTA: one per m-tile pair of a layer
+  int32_t vctas;              // virtual CTAs launched (ctas = vctas * lanes)
+  int32_t min_tiles;          // fewest key tiles a virtual CTA is given
+  int32_t out_fp32;           // 1: fp32 output, 0: bf16
   float scale_log2;           // softmax scale * log2(e)
 };
 
@@ -77,6 +81,8 @@ struct AttnMaps {
 };
 
 int launch_tree_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream);
+// Bytes of one partial-result slot: 256 rows of fp32 O, (m, l) per row, a flag.
+size_t attn_slot_bytes(int head_dim);
 
 struct CommitArgs {
   const uint16_t* k_nodes;    // [total_nodes][Hkv][D]
@@ -95,6 +101,5 @@ struct CommitArgs {
 };
 
 int launch_commit(const CommitArgs& a, cudaStream_t stream);
-size_t tree_attention_smem_bytes(int head_dim);
 
 }  // namespace tv

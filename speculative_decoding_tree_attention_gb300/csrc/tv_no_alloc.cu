@@ -54,13 +54,14 @@ extern "C" int tv_tree_attention_no_alloc(const tv_attn_params* params, const ui
                                           const int32_t* block_table, const uint16_t* k_nodes,
                                           const uint16_t* v_nodes, const int32_t* parent,
                                           const int32_t* prefix_lens,
-                                          const int32_t* node_offsets, uint16_t* out,
+                                          const int32_t* node_offsets, void* out,
                                           int32_t* status, cudaStream_t stream) {
   if (!params) return TV_ERR_INVALID_ARG;
   const size_t need = tv_tree_attention_workspace_size(params);
   if (need > static_cast<size_t>(TV_NO_ALLOC_SCRATCH_BYTES)) return TV_ERR_WORKSPACE;
-  // The partial results are fully written by the attention kernel before the
-  // merge reads them, so nothing in the array has to start at zero.
+  // The arrival counters at the start of the array must be zero: the call
+  // below clears them on the stream before its kernel runs.  The partial
+  // results are written by the kernel before any merge reads them.
   void* scratch = nullptr;
   if (need > 0) {
     const int rc = scratch_address(&scratch);

@@ -48,14 +48,15 @@ def test_version_and_status_strings(lib):
 def _params(**kw):
     base = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
                 max_blocks_per_seq=8, num_blocks=16, max_nodes=64, total_nodes=100,
-                max_prefix_len=128, softmax_scale=0.0)
+                max_prefix_len=128, softmax_scale=0.0, out_dtype=0)
     base.update(kw)
     return tv.AttnParams(**base)
 
 
 @pytest.mark.parametrize("bad", [dict(head_dim=96), dict(num_q_heads=7), dict(block_size=32),
                                  dict(max_nodes=513), dict(max_nodes=0), dict(batch=0),
-                                 dict(max_prefix_len=1000), dict(total_nodes=1)])
+                                 dict(max_prefix_len=1000), dict(total_nodes=1),
+                                 dict(out_dtype=2)])
 def test_attention_argument_errors_before_launch(lib, bad):
     p = _params(**bad)
     dummy = C.c_void_p(4096)  # never dereferenced: the call fails on the host
@@ -74,13 +75,27 @@ def test_attention_null_pointer_rejected(lib):
     assert lib.tv_tree_attention(C.byref(p), *args, None, C.c_size_t(0), None) == tv.TV_ERR_INVALID_ARG
 
 
-def test_attention_needs_no_workspace(lib):
+def test_attention_workspace_size_rules(lib):
     assert lib.tv_tree_attention_workspace_size(C.byref(_params(head_dim=96))) == 0
-    # a long prefix on few (sequence, head) pairs is split over a cluster and
-    # merged on chip: still no device workspace
-    p = _params(batch=1, num_kv_heads=1, num_q_heads=1, max_prefix_len=32768,
-                max_blocks_per_seq=2048, num_blocks=2048, max_nodes=16, total_nodes=16)
-    assert lib.tv_tree_attention_workspace_size(C.byref(p)) == 0
+    assert lib.tv_tree_attention_workspace_size(C.byref(_params(out_dtype=2))) == 0
+    # one counter per CTA (rounded to 256 bytes), then two slots per CTA of
+    # 256 rows x D fp32, 256 (m, l) pairs and a 256-byte flag area
+    for d in (64, 128):
+        plan = tv.attention_plan(_params(head_dim=d), sms=152)
+        ctas = plan["ctas"]
+        slot = 256 * d * 4 + 256 * 8 + 256
+        assert plan["workspace_bytes"] == (ctas * 4 + 255) // 256 * 256 + 2 * ctas * slot
+
+
+def test_attention_refuses_a_short_workspace(lib):
+    p = _params()
+    dummy = C.c_void_p(4096)
+    need = lib.tv_tree_attention_workspace_size(C.byref(p))
+    assert need > 0
+    assert lib.tv_tree_attention(C.byref(p), *([dummy] * 11), None, C.c_size_t(0), None) == \
+        tv.TV_ERR_WORKSPACE
+    assert lib.tv_tree_attention(C.byref(p), *([dummy] * 11), dummy, C.c_size_t(need - 16),
+                                 None) == tv.TV_ERR_WORKSPACE
 
 
 @pytest.mark.parametrize("bad", [dict(vocab=0), dict(vocab=1 << 18), dict(max_nodes=600),
@@ -174,21 +189,37 @@ def test_selftest_wait_timeout_checks_arguments(lib, limit_ns):
 def _plan(batch, hq, hkv, d, max_nodes, max_prefix):
     blocks = (max_prefix + 15) // 16
     return tv.AttnParams(batch, hq, hkv, d, 16, max(1, blocks), max(1, batch * blocks), max_nodes,
-                         batch * max_nodes, max_prefix, 0.0)
+                         batch * max_nodes, max_prefix, 0.0, 0)
 
 
-@pytest.mark.parametrize("shape, splits", [
-    ((1, 4, 4, 64, 15, 128), 1),          # tiny
-    ((1, 32, 32, 128, 64, 1024), 4),      # 7B-like: 32 tiles, latency-bound: split
-    ((16, 32, 8, 128, 64, 3959), 1),      # serving: 256 tiles, two waves already
-    ((4, 28, 4, 128, 128, 1600), 1),      # multimodal: 112 tiles, one wave unsplit
-    ((4, 64, 8, 128, 256, 32768), 2),     # long: 512 tiles; two splits fill the waves
-    ((1, 64, 8, 128, 256, 32768), 1),     # long, one sequence: 128 tiles, one wave
+# (lanes, virtual CTAs) on 152 SMs: lanes = m-tile pairs of the largest tree
+# (256 packed rows each), virtual CTAs = 152 // lanes, fewer when the line of
+# key tiles (batch x Hkv x layers x (prefix tiles + node tiles)) gives fewer
+# than 4 tiles each
+@pytest.mark.parametrize("shape, lanes, vctas", [
+    ((1, 4, 4, 64, 15, 128), 1, 2),          # tiny: 4 heads x 2 tiles = 8 tiles
+    ((1, 32, 32, 128, 64, 1024), 1, 72),     # 7B-like: 32 x 9 = 288 tiles
+    ((16, 32, 8, 128, 64, 3959), 1, 152),    # serving: 16 x 8 x 32 tiles
+    ((4, 28, 4, 128, 128, 1600), 4, 38),     # multimodal: 896 rows = 4 pairs, 224 tiles
+    ((4, 64, 8, 128, 256, 32768), 8, 19),    # long: 2048 rows = 8 pairs, 8256 tiles
+    ((1, 64, 8, 128, 256, 32768), 8, 19),    # long, one sequence
 ])
-def test_split_count_model(lib, shape, splits):
-    assert tv.attention_splits(_plan(*shape)) == splits
+def test_launch_plan(lib, shape, lanes, vctas):
+    plan = tv.attention_plan(_plan(*shape), sms=152)
+    assert (plan["lanes"], plan["virtual_ctas"]) == (lanes, vctas)
+    assert plan["ctas"] == lanes * vctas <= 152 and plan["min_tiles"] == 4
+    # the fixed scratch array of the no-allocation entry point holds every plan
+    assert plan["workspace_bytes"] <= 64 << 20
 
 
-def test_split_count_rejects_invalid_params(lib):
-    assert tv.attention_splits(_plan(1, 6, 4, 128, 64, 1024)) == -1   # Hq % Hkv != 0
-    assert tv.attention_splits(_plan(1, 4, 4, 96, 64, 1024)) == -1    # head size
+def test_launch_plan_scales_with_the_sm_count(lib):
+    p = _plan(16, 32, 8, 128, 64, 3959)
+    for sms in (1, 76, 148, 160):
+        plan = tv.attention_plan(p, sms=sms)
+        assert plan["ctas"] == sms
+
+
+def test_launch_plan_rejects_invalid_params(lib):
+    for p in (_plan(1, 6, 4, 128, 64, 1024), _plan(1, 4, 4, 96, 64, 1024)):
+        with pytest.raises(tv.TVError):
+            tv.attention_plan(p, sms=152)

@@ -1,11 +1,13 @@
 """GPU parity of tv_tree_attention (through the C ABI) against the fp64 oracle.
 
-Tolerance (bf16 inputs, fp32 accumulation), asserted on every comparison by
-tv_testlib.assert_attention_close: max-abs error <= 1e-2 over all elements,
-|g - r| <= 1e-2 + 2e-2*|r| element by element, and every output row (one
-node, one head) within 2e-2 of its largest magnitude.  The element-wise
-relative error over elements with |r| >= 1e-2 is reported
-($TV_PARITY_LOG), not asserted (P is rounded to bf16 before P.V).
+Tolerance (bf16 inputs, fp32 accumulation), asserted on the fp32 output of
+every comparison by tv_testlib.assert_attention_close: max-abs error <= 1e-2
+over all elements, |g - r| <= 1e-2 + 2e-2*|r| element by element, and every
+output row (one node, one head) within 2e-2 of its largest magnitude.  The
+element-wise relative error over elements with |r| >= 1e-2 is reported
+($TV_PARITY_LOG), not asserted (P is rounded to bf16 before P.V).  The bf16
+output of the same inputs must be the fp32 output rounded to nearest even,
+bit for bit.
 
 Full sizes: every element of the 7B-like, serving and multimodal workloads;
 on the long-context workload every row of one KV head of one sequence (all
@@ -16,7 +18,8 @@ import pytest
 
 import oracle
 from speculative_decoding_tree_attention_gb300 import workloads as wl
-from tv_testlib import (assert_attention_close, gather_rows, run_attention, sample_rows)
+from tv_testlib import (assert_attention_close, assert_bf16_is_rounded_fp32, gather_rows,
+                        run_attention, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +28,9 @@ def full_compare(case, what, **kw):
     gpu, status = run_attention(case, **kw)
     assert np.all(status == 0), status
     ref = oracle.tree_attention(case)
-    return assert_attention_close(gpu, ref, what)
+    res = assert_attention_close(gpu, ref, what)
+    assert np.all(assert_bf16_is_rounded_fp32(case, gpu, what, **kw) == 0)
+    return res
 
 
 # ---------------------------------------------------------------- small shapes
@@ -109,6 +114,15 @@ def test_batch_at_and_past_the_ordering_limit(batch):
     full_compare(case, f"batch {batch}")
 
 
+def test_many_tiny_sequences_take_several_scheduling_rounds():
+    """2048 sequences of 1..3 nodes without a prefix on 4 KV heads: each CTA
+    gets more pieces than one scheduling round holds (32), so it rebuilds its
+    piece list several times."""
+    cfg = wl.config(3, batch=2048, hq=4, hkv=4, d=64, prefix=(0, 0), n=(1, 3))
+    case = wl.make_case(cfg, parts=("attn",))
+    full_compare(case, "2048 tiny sequences")
+
+
 def test_max_nodes_512_chain():
     cfg = wl.config(2, batch=1, hq=2, hkv=2, d=64, prefix=(40, 40))
     cfg["parent"] = [[-1] + list(range(511))]
@@ -127,11 +141,14 @@ def test_bad_tree_and_bad_block_report_status_and_zero_output():
     gpu, status = run_attention(case)
     assert list(status) == [0, 5, 5]
     assert np.all(gpu[off[1]:off[3]] == 0)
+    assert list(assert_bf16_is_rounded_fp32(case, gpu, "bad tree")) == [0, 5, 5]
     ref = oracle.tree_attention_rows(case, [(0, i, h) for i in range(4) for h in range(4)])
     assert_attention_close(gpu[off[0]:off[1]].reshape(-1, case["head_dim"]), ref, "good sequence")
 
 
 def test_repeatable_bitwise():
+    """Split units merge their pieces in a fixed order: repeated calls agree
+    bit for bit (here every unit is split over several CTAs)."""
     case = wl.make_case(wl.config(3, batch=3, hq=8, hkv=2, prefix=(100, 900)), parts=("attn",))
     a, _ = run_attention(case)
     b, _ = run_attention(case)
@@ -156,6 +173,8 @@ def test_malformed_sequences_with_prefix_splits_are_zeroed():
         case["block_table"] = np.concatenate([case["block_table"], extra], 1)
     gpu, status = run_attention(case, max_prefix_len=2048)
     assert list(status) == [0, 5, 5, 5, 0], status
+    assert list(assert_bf16_is_rounded_fp32(case, gpu, "malformed", max_prefix_len=2048)) == \
+        [0, 5, 5, 5, 0]
     for b in (1, 2, 3):
         assert np.all(gpu[off[b]:off[b + 1]] == 0), b
     rows = [(b, i, h) for b in (0, 4) for i in range(off[b + 1] - off[b]) for h in range(8)]
@@ -172,6 +191,7 @@ def test_full_size_config_every_element(num):
     assert np.all(status == 0)
     ref = oracle.tree_attention(case)
     assert_attention_close(gpu, ref, f"config {num} every element")
+    assert np.all(assert_bf16_is_rounded_fp32(case, gpu, f"config {num}") == 0)
 
 
 def test_long_context_one_kv_head_every_row_plus_sample():

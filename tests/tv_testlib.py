@@ -8,15 +8,22 @@ from speculative_decoding_tree_attention_gb300 import _build
 from speculative_decoding_tree_attention_gb300 import workloads as wl
 
 # Tolerance for bf16 inputs with fp32 accumulation, as stated for this path:
-# max-abs error 1e-2 and max-rel error 2e-2.  Asserted on every comparison:
+# max-abs error 1e-2 and max-rel error 2e-2.  Asserted on the kernel's fp32
+# output (the arithmetic itself):
 #   * max |g - r| <= ATOL over all elements (the max-abs bound);
 #   * |g - r| <= ATOL + RTOL*|r| element by element (allclose);
 #   * per output row (one node, one head): max |g - r| / max |r| <= RTOL.
-# The element-wise relative error over elements with |r| >= 1e-2 is computed
-# and reported (attention_report) but not asserted against RTOL: rounding P to
-# bf16 before the P.V product moves an element that is a small difference of
-# large terms by up to about 2^-9 of those terms, which is more than 2 % of an
-# element near 1e-2 even when the row is accurate to a fraction of a percent.
+# The element-wise relative error over elements with |r| >= REL_FLOOR is
+# computed and reported (attention_report, $TV_PARITY_LOG) but not asserted
+# against RTOL: rounding P to bf16 before the P.V product moves an element
+# that is a small difference of large terms by up to about 2^-9 of those
+# terms, more than 2 % of an element near 1e-2 even when its row is accurate
+# to a fraction of a percent.
+# The bf16 output is checked to be the fp32 output rounded once to nearest
+# even, bit for bit (assert_bf16_is_rounded_fp32); its error is therefore the
+# fp32 error plus at most half a bf16 ulp, and no bf16 output can do better:
+# on the multimodal workload the exact result alone, rounded to bf16, is off
+# by up to 0.0156 (outputs reach 5.5).
 ATOL, RTOL = 1e-2, 2e-2
 REL_FLOOR = 1e-2   # elements at least this large enter the element-wise max-rel
 
@@ -42,7 +49,8 @@ def attn_device(case, dev="cuda"):
         lens=_i32(case["prefix_lens"], dev), off=_i32(case["node_offsets"], dev))
 
 
-def run_attention(case, dev="cuda", max_prefix_len=None, max_nodes=None):
+def run_attention(case, dev="cuda", max_prefix_len=None, max_nodes=None, out_dtype="fp32"):
+    """tv_tree_attention on the case; returns (output as float32 numpy, status)."""
     ensure_built()
     t = attn_device(case, dev)
     mpl = int(max_prefix_len if max_prefix_len is not None else max(1, int(np.max(case["prefix_lens"]))))
@@ -50,9 +58,21 @@ def run_attention(case, dev="cuda", max_prefix_len=None, max_nodes=None):
     out, status = tv.tree_attention(t["q"], t["kp"], t["vp"], t["table"], t["kn"], t["vn"],
                                     t["parent"], t["lens"], t["off"], max_nodes=mn,
                                     max_prefix_len=mpl,
-                                    softmax_scale=float(case.get("softmax_scale") or 0.0))
+                                    softmax_scale=float(case.get("softmax_scale") or 0.0),
+                                    out_dtype=out_dtype)
     torch.cuda.synchronize()
     return out.float().cpu().numpy(), status.cpu().numpy()
+
+
+def assert_bf16_is_rounded_fp32(case, gpu32, what="", **kw):
+    """The bf16 output of the same call equals the fp32 output rounded to
+    nearest even, element for element (status equal too)."""
+    g16, st16 = run_attention(case, out_dtype="bf16", **kw)
+    want = wl.to_bf16_bits(gpu32)
+    got = wl.to_bf16_bits(g16)
+    bad = np.count_nonzero(want != got)
+    assert bad == 0, f"{what}: {bad} bf16 outputs differ from the rounded fp32 outputs"
+    return st16
 
 
 def attention_errors(gpu, ref):
