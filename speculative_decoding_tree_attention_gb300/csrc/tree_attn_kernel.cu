@@ -443,7 +443,7 @@ __device__ void merge_unit(const AttnArgs& a, const Piece& pc, int sid, int nthr
 
 // ---------------------------------------------------------------- the kernel
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     tree_attn_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps) {
   using Ly = Layout<D>;
   using Sl = Slot<D>;
@@ -1013,12 +1013,19 @@ int launch_tree_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
   }
   const int ctas = a.vctas * a.lanes;
   if (ctas < 1) return -1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  cudaError_t e;
   if (a.head_dim == 128) {
-    tree_attn_kernel<128><<<ctas, kThreads, Layout<128>::kAlloc, stream>>>(a, maps);
+    cfg.dynamicSmemBytes = Layout<128>::kAlloc;
+    e = cudaLaunchKernelEx(&cfg, tree_attn_kernel<128>, a, maps);
   } else {
-    tree_attn_kernel<64><<<ctas, kThreads, Layout<64>::kAlloc, stream>>>(a, maps);
+    cfg.dynamicSmemBytes = Layout<64>::kAlloc;
+    e = cudaLaunchKernelEx(&cfg, tree_attn_kernel<64>, a, maps);
   }
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  return e == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace tv
