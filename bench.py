@@ -14,9 +14,9 @@ verified per second, all ranks) with inputs resident in HBM; L2 is flushed
 between timed steps (a 512 MiB write, outside the timed events).  Under
 torchrun each rank runs an independent replica (no collective on the data
 path: sequences are independent), timing is max over ranks.
-The headline is the 32K long-context workload (config 5); the serving and
-7B-like workloads (configs 3 and 2) are timed in the same run and reported
-under "workloads", each call on its own.
+The headline is the 32K long-context workload (config 5); the multimodal,
+serving and 7B-like workloads (configs 4, 3 and 2) are timed in the same run
+and reported under "workloads", each call on its own.
 `--impl reference` times the fp64 CPU oracle on the host cores instead.
 """
 from __future__ import annotations
@@ -448,7 +448,7 @@ def main():
     cfg = wl.config(args.config, **({"batch": args.batch} if args.batch > 0 else {}))
     case = wl.make_case(cfg, parts=("attn", "accept"), kind=args.mode)
     # the other HBM-bound workloads, reported beside the headline (rank 0)
-    side_nums = [n for n in (3, 2) if n != cfg["num"]] if (rank == 0 and args.side) else []
+    side_nums = [n for n in (4, 3, 2) if n != cfg["num"]] if (rank == 0 and args.side) else []
     side_cases = {n: wl.make_case(wl.config(n), parts=("attn", "accept"), kind=args.mode)
                   for n in side_nums}
     step = Step(tv, case, cfg, args.mode, dev)

@@ -377,65 +377,98 @@ __device__ __forceinline__ int piece_slot(const AttnArgs& a, const Piece& pc, in
 }
 
 // Merges the pieces of a split unit: O = sum_s 2^(m_s - M) O_s /
-// sum_s 2^(m_s - M) l_s over the slots in piece order.  `nthreads` threads
-// (thread sid) take the rows, a warp per row, the lanes D/32 columns each.
+// sum_s 2^(m_s - M) l_s over the slots in piece order.  Warp w of the
+// `nthreads` participants owns rows 32 w .. 32 w + 31 of the unit: first each
+// lane takes one row's (m, l) over every piece (M and the sum, online), then
+// the warp streams the O rows, four rows at a time with every piece's loads
+// in flight, the lanes D/32 columns each.
 template <int D>
-__device__ void merge_unit(const AttnArgs& a, const Piece& pc, int sid, int nthreads) {
+__device__ void merge_unit(const AttnArgs& a, const Piece& pc, int sid) {
   using Sl = Slot<D>;
   constexpr int kCols = D / 32;  // columns per lane
-  const int lane = sid & 31, w = sid >> 5, nw = nthreads >> 5;
+  constexpr int kRows = 4;       // rows in flight per warp
+  const int lane = sid & 31;
+  const int row0 = (sid >> 5) * 32;
+  if (row0 >= pc.rows) return;
+  const int my_row = row0 + lane;
   bool bad = false;
-  for (int s = 0; s < pc.npieces; ++s)
-    bad |= __ldcg(reinterpret_cast<const int*>(a.slots + piece_slot(a, pc, s) * Sl::kBytes +
-                                               Sl::kFlag)) != 0;
+  float M = -INFINITY, l = 0.0f;
+  for (int s = 0; s < pc.npieces; ++s) {
+    const uint8_t* base = a.slots + static_cast<size_t>(piece_slot(a, pc, s)) * Sl::kBytes;
+    bad |= __ldcg(reinterpret_cast<const int*>(base + Sl::kFlag)) != 0;
+    if (my_row < pc.rows) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + my_row);
+      if (ml.x > M) {
+        l = (M == -INFINITY ? 0.0f : l * exp2f(M - ml.x)) + ml.y;
+        M = ml.x;
+      } else if (ml.x != -INFINITY) {
+        l += ml.y * exp2f(ml.x - M);
+      }
+    }
+  }
+  const float inv = (l > 0.0f && !bad) ? 1.0f / l : 0.0f;
   const int g = a.group;
-  for (int ur = w; ur < pc.rows; ur += nw) {
-    float M = -INFINITY;
-    for (int s = 0; s < pc.npieces; ++s) {
-      const float2 ml = __ldcg(
-          reinterpret_cast<const float2*>(a.slots + piece_slot(a, pc, s) * Sl::kBytes + Sl::kMl) + ur);
-      M = fmaxf(M, ml.x);
-    }
-    const float mref = M == -INFINITY ? 0.0f : M;
-    float acc[kCols];
+  for (int r0 = 0; r0 < 32 && row0 + r0 < pc.rows; r0 += kRows) {
+    float acc[kRows][kCols];
+    float mr[kRows], ir[kRows];
 #pragma unroll
-    for (int k = 0; k < kCols; ++k) acc[k] = 0.0f;
-    float lsum = 0.0f;
+    for (int k = 0; k < kRows; ++k) {
+      mr[k] = __shfl_sync(0xffffffffu, M, r0 + k);
+      ir[k] = __shfl_sync(0xffffffffu, inv, r0 + k);
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) acc[k][c] = 0.0f;
+    }
+#pragma unroll 2
     for (int s = 0; s < pc.npieces; ++s) {
-      const uint8_t* base = a.slots + piece_slot(a, pc, s) * Sl::kBytes;
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + ur);
-      const float wgt = ml.x == -INFINITY ? 0.0f : exp2f(ml.x - mref);
-      lsum += wgt * ml.y;
-      const float* o = reinterpret_cast<const float*>(base + Sl::kO) + static_cast<size_t>(ur) * D + lane * kCols;
-      if constexpr (kCols == 4) {
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(o));
-        acc[0] += wgt * x.x;
-        acc[1] += wgt * x.y;
-        acc[2] += wgt * x.z;
-        acc[3] += wgt * x.w;
-      } else {
-        const float2 x = __ldcg(reinterpret_cast<const float2*>(o));
-        acc[0] += wgt * x.x;
-        acc[1] += wgt * x.y;
+      const uint8_t* base = a.slots + static_cast<size_t>(piece_slot(a, pc, s)) * Sl::kBytes;
+      float ms[kRows];
+      float x[kRows][kCols];
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        const int ur = min(row0 + r0 + k, pc.rows - 1);
+        ms[k] = __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + ur).x;
+        const float* o = reinterpret_cast<const float*>(base + Sl::kO) + static_cast<size_t>(ur) * D + lane * kCols;
+        if constexpr (kCols == 4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(o));
+          x[k][0] = v.x;
+          x[k][1] = v.y;
+          x[k][2] = v.z;
+          x[k][3] = v.w;
+        } else {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(o));
+          x[k][0] = v.x;
+          x[k][1] = v.y;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        const float wgt = ms[k] == -INFINITY ? 0.0f : exp2f(ms[k] - mr[k]);
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) acc[k][c] += wgt * x[k][c];
       }
     }
-    const float inv = (lsum > 0.0f && !bad) ? 1.0f / lsum : 0.0f;
-    const int R = pc.mp * kUnitRows + ur;
-    const size_t row = static_cast<size_t>(pc.n0 + R / g) * a.hq + pc.kvh * g + R % g;
-    if (a.out_fp32) {
-      float* dst = static_cast<float*>(a.out) + row * D + lane * kCols;
-      if constexpr (kCols == 4) {
-        *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      const int ur = row0 + r0 + k;
+      if (ur >= pc.rows) continue;
+      const int R = pc.mp * kUnitRows + ur;
+      const size_t row = static_cast<size_t>(pc.n0 + R / g) * a.hq + pc.kvh * g + R % g;
+      if (a.out_fp32) {
+        float* dst = static_cast<float*>(a.out) + row * D + lane * kCols;
+        if constexpr (kCols == 4) {
+          *reinterpret_cast<float4*>(dst) = make_float4(acc[k][0] * ir[k], acc[k][1] * ir[k],
+                                                        acc[k][2] * ir[k], acc[k][3] * ir[k]);
+        } else {
+          *reinterpret_cast<float2*>(dst) = make_float2(acc[k][0] * ir[k], acc[k][1] * ir[k]);
+        }
       } else {
-        *reinterpret_cast<float2*>(dst) = make_float2(acc[0] * inv, acc[1] * inv);
-      }
-    } else {
-      uint16_t* dst = static_cast<uint16_t*>(a.out) + row * D + lane * kCols;
-      if constexpr (kCols == 4) {
-        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
-                                                    pack_bf16x2(acc[2] * inv, acc[3] * inv));
-      } else {
-        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        uint16_t* dst = static_cast<uint16_t*>(a.out) + row * D + lane * kCols;
+        if constexpr (kCols == 4) {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[k][0] * ir[k], acc[k][1] * ir[k]),
+                                                      pack_bf16x2(acc[k][2] * ir[k], acc[k][3] * ir[k]));
+        } else {
+          *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[k][0] * ir[k], acc[k][1] * ir[k]);
+        }
       }
     }
   }
@@ -967,7 +1000,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_sync(bar, nthr);
           if (misc->merge) {
             __threadfence();
-            merge_unit<D>(a, pc, ur, nthr);
+            merge_unit<D>(a, pc, ur);
           }
           named_sync(bar, nthr);  // misc->merge is rewritten by the next split piece
         }

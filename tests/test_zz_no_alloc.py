@@ -73,4 +73,5 @@ def test_no_alloc_plans_fit_the_array():
                           total_nodes=b * n, max_prefix_len=L, softmax_scale=0.0, out_dtype=0)
         assert tv.attention_workspace_size(p) <= lib_scratch_bytes()
         assert tv.attention_plan(p, sms=251)["workspace_bytes"] <= lib_scratch_bytes()
-        assert tv.attention_plan(p, sms=260)["workspace_bytes"] > lib_scratch_bytes()
+        big = tv.attention_plan(p, sms=260)
+        assert (big["workspace_bytes"] > lib_scratch_bytes()) == (big["ctas"] > 251)
