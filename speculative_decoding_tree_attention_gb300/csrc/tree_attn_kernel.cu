@@ -51,8 +51,7 @@
 //                      ancestor bitmask, the row max, fp32 online softmax in
 //                      base 2 against a running max that moves only when it
 //                      grows by more than 2^8 (O is then rescaled in TMEM), and
-//                      P as bf16 pairs into TMEM; the row sum adds the rounded
-//                      P, so O / l weights V exactly as the P V product did.
+//                      P as bf16 pairs into TMEM.
 //                      They also load Q (cp.async, in the 128-byte swizzled
 //                      layout the MMA reads), build the ancestor masks and
 //                      write or merge the results.
@@ -139,11 +138,14 @@ struct Misc {
   int npieces;                // pieces of this round
   int more;                   // another round follows
   int merge;                  // this CTA merges the current split unit
+  int zero_needed;            // a malformed sequence's rows are zeroed by this CTA
   int tree_bad[2];            // per group: the tree of its current piece is malformed
   int piece_bad[kMaxPieces];  // a block id of the piece was out of range
 };
 
-// Partial-result slot: O rows (fp32, unnormalised), (m, l) per row, a flag.
+// Partial-result slot: unnormalised O (fp32) as float4 [D/4][256 rows], so
+// that the lanes of a warp (consecutive rows) store and load consecutive 16
+// bytes; (m, l) per row; a flag.
 template <int D>
 struct Slot {
   static constexpr size_t kO = 0;
@@ -240,7 +242,14 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
   Piece* pieces = reinterpret_cast<Piece*>(smem + Ly::kPieces);
   long long* scratch = reinterpret_cast<long long*>(smem + Ly::kScan);
   const size_t out_elem = a.out_fp32 ? 4 : 2;
-  // the length of the line; malformed sequences of this CTA (b mod grid)
+  // the length of the line; malformed sequences of this CTA (b mod grid).  A
+  // batch of at most 256 is read once and kept in registers for the second
+  // pass.
+  const bool one_chunk = a.batch <= kSoftmaxThreads;
+  SeqInfo kept;
+  kept.W = 0;
+  kept.T = 1;
+  kept.layers = 1;
   long long W = 0;
   for (int base = 0; base < a.batch; base += kSoftmaxThreads) {
     const int b = base + sid;
@@ -248,14 +257,17 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
     if (b < a.batch) {
       const SeqInfo s = seq_info(a, b);
       w = s.W;
-      if (round == 0 && !s.valid && s.N >= 1 && b % gridDim.x == blockIdx.x)
+      if (one_chunk) kept = s;
+      if (round == 0 && !s.valid && s.N >= 1 && b % gridDim.x == blockIdx.x) {
         record_status(a.status, b, kBadTree);
+        misc->zero_needed = 1;
+      }
     }
     long long tot;
     scan256(w, scratch, sid, &tot);
     W += tot;
   }
-  if (round == 0) {
+  if (round == 0 && misc->zero_needed) {
     // the rows of a malformed sequence that can be addressed get zeros
     for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
       const SeqInfo s = seq_info(a, b);
@@ -276,11 +288,13 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
     long long cum = 0;
     for (int base = 0; base < a.batch; base += kSoftmaxThreads) {
       const int b = base + sid;
-      SeqInfo s;
-      s.W = 0;
-      s.T = 1;
-      s.layers = 1;
-      if (b < a.batch) s = seq_info(a, b);
+      SeqInfo s = kept;
+      if (!one_chunk) {
+        s.W = 0;
+        s.T = 1;
+        s.layers = 1;
+        if (b < a.batch) s = seq_info(a, b);
+      }
       long long tot;
       const long long c0 = cum + scan256(s.W, scratch, sid, &tot);
       // the units of b that meet [s_v, e_v), in line order; the unit of a
@@ -377,100 +391,53 @@ __device__ __forceinline__ int piece_slot(const AttnArgs& a, const Piece& pc, in
 }
 
 // Merges the pieces of a split unit: O = sum_s 2^(m_s - M) O_s /
-// sum_s 2^(m_s - M) l_s over the slots in piece order.  Warp w of the
-// `nthreads` participants owns rows 32 w .. 32 w + 31 of the unit: first each
-// lane takes one row's (m, l) over every piece (M and the sum, online), then
-// the warp streams the O rows, four rows at a time with every piece's loads
-// in flight, the lanes D/32 columns each.
+// sum_s 2^(m_s - M) l_s over the slots in piece order.  Thread `ur` of the
+// participants takes row ur of the unit: its (m, l) over every piece first,
+// then O in 32-column chunks, each chunk's loads of every piece in flight
+// (the lanes of a warp read consecutive rows: coalesced).
 template <int D>
-__device__ void merge_unit(const AttnArgs& a, const Piece& pc, int sid) {
+__device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t out_row) {
   using Sl = Slot<D>;
-  constexpr int kCols = D / 32;  // columns per lane
-  constexpr int kRows = 4;       // rows in flight per warp
-  const int lane = sid & 31;
-  const int row0 = (sid >> 5) * 32;
-  if (row0 >= pc.rows) return;
-  const int my_row = row0 + lane;
+  if (ur >= pc.rows) return;
   bool bad = false;
   float M = -INFINITY, l = 0.0f;
   for (int s = 0; s < pc.npieces; ++s) {
     const uint8_t* base = a.slots + static_cast<size_t>(piece_slot(a, pc, s)) * Sl::kBytes;
     bad |= __ldcg(reinterpret_cast<const int*>(base + Sl::kFlag)) != 0;
-    if (my_row < pc.rows) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + my_row);
-      if (ml.x > M) {
-        l = (M == -INFINITY ? 0.0f : l * exp2f(M - ml.x)) + ml.y;
-        M = ml.x;
-      } else if (ml.x != -INFINITY) {
-        l += ml.y * exp2f(ml.x - M);
-      }
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + ur);
+    if (ml.x > M) {
+      l = (M == -INFINITY ? 0.0f : l * exp2f(M - ml.x)) + ml.y;
+      M = ml.x;
+    } else if (ml.x != -INFINITY) {
+      l += ml.y * exp2f(ml.x - M);
     }
   }
   const float inv = (l > 0.0f && !bad) ? 1.0f / l : 0.0f;
-  const int g = a.group;
-  for (int r0 = 0; r0 < 32 && row0 + r0 < pc.rows; r0 += kRows) {
-    float acc[kRows][kCols];
-    float mr[kRows], ir[kRows];
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    float acc[32];
 #pragma unroll
-    for (int k = 0; k < kRows; ++k) {
-      mr[k] = __shfl_sync(0xffffffffu, M, r0 + k);
-      ir[k] = __shfl_sync(0xffffffffu, inv, r0 + k);
-#pragma unroll
-      for (int c = 0; c < kCols; ++c) acc[k][c] = 0.0f;
-    }
-#pragma unroll 2
+    for (int k = 0; k < 32; ++k) acc[k] = 0.0f;
+#pragma unroll 1
     for (int s = 0; s < pc.npieces; ++s) {
       const uint8_t* base = a.slots + static_cast<size_t>(piece_slot(a, pc, s)) * Sl::kBytes;
-      float ms[kRows];
-      float x[kRows][kCols];
+      const float ms = __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + ur).x;
+      const float4* o4 = reinterpret_cast<const float4*>(base + Sl::kO) + static_cast<size_t>(c0 / 4) * kUnitRows + ur;
+      float4 v[8];
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        const int ur = min(row0 + r0 + k, pc.rows - 1);
-        ms[k] = __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + ur).x;
-        const float* o = reinterpret_cast<const float*>(base + Sl::kO) + static_cast<size_t>(ur) * D + lane * kCols;
-        if constexpr (kCols == 4) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(o));
-          x[k][0] = v.x;
-          x[k][1] = v.y;
-          x[k][2] = v.z;
-          x[k][3] = v.w;
-        } else {
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(o));
-          x[k][0] = v.x;
-          x[k][1] = v.y;
-        }
-      }
+      for (int k = 0; k < 8; ++k) v[k] = __ldcg(o4 + k * kUnitRows);
+      const float wgt = ms == -INFINITY ? 0.0f : exp2f(ms - M);
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        const float wgt = ms[k] == -INFINITY ? 0.0f : exp2f(ms[k] - mr[k]);
-#pragma unroll
-        for (int c = 0; c < kCols; ++c) acc[k][c] += wgt * x[k][c];
+      for (int k = 0; k < 8; ++k) {
+        acc[4 * k] += wgt * v[k].x;
+        acc[4 * k + 1] += wgt * v[k].y;
+        acc[4 * k + 2] += wgt * v[k].z;
+        acc[4 * k + 3] += wgt * v[k].w;
       }
     }
 #pragma unroll
-    for (int k = 0; k < kRows; ++k) {
-      const int ur = row0 + r0 + k;
-      if (ur >= pc.rows) continue;
-      const int R = pc.mp * kUnitRows + ur;
-      const size_t row = static_cast<size_t>(pc.n0 + R / g) * a.hq + pc.kvh * g + R % g;
-      if (a.out_fp32) {
-        float* dst = static_cast<float*>(a.out) + row * D + lane * kCols;
-        if constexpr (kCols == 4) {
-          *reinterpret_cast<float4*>(dst) = make_float4(acc[k][0] * ir[k], acc[k][1] * ir[k],
-                                                        acc[k][2] * ir[k], acc[k][3] * ir[k]);
-        } else {
-          *reinterpret_cast<float2*>(dst) = make_float2(acc[k][0] * ir[k], acc[k][1] * ir[k]);
-        }
-      } else {
-        uint16_t* dst = static_cast<uint16_t*>(a.out) + row * D + lane * kCols;
-        if constexpr (kCols == 4) {
-          *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[k][0] * ir[k], acc[k][1] * ir[k]),
-                                                      pack_bf16x2(acc[k][2] * ir[k], acc[k][3] * ir[k]));
-        } else {
-          *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[k][0] * ir[k], acc[k][1] * ir[k]);
-        }
-      }
-    }
+    for (int k = 0; k < 32; ++k) acc[k] *= inv;
+    store_row_chunk<D>(a, out_row, c0, acc);
   }
 }
 
@@ -503,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     misc->abort = 0;
+    misc->zero_needed = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&kfull[s], 1);
       mbar_init(&kempty[s], 1);
@@ -791,6 +759,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4*>(dst + hf * 1024 + c * 16) = make_uint4(0, 0, 0, 0);
           }
         }
+        // the next piece's Q row of this thread into L2, so that its load
+        // after this piece's epilogue is short
+        if (p + 1 < npieces && h < pieces[p + 1].nm) {
+          const Piece& nx = pieces[p + 1];
+          const int nr = nx.mp * kUnitRows + ur;
+          if (ur < nx.rows) {
+            const uint16_t* q = a.q + (static_cast<size_t>(nx.n0 + nr / g) * a.hq + nx.kvh * g + nr % g) * D;
+#pragma unroll
+            for (int k = 0; k < D * 2; k += 128) prefetch_l2(reinterpret_cast<const uint8_t*>(q) + k);
+          }
+        }
         // the tree of the sequence (pieces with node tiles): parents, the
         // check 0 <= parent[i] < i (parent[0] = -1), and this row's
         // ancestor-or-self bitmask
@@ -883,23 +862,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float mref = m_run == -INFINITY ? 0.0f : m_run;
           // P = 2^(s * scale * log2(e) - m) as bf16 pairs (column c holds keys
           // 2c, 2c+1), written over S_h in four 16-column stores; masked
-          // scores are -inf -> 0.  The row sum adds the rounded values.
-          float lsum = 0.0f;
+          // scores are -inf -> 0.  The exponent arguments and the row sum
+          // take two lanes per instruction.
+          const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+          const float2 nm2 = make_float2(-mref, -mref);
+          float2 lacc = make_float2(0.0f, 0.0f);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t pk[16];
-            float part = 0.0f;
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-              const float p0 = ex2_approx(fmaf(x[32 * q4 + 2 * k], a.scale_log2, -mref));
-              const float p1 = ex2_approx(fmaf(x[32 * q4 + 2 * k + 1], a.scale_log2, -mref));
-              const uint32_t pp = pack_bf16x2(p0, p1);
-              pk[k] = pp;
-              part += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xFFFF0000u);
+              const float2 e = fma2(make_float2(x[32 * q4 + 2 * k], x[32 * q4 + 2 * k + 1]), sc2, nm2);
+              const float2 pp = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+              pk[k] = pack_bf16x2(pp.x, pp.y);
+              lacc = add2(lacc, pp);
             }
             tmem_st16(tmem_s + 16 * q4 + lane_off, pk);
-            lsum += part;
           }
+          const float lsum = lacc.x + lacc.y;
           if (__any_sync(0xffffffffu, rescale)) {
             // O holds P(..t-1) V against the old max; P_h(t-1) V is complete
             // (S_h(t), which this thread has seen complete, was issued after it)
@@ -969,7 +949,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // a piece of a split unit: raw O and (m, l) into the slot; the last
           // piece of the unit to arrive merges every slot of the unit
           uint8_t* sl = a.slots + static_cast<size_t>(pc.slot) * Sl::kBytes;
-          float* so = reinterpret_cast<float*>(sl + Sl::kO) + static_cast<size_t>(ur) * D;
+          float4* so4 = reinterpret_cast<float4*>(sl + Sl::kO) + ur;
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
@@ -980,11 +960,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_ld_wait();
             }
             if (live) {
-              float4* dst = reinterpret_cast<float4*>(so + c0);
 #pragma unroll
               for (int k = 0; k < 8; ++k)
-                dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
-                                     __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+                so4[(c0 / 4 + k) * kUnitRows] =
+                    make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
             }
           }
           if (live) reinterpret_cast<float2*>(sl + Sl::kMl)[ur] = make_float2(m_run, l_run);
@@ -1000,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_sync(bar, nthr);
           if (misc->merge) {
             __threadfence();
-            merge_unit<D>(a, pc, ur);
+            merge_unit<D>(a, pc, ur, out_row);
           }
           named_sync(bar, nthr);  // misc->merge is rewritten by the next split piece
         }
