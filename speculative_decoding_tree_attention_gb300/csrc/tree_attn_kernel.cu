@@ -51,7 +51,8 @@
 //                      ancestor bitmask, the row max, fp32 online softmax in
 //                      base 2 against a running max that moves only when it
 //                      grows by more than 2^8 (O is then rescaled in TMEM), and
-//                      P as bf16 pairs into TMEM.
+//                      P as bf16 pairs into TMEM; the row sum adds the rounded
+//                      P, so O / l weights V exactly as the P V product did.
 //                      They also load Q (cp.async, in the 128-byte swizzled
 //                      layout the MMA reads), build the ancestor masks and
 //                      write or merge the results.
@@ -862,8 +863,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float mref = m_run == -INFINITY ? 0.0f : m_run;
           // P = 2^(s * scale * log2(e) - m) as bf16 pairs (column c holds keys
           // 2c, 2c+1), written over S_h in four 16-column stores; masked
-          // scores are -inf -> 0.  The exponent arguments and the row sum
-          // take two lanes per instruction.
+          // scores are -inf -> 0.  The row sum adds the rounded values, so
+          // that O / l weights V exactly as the P V product did (with the
+          // unrounded sum the rounding of a dominant P biases the output by
+          // up to 2^-9 of its V row).  Exponent arguments and sums take two
+          // lanes per instruction.
           const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
           const float2 nm2 = make_float2(-mref, -mref);
           float2 lacc = make_float2(0.0f, 0.0f);
@@ -874,8 +878,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 16; ++k) {
               const float2 e = fma2(make_float2(x[32 * q4 + 2 * k], x[32 * q4 + 2 * k + 1]), sc2, nm2);
               const float2 pp = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-              pk[k] = pack_bf16x2(pp.x, pp.y);
-              lacc = add2(lacc, pp);
+              const uint32_t pb = pack_bf16x2(pp.x, pp.y);
+              pk[k] = pb;
+              lacc = add2(lacc, make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
             }
             tmem_st16(tmem_s + 16 * q4 + lane_off, pk);
           }
