@@ -117,11 +117,11 @@ typedef struct {
 
 /* Bytes of device workspace tv_tree_attention needs for these parameters on
  * the current device (0 if the parameters are invalid).  The workspace holds
- * one arrival counter per CTA (zeroed by every call, on the stream) and two
+ * two arrival counters per CTA (zeroed by every call, on the stream) and two
  * partial-result slots per CTA: when the line of key tiles is cut inside a
- * unit (256 packed rows of one sequence and KV head), each piece leaves its
- * unnormalised output and (max, sum) per row there and the last piece to
- * finish merges them.  About 2 * SMs * (256 * D * 4 + 2 KB) bytes: 40.5 MB at
+ * unit (256 packed rows of one sequence and KV head), every piece but the
+ * last to finish leaves its unnormalised output and (max, sum) per row there,
+ * and the last merges them in a fixed order.  About 2 * SMs * (256 * D * 4 + 2 KB) bytes: 40.5 MB at
  * D = 128 on 152 SMs. */
 size_t tv_tree_attention_workspace_size(const tv_attn_params* params);
 
@@ -194,8 +194,8 @@ int tv_tree_attention(const tv_attn_params* params, const uint16_t* q_nodes,
  *     life of the process; make that first call before any stream capture on
  *     the device, and do not reset the device's primary context afterwards.
  *   - Every call uses the same array and it keeps the last call's contents;
- *     the counters that must start at zero are cleared by each call on its
- *     stream.  Calls that overlap on the GPU (other streams, other host
+ *     the arrival counters that must start at zero are cleared by each call
+ *     on its stream.  Calls that overlap on the GPU (other streams, other host
  *     threads) race on the array: serialise them. */
 #define TV_NO_ALLOC_SCRATCH_BYTES (64u << 20)
 int tv_tree_attention_no_alloc(const tv_attn_params* params, const uint16_t* q_nodes,

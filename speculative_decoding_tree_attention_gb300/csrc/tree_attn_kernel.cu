@@ -181,7 +181,8 @@ struct SeqInfo {
   int mpairs;        // m-tile pairs (units per KV head)
   int layers;        // ceil(mpairs / lanes)
   int valid;         // extent well formed
-  long long W;       // tiles of the sequence on the line
+  int W;             // tiles of the sequence on the line (the host bounds the
+                     // whole line below 2^31)
 };
 
 __device__ __forceinline__ SeqInfo seq_info(const AttnArgs& a, int b) {
@@ -195,26 +196,25 @@ __device__ __forceinline__ SeqInfo seq_info(const AttnArgs& a, int b) {
   s.T = s.P + (s.N + BN - 1) / BN;
   s.mpairs = s.valid ? (s.N * a.group + kUnitRows - 1) / kUnitRows : 0;
   s.layers = (s.mpairs + a.lanes - 1) / a.lanes;
-  s.W = s.valid ? static_cast<long long>(a.hkv) * s.layers * s.T : 0;
+  s.W = s.valid ? a.hkv * s.layers * s.T : 0;
   return s;
 }
 
 // Exclusive scan over the 256 softmax threads; *total = the sum.
-__device__ __forceinline__ long long scan256(long long v, long long* scratch, int sid,
-                                             long long* total) {
+__device__ __forceinline__ int scan256(int v, int* scratch, int sid, int* total) {
   const int lane = sid & 31, w = sid >> 5;
-  long long x = v;
+  int x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) scratch[w] = x;
   named_sync(kBarPair, kSoftmaxThreads);
-  long long before = 0, all = 0;
+  int before = 0, all = 0;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const long long s = scratch[k];
+    const int s = scratch[k];
     if (k < w) before += s;
     all += s;
   }
@@ -223,14 +223,22 @@ __device__ __forceinline__ long long scan256(long long v, long long* scratch, in
   return before + x - v;
 }
 
-// The virtual CTA whose range [floor(v W / V), floor((v+1) W / V)) holds
-// line position p (0 <= p < W).
-__device__ __forceinline__ int vcta_of(long long p, long long W, int V) {
-  int v = static_cast<int>((p * V) / W);
-  while (v + 1 < V && ((v + 1) * W) / V <= p) ++v;
-  while (v > 0 && (v * W) / V > p) --v;
-  return v;
-}
+// Range boundaries of the V virtual CTAs on a line of W tiles: virtual CTA v
+// takes [start(v), start(v+1)) with start(v) = floor(v W / V), computed as
+// v q + floor(v r / V) with W = q V + r (no 64-bit division).
+struct Line {
+  int W, V, q, r;
+  __device__ __forceinline__ int start(int v) const { return v * q + (v * r) / V; }
+  // the virtual CTA whose range holds position p (0 <= p < W)
+  __device__ __forceinline__ int owner(int p) const {
+    int lo = 0, hi = V - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (start(mid) <= p) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  }
+};
 
 // Builds this CTA's pieces of scheduling round `round` into shared memory
 // (run by the 256 softmax threads).  In round 0 it also zeroes the output of
@@ -241,7 +249,7 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
   using Ly = Layout<D>;
   Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
   Piece* pieces = reinterpret_cast<Piece*>(smem + Ly::kPieces);
-  long long* scratch = reinterpret_cast<long long*>(smem + Ly::kScan);
+  int* scratch = reinterpret_cast<int*>(smem + Ly::kScan);
   const size_t out_elem = a.out_fp32 ? 4 : 2;
   // the length of the line; malformed sequences of this CTA (b mod grid).  A
   // batch of at most 256 is read once and kept in registers for the second
@@ -251,10 +259,10 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
   kept.W = 0;
   kept.T = 1;
   kept.layers = 1;
-  long long W = 0;
+  int W = 0;
   for (int base = 0; base < a.batch; base += kSoftmaxThreads) {
     const int b = base + sid;
-    long long w = 0;
+    int w = 0;
     if (b < a.batch) {
       const SeqInfo s = seq_info(a, b);
       w = s.W;
@@ -264,7 +272,7 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
         misc->zero_needed = 1;
       }
     }
-    long long tot;
+    int tot;
     scan256(w, scratch, sid, &tot);
     W += tot;
   }
@@ -281,12 +289,16 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
   }
   const int lanes = a.lanes;
   const int v = static_cast<int>(blockIdx.x) / lanes, li = static_cast<int>(blockIdx.x) % lanes;
-  const int V = static_cast<int>(
-      max(1ll, min(static_cast<long long>(a.vctas), W / max(1, a.min_tiles))));
+  Line line;
+  line.W = W;
+  line.V = max(1, min(a.vctas, W / max(1, a.min_tiles)));
+  line.q = W / line.V;
+  line.r = W % line.V;
+  const int V = line.V;
   int count = 0;  // pieces of this CTA before the current chunk (all rounds)
   if (W > 0 && v < V) {
-    const long long s_v = (v * W) / V, e_v = ((v + 1) * W) / V;
-    long long cum = 0;
+    const int s_v = line.start(v), e_v = line.start(v + 1);
+    int cum = 0;
     for (int base = 0; base < a.batch; base += kSoftmaxThreads) {
       const int b = base + sid;
       SeqInfo s = kept;
@@ -296,37 +308,37 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
         s.layers = 1;
         if (b < a.batch) s = seq_info(a, b);
       }
-      long long tot;
-      const long long c0 = cum + scan256(s.W, scratch, sid, &tot);
+      int tot;
+      const int c0 = cum + scan256(s.W, scratch, sid, &tot);
       // the units of b that meet [s_v, e_v), in line order; the unit of a
       // lane past the sequence's m-tile pairs is idle and skipped
       int mine = 0;
-      long long lo = 0, hi = 0;
+      int lo = 0, hi = 0;
       if (s.W > 0) {
         lo = max(s_v, c0) - c0;
         hi = min(e_v, c0 + s.W) - c0;
         if (lo < hi)
-          for (long long ui = lo / s.T; ui <= (hi - 1) / s.T; ++ui)
-            if (static_cast<int>(ui % s.layers) * lanes + li < s.mpairs) ++mine;
+          for (int ui = lo / s.T; ui <= (hi - 1) / s.T; ++ui)
+            if ((ui % s.layers) * lanes + li < s.mpairs) ++mine;
       }
-      long long ptot;
-      const int first = count + static_cast<int>(scan256(mine, scratch, sid, &ptot));
+      int ptot;
+      const int first = count + scan256(mine, scratch, sid, &ptot);
       if (mine > 0) {
         int k = first;
-        for (long long ui = lo / s.T; ui <= (hi - 1) / s.T; ++ui) {
-          const int kvh = static_cast<int>(ui / s.layers), layer = static_cast<int>(ui % s.layers);
+        for (int ui = lo / s.T; ui <= (hi - 1) / s.T; ++ui) {
+          const int kvh = ui / s.layers, layer = ui % s.layers;
           const int mp = layer * lanes + li;
           if (mp >= s.mpairs) continue;
           const int slot_i = k - round * kMaxPieces;
           ++k;
           if (slot_i < 0 || slot_i >= kMaxPieces) continue;
           Piece pc;
-          const long long u0 = c0 + ui * s.T;  // line position of the unit's first tile
+          const int u0 = c0 + ui * s.T;  // line position of the unit's first tile
           pc.b = b;
           pc.kvh = kvh;
           pc.mp = mp;
-          pc.t0 = static_cast<int>(max(lo, ui * s.T) - ui * s.T);
-          pc.t1 = static_cast<int>(min(hi, (ui + 1) * s.T) - ui * s.T);
+          pc.t0 = max(lo, ui * s.T) - ui * s.T;
+          pc.t1 = min(hi, (ui + 1) * s.T) - ui * s.T;
           pc.P = s.P;
           pc.L = s.L;
           pc.n0 = s.n0;
@@ -341,7 +353,7 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
           } else {
             // the first piece (it holds tile 0) uses the CTA's slot 1, every
             // later piece (it starts the CTA's range) slot 0
-            const int vf = vcta_of(u0, W, V), vl = vcta_of(u0 + s.T - 1, W, V);
+            const int vf = line.owner(u0), vl = line.owner(u0 + s.T - 1);
             pc.vfirst = vf;
             pc.npieces = vl - vf + 1;
             pc.cnt = vf * lanes + li;
@@ -351,7 +363,7 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
           pieces[slot_i] = pc;
         }
       }
-      count += static_cast<int>(ptot);
+      count += ptot;
       cum += tot;
     }
   }
@@ -392,20 +404,25 @@ __device__ __forceinline__ int piece_slot(const AttnArgs& a, const Piece& pc, in
 }
 
 // Merges the pieces of a split unit: O = sum_s 2^(m_s - M) O_s /
-// sum_s 2^(m_s - M) l_s over the slots in piece order.  Thread `ur` of the
-// participants takes row ur of the unit: its (m, l) over every piece first,
-// then O in 32-column chunks, each chunk's loads of every piece in flight
-// (the lanes of a warp read consecutive rows: coalesced).
+// sum_s 2^(m_s - M) l_s in piece order.  Thread `ur` of the participants
+// takes row ur of the unit.  Piece `own` is this CTA's: its (m, l) and O come
+// from registers and TMEM (the values it would have written), the others'
+// from their slots; the lanes of a warp read consecutive rows (coalesced),
+// a 32-column chunk of every piece in flight at a time.
 template <int D>
-__device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t out_row) {
+__device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t out_row, int own,
+                           float m_own, float l_own, bool bad_own, uint32_t tmem_o) {
   using Sl = Slot<D>;
-  if (ur >= pc.rows) return;
-  bool bad = false;
+  const bool row_ok = ur < pc.rows;
+  bool bad = bad_own;
   float M = -INFINITY, l = 0.0f;
   for (int s = 0; s < pc.npieces; ++s) {
-    const uint8_t* base = a.slots + static_cast<size_t>(piece_slot(a, pc, s)) * Sl::kBytes;
-    bad |= __ldcg(reinterpret_cast<const int*>(base + Sl::kFlag)) != 0;
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + ur);
+    float2 ml = make_float2(m_own, l_own);
+    if (s != own) {
+      const uint8_t* base = a.slots + static_cast<size_t>(piece_slot(a, pc, s)) * Sl::kBytes;
+      bad |= __ldcg(reinterpret_cast<const int*>(base + Sl::kFlag)) != 0;
+      ml = row_ok ? __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + ur) : make_float2(-INFINITY, 0.0f);
+    }
     if (ml.x > M) {
       l = (M == -INFINITY ? 0.0f : l * exp2f(M - ml.x)) + ml.y;
       M = ml.x;
@@ -421,21 +438,31 @@ __device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t ou
     for (int k = 0; k < 32; ++k) acc[k] = 0.0f;
 #pragma unroll 1
     for (int s = 0; s < pc.npieces; ++s) {
-      const uint8_t* base = a.slots + static_cast<size_t>(piece_slot(a, pc, s)) * Sl::kBytes;
-      const float ms = __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + ur).x;
-      const float4* o4 = reinterpret_cast<const float4*>(base + Sl::kO) + static_cast<size_t>(c0 / 4) * kUnitRows + ur;
-      float4 v[8];
+      float v[32];
+      float ms = m_own;
+      if (s == own) {
+        // every thread of the warp loads TMEM together (a warp-wide load)
+        tmem_ld32(tmem_o + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld_wait();
+      } else if (row_ok) {
+        const uint8_t* base = a.slots + static_cast<size_t>(piece_slot(a, pc, s)) * Sl::kBytes;
+        ms = __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + ur).x;
+        const float4* o4 = reinterpret_cast<const float4*>(base + Sl::kO) + static_cast<size_t>(c0 / 4) * kUnitRows + ur;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = __ldcg(o4 + k * kUnitRows);
+        for (int k = 0; k < 8; ++k) {
+          const float4 x = __ldcg(o4 + k * kUnitRows);
+          v[4 * k] = x.x;
+          v[4 * k + 1] = x.y;
+          v[4 * k + 2] = x.z;
+          v[4 * k + 3] = x.w;
+        }
+      }
+      if (!row_ok) continue;
       const float wgt = ms == -INFINITY ? 0.0f : exp2f(ms - M);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        acc[4 * k] += wgt * v[k].x;
-        acc[4 * k + 1] += wgt * v[k].y;
-        acc[4 * k + 2] += wgt * v[k].z;
-        acc[4 * k + 3] += wgt * v[k].w;
-      }
+      for (int k = 0; k < 32; ++k) acc[k] += wgt * v[k];
     }
+    if (!row_ok) continue;
 #pragma unroll
     for (int k = 0; k < 32; ++k) acc[k] *= inv;
     store_row_chunk<D>(a, out_row, c0, acc);
@@ -951,41 +978,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (live && done) store_row_chunk<D>(a, out_row, c0, v);
           }
         } else {
-          // a piece of a split unit: raw O and (m, l) into the slot; the last
-          // piece of the unit to arrive merges every slot of the unit
-          uint8_t* sl = a.slots + static_cast<size_t>(pc.slot) * Sl::kBytes;
-          float4* so4 = reinterpret_cast<float4*>(sl + Sl::kO) + ur;
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = 0u;
-            if (done) {
-              tmem_ld32(tmem_o + c0 + lane_off, o);
-              tmem_ld_wait();
-            }
-            if (live) {
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                so4[(c0 / 4 + k) * kUnitRows] =
-                    make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
-                                __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
-            }
-          }
-          if (live) reinterpret_cast<float2*>(sl + Sl::kMl)[ur] = make_float2(m_run, l_run);
-          if (ur == 0) *reinterpret_cast<int*>(sl + Sl::kFlag) = (bad || !done) ? 1 : 0;
-          __threadfence();
+          // a piece of a split unit.  Every piece takes a ticket; all but
+          // the last write raw O and (m, l) to their slot and then count
+          // themselves done; the last waits until the others are done and
+          // merges every piece of the unit, its own from TMEM.
           const int nthr = pc.nm * BM;
           const int bar = pc.nm == 2 ? kBarPair : kBarGroup0;
+          int* ticket = a.counters + 2 * pc.cnt;
+          int* finished = ticket + 1;
           named_sync(bar, nthr);
-          if (ur == 0) {
-            const int prev = atomicAdd(a.counters + pc.cnt, 1);
-            misc->merge = prev == pc.npieces - 1;
-          }
+          if (ur == 0) misc->merge = atomicAdd(ticket, 1) == pc.npieces - 1;
           named_sync(bar, nthr);
-          if (misc->merge) {
+          const bool last = misc->merge != 0;
+          if (!last) {
+            uint8_t* sl = a.slots + static_cast<size_t>(pc.slot) * Sl::kBytes;
+            float4* so4 = reinterpret_cast<float4*>(sl + Sl::kO) + ur;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = 0u;
+              if (done) {
+                tmem_ld32(tmem_o + c0 + lane_off, o);
+                tmem_ld_wait();
+              }
+              if (live) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  so4[(c0 / 4 + k) * kUnitRows] =
+                      make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                  __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+              }
+            }
+            if (live) reinterpret_cast<float2*>(sl + Sl::kMl)[ur] = make_float2(m_run, l_run);
+            if (ur == 0) *reinterpret_cast<int*>(sl + Sl::kFlag) = (bad || !done) ? 1 : 0;
             __threadfence();
-            merge_unit<D>(a, pc, ur, out_row);
+            named_sync(bar, nthr);
+            if (ur == 0) atomicAdd(finished, 1);
+          } else {
+            if (ur == 0) {
+              // the other pieces hold tickets, so they are running; each
+              // only has its slot write left
+              const unsigned long long t0 = global_ns();
+              while (atomicAdd(finished, 0) < pc.npieces - 1) {
+                if (global_ns() - t0 > kWaitLimitNs || *abort_flag) {
+                  record_status(a.status, pc.b, kDeviceTimeout);
+                  misc->abort = 1;
+                  break;
+                }
+              }
+            }
+            named_sync(bar, nthr);
+            __threadfence();
+            merge_unit<D>(a, pc, ur, out_row, static_cast<int>(blockIdx.x) / a.lanes - pc.vfirst,
+                          m_run, l_run, bad || !done, tmem_o + lane_off);
           }
           named_sync(bar, nthr);  // misc->merge is rewritten by the next split piece
         }

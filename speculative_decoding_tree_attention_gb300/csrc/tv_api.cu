@@ -67,7 +67,7 @@ constexpr int kMinTiles = 4;
 // many lanes as the largest tree has pairs, so that the CTAs reading the
 // same K/V tiles run together.  The virtual CTAs (sms / lanes of them, fewer
 // when the host hints bound the work below kMinTiles tiles each) share the
-// line of key tiles equally on the device.  Workspace: one arrival counter
+// line of key tiles equally on the device.  Workspace: two arrival counters
 // per CTA, then two partial-result slots per CTA.
 bool plan_attention(const tv_attn_params* p, int sms, AttnPlan* out) {
   if (!p || sms < 1) return false;
@@ -89,10 +89,11 @@ bool plan_attention(const tv_attn_params* p, int sms, AttnPlan* out) {
   const long long layers = (mpairs + pl.lanes - 1) / pl.lanes;
   const long long tiles = (p->max_prefix_len + 127) / 128 + (p->max_nodes + 127) / 128;
   const long long wmax = static_cast<long long>(p->batch) * p->num_kv_heads * layers * tiles;
+  if (wmax >= (1ll << 31)) return false;  // the device schedule counts tiles in 32 bits
   pl.min_tiles = kMinTiles;
   pl.vctas = static_cast<int>(std::max(1ll, std::min<long long>(sms / pl.lanes, wmax / kMinTiles)));
   const size_t ctas = static_cast<size_t>(pl.vctas) * pl.lanes;
-  pl.workspace = (ctas * 4 + 255) / 256 * 256 + 2 * ctas * tv::attn_slot_bytes(p->head_dim);
+  pl.workspace = (ctas * 8 + 255) / 256 * 256 + 2 * ctas * tv::attn_slot_bytes(p->head_dim);
   *out = pl;
   return true;
 }
@@ -230,7 +231,7 @@ int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
   a.out = out;
   a.status = status;
   a.counters = static_cast<int32_t*>(workspace);
-  a.slots = static_cast<uint8_t*>(workspace) + (ctas * 4 + 255) / 256 * 256;
+  a.slots = static_cast<uint8_t*>(workspace) + (ctas * 8 + 255) / 256 * 256;
   a.batch = p->batch;
   a.hq = p->num_q_heads;
   a.hkv = Hkv;
@@ -251,7 +252,7 @@ int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
   // status and the arrival counters of split units start at zero
   if (cudaMemsetAsync(status, 0, sizeof(int32_t) * p->batch, stream) != cudaSuccess)
     return TV_ERR_CUDA;
-  if (cudaMemsetAsync(a.counters, 0, ctas * 4, stream) != cudaSuccess) return TV_ERR_CUDA;
+  if (cudaMemsetAsync(a.counters, 0, ctas * 8, stream) != cudaSuccess) return TV_ERR_CUDA;
   if (tv::launch_tree_attention(a, maps, stream) != 0) return TV_ERR_CUDA;
   return TV_OK;
 }

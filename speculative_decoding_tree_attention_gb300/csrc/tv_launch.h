@@ -62,7 +62,7 @@ struct AttnArgs {
   const int32_t* node_offsets;// [batch+1]
   void* out;                  // [total_nodes][Hq][D], bf16 or fp32 (out_fp32)
   int32_t* status;            // [batch]
-  int32_t* counters;          // [ctas] arrival counters of split units (zeroed per call)
+  int32_t* counters;          // [ctas][2] ticket and done counters of split units (zeroed per call)
   uint8_t* slots;             // [2 * ctas] partial-result slots of attn_slot_bytes(D)
   int32_t batch, hq, hkv, group, head_dim;
   int32_t max_blocks_per_seq, num_blocks, max_nodes, max_prefix_len, total_nodes;

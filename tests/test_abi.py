@@ -78,13 +78,13 @@ def test_attention_null_pointer_rejected(lib):
 def test_attention_workspace_size_rules(lib):
     assert lib.tv_tree_attention_workspace_size(C.byref(_params(head_dim=96))) == 0
     assert lib.tv_tree_attention_workspace_size(C.byref(_params(out_dtype=2))) == 0
-    # one counter per CTA (rounded to 256 bytes), then two slots per CTA of
+    # two counters per CTA (rounded to 256 bytes), then two slots per CTA of
     # 256 rows x D fp32, 256 (m, l) pairs and a 256-byte flag area
     for d in (64, 128):
         plan = tv.attention_plan(_params(head_dim=d), sms=152)
         ctas = plan["ctas"]
         slot = 256 * d * 4 + 256 * 8 + 256
-        assert plan["workspace_bytes"] == (ctas * 4 + 255) // 256 * 256 + 2 * ctas * slot
+        assert plan["workspace_bytes"] == (ctas * 8 + 255) // 256 * 256 + 2 * ctas * slot
 
 
 def test_attention_refuses_a_short_workspace(lib):
