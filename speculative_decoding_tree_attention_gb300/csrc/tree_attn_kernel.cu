@@ -33,12 +33,12 @@
 // workspace slot, and the last piece to finish (an arrival counter per unit)
 // merges the slots in a fixed order, so results do not depend on timing.
 //
-// One CTA has 320 threads:
-//   warp 8  (TMA)      loads K and V tiles into two shared-memory rings: one 5-D
+// One CTA has 640 threads:
+//   warp 16 (TMA)      loads K and V tiles into two shared-memory rings: one 5-D
 //                      box per 16-token page through the block table (eight
 //                      pages per tile and tensor), or 16 boxes of 8 tree nodes;
 //                      pages past the sequence load as zeros (out of bounds).
-//   warp 9  (MMA)      one thread issues tcgen05.mma for both m-tiles h:
+//   warp 17 (MMA)      one thread issues tcgen05.mma for both m-tiles h:
 //                      S_h = Q_h K^T into TMEM (Q_h and K from shared memory),
 //                      O_h += P_h V with P_h read from TMEM, in the order
 //                      PV_0(t), S_0(t+1), PV_1(t), S_1(t+1).  P_h(t) is written
@@ -46,8 +46,10 @@
 //                      MMAs of one thread in order, so S_h(t+1) overwrites them
 //                      only after PV_h(t) has read them.  While one m-tile's
 //                      softmax runs, the tensor pipe works on the other's.
-//   warps 0-3, 4-7     the softmax of m-tile 0 and of m-tile 1, one thread per
-//                      row: tcgen05.ld of S, the tree mask from a per-row
+//   warps 0-7, 8-15    the softmax of m-tile 0 and of m-tile 1, two threads per
+//                      row (64 keys each; the halves of a row exchange their
+//                      maxima through shared memory): tcgen05.ld of S, the
+//                      tree mask from a per-row
 //                      ancestor bitmask, the row max, fp32 online softmax in
 //                      base 2 against a running max that moves only when it
 //                      grows by more than 2^8 (O is then rescaled in TMEM), and
@@ -56,6 +58,7 @@
 //                      They also load Q (cp.async, in the 128-byte swizzled
 //                      layout the MMA reads), build the ancestor masks and
 //                      write or merge the results.
+//   warps 18-19        no work (the block size keeps 96 registers a thread).
 // TMEM (512 columns): S_0/P_0 at 0, S_1/P_1 at 128, O_0 at 256, O_1 at 256+D.
 // Every wait on an mbarrier is bounded; on expiry the CTA reports
 // TV_ERR_DEVICE_TIMEOUT for its sequence, drains its copies and returns.
@@ -70,10 +73,12 @@ namespace {
 constexpr int BM = 128;               // rows of one m-tile
 constexpr int BN = 128;               // keys per tile
 constexpr int kUnitRows = 2 * BM;     // rows of one m-tile pair
-constexpr int kSoftmaxThreads = 256;  // warps 0-7: two groups of four warps
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;           // issues every MMA; owns the TMEM allocation
-constexpr int kThreads = 320;
+constexpr int kGroupThreads = 256;    // softmax threads of one m-tile: two per row
+constexpr int kSoftmaxThreads = 512;  // warps 0-15: two groups of eight warps
+constexpr int kSoftmaxWarps = kSoftmaxThreads / 32;
+constexpr int kTmaWarp = 16;
+constexpr int kMmaWarp = 17;          // issues every MMA; owns the TMEM allocation
+constexpr int kThreads = 640;         // warps 18-19: no work (96 registers a thread)
 constexpr int kMaxNodes = 512;
 constexpr int kMaxAncWords = kMaxNodes / 32;
 constexpr int kAncStride = kMaxAncWords + 1;  // odd word stride: rows of a warp hit distinct banks
@@ -115,11 +120,14 @@ struct Layout {
   static constexpr int kParentBytes = 2 * kMaxNodes * 4;
   static constexpr int kPieces = kParent + kParentBytes;
   static constexpr int kPiecesBytes = kMaxPieces * static_cast<int>(sizeof(Piece));
-  static constexpr int kScan = kPieces + kPiecesBytes;        // 8 warp sums (int64)
+  static constexpr int kScan = kPieces + kPiecesBytes;        // 16 warp sums
   static constexpr int kScanBytes = 128;
+  // half-row maxima of the two key halves, by tile parity: [2 m-tiles][2][2 halves][128]
+  static constexpr int kXchg = kScan + kScanBytes;
+  static constexpr int kXchgBytes = 2 * 2 * 2 * BM * 4;
   // block ids of the pages of the last 8 K tiles issued (8 per tile), reused
   // by the V copies of the same tiles
-  static constexpr int kBlk = kScan + kScanBytes;
+  static constexpr int kBlk = kXchg + kXchgBytes;
   static constexpr int kBlkBytes = 8 * 8 * 4;
   static constexpr int kBar = kBlk + kBlkBytes;
   // kfull[S], kempty[S], vfull[S], vempty[S], s_full[2], p_full[2],
@@ -200,7 +208,7 @@ __device__ __forceinline__ SeqInfo seq_info(const AttnArgs& a, int b) {
   return s;
 }
 
-// Exclusive scan over the 256 softmax threads; *total = the sum.
+// Exclusive scan over the 512 softmax threads; *total = the sum.
 __device__ __forceinline__ int scan256(int v, int* scratch, int sid, int* total) {
   const int lane = sid & 31, w = sid >> 5;
   int x = v;
@@ -213,7 +221,7 @@ __device__ __forceinline__ int scan256(int v, int* scratch, int sid, int* total)
   named_sync(kBarPair, kSoftmaxThreads);
   int before = 0, all = 0;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < kSoftmaxWarps; ++k) {
     const int s = scratch[k];
     if (k < w) before += s;
     all += s;
@@ -241,7 +249,7 @@ struct Line {
 };
 
 // Builds this CTA's pieces of scheduling round `round` into shared memory
-// (run by the 256 softmax threads).  In round 0 it also zeroes the output of
+// (run by the 512 softmax threads).  In round 0 it also zeroes the output of
 // sequences whose extent is malformed (every row it can address) and records
 // their status.
 template <int D>
@@ -252,7 +260,7 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
   int* scratch = reinterpret_cast<int*>(smem + Ly::kScan);
   const size_t out_elem = a.out_fp32 ? 4 : 2;
   // the length of the line; malformed sequences of this CTA (b mod grid).  A
-  // batch of at most 256 is read once and kept in registers for the second
+  // batch of at most 512 is read once and kept in registers for the second
   // pass.
   const bool one_chunk = a.batch <= kSoftmaxThreads;
   SeqInfo kept;
@@ -404,14 +412,15 @@ __device__ __forceinline__ int piece_slot(const AttnArgs& a, const Piece& pc, in
 }
 
 // Merges the pieces of a split unit: O = sum_s 2^(m_s - M) O_s /
-// sum_s 2^(m_s - M) l_s in piece order.  Thread `ur` of the participants
-// takes row ur of the unit.  Piece `own` is this CTA's: its (m, l) and O come
-// from registers and TMEM (the values it would have written), the others'
-// from their slots; the lanes of a warp read consecutive rows (coalesced),
-// a 32-column chunk of every piece in flight at a time.
+// sum_s 2^(m_s - M) l_s in piece order.  A thread takes columns [col0,
+// col0 + ncols) of row ur of the unit.  Piece `own` is this CTA's: its (m, l)
+// and O come from registers and TMEM (the values it would have written), the
+// others' from their slots; the lanes of a warp read consecutive rows
+// (coalesced), a 32-column chunk of every piece in flight at a time.
 template <int D>
 __device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t out_row, int own,
-                           float m_own, float l_own, bool bad_own, uint32_t tmem_o) {
+                           float m_own, float l_own, bool bad_own, uint32_t tmem_o, int col0,
+                           int ncols) {
   using Sl = Slot<D>;
   const bool row_ok = ur < pc.rows;
   bool bad = bad_own;
@@ -432,7 +441,7 @@ __device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t ou
   }
   const float inv = (l > 0.0f && !bad) ? 1.0f / l : 0.0f;
 #pragma unroll 1
-  for (int c0 = 0; c0 < D; c0 += 32) {
+  for (int c0 = col0; c0 < col0 + ncols; c0 += 32) {
     float acc[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) acc[k] = 0.0f;
@@ -485,9 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* vfull = bars + 2 * kStages;
   uint64_t* vempty = bars + 3 * kStages;
   uint64_t* s_full = bars + 4 * kStages;  // [2]: S_h(t) complete (and every MMA before it)
-  uint64_t* p_full = s_full + 2;          // [2]: P_h(t) in TMEM (128 arrivals)
+  uint64_t* p_full = s_full + 2;          // [2]: P_h(t) in TMEM (256 arrivals)
   uint64_t* o_done = p_full + 2;          // [2]: the last P_h V of a piece complete
-  uint64_t* q_full = o_done + 2;          // [2]: Q_h of a piece in shared memory (128 arrivals)
+  uint64_t* q_full = o_done + 2;          // [2]: Q_h of a piece in shared memory (256 arrivals)
   uint64_t* drain = q_full + 2;           // every MMA issued so far complete (once per round)
   Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
   Piece* pieces = reinterpret_cast<Piece*>(smem + Ly::kPieces);
@@ -507,9 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(&s_full[h], 1);
-      mbar_init(&p_full[h], BM);
+      mbar_init(&p_full[h], kGroupThreads);
       mbar_init(&o_done[h], 1);
-      mbar_init(&q_full[h], BM);
+      mbar_init(&q_full[h], kGroupThreads);
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -532,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int tiles_h0 = 0, tiles_h1 = 0, pieces_h0 = 0, pieces_h1 = 0;
 
   for (int round = 0;; ++round) {
-    if (warp < kTmaWarp) build_schedule<D>(a, smem, round, tid);
+    if (warp < kSoftmaxWarps) build_schedule<D>(a, smem, round, tid);
     __syncthreads();
     const int npieces = misc->npieces;
     const bool more = misc->more != 0;
@@ -737,17 +746,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(drain, round & 1);
       }
       __syncwarp();
-    } else {
+    } else if (warp < kSoftmaxWarps) {
       // ------------------------------------------------------ softmax groups
-      // Warps 4h .. 4h+3 own m-tile h; warp w's rows are its TMEM lane
-      // quarter 32 (w % 4) .. +31.
-      const int h = warp >> 2;
-      const int r = (warp & 3) * 32 + lane;  // row of the m-tile == TMEM lane
+      // Warps 8h .. 8h+7 own m-tile h.  Warp w reads TMEM lane quarter
+      // 32 (w % 4) .. +31 (its rows) and takes key half c = (w / 4) % 2 of
+      // each tile (64 keys) and column half c of O, so the two threads of a
+      // row are in warps w and w ^ 4.
+      const int h = warp >> 3;
+      const int c = (warp >> 2) & 1;
+      const int r = (warp & 3) * 32 + lane;   // row of the m-tile == TMEM lane
+      const int gid = c * BM + r;             // thread of the group (0 .. 255)
+      constexpr int kHalfD = D / 2;           // O columns of this thread
       const uint32_t lane_off = lane_off_q(warp);
       const uint32_t tmem_s = tmem + h * BN;
       const uint32_t tmem_o = tmem + 256 + h * D;
       uint32_t* anc = reinterpret_cast<uint32_t*>(smem + Ly::kAnc) + (h * BM + r) * kAncStride;
       int32_t* par = reinterpret_cast<int32_t*>(smem + Ly::kParent) + h * kMaxNodes;
+      float* xchg = reinterpret_cast<float*>(smem + Ly::kXchg) + h * (2 * 2 * BM);  // [parity][half][row]
       uint8_t* qh = smem + Ly::kQ + h * Ly::kQBytes;
       volatile int* piece_bad = misc->piece_bad;
       int my_tiles = h ? tiles_h1 : tiles_h0;
@@ -755,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int tau = g_tile;  // global index of the piece's first tile
       for (int p = 0; p < npieces; ++p) {
-        const Piece pc = pieces[p];
+        const Piece& pc = pieces[p];  // fields are read from shared memory as needed
         const int T = pc.t1 - pc.t0;
         if (h >= pc.nm) {  // this m-tile has no rows in the unit
           tau += T;
@@ -767,24 +782,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool live = ur < pc.rows;
         const int i_node = live ? R / g : 0;
         const size_t out_row = static_cast<size_t>(pc.n0 + i_node) * a.hq + pc.kvh * g + R % g;
-        // Q rows -> shared memory in the 128-byte swizzled K-major layout
-        // (the 16-byte chunk c of row r sits at chunk c ^ (r % 8)); rows past
-        // the unit are zero.  The buffer is free: the previous piece's last
-        // S_h completed before its epilogue.
+        // Q: this thread's half of its row -> shared memory in the 128-byte
+        // swizzled K-major layout (16-byte chunk k of row r at chunk
+        // k ^ (r % 8) of its 128-byte line); rows past the unit are zero.
+        // The buffer is free: the previous piece's last S_h completed before
+        // its epilogue.
         {
+          constexpr int kChunks = D / 16;  // 16-byte chunks of half a row
           uint8_t* dst = qh + (r >> 3) * Ly::kGroupBytes + (r & 7) * 128;
-          if (live) {
-            const uint16_t* src = a.q + out_row * D;
+          const uint16_t* src = a.q + out_row * D;
 #pragma unroll
-            for (int hf = 0; hf < Ly::kHalves; ++hf)
-#pragma unroll
-              for (int c = 0; c < 8; ++c) cpa16(dst + hf * 1024 + ((c ^ (r & 7)) << 4), src + hf * 64 + c * 8);
-          } else {
-#pragma unroll
-            for (int hf = 0; hf < Ly::kHalves; ++hf)
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(dst + hf * 1024 + c * 16) = make_uint4(0, 0, 0, 0);
+          for (int k = c * kChunks; k < (c + 1) * kChunks; ++k) {
+            uint8_t* d = dst + (k >> 3) * 1024 + (((k & 7) ^ (r & 7)) << 4);
+            if (live) {
+              cpa16(d, src + k * 8);
+            } else {
+              *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
+            }
           }
         }
         // the next piece's Q row of this thread into L2, so that its load
@@ -794,88 +808,94 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nr = nx.mp * kUnitRows + ur;
           if (ur < nx.rows) {
             const uint16_t* q = a.q + (static_cast<size_t>(nx.n0 + nr / g) * a.hq + nx.kvh * g + nr % g) * D;
-#pragma unroll
-            for (int k = 0; k < D * 2; k += 128) prefetch_l2(reinterpret_cast<const uint8_t*>(q) + k);
+            prefetch_l2(reinterpret_cast<const uint8_t*>(q) + c * D);
           }
         }
         // the tree of the sequence (pieces with node tiles): parents, the
-        // check 0 <= parent[i] < i (parent[0] = -1), and this row's
-        // ancestor-or-self bitmask
+        // check 0 <= parent[i] < i (parent[0] = -1), and the row's
+        // ancestor-or-self bitmask (built by the thread of key half 0)
         const bool has_nodes = pc.t1 > pc.P;
         bool tree_bad = false;
         if (has_nodes) {
-          if (r == 0) misc->tree_bad[h] = 0;
-          named_sync(bar_group, BM);
-          for (int k = r; k < pc.N; k += BM) {
+          if (gid == 0) misc->tree_bad[h] = 0;
+          named_sync(bar_group, kGroupThreads);
+          for (int k = gid; k < pc.N; k += kGroupThreads) {
             const int q = __ldg(a.parent + pc.n0 + k);
             par[k] = q;
             if (!(k == 0 ? q == -1 : (q >= 0 && q < k))) misc->tree_bad[h] = 1;
           }
-          named_sync(bar_group, BM);
+          named_sync(bar_group, kGroupThreads);
           tree_bad = misc->tree_bad[h] != 0;
+          if (c == 0) {
 #pragma unroll
-          for (int k = 0; k < kMaxAncWords; ++k) anc[k] = 0u;
-          if (!tree_bad && live)
-            for (int k = i_node; k >= 0; k = par[k]) anc[k >> 5] |= 1u << (k & 31);
-          if (tree_bad && r == 0) record_status(a.status, pc.b, kBadTree);
-          named_sync(bar_group, BM);  // tree_bad is reset by the next piece
+            for (int k = 0; k < kMaxAncWords; ++k) anc[k] = 0u;
+            if (!tree_bad && live)
+              for (int k = i_node; k >= 0; k = par[k]) anc[k >> 5] |= 1u << (k & 31);
+          }
+          if (tree_bad && gid == 0) record_status(a.status, pc.b, kBadTree);
+          named_sync(bar_group, kGroupThreads);  // masks complete; tree_bad is reset by the next piece
         }
         cpa_wait_all();
         fence_proxy_async_smem();  // generic writes of Q, read by the MMA
         mbar_arrive(&q_full[h]);
 
-        float m_run = -INFINITY;  // running max (log2 units)
-        float l_run = 0.0f;       // row sum against m_run
+        float m_run = -INFINITY;  // running max (log2 units), the same in both halves
+        float l_half = 0.0f;      // this half's row sum against m_run
         for (int i = 0; i < T; ++i) {
           const int t = pc.t0 + i;  // tile of the unit
           const int gt = tau + i;   // global tile (ring slot)
+          const int par_t = my_tiles & 1;
           if (ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[h], my_tiles & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[h], par_t, abort_flag));
             if (!ok) misc->abort = 1;
           }
           ++my_tiles;
-          if (!ok) {
-            mbar_arrive(&p_full[h]);
-            continue;
-          }
-          float x[128];
-          tc_fence_after();
+          // this half's 64 scores of the tile
+          float x[64];
+          if (ok) {
+            tc_fence_after();
+            tmem_ld32(tmem_s + 64 * c + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+            tmem_ld32(tmem_s + 64 * c + 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+            tmem_ld_wait();
+          } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tmem_ld32(tmem_s + 32 * c + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
-          tmem_ld_wait();
+            for (int k = 0; k < 64; ++k) x[k] = -INFINITY;
+          }
           // mask (scores stay unscaled; the scale is folded into the exponent)
           int valid_keys = BN;
           if (t < pc.P) {
             valid_keys = min(BN, pc.L - t * BN);
-            if (valid_keys < BN) {
+            const int v_half = valid_keys - 64 * c;  // valid keys of this half
+            if (v_half < 64) {
 #pragma unroll
-              for (int c = 0; c < 128; ++c)
-                if (c >= valid_keys) x[c] = -INFINITY;
+              for (int k = 0; k < 64; ++k)
+                if (k >= v_half) x[k] = -INFINITY;
             }
           } else {
             // only ancestors-or-self of this node carry a bit, all of them
             // < N, so node columns past the tree are masked as well
-            const int j0 = (t - pc.P) * BN;
+            const int j0 = (t - pc.P) * BN + 64 * c;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < 2; ++k) {
               const uint32_t bits = live ? anc[(j0 >> 5) + k] : 0u;
 #pragma unroll
-              for (int c = 0; c < 32; ++c) x[32 * k + c] = (bits & (1u << c)) ? x[32 * k + c] : -INFINITY;
+              for (int b = 0; b < 32; ++b) x[32 * k + b] = (bits & (1u << b)) ? x[32 * k + b] : -INFINITY;
             }
           }
-          // max of the 128 scores: eight running three-input maxima
-          float mx[8];
+          // max of this half: four running three-input maxima, then the
+          // row's max with the other half through shared memory
+          float mx[4];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            mx[j] = fmax3(x[j], x[j + 8], x[j + 16]);
+          for (int j = 0; j < 4; ++j) {
+            mx[j] = fmax3(x[j], x[j + 4], x[j + 8]);
 #pragma unroll
-            for (int k = 3; k < 15; k += 2) mx[j] = fmax3(mx[j], x[j + 8 * k], x[j + 8 * k + 8]);
-            mx[j] = fmaxf(mx[j], x[j + 120]);
+            for (int k = 3; k < 15; k += 2) mx[j] = fmax3(mx[j], x[j + 4 * k], x[j + 4 * k + 4]);
+            mx[j] = fmaxf(mx[j], x[j + 60]);
           }
-          const float smax =
-              fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
-              a.scale_log2;
+          const float hmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          xchg[(par_t * 2 + c) * BM + r] = hmax;
+          named_sync(bar_group, kGroupThreads);  // S_h is read by both halves before P overwrites it
+          const float smax = fmaxf(hmax, xchg[(par_t * 2 + (c ^ 1)) * BM + r]) * a.scale_log2;
           float alpha = 1.0f;
           bool rescale = false;
           if (smax != -INFINITY) {
@@ -887,46 +907,49 @@ __global__ void __launch_bounds__(kThreads, 1)
               rescale = true;
             }
           }
+          if (!ok) {
+            mbar_arrive(&p_full[h]);
+            continue;
+          }
           const float mref = m_run == -INFINITY ? 0.0f : m_run;
-          // P = 2^(s * scale * log2(e) - m) as bf16 pairs (column c holds keys
-          // 2c, 2c+1), written over S_h in four 16-column stores; masked
-          // scores are -inf -> 0.  The row sum adds the rounded values, so
-          // that O / l weights V exactly as the P V product did (with the
-          // unrounded sum the rounding of a dominant P biases the output by
-          // up to 2^-9 of its V row).  Exponent arguments and sums take two
-          // lanes per instruction.
+          // P = 2^(s * scale * log2(e) - m) as bf16 pairs (column j holds keys
+          // 2j, 2j+1): this half's 32 columns, written over S_h; masked scores
+          // are -inf -> 0.  The row sum adds the rounded values, so that O / l
+          // weights V exactly as the P V product did (with the unrounded sum
+          // the rounding of a dominant P biases the output by up to 2^-9 of
+          // its V row).  Exponent arguments and sums take two lanes per
+          // instruction.
           const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
           const float2 nm2 = make_float2(-mref, -mref);
           float2 lacc = make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q2 = 0; q2 < 2; ++q2) {
             uint32_t pk[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-              const float2 e = fma2(make_float2(x[32 * q4 + 2 * k], x[32 * q4 + 2 * k + 1]), sc2, nm2);
-              const float2 pp = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-              const uint32_t pb = pack_bf16x2(pp.x, pp.y);
+              const float2 e = fma2(make_float2(x[32 * q2 + 2 * k], x[32 * q2 + 2 * k + 1]), sc2, nm2);
+              const uint32_t pb = pack_bf16x2(ex2_approx(e.x), ex2_approx(e.y));
               pk[k] = pb;
               lacc = add2(lacc, make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
             }
-            tmem_st16(tmem_s + 16 * q4 + lane_off, pk);
+            tmem_st16(tmem_s + 32 * c + 16 * q2 + lane_off, pk);
           }
-          const float lsum = lacc.x + lacc.y;
           if (__any_sync(0xffffffffu, rescale)) {
             // O holds P(..t-1) V against the old max; P_h(t-1) V is complete
-            // (S_h(t), which this thread has seen complete, was issued after it)
+            // (S_h(t), which this thread has seen complete, was issued after
+            // it).  This thread rescales its half of the O columns.
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < kHalfD; c0 += 32) {
               uint32_t o[32];
-              tmem_ld32(tmem_o + c0 + lane_off, o);
+              tmem_ld32(tmem_o + c * kHalfD + c0 + lane_off, o);
               tmem_ld_wait();
 #pragma unroll
               for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st32(tmem_o + c0 + lane_off, o);
+              tmem_st32(tmem_o + c * kHalfD + c0 + lane_off, o);
             }
-            l_run *= alpha;  // (this tile's sum is added below, against the new max)
+            l_half *= alpha;  // (this tile's sum is added below, against the new max)
           }
-          l_run += lsum;
+          l_half += lacc.x + lacc.y;
           // keys past the prefix end in this tile: clear their V rows (page
           // tails may hold stale data; P is 0 there but 0 * NaN would poison
           // O).  Group 0 does it before P_0(t) V(t), the tile's first reader.
@@ -934,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int st = gt % kStages;
             mbar_wait(&vfull[st], (gt / kStages) & 1, abort_flag);  // acquire the TMA writes
             uint8_t* vtile = smem + Ly::kVRing + st * Ly::kTileBytes;
-            for (int idx = r; idx < (BN - valid_keys) * Ly::kHalves; idx += BM) {
+            for (int idx = gid; idx < (BN - valid_keys) * Ly::kHalves; idx += kGroupThreads) {
               const int row = valid_keys + idx / Ly::kHalves, hf = idx % Ly::kHalves;
               uint4* pz = reinterpret_cast<uint4*>(vtile + (row >> 3) * Ly::kGroupBytes + hf * 1024 +
                                                    (row & 7) * 128);
@@ -958,65 +981,70 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ++my_pieces;
+        // the row sum: both halves' parts (the same order in both threads)
+        xchg[c * BM + r] = l_half;
+        named_sync(bar_group, kGroupThreads);
+        const float l_row = xchg[r] + xchg[BM + r];
+        named_sync(bar_group, kGroupThreads);  // the slots are reused by the next piece
         const bool bad = tree_bad || piece_bad[p] != 0;
         tc_fence_after();
         if (pc.slot < 0) {
-          // the whole unit: normalise and write
-          const float inv_l = (l_run > 0.0f && !bad) ? 1.0f / l_run : 0.0f;
+          // the whole unit: normalise and write this half of the row
+          const float inv_l = (l_row > 0.0f && !bad) ? 1.0f / l_row : 0.0f;
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < kHalfD; c0 += 32) {
             uint32_t o[32];
 #pragma unroll
             for (int k = 0; k < 32; ++k) o[k] = 0u;
             if (done) {
-              tmem_ld32(tmem_o + c0 + lane_off, o);
+              tmem_ld32(tmem_o + c * kHalfD + c0 + lane_off, o);
               tmem_ld_wait();
             }
             float v[32];
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv_l;
-            if (live && done) store_row_chunk<D>(a, out_row, c0, v);
+            if (live && done) store_row_chunk<D>(a, out_row, c * kHalfD + c0, v);
           }
         } else {
           // a piece of a split unit.  Every piece takes a ticket; all but
           // the last write raw O and (m, l) to their slot and then count
           // themselves done; the last waits until the others are done and
           // merges every piece of the unit, its own from TMEM.
-          const int nthr = pc.nm * BM;
+          const int nthr = pc.nm * kGroupThreads;
           const int bar = pc.nm == 2 ? kBarPair : kBarGroup0;
           int* ticket = a.counters + 2 * pc.cnt;
           int* finished = ticket + 1;
           named_sync(bar, nthr);
-          if (ur == 0) misc->merge = atomicAdd(ticket, 1) == pc.npieces - 1;
+          if (ur == 0 && c == 0) misc->merge = atomicAdd(ticket, 1) == pc.npieces - 1;
           named_sync(bar, nthr);
           const bool last = misc->merge != 0;
           if (!last) {
             uint8_t* sl = a.slots + static_cast<size_t>(pc.slot) * Sl::kBytes;
             float4* so4 = reinterpret_cast<float4*>(sl + Sl::kO) + ur;
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < kHalfD; c0 += 32) {
               uint32_t o[32];
 #pragma unroll
               for (int k = 0; k < 32; ++k) o[k] = 0u;
               if (done) {
-                tmem_ld32(tmem_o + c0 + lane_off, o);
+                tmem_ld32(tmem_o + c * kHalfD + c0 + lane_off, o);
                 tmem_ld_wait();
               }
               if (live) {
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                  so4[(c0 / 4 + k) * kUnitRows] =
+                  so4[((c * kHalfD + c0) / 4 + k) * kUnitRows] =
                       make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
                                   __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
               }
             }
-            if (live) reinterpret_cast<float2*>(sl + Sl::kMl)[ur] = make_float2(m_run, l_run);
-            if (ur == 0) *reinterpret_cast<int*>(sl + Sl::kFlag) = (bad || !done) ? 1 : 0;
+            if (live && c == 0) reinterpret_cast<float2*>(sl + Sl::kMl)[ur] = make_float2(m_run, l_row);
+            if (ur == 0 && c == 0) *reinterpret_cast<int*>(sl + Sl::kFlag) = (bad || !done) ? 1 : 0;
             __threadfence();
             named_sync(bar, nthr);
-            if (ur == 0) atomicAdd(finished, 1);
+            if (ur == 0 && c == 0) atomicAdd(finished, 1);
           } else {
-            if (ur == 0) {
+            if (ur == 0 && c == 0) {
               // the other pieces hold tickets, so they are running; each
               // only has its slot write left
               const unsigned long long t0 = global_ns();
@@ -1031,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(bar, nthr);
             __threadfence();
             merge_unit<D>(a, pc, ur, out_row, static_cast<int>(blockIdx.x) / a.lanes - pc.vfirst,
-                          m_run, l_run, bad || !done, tmem_o + lane_off);
+                          m_run, l_row, bad || !done, tmem_o + lane_off, c * kHalfD, kHalfD);
           }
           named_sync(bar, nthr);  // misc->merge is rewritten by the next split piece
         }
