@@ -33,23 +33,22 @@
 // workspace slot, and the last piece to finish (an arrival counter per unit)
 // merges the slots in a fixed order, so results do not depend on timing.
 //
-// One CTA has 640 threads:
-//   warp 16 (TMA)      loads K and V tiles into two shared-memory rings: one 5-D
+// One CTA has 320 threads:
+//   warp 8  (TMA)      loads K and V tiles into two shared-memory rings: one 5-D
 //                      box per 16-token page through the block table (eight
 //                      pages per tile and tensor), or 16 boxes of 8 tree nodes;
 //                      pages past the sequence load as zeros (out of bounds).
-//   warp 17 (MMA)      one thread issues tcgen05.mma for both m-tiles h:
-//                      S_h = Q_h K^T into TMEM (Q_h and K from shared memory),
-//                      O_h += P_h V with P_h read from TMEM, in the order
-//                      PV_0(t), S_0(t+1), PV_1(t), S_1(t+1).  P_h(t) is written
-//                      over the columns of S_h(t); the tensor pipe runs the
-//                      MMAs of one thread in order, so S_h(t+1) overwrites them
-//                      only after PV_h(t) has read them.  While one m-tile's
-//                      softmax runs, the tensor pipe works on the other's.
-//   warps 0-7, 8-15    the softmax of m-tile 0 and of m-tile 1, two threads per
-//                      row (64 keys each; the halves of a row exchange their
-//                      maxima through shared memory): tcgen05.ld of S, the
-//                      tree mask from a per-row
+//   warp 9  (MMA)      one thread issues tcgen05.mma for both m-tiles h from
+//                      two in-order streams, whichever is ready first:
+//                      S_h(t) = Q_h K(t)^T (Q_h and K from shared memory) into
+//                      the one TMEM score buffer the two m-tiles take turns
+//                      in (S_0(t), S_1(t), S_0(t+1), ...; the buffer is free
+//                      as soon as the softmax has loaded it), and
+//                      O_h += P_h(t) V(t) with P_h read from its own TMEM
+//                      columns.  So the next S runs while a softmax computes,
+//                      and P V while the next softmax runs.
+//   warps 0-3, 4-7     the softmax of m-tile 0 and of m-tile 1, one thread per
+//                      row: tcgen05.ld of S, the tree mask from a per-row
 //                      ancestor bitmask, the row max, fp32 online softmax in
 //                      base 2 against a running max that moves only when it
 //                      grows by more than 2^8 (O is then rescaled in TMEM), and
@@ -58,8 +57,7 @@
 //                      They also load Q (cp.async, in the 128-byte swizzled
 //                      layout the MMA reads), build the ancestor masks and
 //                      write or merge the results.
-//   warps 18-19        no work (the block size keeps 96 registers a thread).
-// TMEM (512 columns): S_0/P_0 at 0, S_1/P_1 at 128, O_0 at 256, O_1 at 256+D.
+// TMEM (512 columns): S at 0, P_0 at 128, P_1 at 192, O_0 at 256, O_1 at 256+D.
 // Every wait on an mbarrier is bounded; on expiry the CTA reports
 // TV_ERR_DEVICE_TIMEOUT for its sequence, drains its copies and returns.
 #include <climits>
@@ -73,12 +71,10 @@ namespace {
 constexpr int BM = 128;               // rows of one m-tile
 constexpr int BN = 128;               // keys per tile
 constexpr int kUnitRows = 2 * BM;     // rows of one m-tile pair
-constexpr int kGroupThreads = 256;    // softmax threads of one m-tile: two per row
-constexpr int kSoftmaxThreads = 512;  // warps 0-15: two groups of eight warps
-constexpr int kSoftmaxWarps = kSoftmaxThreads / 32;
-constexpr int kTmaWarp = 16;
-constexpr int kMmaWarp = 17;          // issues every MMA; owns the TMEM allocation
-constexpr int kThreads = 640;         // warps 18-19: no work (96 registers a thread)
+constexpr int kSoftmaxThreads = 256;  // warps 0-7: two groups of four warps
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;           // issues every MMA; owns the TMEM allocation
+constexpr int kThreads = 320;
 constexpr int kMaxNodes = 512;
 constexpr int kMaxAncWords = kMaxNodes / 32;
 constexpr int kAncStride = kMaxAncWords + 1;  // odd word stride: rows of a warp hit distinct banks
@@ -120,19 +116,16 @@ struct Layout {
   static constexpr int kParentBytes = 2 * kMaxNodes * 4;
   static constexpr int kPieces = kParent + kParentBytes;
   static constexpr int kPiecesBytes = kMaxPieces * static_cast<int>(sizeof(Piece));
-  static constexpr int kScan = kPieces + kPiecesBytes;        // 16 warp sums
+  static constexpr int kScan = kPieces + kPiecesBytes;        // 8 warp sums (int64)
   static constexpr int kScanBytes = 128;
-  // half-row maxima of the two key halves, by tile parity: [2 m-tiles][2][2 halves][128]
-  static constexpr int kXchg = kScan + kScanBytes;
-  static constexpr int kXchgBytes = 2 * 2 * 2 * BM * 4;
   // block ids of the pages of the last 8 K tiles issued (8 per tile), reused
   // by the V copies of the same tiles
-  static constexpr int kBlk = kXchg + kXchgBytes;
+  static constexpr int kBlk = kScan + kScanBytes;
   static constexpr int kBlkBytes = 8 * 8 * 4;
   static constexpr int kBar = kBlk + kBlkBytes;
-  // kfull[S], kempty[S], vfull[S], vempty[S], s_full[2], p_full[2],
-  // o_done[2], q_full[2], drain
-  static constexpr int kNumBars = 4 * kStages + 9;
+  // kfull[S], kempty[S], vfull[S], vempty[S], s_full[2], s_free[2],
+  // p_full[2], p_free[2], q_full[2], drain
+  static constexpr int kNumBars = 4 * kStages + 11;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kMiscBytes = 512;
   static constexpr int kTotal = kMisc + kMiscBytes;
@@ -208,7 +201,7 @@ __device__ __forceinline__ SeqInfo seq_info(const AttnArgs& a, int b) {
   return s;
 }
 
-// Exclusive scan over the 512 softmax threads; *total = the sum.
+// Exclusive scan over the 256 softmax threads; *total = the sum.
 __device__ __forceinline__ int scan256(int v, int* scratch, int sid, int* total) {
   const int lane = sid & 31, w = sid >> 5;
   int x = v;
@@ -221,7 +214,7 @@ __device__ __forceinline__ int scan256(int v, int* scratch, int sid, int* total)
   named_sync(kBarPair, kSoftmaxThreads);
   int before = 0, all = 0;
 #pragma unroll
-  for (int k = 0; k < kSoftmaxWarps; ++k) {
+  for (int k = 0; k < 8; ++k) {
     const int s = scratch[k];
     if (k < w) before += s;
     all += s;
@@ -249,7 +242,7 @@ struct Line {
 };
 
 // Builds this CTA's pieces of scheduling round `round` into shared memory
-// (run by the 512 softmax threads).  In round 0 it also zeroes the output of
+// (run by the 256 softmax threads).  In round 0 it also zeroes the output of
 // sequences whose extent is malformed (every row it can address) and records
 // their status.
 template <int D>
@@ -260,7 +253,7 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
   int* scratch = reinterpret_cast<int*>(smem + Ly::kScan);
   const size_t out_elem = a.out_fp32 ? 4 : 2;
   // the length of the line; malformed sequences of this CTA (b mod grid).  A
-  // batch of at most 512 is read once and kept in registers for the second
+  // batch of at most 256 is read once and kept in registers for the second
   // pass.
   const bool one_chunk = a.batch <= kSoftmaxThreads;
   SeqInfo kept;
@@ -412,15 +405,14 @@ __device__ __forceinline__ int piece_slot(const AttnArgs& a, const Piece& pc, in
 }
 
 // Merges the pieces of a split unit: O = sum_s 2^(m_s - M) O_s /
-// sum_s 2^(m_s - M) l_s in piece order.  A thread takes columns [col0,
-// col0 + ncols) of row ur of the unit.  Piece `own` is this CTA's: its (m, l)
-// and O come from registers and TMEM (the values it would have written), the
-// others' from their slots; the lanes of a warp read consecutive rows
-// (coalesced), a 32-column chunk of every piece in flight at a time.
+// sum_s 2^(m_s - M) l_s in piece order.  Thread `ur` of the participants
+// takes row ur of the unit.  Piece `own` is this CTA's: its (m, l) and O come
+// from registers and TMEM (the values it would have written), the others'
+// from their slots; the lanes of a warp read consecutive rows (coalesced),
+// a 32-column chunk of every piece in flight at a time.
 template <int D>
 __device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t out_row, int own,
-                           float m_own, float l_own, bool bad_own, uint32_t tmem_o, int col0,
-                           int ncols) {
+                           float m_own, float l_own, bool bad_own, uint32_t tmem_o) {
   using Sl = Slot<D>;
   const bool row_ok = ur < pc.rows;
   bool bad = bad_own;
@@ -441,7 +433,7 @@ __device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t ou
   }
   const float inv = (l > 0.0f && !bad) ? 1.0f / l : 0.0f;
 #pragma unroll 1
-  for (int c0 = col0; c0 < col0 + ncols; c0 += 32) {
+  for (int c0 = 0; c0 < D; c0 += 32) {
     float acc[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) acc[k] = 0.0f;
@@ -493,10 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kempty = bars + kStages;
   uint64_t* vfull = bars + 2 * kStages;
   uint64_t* vempty = bars + 3 * kStages;
-  uint64_t* s_full = bars + 4 * kStages;  // [2]: S_h(t) complete (and every MMA before it)
-  uint64_t* p_full = s_full + 2;          // [2]: P_h(t) in TMEM (256 arrivals)
-  uint64_t* o_done = p_full + 2;          // [2]: the last P_h V of a piece complete
-  uint64_t* q_full = o_done + 2;          // [2]: Q_h of a piece in shared memory (256 arrivals)
+  uint64_t* s_full = bars + 4 * kStages;  // [2]: S_h(t) in the score buffer (and every MMA before it)
+  uint64_t* s_free = s_full + 2;          // [2]: group h has loaded its S (128 arrivals)
+  uint64_t* p_full = s_free + 2;          // [2]: P_h(t) in TMEM (128 arrivals)
+  uint64_t* p_free = p_full + 2;          // [2]: P_h(t) V complete (P_h and O_h may be rewritten)
+  uint64_t* q_full = p_free + 2;          // [2]: Q_h of a piece in shared memory (128 arrivals)
   uint64_t* drain = q_full + 2;           // every MMA issued so far complete (once per round)
   Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
   Piece* pieces = reinterpret_cast<Piece*>(smem + Ly::kPieces);
@@ -516,9 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(&s_full[h], 1);
-      mbar_init(&p_full[h], kGroupThreads);
-      mbar_init(&o_done[h], 1);
-      mbar_init(&q_full[h], kGroupThreads);
+      mbar_init(&s_free[h], BM);
+      mbar_init(&p_full[h], BM);
+      mbar_init(&p_free[h], 1);
+      mbar_init(&q_full[h], BM);
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -539,9 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // pieces of m-tile h so far (MMA: both m-tiles; softmax: its own).
   int g_tile = 0;
   int tiles_h0 = 0, tiles_h1 = 0, pieces_h0 = 0, pieces_h1 = 0;
+  int last_s_group = -1;  // MMA: the m-tile of the last S issued (its buffer turn)
 
   for (int round = 0;; ++round) {
-    if (warp < kSoftmaxWarps) build_schedule<D>(a, smem, round, tid);
+    if (warp < kTmaWarp) build_schedule<D>(a, smem, round, tid);
     __syncthreads();
     const int npieces = misc->npieces;
     const bool more = misc->more != 0;
@@ -664,6 +659,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == kMmaWarp) {
       // ------------------------------------------------------ MMA issuer
+      // Two streams in piece, tile and m-tile order: S_h(t) once K(t) has
+      // landed, Q_h of the piece is loaded and the previous S has been
+      // loaded out of the score buffer; P_h(t) V(t) once P_h(t) is in TMEM
+      // and V(t) has landed.  The thread issues whichever is ready, so
+      // neither stream waits behind the other.
       if (lane == 0) {
         constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);  // M=128, N=128, K-major K
         constexpr uint32_t idesc_o = idesc_bf16(BM, D, 1);   // M=128, N=D, MN-major V
@@ -674,13 +674,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dk0 = smem_desc(smem_u32(smem + Ly::kKRing), 16, Ly::kGroupBytes);
         const uint64_t dv0 = smem_desc(smem_u32(smem + Ly::kVRing), 1024, Ly::kGroupBytes);
         const uint64_t dq0 = smem_desc(smem_u32(smem + Ly::kQ), 16, Ly::kGroupBytes);
-        auto issue_s = [&](int h, int t) {  // S_h = Q_h K(t)^T into columns 128 h
+        auto issue_s = [&](int h, int t) {  // S = Q_h K(t)^T into the score buffer
           const uint64_t dk = dk0 + static_cast<uint64_t>((t % kStages) * (Ly::kTileBytes >> 4));
           const uint64_t dq = dq0 + static_cast<uint64_t>(h * (Ly::kQBytes >> 4));
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
-            mma_bf16_ss(tmem + h * BN, dq + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem, dq + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(&s_full[h]);
         };
@@ -688,57 +688,81 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t dv = dv0 + static_cast<uint64_t>((t % kStages) * (Ly::kTileBytes >> 4));
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_bf16_ts(tmem + 256 + h * D, tmem + h * BN + kk * 8,
+            mma_bf16_ts(tmem + 256 + h * D, tmem + 128 + 64 * h + kk * 8,
                         dv + ((kk * 2 * Ly::kGroupBytes) >> 4), idesc_o, (acc || kk > 0) ? 1u : 0u);
+          mma_commit(&p_free[h]);
         };
+        // S stream: piece sp, tile si of the piece, m-tile sh, global tile s_tau
+        int sp = 0, si = 0, sh = 0, s_tau = g_tile;
+        // P V stream
+        int vp = 0, vi = 0, vh = 0, v_tau = g_tile;
+        int s_cnt[2] = {tiles_h0, tiles_h1};    // S_h issued so far
+        int pv_cnt[2] = {tiles_h0, tiles_h1};   // P_h V issued so far
+        int q_cnt[2] = {pieces_h0, pieces_h1};  // pieces whose Q_h was taken
         bool ok = true;
-        int tau = g_tile;
-        for (int p = 0; p < npieces && ok; ++p) {
-          const Piece& pc = pieces[p];
-          const int nm = pc.nm, T = pc.t1 - pc.t0;
-          // the piece's first S of each m-tile, once its Q is loaded and K has landed
-          for (int h = 0; h < nm && ok; ++h) {
-            ok = mbar_wait(&q_full[h], (h ? pieces_h1 : pieces_h0) & 1, abort_flag);
-            if (ok && h == 0) ok = mbar_wait(&kfull[tau % kStages], (tau / kStages) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(h, tau);
-          }
-          if (!ok) break;
-          mma_commit(&kempty[tau % kStages]);
-          for (int i = 0; i < T && ok; ++i) {
-            const int t = tau + i;
-            for (int h = 0; h < nm; ++h) {
-              ok = mbar_wait(&p_full[h], (h ? tiles_h1 : tiles_h0) & 1, abort_flag);
-              if (ok && h == 0) ok = mbar_wait(&vfull[t % kStages], (t / kStages) & 1, abort_flag);
-              if (!ok) break;
+        unsigned long long t_idle = 0;
+        while (vp < npieces) {
+          bool progressed = false;
+          if (sp < npieces) {
+            const Piece& pc = pieces[sp];
+            bool ready = true;
+            if (si == 0) ready = mbar_test_wait(&q_full[sh], q_cnt[sh] & 1);
+            if (ready && last_s_group >= 0)
+              ready = mbar_test_wait(&s_free[last_s_group], (s_cnt[last_s_group] - 1) & 1);
+            if (ready && sh == 0) ready = mbar_test_wait(&kfull[s_tau % kStages], (s_tau / kStages) & 1);
+            if (ready) {
               tc_fence_after();
-              issue_pv(h, t, i > 0);
-              if (i + 1 < T) {
-                if (h == 0) {
-                  ok = mbar_wait(&kfull[(t + 1) % kStages], ((t + 1) / kStages) & 1, abort_flag);
-                  if (!ok) break;
-                  tc_fence_after();
+              issue_s(sh, s_tau);
+              if (si == 0) ++q_cnt[sh];
+              ++s_cnt[sh];
+              last_s_group = sh;
+              if (sh == pc.nm - 1) mma_commit(&kempty[s_tau % kStages]);  // the tile's last S
+              if (++sh == pc.nm) {
+                sh = 0;
+                ++s_tau;
+                if (++si == pc.t1 - pc.t0) {
+                  si = 0;
+                  ++sp;
                 }
-                issue_s(h, t + 1);
               }
-              if (h) ++tiles_h1; else ++tiles_h0;
+              progressed = true;
             }
-            if (!ok) break;
-            mma_commit(&vempty[t % kStages]);
-            if (i + 1 < T) mma_commit(&kempty[(t + 1) % kStages]);
           }
-          if (!ok) break;
-          mma_commit(&o_done[0]);
-          ++pieces_h0;
-          if (nm == 2) {
-            mma_commit(&o_done[1]);
-            ++pieces_h1;
+          {
+            const Piece& pc = pieces[vp];
+            bool ready = mbar_test_wait(&p_full[vh], pv_cnt[vh] & 1);
+            if (ready && vh == 0) ready = mbar_test_wait(&vfull[v_tau % kStages], (v_tau / kStages) & 1);
+            if (ready) {
+              tc_fence_after();
+              issue_pv(vh, v_tau, vi > 0);
+              ++pv_cnt[vh];
+              if (vh == pc.nm - 1) mma_commit(&vempty[v_tau % kStages]);  // the tile's last P V
+              if (++vh == pc.nm) {
+                vh = 0;
+                ++v_tau;
+                if (++vi == pc.t1 - pc.t0) {
+                  vi = 0;
+                  ++vp;
+                }
+              }
+              progressed = true;
+            }
           }
-          tau += T;
+          if (progressed) {
+            t_idle = 0;
+          } else if (t_idle == 0) {
+            t_idle = global_ns();
+          } else if (global_ns() - t_idle > kWaitLimitNs || *abort_flag) {
+            ok = false;
+            break;
+          }
         }
+        tiles_h0 = pv_cnt[0];
+        tiles_h1 = pv_cnt[1];
+        pieces_h0 = q_cnt[0];
+        pieces_h1 = q_cnt[1];
         if (!ok) {
-          record_status(a.status, pieces[0].b, kDeviceTimeout);
+          record_status(a.status, pieces[min(vp, npieces - 1)].b, kDeviceTimeout);
           misc->abort = 1;
         }
         // every MMA issued so far completes before the next round or the exit
@@ -746,23 +770,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(drain, round & 1);
       }
       __syncwarp();
-    } else if (warp < kSoftmaxWarps) {
+    } else {
       // ------------------------------------------------------ softmax groups
-      // Warps 8h .. 8h+7 own m-tile h.  Warp w reads TMEM lane quarter
-      // 32 (w % 4) .. +31 (its rows) and takes key half c = (w / 4) % 2 of
-      // each tile (64 keys) and column half c of O, so the two threads of a
-      // row are in warps w and w ^ 4.
-      const int h = warp >> 3;
-      const int c = (warp >> 2) & 1;
-      const int r = (warp & 3) * 32 + lane;   // row of the m-tile == TMEM lane
-      const int gid = c * BM + r;             // thread of the group (0 .. 255)
-      constexpr int kHalfD = D / 2;           // O columns of this thread
+      // Warps 4h .. 4h+3 own m-tile h; warp w's rows are its TMEM lane
+      // quarter 32 (w % 4) .. +31.
+      const int h = warp >> 2;
+      const int r = (warp & 3) * 32 + lane;  // row of the m-tile == TMEM lane
       const uint32_t lane_off = lane_off_q(warp);
-      const uint32_t tmem_s = tmem + h * BN;
+      const uint32_t tmem_p = tmem + 128 + 64 * h;  // P_h: 128 keys as bf16 pairs
       const uint32_t tmem_o = tmem + 256 + h * D;
       uint32_t* anc = reinterpret_cast<uint32_t*>(smem + Ly::kAnc) + (h * BM + r) * kAncStride;
       int32_t* par = reinterpret_cast<int32_t*>(smem + Ly::kParent) + h * kMaxNodes;
-      float* xchg = reinterpret_cast<float*>(smem + Ly::kXchg) + h * (2 * 2 * BM);  // [parity][half][row]
       uint8_t* qh = smem + Ly::kQ + h * Ly::kQBytes;
       volatile int* piece_bad = misc->piece_bad;
       int my_tiles = h ? tiles_h1 : tiles_h0;
@@ -770,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int tau = g_tile;  // global index of the piece's first tile
       for (int p = 0; p < npieces; ++p) {
-        const Piece& pc = pieces[p];  // fields are read from shared memory as needed
+        const Piece pc = pieces[p];
         const int T = pc.t1 - pc.t0;
         if (h >= pc.nm) {  // this m-tile has no rows in the unit
           tau += T;
@@ -782,23 +800,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool live = ur < pc.rows;
         const int i_node = live ? R / g : 0;
         const size_t out_row = static_cast<size_t>(pc.n0 + i_node) * a.hq + pc.kvh * g + R % g;
-        // Q: this thread's half of its row -> shared memory in the 128-byte
-        // swizzled K-major layout (16-byte chunk k of row r at chunk
-        // k ^ (r % 8) of its 128-byte line); rows past the unit are zero.
-        // The buffer is free: the previous piece's last S_h completed before
-        // its epilogue.
+        // Q rows -> shared memory in the 128-byte swizzled K-major layout
+        // (the 16-byte chunk c of row r sits at chunk c ^ (r % 8)); rows past
+        // the unit are zero.  The buffer is free: the previous piece's last
+        // S_h completed before its epilogue.
         {
-          constexpr int kChunks = D / 16;  // 16-byte chunks of half a row
           uint8_t* dst = qh + (r >> 3) * Ly::kGroupBytes + (r & 7) * 128;
-          const uint16_t* src = a.q + out_row * D;
+          if (live) {
+            const uint16_t* src = a.q + out_row * D;
 #pragma unroll
-          for (int k = c * kChunks; k < (c + 1) * kChunks; ++k) {
-            uint8_t* d = dst + (k >> 3) * 1024 + (((k & 7) ^ (r & 7)) << 4);
-            if (live) {
-              cpa16(d, src + k * 8);
-            } else {
-              *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
-            }
+            for (int hf = 0; hf < Ly::kHalves; ++hf)
+#pragma unroll
+              for (int c = 0; c < 8; ++c) cpa16(dst + hf * 1024 + ((c ^ (r & 7)) << 4), src + hf * 64 + c * 8);
+          } else {
+#pragma unroll
+            for (int hf = 0; hf < Ly::kHalves; ++hf)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(dst + hf * 1024 + c * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         // the next piece's Q row of this thread into L2, so that its load
@@ -808,94 +827,91 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nr = nx.mp * kUnitRows + ur;
           if (ur < nx.rows) {
             const uint16_t* q = a.q + (static_cast<size_t>(nx.n0 + nr / g) * a.hq + nx.kvh * g + nr % g) * D;
-            prefetch_l2(reinterpret_cast<const uint8_t*>(q) + c * D);
+#pragma unroll
+            for (int k = 0; k < D * 2; k += 128) prefetch_l2(reinterpret_cast<const uint8_t*>(q) + k);
           }
         }
         // the tree of the sequence (pieces with node tiles): parents, the
-        // check 0 <= parent[i] < i (parent[0] = -1), and the row's
-        // ancestor-or-self bitmask (built by the thread of key half 0)
+        // check 0 <= parent[i] < i (parent[0] = -1), and this row's
+        // ancestor-or-self bitmask
         const bool has_nodes = pc.t1 > pc.P;
         bool tree_bad = false;
         if (has_nodes) {
-          if (gid == 0) misc->tree_bad[h] = 0;
-          named_sync(bar_group, kGroupThreads);
-          for (int k = gid; k < pc.N; k += kGroupThreads) {
+          if (r == 0) misc->tree_bad[h] = 0;
+          named_sync(bar_group, BM);
+          for (int k = r; k < pc.N; k += BM) {
             const int q = __ldg(a.parent + pc.n0 + k);
             par[k] = q;
             if (!(k == 0 ? q == -1 : (q >= 0 && q < k))) misc->tree_bad[h] = 1;
           }
-          named_sync(bar_group, kGroupThreads);
+          named_sync(bar_group, BM);
           tree_bad = misc->tree_bad[h] != 0;
-          if (c == 0) {
 #pragma unroll
-            for (int k = 0; k < kMaxAncWords; ++k) anc[k] = 0u;
-            if (!tree_bad && live)
-              for (int k = i_node; k >= 0; k = par[k]) anc[k >> 5] |= 1u << (k & 31);
-          }
-          if (tree_bad && gid == 0) record_status(a.status, pc.b, kBadTree);
-          named_sync(bar_group, kGroupThreads);  // masks complete; tree_bad is reset by the next piece
+          for (int k = 0; k < kMaxAncWords; ++k) anc[k] = 0u;
+          if (!tree_bad && live)
+            for (int k = i_node; k >= 0; k = par[k]) anc[k >> 5] |= 1u << (k & 31);
+          if (tree_bad && r == 0) record_status(a.status, pc.b, kBadTree);
+          named_sync(bar_group, BM);  // tree_bad is reset by the next piece
         }
         cpa_wait_all();
         fence_proxy_async_smem();  // generic writes of Q, read by the MMA
         mbar_arrive(&q_full[h]);
 
-        float m_run = -INFINITY;  // running max (log2 units), the same in both halves
-        float l_half = 0.0f;      // this half's row sum against m_run
+        float m_run = -INFINITY;  // running max (log2 units)
+        float l_run = 0.0f;       // row sum against m_run
         for (int i = 0; i < T; ++i) {
           const int t = pc.t0 + i;  // tile of the unit
           const int gt = tau + i;   // global tile (ring slot)
-          const int par_t = my_tiles & 1;
+          const int k = my_tiles++;  // this tile's index in the m-tile's sequence
           if (ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[h], par_t, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[h], k & 1, abort_flag));
             if (!ok) misc->abort = 1;
           }
-          ++my_tiles;
-          // this half's 64 scores of the tile
-          float x[64];
-          if (ok) {
-            tc_fence_after();
-            tmem_ld32(tmem_s + 64 * c + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-            tmem_ld32(tmem_s + 64 * c + 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int k = 0; k < 64; ++k) x[k] = -INFINITY;
+          if (!ok) {
+            mbar_arrive(&s_free[h]);
+            mbar_arrive(&p_full[h]);
+            continue;
           }
+          float x[128];
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tmem_ld32(tmem + 32 * c + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&s_free[h]);  // the score buffer may take the next S
           // mask (scores stay unscaled; the scale is folded into the exponent)
           int valid_keys = BN;
           if (t < pc.P) {
             valid_keys = min(BN, pc.L - t * BN);
-            const int v_half = valid_keys - 64 * c;  // valid keys of this half
-            if (v_half < 64) {
+            if (valid_keys < BN) {
 #pragma unroll
-              for (int k = 0; k < 64; ++k)
-                if (k >= v_half) x[k] = -INFINITY;
+              for (int c = 0; c < 128; ++c)
+                if (c >= valid_keys) x[c] = -INFINITY;
             }
           } else {
             // only ancestors-or-self of this node carry a bit, all of them
             // < N, so node columns past the tree are masked as well
-            const int j0 = (t - pc.P) * BN + 64 * c;
+            const int j0 = (t - pc.P) * BN;
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
+            for (int k = 0; k < 4; ++k) {
               const uint32_t bits = live ? anc[(j0 >> 5) + k] : 0u;
 #pragma unroll
-              for (int b = 0; b < 32; ++b) x[32 * k + b] = (bits & (1u << b)) ? x[32 * k + b] : -INFINITY;
+              for (int c = 0; c < 32; ++c) x[32 * k + c] = (bits & (1u << c)) ? x[32 * k + c] : -INFINITY;
             }
           }
-          // max of this half: four running three-input maxima, then the
-          // row's max with the other half through shared memory
-          float mx[4];
+          // max of the 128 scores: eight running three-input maxima
+          float mx[8];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            mx[j] = fmax3(x[j], x[j + 4], x[j + 8]);
+          for (int j = 0; j < 8; ++j) {
+            mx[j] = fmax3(x[j], x[j + 8], x[j + 16]);
 #pragma unroll
-            for (int k = 3; k < 15; k += 2) mx[j] = fmax3(mx[j], x[j + 4 * k], x[j + 4 * k + 4]);
-            mx[j] = fmaxf(mx[j], x[j + 60]);
+            for (int k = 3; k < 15; k += 2) mx[j] = fmax3(mx[j], x[j + 8 * k], x[j + 8 * k + 8]);
+            mx[j] = fmaxf(mx[j], x[j + 120]);
           }
-          const float hmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-          xchg[(par_t * 2 + c) * BM + r] = hmax;
-          named_sync(bar_group, kGroupThreads);  // S_h is read by both halves before P overwrites it
-          const float smax = fmaxf(hmax, xchg[(par_t * 2 + (c ^ 1)) * BM + r]) * a.scale_log2;
+          const float smax =
+              fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+              a.scale_log2;
           float alpha = 1.0f;
           bool rescale = false;
           if (smax != -INFINITY) {
@@ -907,49 +923,55 @@ __global__ void __launch_bounds__(kThreads, 1)
               rescale = true;
             }
           }
-          if (!ok) {
-            mbar_arrive(&p_full[h]);
-            continue;
-          }
           const float mref = m_run == -INFINITY ? 0.0f : m_run;
-          // P = 2^(s * scale * log2(e) - m) as bf16 pairs (column j holds keys
-          // 2j, 2j+1): this half's 32 columns, written over S_h; masked scores
-          // are -inf -> 0.  The row sum adds the rounded values, so that O / l
-          // weights V exactly as the P V product did (with the unrounded sum
-          // the rounding of a dominant P biases the output by up to 2^-9 of
-          // its V row).  Exponent arguments and sums take two lanes per
-          // instruction.
+          // P_h(k-1) V must be complete before P_h and O_h are rewritten
+          if (k >= 1) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&p_free[h], (k - 1) & 1, abort_flag));
+            if (!ok) {
+              misc->abort = 1;
+              mbar_arrive(&p_full[h]);
+              continue;
+            }
+            tc_fence_after();
+          }
+          // P = 2^(s * scale * log2(e) - m) as bf16 pairs (column c holds keys
+          // 2c, 2c+1), into P_h in four 16-column stores; masked
+          // scores are -inf -> 0.  The row sum adds the rounded values, so
+          // that O / l weights V exactly as the P V product did (with the
+          // unrounded sum the rounding of a dominant P biases the output by
+          // up to 2^-9 of its V row).  Exponent arguments and sums take two
+          // lanes per instruction.
           const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
           const float2 nm2 = make_float2(-mref, -mref);
           float2 lacc = make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
+          for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t pk[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-              const float2 e = fma2(make_float2(x[32 * q2 + 2 * k], x[32 * q2 + 2 * k + 1]), sc2, nm2);
-              const uint32_t pb = pack_bf16x2(ex2_approx(e.x), ex2_approx(e.y));
+              const float2 e = fma2(make_float2(x[32 * q4 + 2 * k], x[32 * q4 + 2 * k + 1]), sc2, nm2);
+              const float2 pp = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+              const uint32_t pb = pack_bf16x2(pp.x, pp.y);
               pk[k] = pb;
               lacc = add2(lacc, make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
             }
-            tmem_st16(tmem_s + 32 * c + 16 * q2 + lane_off, pk);
+            tmem_st16(tmem_p + 16 * q4 + lane_off, pk);
           }
+          const float lsum = lacc.x + lacc.y;
           if (__any_sync(0xffffffffu, rescale)) {
-            // O holds P(..t-1) V against the old max; P_h(t-1) V is complete
-            // (S_h(t), which this thread has seen complete, was issued after
-            // it).  This thread rescales its half of the O columns.
+            // O holds P(..t-1) V against the old max (P_h(t-1) V is complete)
 #pragma unroll
-            for (int c0 = 0; c0 < kHalfD; c0 += 32) {
+            for (int c0 = 0; c0 < D; c0 += 32) {
               uint32_t o[32];
-              tmem_ld32(tmem_o + c * kHalfD + c0 + lane_off, o);
+              tmem_ld32(tmem_o + c0 + lane_off, o);
               tmem_ld_wait();
 #pragma unroll
               for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st32(tmem_o + c * kHalfD + c0 + lane_off, o);
+              tmem_st32(tmem_o + c0 + lane_off, o);
             }
-            l_half *= alpha;  // (this tile's sum is added below, against the new max)
+            l_run *= alpha;  // (this tile's sum is added below, against the new max)
           }
-          l_half += lacc.x + lacc.y;
+          l_run += lsum;
           // keys past the prefix end in this tile: clear their V rows (page
           // tails may hold stale data; P is 0 there but 0 * NaN would poison
           // O).  Group 0 does it before P_0(t) V(t), the tile's first reader.
@@ -957,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int st = gt % kStages;
             mbar_wait(&vfull[st], (gt / kStages) & 1, abort_flag);  // acquire the TMA writes
             uint8_t* vtile = smem + Ly::kVRing + st * Ly::kTileBytes;
-            for (int idx = gid; idx < (BN - valid_keys) * Ly::kHalves; idx += kGroupThreads) {
+            for (int idx = r; idx < (BN - valid_keys) * Ly::kHalves; idx += BM) {
               const int row = valid_keys + idx / Ly::kHalves, hf = idx % Ly::kHalves;
               uint4* pz = reinterpret_cast<uint4*>(vtile + (row >> 3) * Ly::kGroupBytes + hf * 1024 +
                                                    (row & 7) * 128);
@@ -973,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------- piece epilogue
         bool done = false;
         if (ok) {
-          done = __all_sync(0xffffffffu, mbar_wait(&o_done[h], my_pieces & 1, abort_flag));
+          done = __all_sync(0xffffffffu, mbar_wait(&p_free[h], (my_tiles - 1) & 1, abort_flag));
           if (!done) {
             ok = false;
             misc->abort = 1;
@@ -981,70 +1003,65 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ++my_pieces;
-        // the row sum: both halves' parts (the same order in both threads)
-        xchg[c * BM + r] = l_half;
-        named_sync(bar_group, kGroupThreads);
-        const float l_row = xchg[r] + xchg[BM + r];
-        named_sync(bar_group, kGroupThreads);  // the slots are reused by the next piece
         const bool bad = tree_bad || piece_bad[p] != 0;
         tc_fence_after();
         if (pc.slot < 0) {
-          // the whole unit: normalise and write this half of the row
-          const float inv_l = (l_row > 0.0f && !bad) ? 1.0f / l_row : 0.0f;
+          // the whole unit: normalise and write
+          const float inv_l = (l_run > 0.0f && !bad) ? 1.0f / l_run : 0.0f;
 #pragma unroll
-          for (int c0 = 0; c0 < kHalfD; c0 += 32) {
+          for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
 #pragma unroll
             for (int k = 0; k < 32; ++k) o[k] = 0u;
             if (done) {
-              tmem_ld32(tmem_o + c * kHalfD + c0 + lane_off, o);
+              tmem_ld32(tmem_o + c0 + lane_off, o);
               tmem_ld_wait();
             }
             float v[32];
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv_l;
-            if (live && done) store_row_chunk<D>(a, out_row, c * kHalfD + c0, v);
+            if (live && done) store_row_chunk<D>(a, out_row, c0, v);
           }
         } else {
           // a piece of a split unit.  Every piece takes a ticket; all but
           // the last write raw O and (m, l) to their slot and then count
           // themselves done; the last waits until the others are done and
           // merges every piece of the unit, its own from TMEM.
-          const int nthr = pc.nm * kGroupThreads;
+          const int nthr = pc.nm * BM;
           const int bar = pc.nm == 2 ? kBarPair : kBarGroup0;
           int* ticket = a.counters + 2 * pc.cnt;
           int* finished = ticket + 1;
           named_sync(bar, nthr);
-          if (ur == 0 && c == 0) misc->merge = atomicAdd(ticket, 1) == pc.npieces - 1;
+          if (ur == 0) misc->merge = atomicAdd(ticket, 1) == pc.npieces - 1;
           named_sync(bar, nthr);
           const bool last = misc->merge != 0;
           if (!last) {
             uint8_t* sl = a.slots + static_cast<size_t>(pc.slot) * Sl::kBytes;
             float4* so4 = reinterpret_cast<float4*>(sl + Sl::kO) + ur;
 #pragma unroll
-            for (int c0 = 0; c0 < kHalfD; c0 += 32) {
+            for (int c0 = 0; c0 < D; c0 += 32) {
               uint32_t o[32];
 #pragma unroll
               for (int k = 0; k < 32; ++k) o[k] = 0u;
               if (done) {
-                tmem_ld32(tmem_o + c * kHalfD + c0 + lane_off, o);
+                tmem_ld32(tmem_o + c0 + lane_off, o);
                 tmem_ld_wait();
               }
               if (live) {
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                  so4[((c * kHalfD + c0) / 4 + k) * kUnitRows] =
+                  so4[(c0 / 4 + k) * kUnitRows] =
                       make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
                                   __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
               }
             }
-            if (live && c == 0) reinterpret_cast<float2*>(sl + Sl::kMl)[ur] = make_float2(m_run, l_row);
-            if (ur == 0 && c == 0) *reinterpret_cast<int*>(sl + Sl::kFlag) = (bad || !done) ? 1 : 0;
+            if (live) reinterpret_cast<float2*>(sl + Sl::kMl)[ur] = make_float2(m_run, l_run);
+            if (ur == 0) *reinterpret_cast<int*>(sl + Sl::kFlag) = (bad || !done) ? 1 : 0;
             __threadfence();
             named_sync(bar, nthr);
-            if (ur == 0 && c == 0) atomicAdd(finished, 1);
+            if (ur == 0) atomicAdd(finished, 1);
           } else {
-            if (ur == 0 && c == 0) {
+            if (ur == 0) {
               // the other pieces hold tickets, so they are running; each
               // only has its slot write left
               const unsigned long long t0 = global_ns();
@@ -1059,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(bar, nthr);
             __threadfence();
             merge_unit<D>(a, pc, ur, out_row, static_cast<int>(blockIdx.x) / a.lanes - pc.vfirst,
-                          m_run, l_row, bad || !done, tmem_o + lane_off, c * kHalfD, kHalfD);
+                          m_run, l_run, bad || !done, tmem_o + lane_off);
           }
           named_sync(bar, nthr);  // misc->merge is rewritten by the next split piece
         }
