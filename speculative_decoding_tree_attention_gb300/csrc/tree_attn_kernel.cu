@@ -38,15 +38,14 @@
 //                      box per 16-token page through the block table (eight
 //                      pages per tile and tensor), or 16 boxes of 8 tree nodes;
 //                      pages past the sequence load as zeros (out of bounds).
-//   warp 9  (MMA)      one thread issues tcgen05.mma for both m-tiles h from
-//                      two in-order streams, whichever is ready first:
-//                      S_h(t) = Q_h K(t)^T (Q_h and K from shared memory) into
-//                      the one TMEM score buffer the two m-tiles take turns
-//                      in (S_0(t), S_1(t), S_0(t+1), ...; the buffer is free
-//                      as soon as the softmax has loaded it), and
-//                      O_h += P_h(t) V(t) with P_h read from its own TMEM
-//                      columns.  So the next S runs while a softmax computes,
-//                      and P V while the next softmax runs.
+//   warp 9  (MMA)      one thread issues tcgen05.mma for both m-tiles h:
+//                      S_h = Q_h K^T into TMEM (Q_h and K from shared memory),
+//                      O_h += P_h V with P_h read from TMEM, in the order
+//                      PV_0(t), S_0(t+1), PV_1(t), S_1(t+1).  P_h(t) is written
+//                      over the columns of S_h(t); the tensor pipe runs the
+//                      MMAs of one thread in order, so S_h(t+1) overwrites them
+//                      only after PV_h(t) has read them.  While one m-tile's
+//                      softmax runs, the tensor pipe works on the other's.
 //   warps 0-3, 4-7     the softmax of m-tile 0 and of m-tile 1, one thread per
 //                      row: tcgen05.ld of S, the tree mask from a per-row
 //                      ancestor bitmask, the row max, fp32 online softmax in
@@ -57,7 +56,7 @@
 //                      They also load Q (cp.async, in the 128-byte swizzled
 //                      layout the MMA reads), build the ancestor masks and
 //                      write or merge the results.
-// TMEM (512 columns): S at 0, P_0 at 128, P_1 at 192, O_0 at 256, O_1 at 256+D.
+// TMEM (512 columns): S_0/P_0 at 0, S_1/P_1 at 128, O_0 at 256, O_1 at 256+D.
 // Every wait on an mbarrier is bounded; on expiry the CTA reports
 // TV_ERR_DEVICE_TIMEOUT for its sequence, drains its copies and returns.
 #include <climits>
@@ -123,9 +122,9 @@ struct Layout {
   static constexpr int kBlk = kScan + kScanBytes;
   static constexpr int kBlkBytes = 8 * 8 * 4;
   static constexpr int kBar = kBlk + kBlkBytes;
-  // kfull[S], kempty[S], vfull[S], vempty[S], s_full[2], s_free[2],
-  // p_full[2], p_free[2], q_full[2], drain
-  static constexpr int kNumBars = 4 * kStages + 11;
+  // kfull[S], kempty[S], vfull[S], vempty[S], s_full[2], p_full[2],
+  // o_done[2], q_full[2], drain
+  static constexpr int kNumBars = 4 * kStages + 9;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kMiscBytes = 512;
   static constexpr int kTotal = kMisc + kMiscBytes;
@@ -485,11 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kempty = bars + kStages;
   uint64_t* vfull = bars + 2 * kStages;
   uint64_t* vempty = bars + 3 * kStages;
-  uint64_t* s_full = bars + 4 * kStages;  // [2]: S_h(t) in the score buffer (and every MMA before it)
-  uint64_t* s_free = s_full + 2;          // [2]: group h has loaded its S (128 arrivals)
-  uint64_t* p_full = s_free + 2;          // [2]: P_h(t) in TMEM (128 arrivals)
-  uint64_t* p_free = p_full + 2;          // [2]: P_h(t) V complete (P_h and O_h may be rewritten)
-  uint64_t* q_full = p_free + 2;          // [2]: Q_h of a piece in shared memory (128 arrivals)
+  uint64_t* s_full = bars + 4 * kStages;  // [2]: S_h(t) complete (and every MMA before it)
+  uint64_t* p_full = s_full + 2;          // [2]: P_h(t) in TMEM (128 arrivals)
+  uint64_t* o_done = p_full + 2;          // [2]: the last P_h V of a piece complete
+  uint64_t* q_full = o_done + 2;          // [2]: Q_h of a piece in shared memory (128 arrivals)
   uint64_t* drain = q_full + 2;           // every MMA issued so far complete (once per round)
   Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
   Piece* pieces = reinterpret_cast<Piece*>(smem + Ly::kPieces);
@@ -509,9 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(&s_full[h], 1);
-      mbar_init(&s_free[h], BM);
       mbar_init(&p_full[h], BM);
-      mbar_init(&p_free[h], 1);
+      mbar_init(&o_done[h], 1);
       mbar_init(&q_full[h], BM);
     }
     mbar_init(drain, 1);
@@ -533,7 +530,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // pieces of m-tile h so far (MMA: both m-tiles; softmax: its own).
   int g_tile = 0;
   int tiles_h0 = 0, tiles_h1 = 0, pieces_h0 = 0, pieces_h1 = 0;
-  int last_s_group = -1;  // MMA: the m-tile of the last S issued (its buffer turn)
 
   for (int round = 0;; ++round) {
     if (warp < kTmaWarp) build_schedule<D>(a, smem, round, tid);
@@ -659,11 +655,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == kMmaWarp) {
       // ------------------------------------------------------ MMA issuer
-      // Two streams in piece, tile and m-tile order: S_h(t) once K(t) has
-      // landed, Q_h of the piece is loaded and the previous S has been
-      // loaded out of the score buffer; P_h(t) V(t) once P_h(t) is in TMEM
-      // and V(t) has landed.  The thread issues whichever is ready, so
-      // neither stream waits behind the other.
       if (lane == 0) {
         constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);  // M=128, N=128, K-major K
         constexpr uint32_t idesc_o = idesc_bf16(BM, D, 1);   // M=128, N=D, MN-major V
@@ -674,13 +665,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dk0 = smem_desc(smem_u32(smem + Ly::kKRing), 16, Ly::kGroupBytes);
         const uint64_t dv0 = smem_desc(smem_u32(smem + Ly::kVRing), 1024, Ly::kGroupBytes);
         const uint64_t dq0 = smem_desc(smem_u32(smem + Ly::kQ), 16, Ly::kGroupBytes);
-        auto issue_s = [&](int h, int t) {  // S = Q_h K(t)^T into the score buffer
+        auto issue_s = [&](int h, int t) {  // S_h = Q_h K(t)^T into columns 128 h
           const uint64_t dk = dk0 + static_cast<uint64_t>((t % kStages) * (Ly::kTileBytes >> 4));
           const uint64_t dq = dq0 + static_cast<uint64_t>(h * (Ly::kQBytes >> 4));
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
-            mma_bf16_ss(tmem, dq + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + h * BN, dq + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(&s_full[h]);
         };
@@ -688,81 +679,57 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t dv = dv0 + static_cast<uint64_t>((t % kStages) * (Ly::kTileBytes >> 4));
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_bf16_ts(tmem + 256 + h * D, tmem + 128 + 64 * h + kk * 8,
+            mma_bf16_ts(tmem + 256 + h * D, tmem + h * BN + kk * 8,
                         dv + ((kk * 2 * Ly::kGroupBytes) >> 4), idesc_o, (acc || kk > 0) ? 1u : 0u);
-          mma_commit(&p_free[h]);
         };
-        // S stream: piece sp, tile si of the piece, m-tile sh, global tile s_tau
-        int sp = 0, si = 0, sh = 0, s_tau = g_tile;
-        // P V stream
-        int vp = 0, vi = 0, vh = 0, v_tau = g_tile;
-        int s_cnt[2] = {tiles_h0, tiles_h1};    // S_h issued so far
-        int pv_cnt[2] = {tiles_h0, tiles_h1};   // P_h V issued so far
-        int q_cnt[2] = {pieces_h0, pieces_h1};  // pieces whose Q_h was taken
         bool ok = true;
-        unsigned long long t_idle = 0;
-        while (vp < npieces) {
-          bool progressed = false;
-          if (sp < npieces) {
-            const Piece& pc = pieces[sp];
-            bool ready = true;
-            if (si == 0) ready = mbar_test_wait(&q_full[sh], q_cnt[sh] & 1);
-            if (ready && last_s_group >= 0)
-              ready = mbar_test_wait(&s_free[last_s_group], (s_cnt[last_s_group] - 1) & 1);
-            if (ready && sh == 0) ready = mbar_test_wait(&kfull[s_tau % kStages], (s_tau / kStages) & 1);
-            if (ready) {
+        int tau = g_tile;
+        for (int p = 0; p < npieces && ok; ++p) {
+          const Piece& pc = pieces[p];
+          const int nm = pc.nm, T = pc.t1 - pc.t0;
+          // the piece's first S of each m-tile, once its Q is loaded and K has landed
+          for (int h = 0; h < nm && ok; ++h) {
+            ok = mbar_wait(&q_full[h], (h ? pieces_h1 : pieces_h0) & 1, abort_flag);
+            if (ok && h == 0) ok = mbar_wait(&kfull[tau % kStages], (tau / kStages) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(h, tau);
+          }
+          if (!ok) break;
+          mma_commit(&kempty[tau % kStages]);
+          for (int i = 0; i < T && ok; ++i) {
+            const int t = tau + i;
+            for (int h = 0; h < nm; ++h) {
+              ok = mbar_wait(&p_full[h], (h ? tiles_h1 : tiles_h0) & 1, abort_flag);
+              if (ok && h == 0) ok = mbar_wait(&vfull[t % kStages], (t / kStages) & 1, abort_flag);
+              if (!ok) break;
               tc_fence_after();
-              issue_s(sh, s_tau);
-              if (si == 0) ++q_cnt[sh];
-              ++s_cnt[sh];
-              last_s_group = sh;
-              if (sh == pc.nm - 1) mma_commit(&kempty[s_tau % kStages]);  // the tile's last S
-              if (++sh == pc.nm) {
-                sh = 0;
-                ++s_tau;
-                if (++si == pc.t1 - pc.t0) {
-                  si = 0;
-                  ++sp;
+              issue_pv(h, t, i > 0);
+              if (i + 1 < T) {
+                if (h == 0) {
+                  ok = mbar_wait(&kfull[(t + 1) % kStages], ((t + 1) / kStages) & 1, abort_flag);
+                  if (!ok) break;
+                  tc_fence_after();
                 }
+                issue_s(h, t + 1);
               }
-              progressed = true;
+              if (h) ++tiles_h1; else ++tiles_h0;
             }
+            if (!ok) break;
+            mma_commit(&vempty[t % kStages]);
+            if (i + 1 < T) mma_commit(&kempty[(t + 1) % kStages]);
           }
-          {
-            const Piece& pc = pieces[vp];
-            bool ready = mbar_test_wait(&p_full[vh], pv_cnt[vh] & 1);
-            if (ready && vh == 0) ready = mbar_test_wait(&vfull[v_tau % kStages], (v_tau / kStages) & 1);
-            if (ready) {
-              tc_fence_after();
-              issue_pv(vh, v_tau, vi > 0);
-              ++pv_cnt[vh];
-              if (vh == pc.nm - 1) mma_commit(&vempty[v_tau % kStages]);  // the tile's last P V
-              if (++vh == pc.nm) {
-                vh = 0;
-                ++v_tau;
-                if (++vi == pc.t1 - pc.t0) {
-                  vi = 0;
-                  ++vp;
-                }
-              }
-              progressed = true;
-            }
+          if (!ok) break;
+          mma_commit(&o_done[0]);
+          ++pieces_h0;
+          if (nm == 2) {
+            mma_commit(&o_done[1]);
+            ++pieces_h1;
           }
-          if (progressed) {
-            t_idle = 0;
-          } else if (t_idle == 0) {
-            t_idle = global_ns();
-          } else if (global_ns() - t_idle > kWaitLimitNs || *abort_flag) {
-            ok = false;
-            break;
-          }
+          tau += T;
         }
-        tiles_h0 = pv_cnt[0];
-        tiles_h1 = pv_cnt[1];
-        pieces_h0 = q_cnt[0];
-        pieces_h1 = q_cnt[1];
         if (!ok) {
-          record_status(a.status, pieces[min(vp, npieces - 1)].b, kDeviceTimeout);
+          record_status(a.status, pieces[0].b, kDeviceTimeout);
           misc->abort = 1;
         }
         // every MMA issued so far completes before the next round or the exit
@@ -777,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = warp >> 2;
       const int r = (warp & 3) * 32 + lane;  // row of the m-tile == TMEM lane
       const uint32_t lane_off = lane_off_q(warp);
-      const uint32_t tmem_p = tmem + 128 + 64 * h;  // P_h: 128 keys as bf16 pairs
+      const uint32_t tmem_s = tmem + h * BN;
       const uint32_t tmem_o = tmem + 256 + h * D;
       uint32_t* anc = reinterpret_cast<uint32_t*>(smem + Ly::kAnc) + (h * BM + r) * kAncStride;
       int32_t* par = reinterpret_cast<int32_t*>(smem + Ly::kParent) + h * kMaxNodes;
@@ -862,13 +829,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < T; ++i) {
           const int t = pc.t0 + i;  // tile of the unit
           const int gt = tau + i;   // global tile (ring slot)
-          const int k = my_tiles++;  // this tile's index in the m-tile's sequence
           if (ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[h], k & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[h], my_tiles & 1, abort_flag));
             if (!ok) misc->abort = 1;
           }
+          ++my_tiles;
           if (!ok) {
-            mbar_arrive(&s_free[h]);
             mbar_arrive(&p_full[h]);
             continue;
           }
@@ -876,10 +842,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            tmem_ld32(tmem + 32 * c + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+            tmem_ld32(tmem_s + 32 * c + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
           tmem_ld_wait();
-          tc_fence_before();
-          mbar_arrive(&s_free[h]);  // the score buffer may take the next S
           // mask (scores stay unscaled; the scale is folded into the exponent)
           int valid_keys = BN;
           if (t < pc.P) {
@@ -924,18 +888,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           const float mref = m_run == -INFINITY ? 0.0f : m_run;
-          // P_h(k-1) V must be complete before P_h and O_h are rewritten
-          if (k >= 1) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&p_free[h], (k - 1) & 1, abort_flag));
-            if (!ok) {
-              misc->abort = 1;
-              mbar_arrive(&p_full[h]);
-              continue;
-            }
-            tc_fence_after();
-          }
           // P = 2^(s * scale * log2(e) - m) as bf16 pairs (column c holds keys
-          // 2c, 2c+1), into P_h in four 16-column stores; masked
+          // 2c, 2c+1), written over S_h in four 16-column stores; masked
           // scores are -inf -> 0.  The row sum adds the rounded values, so
           // that O / l weights V exactly as the P V product did (with the
           // unrounded sum the rounding of a dominant P biases the output by
@@ -955,11 +909,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk[k] = pb;
               lacc = add2(lacc, make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
             }
-            tmem_st16(tmem_p + 16 * q4 + lane_off, pk);
+            tmem_st16(tmem_s + 16 * q4 + lane_off, pk);
           }
           const float lsum = lacc.x + lacc.y;
           if (__any_sync(0xffffffffu, rescale)) {
-            // O holds P(..t-1) V against the old max (P_h(t-1) V is complete)
+            // O holds P(..t-1) V against the old max; P_h(t-1) V is complete
+            // (S_h(t), which this thread has seen complete, was issued after it)
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
               uint32_t o[32];
@@ -995,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------- piece epilogue
         bool done = false;
         if (ok) {
-          done = __all_sync(0xffffffffu, mbar_wait(&p_free[h], (my_tiles - 1) & 1, abort_flag));
+          done = __all_sync(0xffffffffu, mbar_wait(&o_done[h], my_pieces & 1, abort_flag));
           if (!done) {
             ok = false;
             misc->abort = 1;
