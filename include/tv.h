@@ -173,6 +173,37 @@ int tv_tree_attention(const tv_attn_params* params, const uint16_t* q_nodes,
                       cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * FP8 tree attention ([EC] §9.2: FP8 mixed-precision tree verification,
+ * E4M3 values with fp32 accumulation and one scale per 128-element block).
+ *
+ * The same attention as tv_tree_attention (same mask, key list, layouts of
+ * the index arrays, output, status and workspace), on E4M3 inputs: q_nodes,
+ * the pools and the tree K/V hold one-byte E4M3 codes (OCP layout: bias 7,
+ * subnormals, NaN at S.1111.111, no infinities), and every row of D codes
+ * (a token of one head: the 128-element block at D = 128) carries one fp32
+ * scale; the value is code x scale.  head_dim must be 128
+ * (TV_ERR_UNSUPPORTED otherwise).
+ *   q_nodes          u8 [total_nodes][Hq][128],        q_scale fp32 [total_nodes][Hq]
+ *   k_prefix_blocks  u8 [num_blocks][Hkv][16][128],    k_prefix_scale fp32 [num_blocks][Hkv][16]
+ *   v_prefix_blocks  u8 [num_blocks][Hkv][16][128],    v_prefix_scale fp32 [num_blocks][Hkv][16]
+ *   k_nodes, v_nodes u8 [total_nodes][Hkv][128],       k_nodes_scale, v_nodes_scale fp32 [total_nodes][Hkv]
+ * Arithmetic: S = Q K^T on the tensor cores over the codes (E4M3 x E4M3,
+ * fp32 accumulation), each score times its query row's and key row's scale;
+ * fp32 online softmax; V converted exactly to fp16 and its row scale applied
+ * to P (P' = P * scale in fp16, the row sum taking P' / scale), P' V in fp16
+ * with fp32 accumulation.  The V scales times 256 must stay below 65504 (the
+ * fp16 range of P').  All device pointers 16-byte aligned. */
+int tv_tree_attention_fp8(const tv_attn_params* params, const uint8_t* q_nodes,
+                          const float* q_scale, const uint8_t* k_prefix_blocks,
+                          const float* k_prefix_scale, const uint8_t* v_prefix_blocks,
+                          const float* v_prefix_scale, const int32_t* block_table,
+                          const uint8_t* k_nodes, const float* k_nodes_scale,
+                          const uint8_t* v_nodes, const float* v_nodes_scale,
+                          const int32_t* parent, const int32_t* prefix_lens,
+                          const int32_t* node_offsets, void* out, int32_t* status,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Tree attention for callers that cannot allocate (no counterpart on the
  * pages: an engineering addition of this library).
  *

@@ -8,6 +8,7 @@ the functions raise if the library cannot be loaded.
 PyTorch is used for device memory and the current CUDA stream only.
 
     tree_attention(...)  -> out, status      (tv_tree_attention)
+    tree_attention_fp8(...) -> out, status   (tv_tree_attention_fp8, E4M3 inputs)
     accept(...)          -> dict of outputs  (tv_accept)
     commit_kv(...)       -> new_prefix_lens, status (tv_commit_kv)
     retained_set(...)    -> mask, z_fixed, z, kept (tv_retained_set)
@@ -17,7 +18,7 @@ from __future__ import annotations
 import ctypes as C
 import os
 
-__all__ = ["TVError", "load", "tree_attention", "accept", "commit_kv", "retained_set",
+__all__ = ["TVError", "load", "tree_attention", "tree_attention_fp8", "accept", "commit_kv", "retained_set",
            "attention_workspace_size", "attention_plan", "attention_params",
            "TV_MAX_NODES", "TV_OK", "TV_ERR_BAD_TREE", "TV_ERR_DEVICE_TIMEOUT", "TV_ERR_NO_PAGE",
            "status_string"]
@@ -39,7 +40,7 @@ EXPORTS = ("tv_status_string", "tv_version", "tv_tree_attention_workspace_size",
            "tv_tree_attention", "tv_accept_workspace_size", "tv_accept", "tv_accept_ex",
            "tv_commit_kv",
            "tv_retained_set", "tv_selftest_wait_timeout", "tv_tree_attention_plan",
-           "tv_tree_attention_no_alloc")
+           "tv_tree_attention_no_alloc", "tv_tree_attention_fp8")
 
 
 class TVError(RuntimeError):
@@ -102,6 +103,8 @@ def load(path: str | None = None) -> C.CDLL:
     lib.tv_tree_attention_workspace_size.restype = sz
     lib.tv_tree_attention.argtypes = [C.POINTER(AttnParams)] + [vp] * 11 + [vp, sz, vp]
     lib.tv_tree_attention.restype = C.c_int
+    lib.tv_tree_attention_fp8.argtypes = [C.POINTER(AttnParams)] + [vp] * 16 + [vp, sz, vp]
+    lib.tv_tree_attention_fp8.restype = C.c_int
     lib.tv_accept_workspace_size.argtypes = [C.POINTER(AcceptParams)]
     lib.tv_accept_workspace_size.restype = sz
     lib.tv_accept.argtypes = [C.POINTER(AcceptParams)] + [vp] * 12 + [vp, sz, vp]
@@ -209,6 +212,47 @@ def tree_attention(q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nod
                                C.c_size_t(ws_bytes), _stream(stream))
     if rc != TV_OK:
         raise TVError(rc, "tv_tree_attention")
+    return out, status
+
+
+def tree_attention_fp8(q_codes, q_scale, k_prefix_blocks, k_prefix_scale, v_prefix_blocks,
+                       v_prefix_scale, block_table, k_nodes, k_nodes_scale, v_nodes,
+                       v_nodes_scale, parent, prefix_lens, node_offsets, *, max_nodes: int,
+                       max_prefix_len: int, softmax_scale: float = 0.0, out=None, status=None,
+                       workspace=None, stream=None, out_dtype: str = "bf16"):
+    """tv_tree_attention_fp8 on the current stream: E4M3 codes (uint8) with one
+    fp32 scale per row of D = 128 codes.  q_codes [total, Hq, 128],
+    q_scale [total, Hq]; k/v_prefix_blocks [num_blocks, Hkv, 16, 128],
+    k/v_prefix_scale [num_blocks, Hkv, 16]; k/v_nodes [total, Hkv, 128],
+    k/v_nodes_scale [total, Hkv]; the index arrays as for tree_attention.
+    Returns (out, status); nothing is synchronised."""
+    import torch
+    lib = load()
+    _check_dev(q_codes, q_scale, k_prefix_blocks, k_prefix_scale, v_prefix_blocks,
+               v_prefix_scale, block_table, k_nodes, k_nodes_scale, v_nodes, v_nodes_scale,
+               parent, prefix_lens, node_offsets)
+    prm = attention_params(q_codes, k_prefix_blocks, block_table, prefix_lens,
+                           num_kv_heads=k_prefix_blocks.shape[1], max_nodes=max_nodes,
+                           max_prefix_len=max_prefix_len, softmax_scale=softmax_scale,
+                           out_dtype=out_dtype)
+    if out is None:
+        out = torch.empty(q_codes.shape, device=q_codes.device,
+                          dtype=torch.float32 if out_dtype == "fp32" else torch.bfloat16)
+    if status is None:
+        status = torch.empty(prm.batch, dtype=torch.int32, device=q_codes.device)
+    need = int(lib.tv_tree_attention_workspace_size(C.byref(prm)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_codes.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.tv_tree_attention_fp8(C.byref(prm), _ptr(q_codes), _ptr(q_scale),
+                                   _ptr(k_prefix_blocks), _ptr(k_prefix_scale),
+                                   _ptr(v_prefix_blocks), _ptr(v_prefix_scale), _ptr(block_table),
+                                   _ptr(k_nodes), _ptr(k_nodes_scale), _ptr(v_nodes),
+                                   _ptr(v_nodes_scale), _ptr(parent), _ptr(prefix_lens),
+                                   _ptr(node_offsets), _ptr(out), _ptr(status), _ptr(workspace),
+                                   C.c_size_t(ws_bytes), _stream(stream))
+    if rc != TV_OK:
+        raise TVError(rc, "tv_tree_attention_fp8")
     return out, status
 
 

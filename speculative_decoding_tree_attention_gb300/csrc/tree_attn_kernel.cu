@@ -73,7 +73,10 @@ constexpr int kUnitRows = 2 * BM;     // rows of one m-tile pair
 constexpr int kSoftmaxThreads = 256;  // warps 0-7: two groups of four warps
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;           // issues every MMA; owns the TMEM allocation
+constexpr int kConvWarp = 10;         // E4M3 inputs: warps 10-11 convert V tiles to fp16
+constexpr int kConvThreads = 64;
 constexpr int kThreads = 320;
+constexpr int kThreadsF8 = 384;       // (registers are allocated for 12 warps either way)
 constexpr int kMaxNodes = 512;
 constexpr int kMaxAncWords = kMaxNodes / 32;
 constexpr int kAncStride = kMaxAncWords + 1;  // odd word stride: rows of a warp hit distinct banks
@@ -99,32 +102,43 @@ struct Piece {
   int pad;
 };
 
-template <int D>
+// Shared memory of one CTA.  bf16 inputs: K and V tiles of 128 keys x D bf16
+// in 2-stage rings.  E4M3 inputs (F8, D = 128): K and raw V tiles of 128 keys
+// x 128 one-byte codes (a K ring of 3, a raw V ring of 2), two converted fp16
+// V tiles, and 4 slots of per-key scales (K scale, V scale, 1 / V scale).
+template <int D, bool F8>
 struct Layout {
-  static constexpr int kHalves = D / 64;
-  static constexpr int kStages = D == 128 ? 2 : 4;     // depth of the K ring and of the V ring
-  static constexpr int kGroupBytes = kHalves * 1024;   // 8 rows, all columns
-  static constexpr int kTileBytes = BN * D * 2;        // one K or V tile
-  static constexpr int kQBytes = BM * D * 2;           // Q of one m-tile
+  static_assert(!F8 || D == 128, "E4M3 inputs need D = 128");
+  static constexpr int kHalves = D / 64;               // 64-column halves of a 16-bit row
+  static constexpr int kStages = F8 ? 3 : (D == 128 ? 2 : 4);  // K ring depth
+  static constexpr int kVStages = F8 ? 2 : kStages;    // V (raw) ring depth
+  static constexpr int kGroupBytes = kHalves * 1024;   // 8 rows of a 16-bit tile
+  static constexpr int kTileBytes = BN * D * 2;        // a 16-bit (bf16 or fp16) K or V tile
+  static constexpr int kKTileBytes = F8 ? BN * D : kTileBytes;  // a K or raw V tile as loaded
+  static constexpr int kQBytes = F8 ? BM * D : BM * D * 2;     // Q of one m-tile
   static constexpr int kQ = 0;                         // Q_0, Q_1
   static constexpr int kKRing = kQ + 2 * kQBytes;
-  static constexpr int kVRing = kKRing + kStages * kTileBytes;
-  static constexpr int kAnc = kVRing + kStages * kTileBytes;  // [2][128][kAncStride] words
+  static constexpr int kVRing = kKRing + kStages * kKTileBytes;
+  static constexpr int kV16 = kVRing + kVStages * kKTileBytes;  // F8: converted V, 2 slots
+  static constexpr int kV16Bytes = F8 ? 2 * kTileBytes : 0;
+  static constexpr int kScl = kV16 + kV16Bytes;        // F8: [4][3][128] floats
+  static constexpr int kSclBytes = F8 ? 4 * 3 * BN * 4 : 0;
+  static constexpr int kAnc = kScl + kSclBytes;        // [2][128][kAncStride] words
   static constexpr int kAncBytes = 2 * BM * kAncStride * 4;
-  static constexpr int kParent = kAnc + kAncBytes;            // [2][512]
+  static constexpr int kParent = kAnc + kAncBytes;     // [2][512]
   static constexpr int kParentBytes = 2 * kMaxNodes * 4;
   static constexpr int kPieces = kParent + kParentBytes;
   static constexpr int kPiecesBytes = kMaxPieces * static_cast<int>(sizeof(Piece));
-  static constexpr int kScan = kPieces + kPiecesBytes;        // 8 warp sums (int64)
+  static constexpr int kScan = kPieces + kPiecesBytes; // 8 warp sums
   static constexpr int kScanBytes = 128;
   // block ids of the pages of the last 8 K tiles issued (8 per tile), reused
-  // by the V copies of the same tiles
+  // by the V copies (and, for E4M3 inputs, the V conversion) of the same tiles
   static constexpr int kBlk = kScan + kScanBytes;
   static constexpr int kBlkBytes = 8 * 8 * 4;
   static constexpr int kBar = kBlk + kBlkBytes;
-  // kfull[S], kempty[S], vfull[S], vempty[S], s_full[2], p_full[2],
-  // o_done[2], q_full[2], drain
-  static constexpr int kNumBars = 4 * kStages + 9;
+  // kfull[S], kempty[S], vfull[VS], vempty[VS], s_full[2], p_full[2],
+  // o_done[2], q_full[2], drain, v16full[2], v16empty[2]
+  static constexpr int kNumBars = 2 * kStages + 2 * kVStages + 13;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kMiscBytes = 512;
   static constexpr int kTotal = kMisc + kMiscBytes;
@@ -244,9 +258,9 @@ struct Line {
 // (run by the 256 softmax threads).  In round 0 it also zeroes the output of
 // sequences whose extent is malformed (every row it can address) and records
 // their status.
-template <int D>
+template <int D, bool F8>
 __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int sid) {
-  using Ly = Layout<D>;
+  using Ly = Layout<D, F8>;
   Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
   Piece* pieces = reinterpret_cast<Piece*>(smem + Ly::kPieces);
   int* scratch = reinterpret_cast<int*>(smem + Ly::kScan);
@@ -470,25 +484,32 @@ __device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t ou
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+// F8: E4M3 inputs (tv_tree_attention_fp8): S = Q K^T on kind::f8f6f4 over the
+// codes, the K and Q row scales applied to the scores; V converted to fp16 by
+// warps 10-11 and its row scale folded into P (P' = P s_v in fp16, the row
+// sum takes P' / s_v); P' V on kind::f16 in fp16.
+template <int D, bool F8>
+__global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     tree_attn_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps) {
-  using Ly = Layout<D>;
+  using Ly = Layout<D, F8>;
   using Sl = Slot<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   constexpr int kStages = Ly::kStages;
+  constexpr int kVStages = Ly::kVStages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kBar);
   uint64_t* kfull = bars;
   uint64_t* kempty = bars + kStages;
   uint64_t* vfull = bars + 2 * kStages;
-  uint64_t* vempty = bars + 3 * kStages;
-  uint64_t* s_full = bars + 4 * kStages;  // [2]: S_h(t) complete (and every MMA before it)
+  uint64_t* vempty = vfull + kVStages;    // F8: the converters have read the raw V
+  uint64_t* s_full = vempty + kVStages;   // [2]: S_h(t) complete (and every MMA before it)
   uint64_t* p_full = s_full + 2;          // [2]: P_h(t) in TMEM (128 arrivals)
   uint64_t* o_done = p_full + 2;          // [2]: the last P_h V of a piece complete
   uint64_t* q_full = o_done + 2;          // [2]: Q_h of a piece in shared memory (128 arrivals)
   uint64_t* drain = q_full + 2;           // every MMA issued so far complete (once per round)
+  uint64_t* v16full = drain + 1;          // F8 [2]: V(t) converted and its scales staged (64 arrivals)
+  uint64_t* v16empty = v16full + 2;       // F8 [2]: the P V of tile t complete
   Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
   Piece* pieces = reinterpret_cast<Piece*>(smem + Ly::kPieces);
 
@@ -502,8 +523,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&kfull[s], 1);
       mbar_init(&kempty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&vfull[s], 1);
-      mbar_init(&vempty[s], 1);
+      mbar_init(&vempty[s], F8 ? kConvThreads : 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&v16full[k], kConvThreads);
+      mbar_init(&v16empty[k], 1);
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(&s_full[h], 1);
@@ -532,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int tiles_h0 = 0, tiles_h1 = 0, pieces_h0 = 0, pieces_h1 = 0;
 
   for (int round = 0;; ++round) {
-    if (warp < kTmaWarp) build_schedule<D>(a, smem, round, tid);
+    if (warp < kTmaWarp) build_schedule<D, F8>(a, smem, round, tid);
     __syncthreads();
     const int npieces = misc->npieces;
     const bool more = misc->more != 0;
@@ -569,11 +596,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       // issues tile t of piece p (global tile tau) of tensor kv (0 = K, 1 = V)
       auto issue = [&](int p, int t, int tau, int kv, int blk) {
         const Piece& pc = pieces[p];
-        const int st = tau % kStages;
+        const int st = kv ? tau % kVStages : tau % kStages;
         uint64_t* bar = kv ? &vfull[st] : &kfull[st];
-        if (lane == 0) mbar_arrive_expect_tx(bar, Ly::kTileBytes);
+        if (lane == 0) mbar_arrive_expect_tx(bar, Ly::kKTileBytes);
         __syncwarp();
-        uint8_t* tile = smem + (kv ? Ly::kVRing : Ly::kKRing) + st * Ly::kTileBytes;
+        uint8_t* tile = smem + (kv ? Ly::kVRing : Ly::kKRing) + st * Ly::kKTileBytes;
+        if constexpr (F8) {
+          // E4M3 codes: a page is 16 rows of 128 bytes (2 KB), a node box 8
+          if (t < pc.P) {
+            if (page_lane) {
+              int page = pool_pages;  // out of bounds: zero fill
+              if (blk >= 0 && blk < a.num_blocks) {
+                page = blk * a.hkv + pc.kvh;
+              } else if (blk != kPastEnd && kv == 0) {
+                piece_bad[p] = 1;
+                record_status(a.status, pc.b, kBadTree);
+              }
+              tma_load_3d(tile + lane * 2048, kv ? &maps.v_pool : &maps.k_pool, bar, 0, 0, page);
+            }
+          } else if (lane < BN / 8) {
+            const int node0 = pc.n0 + (t - pc.P) * BN + lane * 8;
+            tma_load_3d(tile + lane * 1024, kv ? &maps.v_nodes : &maps.k_nodes, bar, 0, node0, pc.kvh);
+          }
+          return;
+        }
         if (t < pc.P) {
           if (page_lane) {
             int page = pool_pages;  // out of bounds: zero fill
@@ -617,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (tv < tk) {
-          int ready = lane == 0 ? mbar_test_wait(&vempty[tv % kStages], ((tv / kStages) & 1) ^ 1) : 0;
+          int ready = lane == 0 ? mbar_test_wait(&vempty[tv % kVStages], ((tv / kVStages) & 1) ^ 1) : 0;
           if (__shfl_sync(0xffffffffu, ready, 0)) {
             issue(vp, vt, tv, 1, page_lane ? blk_ring[(tv & 7) * 8 + lane] : kPastEnd);
             ++tv;
@@ -649,34 +695,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         // exits (at most kStages of each ring can still be in flight)
         for (int t = max(g_tile, tk - kStages); t < tk; ++t)
           mbar_wait(&kfull[t % kStages], (t / kStages) & 1);
-        for (int t = max(g_tile, tv - kStages); t < tv; ++t)
-          mbar_wait(&vfull[t % kStages], (t / kStages) & 1);
+        for (int t = max(g_tile, tv - kVStages); t < tv; ++t)
+          mbar_wait(&vfull[t % kVStages], (t / kVStages) & 1);
       }
       __syncwarp();
     } else if (warp == kMmaWarp) {
       // ------------------------------------------------------ MMA issuer
       if (lane == 0) {
-        constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0);  // M=128, N=128, K-major K
-        constexpr uint32_t idesc_o = idesc_bf16(BM, D, 1);   // M=128, N=D, MN-major V
+        // bf16: S and P V on kind::f16 in bf16.  E4M3: S on kind::f8f6f4 over
+        // the codes, P V on kind::f16 in fp16 (P' and the converted V).
+        constexpr uint32_t idesc_s = F8 ? idesc_e4m3(BM, BN) : idesc_bf16(BM, BN, 0);
+        constexpr uint32_t idesc_o = F8 ? idesc_f16(BM, D, 1) : idesc_bf16(BM, D, 1);
         // Descriptors are built once; each MMA adds an offset to the start
         // address field (16-byte units).  K and Q (K-major): 8-row groups at
-        // kGroupBytes, 64-column halves at +1024.  V (MN-major): 8-key groups
-        // at kGroupBytes, column halves at +1024.
-        const uint64_t dk0 = smem_desc(smem_u32(smem + Ly::kKRing), 16, Ly::kGroupBytes);
-        const uint64_t dv0 = smem_desc(smem_u32(smem + Ly::kVRing), 1024, Ly::kGroupBytes);
-        const uint64_t dq0 = smem_desc(smem_u32(smem + Ly::kQ), 16, Ly::kGroupBytes);
+        // kGroupBytes (16-bit) or 1024 (8-bit: one 128-byte line per row),
+        // 64-column halves at +1024.  V (MN-major): 8-key groups at
+        // kGroupBytes, column halves at +1024.
+        constexpr uint32_t kKRow8 = F8 ? 1024 : Ly::kGroupBytes;
+        const uint64_t dk0 = smem_desc(smem_u32(smem + Ly::kKRing), 16, kKRow8);
+        const uint64_t dv0 = smem_desc(smem_u32(smem + (F8 ? Ly::kV16 : Ly::kVRing)), 1024, Ly::kGroupBytes);
+        const uint64_t dq0 = smem_desc(smem_u32(smem + Ly::kQ), 16, kKRow8);
         auto issue_s = [&](int h, int t) {  // S_h = Q_h K(t)^T into columns 128 h
-          const uint64_t dk = dk0 + static_cast<uint64_t>((t % kStages) * (Ly::kTileBytes >> 4));
+          const uint64_t dk = dk0 + static_cast<uint64_t>((t % kStages) * (Ly::kKTileBytes >> 4));
           const uint64_t dq = dq0 + static_cast<uint64_t>(h * (Ly::kQBytes >> 4));
+          if constexpr (F8) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
-            mma_bf16_ss(tmem + h * BN, dq + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 32; ++kk)  // 32 codes (bytes) of each row per MMA
+              mma_f8_ss(tmem + h * BN, dq + kk * 2, dk + kk * 2, idesc_s, kk > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
+              mma_bf16_ss(tmem + h * BN, dq + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
+            }
           }
           mma_commit(&s_full[h]);
         };
         auto issue_pv = [&](int h, int t, bool acc) {  // O_h (+)= P_h V(t)
-          const uint64_t dv = dv0 + static_cast<uint64_t>((t % kStages) * (Ly::kTileBytes >> 4));
+          const uint64_t dv = dv0 + static_cast<uint64_t>((F8 ? (t & 1) : (t % kStages)) * (Ly::kTileBytes >> 4));
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_bf16_ts(tmem + 256 + h * D, tmem + h * BN + kk * 8,
@@ -701,7 +757,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = tau + i;
             for (int h = 0; h < nm; ++h) {
               ok = mbar_wait(&p_full[h], (h ? tiles_h1 : tiles_h0) & 1, abort_flag);
-              if (ok && h == 0) ok = mbar_wait(&vfull[t % kStages], (t / kStages) & 1, abort_flag);
+              if (ok && h == 0) {
+                if constexpr (F8) {
+                  ok = mbar_wait(&v16full[t & 1], (t >> 1) & 1, abort_flag);  // V(t) in fp16
+                } else {
+                  ok = mbar_wait(&vfull[t % kStages], (t / kStages) & 1, abort_flag);
+                }
+              }
               if (!ok) break;
               tc_fence_after();
               issue_pv(h, t, i > 0);
@@ -716,7 +778,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (h) ++tiles_h1; else ++tiles_h0;
             }
             if (!ok) break;
-            mma_commit(&vempty[t % kStages]);
+            if constexpr (F8) {
+              mma_commit(&v16empty[t & 1]);  // the converted V slot may take tile t + 2
+            } else {
+              mma_commit(&vempty[t % kStages]);
+            }
             if (i + 1 < T) mma_commit(&kempty[(t + 1) % kStages]);
           }
           if (!ok) break;
@@ -737,6 +803,91 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(drain, round & 1);
       }
       __syncwarp();
+    } else if (F8 && warp >= kConvWarp) {
+      // ------------------------------------------------------ V conversion (E4M3)
+      // Per tile, once its raw V has landed and the converted slot is free
+      // (the P V of tile t - 2 is complete): the 128 keys' K scales, V
+      // scales and reciprocal V scales into scale slot t % 4, and the V codes
+      // as fp16 (exact) into converted slot t % 2, in the MN-major layout the
+      // P V MMA reads.  Keys past the prefix end or the tree get scale 0 and
+      // zero rows (page tails may hold stale codes).
+      if constexpr (F8) {
+        const int ct = tid - kConvWarp * 32;  // 0 .. 63
+        const int* blk_ring = reinterpret_cast<const int*>(smem + Ly::kBlk);
+        float* scl = reinterpret_cast<float*>(smem + Ly::kScl);
+        bool ok = true;
+        int tau = g_tile;
+        for (int p = 0; p < npieces; ++p) {
+          const Piece& pc = pieces[p];
+          for (int t = pc.t0; t < pc.t1; ++t, ++tau) {
+            const int vs = tau % kVStages;
+            if (ok) ok = mbar_wait(&vfull[vs], (tau / kVStages) & 1, abort_flag);
+            if (ok && tau >= 2) ok = mbar_wait(&v16empty[tau & 1], ((tau - 2) >> 1) & 1, abort_flag);
+            if (!ok) {
+              misc->abort = 1;
+            } else {
+              float* sc = scl + (tau & 3) * 3 * BN;
+              const bool prefix = t < pc.P;
+              const int valid = prefix ? min(BN, pc.L - t * BN) : min(BN, pc.N - (t - pc.P) * BN);
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const int key = 2 * ct + j;
+                float sk = 0.0f, sv = 0.0f;
+                if (key < valid) {
+                  if (prefix) {
+                    const int blk = blk_ring[(tau & 7) * 8 + key / 16];
+                    if (blk >= 0 && blk < a.num_blocks) {
+                      const size_t idx = (static_cast<size_t>(blk) * a.hkv + pc.kvh) * 16 + (key & 15);
+                      sk = __ldg(a.kp_scale + idx);
+                      sv = __ldg(a.vp_scale + idx);
+                    }
+                  } else {
+                    const size_t idx = static_cast<size_t>(pc.n0 + (t - pc.P) * BN + key) * a.hkv + pc.kvh;
+                    sk = __ldg(a.kn_scale + idx);
+                    sv = __ldg(a.vn_scale + idx);
+                  }
+                }
+                sc[key] = sk;
+                sc[BN + key] = sv;
+                sc[2 * BN + key] = sv != 0.0f ? 1.0f / sv : 0.0f;
+              }
+              const uint8_t* raw = smem + Ly::kVRing + vs * Ly::kKTileBytes;
+              uint8_t* v16 = smem + Ly::kV16 + (tau & 1) * Ly::kTileBytes;
+              // item (key, c): codes of columns 16c .. 16c+15 of a key's row
+              // (raw: 128 bytes a row, 16-byte chunk c at chunk c ^ (key % 8))
+              for (int it = ct; it < BN * 8; it += kConvThreads) {
+                const int key = it >> 3, c = it & 7;
+                uint32_t h[8];
+                if (key < valid) {
+                  const uint4 w = *reinterpret_cast<const uint4*>(raw + key * 128 + ((c ^ (key & 7)) << 4));
+                  h[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.x));
+                  h[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16));
+                  h[2] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.y));
+                  h[3] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16));
+                  h[4] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.z));
+                  h[5] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16));
+                  h[6] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.w));
+                  h[7] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16));
+                } else {
+#pragma unroll
+                  for (int k = 0; k < 8; ++k) h[k] = 0u;
+                }
+                // fp16 layout: [8-key group][64-column half][key][128 B],
+                // 16-byte chunk q of a line at chunk q ^ (key % 8)
+                uint8_t* dst = v16 + (key >> 3) * Ly::kGroupBytes + (c >> 2) * 1024 + (key & 7) * 128;
+                *reinterpret_cast<uint4*>(dst + ((((2 * c) & 7) ^ (key & 7)) << 4)) =
+                    make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(dst + ((((2 * c + 1) & 7) ^ (key & 7)) << 4)) =
+                    make_uint4(h[4], h[5], h[6], h[7]);
+              }
+              fence_proxy_async_smem();  // generic writes, read by the MMA
+            }
+            mbar_arrive(&v16full[tau & 1]);
+            mbar_arrive(&vempty[vs]);
+          }
+        }
+        if (!ok) record_status(a.status, pieces[0].b, kDeviceTimeout);
+      }
     } else {
       // ------------------------------------------------------ softmax groups
       // Warps 4h .. 4h+3 own m-tile h; warp w's rows are its TMEM lane
@@ -770,21 +921,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Q rows -> shared memory in the 128-byte swizzled K-major layout
         // (the 16-byte chunk c of row r sits at chunk c ^ (r % 8)); rows past
         // the unit are zero.  The buffer is free: the previous piece's last
-        // S_h completed before its epilogue.
+        // S_h completed before its epilogue.  E4M3: one 128-byte line of
+        // codes a row, and the row's scale folded into the exponent factor.
+        float cq = a.scale_log2;
         {
-          uint8_t* dst = qh + (r >> 3) * Ly::kGroupBytes + (r & 7) * 128;
+          constexpr int kRowBytes = F8 ? D : 2 * D;
+          constexpr int kLineBytes = F8 ? 1024 : Ly::kGroupBytes;  // 8 rows
+          uint8_t* dst = qh + (r >> 3) * kLineBytes + (r & 7) * 128;
           if (live) {
-            const uint16_t* src = a.q + out_row * D;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(a.q) + out_row * kRowBytes;
 #pragma unroll
-            for (int hf = 0; hf < Ly::kHalves; ++hf)
-#pragma unroll
-              for (int c = 0; c < 8; ++c) cpa16(dst + hf * 1024 + ((c ^ (r & 7)) << 4), src + hf * 64 + c * 8);
+            for (int k = 0; k < kRowBytes / 16; ++k)
+              cpa16(dst + (k >> 3) * 1024 + (((k & 7) ^ (r & 7)) << 4), src + k * 16);
+            if constexpr (F8) cq = a.scale_log2 * __ldg(a.q_scale + out_row);
           } else {
 #pragma unroll
-            for (int hf = 0; hf < Ly::kHalves; ++hf)
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(dst + hf * 1024 + c * 16) = make_uint4(0, 0, 0, 0);
+            for (int k = 0; k < kRowBytes / 16; ++k)
+              *reinterpret_cast<uint4*>(dst + (k >> 3) * 1024 + k % 8 * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         // the next piece's Q row of this thread into L2, so that its load
@@ -844,7 +997,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 4; ++c)
             tmem_ld32(tmem_s + 32 * c + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
           tmem_ld_wait();
-          // mask (scores stay unscaled; the scale is folded into the exponent)
+          const float* scl = reinterpret_cast<const float*>(smem + Ly::kScl) + (gt & 3) * 3 * BN;
+          if constexpr (F8) {
+            // the keys' scales of this tile are staged with its converted V
+            if (!__all_sync(0xffffffffu, mbar_wait(&v16full[gt & 1], (gt >> 1) & 1, abort_flag))) {
+              ok = false;
+              misc->abort = 1;
+              mbar_arrive(&p_full[h]);
+              continue;
+            }
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+              const float4 sk = *reinterpret_cast<const float4*>(scl + c);
+              x[c] *= sk.x;
+              x[c + 1] *= sk.y;
+              x[c + 2] *= sk.z;
+              x[c + 3] *= sk.w;
+            }
+          }
+          // mask (scores stay unscaled by the softmax scale, which is folded
+          // into the exponent)
           int valid_keys = BN;
           if (t < pc.P) {
             valid_keys = min(BN, pc.L - t * BN);
@@ -874,8 +1046,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx[j] = fmaxf(mx[j], x[j + 120]);
           }
           const float smax =
-              fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
-              a.scale_log2;
+              fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * cq;
           float alpha = 1.0f;
           bool rescale = false;
           if (smax != -INFINITY) {
@@ -895,7 +1066,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // unrounded sum the rounding of a dominant P biases the output by
           // up to 2^-9 of its V row).  Exponent arguments and sums take two
           // lanes per instruction.
-          const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+          const float2 sc2 = make_float2(cq, cq);
           const float2 nm2 = make_float2(-mref, -mref);
           float2 lacc = make_float2(0.0f, 0.0f);
 #pragma unroll
@@ -905,9 +1076,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 16; ++k) {
               const float2 e = fma2(make_float2(x[32 * q4 + 2 * k], x[32 * q4 + 2 * k + 1]), sc2, nm2);
               const float2 pp = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-              const uint32_t pb = pack_bf16x2(pp.x, pp.y);
-              pk[k] = pb;
-              lacc = add2(lacc, make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
+              if constexpr (F8) {
+                // P' = P s_v in fp16; the row sum takes P' / s_v
+                const int c = 32 * q4 + 2 * k;
+                const float2 sv = *reinterpret_cast<const float2*>(scl + BN + c);
+                const float2 iv = *reinterpret_cast<const float2*>(scl + 2 * BN + c);
+                const uint32_t ph = pack_f16x2(pp.x * sv.x, pp.y * sv.y);
+                pk[k] = ph;
+                const float2 pr = unpack_f16x2(ph);
+                lacc = fma2(pr, iv, lacc);
+              } else {
+                const uint32_t pb = pack_bf16x2(pp.x, pp.y);
+                pk[k] = pb;
+                lacc = add2(lacc, make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
+              }
             }
             tmem_st16(tmem_s + 16 * q4 + lane_off, pk);
           }
@@ -930,7 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // keys past the prefix end in this tile: clear their V rows (page
           // tails may hold stale data; P is 0 there but 0 * NaN would poison
           // O).  Group 0 does it before P_0(t) V(t), the tile's first reader.
-          if (h == 0 && valid_keys < BN) {
+          if (!F8 && h == 0 && valid_keys < BN) {
             const int st = gt % kStages;
             mbar_wait(&vfull[st], (gt / kStages) & 1, abort_flag);  // acquire the TMA writes
             uint8_t* vtile = smem + Ly::kVRing + st * Ly::kTileBytes;
@@ -1069,25 +1251,31 @@ int launch_tree_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_set_device != dev) {
-    cudaFuncSetAttribute(tree_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Layout<128>::kAlloc);
-    cudaFuncSetAttribute(tree_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Layout<64>::kAlloc);
+    cudaFuncSetAttribute(tree_attn_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Layout<128, false>::kAlloc);
+    cudaFuncSetAttribute(tree_attn_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Layout<64, false>::kAlloc);
+    cudaFuncSetAttribute(tree_attn_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Layout<128, true>::kAlloc);
     attr_set_device = dev;
   }
   const int ctas = a.vctas * a.lanes;
   if (ctas < 1) return -1;
+  if (a.fp8 && a.head_dim != 128) return -1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(a.fp8 ? kThreadsF8 : kThreads, 1, 1);
   cfg.stream = stream;
   cudaError_t e;
-  if (a.head_dim == 128) {
-    cfg.dynamicSmemBytes = Layout<128>::kAlloc;
-    e = cudaLaunchKernelEx(&cfg, tree_attn_kernel<128>, a, maps);
+  if (a.fp8) {
+    cfg.dynamicSmemBytes = Layout<128, true>::kAlloc;
+    e = cudaLaunchKernelEx(&cfg, tree_attn_kernel<128, true>, a, maps);
+  } else if (a.head_dim == 128) {
+    cfg.dynamicSmemBytes = Layout<128, false>::kAlloc;
+    e = cudaLaunchKernelEx(&cfg, tree_attn_kernel<128, false>, a, maps);
   } else {
-    cfg.dynamicSmemBytes = Layout<64>::kAlloc;
-    e = cudaLaunchKernelEx(&cfg, tree_attn_kernel<64>, a, maps);
+    cfg.dynamicSmemBytes = Layout<64, false>::kAlloc;
+    e = cudaLaunchKernelEx(&cfg, tree_attn_kernel<64, false>, a, maps);
   }
   return e == cudaSuccess ? 0 : -1;
 }

@@ -99,11 +99,12 @@ bool plan_attention(const tv_attn_params* p, int sms, AttnPlan* out) {
 }
 
 bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+            const cuuint64_t* strides_bytes, const cuuint32_t* box,
+            CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+  return fn(m, type, rank, const_cast<void*>(base), dims,
             strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -174,56 +175,92 @@ int tv_tree_attention_plan(const tv_attn_params* p, int32_t sms, tv_attn_plan* o
   return TV_OK;
 }
 
-int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
-                      const uint16_t* k_prefix_blocks, const uint16_t* v_prefix_blocks,
-                      const int32_t* block_table, const uint16_t* k_nodes,
-                      const uint16_t* v_nodes, const int32_t* parent,
-                      const int32_t* prefix_lens, const int32_t* node_offsets, void* out,
-                      int32_t* status, void* workspace, size_t workspace_bytes,
-                      cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+struct Fp8Scales {
+  const float *q, *kp, *vp, *kn, *vn;
+};
+
+// The shared path of tv_tree_attention and tv_tree_attention_fp8: checks,
+// tensor maps, arguments, the status and counter memsets and the launch.
+int attention_call(const tv_attn_params* p, const Fp8Scales* f8, const void* q_nodes,
+                   const void* k_prefix_blocks, const void* v_prefix_blocks,
+                   const int32_t* block_table, const void* k_nodes, const void* v_nodes,
+                   const int32_t* parent, const int32_t* prefix_lens,
+                   const int32_t* node_offsets, void* out, int32_t* status, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
   if (!p) return TV_ERR_INVALID_ARG;
   if (p->head_dim != 64 && p->head_dim != 128) return TV_ERR_UNSUPPORTED;
+  if (f8 && p->head_dim != 128) return TV_ERR_UNSUPPORTED;
   AttnPlan pl;
   if (!plan_attention(p, sm_count(), &pl)) return TV_ERR_INVALID_ARG;
   const void* ptrs[] = {q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nodes,
                         v_nodes, parent, prefix_lens, node_offsets, out, status};
   for (const void* q : ptrs)
     if (!q || !aligned16(q)) return TV_ERR_INVALID_ARG;
+  if (f8) {
+    const void* sc[] = {f8->q, f8->kp, f8->vp, f8->kn, f8->vn};
+    for (const void* q : sc)
+      if (!q || !aligned16(q)) return TV_ERR_INVALID_ARG;
+  }
   if (!workspace || workspace_bytes < pl.workspace || !aligned16(workspace))
     return TV_ERR_WORKSPACE;
 
   const int D = p->head_dim, Hkv = p->num_kv_heads;
   tv::AttnMaps maps;
   std::memset(&maps, 0, sizeof maps);
-  // Paged pool as a 5-D tensor so that one box is one 16-token page of one
-  // KV head, landing in shared memory as [8-row group][64-column half][8 rows]
-  // [128 B]: dims (64 columns, 8 rows, halves, 2 row groups, pages), box
-  // (64, 8, halves, 2, 1).
-  const int halves = D / 64;
-  {
-    const cuuint64_t dims[5] = {64, 8, static_cast<cuuint64_t>(halves), 2,
-                                static_cast<cuuint64_t>(p->num_blocks) * Hkv};
-    const cuuint64_t str[4] = {static_cast<cuuint64_t>(D) * 2, 128,
-                               static_cast<cuuint64_t>(D) * 2 * 8, static_cast<cuuint64_t>(D) * 2 * 16};
-    const cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(halves), 2, 1};
-    if (!encode(&maps.k_pool, k_prefix_blocks, 5, dims, str, box)) return TV_ERR_CUDA;
-    if (!encode(&maps.v_pool, v_prefix_blocks, 5, dims, str, box)) return TV_ERR_CUDA;
-  }
-  // Tree K/V as a 4-D tensor (64 columns, nodes, halves, KV heads); a box is
-  // 8 consecutive nodes of one head: [half][8 rows][128 B].
-  {
-    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(p->total_nodes),
-                                static_cast<cuuint64_t>(halves), static_cast<cuuint64_t>(Hkv)};
-    const cuuint64_t str[3] = {static_cast<cuuint64_t>(D) * 2 * Hkv, 128,
-                               static_cast<cuuint64_t>(D) * 2};
-    const cuuint32_t box[4] = {64, 8, static_cast<cuuint32_t>(halves), 1};
-    if (!encode(&maps.k_nodes, k_nodes, 4, dims, str, box)) return TV_ERR_CUDA;
-    if (!encode(&maps.v_nodes, v_nodes, 4, dims, str, box)) return TV_ERR_CUDA;
+  if (f8) {
+    // E4M3 codes, one byte each, 128-byte rows.  Pool: (128 bytes, 16 rows,
+    // pages), box = one page (2 KB).  Tree K/V: (128 bytes, nodes, KV heads),
+    // box = 8 nodes of one head (1 KB).  128-byte swizzle.
+    const cuuint64_t pdims[3] = {128, 16, static_cast<cuuint64_t>(p->num_blocks) * Hkv};
+    const cuuint64_t pstr[2] = {128, 2048};
+    const cuuint32_t pbox[3] = {128, 16, 1};
+    if (!encode(&maps.k_pool, k_prefix_blocks, 3, pdims, pstr, pbox, CU_TENSOR_MAP_DATA_TYPE_UINT8))
+      return TV_ERR_CUDA;
+    if (!encode(&maps.v_pool, v_prefix_blocks, 3, pdims, pstr, pbox, CU_TENSOR_MAP_DATA_TYPE_UINT8))
+      return TV_ERR_CUDA;
+    const cuuint64_t ndims[3] = {128, static_cast<cuuint64_t>(p->total_nodes), static_cast<cuuint64_t>(Hkv)};
+    const cuuint64_t nstr[2] = {static_cast<cuuint64_t>(Hkv) * 128, 128};
+    const cuuint32_t nbox[3] = {128, 8, 1};
+    if (!encode(&maps.k_nodes, k_nodes, 3, ndims, nstr, nbox, CU_TENSOR_MAP_DATA_TYPE_UINT8))
+      return TV_ERR_CUDA;
+    if (!encode(&maps.v_nodes, v_nodes, 3, ndims, nstr, nbox, CU_TENSOR_MAP_DATA_TYPE_UINT8))
+      return TV_ERR_CUDA;
+  } else {
+    // Paged pool as a 5-D tensor so that one box is one 16-token page of one
+    // KV head, landing in shared memory as [8-row group][64-column half][8
+    // rows][128 B]: dims (64 columns, 8 rows, halves, 2 row groups, pages),
+    // box (64, 8, halves, 2, 1).
+    const int halves = D / 64;
+    {
+      const cuuint64_t dims[5] = {64, 8, static_cast<cuuint64_t>(halves), 2,
+                                  static_cast<cuuint64_t>(p->num_blocks) * Hkv};
+      const cuuint64_t str[4] = {static_cast<cuuint64_t>(D) * 2, 128,
+                                 static_cast<cuuint64_t>(D) * 2 * 8, static_cast<cuuint64_t>(D) * 2 * 16};
+      const cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(halves), 2, 1};
+      if (!encode(&maps.k_pool, k_prefix_blocks, 5, dims, str, box)) return TV_ERR_CUDA;
+      if (!encode(&maps.v_pool, v_prefix_blocks, 5, dims, str, box)) return TV_ERR_CUDA;
+    }
+    // Tree K/V as a 4-D tensor (64 columns, nodes, halves, KV heads); a box
+    // is 8 consecutive nodes of one head: [half][8 rows][128 B].
+    {
+      const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(p->total_nodes),
+                                  static_cast<cuuint64_t>(halves), static_cast<cuuint64_t>(Hkv)};
+      const cuuint64_t str[3] = {static_cast<cuuint64_t>(D) * 2 * Hkv, 128,
+                                 static_cast<cuuint64_t>(D) * 2};
+      const cuuint32_t box[4] = {64, 8, static_cast<cuuint32_t>(halves), 1};
+      if (!encode(&maps.k_nodes, k_nodes, 4, dims, str, box)) return TV_ERR_CUDA;
+      if (!encode(&maps.v_nodes, v_nodes, 4, dims, str, box)) return TV_ERR_CUDA;
+    }
   }
 
   const size_t ctas = static_cast<size_t>(pl.vctas) * pl.lanes;
   tv::AttnArgs a;
-  a.q = q_nodes;
+  std::memset(&a, 0, sizeof a);
+  a.q = static_cast<const uint16_t*>(q_nodes);
   a.block_table = block_table;
   a.parent = parent;
   a.prefix_lens = prefix_lens;
@@ -248,6 +285,14 @@ int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
   a.out_fp32 = p->out_dtype == TV_OUT_FP32 ? 1 : 0;
   const float scale = p->softmax_scale > 0.0f ? p->softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
   a.scale_log2 = scale * 1.4426950408889634f;
+  if (f8) {
+    a.fp8 = 1;
+    a.q_scale = f8->q;
+    a.kp_scale = f8->kp;
+    a.vp_scale = f8->vp;
+    a.kn_scale = f8->kn;
+    a.vn_scale = f8->vn;
+  }
 
   // status and the arrival counters of split units start at zero
   if (cudaMemsetAsync(status, 0, sizeof(int32_t) * p->batch, stream) != cudaSuccess)
@@ -255,6 +300,37 @@ int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
   if (cudaMemsetAsync(a.counters, 0, ctas * 8, stream) != cudaSuccess) return TV_ERR_CUDA;
   if (tv::launch_tree_attention(a, maps, stream) != 0) return TV_ERR_CUDA;
   return TV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tv_tree_attention(const tv_attn_params* p, const uint16_t* q_nodes,
+                      const uint16_t* k_prefix_blocks, const uint16_t* v_prefix_blocks,
+                      const int32_t* block_table, const uint16_t* k_nodes,
+                      const uint16_t* v_nodes, const int32_t* parent,
+                      const int32_t* prefix_lens, const int32_t* node_offsets, void* out,
+                      int32_t* status, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  return attention_call(p, nullptr, q_nodes, k_prefix_blocks, v_prefix_blocks, block_table,
+                        k_nodes, v_nodes, parent, prefix_lens, node_offsets, out, status,
+                        workspace, workspace_bytes, stream);
+}
+
+int tv_tree_attention_fp8(const tv_attn_params* p, const uint8_t* q_nodes, const float* q_scale,
+                          const uint8_t* k_prefix_blocks, const float* k_prefix_scale,
+                          const uint8_t* v_prefix_blocks, const float* v_prefix_scale,
+                          const int32_t* block_table, const uint8_t* k_nodes,
+                          const float* k_nodes_scale, const uint8_t* v_nodes,
+                          const float* v_nodes_scale, const int32_t* parent,
+                          const int32_t* prefix_lens, const int32_t* node_offsets, void* out,
+                          int32_t* status, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
+  const Fp8Scales sc = {q_scale, k_prefix_scale, v_prefix_scale, k_nodes_scale, v_nodes_scale};
+  return attention_call(p, &sc, q_nodes, k_prefix_blocks, v_prefix_blocks, block_table, k_nodes,
+                        v_nodes, parent, prefix_lens, node_offsets, out, status, workspace,
+                        workspace_bytes, stream);
 }
 
 size_t tv_accept_workspace_size(const tv_accept_params* p) {

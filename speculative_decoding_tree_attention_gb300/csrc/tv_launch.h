@@ -71,6 +71,14 @@ struct AttnArgs {
   int32_t min_tiles;          // fewest key tiles a virtual CTA is given
   int32_t out_fp32;           // 1: fp32 output, 0: bf16
   float scale_log2;           // softmax scale * log2(e)
+  // E4M3 inputs (tv_tree_attention_fp8): q, pools and tree K/V hold codes,
+  // each row of D codes with one fp32 scale
+  int32_t fp8;
+  const float* q_scale;       // [total_nodes][Hq]
+  const float* kp_scale;      // [num_blocks][Hkv][16]
+  const float* vp_scale;
+  const float* kn_scale;      // [total_nodes][Hkv]
+  const float* vn_scale;
 };
 
 struct AttnMaps {
