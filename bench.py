@@ -97,6 +97,32 @@ def attention_flops(case):
     return int(f)
 
 
+def attention_bytes_fp8(case):
+    """Algorithmic bytes of one FP8 tree-attention launch: prefix K+V codes and
+    their row scales once per (sequence, KV head), Q codes and scales, tree K/V
+    codes and scales, and the bf16 output."""
+    hq, hkv, D = case["num_q_heads"], case["num_kv_heads"], case["head_dim"]
+    L = np.asarray(case["prefix_lens"], np.int64)
+    tot = int(case["node_offsets"][-1])
+    return int(L.sum() * hkv * (2 * D + 8) + tot * hq * (D + 4) + tot * hkv * (2 * D + 8)
+               + tot * hq * D * 2)
+
+
+def fp8_inputs(d):
+    """E4M3 codes and per-row scales of a resident bf16 workload (the input
+    recipe's quantiser: scale = max |row| / 448, 1 for an all-zero row; codes
+    rounded to nearest even), made on the device with torch."""
+    import torch
+    out = {}
+    for k in ("q", "kp", "vp", "kn", "vn"):
+        x = d[k].float()
+        amax = x.abs().amax(dim=-1)
+        scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+        out[k] = (x / scale.unsqueeze(-1)).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+        out[k + "_scale"] = scale.contiguous()
+    return out
+
+
 def accept_bytes(case):
     """Algorithmic bytes of one accept launch (logits mode): the target row of
     every node with children (LSE), the draft rows of those nodes and the mask
@@ -371,6 +397,14 @@ class Step:
     def check(self):
         assert int(self.st_attn.max()) == 0 and int(self.acc_out["status"].max()) == 0, "status"
 
+    def attn_fp8(self, f):
+        d = self.d
+        self.tv.tree_attention_fp8(f["q"], f["q_scale"], f["kp"], f["kp_scale"], f["vp"],
+                                   f["vp_scale"], d["table"], f["kn"], f["kn_scale"], f["vn"],
+                                   f["vn_scale"], d["parent"], d["lens"], d["off"],
+                                   max_nodes=self.max_nodes, max_prefix_len=self.mpl,
+                                   out=self.out, status=self.st_attn, workspace=self.ws)
+
 
 def timed(fn, n, stream, flush, warm=3):
     """CUDA-event times (ms) of n calls of fn on `stream`, each after an L2
@@ -530,6 +564,30 @@ def main():
             "step_us": (statistics.mean(a_ms) + statistics.mean(c_ms)) * 1e3,
             "plan": tv.attention_plan(st.prm)}
         del st, ra, rc
+    # ---- FP8 tree attention (E4M3 inputs, [EC] §9.2) on the headline workload
+    # and on serving: half the K/V bytes
+    fp8 = {}
+    fp8_runs = ((("headline", step),) if cfg["d"] == 128 else ()) + \
+        (((f"{wl.config(3)['name']} (config 3)", None),) if 3 in side_cases else ())
+    for name, st in fp8_runs:
+        if st is None:
+            st = Step(tv, side_cases[3], wl.config(3), args.mode, dev)
+        f = fp8_inputs(st.d)
+        with torch.cuda.stream(stream):
+            st.attn_fp8(f)
+        stream.synchronize()
+        assert int(st.st_attn.max()) == 0, "fp8 attention status"
+        rf = graphed(lambda: st.attn_fp8(f), stream) if not args.no_graph else (lambda: st.attn_fp8(f))
+        f_ms = timed(rf, nb, stream, flush, warm=5)
+        f_s = statistics.mean(f_ms) / 1e3
+        fb, ff = attention_bytes_fp8(st.case), attention_flops(st.case)
+        fp8[name if st is not step else f"{cfg['name']} (config {cfg['num']})"] = {
+            "mean_us": f_s * 1e6, "algorithmic_bytes": fb, "hbm_gbs": fb / f_s / 1e9,
+            "hbm_frac": fb / f_s / 1e9 / peaks[0], "tflops": ff / f_s / 1e12,
+            "note": "tv_tree_attention_fp8: E4M3 Q/K/V, one scale per 128-code row"}
+        del f, rf
+        if st is not step:
+            del st
     torch.cuda.synchronize()
     clocks.load(t_load0, time.time())
     clk = clocks.stop()
@@ -627,6 +685,7 @@ def main():
         "roofline": roof,
         "accept": acc_entry,
         "workloads": side,
+        "fp8_attention": fp8,
         "e2e": {"value": world * tot * e2e_steps / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": step.launches_per_step * args.steps,

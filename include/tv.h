@@ -189,10 +189,12 @@ int tv_tree_attention(const tv_attn_params* params, const uint16_t* q_nodes,
  *   k_nodes, v_nodes u8 [total_nodes][Hkv][128],       k_nodes_scale, v_nodes_scale fp32 [total_nodes][Hkv]
  * Arithmetic: S = Q K^T on the tensor cores over the codes (E4M3 x E4M3,
  * fp32 accumulation), each score times its query row's and key row's scale;
- * fp32 online softmax; V converted exactly to fp16 and its row scale applied
- * to P (P' = P * scale in fp16, the row sum taking P' / scale), P' V in fp16
- * with fp32 accumulation.  The V scales times 256 must stay below 65504 (the
- * fp16 range of P').  All device pointers 16-byte aligned. */
+ * fp32 online softmax; each V row converted to fp16 as code x scale (the
+ * exact product rounded once), P rounded to fp16 (the row sum adds the
+ * rounded values), P V in fp16 with fp32 accumulation.  The dequantised V
+ * values must lie in the fp16 range (|code x scale| <= 65504, i.e. a V scale
+ * of at most 146 for codes up to 448); larger ones become infinite.  All
+ * device pointers 16-byte aligned (the scale arrays 4-byte). */
 int tv_tree_attention_fp8(const tv_attn_params* params, const uint8_t* q_nodes,
                           const float* q_scale, const uint8_t* k_prefix_blocks,
                           const float* k_prefix_scale, const uint8_t* v_prefix_blocks,

@@ -33,7 +33,7 @@
 // workspace slot, and the last piece to finish (an arrival counter per unit)
 // merges the slots in a fixed order, so results do not depend on timing.
 //
-// One CTA has 320 threads:
+// One CTA has 320 threads (384 for E4M3 inputs):
 //   warp 8  (TMA)      loads K and V tiles into two shared-memory rings: one 5-D
 //                      box per 16-token page through the block table (eight
 //                      pages per tile and tensor), or 16 boxes of 8 tree nodes;
@@ -51,11 +51,13 @@
 //                      ancestor bitmask, the row max, fp32 online softmax in
 //                      base 2 against a running max that moves only when it
 //                      grows by more than 2^8 (O is then rescaled in TMEM), and
-//                      P as bf16 pairs into TMEM; the row sum adds the rounded
+//                      P as 16-bit pairs into TMEM; the row sum adds the rounded
 //                      P, so O / l weights V exactly as the P V product did.
 //                      They also load Q (cp.async, in the 128-byte swizzled
 //                      layout the MMA reads), build the ancestor masks and
 //                      write or merge the results.
+//   warps 10-11        (E4M3 inputs) convert V tiles to fp16 with their row
+//                      scales.
 // TMEM (512 columns): S_0/P_0 at 0, S_1/P_1 at 128, O_0 at 256, O_1 at 256+D.
 // Every wait on an mbarrier is bounded; on expiry the CTA reports
 // TV_ERR_DEVICE_TIMEOUT for its sequence, drains its copies and returns.
@@ -82,6 +84,7 @@ constexpr int kMaxAncWords = kMaxNodes / 32;
 constexpr int kAncStride = kMaxAncWords + 1;  // odd word stride: rows of a warp hit distinct banks
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxPieces = 32;        // pieces per scheduling round
+constexpr int kSclSlots = 8;          // E4M3: scale slots (tile tau in slot tau % 8)
 
 // Named barriers (0 is __syncthreads): one per softmax group, both groups.
 constexpr int kBarGroup0 = 1;         // group h uses kBarGroup0 + h
@@ -104,14 +107,14 @@ struct Piece {
 
 // Shared memory of one CTA.  bf16 inputs: K and V tiles of 128 keys x D bf16
 // in 2-stage rings.  E4M3 inputs (F8, D = 128): K and raw V tiles of 128 keys
-// x 128 one-byte codes (a K ring of 3, a raw V ring of 2), two converted fp16
-// V tiles, and 4 slots of per-key scales (K scale, V scale, 1 / V scale).
+// x 128 one-byte codes (a K ring of 3, a raw V ring of 3), two converted fp16
+// V tiles, and 8 slots of per-key scales (K scales, V scales).
 template <int D, bool F8>
 struct Layout {
   static_assert(!F8 || D == 128, "E4M3 inputs need D = 128");
   static constexpr int kHalves = D / 64;               // 64-column halves of a 16-bit row
   static constexpr int kStages = F8 ? 3 : (D == 128 ? 2 : 4);  // K ring depth
-  static constexpr int kVStages = F8 ? 2 : kStages;    // V (raw) ring depth
+  static constexpr int kVStages = F8 ? 3 : kStages;    // V (raw) ring depth
   static constexpr int kGroupBytes = kHalves * 1024;   // 8 rows of a 16-bit tile
   static constexpr int kTileBytes = BN * D * 2;        // a 16-bit (bf16 or fp16) K or V tile
   static constexpr int kKTileBytes = F8 ? BN * D : kTileBytes;  // a K or raw V tile as loaded
@@ -121,8 +124,8 @@ struct Layout {
   static constexpr int kVRing = kKRing + kStages * kKTileBytes;
   static constexpr int kV16 = kVRing + kVStages * kKTileBytes;  // F8: converted V, 2 slots
   static constexpr int kV16Bytes = F8 ? 2 * kTileBytes : 0;
-  static constexpr int kScl = kV16 + kV16Bytes;        // F8: [4][3][128] floats
-  static constexpr int kSclBytes = F8 ? 4 * 3 * BN * 4 : 0;
+  static constexpr int kScl = kV16 + kV16Bytes;        // F8: [8][2][128] floats
+  static constexpr int kSclBytes = F8 ? kSclSlots * 2 * BN * 4 : 0;
   static constexpr int kAnc = kScl + kSclBytes;        // [2][128][kAncStride] words
   static constexpr int kAncBytes = 2 * BM * kAncStride * 4;
   static constexpr int kParent = kAnc + kAncBytes;     // [2][512]
@@ -137,10 +140,10 @@ struct Layout {
   static constexpr int kBlkBytes = 8 * 8 * 4;
   static constexpr int kBar = kBlk + kBlkBytes;
   // kfull[S], kempty[S], vfull[VS], vempty[VS], s_full[2], p_full[2],
-  // o_done[2], q_full[2], drain, v16full[2], v16empty[2]
-  static constexpr int kNumBars = 2 * kStages + 2 * kVStages + 13;
+  // o_done[2], q_full[2], drain, v16full[2], v16empty[2], sfull[8]
+  static constexpr int kNumBars = 2 * kStages + 2 * kVStages + 13 + kSclSlots;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kMiscBytes = 512;
+  static constexpr int kMiscBytes = 256;
   static constexpr int kTotal = kMisc + kMiscBytes;
   static constexpr int kAlloc = kTotal + 1024;  // slack for 1024-byte alignment
   static constexpr int kTmemCols = 512;
@@ -157,6 +160,7 @@ struct Misc {
   int tree_bad[2];            // per group: the tree of its current piece is malformed
   int piece_bad[kMaxPieces];  // a block id of the piece was out of range
 };
+static_assert(sizeof(Misc) <= Layout<128, true>::kMiscBytes, "Misc fits its area");
 
 // Partial-result slot: unnormalised O (fp32) as float4 [D/4][256 rows], so
 // that the lanes of a warp (consecutive rows) store and load consecutive 16
@@ -485,9 +489,10 @@ __device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t ou
 
 // ---------------------------------------------------------------- the kernel
 // F8: E4M3 inputs (tv_tree_attention_fp8): S = Q K^T on kind::f8f6f4 over the
-// codes, the K and Q row scales applied to the scores; V converted to fp16 by
-// warps 10-11 and its row scale folded into P (P' = P s_v in fp16, the row
-// sum takes P' / s_v); P' V on kind::f16 in fp16.
+// codes, the K and Q row scales applied to the scores; the keys' scales come
+// with the K tile (4-byte asynchronous copies by the TMA warp); V rows
+// converted to fp16 with their scale (one rounding of code x scale) by warps
+// 10-11; P in fp16 and P V on kind::f16.
 template <int D, bool F8>
 __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     tree_attn_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps) {
@@ -510,6 +515,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
   uint64_t* drain = q_full + 2;           // every MMA issued so far complete (once per round)
   uint64_t* v16full = drain + 1;          // F8 [2]: V(t) converted and its scales staged (64 arrivals)
   uint64_t* v16empty = v16full + 2;       // F8 [2]: the P V of tile t complete
+  uint64_t* sfull = v16empty + 2;         // F8 [8]: the K and V scales of tile t landed (32 arrivals)
   Misc* misc = reinterpret_cast<Misc*>(smem + Ly::kMisc);
   Piece* pieces = reinterpret_cast<Piece*>(smem + Ly::kPieces);
 
@@ -532,6 +538,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
       mbar_init(&v16full[k], kConvThreads);
       mbar_init(&v16empty[k], 1);
     }
+    for (int k = 0; k < kSclSlots; ++k) mbar_init(&sfull[k], 32);
     for (int h = 0; h < 2; ++h) {
       mbar_init(&s_full[h], 1);
       mbar_init(&p_full[h], BM);
@@ -618,6 +625,40 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
             const int node0 = pc.n0 + (t - pc.P) * BN + lane * 8;
             tma_load_3d(tile + lane * 1024, kv ? &maps.v_nodes : &maps.k_nodes, bar, 0, node0, pc.kvh);
           }
+          if (kv == 0) {
+            // the tile's K and V scales into slot tau % 8, lane u the keys
+            // 4u .. 4u+3 (page u / 4 of a prefix tile); keys past the prefix
+            // end or the tree, and pages with a bad block id, get 0
+            float* sc = reinterpret_cast<float*>(smem + Ly::kScl) + (tau % kSclSlots) * 2 * BN;
+            const bool prefix = t < pc.P;
+            const int valid = prefix ? min(BN, pc.L - t * BN) : min(BN, pc.N - (t - pc.P) * BN);
+            const int pblk = __shfl_sync(0xffffffffu, blk, lane >> 2);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int key = 4 * lane + j;
+              const float* sk = a.kp_scale;
+              const float* sv = a.vp_scale;
+              uint32_t n = 0;
+              if (key < valid) {
+                if (prefix) {
+                  if (pblk >= 0 && pblk < a.num_blocks) {
+                    const size_t idx = (static_cast<size_t>(pblk) * a.hkv + pc.kvh) * 16 + (key & 15);
+                    sk += idx;
+                    sv += idx;
+                    n = 4;
+                  }
+                } else {
+                  const size_t idx = static_cast<size_t>(pc.n0 + (t - pc.P) * BN + key) * a.hkv + pc.kvh;
+                  sk = a.kn_scale + idx;
+                  sv = a.vn_scale + idx;
+                  n = 4;
+                }
+              }
+              cpa4_zfill(sc + key, sk, n);
+              cpa4_zfill(sc + BN + key, sv, n);
+            }
+            cpa_arrive_noinc(&sfull[tau % kSclSlots]);
+          }
           return;
         }
         if (t < pc.P) {
@@ -672,6 +713,18 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
           }
         }
         int stop = 0;
+        if (!progressed && lane == 0) {
+          // sleep (at most about 200 ns) in try_wait on the slot likely to
+          // free first (bf16: the MMAs free K(x) after V(x - 1) and before
+          // V(x)) instead of polling, which takes issue slots from the
+          // softmax warps of this SM sub-partition
+          const bool k_next = kp < npieces;
+          const bool v_next = tv < tk;
+          if (v_next && (!k_next || tv - kVStages < tk - kStages))
+            mbar_try_wait_ns(&vempty[tv % kVStages], ((tv / kVStages) & 1) ^ 1, 200);
+          else if (k_next)
+            mbar_try_wait_ns(&kempty[tk % kStages], ((tk / kStages) & 1) ^ 1, 200);
+        }
         if (lane == 0) {
           if (progressed) {
             t_idle = 0;
@@ -686,6 +739,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
           break;
         }
       }
+      if constexpr (F8) cpa_wait_all();  // this lane's scale copies have landed
       if (lane == 0) {
         if (!ok) {
           record_status(a.status, pieces[min(vp, npieces - 1)].b, kDeviceTimeout);
@@ -805,16 +859,15 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
       __syncwarp();
     } else if (F8 && warp >= kConvWarp) {
       // ------------------------------------------------------ V conversion (E4M3)
-      // Per tile, once its raw V has landed and the converted slot is free
-      // (the P V of tile t - 2 is complete): the 128 keys' K scales, V
-      // scales and reciprocal V scales into scale slot t % 4, and the V codes
-      // as fp16 (exact) into converted slot t % 2, in the MN-major layout the
-      // P V MMA reads.  Keys past the prefix end or the tree get scale 0 and
-      // zero rows (page tails may hold stale codes).
+      // Per tile, once its raw V and its scales have landed and the converted
+      // slot is free (the P V of tile t - 2 is complete): each key's row as
+      // fp16 of code x V scale (one rounding of the exact product) into
+      // converted slot t % 2, in the MN-major layout the P V MMA reads.  Keys
+      // past the prefix end or the tree get zero rows (page tails may hold
+      // stale codes).
       if constexpr (F8) {
         const int ct = tid - kConvWarp * 32;  // 0 .. 63
-        const int* blk_ring = reinterpret_cast<const int*>(smem + Ly::kBlk);
-        float* scl = reinterpret_cast<float*>(smem + Ly::kScl);
+        const float* scl = reinterpret_cast<const float*>(smem + Ly::kScl);
         bool ok = true;
         int tau = g_tile;
         for (int p = 0; p < npieces; ++p) {
@@ -822,63 +875,57 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
           for (int t = pc.t0; t < pc.t1; ++t, ++tau) {
             const int vs = tau % kVStages;
             if (ok) ok = mbar_wait(&vfull[vs], (tau / kVStages) & 1, abort_flag);
+            if (ok) ok = mbar_wait(&sfull[tau % kSclSlots], (tau / kSclSlots) & 1, abort_flag);
             if (ok && tau >= 2) ok = mbar_wait(&v16empty[tau & 1], ((tau - 2) >> 1) & 1, abort_flag);
             if (!ok) {
               misc->abort = 1;
             } else {
-              float* sc = scl + (tau & 3) * 3 * BN;
+              const float* sv = scl + (tau % kSclSlots) * 2 * BN + BN;
               const bool prefix = t < pc.P;
               const int valid = prefix ? min(BN, pc.L - t * BN) : min(BN, pc.N - (t - pc.P) * BN);
-#pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                const int key = 2 * ct + j;
-                float sk = 0.0f, sv = 0.0f;
-                if (key < valid) {
-                  if (prefix) {
-                    const int blk = blk_ring[(tau & 7) * 8 + key / 16];
-                    if (blk >= 0 && blk < a.num_blocks) {
-                      const size_t idx = (static_cast<size_t>(blk) * a.hkv + pc.kvh) * 16 + (key & 15);
-                      sk = __ldg(a.kp_scale + idx);
-                      sv = __ldg(a.vp_scale + idx);
-                    }
-                  } else {
-                    const size_t idx = static_cast<size_t>(pc.n0 + (t - pc.P) * BN + key) * a.hkv + pc.kvh;
-                    sk = __ldg(a.kn_scale + idx);
-                    sv = __ldg(a.vn_scale + idx);
-                  }
-                }
-                sc[key] = sk;
-                sc[BN + key] = sv;
-                sc[2 * BN + key] = sv != 0.0f ? 1.0f / sv : 0.0f;
-              }
-              const uint8_t* raw = smem + Ly::kVRing + vs * Ly::kKTileBytes;
-              uint8_t* v16 = smem + Ly::kV16 + (tau & 1) * Ly::kTileBytes;
-              // item (key, c): codes of columns 16c .. 16c+15 of a key's row
-              // (raw: 128 bytes a row, 16-byte chunk c at chunk c ^ (key % 8))
-              for (int it = ct; it < BN * 8; it += kConvThreads) {
-                const int key = it >> 3, c = it & 7;
+              // thread ct: the 16 codes of columns 16c .. 16c+15 (c = ct % 8)
+              // of keys k0 + 8i, k0 = ct / 8, i = 0 .. 15.  Raw: 128 bytes a
+              // key, 16-byte chunk c at chunk c ^ (key % 8); fp16: [8-key
+              // group][64-column half][key][128 B], 16-byte chunk q of a
+              // line at chunk q ^ (key % 8).  key % 8 = k0 for every i.
+              const int k0 = ct >> 3, c = ct & 7;
+              const uint8_t* raw = smem + Ly::kVRing + vs * Ly::kKTileBytes + k0 * 128 + ((c ^ k0) << 4);
+              uint8_t* v16 = smem + Ly::kV16 + (tau & 1) * Ly::kTileBytes + (c >> 2) * 1024 + k0 * 128;
+              const int q0 = (((2 * c) & 7) ^ k0) << 4, q1 = (((2 * c + 1) & 7) ^ k0) << 4;
+              auto convert = [&](int i, bool live) {
                 uint32_t h[8];
-                if (key < valid) {
-                  const uint4 w = *reinterpret_cast<const uint4*>(raw + key * 128 + ((c ^ (key & 7)) << 4));
-                  h[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.x));
-                  h[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16));
-                  h[2] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.y));
-                  h[3] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16));
-                  h[4] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.z));
-                  h[5] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16));
-                  h[6] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.w));
-                  h[7] = e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16));
+                if (live) {
+                  const uint4 w = *reinterpret_cast<const uint4*>(raw + i * 1024);
+                  const float s1 = sv[k0 + 8 * i];
+                  const float2 s2 = make_float2(s1, s1);
+                  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    // codes -> fp16 (exact) -> fp32, times the scale, -> fp16
+                    uint32_t c01, c23;
+                    e4m3x4_to_f16x2x2(ww[k], c01, c23);
+                    const float2 v01 = mul2(unpack_f16x2(c01), s2);
+                    const float2 v23 = mul2(unpack_f16x2(c23), s2);
+                    h[2 * k] = pack_f16x2(v01.x, v01.y);
+                    h[2 * k + 1] = pack_f16x2(v23.x, v23.y);
+                  }
                 } else {
 #pragma unroll
                   for (int k = 0; k < 8; ++k) h[k] = 0u;
                 }
-                // fp16 layout: [8-key group][64-column half][key][128 B],
-                // 16-byte chunk q of a line at chunk q ^ (key % 8)
-                uint8_t* dst = v16 + (key >> 3) * Ly::kGroupBytes + (c >> 2) * 1024 + (key & 7) * 128;
-                *reinterpret_cast<uint4*>(dst + ((((2 * c) & 7) ^ (key & 7)) << 4)) =
-                    make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(dst + ((((2 * c + 1) & 7) ^ (key & 7)) << 4)) =
-                    make_uint4(h[4], h[5], h[6], h[7]);
+                uint8_t* dst = v16 + i * Ly::kGroupBytes;
+                *reinterpret_cast<uint4*>(dst + q0) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(dst + q1) = make_uint4(h[4], h[5], h[6], h[7]);
+              };
+              // a rolled loop: unrolled, the converter's bursts of independent
+              // instructions crowd out the softmax warps it shares an SM
+              // sub-partition with (measured slower)
+              if (valid == BN) {
+#pragma unroll 1
+                for (int i = 0; i < 16; ++i) convert(i, true);
+              } else {
+#pragma unroll 1
+                for (int i = 0; i < 16; ++i) convert(i, k0 + 8 * i < valid);
               }
               fence_proxy_async_smem();  // generic writes, read by the MMA
             }
@@ -946,9 +993,10 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
           const Piece& nx = pieces[p + 1];
           const int nr = nx.mp * kUnitRows + ur;
           if (ur < nx.rows) {
-            const uint16_t* q = a.q + (static_cast<size_t>(nx.n0 + nr / g) * a.hq + nx.kvh * g + nr % g) * D;
+            const uint8_t* q = reinterpret_cast<const uint8_t*>(a.q) +
+                               (static_cast<size_t>(nx.n0 + nr / g) * a.hq + nx.kvh * g + nr % g) * (F8 ? D : 2 * D);
 #pragma unroll
-            for (int k = 0; k < D * 2; k += 128) prefetch_l2(reinterpret_cast<const uint8_t*>(q) + k);
+            for (int k = 0; k < (F8 ? D : 2 * D); k += 128) prefetch_l2(q + k);
           }
         }
         // the tree of the sequence (pieces with node tiles): parents, the
@@ -997,22 +1045,25 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
           for (int c = 0; c < 4; ++c)
             tmem_ld32(tmem_s + 32 * c + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
           tmem_ld_wait();
-          const float* scl = reinterpret_cast<const float*>(smem + Ly::kScl) + (gt & 3) * 3 * BN;
           if constexpr (F8) {
-            // the keys' scales of this tile are staged with its converted V
-            if (!__all_sync(0xffffffffu, mbar_wait(&v16full[gt & 1], (gt >> 1) & 1, abort_flag))) {
+            // the keys' K scales (landed with the K tile, slot gt % 8)
+            if (!__all_sync(0xffffffffu, mbar_wait(&sfull[gt % kSclSlots], (gt / kSclSlots) & 1,
+                                                   abort_flag))) {
               ok = false;
               misc->abort = 1;
               mbar_arrive(&p_full[h]);
               continue;
             }
+            const float* sk = reinterpret_cast<const float*>(smem + Ly::kScl) + (gt % kSclSlots) * 2 * BN;
 #pragma unroll
             for (int c = 0; c < 128; c += 4) {
-              const float4 sk = *reinterpret_cast<const float4*>(scl + c);
-              x[c] *= sk.x;
-              x[c + 1] *= sk.y;
-              x[c + 2] *= sk.z;
-              x[c + 3] *= sk.w;
+              const float4 s4 = *reinterpret_cast<const float4*>(sk + c);
+              const float2 a2 = mul2(make_float2(x[c], x[c + 1]), make_float2(s4.x, s4.y));
+              const float2 b2 = mul2(make_float2(x[c + 2], x[c + 3]), make_float2(s4.z, s4.w));
+              x[c] = a2.x;
+              x[c + 1] = a2.y;
+              x[c + 2] = b2.x;
+              x[c + 3] = b2.y;
             }
           }
           // mask (scores stay unscaled by the softmax scale, which is folded
@@ -1059,13 +1110,14 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
             }
           }
           const float mref = m_run == -INFINITY ? 0.0f : m_run;
-          // P = 2^(s * scale * log2(e) - m) as bf16 pairs (column c holds keys
-          // 2c, 2c+1), written over S_h in four 16-column stores; masked
-          // scores are -inf -> 0.  The row sum adds the rounded values, so
-          // that O / l weights V exactly as the P V product did (with the
-          // unrounded sum the rounding of a dominant P biases the output by
-          // up to 2^-9 of its V row).  Exponent arguments and sums take two
-          // lanes per instruction.
+          // P = 2^(s * scale * log2(e) - m) as 16-bit pairs (column c holds
+          // keys 2c, 2c+1), written over S_h in four 16-column stores; masked
+          // scores are -inf -> 0.  bf16 P for bf16 inputs, fp16 P for E4M3
+          // inputs (the converted V is fp16).  The row sum adds the rounded
+          // values, so that O / l weights V exactly as the P V product did
+          // (with the unrounded sum the rounding of a dominant P biases the
+          // output by up to 2^-9 of its V row in bf16).  Exponent arguments
+          // and sums take two lanes per instruction.
           const float2 sc2 = make_float2(cq, cq);
           const float2 nm2 = make_float2(-mref, -mref);
           float2 lacc = make_float2(0.0f, 0.0f);
@@ -1077,14 +1129,10 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
               const float2 e = fma2(make_float2(x[32 * q4 + 2 * k], x[32 * q4 + 2 * k + 1]), sc2, nm2);
               const float2 pp = make_float2(ex2_approx(e.x), ex2_approx(e.y));
               if constexpr (F8) {
-                // P' = P s_v in fp16; the row sum takes P' / s_v
-                const int c = 32 * q4 + 2 * k;
-                const float2 sv = *reinterpret_cast<const float2*>(scl + BN + c);
-                const float2 iv = *reinterpret_cast<const float2*>(scl + 2 * BN + c);
-                const uint32_t ph = pack_f16x2(pp.x * sv.x, pp.y * sv.y);
+                // P in fp16 (the V scales are in the converted V rows)
+                const uint32_t ph = pack_f16x2(pp.x, pp.y);
                 pk[k] = ph;
-                const float2 pr = unpack_f16x2(ph);
-                lacc = fma2(pr, iv, lacc);
+                lacc = add2(lacc, unpack_f16x2(ph));
               } else {
                 const uint32_t pb = pack_bf16x2(pp.x, pp.y);
                 pk[k] = pb;

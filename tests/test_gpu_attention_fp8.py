@@ -85,6 +85,31 @@ def test_stale_page_tails_hold_nan_codes():
     full_compare_fp8(case, "fp8 NaN page tails")
 
 
+def test_v_scales_across_decades():
+    """V row scales set per sequence from 1e-3 to 5e3 times the quantiser's
+    (dequantised V up to about 3e4, inside the fp16 range of the converted
+    rows) and, in one sequence, spread per row over a decade each way: each
+    sequence's output divided by its factor matches the oracle's divided by it."""
+    case = fp8(wl.config(3, batch=4, hq=8, hkv=2, prefix=(200, 600), n=(10, 40)))
+    fac = [1e-3, 1.0, 30.0, 5e3]
+    off, L = case["node_offsets"], case["prefix_lens"]
+    spread = 10.0 ** wl.rng(77, 1).uniform(-1.0, 1.0, size=case["v_prefix_scale"].shape[1:])
+    seen = set()
+    for b in range(4):
+        pages = case["block_table"][b, : (int(L[b]) + 15) // 16]
+        assert not seen.intersection(pages.tolist())
+        seen.update(pages.tolist())
+        for pg in pages:
+            case["v_prefix_scale"][pg] *= np.float32(fac[b]) * (spread if b == 1 else 1.0)
+        case["v_nodes_scale"][off[b]:off[b + 1]] *= np.float32(fac[b])
+    gpu, st = run_fp8(case)
+    assert np.all(st == 0), st
+    ref = oracle.tree_attention(case)
+    for b in range(4):
+        sl = slice(off[b], off[b + 1])
+        assert_attention_close(gpu[sl] / fac[b], ref[sl] / fac[b], f"fp8 V scale x{fac[b]:g}")
+
+
 def test_bad_tree_status_and_zeros():
     case = fp8(wl.config(3, batch=3, hq=4, hkv=2, prefix=(40, 40), n=(4, 4)))
     off = case["node_offsets"]
