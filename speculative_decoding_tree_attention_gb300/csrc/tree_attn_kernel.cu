@@ -243,18 +243,32 @@ __device__ __forceinline__ int scan256(int v, int* scratch, int sid, int* total)
 
 // Range boundaries of the V virtual CTAs on a line of W tiles: virtual CTA v
 // takes [start(v), start(v+1)) with start(v) = floor(v W / V), computed as
-// v q + floor(v r / V) with W = q V + r (no 64-bit division).
+// v q + floor(v r / V) with W = q V + r.  floor(v r / V) (v r <= V^2 < 2^24)
+// comes from the fp32 product with 1/V, within one of the quotient, and one
+// exact integer correction: no division on the schedule's critical path.
 struct Line {
   int W, V, q, r;
-  __device__ __forceinline__ int start(int v) const { return v * q + (v * r) / V; }
-  // the virtual CTA whose range holds position p (0 <= p < W)
-  __device__ __forceinline__ int owner(int p) const {
-    int lo = 0, hi = V - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (start(mid) <= p) lo = mid; else hi = mid - 1;
+  float rV;  // 1 / V
+  __device__ __forceinline__ int start(int v) const {
+    const int n = v * r;
+    int k = static_cast<int>(static_cast<float>(n) * rV);
+    if (k * V > n) {
+      --k;
+    } else if ((k + 1) * V <= n) {
+      ++k;
     }
-    return lo;
+    return v * q + k;
+  }
+  float VW;  // V / W
+  // the virtual CTA whose range holds position p (0 <= p < W): the fp32
+  // estimate p V / W is within two of it; exact integer steps finish it
+  __device__ __forceinline__ int owner(int p) const {
+    int o = min(V - 1, max(0, static_cast<int>(static_cast<float>(p) * VW)));
+#pragma unroll 1
+    for (int k = 0; k < 4 && o > 0 && start(o) > p; ++k) --o;
+#pragma unroll 1
+    for (int k = 0; k < 4 && o + 1 < V && start(o + 1) <= p; ++k) ++o;
+    return o;
   }
 };
 
@@ -312,6 +326,8 @@ __device__ void build_schedule(const AttnArgs& a, uint8_t* smem, int round, int 
   line.V = max(1, min(a.vctas, W / max(1, a.min_tiles)));
   line.q = W / line.V;
   line.r = W % line.V;
+  line.rV = 1.0f / static_cast<float>(line.V);
+  line.VW = W > 0 ? static_cast<float>(line.V) / static_cast<float>(W) : 0.0f;
   const int V = line.V;
   int count = 0;  // pieces of this CTA before the current chunk (all rounds)
   if (W > 0 && v < V) {
@@ -425,12 +441,14 @@ __device__ __forceinline__ int piece_slot(const AttnArgs& a, const Piece& pc, in
 // sum_s 2^(m_s - M) l_s in piece order.  Thread `ur` of the participants
 // takes row ur of the unit.  Piece `own` is this CTA's: its (m, l) and O come
 // from registers and TMEM (the values it would have written), the others'
-// from their slots; the lanes of a warp read consecutive rows (coalesced),
-// a 32-column chunk of every piece in flight at a time.
+// from their slots; the lanes of a warp read consecutive rows (coalesced).
+// Half a row of a piece is loaded at a time (all its loads in flight
+// together), so a piece costs two round trips to L2, not one per 32 columns.
 template <int D>
 __device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t out_row, int own,
                            float m_own, float l_own, bool bad_own, uint32_t tmem_o) {
   using Sl = Slot<D>;
+  constexpr int kH = D / 2;
   const bool row_ok = ur < pc.rows;
   bool bad = bad_own;
   float M = -INFINITY, l = 0.0f;
@@ -450,24 +468,26 @@ __device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t ou
   }
   const float inv = (l > 0.0f && !bad) ? 1.0f / l : 0.0f;
 #pragma unroll 1
-  for (int c0 = 0; c0 < D; c0 += 32) {
-    float acc[32];
+  for (int c0 = 0; c0 < D; c0 += kH) {
+    float acc[kH];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) acc[k] = 0.0f;
+    for (int k = 0; k < kH; ++k) acc[k] = 0.0f;
 #pragma unroll 1
     for (int s = 0; s < pc.npieces; ++s) {
-      float v[32];
+      float v[kH];
       float ms = m_own;
       if (s == own) {
         // every thread of the warp loads TMEM together (a warp-wide load)
-        tmem_ld32(tmem_o + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
+#pragma unroll
+        for (int c = 0; c < kH; c += 32)
+          tmem_ld32(tmem_o + c0 + c, *reinterpret_cast<uint32_t(*)[32]>(&v[c]));
         tmem_ld_wait();
       } else if (row_ok) {
         const uint8_t* base = a.slots + static_cast<size_t>(piece_slot(a, pc, s)) * Sl::kBytes;
         ms = __ldcg(reinterpret_cast<const float2*>(base + Sl::kMl) + ur).x;
         const float4* o4 = reinterpret_cast<const float4*>(base + Sl::kO) + static_cast<size_t>(c0 / 4) * kUnitRows + ur;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kH / 4; ++k) {
           const float4 x = __ldcg(o4 + k * kUnitRows);
           v[4 * k] = x.x;
           v[4 * k + 1] = x.y;
@@ -478,12 +498,14 @@ __device__ void merge_unit(const AttnArgs& a, const Piece& pc, int ur, size_t ou
       if (!row_ok) continue;
       const float wgt = ms == -INFINITY ? 0.0f : exp2f(ms - M);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) acc[k] += wgt * v[k];
+      for (int k = 0; k < kH; ++k) acc[k] += wgt * v[k];
     }
     if (!row_ok) continue;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) acc[k] *= inv;
-    store_row_chunk<D>(a, out_row, c0, acc);
+    for (int k = 0; k < kH; ++k) acc[k] *= inv;
+#pragma unroll
+    for (int c = 0; c < kH; c += 32)
+      store_row_chunk<D>(a, out_row, c0 + c, *reinterpret_cast<const float(*)[32]>(&acc[c]));
   }
 }
 
@@ -987,10 +1009,11 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
               *reinterpret_cast<uint4*>(dst + (k >> 3) * 1024 + k % 8 * 16) = make_uint4(0, 0, 0, 0);
           }
         }
-        // the next piece's Q row of this thread into L2, so that its load
-        // after this piece's epilogue is short
+        // the next piece's Q row of this thread (and its tree's parents)
+        // into L2, so that its prologue after this piece's epilogue is short
         if (p + 1 < npieces && h < pieces[p + 1].nm) {
           const Piece& nx = pieces[p + 1];
+          if (nx.t1 > nx.P && r * 32 < nx.N) prefetch_l2(a.parent + nx.n0 + r * 32);
           const int nr = nx.mp * kUnitRows + ur;
           if (ur < nx.rows) {
             const uint8_t* q = reinterpret_cast<const uint8_t*>(a.q) +
@@ -1120,7 +1143,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
           // and sums take two lanes per instruction.
           const float2 sc2 = make_float2(cq, cq);
           const float2 nm2 = make_float2(-mref, -mref);
-          float2 lacc = make_float2(0.0f, 0.0f);
+          float2 lacc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t pk[16];
@@ -1132,16 +1155,16 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
                 // P in fp16 (the V scales are in the converted V rows)
                 const uint32_t ph = pack_f16x2(pp.x, pp.y);
                 pk[k] = ph;
-                lacc = add2(lacc, unpack_f16x2(ph));
+                acc_f16x2(ph, lacc[k & 1]);
               } else {
                 const uint32_t pb = pack_bf16x2(pp.x, pp.y);
                 pk[k] = pb;
-                lacc = add2(lacc, make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
+                acc_bf16x2(pb, lacc[k & 1]);
               }
             }
             tmem_st16(tmem_s + 16 * q4 + lane_off, pk);
           }
-          const float lsum = lacc.x + lacc.y;
+          const float lsum = (lacc[0].x + lacc[1].x) + (lacc[0].y + lacc[1].y);
           if (__any_sync(0xffffffffu, rescale)) {
             // O holds P(..t-1) V against the old max; P_h(t-1) V is complete
             // (S_h(t), which this thread has seen complete, was issued after it)

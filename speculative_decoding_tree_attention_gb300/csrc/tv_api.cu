@@ -91,7 +91,10 @@ bool plan_attention(const tv_attn_params* p, int sms, AttnPlan* out) {
   const long long wmax = static_cast<long long>(p->batch) * p->num_kv_heads * layers * tiles;
   if (wmax >= (1ll << 31)) return false;  // the device schedule counts tiles in 32 bits
   pl.min_tiles = kMinTiles;
-  pl.vctas = static_cast<int>(std::max(1ll, std::min<long long>(sms / pl.lanes, wmax / kMinTiles)));
+  // at most 4096 virtual CTAs: the device computes range boundaries with
+  // fp32 products of v r < 4096^2 = 2^24 (exact integers)
+  pl.vctas = static_cast<int>(
+      std::max(1ll, std::min<long long>({sms / pl.lanes, wmax / kMinTiles, 4096ll})));
   const size_t ctas = static_cast<size_t>(pl.vctas) * pl.lanes;
   pl.workspace = (ctas * 8 + 255) / 256 * 256 + 2 * ctas * tv::attn_slot_bytes(p->head_dim);
   *out = pl;

@@ -310,6 +310,21 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
 }
+// acc.x += lo(v), acc.y += hi(v) for a bf16 or fp16 pair v: the 16-bit
+// value widened exactly, one fp32 rounding (the same result as unpacking
+// and adding in fp32, in one instruction per value).
+__device__ __forceinline__ void acc_bf16x2(uint32_t v, float2& acc) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(v));
+}
+__device__ __forceinline__ void acc_f16x2(uint32_t v, float2& acc) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(v));
+}
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   float2 d;
   asm("{\n\t.reg .b64 ra, rb, rd;\n\t"

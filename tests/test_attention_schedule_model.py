@@ -29,7 +29,7 @@ def plan(batch, hq, hkv, max_nodes, max_prefix, sms=152, min_tiles=4):
     layers = -(-mpairs // lanes)
     tiles = -(-max_prefix // BN) + -(-max_nodes // BN)
     wmax = batch * hkv * layers * tiles
-    vctas = max(1, min(sms // lanes, wmax // min_tiles))
+    vctas = max(1, min(sms // lanes, wmax // min_tiles, 4096))
     return dict(g=g, lanes=lanes, vctas=vctas, min_tiles=min_tiles)
 
 
@@ -164,3 +164,56 @@ def test_random_batches(seed):
 def test_many_tiny_sequences_need_several_rounds():
     sched, W, V = check([0] * 2048, [1 + (i % 3) for i in range(2048)], 4, 4)
     assert max(len(p) for p in sched.values()) > 32   # more than one round of 32 pieces
+
+
+def start_fp32(v, W, V):
+    """The kernel's range boundary: v q + k, k = int(fp32(v r) * fp32(1 / V))
+    corrected once each way (W = q V + r)."""
+    q, r = divmod(W, V)
+    n = v * r
+    rV = np.float32(1.0) / np.float32(V)
+    k = int(np.float32(n) * rV)
+    if k * V > n:
+        k -= 1
+    elif (k + 1) * V <= n:
+        k += 1
+    return v * q + k
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 7, 19, 38, 76, 151, 152, 1000, 4095, 4096])
+def test_division_free_range_starts_are_exact(V):
+    rng = np.random.default_rng(V)
+    Ws = {V, V + 1, 2 * V - 1, 4 * V + 3, 2**31 - 1, 2**31 - 2}
+    Ws.update(int(x) for x in rng.integers(V, 2**31 - 1, 40))
+    for W in sorted(Ws):
+        vs = range(V + 1) if V <= 200 else sorted({0, 1, V - 1, V, *rng.integers(0, V + 1, 300).tolist()})
+        for v in vs:
+            assert start_fp32(v, W, V) == (v * W) // V, (v, W, V)
+
+
+def owner_fp32(p, W, V):
+    """The kernel's owner of line position p: int(fp32(p) * fp32(V / W)),
+    clamped to [0, V), then up to four exact steps each way."""
+    VW = np.float32(V) / np.float32(W)
+    o = min(V - 1, max(0, int(np.float32(p) * VW)))
+    for _ in range(4):
+        if o > 0 and start_fp32(o, W, V) > p:
+            o -= 1
+    for _ in range(4):
+        if o + 1 < V and start_fp32(o + 1, W, V) <= p:
+            o += 1
+    return o
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 19, 38, 152, 1000, 4096])
+def test_owner_estimate_finds_the_range(V):
+    rng = np.random.default_rng(100 + V)
+    for W in [V, V + 1, 2 * V + 1, 2**31 - 1] + [int(x) for x in rng.integers(V, 2**31 - 1, 25)]:
+        bounds = [(v * W) // V for v in range(V + 1)]
+        ps = {0, W - 1}
+        for v in range(0, V, max(1, V // 64)):
+            ps.update({bounds[v], max(0, bounds[v] - 1), min(W - 1, bounds[v + 1] - 1)})
+        ps.update(int(x) for x in rng.integers(0, W, 200))
+        for p in ps:
+            o = owner_fp32(p, W, V)
+            assert bounds[o] <= p < bounds[o + 1], (p, W, V, o)
