@@ -433,6 +433,21 @@ def graphed(fn, stream):
     return g.replay
 
 
+def time_retained(tv, d, cfg, rows, nb, stream, flush, peaks):
+    """tv_retained_set of every draft row of a workload that prunes, timed on
+    its own; the masks must equal the workload's."""
+    import torch
+    res = {}
+    r_ms = timed(lambda: res.__setitem__("m", tv.retained_set(d["draft"], float(cfg["mask_mass"]))),
+                 nb, stream, flush)
+    assert torch.equal(res["m"][0], d["mask"]), "retained set differs from the workload's masks"
+    r_s = statistics.mean(r_ms) / 1e3
+    r_bytes = rows * int(cfg["vocab"]) * 4 + res["m"][0].numel() * 4
+    return {"workload": f"{cfg['name']} (config {cfg['num']})", "mean_us": r_s * 1e6, "rows": rows,
+            "bytes": r_bytes, "achieved_gbs": r_bytes / r_s / 1e9, "frac": r_bytes / r_s / 1e9 / peaks[0],
+            "note": "tv_retained_set of every draft row (one CTA per row), timed on its own"}
+
+
 def kernel_entries(step, attn_ms, acc_ms, peaks, cfg_num):
     """Roofline of the attention call and the HBM fraction of the accept call."""
     peak_bw, peak_tf, peak_kind = peaks
@@ -562,7 +577,9 @@ def main():
         side[f"{wl.config(n)['name']} (config {n})"] = {
             "tree_nodes": st.tot, "attention": r, "accept": a,
             "step_us": (statistics.mean(a_ms) + statistics.mean(c_ms)) * 1e3,
-            "plan": tv.attention_plan(st.prm)}
+            "plan": tv.attention_plan(st.prm),
+            "retained_set": time_retained(tv, st.d, wl.config(n), st.tot, nb, stream, flush, peaks)
+            if wl.config(n).get("mask_mass") else None}
         del st, ra, rc
     # ---- FP8 tree attention (E4M3 inputs, [EC] §9.2) on the headline workload
     # and on serving: half the K/V bytes
@@ -613,17 +630,9 @@ def main():
     del cm
     # ---- retained set of the draft rows (the step before the accept pass's
     # renormalisation, for workloads that prune): reported on its own
-    retained = None
-    if cfg.get("mask_mass"):
-        res = {}
-        r_ms = timed(lambda: res.__setitem__("m", tv.retained_set(d["draft"], float(cfg["mask_mass"]))),
-                     nb, stream, flush)
-        assert torch.equal(res["m"][0], d["mask"]), "retained set differs from the workload's masks"
-        r_s = statistics.mean(r_ms) / 1e3
-        r_bytes = tot * int(cfg["vocab"]) * 4 + res["m"][0].numel() * 4
-        retained = {"mean_us": r_s * 1e6, "rows": tot, "bytes": r_bytes,
-                    "achieved_gbs": r_bytes / r_s / 1e9, "frac": r_bytes / r_s / 1e9 / peaks[0],
-                    "note": "tv_retained_set of every draft row, timed on its own"}
+    retained = time_retained(tv, d, cfg, tot, nb, stream, flush, peaks) if cfg.get("mask_mass") else None
+    if retained is None:
+        retained = next((w["retained_set"] for w in side.values() if w.get("retained_set")), None)
     # ---- the multi-candidate accept variant (siblings tried in order with
     # residual updates) on the same inputs, reported on its own
     m_out = {k: torch.empty_like(v) for k, v in acc_out.items()}

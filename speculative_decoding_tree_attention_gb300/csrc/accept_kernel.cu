@@ -846,174 +846,254 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
 // R = the shortest prefix of that order whose fixed-point mass sum of fix40
 // quanta reaches T (the caller's floor(mass * 2^40)), or the whole row.
 //
-// One cluster of C CTAs per row; thread t of rank k owns the 32 entries of
-// mask word k*512 + t.  Each thread sorts its 32 (key, id) pairs in registers
-// (key = the fp32 bit pattern, which orders non-negative floats; key desc, id
-// asc), so that the entries of one digit form runs.  A radix select over the
-// key, 8 bits a pass from the top, finds the key tau at which the cumulative
-// mass crosses T: each pass adds the quanta of the matching entries into
-// per-warp 256-bucket histograms with one atomic per run, the CTA histograms
-// are added over the cluster through distributed shared memory, and a suffix
-// scan picks the crossing digit.  Keys above tau are kept; of the keys equal
-// to tau, the c lowest ids with c = ceil((T - mass above tau) / fix40(tau)),
-// ranked by a block scan plus the cluster prefix of the per-CTA tie counts.
-// Every sum is an exact integer, so every CTA of the cluster takes the same
-// decisions.
-constexpr int kRsThreads = 512;
+// One CTA of 1024 threads per row, no cluster: a wave of one CTA per SM holds
+// about 150 rows (90 MB at V = 151936), so the row, read from HBM by the first
+// pass, is still in L2 for the later ones.  Every warp load is contiguous:
+// the order-free passes read 512-byte runs of float4s (16-byte aligned rows)
+// or 128-byte words, and the mask pass reads word by word with lane L on id
+// 32 word + L, so a word's mask bits are a ballot.  A radix select over the key (the
+// fp32 bit pattern, which orders non-negative floats), 8 bits a pass from the
+// top, finds the key tau at which the cumulative mass crosses T; each pass
+// sums the fix40 weights of the entries that match the digits found so far
+// into 256 buckets and picks the crossing digit by a suffix scan.
+//   pass 0 (every entry): private per-thread histograms of the 24 top bytes
+//     that can carry weight (plain adds, no conflicts: most entries share a
+//     few top bytes);
+//   pass 1 (the entries of the crossing top byte): per-warp-pair histograms
+//     of three 16-bit weight parts with 32-bit shared atomics, and the
+//     matching keys copied into shared memory (a slice per warp);
+//   passes 2, 3: the same over the copied keys (or the row again, if they
+//     did not fit).
+// Keys above tau are kept; of the keys equal to tau, the c lowest ids with
+// c = ceil((T - mass above tau) / fix40(tau)), ranked in id order by a block
+// scan of per-word tie counts.  Every sum is an exact integer.
+constexpr int kRsThreads = 1024;
 constexpr int kRsWarps = kRsThreads / 32;
-constexpr int kRsChunk = kRsThreads * 32;  // entries per CTA: one mask word per thread
-constexpr int kRsMaxCluster = 16;
+// Top bytes of keys with fix40 weight > 0 (q >= 2^-40): 43 .. 66 for q < 2^7;
+// larger top bytes (q >= 2^7, weight clamped) go to shared buckets.
+constexpr int kRsByte0 = 43;
+constexpr int kRsBytes = 24;
+constexpr int kRsHists = kRsWarps / 2;                      // one per warp pair
+constexpr int kRsPoolBytes = kRsBytes * kRsThreads * 8;     // pass 0's private histograms
+constexpr int kRsHistWords = kRsHists * 3 * 256;            // later passes' histograms (u32)
+constexpr int kRsKeysCap = kRsPoolBytes / 4 - kRsHistWords; // keys copied by pass 1
+constexpr int kRsSlice = kRsKeysCap / kRsWarps;             // ... in one slice per warp
 
 struct RsSmem {
-  uint32_t key[kRsChunk + kRsThreads];          // padded: entry i at i + i/32
-  unsigned long long whist[kRsWarps][256];      // per-warp digit histograms
-  unsigned long long slot[4][256];              // this CTA's histogram of pass p
+  // pass 0: u64 [24][1024]; passes 1-3: u32 [16][3][256] histograms, then
+  // the copied keys
+  alignas(16) uint8_t pool[kRsPoolBytes];
+  unsigned long long big[256];  // pass 0: top bytes above 66
+  unsigned long long hist[256];
   unsigned long long red[kRsWarps];
-  unsigned long long x_total, x_gt_count;       // cluster exchange slots
-  int x_ties;
-  int scan[kRsWarps];
+  int iscan[kRsWarps];
   int digit;
+  int nkeys[kRsWarps];  // keys pass 1 found, per warp (its slice holds the first kRsSlice)
   unsigned long long above;
+  unsigned long long total;
 };
 
-// fix40 of the float whose bit pattern is `key` (a q > 0, or 0), in integer
-// arithmetic: a normal q is m * 2^(e - 150) with m the 24-bit significand and
-// e the exponent field, so q * 2^40 = m * 2^(e - 110) and its floor is a
-// shift of m; q >= 32 (and +inf) clamps to 32 * 2^40; denormals give 0.
-__device__ __forceinline__ unsigned long long rs_weight(uint32_t key) {
-  if (key >= 0x42000000u) return 1ull << 45;
-  const uint32_t e = key >> 23;
-  const unsigned long long m = (key & 0x7fffffu) | (e ? 0x800000u : 0u);
-  const int sh = static_cast<int>(e) - 110;
-  return sh >= 0 ? (m << sh) : (sh > -32 ? (m >> -sh) : 0ull);
+// fix40 of the float whose bit pattern is `key` (a q > 0, or 0) in integer
+// arithmetic, without branches: a normal q is m * 2^(e - 150) with m the
+// 24-bit significand and e the exponent field, so floor(q * 2^40) =
+// m << (e - 110) for e >= 110 and m >> (110 - e) below; e < 87 (and 0,
+// denormals) gives 0, q >= 32 (and +inf) clamps to 32 * 2^40.
+__device__ __forceinline__ unsigned long long rs_weight_key(uint32_t key) {
+  const int e = static_cast<int>(key >> 23);
+  const uint32_t m = (key & 0x7fffffu) | 0x800000u;
+  const int s = e - 110;
+  const uint32_t lo = m >> min(max(-s, 0), 31);         // e < 110: the right shift
+  const unsigned long long w = static_cast<unsigned long long>(lo) << max(s, 0);  // e >= 110
+  return key >= 0x42000000u ? (1ull << 45) : (e < 87 ? 0ull : w);
+}
+__device__ __forceinline__ uint32_t rs_key(float x) { return x > 0.0f ? __float_as_uint(x) : 0u; }
+// fix40 of q = x if x > 0 else 0 (NaN gives 0)
+__device__ __forceinline__ unsigned long long rs_weight(float x) { return rs_weight_key(rs_key(x)); }
+
+// Lane L of a warp reads id 32 word + L: a warp's load of one word is one
+// 128-byte line, and the words w, w + 32, ... of the 32 warps make the CTA
+// read 4 KB of consecutive ids at a time.  Ids past V read as 0.
+__device__ __forceinline__ float rs_load(const float* q, int V, int id) {
+  return id < V ? __ldcg(q + id) : 0.0f;
+}
+
+// Adds weight w (< 2^46) of digit d as three 16-bit parts: at most 16384
+// entries of a pass reach one histogram (two warps, at most 8192 words of a
+// row for V <= 2^18, one entry a word per lane), so each part sum stays below
+// 2^30.
+__device__ __forceinline__ void rs_add(uint32_t* h, uint32_t d, unsigned long long w) {
+  if (w & 0xffffull) atomicAdd(h + d, static_cast<uint32_t>(w & 0xffffull));
+  if ((w >> 16) & 0xffffull) atomicAdd(h + 256 + d, static_cast<uint32_t>((w >> 16) & 0xffffull));
+  if (w >> 32) atomicAdd(h + 512 + d, static_cast<uint32_t>(w >> 32));
+}
+
+constexpr int kRsUnroll = 8;  // loads of a warp in flight
+
+// The order-free passes (0 and 1) on a 16-byte aligned row (V % 4 == 0):
+// lane L of warp w reads float4 (32 g + L) for the groups g = w, w + 32, ...,
+// so a warp load is 512 consecutive bytes and a CTA keeps 8 x 16 KB in
+// flight.  Float4s past the row read as zeros.
+__device__ __forceinline__ float4 rs_load4(const float* q, int nf, int f) {
+  return f < nf ? __ldcg(reinterpret_cast<const float4*>(q) + f) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+}
+
+// Pass 0's update for one entry: its weight into this thread's private
+// bucket of its top byte (or the shared bucket of a top byte above 66).
+__device__ __forceinline__ void rs_count0(RsSmem& sm, unsigned long long* priv, int tid, float x) {
+  const unsigned long long w = rs_weight(x);
+  if (w) {  // x > 0 and its top byte >= 43
+    const int d = static_cast<int>(__float_as_uint(x) >> 24) - kRsByte0;
+    if (d < kRsBytes) {
+      priv[d * kRsThreads + tid] += w;
+    } else {
+      atomicAdd(&sm.big[d + kRsByte0], w);
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kRsThreads, 1)
     retained_set_kernel(const RetainArgs a) {
   extern __shared__ __align__(16) uint8_t rs_raw[];
   RsSmem& sm = *reinterpret_cast<RsSmem*>(rs_raw);
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = static_cast<int>(cluster.num_blocks());
-  const int rank = static_cast<int>(cluster.block_rank());
-  const int row = blockIdx.y;
+  const int row = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t lt_mask = (1u << lane) - 1u;
   const int V = a.vocab;
-  const int lo = rank * kRsChunk;
-  const float* q = a.draft + static_cast<size_t>(row) * V;
-
-  // keys into shared memory (coalesced loads, all 32 of a thread in flight)
-  {
-    float xv[32];
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const int v = lo + tid + r * kRsThreads;
-      xv[r] = v < V ? __ldg(q + v) : 0.0f;
-    }
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const int i = tid + r * kRsThreads;
-      sm.key[i + (i >> 5)] = (xv[r] > 0.0f) ? __float_as_uint(xv[r]) : 0u;
-    }
-  }
-  __syncthreads();
-  // this thread's 32 entries as (key << 5 | 31 - j), sorted descending: key
-  // desc, then id asc
-  unsigned long long e[32];
-  unsigned long long mine = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const uint32_t k = sm.key[tid * 33 + j];
-    e[j] = (static_cast<unsigned long long>(k) << 5) | static_cast<unsigned long long>(31 - j);
-    mine += rs_weight(k);
-  }
-#pragma unroll
-  for (int kk = 2; kk <= 32; kk <<= 1) {
-#pragma unroll
-    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int l = i ^ jj;
-        if (l > i) {
-          const bool desc = (i & kk) == 0;
-          const unsigned long long x = e[i], y = e[l];
-          const bool sw = desc ? (x < y) : (x > y);
-          e[i] = sw ? y : x;
-          e[l] = sw ? x : y;
-        }
-      }
-    }
-  }
-  // total mass of the row
-  for (int o = 16; o; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-  if (lane == 0) sm.red[warp] = mine;
-  __syncthreads();
-  if (tid == 0) {
-    unsigned long long t = 0;
-    for (int w = 0; w < kRsWarps; ++w) t += sm.red[w];
-    sm.x_total = t;
-  }
-  cluster.sync();
-  unsigned long long total = lane < C ? *cluster.map_shared_rank(&sm.x_total, lane) : 0ull;
-  for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-  const unsigned long long T = a.threshold;
   const int words = (V + 31) >> 5;
+  const bool vec = (V & 3) == 0;  // the row starts 16-byte aligned
+  const int nf = V >> 2;          // its float4s when vec
+  const float* q = a.draft + static_cast<size_t>(row) * V;
   uint32_t* mrow = a.mask + static_cast<size_t>(row) * words;
-  const int word = rank * kRsThreads + tid;  // this thread's mask word
+  const unsigned long long T = a.threshold;
+  unsigned long long* priv = reinterpret_cast<unsigned long long*>(sm.pool);
+  uint32_t* whist = reinterpret_cast<uint32_t*>(sm.pool);
+  uint32_t* keys = whist + kRsHistWords + warp * kRsSlice;  // this warp's slice
+  uint32_t* myh = whist + (warp >> 1) * 3 * 256;
 
-  if (total < T) {  // the mass never reaches T: every token is kept
-    if (word < words) {
-      const int v0 = word * 32;
-      mrow[word] = (V - v0 >= 32) ? 0xffffffffu : ((1u << (V - v0)) - 1u);
-    }
-    if (rank == 0 && tid == 0) {
-      if (a.z_fixed) a.z_fixed[row] = total;
-      if (a.z) a.z[row] = __fmul_rn(__ull2float_rn(total), kTwoM40);
-      if (a.kept) a.kept[row] = V;
-    }
-    cluster.sync();  // no CTA leaves while another may read its slots
-    return;
-  }
-
-  // radix select: the key tau at which the cumulative mass (keys in
-  // descending order) first reaches T
   uint32_t prefix = 0;
   unsigned long long above = 0;  // mass of the keys above the current prefix range
+  bool copied = false;           // pass 1 copied every matching key
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < kRsWarps * 256; i += kRsThreads) (&sm.whist[0][0])[i] = 0ull;
-    __syncthreads();
-    // matching entries are contiguous in the sorted order, and so are the
-    // entries of one digit: one atomic per run
-    uint32_t cur = 256u;
-    unsigned long long acc = 0;
+    if (pass == 0) {
+      // ---- top byte, every entry: private histograms [byte][thread]
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t k = static_cast<uint32_t>(e[j] >> 5);
-      if (pass == 0 || (k >> (shift + 8)) == prefix) {
-        const unsigned long long w = rs_weight(k);
-        const uint32_t d = (k >> shift) & 255u;
-        if (d != cur) {
-          if (acc) atomicAdd(&sm.whist[warp][cur], acc);
-          cur = d;
-          acc = 0;
+      for (int b = 0; b < kRsBytes; ++b) priv[b * kRsThreads + tid] = 0ull;
+      if (tid < 256) sm.big[tid] = 0ull;
+      __syncthreads();
+      if (vec) {
+        for (int g0 = warp; g0 * 32 < nf; g0 += kRsWarps * kRsUnroll) {
+          float4 x[kRsUnroll];
+#pragma unroll
+          for (int u = 0; u < kRsUnroll; ++u) x[u] = rs_load4(q, nf, (g0 + u * kRsWarps) * 32 + lane);
+#pragma unroll
+          for (int u = 0; u < kRsUnroll; ++u) {
+            rs_count0(sm, priv, tid, x[u].x);
+            rs_count0(sm, priv, tid, x[u].y);
+            rs_count0(sm, priv, tid, x[u].z);
+            rs_count0(sm, priv, tid, x[u].w);
+          }
         }
-        acc += w;
+      } else {
+        for (int w0 = warp; w0 < words; w0 += kRsWarps * kRsUnroll) {
+          float x[kRsUnroll];
+#pragma unroll
+          for (int u = 0; u < kRsUnroll; ++u) {
+            const int word = w0 + u * kRsWarps;
+            x[u] = word < words ? rs_load(q, V, word * 32 + lane) : 0.0f;
+          }
+#pragma unroll
+          for (int u = 0; u < kRsUnroll; ++u) rs_count0(sm, priv, tid, x[u]);
+        }
+      }
+      __syncthreads();
+      // bucket sums: a warp per weight-carrying byte, then a warp sum
+      for (int b = warp; b < kRsBytes; b += kRsWarps) {
+        unsigned long long y = 0;
+        for (int i = lane; i < kRsThreads; i += 32) y += priv[b * kRsThreads + i];
+        for (int o = 16; o; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+        if (lane == 0) sm.hist[kRsByte0 + b] = y;
+      }
+      if (tid < 256 && (tid < kRsByte0 || tid >= kRsByte0 + kRsBytes))
+        sm.hist[tid] = tid < kRsByte0 ? 0ull : sm.big[tid];
+    } else {
+      for (int i = tid; i < kRsHistWords; i += kRsThreads) whist[i] = 0u;
+      __syncthreads();
+      if (pass == 1 || !copied) {
+        // ---- the row again (from L2): entries matching the prefix.  Zero
+        // entries (past the row, q <= 0) match no prefix: every prefix holds
+        // a top byte >= 43.  `take` adds one entry whose warp-wide match
+        // ballot is mb and, in pass 1, copies its key to slot wpos + (its
+        // rank among the ballot's lanes) of the warp's slice; wpos (the
+        // warp's keys so far) is the same in every lane.
+        int wpos = 0;
+        auto take = [&](float x, uint32_t mb) {
+          if ((mb >> lane) & 1u) {
+            const uint32_t k = rs_key(x);
+            rs_add(myh, (k >> shift) & 255u, rs_weight(x));
+            if (pass == 1) {
+              const int p = wpos + __popc(mb & lt_mask);
+              if (p < kRsSlice) keys[p] = k;
+            }
+          }
+          wpos += __popc(mb);
+        };
+        auto match = [&](float x) { return __ballot_sync(0xffffffffu, (rs_key(x) >> (shift + 8)) == prefix); };
+        if (vec) {
+          for (int g0 = warp; g0 * 32 < nf; g0 += kRsWarps * kRsUnroll) {
+            float4 x[kRsUnroll];
+#pragma unroll
+            for (int u = 0; u < kRsUnroll; ++u) x[u] = rs_load4(q, nf, (g0 + u * kRsWarps) * 32 + lane);
+#pragma unroll
+            for (int u = 0; u < kRsUnroll; ++u) {
+              take(x[u].x, match(x[u].x));
+              take(x[u].y, match(x[u].y));
+              take(x[u].z, match(x[u].z));
+              take(x[u].w, match(x[u].w));
+            }
+          }
+        } else {
+          for (int w0 = warp; w0 < words; w0 += kRsWarps * kRsUnroll) {
+            float x[kRsUnroll];
+#pragma unroll
+            for (int u = 0; u < kRsUnroll; ++u) {
+              const int word = w0 + u * kRsWarps;
+              x[u] = word < words ? rs_load(q, V, word * 32 + lane) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < kRsUnroll; ++u) take(x[u], match(x[u]));
+          }
+        }
+        if (pass == 1 && lane == 0) sm.nkeys[warp] = wpos;
+      } else {
+        // ---- the keys pass 1 copied: each warp its own slice
+        const int n = sm.nkeys[warp];
+        for (int i = lane; i < n; i += 32) {
+          const uint32_t k = keys[i];
+          if ((k >> (shift + 8)) == prefix) rs_add(myh, (k >> shift) & 255u, rs_weight(__uint_as_float(k)));
+        }
+      }
+      __syncthreads();
+      if (tid < 256) {
+        unsigned long long h = 0;
+        for (int g = 0; g < kRsHists; ++g) {
+          const uint32_t* hg = whist + g * 3 * 256;
+          h += static_cast<unsigned long long>(hg[tid]) + (static_cast<unsigned long long>(hg[256 + tid]) << 16) +
+               (static_cast<unsigned long long>(hg[512 + tid]) << 32);
+        }
+        sm.hist[tid] = h;
+      }
+      if (pass == 1) {  // every warp's keys fit its slice (counts written before the barrier above)
+        int most = 0;
+        for (int w = 0; w < kRsWarps; ++w) most = max(most, sm.nkeys[w]);
+        copied = most <= kRsSlice;
       }
     }
-    if (acc) atomicAdd(&sm.whist[warp][cur], acc);
     __syncthreads();
-    if (tid < 256) {
-      unsigned long long h = 0;
-      for (int w = 0; w < kRsWarps; ++w) h += sm.whist[w][tid];
-      sm.slot[pass][tid] = h;
-    }
-    cluster.sync();
-    // digit d = tid (< 256): cluster histogram H[d] and the suffix mass above d
-    unsigned long long H = 0;
-    if (tid < 256)
-      for (int c = 0; c < C; ++c) H += cluster.map_shared_rank(&sm.slot[pass][0], c)[tid];
-    // suffix sums over the 256 digits, descending: warps 0-7 hold digits
-    // 32w .. 32w+31; first within the warp, then across the 8 warps
+    // digit d = tid (< 256): the suffix mass over the buckets; warps 0-7
+    // hold digits 32w .. 32w+31, first summed within the warp (descending),
+    // then across the 8 warps
+    const unsigned long long H = tid < 256 ? sm.hist[tid] : 0ull;
     unsigned long long incl = H;  // sum over digits >= d within the warp
     for (int o = 1; o < 32; o <<= 1) {
       const unsigned long long y = __shfl_down_sync(0xffffffffu, incl, o);
@@ -1026,91 +1106,108 @@ __global__ void __launch_bounds__(kRsThreads, 1)
       for (int w = warp + 1; w < 8; ++w) higher += sm.red[w];
       const unsigned long long ge = above + higher + incl;  // mass of digits >= d
       const unsigned long long gt = ge - H;                 // mass of digits > d
+      if (pass == 0 && tid == 0) sm.total = ge;             // digit 0: the whole row
       if (gt < T && ge >= T) {
         sm.digit = tid;
         sm.above = gt;
       }
     }
     __syncthreads();
+    if (pass == 0 && sm.total < T) {  // the mass never reaches T: every token is kept
+      const unsigned long long total = sm.total;
+      for (int word = tid; word < words; word += kRsThreads) {
+        const int v0 = word * 32;
+        mrow[word] = (V - v0 >= 32) ? 0xffffffffu : ((1u << (V - v0)) - 1u);
+      }
+      if (tid == 0) {
+        if (a.z_fixed) a.z_fixed[row] = total;
+        if (a.z) a.z[row] = __fmul_rn(__ull2float_rn(total), kTwoM40);
+        if (a.kept) a.kept[row] = V;
+      }
+      return;
+    }
     prefix = (prefix << 8) | static_cast<uint32_t>(sm.digit);
     above = sm.above;
-    __syncthreads();  // sm.red / sm.digit are rewritten next pass
+    __syncthreads();  // sm.red / sm.digit / sm.hist / the histograms are rewritten next pass
   }
   const uint32_t tau = prefix;
-  const unsigned long long wt = rs_weight(tau);  // > 0: the crossing adds mass
-  const unsigned long long need = (T - above + wt - 1) / wt;  // ties to keep
+  const unsigned long long wt = rs_weight(__uint_as_float(tau));  // > 0: the crossing adds mass
+  const unsigned long long need = (T - above + wt - 1) / wt;       // ties to keep
 
-  // ranks of the ties (key == tau) in id order: the thread's ties are in id
-  // order already; block scan of the per-thread counts, plus the counts of
-  // the lower-ranked CTAs of the cluster
-  int nt = 0, ngt = 0;
+  // the mask, in rounds of 1024 consecutive words: warp w reads words
+  // base + 32w + j (j = 0..31, lane L holding id 32 word + L), so a word's
+  // keep and tie bits are two ballots, and lane L keeps those of word
+  // base + 32w + L.  The ties' ranks in id order are the ties of the earlier
+  // rounds plus a block scan of the per-word counts of this round.
+  unsigned long long ties_before = 0;  // ties in the earlier rounds
+  int n_gt = 0;                        // kept keys above tau in this thread's words
+  for (int base = 0; base < words; base += kRsThreads) {
+    const int wb = base + 32 * warp;
+    uint32_t gtb = 0, tieb = 0;
+    {
+      float x[32];  // the warp's 32 words of the round, all loads in flight
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const uint32_t k = static_cast<uint32_t>(e[j] >> 5);
-    nt += k == tau;
-    ngt += k > tau;
-  }
-  int incl_t = nt;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl_t, o);
-    if (lane >= o) incl_t += y;
-  }
-  int gtw = ngt;
-  for (int o = 16; o; o >>= 1) gtw += __shfl_xor_sync(0xffffffffu, gtw, o);
-  if (lane == 31) sm.scan[warp] = incl_t;
-  if (lane == 0) sm.red[warp] = static_cast<unsigned long long>(gtw);
-  __syncthreads();
-  int before = incl_t - nt;
-  for (int w = 0; w < warp; ++w) before += sm.scan[w];
-  if (tid == 0) {
-    int ties = 0;
-    unsigned long long g = 0;
-    for (int w = 0; w < kRsWarps; ++w) {
-      ties += sm.scan[w];
-      g += sm.red[w];
-    }
-    sm.x_ties = ties;
-    sm.x_gt_count = g;
-  }
-  cluster.sync();
-  int ties_below = 0;
-  unsigned long long n_gt = 0;
-  {
-    const int t = lane < C ? *cluster.map_shared_rank(&sm.x_ties, lane) : 0;
-    const unsigned long long g = lane < C ? *cluster.map_shared_rank(&sm.x_gt_count, lane) : 0ull;
-    int tb = lane < rank ? t : 0;
-    n_gt = g;
-    for (int o = 16; o; o >>= 1) {
-      tb += __shfl_xor_sync(0xffffffffu, tb, o);
-      n_gt += __shfl_xor_sync(0xffffffffu, n_gt, o);
-    }
-    ties_below = tb;
-  }
-  // this thread's mask word, from the sorted entries (bit = id within word)
-  if (word < words) {
-    uint32_t m = 0;
-    int r = ties_below + before;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t k = static_cast<uint32_t>(e[j] >> 5);
-      const int id = 31 - static_cast<int>(e[j] & 31ull);
-      bool keep = k > tau;
-      if (k == tau) {
-        keep = static_cast<unsigned long long>(r) < need;
-        ++r;
+      for (int u = 0; u < 32; ++u) {
+        const int word = wb + u;
+        x[u] = word < words ? rs_load(q, V, word * 32 + lane) : 0.0f;
       }
-      if (keep) m |= 1u << id;
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        const uint32_t k = rs_key(x[u]);
+        const uint32_t g = __ballot_sync(0xffffffffu, k > tau);
+        const uint32_t t = __ballot_sync(0xffffffffu, k == tau);
+        if (lane == u) {
+          gtb = g;
+          tieb = t;
+        }
+      }
     }
-    if (V - word * 32 < 32) m &= (1u << (V - word * 32)) - 1u;  // no bits past the row
-    mrow[word] = m;
+    const int word = wb + lane;  // this thread's word (masks 0 past the row)
+    const int c = __popc(tieb);
+    n_gt += __popc(gtb);
+    int incl_t = c;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl_t, o);
+      if (lane >= o) incl_t += y;
+    }
+    if (lane == 31) sm.iscan[warp] = incl_t;
+    __syncthreads();
+    int before = incl_t - c;
+    int round_ties = 0;
+    for (int w = 0; w < kRsWarps; ++w) {
+      const int y = sm.iscan[w];
+      if (w < warp) before += y;
+      round_ties += y;
+    }
+    if (word < words) {
+      // keep this word's ties of rank < need, lowest ids first
+      const unsigned long long r0 = ties_before + static_cast<unsigned long long>(before);
+      uint32_t keep = 0;
+      if (r0 < need) {
+        const unsigned long long m = need - r0;
+        uint32_t t = tieb;
+        for (unsigned long long i = 0; i < m && t; ++i) {
+          keep |= t & (0u - t);
+          t &= t - 1u;
+        }
+      }
+      mrow[word] = gtb | keep;
+    }
+    ties_before += static_cast<unsigned long long>(round_ties);
+    __syncthreads();  // sm.iscan is rewritten next round
   }
-  if (rank == 0 && tid == 0) {
+  // keys above tau over the row
+  for (int o = 16; o; o >>= 1) n_gt += __shfl_xor_sync(0xffffffffu, n_gt, o);
+  if (lane == 0) sm.iscan[warp] = n_gt;
+  __syncthreads();
+  if (tid == 0) {
+    long long g = 0;
+    for (int w = 0; w < kRsWarps; ++w) g += sm.iscan[w];
     const unsigned long long Z = above + need * wt;
     if (a.z_fixed) a.z_fixed[row] = Z;
     if (a.z) a.z[row] = __fmul_rn(__ull2float_rn(Z), kTwoM40);
-    if (a.kept) a.kept[row] = static_cast<int>(n_gt + need);
+    if (a.kept) a.kept[row] = static_cast<int>(g + static_cast<long long>(need));
   }
-  cluster.sync();  // no CTA leaves while another may read its slots
 }
 }  // namespace
 
@@ -1192,33 +1289,17 @@ size_t accept_workspace_bytes(int vocab, int total_nodes) {
 
 int accept_max_nodes() { return kMaxN; }
 
-int retained_cluster_size(int vocab) { return (vocab + kRsChunk - 1) / kRsChunk; }
-
 int launch_retained_set(const RetainArgs& a, cudaStream_t stream) {
-  const int C = retained_cluster_size(a.vocab);
-  if (C < 1 || C > kRsMaxCluster) return -1;
   static thread_local int attr_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_dev != dev) {
-    cudaFuncSetAttribute(retained_set_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaFuncSetAttribute(retained_set_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(sizeof(RsSmem)));
     attr_dev = dev;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, a.rows, 1);
-  cfg.blockDim = dim3(kRsThreads, 1, 1);
-  cfg.dynamicSmemBytes = sizeof(RsSmem);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, retained_set_kernel, a) == cudaSuccess ? 0 : -1;
+  retained_set_kernel<<<static_cast<unsigned>(a.rows), kRsThreads, sizeof(RsSmem), stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 

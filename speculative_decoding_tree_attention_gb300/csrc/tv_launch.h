@@ -47,9 +47,8 @@ struct RetainArgs {
   int32_t rows, vocab;
 };
 
-// Retained set of every row (one cluster of CTAs per row).
+// Retained set of every row (one CTA per row).
 int launch_retained_set(const RetainArgs& a, cudaStream_t stream);
-int retained_cluster_size(int vocab);
 size_t accept_workspace_bytes(int vocab, int total_nodes);
 int accept_cluster_size(int vocab, int batch, int sms);
 int accept_max_nodes();

@@ -69,3 +69,31 @@ def test_many_rows():
     logits = g.standard_normal((300, 4099)) * 3.0
     p = np.exp(logits - logits.max(axis=1, keepdims=True))
     _check((p / p.sum(axis=1, keepdims=True)).astype(np.float32), 0.7)
+
+
+def test_flat_rows_overflow_the_key_copy():
+    """Rows whose crossing top-byte bucket holds more keys than shared memory
+    keeps (the later passes read the row again): all tied, and mostly tied."""
+    V = 1 << 18
+    g = np.random.default_rng(21)
+    rows = np.zeros((3, V), np.float32)
+    rows[0] = np.float32(1.0 / V)
+    rows[1] = np.float32(1.0 / V)
+    rows[1, g.integers(0, V, 3000)] = np.float32(3.0 / V)
+    rows[2] = (np.float32(1.0 / V) * (1.0 + 0.9 * g.random(V))).astype(np.float32)
+    _check(rows, 0.7)
+    _check(rows, 0.31)
+
+
+def test_values_above_128():
+    """Unnormalised rows with values >= 2^7 (top bytes above the 24 private
+    buckets; weights clamped at 32)."""
+    g = np.random.default_rng(22)
+    V = 5000
+    rows = (g.random((4, V)) * 1e-3).astype(np.float32)
+    rows[0, g.integers(0, V, 5)] = np.float32(200.0)
+    rows[1, :40] = (g.random(40) * 1e4 + 128.0).astype(np.float32)
+    rows[2, 7] = np.float32(np.inf)
+    rows[3, 100:110] = np.float32(31.5)
+    for mass in (0.5, 20.0, 32.0):
+        _check(rows, mass)
