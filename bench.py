@@ -60,6 +60,10 @@ def parse():
                     help="skip the serving and 7B-like figures reported beside the headline")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiler captures)")
+    ap.add_argument("--profile", choices=["attention", "attention_fp8", "accept", "retained"],
+                    default=None,
+                    help="profiler-capture mode: launch only this call of the workload "
+                         "--warmup + --steps times, eagerly, then exit (no JSON line)")
     return ap.parse_args()
 
 
@@ -433,6 +437,24 @@ def graphed(fn, stream):
     return g.replay
 
 
+def run_profile(tv, step, cfg, args, dev):
+    """--profile: the chosen call alone, warmup + steps times on the default
+    stream, checked once, for a profiler to capture (say the last launch)."""
+    import torch
+    f = fp8_inputs(step.d) if args.profile == "attention_fp8" else None
+    if args.profile == "retained" and not cfg.get("mask_mass"):
+        raise SystemExit(f"--profile retained: workload {cfg['name']} does not prune")
+    call = {"attention": step.attn, "attention_fp8": lambda: step.attn_fp8(f), "accept": step.acc,
+            "retained": lambda: tv.retained_set(step.d["draft"], float(cfg["mask_mass"]))}[args.profile]
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    if args.profile.startswith("attention"):
+        assert int(step.st_attn.max()) == 0, "attention status"
+    print(f"profile {args.profile}: {cfg['name']} (config {cfg['num']}, batch {cfg['batch']}), "
+          f"{args.warmup + args.steps} launches", flush=True)
+
+
 def time_retained(tv, d, cfg, rows, nb, stream, flush, peaks):
     """tv_retained_set of every draft row of a workload that prunes, timed on
     its own; the masks must equal the workload's."""
@@ -497,11 +519,14 @@ def main():
     cfg = wl.config(args.config, **({"batch": args.batch} if args.batch > 0 else {}))
     case = wl.make_case(cfg, parts=("attn", "accept"), kind=args.mode)
     # the other HBM-bound workloads, reported beside the headline (rank 0)
-    side_nums = [n for n in (4, 3, 2) if n != cfg["num"]] if (rank == 0 and args.side) else []
+    side_nums = [n for n in (4, 3, 2) if n != cfg["num"]] if (rank == 0 and args.side and not args.profile) else []
     side_cases = {n: wl.make_case(wl.config(n), parts=("attn", "accept"), kind=args.mode)
                   for n in side_nums}
     step = Step(tv, case, cfg, args.mode, dev)
     tot, B = step.tot, step.B
+    if args.profile:
+        run_profile(tv, step, cfg, args, dev)
+        return
 
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
