@@ -59,8 +59,10 @@ struct AttnPlan {
 
 // Fewest 128-key tiles a virtual CTA is given: below this a unit is not split
 // further, since a split piece costs about this much in fixed work (its Q
-// load, the pipeline fill and its partial-result write).
-constexpr int kMinTiles = 4;
+// load, the pipeline fill and its partial-result write).  Timed at 2, 3, 4
+// and 6: only the short-prefix MHA line (32 heads x 9 tiles) moved, and 3 was
+// fastest there (each unit then splits into three whole ranges).
+constexpr int kMinTiles = 3;
 
 // Launch plan for `sms` SMs (one persistent CTA per SM).  A layer of `lanes`
 // CTAs takes the m-tile pairs (256 packed rows) of a (sequence, KV head): as

@@ -195,10 +195,10 @@ def _plan(batch, hq, hkv, d, max_nodes, max_prefix):
 # (lanes, virtual CTAs) on 152 SMs: lanes = m-tile pairs of the largest tree
 # (256 packed rows each), virtual CTAs = 152 // lanes, fewer when the line of
 # key tiles (batch x Hkv x layers x (prefix tiles + node tiles)) gives fewer
-# than 4 tiles each
+# than 3 tiles each
 @pytest.mark.parametrize("shape, lanes, vctas", [
     ((1, 4, 4, 64, 15, 128), 1, 2),          # tiny: 4 heads x 2 tiles = 8 tiles
-    ((1, 32, 32, 128, 64, 1024), 1, 72),     # 7B-like: 32 x 9 = 288 tiles
+    ((1, 32, 32, 128, 64, 1024), 1, 96),     # 7B-like: 32 x 9 = 288 tiles
     ((16, 32, 8, 128, 64, 3959), 1, 152),    # serving: 16 x 8 x 32 tiles
     ((4, 28, 4, 128, 128, 1600), 4, 38),     # multimodal: 896 rows = 4 pairs, 224 tiles
     ((4, 64, 8, 128, 256, 32768), 8, 19),    # long: 2048 rows = 8 pairs, 8256 tiles
@@ -207,7 +207,7 @@ def _plan(batch, hq, hkv, d, max_nodes, max_prefix):
 def test_launch_plan(lib, shape, lanes, vctas):
     plan = tv.attention_plan(_plan(*shape), sms=152)
     assert (plan["lanes"], plan["virtual_ctas"]) == (lanes, vctas)
-    assert plan["ctas"] == lanes * vctas <= 152 and plan["min_tiles"] == 4
+    assert plan["ctas"] == lanes * vctas <= 152 and plan["min_tiles"] == 3
     # the fixed scratch array of the no-allocation entry point holds every plan
     assert plan["workspace_bytes"] <= 64 << 20
 

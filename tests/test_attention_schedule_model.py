@@ -22,7 +22,7 @@ import pytest
 BN, UNIT_ROWS = 128, 256
 
 
-def plan(batch, hq, hkv, max_nodes, max_prefix, sms=152, min_tiles=4):
+def plan(batch, hq, hkv, max_nodes, max_prefix, sms=152, min_tiles=3):
     g = hq // hkv
     mpairs = -(-max_nodes * g // UNIT_ROWS)
     lanes = min(mpairs, sms)
