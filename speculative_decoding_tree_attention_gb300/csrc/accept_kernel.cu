@@ -853,67 +853,74 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
 //
 // One CTA of 1024 threads per row, no cluster: a wave of one CTA per SM holds
 // about 150 rows (90 MB at V = 151936), so the row, read from HBM by the first
-// pass, is still in L2 for the later ones.  Every warp load is contiguous:
-// the order-free passes read 512-byte runs of float4s (16-byte aligned rows)
-// or 128-byte words, and the mask pass reads word by word with lane L on id
-// 32 word + L, so a word's mask bits are a ballot.  A radix select over the key (the
-// fp32 bit pattern, which orders non-negative floats), 8 bits a pass from the
-// top, finds the key tau at which the cumulative mass crosses T; each pass
-// sums the fix40 weights of the entries that match the digits found so far
-// into 256 buckets and picks the crossing digit by a suffix scan.
-//   pass 0 (every entry): private per-thread histograms of the 24 top bytes
-//     that can carry weight (plain adds, no conflicts: most entries share a
-//     few top bytes);
-//   pass 1 (the entries of the crossing top byte): per-warp-pair histograms
-//     of three 16-bit weight parts with 32-bit shared atomics, and the
-//     matching keys copied into shared memory (a slice per warp);
-//   passes 2, 3: the same over the copied keys (or the row again, if they
-//     did not fit).
-// Keys above tau are kept; of the keys equal to tau, the c lowest ids with
-// c = ceil((T - mass above tau) / fix40(tau)), ranked in id order by a block
-// scan of per-word tie counts.  Every sum is an exact integer.
+// pass, is still in L2 for the second.  A radix select over the key (the
+// fp32 bit pattern, which orders non-negative floats) finds the key tau at
+// which the cumulative mass crosses T, a digit at a time from the top: the
+// exponent field (key bits 30..23), then bits 22..15, 14..7 and 6..0.  Every
+// sum is an exact integer: within one exponent field e the fix40 weight of an
+// entry is a << s, with m its 24-bit significand, a = m (e >= 110) or
+// m >> (110 - e) (e < 110: the truncation of fix40) and s = max(e - 110, 0),
+// so the mass of a digit is (the sum of a) << s.
+//   pass 0 (the row): private u32 sums of a per thread for each of the 45
+//     fields 87..131 that carry weight below the clamp (plain adds, no
+//     conflicts: most entries share a few fields; a thread reads at most 256
+//     entries, so a sum stays below 2^32); fields 132 and up (q >= 32 or
+//     +inf, weight clamped to 2^45) go to shared u64 buckets.
+//   pass 1 (the row again): with the crossing field e* known, the mask bits
+//     of the keys above it go to a bitmap in shared memory and those of the
+//     keys of field e* to a second one, from which a block scan lists the ids
+//     of field e* in id order.
+//   The rest gathers those keys again by id (from L2), each thread keeping
+//     bits 30..15 of its keys in registers: the histogram of bits 22..15, then
+//     a filter that sets the mask bits of the keys above the new 16-bit prefix
+//     and copies the keys at it, with their ids, into a small list, whose
+//     histograms of bits 14..7 and 6..0 give tau.  The mask is the bitmap
+//     plus the small list's keys above tau and its ties at tau: all of them
+//     when their number is the number of ties to keep, c = ceil((T - mass
+//     above tau) / fix40(tau)), else the c of lowest id.
+// A row whose field e* holds more keys than the id list, or whose 16-bit
+// prefix more than the small list, takes its remaining digits by passes over
+// the row and its mask by a pass over the row that ranks the ties in id order
+// with a block scan.
 constexpr int kRsThreads = 1024;
 constexpr int kRsWarps = kRsThreads / 32;
-// Top bytes of keys with fix40 weight > 0 (q >= 2^-40): 43 .. 66 for q < 2^7;
-// larger top bytes (q >= 2^7, weight clamped) go to shared buckets.
-constexpr int kRsByte0 = 43;
-constexpr int kRsBytes = 24;
-constexpr int kRsHists = kRsWarps / 2;                      // one per warp pair
-constexpr int kRsPoolBytes = kRsBytes * kRsThreads * 8;     // pass 0's private histograms
-constexpr int kRsHistWords = kRsHists * 3 * 256;            // later passes' histograms (u32)
-constexpr int kRsKeysCap = kRsPoolBytes / 4 - kRsHistWords; // keys copied by pass 1
-constexpr int kRsSlice = kRsKeysCap / kRsWarps;             // ... in one slice per warp
+constexpr int kRsE0 = 87;                          // lowest field with weight (q >= 2^-40)
+constexpr int kRsEBig = 132;                       // fields from here on: weight clamped to 2^45
+constexpr int kRsExps = kRsEBig - kRsE0;           // pass 0's private sums per thread
+constexpr int kRsPoolWords = kRsExps * kRsThreads; // ... as u32 [field][thread]
+constexpr int kRsHists = kRsWarps / 2;             // later histograms: one per warp pair,
+constexpr int kRsHistWords = kRsHists * 2 * 256;   // of two 16-bit weight parts
+constexpr int kRsMaskWords = 8192;                 // a row's mask words (V <= 2^18)
+constexpr int kRsSmallCap = 2048;                  // keys at the 16-bit prefix
+// ids of field e* the pool holds after the histograms, two bitmaps and the
+// small list: at least 17408 (V = 2^18), 24296 at V = 151936
+static_assert(kRsPoolWords - (kRsHistWords + 2 * kRsMaskWords + 2 * kRsSmallCap) >= 17408, "pool");
+constexpr int kRsGather = 16;  // ids of field e* a thread gathers at once (kept in registers)
 
 struct RsSmem {
-  // pass 0: u64 [24][1024]; passes 1-3: u32 [16][3][256] histograms, then
-  // the copied keys
-  alignas(16) uint8_t pool[kRsPoolBytes];
-  unsigned long long big[256];  // pass 0: top bytes above 66
+  // pass 0: private sums [field][thread]; then the histograms, the mask
+  // bitmaps and the small list (keys, ids)
+  alignas(16) uint32_t pool[kRsPoolWords];
+  unsigned long long big[256];  // pass 0: fields 132..255
   unsigned long long hist[256];
   unsigned long long red[kRsWarps];
   int iscan[kRsWarps];
   int digit;
-  int nkeys[kRsWarps];  // keys pass 1 found, per warp (its slice holds the first kRsSlice)
+  int nsmall;
+  int nties;
   unsigned long long above;
   unsigned long long total;
 };
 
-// fix40 of the float whose bit pattern is `key` (a q > 0, or 0) in integer
-// arithmetic, without branches: a normal q is m * 2^(e - 150) with m the
-// 24-bit significand and e the exponent field, so floor(q * 2^40) =
-// m << (e - 110) for e >= 110 and m >> (110 - e) below; e < 87 (and 0,
-// denormals) gives 0, q >= 32 (and +inf) clamps to 32 * 2^40.
-__device__ __forceinline__ unsigned long long rs_weight_key(uint32_t key) {
-  const int e = static_cast<int>(key >> 23);
-  const uint32_t m = (key & 0x7fffffu) | 0x800000u;
-  const int s = e - 110;
-  const uint32_t lo = m >> min(max(-s, 0), 31);         // e < 110: the right shift
-  const unsigned long long w = static_cast<unsigned long long>(lo) << max(s, 0);  // e >= 110
-  return key >= 0x42000000u ? (1ull << 45) : (e < 87 ? 0ull : w);
-}
+// Key bits below digit p: digit 0 is bits 30..23, digits 1..3 bits 22..15,
+// 14..7 and 6..0.
+__device__ __forceinline__ int rs_shift(int p) { return max(23 - 8 * p, 0); }
 __device__ __forceinline__ uint32_t rs_key(float x) { return x > 0.0f ? __float_as_uint(x) : 0u; }
-// fix40 of q = x if x > 0 else 0 (NaN gives 0)
-__device__ __forceinline__ unsigned long long rs_weight(float x) { return rs_weight_key(rs_key(x)); }
+// a of a key of field ex (weight = a << rs_wshift(ex)); 1 above the clamp
+__device__ __forceinline__ uint32_t rs_addend(uint32_t key, int ex) {
+  return ex >= kRsEBig ? 1u : (((key & 0x7fffffu) | 0x800000u) >> max(110 - ex, 0));
+}
+__device__ __forceinline__ int rs_wshift(int ex) { return ex >= kRsEBig ? 45 : max(ex - 110, 0); }
 
 // Lane L of a warp reads id 32 word + L: a warp's load of one word is one
 // 128-byte line, and the words w, w + 32, ... of the 32 warps make the CTA
@@ -922,38 +929,80 @@ __device__ __forceinline__ float rs_load(const float* q, int V, int id) {
   return id < V ? __ldcg(q + id) : 0.0f;
 }
 
-// Adds weight w (< 2^46) of digit d as three 16-bit parts: at most 16384
-// entries of a pass reach one histogram (two warps, at most 8192 words of a
-// row for V <= 2^18, one entry a word per lane), so each part sum stays below
-// 2^30.
-__device__ __forceinline__ void rs_add(uint32_t* h, uint32_t d, unsigned long long w) {
-  if (w & 0xffffull) atomicAdd(h + d, static_cast<uint32_t>(w & 0xffffull));
-  if ((w >> 16) & 0xffffull) atomicAdd(h + 256 + d, static_cast<uint32_t>((w >> 16) & 0xffffull));
-  if (w >> 32) atomicAdd(h + 512 + d, static_cast<uint32_t>(w >> 32));
-}
-
 constexpr int kRsUnroll = 8;  // loads of a warp in flight
 
-// The order-free passes (0 and 1) on a 16-byte aligned row (V % 4 == 0):
-// lane L of warp w reads float4 (32 g + L) for the groups g = w, w + 32, ...,
-// so a warp load is 512 consecutive bytes and a CTA keeps 8 x 16 KB in
-// flight.  Float4s past the row read as zeros.
+// The order-free passes on a 16-byte aligned row (V % 4 == 0): lane L of warp
+// w reads float4 (32 g + L) for the groups g = w, w + 32, ..., so a warp load
+// is 512 consecutive bytes and a CTA keeps 8 x 16 KB in flight.  Float4s past
+// the row read as zeros.
 __device__ __forceinline__ float4 rs_load4(const float* q, int nf, int f) {
   return f < nf ? __ldcg(reinterpret_cast<const float4*>(q) + f) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 }
 
-// Pass 0's update for one entry: its weight into this thread's private
-// bucket of its top byte (or the shared bucket of a top byte above 66).
-__device__ __forceinline__ void rs_count0(RsSmem& sm, unsigned long long* priv, int tid, float x) {
-  const unsigned long long w = rs_weight(x);
-  if (w) {  // x > 0 and its top byte >= 43
-    const int d = static_cast<int>(__float_as_uint(x) >> 24) - kRsByte0;
-    if (d < kRsBytes) {
-      priv[d * kRsThreads + tid] += w;
-    } else {
-      atomicAdd(&sm.big[d + kRsByte0], w);
+// Pass 0's update for one entry (x as loaded, any value): a into this
+// thread's private sum of its field, or 2^45 into the shared bucket of a
+// field above the clamp.  Non-positive entries (field >= 256 as bits), NaN,
+// zeros, denormals and fields below 87 add nothing.
+__device__ __forceinline__ void rs_count0(RsSmem& sm, int tid, float x) {
+  const uint32_t k = __float_as_uint(x);
+  const uint32_t e = k >> 23;
+  const uint32_t b = e - kRsE0;
+  if (b < static_cast<uint32_t>(kRsExps)) {
+    const uint32_t m = (k & 0x7fffffu) | 0x800000u;
+    sm.pool[b * kRsThreads + tid] += m >> max(110 - static_cast<int>(e), 0);
+  } else if (e - kRsEBig < static_cast<uint32_t>(256 - kRsEBig) && k <= 0x7f800000u) {
+    atomicAdd(&sm.big[e], 1ull << 45);
+  }
+}
+
+// Adds a (< 2^24) to digit d as two 16-bit parts: at most 16384 entries of a
+// pass reach one histogram (two warps, each at most 8192 entries of a row for
+// V <= 2^18), so the low part sums stay below 2^30 and the high below 2^22.
+__device__ __forceinline__ void rs_add2(uint32_t* h, uint32_t d, uint32_t a) {
+  if (a & 0xffffu) atomicAdd(h + d, a & 0xffffu);
+  if (a >> 16) atomicAdd(h + 256 + d, a >> 16);
+}
+
+// sm.hist[d] = the warp-pair histograms' sum for digit d, times 2^wsh.
+__device__ __forceinline__ void rs_reduce(RsSmem& sm, int tid, int wsh) {
+  if (tid < 256) {
+    unsigned long long h = 0;
+    for (int g = 0; g < kRsHists; ++g) {
+      const uint32_t* hg = sm.pool + g * 512;
+      h += static_cast<unsigned long long>(hg[tid]) + (static_cast<unsigned long long>(hg[256 + tid]) << 16);
+    }
+    sm.hist[tid] = h << wsh;
+  }
+}
+
+// The crossing digit of sm.hist (written before a barrier): the one digit d
+// with above + mass(digits > d) < T <= above + mass(digits >= d), where above
+// is the mass of the keys above the current prefix range.  Sets sm.digit and
+// sm.above (and sm.total, the whole row, when `first`).  Digit d = tid < 256;
+// warps 0-7 scan their 32 digits (descending), then across the 8 warps.
+// Every thread calls it; it ends with a barrier.
+__device__ void rs_pick(RsSmem& sm, int tid, unsigned long long above, unsigned long long T, bool first) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const unsigned long long H = tid < 256 ? sm.hist[tid] : 0ull;
+  unsigned long long incl = H;  // sum over digits >= d within the warp
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += y;
+  }
+  if (tid < 256 && lane == 0) sm.red[warp] = incl;  // warp totals
+  __syncthreads();
+  if (tid < 256) {
+    unsigned long long higher = 0;  // digits of the warps above
+    for (int w = warp + 1; w < 8; ++w) higher += sm.red[w];
+    const unsigned long long ge = above + higher + incl;  // mass of digits >= d
+    const unsigned long long gt = ge - H;                 // mass of digits > d
+    if (first && tid == 0) sm.total = ge;                 // digit 0: the whole row
+    if (gt < T && ge >= T) {
+      sm.digit = tid;
+      sm.above = gt;
     }
   }
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kRsThreads, 1)
@@ -970,176 +1019,350 @@ __global__ void __launch_bounds__(kRsThreads, 1)
   const float* q = a.draft + static_cast<size_t>(row) * V;
   uint32_t* mrow = a.mask + static_cast<size_t>(row) * words;
   const unsigned long long T = a.threshold;
-  unsigned long long* priv = reinterpret_cast<unsigned long long*>(sm.pool);
-  uint32_t* whist = reinterpret_cast<uint32_t*>(sm.pool);
-  uint32_t* keys = whist + kRsHistWords + warp * kRsSlice;  // this warp's slice
-  uint32_t* myh = whist + (warp >> 1) * 3 * 256;
+  uint32_t* whist = sm.pool;
+  uint32_t* myh = whist + (warp >> 1) * 512;
+  // the pool after pass 0: histograms, the two bitmaps, the small list, the ids
+  uint32_t* bits = sm.pool + kRsHistWords;
+  uint32_t* mbits = bits + words;
+  uint32_t* skeys = mbits + words;
+  uint32_t* sids = skeys + kRsSmallCap;
+  uint32_t* ids = sids + kRsSmallCap;
+  const int cap = kRsPoolWords - (kRsHistWords + 2 * words + 2 * kRsSmallCap);  // >= 17408
 
-  uint32_t prefix = 0;
-  unsigned long long above = 0;  // mass of the keys above the current prefix range
-  bool copied = false;           // pass 1 copied every matching key
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    if (pass == 0) {
-      // ---- top byte, every entry: private histograms [byte][thread]
+  // ---- pass 0: the field of every entry
 #pragma unroll
-      for (int b = 0; b < kRsBytes; ++b) priv[b * kRsThreads + tid] = 0ull;
-      if (tid < 256) sm.big[tid] = 0ull;
-      __syncthreads();
-      if (vec) {
-        for (int g0 = warp; g0 * 32 < nf; g0 += kRsWarps * kRsUnroll) {
-          float4 x[kRsUnroll];
+  for (int b = 0; b < kRsExps; ++b) sm.pool[b * kRsThreads + tid] = 0u;
+  if (tid < 256) sm.big[tid] = 0ull;
+  __syncthreads();
+  if (vec) {
+    for (int g0 = warp; g0 * 32 < nf; g0 += kRsWarps * kRsUnroll) {
+      float4 x[kRsUnroll];
 #pragma unroll
-          for (int u = 0; u < kRsUnroll; ++u) x[u] = rs_load4(q, nf, (g0 + u * kRsWarps) * 32 + lane);
+      for (int u = 0; u < kRsUnroll; ++u) x[u] = rs_load4(q, nf, (g0 + u * kRsWarps) * 32 + lane);
 #pragma unroll
-          for (int u = 0; u < kRsUnroll; ++u) {
-            rs_count0(sm, priv, tid, x[u].x);
-            rs_count0(sm, priv, tid, x[u].y);
-            rs_count0(sm, priv, tid, x[u].z);
-            rs_count0(sm, priv, tid, x[u].w);
+      for (int u = 0; u < kRsUnroll; ++u) {
+        rs_count0(sm, tid, x[u].x);
+        rs_count0(sm, tid, x[u].y);
+        rs_count0(sm, tid, x[u].z);
+        rs_count0(sm, tid, x[u].w);
+      }
+    }
+  } else {
+    for (int w0 = warp; w0 < words; w0 += kRsWarps * kRsUnroll) {
+      float x[kRsUnroll];
+#pragma unroll
+      for (int u = 0; u < kRsUnroll; ++u) {
+        const int word = w0 + u * kRsWarps;
+        x[u] = word < words ? rs_load(q, V, word * 32 + lane) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < kRsUnroll; ++u) rs_count0(sm, tid, x[u]);
+    }
+  }
+  __syncthreads();
+  // field masses: a warp per field sums the 1024 private sums (< 2^42: at
+  // most 2^18 entries of a < 2^24), then shifts
+  for (int b = warp; b < kRsExps; b += kRsWarps) {
+    unsigned long long y = 0;
+    for (int i = lane; i < kRsThreads; i += 32) y += sm.pool[b * kRsThreads + i];
+    for (int o = 16; o; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+    if (lane == 0) sm.hist[kRsE0 + b] = y << max(kRsE0 + b - 110, 0);
+  }
+  if (tid < 256 && (tid < kRsE0 || tid >= kRsEBig)) sm.hist[tid] = tid < kRsE0 ? 0ull : sm.big[tid];
+  __syncthreads();
+  rs_pick(sm, tid, 0ull, T, true);
+  if (sm.total < T) {  // the mass never reaches T: every token is kept
+    const unsigned long long total = sm.total;
+    for (int word = tid; word < words; word += kRsThreads) {
+      const int v0 = word * 32;
+      mrow[word] = (V - v0 >= 32) ? 0xffffffffu : ((1u << (V - v0)) - 1u);
+    }
+    if (tid == 0) {
+      if (a.z_fixed) a.z_fixed[row] = total;
+      if (a.z) a.z[row] = __fmul_rn(__ull2float_rn(total), kTwoM40);
+      if (a.kept) a.kept[row] = V;
+    }
+    return;
+  }
+  const int ex = sm.digit;  // e*: 87..255 (its mass is > 0)
+  const int wsh = rs_wshift(ex);
+  uint32_t prefix = static_cast<uint32_t>(ex);
+  unsigned long long above = sm.above;  // mass of the keys above the prefix range
+
+  // ---- pass 1: mask bits of the keys of fields above e* (bits) and of
+  // field e* (mbits), each word written once
+  {
+    const uint32_t lim = static_cast<uint32_t>(ex + 1) << 23;  // keys of fields > e*
+    const uint32_t lo = static_cast<uint32_t>(ex) << 23;       // keys of field e*: [lo, lim)
+    if (vec) {
+      for (int g0 = warp; g0 * 32 < nf; g0 += kRsWarps * kRsUnroll) {
+        float4 x[kRsUnroll];
+#pragma unroll
+        for (int u = 0; u < kRsUnroll; ++u) x[u] = rs_load4(q, nf, (g0 + u * kRsWarps) * 32 + lane);
+#pragma unroll
+        for (int u = 0; u < kRsUnroll; ++u) {
+          const int f = (g0 + u * kRsWarps) * 32 + lane;  // ids 4f .. 4f + 3
+          const uint32_t k0 = rs_key(x[u].x), k1 = rs_key(x[u].y), k2 = rs_key(x[u].z), k3 = rs_key(x[u].w);
+          // mask word f / 8 holds the nibbles of lanes 8j .. 8j + 7, the
+          // nibble of lane L at bit 4 (L % 8)
+          const int sh = 4 * (lane & 7);
+          uint32_t av = (static_cast<uint32_t>(k0 >= lim) | (static_cast<uint32_t>(k1 >= lim) << 1) |
+                         (static_cast<uint32_t>(k2 >= lim) << 2) | (static_cast<uint32_t>(k3 >= lim) << 3))
+                        << sh;
+          uint32_t mv = (static_cast<uint32_t>(k0 - lo < 0x800000u) |
+                         (static_cast<uint32_t>(k1 - lo < 0x800000u) << 1) |
+                         (static_cast<uint32_t>(k2 - lo < 0x800000u) << 2) |
+                         (static_cast<uint32_t>(k3 - lo < 0x800000u) << 3))
+                        << sh;
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1) {
+            av |= __shfl_xor_sync(0xffffffffu, av, o);
+            mv |= __shfl_xor_sync(0xffffffffu, mv, o);
+          }
+          if ((lane & 7) == 0 && (f >> 3) < words) {
+            bits[f >> 3] = av;
+            mbits[f >> 3] = mv;
           }
         }
-      } else {
-        for (int w0 = warp; w0 < words; w0 += kRsWarps * kRsUnroll) {
-          float x[kRsUnroll];
-#pragma unroll
-          for (int u = 0; u < kRsUnroll; ++u) {
-            const int word = w0 + u * kRsWarps;
-            x[u] = word < words ? rs_load(q, V, word * 32 + lane) : 0.0f;
-          }
-#pragma unroll
-          for (int u = 0; u < kRsUnroll; ++u) rs_count0(sm, priv, tid, x[u]);
-        }
       }
-      __syncthreads();
-      // bucket sums: a warp per weight-carrying byte, then a warp sum
-      for (int b = warp; b < kRsBytes; b += kRsWarps) {
-        unsigned long long y = 0;
-        for (int i = lane; i < kRsThreads; i += 32) y += priv[b * kRsThreads + i];
-        for (int o = 16; o; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
-        if (lane == 0) sm.hist[kRsByte0 + b] = y;
-      }
-      if (tid < 256 && (tid < kRsByte0 || tid >= kRsByte0 + kRsBytes))
-        sm.hist[tid] = tid < kRsByte0 ? 0ull : sm.big[tid];
     } else {
-      for (int i = tid; i < kRsHistWords; i += kRsThreads) whist[i] = 0u;
-      __syncthreads();
-      if (pass == 1 || !copied) {
-        // ---- the row again (from L2): entries matching the prefix.  Zero
-        // entries (past the row, q <= 0) match no prefix: every prefix holds
-        // a top byte >= 43.  `take` adds one entry whose warp-wide match
-        // ballot is mb and, in pass 1, copies its key to slot wpos + (its
-        // rank among the ballot's lanes) of the warp's slice; wpos (the
-        // warp's keys so far) is the same in every lane.
-        int wpos = 0;
-        auto take = [&](float x, uint32_t mb) {
-          if ((mb >> lane) & 1u) {
-            const uint32_t k = rs_key(x);
-            rs_add(myh, (k >> shift) & 255u, rs_weight(x));
-            if (pass == 1) {
-              const int p = wpos + __popc(mb & lt_mask);
-              if (p < kRsSlice) keys[p] = k;
-            }
-          }
-          wpos += __popc(mb);
-        };
-        auto match = [&](float x) { return __ballot_sync(0xffffffffu, (rs_key(x) >> (shift + 8)) == prefix); };
-        if (vec) {
-          for (int g0 = warp; g0 * 32 < nf; g0 += kRsWarps * kRsUnroll) {
-            float4 x[kRsUnroll];
+      for (int w0 = warp; w0 < words; w0 += kRsWarps * kRsUnroll) {
+        float x[kRsUnroll];
 #pragma unroll
-            for (int u = 0; u < kRsUnroll; ++u) x[u] = rs_load4(q, nf, (g0 + u * kRsWarps) * 32 + lane);
+        for (int u = 0; u < kRsUnroll; ++u) {
+          const int word = w0 + u * kRsWarps;
+          x[u] = word < words ? rs_load(q, V, word * 32 + lane) : 0.0f;
+        }
 #pragma unroll
-            for (int u = 0; u < kRsUnroll; ++u) {
-              take(x[u].x, match(x[u].x));
-              take(x[u].y, match(x[u].y));
-              take(x[u].z, match(x[u].z));
-              take(x[u].w, match(x[u].w));
-            }
-          }
-        } else {
-          for (int w0 = warp; w0 < words; w0 += kRsWarps * kRsUnroll) {
-            float x[kRsUnroll];
-#pragma unroll
-            for (int u = 0; u < kRsUnroll; ++u) {
-              const int word = w0 + u * kRsWarps;
-              x[u] = word < words ? rs_load(q, V, word * 32 + lane) : 0.0f;
-            }
-#pragma unroll
-            for (int u = 0; u < kRsUnroll; ++u) take(x[u], match(x[u]));
+        for (int u = 0; u < kRsUnroll; ++u) {
+          const int word = w0 + u * kRsWarps;
+          const uint32_t k = rs_key(x[u]);
+          const uint32_t av = __ballot_sync(0xffffffffu, k >= lim);
+          const uint32_t mv = __ballot_sync(0xffffffffu, k - lo < 0x800000u);
+          if (lane == 0 && word < words) {
+            bits[word] = av;
+            mbits[word] = mv;
           }
         }
-        if (pass == 1 && lane == 0) sm.nkeys[warp] = wpos;
-      } else {
-        // ---- the keys pass 1 copied: each warp its own slice
-        const int n = sm.nkeys[warp];
-        for (int i = lane; i < n; i += 32) {
-          const uint32_t k = keys[i];
-          if ((k >> (shift + 8)) == prefix) rs_add(myh, (k >> shift) & 255u, rs_weight(__uint_as_float(k)));
-        }
-      }
-      __syncthreads();
-      if (tid < 256) {
-        unsigned long long h = 0;
-        for (int g = 0; g < kRsHists; ++g) {
-          const uint32_t* hg = whist + g * 3 * 256;
-          h += static_cast<unsigned long long>(hg[tid]) + (static_cast<unsigned long long>(hg[256 + tid]) << 16) +
-               (static_cast<unsigned long long>(hg[512 + tid]) << 32);
-        }
-        sm.hist[tid] = h;
-      }
-      if (pass == 1) {  // every warp's keys fit its slice (counts written before the barrier above)
-        int most = 0;
-        for (int w = 0; w < kRsWarps; ++w) most = max(most, sm.nkeys[w]);
-        copied = most <= kRsSlice;
       }
     }
-    __syncthreads();
-    // digit d = tid (< 256): the suffix mass over the buckets; warps 0-7
-    // hold digits 32w .. 32w+31, first summed within the warp (descending),
-    // then across the 8 warps
-    const unsigned long long H = tid < 256 ? sm.hist[tid] : 0ull;
-    unsigned long long incl = H;  // sum over digits >= d within the warp
+  }
+  __syncthreads();
+  // ---- the ids of field e*, in id order: thread t takes words [t c, t c + c)
+  // and writes its ids after those of the threads before it (a block scan)
+  int n = 0;  // ids of field e*
+  {
+    const int c = (words + kRsThreads - 1) / kRsThreads;
+    const int w0 = min(tid * c, words), w1 = min(w0 + c, words);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(mbits[w]);
+    int incl = cnt;
     for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y = __shfl_down_sync(0xffffffffu, incl, o);
-      if (lane + o < 32) incl += y;
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
-    if (tid < 256 && lane == 0) sm.red[warp] = incl;  // warp totals
+    if (lane == 31) sm.iscan[warp] = incl;
     __syncthreads();
-    if (tid < 256) {
-      unsigned long long higher = 0;  // digits of the warps above
-      for (int w = warp + 1; w < 8; ++w) higher += sm.red[w];
-      const unsigned long long ge = above + higher + incl;  // mass of digits >= d
-      const unsigned long long gt = ge - H;                 // mass of digits > d
-      if (pass == 0 && tid == 0) sm.total = ge;             // digit 0: the whole row
-      if (gt < T && ge >= T) {
-        sm.digit = tid;
-        sm.above = gt;
+    int before = incl - cnt;
+    for (int w = 0; w < kRsWarps; ++w) {
+      const int y = sm.iscan[w];
+      if (w < warp) before += y;
+      n += y;
+    }
+    if (n <= cap) {
+      for (int w = w0; w < w1; ++w) {
+        for (uint32_t v = mbits[w]; v; v &= v - 1u) ids[before++] = 32u * w + (__ffs(v) - 1);
+      }
+    }
+    __syncthreads();  // the ids are complete; sm.iscan is rewritten below
+  }
+
+  int p = 1;  // the next digit
+  if (n <= cap) {
+    // ---- digit 1 (bits 22..15) over the listed keys, gathered again by id:
+    // thread t takes entries t + 1024 u, and keeps bits 30..15 of the keys of
+    // the first round in registers (two to a register) for the filter
+    for (int i = tid; i < kRsHistWords; i += kRsThreads) whist[i] = 0u;
+    if (tid == 0) {
+      sm.nsmall = 0;
+      sm.nties = 0;
+    }
+    __syncthreads();
+    uint32_t hk[kRsGather / 2];
+#pragma unroll
+    for (int u = 0; u < kRsGather / 2; ++u) hk[u] = 0u;
+    for (int r0 = 0; r0 < n; r0 += kRsThreads * kRsGather) {
+      float x[kRsGather];
+#pragma unroll
+      for (int u = 0; u < kRsGather; ++u) {
+        const int i = r0 + tid + kRsThreads * u;
+        x[u] = i < n ? __ldcg(q + ids[i]) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < kRsGather; ++u) {
+        if (r0 + tid + kRsThreads * u < n) {
+          const uint32_t k = rs_key(x[u]);
+          rs_add2(myh, (k >> 15) & 255u, rs_addend(k, ex));
+          if (r0 == 0) hk[u / 2] |= (k >> 15) << (16 * (u & 1));
+        }
       }
     }
     __syncthreads();
-    if (pass == 0 && sm.total < T) {  // the mass never reaches T: every token is kept
-      const unsigned long long total = sm.total;
-      for (int word = tid; word < words; word += kRsThreads) {
-        const int v0 = word * 32;
-        mrow[word] = (V - v0 >= 32) ? 0xffffffffu : ((1u << (V - v0)) - 1u);
+    rs_reduce(sm, tid, wsh);
+    __syncthreads();
+    rs_pick(sm, tid, above, T, false);
+    prefix = (prefix << 8) | static_cast<uint32_t>(sm.digit);  // key >> 15 of tau
+    above = sm.above;
+    p = 2;
+    // ---- filter: keys above the 16-bit prefix into the bitmap, keys at it
+    // (with their ids) into the small list
+    for (int r0 = 0; r0 < n; r0 += kRsThreads * kRsGather) {
+      uint32_t hv[kRsGather];
+      if (r0 == 0) {
+#pragma unroll
+        for (int u = 0; u < kRsGather; ++u) hv[u] = (hk[u / 2] >> (16 * (u & 1))) & 0xffffu;
+      } else {
+#pragma unroll
+        for (int u = 0; u < kRsGather; ++u) {
+          const int i = r0 + tid + kRsThreads * u;
+          hv[u] = i < n ? __float_as_uint(__ldcg(q + ids[i])) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kRsGather; ++u) hv[u] = rs_key(__uint_as_float(hv[u])) >> 15;
       }
+#pragma unroll
+      for (int u = 0; u < kRsGather; ++u) {
+        const int i = r0 + tid + kRsThreads * u;
+        if (i < n) {
+          const uint32_t id = ids[i];
+          if (hv[u] > prefix) {
+            atomicOr(bits + (id >> 5), 1u << (id & 31u));
+          } else if (hv[u] == prefix) {
+            const int s = atomicAdd(&sm.nsmall, 1);
+            if (s < kRsSmallCap) {
+              skeys[s] = rs_key(__ldcg(q + id));
+              sids[s] = id;
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();  // also: sm.digit / sm.above are rewritten by the next pick
+    const int nsmall = sm.nsmall;
+    if (nsmall <= kRsSmallCap) {
+      // ---- digits 2 and 3 over the small list
+      for (; p < 4; ++p) {
+        const int sh = rs_shift(p), shp = rs_shift(p - 1);
+        const uint32_t dm = (1u << (shp - sh)) - 1u;
+        for (int i = tid; i < kRsHistWords; i += kRsThreads) whist[i] = 0u;
+        __syncthreads();
+        for (int i = tid; i < nsmall; i += kRsThreads) {
+          const uint32_t k = skeys[i];
+          if ((k >> shp) == prefix) rs_add2(myh, (k >> sh) & dm, rs_addend(k, ex));
+        }
+        __syncthreads();
+        rs_reduce(sm, tid, wsh);
+        __syncthreads();
+        rs_pick(sm, tid, above, T, false);
+        prefix = (prefix << (shp - sh)) | static_cast<uint32_t>(sm.digit);
+        above = sm.above;
+        __syncthreads();
+      }
+      // ---- the mask: the bitmap, the small list's keys above tau, its ties
+      const uint32_t tau = prefix;
+      const unsigned long long wt = static_cast<unsigned long long>(rs_addend(tau, ex)) << wsh;  // > 0
+      const unsigned long long need = (T - above + wt - 1) / wt;  // ties to keep (<= the ties)
+      for (int i = tid; i < nsmall; i += kRsThreads) {
+        const uint32_t k = skeys[i], id = sids[i];
+        if (k > tau) {
+          atomicOr(bits + (id >> 5), 1u << (id & 31u));
+        } else if (k == tau) {
+          atomicAdd(&sm.nties, 1);
+        }
+      }
+      __syncthreads();
+      const unsigned long long nties = static_cast<unsigned long long>(sm.nties);
+      for (int i = tid; i < nsmall; i += kRsThreads) {
+        if (skeys[i] != tau) continue;
+        const uint32_t id = sids[i];
+        bool keep = nties <= need;  // all of them
+        if (!keep) {                // else the need of lowest id
+          unsigned long long r = 0;
+          for (int j = 0; j < nsmall; ++j) r += (skeys[j] == tau && sids[j] < id) ? 1ull : 0ull;
+          keep = r < need;
+        }
+        if (keep) atomicOr(bits + (id >> 5), 1u << (id & 31u));
+      }
+      __syncthreads();
+      int cnt = 0;
+      for (int w = tid; w < words; w += kRsThreads) {
+        const uint32_t v = bits[w];
+        mrow[w] = v;
+        cnt += __popc(v);
+      }
+      for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      if (lane == 0) sm.iscan[warp] = cnt;
+      __syncthreads();
       if (tid == 0) {
-        if (a.z_fixed) a.z_fixed[row] = total;
-        if (a.z) a.z[row] = __fmul_rn(__ull2float_rn(total), kTwoM40);
-        if (a.kept) a.kept[row] = V;
+        int kept = 0;
+        for (int w = 0; w < kRsWarps; ++w) kept += sm.iscan[w];
+        const unsigned long long Z = above + need * wt;
+        if (a.z_fixed) a.z_fixed[row] = Z;
+        if (a.z) a.z[row] = __fmul_rn(__ull2float_rn(Z), kTwoM40);
+        if (a.kept) a.kept[row] = kept;
       }
       return;
     }
-    prefix = (prefix << 8) | static_cast<uint32_t>(sm.digit);
+  }
+
+  // ---- the remaining digits by passes over the row (from L2)
+  for (; p < 4; ++p) {
+    const int sh = rs_shift(p), shp = rs_shift(p - 1);
+    const uint32_t dm = (1u << (shp - sh)) - 1u;
+    for (int i = tid; i < kRsHistWords; i += kRsThreads) whist[i] = 0u;
+    __syncthreads();
+    auto add = [&](float x) {
+      const uint32_t k = rs_key(x);
+      if ((k >> shp) == prefix) rs_add2(myh, (k >> sh) & dm, rs_addend(k, ex));
+    };
+    if (vec) {
+      for (int g0 = warp; g0 * 32 < nf; g0 += kRsWarps * kRsUnroll) {
+        float4 x[kRsUnroll];
+#pragma unroll
+        for (int u = 0; u < kRsUnroll; ++u) x[u] = rs_load4(q, nf, (g0 + u * kRsWarps) * 32 + lane);
+#pragma unroll
+        for (int u = 0; u < kRsUnroll; ++u) {
+          add(x[u].x);
+          add(x[u].y);
+          add(x[u].z);
+          add(x[u].w);
+        }
+      }
+    } else {
+      for (int w0 = warp; w0 < words; w0 += kRsWarps * kRsUnroll) {
+        float x[kRsUnroll];
+#pragma unroll
+        for (int u = 0; u < kRsUnroll; ++u) {
+          const int word = w0 + u * kRsWarps;
+          x[u] = word < words ? rs_load(q, V, word * 32 + lane) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < kRsUnroll; ++u) add(x[u]);
+      }
+    }
+    __syncthreads();
+    rs_reduce(sm, tid, wsh);
+    __syncthreads();
+    rs_pick(sm, tid, above, T, false);
+    prefix = (prefix << (shp - sh)) | static_cast<uint32_t>(sm.digit);
     above = sm.above;
-    __syncthreads();  // sm.red / sm.digit / sm.hist / the histograms are rewritten next pass
+    __syncthreads();  // sm.digit / sm.above / sm.red are rewritten by the next pick
   }
   const uint32_t tau = prefix;
-  const unsigned long long wt = rs_weight(__uint_as_float(tau));  // > 0: the crossing adds mass
-  const unsigned long long need = (T - above + wt - 1) / wt;       // ties to keep
+  const unsigned long long wt = static_cast<unsigned long long>(rs_addend(tau, ex)) << wsh;  // > 0
+  const unsigned long long need = (T - above + wt - 1) / wt;  // ties to keep
 
-  // the mask, in rounds of 1024 consecutive words: warp w reads words
+  // ---- the mask by a pass over the row, in rounds of 512 consecutive words: warp w reads words
   // base + 32w + j (j = 0..31, lane L holding id 32 word + L), so a word's
   // keep and tie bits are two ballots, and lane L keeps those of word
   // base + 32w + L.  The ties' ranks in id order are the ties of the earlier

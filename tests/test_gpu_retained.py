@@ -72,8 +72,10 @@ def test_many_rows():
 
 
 def test_flat_rows_overflow_the_key_copy():
-    """Rows whose crossing top-byte bucket holds more keys than shared memory
-    keeps (the later passes read the row again): all tied, and mostly tied."""
+    """Rows whose crossing exponent field holds more keys than the id list
+    keeps (the later digits and the mask come from passes over the row): all
+    tied, and mostly tied.  (A row of 20000 equal values, whose 16-bit prefix
+    overflows only the small list, is in the ties test.)"""
     V = 1 << 18
     g = np.random.default_rng(21)
     rows = np.zeros((3, V), np.float32)
@@ -86,8 +88,8 @@ def test_flat_rows_overflow_the_key_copy():
 
 
 def test_values_above_128():
-    """Unnormalised rows with values >= 2^7 (top bytes above the 24 private
-    buckets; weights clamped at 32)."""
+    """Unnormalised rows with values >= 32 (exponent fields 132 and up, whose
+    weights are clamped to 32, counted in shared buckets) and +inf."""
     g = np.random.default_rng(22)
     V = 5000
     rows = (g.random((4, V)) * 1e-3).astype(np.float32)
@@ -96,4 +98,33 @@ def test_values_above_128():
     rows[2, 7] = np.float32(np.inf)
     rows[3, 100:110] = np.float32(31.5)
     for mass in (0.5, 20.0, 32.0):
+        _check(rows, mass)
+
+
+def test_ties_at_tau_ranked_by_id():
+    """Rows whose crossing key is shared by more entries than the ties to
+    keep: the kept ties are those of lowest id.  7, 300 and 1500 ties, alone
+    at their 16-bit key prefix (ranked in the small list), and 5000 ties, more
+    than the small list holds (ranked by the pass over the row)."""
+    g = np.random.default_rng(23)
+    V = 6000
+    rows = (g.random((4, V)) * 1e-4).astype(np.float32)
+    for r, n in enumerate((7, 300, 1500, 5000)):
+        rows[r, g.choice(V, n, replace=False)] = np.float32(2e-4)
+    for mass in (0.0005, 0.03, 0.2, 0.45):
+        _check(rows, mass)
+
+
+def test_small_list_neighbours_of_tau():
+    """Keys sharing tau's 16-bit prefix on both sides of it: one field, a few
+    hundred distinct keys within one 2^-7 relative step, and exact ties."""
+    g = np.random.default_rng(24)
+    V = 50000
+    rows = (g.random((2, V)) * 1e-6).astype(np.float32)
+    base = np.float32(1e-4).view(np.uint32) & np.uint32(0xffff8000)
+    for r in range(2):
+        idx = g.choice(V, 600, replace=False)
+        bits_ = base + g.integers(0, 1 << 15, 600).astype(np.uint32) // (1 << (8 * r))
+        rows[r, idx] = bits_.view(np.float32)
+    for mass in (0.01, 0.03, 0.05):
         _check(rows, mass)
