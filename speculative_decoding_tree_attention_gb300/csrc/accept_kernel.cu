@@ -910,6 +910,8 @@ struct RsSmem {
   int nties;
   unsigned long long above;
   unsigned long long total;
+  unsigned long long xh[2][256];  // a CTA's histogram, read by the other CTAs of its row
+  unsigned long long xs[2];       // ... and one value
 };
 
 // Key bits below digit p: digit 0 is bits 30..23, digits 1..3 bits 22..15,
@@ -975,15 +977,65 @@ __device__ __forceinline__ void rs_reduce(RsSmem& sm, int tid, int wsh) {
   }
 }
 
-// The crossing digit of sm.hist (written before a barrier): the one digit d
-// with above + mass(digits > d) < T <= above + mass(digits >= d), where above
-// is the mass of the keys above the current prefix range.  Sets sm.digit and
-// sm.above (and sm.total, the whole row, when `first`).  Digit d = tid < 256;
-// warps 0-7 scan their 32 digits (descending), then across the 8 warps.
-// Every thread calls it; it ends with a barrier.
-__device__ void rs_pick(RsSmem& sm, int tid, unsigned long long above, unsigned long long T, bool first) {
+// The CTAs of a row in a cluster of C (C = 2: each takes half the row)
+// combine their histograms and counts through distributed shared memory.  An
+// exchange publishes into buffer xi & 1, meets the others at a cluster
+// barrier and reads theirs: a CTA writes a buffer again two exchanges later,
+// after the barrier of the exchange between, which the others reach only
+// after reading it.
+template <int C>
+__device__ __forceinline__ void rs_done() {
+  if constexpr (C > 1) cg::this_cluster().sync();  // no CTA leaves while another may read its buffers
+}
+
+// The sum over the row's CTAs of v (the same in every thread of a CTA);
+// *lower = the sum over the CTAs of lower rank (the earlier ids).  Every
+// thread calls it.
+template <int C>
+__device__ unsigned long long rs_xsum(RsSmem& sm, int& xi, unsigned long long v, unsigned long long* lower) {
+  if constexpr (C == 1) {
+    if (lower) *lower = 0ull;
+    return v;
+  } else {
+    cg::cluster_group cl = cg::this_cluster();
+    const int b = xi & 1;
+    if (threadIdx.x == 0) sm.xs[b] = v;
+    cl.sync();
+    const int me = static_cast<int>(cl.block_rank());
+    unsigned long long t = 0, lo = 0;
+    for (int r = 0; r < C; ++r) {
+      const unsigned long long y = *cl.map_shared_rank(&sm.xs[b], r);
+      t += y;
+      if (r < me) lo += y;
+    }
+    if (lower) *lower = lo;
+    ++xi;
+    return t;
+  }
+}
+
+// The crossing digit of sm.hist (written before a barrier; summed over the
+// row's CTAs): the one digit d with above + mass(digits > d) < T <= above +
+// mass(digits >= d), where above is the mass of the keys above the current
+// prefix range.  Sets sm.digit and sm.above (and sm.total, the whole row,
+// when `first`).  Digit d = tid < 256; warps 0-7 scan their 32 digits
+// (descending), then across the 8 warps.  Every thread calls it; it ends
+// with a barrier.
+template <int C>
+__device__ void rs_pick(RsSmem& sm, int tid, unsigned long long above, unsigned long long T, bool first, int& xi) {
   const int warp = tid >> 5, lane = tid & 31;
-  const unsigned long long H = tid < 256 ? sm.hist[tid] : 0ull;
+  unsigned long long H = tid < 256 ? sm.hist[tid] : 0ull;
+  if constexpr (C > 1) {
+    cg::cluster_group cl = cg::this_cluster();
+    const int b = xi & 1;
+    if (tid < 256) sm.xh[b][tid] = H;
+    cl.sync();
+    if (tid < 256) {
+      H = 0ull;
+      for (int r = 0; r < C; ++r) H += *cl.map_shared_rank(&sm.xh[b][tid], r);
+    }
+    ++xi;
+  }
   unsigned long long incl = H;  // sum over digits >= d within the warp
   for (int o = 1; o < 32; o <<= 1) {
     const unsigned long long y = __shfl_down_sync(0xffffffffu, incl, o);
@@ -1005,19 +1057,28 @@ __device__ void rs_pick(RsSmem& sm, int tid, unsigned long long above, unsigned 
   __syncthreads();
 }
 
+// Rows row0 + blockIdx.x / C; CTA h = blockIdx.x % C of a row (its rank in
+// the cluster) takes mask words [h wp, h wp + wp) of it, wp = ceil(words / C)
+// rounded up to 4 words (128 ids): V, words, q and mrow below are the part's.
+template <int C>
 __global__ void __launch_bounds__(kRsThreads, 1)
-    retained_set_kernel(const RetainArgs a) {
+    retained_set_kernel(const RetainArgs a, int row0) {
   extern __shared__ __align__(16) uint8_t rs_raw[];
   RsSmem& sm = *reinterpret_cast<RsSmem*>(rs_raw);
-  const int row = blockIdx.x;
+  const int row = row0 + static_cast<int>(blockIdx.x) / C;
+  const int h = static_cast<int>(blockIdx.x) % C;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t lt_mask = (1u << lane) - 1u;
-  const int V = a.vocab;
-  const int words = (V + 31) >> 5;
-  const bool vec = (V & 3) == 0;  // the row starts 16-byte aligned
-  const int nf = V >> 2;          // its float4s when vec
-  const float* q = a.draft + static_cast<size_t>(row) * V;
-  uint32_t* mrow = a.mask + static_cast<size_t>(row) * words;
+  const int Vrow = a.vocab, wrow = (Vrow + 31) >> 5;
+  const int wp = C == 1 ? wrow : (((wrow + C - 1) / C + 3) & ~3);
+  const int wlo = min(h * wp, wrow);
+  const int words = min(wlo + wp, wrow) - wlo;
+  const int V = max(0, min(Vrow, 32 * (wlo + words)) - 32 * wlo);
+  const bool vec = (Vrow & 3) == 0;  // the row (and so the part) starts 16-byte aligned
+  const int nf = V >> 2;             // its float4s when vec
+  const float* q = a.draft + static_cast<size_t>(row) * Vrow + 32 * wlo;
+  uint32_t* mrow = a.mask + static_cast<size_t>(row) * wrow + wlo;
+  int xi = 0;  // exchanges so far
   const unsigned long long T = a.threshold;
   uint32_t* whist = sm.pool;
   uint32_t* myh = whist + (warp >> 1) * 512;
@@ -1070,18 +1131,19 @@ __global__ void __launch_bounds__(kRsThreads, 1)
   }
   if (tid < 256 && (tid < kRsE0 || tid >= kRsEBig)) sm.hist[tid] = tid < kRsE0 ? 0ull : sm.big[tid];
   __syncthreads();
-  rs_pick(sm, tid, 0ull, T, true);
+  rs_pick<C>(sm, tid, 0ull, T, true, xi);
   if (sm.total < T) {  // the mass never reaches T: every token is kept
     const unsigned long long total = sm.total;
     for (int word = tid; word < words; word += kRsThreads) {
       const int v0 = word * 32;
       mrow[word] = (V - v0 >= 32) ? 0xffffffffu : ((1u << (V - v0)) - 1u);
     }
-    if (tid == 0) {
+    if (tid == 0 && h == 0) {
       if (a.z_fixed) a.z_fixed[row] = total;
       if (a.z) a.z[row] = __fmul_rn(__ull2float_rn(total), kTwoM40);
-      if (a.kept) a.kept[row] = V;
+      if (a.kept) a.kept[row] = Vrow;
     }
+    rs_done<C>();
     return;
   }
   const int ex = sm.digit;  // e*: 87..255 (its mass is > 0)
@@ -1178,7 +1240,7 @@ __global__ void __launch_bounds__(kRsThreads, 1)
   }
 
   int p = 1;  // the next digit
-  if (n <= cap) {
+  if (rs_xsum<C>(sm, xi, n > cap ? 1ull : 0ull, nullptr) == 0ull) {  // every part's ids listed
     // ---- digit 1 (bits 22..15) over the listed keys, gathered again by id:
     // thread t takes entries t + 1024 u, and keeps bits 30..15 of the keys of
     // the first round in registers (two to a register) for the filter
@@ -1210,7 +1272,7 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     __syncthreads();
     rs_reduce(sm, tid, wsh);
     __syncthreads();
-    rs_pick(sm, tid, above, T, false);
+    rs_pick<C>(sm, tid, above, T, false, xi);
     prefix = (prefix << 8) | static_cast<uint32_t>(sm.digit);  // key >> 15 of tau
     above = sm.above;
     p = 2;
@@ -1249,7 +1311,7 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     }
     __syncthreads();  // also: sm.digit / sm.above are rewritten by the next pick
     const int nsmall = sm.nsmall;
-    if (nsmall <= kRsSmallCap) {
+    if (rs_xsum<C>(sm, xi, nsmall > kRsSmallCap ? 1ull : 0ull, nullptr) == 0ull) {
       // ---- digits 2 and 3 over the small list
       for (; p < 4; ++p) {
         const int sh = rs_shift(p), shp = rs_shift(p - 1);
@@ -1263,7 +1325,7 @@ __global__ void __launch_bounds__(kRsThreads, 1)
         __syncthreads();
         rs_reduce(sm, tid, wsh);
         __syncthreads();
-        rs_pick(sm, tid, above, T, false);
+        rs_pick<C>(sm, tid, above, T, false, xi);
         prefix = (prefix << (shp - sh)) | static_cast<uint32_t>(sm.digit);
         above = sm.above;
         __syncthreads();
@@ -1281,7 +1343,9 @@ __global__ void __launch_bounds__(kRsThreads, 1)
         }
       }
       __syncthreads();
-      const unsigned long long nties = static_cast<unsigned long long>(sm.nties);
+      unsigned long long lower_ties = 0;  // ties in the parts of lower id
+      const unsigned long long nties =
+          rs_xsum<C>(sm, xi, static_cast<unsigned long long>(sm.nties), &lower_ties);
       for (int i = tid; i < nsmall; i += kRsThreads) {
         if (skeys[i] != tau) continue;
         const uint32_t id = sids[i];
@@ -1289,7 +1353,7 @@ __global__ void __launch_bounds__(kRsThreads, 1)
         if (!keep) {                // else the need of lowest id
           unsigned long long r = 0;
           for (int j = 0; j < nsmall; ++j) r += (skeys[j] == tau && sids[j] < id) ? 1ull : 0ull;
-          keep = r < need;
+          keep = lower_ties + r < need;
         }
         if (keep) atomicOr(bits + (id >> 5), 1u << (id & 31u));
       }
@@ -1303,14 +1367,16 @@ __global__ void __launch_bounds__(kRsThreads, 1)
       for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
       if (lane == 0) sm.iscan[warp] = cnt;
       __syncthreads();
-      if (tid == 0) {
-        int kept = 0;
-        for (int w = 0; w < kRsWarps; ++w) kept += sm.iscan[w];
+      unsigned long long kept = 0;
+      for (int w = 0; w < kRsWarps; ++w) kept += static_cast<unsigned long long>(sm.iscan[w]);
+      kept = rs_xsum<C>(sm, xi, kept, nullptr);
+      if (tid == 0 && h == 0) {
         const unsigned long long Z = above + need * wt;
         if (a.z_fixed) a.z_fixed[row] = Z;
         if (a.z) a.z[row] = __fmul_rn(__ull2float_rn(Z), kTwoM40);
-        if (a.kept) a.kept[row] = kept;
+        if (a.kept) a.kept[row] = static_cast<int>(kept);
       }
+      rs_done<C>();
       return;
     }
   }
@@ -1353,7 +1419,7 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     __syncthreads();
     rs_reduce(sm, tid, wsh);
     __syncthreads();
-    rs_pick(sm, tid, above, T, false);
+    rs_pick<C>(sm, tid, above, T, false, xi);
     prefix = (prefix << (shp - sh)) | static_cast<uint32_t>(sm.digit);
     above = sm.above;
     __syncthreads();  // sm.digit / sm.above / sm.red are rewritten by the next pick
@@ -1362,12 +1428,23 @@ __global__ void __launch_bounds__(kRsThreads, 1)
   const unsigned long long wt = static_cast<unsigned long long>(rs_addend(tau, ex)) << wsh;  // > 0
   const unsigned long long need = (T - above + wt - 1) / wt;  // ties to keep
 
-  // ---- the mask by a pass over the row, in rounds of 512 consecutive words: warp w reads words
-  // base + 32w + j (j = 0..31, lane L holding id 32 word + L), so a word's
-  // keep and tie bits are two ballots, and lane L keeps those of word
-  // base + 32w + L.  The ties' ranks in id order are the ties of the earlier
-  // rounds plus a block scan of the per-word counts of this round.
-  unsigned long long ties_before = 0;  // ties in the earlier rounds
+  // ---- the mask by a pass over the row, in rounds of 1024 consecutive
+  // words: warp w reads words base + 32w + j (j = 0..31, lane L holding id
+  // 32 word + L), so a word's keep and tie bits are two ballots, and lane L
+  // keeps those of word base + 32w + L.  The ties' ranks in id order are the
+  // ties of the parts of lower id and of the earlier rounds plus a block scan
+  // of the per-word counts of this round.
+  unsigned long long ties_before = 0;  // ties in the lower parts and the earlier rounds
+  if constexpr (C > 1) {
+    int t = 0;
+    for (int w = warp; w < words; w += kRsWarps) t += rs_key(rs_load(q, V, w * 32 + lane)) == tau ? 1 : 0;
+    for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) sm.iscan[warp] = t;
+    __syncthreads();
+    unsigned long long own = 0;
+    for (int w = 0; w < kRsWarps; ++w) own += static_cast<unsigned long long>(sm.iscan[w]);
+    rs_xsum<C>(sm, xi, own, &ties_before);  // its barrier also orders sm.iscan
+  }
   int n_gt = 0;                        // kept keys above tau in this thread's words
   for (int base = 0; base < words; base += kRsThreads) {
     const int wb = base + 32 * warp;
@@ -1428,14 +1505,16 @@ __global__ void __launch_bounds__(kRsThreads, 1)
   for (int o = 16; o; o >>= 1) n_gt += __shfl_xor_sync(0xffffffffu, n_gt, o);
   if (lane == 0) sm.iscan[warp] = n_gt;
   __syncthreads();
-  if (tid == 0) {
-    long long g = 0;
-    for (int w = 0; w < kRsWarps; ++w) g += sm.iscan[w];
+  unsigned long long g = 0;
+  for (int w = 0; w < kRsWarps; ++w) g += static_cast<unsigned long long>(sm.iscan[w]);
+  g = rs_xsum<C>(sm, xi, g, nullptr);
+  if (tid == 0 && h == 0) {
     const unsigned long long Z = above + need * wt;
     if (a.z_fixed) a.z_fixed[row] = Z;
     if (a.z) a.z[row] = __fmul_rn(__ull2float_rn(Z), kTwoM40);
-    if (a.kept) a.kept[row] = static_cast<int>(g + static_cast<long long>(need));
+    if (a.kept) a.kept[row] = static_cast<int>(g + need);
   }
+  rs_done<C>();
 }
 }  // namespace
 
@@ -1517,17 +1596,43 @@ size_t accept_workspace_bytes(int vocab, int total_nodes) {
 
 int accept_max_nodes() { return kMaxN; }
 
+// One CTA per row, or two (a cluster of two, half the row each) when the
+// rows fill at most half of the SMs.
 int launch_retained_set(const RetainArgs& a, cudaStream_t stream) {
-  static thread_local int attr_dev = -1;
+  static thread_local int attr_dev = -1, sms = 148;
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_dev != dev) {
-    cudaFuncSetAttribute(retained_set_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(retained_set_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(sizeof(RsSmem)));
+    cudaFuncSetAttribute(retained_set_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(sizeof(RsSmem)));
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) sms = n;
     attr_dev = dev;
   }
-  retained_set_kernel<<<static_cast<unsigned>(a.rows), kRsThreads, sizeof(RsSmem), stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  const int split = 2 * a.rows <= sms ? a.rows : 0;  // rows of two CTAs
+  const int whole = a.rows - split;
+  if (whole > 0) {
+    retained_set_kernel<1><<<static_cast<unsigned>(whole), kRsThreads, sizeof(RsSmem), stream>>>(a, 0);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+  }
+  if (split > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * split, 1, 1);
+    cfg.blockDim = dim3(kRsThreads, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(RsSmem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, retained_set_kernel<2>, a, whole) != cudaSuccess) return -1;
+  }
+  return 0;
 }
 
 

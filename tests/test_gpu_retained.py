@@ -23,10 +23,20 @@ def _run(rows, mass):
 
 
 def _check(rows, mass):
-    got = _run(rows, mass)
+    """The rows alone (up to half a wave of rows: two CTAs a row), then
+    repeated past a full wave of SMs, so that every row is also computed by
+    one CTA (the full waves) and the last copies again by two."""
+    rows = np.ascontiguousarray(rows, np.float32)
     ref = oracle.retained_set(rows, mass)
+    got = _run(rows, mass)
     for name, g, r in zip(("mask", "z_fixed", "z", "kept"), got, ref):
         assert np.array_equal(g, r), (name, np.nonzero(np.any(np.atleast_2d(g != r), axis=-1)))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    k = -(-sms // rows.shape[0]) + 1
+    tiled = _run(np.concatenate([rows] * k), mass)
+    for name, g, r in zip(("mask", "z_fixed", "z", "kept"), tiled, ref):
+        want = np.concatenate([r] * k)
+        assert np.array_equal(g, want), (name, "tiled", np.nonzero(np.any(np.atleast_2d(g != want), axis=-1)))
     return got
 
 
