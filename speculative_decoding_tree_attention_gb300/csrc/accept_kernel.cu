@@ -874,7 +874,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
 //     bits 30..15 of its keys in registers: the histogram of bits 22..15, then
 //     a filter that sets the mask bits of the keys above the new 16-bit prefix
 //     and copies the keys at it, with their ids, into a small list, whose
-//     histograms of bits 14..7 and 6..0 give tau.  The mask is the bitmap
+//     keys give tau (by pairwise mass sums for up to 256 keys in a one-CTA
+//     row, else the histograms of bits 14..7 and 6..0).  The mask is the bitmap
 //     plus the small list's keys above tau and its ties at tau: all of them
 //     when their number is the number of ties to keep, c = ceil((T - mass
 //     above tau) / fix40(tau)), else the c of lowest id.
@@ -892,6 +893,7 @@ constexpr int kRsHists = kRsWarps / 2;             // later histograms: one per 
 constexpr int kRsHistWords = kRsHists * 2 * 256;   // of two 16-bit weight parts
 constexpr int kRsMaskWords = 8192;                 // a row's mask words (V <= 2^18)
 constexpr int kRsSmallCap = 2048;                  // keys at the 16-bit prefix
+constexpr int kRsDirect = 256;  // up to this many, tau is picked from the small list by pairwise sums
 // ids of field e* the pool holds after the histograms, two bitmaps and the
 // small list: at least 17408 (V = 2^18), 24296 at V = 151936
 static_assert(kRsPoolWords - (kRsHistWords + 2 * kRsMaskWords + 2 * kRsSmallCap) >= 17408, "pool");
@@ -1312,6 +1314,30 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     __syncthreads();  // also: sm.digit / sm.above are rewritten by the next pick
     const int nsmall = sm.nsmall;
     if (rs_xsum<C>(sm, xi, nsmall > kRsSmallCap ? 1ull : 0ull, nullptr) == 0ull) {
+      if (C == 1 && nsmall <= kRsDirect) {
+        // ---- tau directly: the key of the small list (all keys at the
+        // 16-bit prefix) whose mass above, plus the mass above the prefix,
+        // is < T while that plus its own ties' mass is >= T; exactly one
+        // distinct key qualifies, and its entries all write the same values
+        for (int i = tid; i < nsmall; i += kRsThreads) {
+          const uint32_t ki = skeys[i];
+          unsigned long long gt = 0, eq = 0;
+          for (int k = 0; k < nsmall; ++k) {
+            const uint32_t kj = skeys[k];
+            const unsigned long long w = static_cast<unsigned long long>(rs_addend(kj, ex)) << wsh;
+            gt += kj > ki ? w : 0ull;
+            eq += kj == ki ? w : 0ull;
+          }
+          if (above + gt < T && above + gt + eq >= T) {
+            sm.digit = static_cast<int>(ki);
+            sm.above = above + gt;
+          }
+        }
+        __syncthreads();
+        prefix = static_cast<uint32_t>(sm.digit);
+        above = sm.above;
+        p = 4;
+      }
       // ---- digits 2 and 3 over the small list
       for (; p < 4; ++p) {
         const int sh = rs_shift(p), shp = rs_shift(p - 1);
