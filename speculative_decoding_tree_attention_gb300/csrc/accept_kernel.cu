@@ -905,7 +905,6 @@ struct RsSmem {
   alignas(16) uint32_t pool[kRsPoolWords];
   unsigned long long big[256];  // pass 0: fields 132..255
   unsigned long long hist[256];
-  unsigned long long red[kRsWarps];
   int iscan[kRsWarps];
   int digit;
   int nsmall;
@@ -1020,40 +1019,49 @@ __device__ unsigned long long rs_xsum(RsSmem& sm, int& xi, unsigned long long v,
 // row's CTAs): the one digit d with above + mass(digits > d) < T <= above +
 // mass(digits >= d), where above is the mass of the keys above the current
 // prefix range.  Sets sm.digit and sm.above (and sm.total, the whole row,
-// when `first`).  Digit d = tid < 256; warps 0-7 scan their 32 digits
-// (descending), then across the 8 warps.  Every thread calls it; it ends
-// with a barrier.
+// when `first`).  Warp 0 alone scans: lane L holds digits 8L .. 8L + 7, a
+// shuffle scan sums the lanes above, and each lane walks its own digits.
+// Every thread calls it; it ends with a barrier.
 template <int C>
 __device__ void rs_pick(RsSmem& sm, int tid, unsigned long long above, unsigned long long T, bool first, int& xi) {
-  const int warp = tid >> 5, lane = tid & 31;
-  unsigned long long H = tid < 256 ? sm.hist[tid] : 0ull;
+  const int lane = tid & 31;
   if constexpr (C > 1) {
     cg::cluster_group cl = cg::this_cluster();
     const int b = xi & 1;
-    if (tid < 256) sm.xh[b][tid] = H;
+    if (tid < 256) sm.xh[b][tid] = sm.hist[tid];
     cl.sync();
     if (tid < 256) {
-      H = 0ull;
+      unsigned long long H = 0ull;
       for (int r = 0; r < C; ++r) H += *cl.map_shared_rank(&sm.xh[b][tid], r);
+      sm.hist[tid] = H;
     }
     ++xi;
+    __syncthreads();
   }
-  unsigned long long incl = H;  // sum over digits >= d within the warp
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_down_sync(0xffffffffu, incl, o);
-    if (lane + o < 32) incl += y;
-  }
-  if (tid < 256 && lane == 0) sm.red[warp] = incl;  // warp totals
-  __syncthreads();
-  if (tid < 256) {
-    unsigned long long higher = 0;  // digits of the warps above
-    for (int w = warp + 1; w < 8; ++w) higher += sm.red[w];
-    const unsigned long long ge = above + higher + incl;  // mass of digits >= d
-    const unsigned long long gt = ge - H;                 // mass of digits > d
-    if (first && tid == 0) sm.total = ge;                 // digit 0: the whole row
-    if (gt < T && ge >= T) {
-      sm.digit = tid;
-      sm.above = gt;
+  if (tid < 32) {
+    unsigned long long h[8], own = 0ull;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      h[k] = sm.hist[8 * lane + k];
+      own += h[k];
+    }
+    unsigned long long incl = own;  // the digits of this lane and of the lanes above
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_down_sync(0xffffffffu, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    const unsigned long long ge0 = above + incl;  // mass of digits >= 8 lane
+    if (first && lane == 0) sm.total = ge0;       // digit 0: the whole row
+    unsigned long long lower = 0ull;              // this lane's digits below k
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const unsigned long long gek = ge0 - lower;  // mass of digits >= 8 lane + k
+      const unsigned long long gtk = gek - h[k];   // mass of digits > 8 lane + k
+      if (gtk < T && gek >= T) {
+        sm.digit = 8 * lane + k;
+        sm.above = gtk;
+      }
+      lower += h[k];
     }
   }
   __syncthreads();
@@ -1154,7 +1162,13 @@ __global__ void __launch_bounds__(kRsThreads, 1)
   unsigned long long above = sm.above;  // mass of the keys above the prefix range
 
   // ---- pass 1: mask bits of the keys of fields above e* (bits) and of
-  // field e* (mbits), each word written once
+  // field e* (mbits), each word written once; the histograms of the next
+  // digit are cleared meanwhile (pass 0's sums are read)
+  for (int i = tid; i < kRsHistWords; i += kRsThreads) whist[i] = 0u;
+  if (tid == 0) {
+    sm.nsmall = 0;
+    sm.nties = 0;
+  }
   {
     const uint32_t lim = static_cast<uint32_t>(ex + 1) << 23;  // keys of fields > e*
     const uint32_t lo = static_cast<uint32_t>(ex) << 23;       // keys of field e*: [lo, lim)
@@ -1246,12 +1260,6 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     // ---- digit 1 (bits 22..15) over the listed keys, gathered again by id:
     // thread t takes entries t + 1024 u, and keeps bits 30..15 of the keys of
     // the first round in registers (two to a register) for the filter
-    for (int i = tid; i < kRsHistWords; i += kRsThreads) whist[i] = 0u;
-    if (tid == 0) {
-      sm.nsmall = 0;
-      sm.nties = 0;
-    }
-    __syncthreads();
     uint32_t hk[kRsGather / 2];
 #pragma unroll
     for (int u = 0; u < kRsGather / 2; ++u) hk[u] = 0u;
@@ -1448,7 +1456,7 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     rs_pick<C>(sm, tid, above, T, false, xi);
     prefix = (prefix << (shp - sh)) | static_cast<uint32_t>(sm.digit);
     above = sm.above;
-    __syncthreads();  // sm.digit / sm.above / sm.red are rewritten by the next pick
+    __syncthreads();  // sm.digit / sm.above are rewritten by the next pick
   }
   const uint32_t tau = prefix;
   const unsigned long long wt = static_cast<unsigned long long>(rs_addend(tau, ex)) << wsh;  // > 0
