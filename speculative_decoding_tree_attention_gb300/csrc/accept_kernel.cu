@@ -943,8 +943,9 @@ __device__ __forceinline__ float4 rs_load4(const float* q, int nf, int f) {
 }
 
 // Pass 0's update for one entry (x as loaded, any value): a into this
-// thread's private sum of its field, or 2^45 into the shared bucket of a
-// field above the clamp.  Non-positive entries (field >= 256 as bits), NaN,
+// thread's private sum of its field (a shared atomic add: one instruction
+// where a load, add and store take three; no other thread touches the
+// word), or 2^45 into the shared bucket of a field above the clamp.  Non-positive entries (field >= 256 as bits), NaN,
 // zeros, denormals and fields below 87 add nothing.
 __device__ __forceinline__ void rs_count0(RsSmem& sm, int tid, float x) {
   const uint32_t k = __float_as_uint(x);
@@ -952,7 +953,7 @@ __device__ __forceinline__ void rs_count0(RsSmem& sm, int tid, float x) {
   const uint32_t b = e - kRsE0;
   if (b < static_cast<uint32_t>(kRsExps)) {
     const uint32_t m = (k & 0x7fffffu) | 0x800000u;
-    sm.pool[b * kRsThreads + tid] += m >> max(110 - static_cast<int>(e), 0);
+    atomicAdd(&sm.pool[b * kRsThreads + tid], m >> max(110 - static_cast<int>(e), 0));
   } else if (e - kRsEBig < static_cast<uint32_t>(256 - kRsEBig) && k <= 0x7f800000u) {
     atomicAdd(&sm.big[e], 1ull << 45);
   }
@@ -1172,6 +1173,11 @@ __global__ void __launch_bounds__(kRsThreads, 1)
   {
     const uint32_t lim = static_cast<uint32_t>(ex + 1) << 23;  // keys of fields > e*
     const uint32_t lo = static_cast<uint32_t>(ex) << 23;       // keys of field e*: [lo, lim)
+    // the same tests on the floats (false for NaN and for x <= 0): x above
+    // field e* iff x >= flim (NaN bound for e* = 255: nothing is above), x
+    // in it iff x >= flo and not above
+    const float flim = __uint_as_float(ex < 255 ? lim : 0x7fc00000u);
+    const float flo = __uint_as_float(lo);
     if (vec) {
       for (int g0 = warp; g0 * 32 < nf; g0 += kRsWarps * kRsUnroll) {
         float4 x[kRsUnroll];
@@ -1180,18 +1186,17 @@ __global__ void __launch_bounds__(kRsThreads, 1)
 #pragma unroll
         for (int u = 0; u < kRsUnroll; ++u) {
           const int f = (g0 + u * kRsWarps) * 32 + lane;  // ids 4f .. 4f + 3
-          const uint32_t k0 = rs_key(x[u].x), k1 = rs_key(x[u].y), k2 = rs_key(x[u].z), k3 = rs_key(x[u].w);
           // mask word f / 8 holds the nibbles of lanes 8j .. 8j + 7, the
           // nibble of lane L at bit 4 (L % 8)
           const int sh = 4 * (lane & 7);
-          uint32_t av = (static_cast<uint32_t>(k0 >= lim) | (static_cast<uint32_t>(k1 >= lim) << 1) |
-                         (static_cast<uint32_t>(k2 >= lim) << 2) | (static_cast<uint32_t>(k3 >= lim) << 3))
-                        << sh;
-          uint32_t mv = (static_cast<uint32_t>(k0 - lo < 0x800000u) |
-                         (static_cast<uint32_t>(k1 - lo < 0x800000u) << 1) |
-                         (static_cast<uint32_t>(k2 - lo < 0x800000u) << 2) |
-                         (static_cast<uint32_t>(k3 - lo < 0x800000u) << 3))
-                        << sh;
+          const uint32_t an = static_cast<uint32_t>(x[u].x >= flim) | (static_cast<uint32_t>(x[u].y >= flim) << 1) |
+                              (static_cast<uint32_t>(x[u].z >= flim) << 2) |
+                              (static_cast<uint32_t>(x[u].w >= flim) << 3);
+          const uint32_t gn = static_cast<uint32_t>(x[u].x >= flo) | (static_cast<uint32_t>(x[u].y >= flo) << 1) |
+                              (static_cast<uint32_t>(x[u].z >= flo) << 2) |
+                              (static_cast<uint32_t>(x[u].w >= flo) << 3);
+          uint32_t av = an << sh;
+          uint32_t mv = (gn & ~an) << sh;
 #pragma unroll
           for (int o = 1; o < 8; o <<= 1) {
             av |= __shfl_xor_sync(0xffffffffu, av, o);
@@ -1214,9 +1219,8 @@ __global__ void __launch_bounds__(kRsThreads, 1)
 #pragma unroll
         for (int u = 0; u < kRsUnroll; ++u) {
           const int word = w0 + u * kRsWarps;
-          const uint32_t k = rs_key(x[u]);
-          const uint32_t av = __ballot_sync(0xffffffffu, k >= lim);
-          const uint32_t mv = __ballot_sync(0xffffffffu, k - lo < 0x800000u);
+          const uint32_t av = __ballot_sync(0xffffffffu, x[u] >= flim);
+          const uint32_t mv = __ballot_sync(0xffffffffu, x[u] >= flo) & ~av;
           if (lane == 0 && word < words) {
             bits[word] = av;
             mbits[word] = mv;
