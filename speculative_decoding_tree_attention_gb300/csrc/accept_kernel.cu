@@ -68,8 +68,8 @@ __host__ __device__ inline int tree_smem_bytes(int chunk, bool multi) {
   return (multi ? 3 : 2) * chunk * 4 + (chunk / 32) * 4;
 }
 constexpr int kRowThreads = 256;
-constexpr int kRowVec = 8;             // float4 per thread per chunk
-constexpr int kChunk = kRowThreads * kRowVec * 4;  // 8192 entries per row chunk
+constexpr int kRowVec = 8;             // float4 per thread per chunk (logits rows)
+constexpr int kChunk = kRowThreads * kRowVec * 4;  // 8192 entries per row chunk (workspace unit)
 constexpr float kTwo40 = 1099511627776.0f;
 constexpr float kTwoM40 = 9.094947017729282379150390625e-13f;
 
@@ -129,9 +129,15 @@ __device__ bool block_has_child(const int32_t* parent, int n0, int N, int j) {
 }
 
 // ============================================================ row statistics
-__global__ void __launch_bounds__(kRowThreads, 3)
+// RV float4 per thread per chunk of kRowThreads * RV * 4 entries: 8 (three
+// CTAs per SM) for logits rows alone; 4 (six CTAs per SM, more of them in
+// flight) when draft rows and a mask are read as well.  nchunk counts chunks
+// of that size.
+template <int RV>
+__global__ void __launch_bounds__(kRowThreads, RV == 8 ? 3 : 6)
     accept_rowstats_kernel(const AcceptArgs a, int nchunk, int nparts, float2* ws_ms,
                            unsigned long long* ws_z) {
+  constexpr int kCh = kRowThreads * RV * 4;
   // the per-tree kernel may start now: its prologue (tree loads and checks)
   // overlaps this kernel; it waits for our results in griddepcontrol.wait
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -164,11 +170,11 @@ __global__ void __launch_bounds__(kRowThreads, 3)
   float m = -INFINITY, s = 0.0f;
   unsigned long long z = 0;
   for (int c = part; c < nchunk; c += nparts) {
-    const int v0 = c * kChunk, v1 = min(V, v0 + kChunk);
+    const int v0 = c * kCh, v1 = min(V, v0 + kCh);
     if (vec) {
-      float4 tv[kRowVec], dv[kRowVec];
+      float4 tv[RV], dv[RV];
 #pragma unroll
-      for (int k = 0; k < kRowVec; ++k) {
+      for (int k = 0; k < RV; ++k) {
         const int v = v0 + (k * kRowThreads + threadIdx.x) * 4;
         tv[k] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         dv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -190,12 +196,12 @@ __global__ void __launch_bounds__(kRowThreads, 3)
         // is held to; terms below 2^-126 flush to zero)
         float cm = -INFINITY, cs = 0.0f;
 #pragma unroll
-        for (int k = 0; k < kRowVec; ++k)
+        for (int k = 0; k < RV; ++k)
           cm = fmaxf(cm, fmaxf(fmaxf(tv[k].x, tv[k].y), fmaxf(tv[k].z, tv[k].w)));
         if (cm != -INFINITY) {
           constexpr float kLog2e = 1.4426950408889634f;
 #pragma unroll
-          for (int k = 0; k < kRowVec; ++k)
+          for (int k = 0; k < RV; ++k)
             cs += (ex2_approx((tv[k].x - cm) * kLog2e) + ex2_approx((tv[k].y - cm) * kLog2e)) +
                   (ex2_approx((tv[k].z - cm) * kLog2e) + ex2_approx((tv[k].w - cm) * kLog2e));
         }
@@ -204,7 +210,7 @@ __global__ void __launch_bounds__(kRowThreads, 3)
       }
       if (masked) {
 #pragma unroll
-        for (int k = 0; k < kRowVec; ++k) {
+        for (int k = 0; k < RV; ++k) {
           const int v = v0 + (k * kRowThreads + threadIdx.x) * 4;
           if (v >= v1) continue;
           const uint32_t w = __ldg(mrow + (v >> 5)) >> (v & 31);
@@ -1589,12 +1595,21 @@ int launch_accept(const AcceptArgs& a, void* workspace, cudaStream_t stream) {
       static_cast<char*>(workspace) + sizeof(float2) * static_cast<size_t>(a.total_nodes) * nchunk);
   const bool stats = a.kind == 1 || a.mask != nullptr;
   // CTAs per row: enough for about four CTAs per SM over all rows (most of
-  // which are leaves and exit at once); each takes every nparts-th chunk
-  const int nparts = max(1, min(nchunk, static_cast<int>((4l * sms + a.total_nodes - 1) / a.total_nodes)));
+  // which are leaves and exit at once), twelve when draft rows and a mask
+  // are read too (rows of twice the bytes, six CTAs per SM); each takes
+  // every nparts-th chunk.  At most one per workspace chunk.
+  const bool masked = a.mask != nullptr;
+  const long per_sm = masked ? 12l : 4l;
+  const int nparts = max(1, min(nchunk, static_cast<int>((per_sm * sms + a.total_nodes - 1) / a.total_nodes)));
   if (stats) {
-    const long items = static_cast<long>(a.total_nodes) * nparts;
-    accept_rowstats_kernel<<<static_cast<unsigned>(items), kRowThreads, 0, stream>>>(a, nchunk, nparts, ws_ms,
-                                                                                    ws_z);
+    const unsigned items = static_cast<unsigned>(static_cast<long>(a.total_nodes) * nparts);
+    if (masked) {
+      constexpr int kCh4 = kRowThreads * 4 * 4;
+      accept_rowstats_kernel<4><<<items, kRowThreads, 0, stream>>>(a, (a.vocab + kCh4 - 1) / kCh4, nparts,
+                                                                   ws_ms, ws_z);
+    } else {
+      accept_rowstats_kernel<kRowVec><<<items, kRowThreads, 0, stream>>>(a, nchunk, nparts, ws_ms, ws_z);
+    }
     if (cudaGetLastError() != cudaSuccess) return -1;
   }
   static thread_local int attr_dev = -1;
