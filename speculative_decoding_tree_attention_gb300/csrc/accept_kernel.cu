@@ -874,8 +874,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
 //     +inf, weight clamped to 2^45) go to shared u64 buckets.
 //   pass 1 (the row again): with the crossing field e* known, the mask bits
 //     of the keys above it go to a bitmap in shared memory and those of the
-//     keys of field e* to a second one, from which a block scan lists the ids
-//     of field e* in id order.
+//     keys of field e* to a second one, from which each warp lists the ids
+//     of its run of mask words (a warp scan) in its slice of the id list.
 //   The rest gathers those keys again by id (from L2), each thread keeping
 //     bits 30..15 of its keys in registers: the histogram of bits 22..15, then
 //     a filter that sets the mask bits of the keys above the new 16-bit prefix
@@ -885,7 +885,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
 //     plus the small list's keys above tau and its ties at tau: all of them
 //     when their number is the number of ties to keep, c = ceil((T - mass
 //     above tau) / fix40(tau)), else the c of lowest id.
-// A row whose field e* holds more keys than the id list, or whose 16-bit
+// A row whose field e* holds more keys in some warp's words than its slice,
+// or whose 16-bit
 // prefix more than the small list, takes its remaining digits by passes over
 // the row and its mask by a pass over the row that ranks the ties in id order
 // with a block scan.
@@ -915,6 +916,7 @@ struct RsSmem {
   int digit;
   int nsmall;
   int nties;
+  int ovf;  // a warp's ids of field e* overflowed its slice
   unsigned long long above;
   unsigned long long total;
   unsigned long long xh[2][256];  // a CTA's histogram, read by the other CTAs of its row
@@ -1175,6 +1177,7 @@ __global__ void __launch_bounds__(kRsThreads, 1)
   if (tid == 0) {
     sm.nsmall = 0;
     sm.nties = 0;
+    sm.ovf = 0;
   }
   {
     const uint32_t lim = static_cast<uint32_t>(ex + 1) << 23;  // keys of fields > e*
@@ -1236,60 +1239,62 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     }
   }
   __syncthreads();
-  // ---- the ids of field e*, in id order: thread t takes words [t c, t c + c)
-  // and writes its ids after those of the threads before it (a block scan)
-  int n = 0;  // ids of field e*
+  // ---- the ids of field e*: warp w takes mask words [w wpw, w wpw + wpw),
+  // 32 at a time (lane L word base + L), and lists their ids in id order in
+  // its own slice of the list (a warp scan of the words' counts); no block
+  // barrier until the histogram below is complete
+  const int wpw = (words + kRsWarps - 1) / kRsWarps;
+  const int slice = cap / kRsWarps;
+  uint32_t* wids = ids + warp * slice;
+  int n = 0;  // ids of field e* in this warp's words (the same in every lane)
   {
-    const int c = (words + kRsThreads - 1) / kRsThreads;
-    const int w0 = min(tid * c, words), w1 = min(w0 + c, words);
-    int cnt = 0;
-    for (int w = w0; w < w1; ++w) cnt += __popc(mbits[w]);
-    int incl = cnt;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+    const int wb = min(warp * wpw, words), we = min(wb + wpw, words);
+    for (int base = wb; base < we; base += 32) {
+      const int w = base + lane;
+      const uint32_t v0 = w < we ? mbits[w] : 0u;
+      const int c = __popc(v0);
+      int incl = c;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int pos = n + incl - c;
+      for (uint32_t v = v0; v; v &= v - 1u, ++pos)
+        if (pos < slice) wids[pos] = 32u * static_cast<uint32_t>(w) + static_cast<uint32_t>(__ffs(v) - 1);
+      n += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 31) sm.iscan[warp] = incl;
-    __syncthreads();
-    int before = incl - cnt;
-    for (int w = 0; w < kRsWarps; ++w) {
-      const int y = sm.iscan[w];
-      if (w < warp) before += y;
-      n += y;
+    if (lane == 0 && n > slice) sm.ovf = 1;
+  }
+  const int nw = min(n, slice);
+
+  // ---- digit 1 (bits 22..15) over the listed keys, gathered again by id:
+  // lane L of a warp takes its slice's entries L + 32 u, and keeps bits
+  // 30..15 of the keys of the first round in registers (two to a register)
+  // for the filter.  (A warp whose slice overflowed makes the whole row take
+  // the passes over the row below, so its partial sums do not matter.)
+  uint32_t hk[kRsGather / 2];
+#pragma unroll
+  for (int u = 0; u < kRsGather / 2; ++u) hk[u] = 0u;
+  for (int r0 = 0; r0 < nw; r0 += 32 * kRsGather) {
+    float x[kRsGather];
+#pragma unroll
+    for (int u = 0; u < kRsGather; ++u) {
+      const int i = r0 + lane + 32 * u;
+      x[u] = i < nw ? __ldcg(q + wids[i]) : 0.0f;
     }
-    if (n <= cap) {
-      for (int w = w0; w < w1; ++w) {
-        for (uint32_t v = mbits[w]; v; v &= v - 1u) ids[before++] = 32u * w + (__ffs(v) - 1);
+#pragma unroll
+    for (int u = 0; u < kRsGather; ++u) {
+      if (r0 + lane + 32 * u < nw) {
+        const uint32_t k = rs_key(x[u]);
+        rs_add2(myh, (k >> 15) & 255u, rs_addend(k, ex));
+        if (r0 == 0) hk[u / 2] |= (k >> 15) << (16 * (u & 1));
       }
     }
-    __syncthreads();  // the ids are complete; sm.iscan is rewritten below
   }
+  __syncthreads();
 
   int p = 1;  // the next digit
-  if (rs_xsum<C>(sm, xi, n > cap ? 1ull : 0ull, nullptr) == 0ull) {  // every part's ids listed
-    // ---- digit 1 (bits 22..15) over the listed keys, gathered again by id:
-    // thread t takes entries t + 1024 u, and keeps bits 30..15 of the keys of
-    // the first round in registers (two to a register) for the filter
-    uint32_t hk[kRsGather / 2];
-#pragma unroll
-    for (int u = 0; u < kRsGather / 2; ++u) hk[u] = 0u;
-    for (int r0 = 0; r0 < n; r0 += kRsThreads * kRsGather) {
-      float x[kRsGather];
-#pragma unroll
-      for (int u = 0; u < kRsGather; ++u) {
-        const int i = r0 + tid + kRsThreads * u;
-        x[u] = i < n ? __ldcg(q + ids[i]) : 0.0f;
-      }
-#pragma unroll
-      for (int u = 0; u < kRsGather; ++u) {
-        if (r0 + tid + kRsThreads * u < n) {
-          const uint32_t k = rs_key(x[u]);
-          rs_add2(myh, (k >> 15) & 255u, rs_addend(k, ex));
-          if (r0 == 0) hk[u / 2] |= (k >> 15) << (16 * (u & 1));
-        }
-      }
-    }
-    __syncthreads();
+  if (rs_xsum<C>(sm, xi, sm.ovf ? 1ull : 0ull, nullptr) == 0ull) {  // every part's ids listed
     rs_reduce(sm, tid, wsh);
     __syncthreads();
     rs_pick<C>(sm, tid, above, T, false, xi);
@@ -1298,7 +1303,7 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     p = 2;
     // ---- filter: keys above the 16-bit prefix into the bitmap, keys at it
     // (with their ids) into the small list
-    for (int r0 = 0; r0 < n; r0 += kRsThreads * kRsGather) {
+    for (int r0 = 0; r0 < nw; r0 += 32 * kRsGather) {
       uint32_t hv[kRsGather];
       if (r0 == 0) {
 #pragma unroll
@@ -1306,17 +1311,17 @@ __global__ void __launch_bounds__(kRsThreads, 1)
       } else {
 #pragma unroll
         for (int u = 0; u < kRsGather; ++u) {
-          const int i = r0 + tid + kRsThreads * u;
-          hv[u] = i < n ? __float_as_uint(__ldcg(q + ids[i])) : 0u;
+          const int i = r0 + lane + 32 * u;
+          hv[u] = i < nw ? __float_as_uint(__ldcg(q + wids[i])) : 0u;
         }
 #pragma unroll
         for (int u = 0; u < kRsGather; ++u) hv[u] = rs_key(__uint_as_float(hv[u])) >> 15;
       }
 #pragma unroll
       for (int u = 0; u < kRsGather; ++u) {
-        const int i = r0 + tid + kRsThreads * u;
-        if (i < n) {
-          const uint32_t id = ids[i];
+        const int i = r0 + lane + 32 * u;
+        if (i < nw) {
+          const uint32_t id = wids[i];
           if (hv[u] > prefix) {
             atomicOr(bits + (id >> 5), 1u << (id & 31u));
           } else if (hv[u] == prefix) {
