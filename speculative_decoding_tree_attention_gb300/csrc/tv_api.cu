@@ -59,9 +59,9 @@ struct AttnPlan {
 
 // Fewest 128-key tiles a virtual CTA is given: below this a unit is not split
 // further, since a split piece costs about this much in fixed work (its Q
-// load, the pipeline fill and its partial-result write).  Timed at 2, 3, 4
-// and 6: only the short-prefix MHA line (32 heads x 9 tiles) moved, and 3 was
-// fastest there (each unit then splits into three whole ranges).
+// load, the pipeline fill and its partial-result write).  Timed at 2, 3, 4,
+// 5, 6 and 9: only the short-prefix MHA line (32 heads x 9 tiles) moved, and
+// 3 was fastest there (each unit then splits into three whole ranges).
 constexpr int kMinTiles = 3;
 
 // Launch plan for `sms` SMs (one persistent CTA per SM).  A layer of `lanes`
