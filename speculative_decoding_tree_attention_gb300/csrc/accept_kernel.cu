@@ -857,10 +857,11 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
 // R = the shortest prefix of that order whose fixed-point mass sum of fix40
 // quanta reaches T (the caller's floor(mass * 2^40)), or the whole row.
 //
-// One CTA of 1024 threads per row, no cluster: a wave of one CTA per SM holds
-// about 150 rows (90 MB at V = 151936), so the row, read from HBM by the first
-// pass, is still in L2 for the second.  A radix select over the key (the
-// fp32 bit pattern, which orders non-negative floats) finds the key tau at
+// One CTA of 1024 threads per row (or, when the rows fill at most half of the
+// SMs, a cluster of two CTAs, half the row each): a wave of one CTA per SM
+// holds about 150 rows (90 MB at V = 151936), so the row, read from HBM by
+// the first pass, is still in L2 for the second.  A radix select over the key
+// (the fp32 bit pattern, which orders non-negative floats) finds the key tau at
 // which the cumulative mass crosses T, a digit at a time from the top: the
 // exponent field (key bits 30..23), then bits 22..15, 14..7 and 6..0.  Every
 // sum is an exact integer: within one exponent field e the fix40 weight of an
@@ -868,15 +869,15 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
 // m >> (110 - e) (e < 110: the truncation of fix40) and s = max(e - 110, 0),
 // so the mass of a digit is (the sum of a) << s.
 //   pass 0 (the row): private u32 sums of a per thread for each of the 45
-//     fields 87..131 that carry weight below the clamp (plain adds, no
-//     conflicts: most entries share a few fields; a thread reads at most 256
-//     entries, so a sum stays below 2^32); fields 132 and up (q >= 32 or
-//     +inf, weight clamped to 2^45) go to shared u64 buckets.
+//     fields 87..131 that carry weight below the clamp (no conflicts: most
+//     entries share a few fields, so shared buckets would; a thread reads at
+//     most 256 entries, so a sum stays below 2^32); fields 132 and up (q >= 32
+//     or +inf, weight clamped to 2^45) go to shared u64 buckets.
 //   pass 1 (the row again): with the crossing field e* known, the mask bits
 //     of the keys above it go to a bitmap in shared memory and those of the
 //     keys of field e* to a second one, from which each warp lists the ids
 //     of its run of mask words (a warp scan) in its slice of the id list.
-//   The rest gathers those keys again by id (from L2), each thread keeping
+//   Each warp gathers its keys again by id (from L2), each lane keeping
 //     bits 30..15 of its keys in registers: the histogram of bits 22..15, then
 //     a filter that sets the mask bits of the keys above the new 16-bit prefix
 //     and copies the keys at it, with their ids, into a small list, whose
@@ -886,10 +887,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
 //     when their number is the number of ties to keep, c = ceil((T - mass
 //     above tau) / fix40(tau)), else the c of lowest id.
 // A row whose field e* holds more keys in some warp's words than its slice,
-// or whose 16-bit
-// prefix more than the small list, takes its remaining digits by passes over
-// the row and its mask by a pass over the row that ranks the ties in id order
-// with a block scan.
+// or whose 16-bit prefix more than the small list, takes its remaining digits
+// by passes over the row and its mask by a pass over the row that ranks the
+// ties in id order with a block scan.  The two CTAs of a cluster row sum every
+// histogram and count through distributed shared memory.
 constexpr int kRsThreads = 1024;
 constexpr int kRsWarps = kRsThreads / 32;
 constexpr int kRsE0 = 87;                          // lowest field with weight (q >= 2^-40)
