@@ -714,23 +714,31 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
       unsigned long long t_idle = 0;
       while (vp < npieces) {
         bool progressed = false;
-        if (kp < npieces) {
-          int ready = lane == 0 ? mbar_test_wait(&kempty[tk % kStages], ((tk / kStages) & 1) ^ 1) : 0;
-          if (__shfl_sync(0xffffffffu, ready, 0)) {
-            if (page_lane) blk_ring[(tk & 7) * 8 + lane] = blk_k;
-            issue(kp, kt, tk, 0, blk_k);
-            ++tk;
-            advance(kp, kt);
-            blk_k = fetch_block(kp, kt);
-            progressed = true;
-          }
-        }
+        // V before K: the next P V needs its V tile about a tile period
+        // before the S after it needs its K tile, and the copies of one warp
+        // land in issue order
         if (tv < tk) {
           int ready = lane == 0 ? mbar_test_wait(&vempty[tv % kVStages], ((tv / kVStages) & 1) ^ 1) : 0;
           if (__shfl_sync(0xffffffffu, ready, 0)) {
             issue(vp, vt, tv, 1, page_lane ? blk_ring[(tv & 7) * 8 + lane] : kPastEnd);
             ++tv;
             advance(vp, vt);
+            progressed = true;
+          }
+        }
+        if (kp < npieces) {
+          // a K tile only when no V copy could be issued now instead
+          int ready = 0;
+          if (lane == 0) {
+            const bool v_free = tv < tk && mbar_test_wait(&vempty[tv % kVStages], ((tv / kVStages) & 1) ^ 1);
+            ready = !v_free && mbar_test_wait(&kempty[tk % kStages], ((tk / kStages) & 1) ^ 1);
+          }
+          if (__shfl_sync(0xffffffffu, ready, 0)) {
+            if (page_lane) blk_ring[(tk & 7) * 8 + lane] = blk_k;
+            issue(kp, kt, tk, 0, blk_k);
+            ++tk;
+            advance(kp, kt);
+            blk_k = fetch_block(kp, kt);
             progressed = true;
           }
         }
