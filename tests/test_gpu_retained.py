@@ -138,3 +138,12 @@ def test_small_list_neighbours_of_tau():
         rows[r, idx] = bits_.view(np.float32)
     for mass in (0.01, 0.03, 0.05):
         _check(rows, mass)
+
+
+def test_full_size_multimodal_rows():
+    """The multimodal workload's 512 draft rows of 151936 at mass 0.7, the
+    launch the benchmark times (four waves of one-CTA rows), bit for bit;
+    the workload's own masks come from the fp64 recipe."""
+    case = wl.make_case(wl.config(4), parts=("accept",))
+    got = _check(case["draft_probs"], float(wl.config(4)["mask_mass"]))
+    assert np.array_equal(got[0], case["retained_mask"])
